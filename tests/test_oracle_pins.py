@@ -1,0 +1,474 @@
+"""Pins of the CPU oracle to things other than itself.
+
+Each test checks the oracle against a library routine on a special case, a
+closed form, a brute-force search, an invariant, or a value the pages print
+(tests/golden/page_facts.json, each entry with its citation).  They are
+chosen so that a plausible slip in the oracle (a dropped term, a wrong sign
+or index, a transposed operand, a wrong GQA mapping, a missing mask) fails
+at least one of them.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "page_facts.json")
+FACTS = json.load(open(GOLDEN))
+
+
+# ------------------------------------------------------------------ formulas
+def test_kv_size_formula_160_gib():
+    f = FACTS["kv_bytes_70b_example"]
+    b = oracle.kv_cache_bytes(f["layers"], f["heads"], f["head_dim"], f["seq_len"], f["batch"],
+                              f["bytes_per_elem"])
+    assert b / 2**30 == f["gib"]
+
+
+def test_kv_size_formula_13b_per_token():
+    f = FACTS["llama2_13b_bytes_per_token"]
+    b = oracle.kv_cache_bytes(f["layers"], f["heads"], f["head_dim"], f["seq_len"], f["batch"],
+                              f["bytes_per_elem"])
+    assert b == 819200
+    assert b / 1024 == f["approx_kilobytes"]
+    g = FACTS["llama2_13b_4000_tokens_over_gb"]
+    assert b * g["tokens"] > g["at_least_bytes"]
+
+
+@pytest.mark.parametrize("key", ["pages_512_tokens_page_16", "pages_2048_tokens_page_16"])
+def test_num_pages(key):
+    f = FACTS[key]
+    assert oracle.num_pages(f["tokens"], f["page_size"]) == f["pages"]
+    # ceil, not floor: one token more needs one more page
+    assert oracle.num_pages(f["tokens"] + 1, f["page_size"]) == f["pages"] + 1
+
+
+def test_snippet3_address_translation():
+    f = FACTS["snippet3_address"]
+    free = list(range(f["pool_blocks"]))
+    needed = -(-f["allocated_tokens"] // f["block_size"])
+    table = [free.pop(0) for _ in range(needed)]
+    phys, off = oracle.physical_address(table, f["block_size"], f["token_index"])
+    assert (phys, off) == (f["physical_block"], f["offset"])
+    with pytest.raises(IndexError):
+        oracle.physical_address(table, f["block_size"], needed * f["block_size"])
+
+
+# ------------------------------------------------------------------ 16-bit decoders
+def test_f16_decode_all_codes_vs_numpy():
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.f16_to_double(int(b)) for b in bits])
+    fin = np.isfinite(ref)
+    assert np.array_equal(got[fin], ref[fin])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(np.isinf(got), np.isinf(ref))
+
+
+def test_bf16_decode_all_codes_vs_torch():
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    got = np.array([oracle.bf16_to_double(int(b)) for b in bits])
+    fin = np.isfinite(ref)
+    assert np.array_equal(got[fin], ref[fin])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+
+
+def _dense_f32_sweep(rng, n=40000, lo=-30, hi=18):
+    mags = np.exp2(rng.uniform(lo, hi, n)).astype(np.float32)
+    signs = np.where(rng.random(n) < 0.5, -1, 1).astype(np.float32)
+    return np.concatenate([mags * signs, np.float32([0.0, -0.0, 65504, 65519.99, 65520,
+                                                     -65520, 6.1035156e-05, 5.9604645e-08,
+                                                     2.9802322e-08, 2.9802326e-08])])
+
+
+def test_f32_to_f16_rne_vs_numpy():
+    rng = np.random.default_rng(7)
+    x = _dense_f32_sweep(rng)
+    # every f16 midpoint, exactly: ties must go to the even code
+    f16 = np.arange(0, 0x7BFF, dtype=np.uint16).view(np.float16).astype(np.float64)
+    mids = ((f16[:-1] + f16[1:]) / 2).astype(np.float32)
+    x = np.concatenate([x, mids, -mids])
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    got = np.array([oracle.f32_to_f16_rne(float(v)) for v in x], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+
+
+# ------------------------------------------------------------------ E4M3
+def _finite_e4m3_table():
+    codes = [c for c in range(256) if (c & 0x7F) != 0x7F]
+    return codes, np.array([oracle.e4m3_to_double(c) for c in codes])
+
+
+def test_e4m3_decode_all_codes_vs_torch():
+    f = FACTS["e4m3_format"]
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    got = np.array([oracle.e4m3_to_double(int(c)) for c in codes])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(got[fin], ref[fin])
+    assert np.nanmax(got) == f["max_finite"] == oracle.e4m3_to_double(0x7E)
+    assert oracle.e4m3_to_double(0x08) == 2.0**-6
+    assert oracle.e4m3_to_double(0x01) == 2.0**-9
+    # 1/4/3 bits: 2^3 mantissa steps per binade, 15 usable exponents
+    assert oracle.e4m3_to_double(0x39) - oracle.e4m3_to_double(0x38) == 2.0**-3
+
+
+def _brute_force_e4m3(y: float, codes, vals) -> int:
+    """Nearest finite E4M3 value, ties to the even code; saturate at +-448."""
+    a = abs(y)
+    if a >= 448.0:
+        return 0xFE if math.copysign(1, y) < 0 else 0x7E
+    best, bestd = None, None
+    for c, v in zip(codes, vals):
+        if c & 0x80:
+            continue
+        d = abs(a - v)
+        if bestd is None or d < bestd or (d == bestd and (c & 1) == 0):
+            best, bestd = c, d
+    return best | (0x80 if math.copysign(1, y) < 0 else 0)
+
+
+def test_e4m3_encode_vs_brute_force_nearest_even():
+    codes, vals = _finite_e4m3_table()
+    pos = sorted(set(v for c, v in zip(codes, vals) if not c & 0x80))
+    mids = [(a + b) / 2 for a, b in zip(pos[:-1], pos[1:])]
+    rng = np.random.default_rng(11)
+    xs = list(np.float32(pos)) + list(np.float32(mids))
+    xs += [np.nextafter(np.float32(m), np.float32(np.inf)) for m in mids]
+    xs += [np.nextafter(np.float32(m), np.float32(-np.inf)) for m in mids]
+    xs += list(np.exp2(rng.uniform(-14, 10, 3000)).astype(np.float32))
+    xs += [np.float32(v) for v in (448.0, 449.0, 463.9, 464.0, 479.0, 480.0, 1e6, 1e-30)]
+    for x in xs:
+        for y in (float(x), -float(x)):
+            assert oracle.e4m3_encode(y) == _brute_force_e4m3(y, codes, vals), y
+
+
+def test_e4m3_encode_vs_torch_cast_in_range():
+    rng = np.random.default_rng(12)
+    y = np.concatenate([rng.standard_normal(20000) * 60,
+                        np.exp2(rng.uniform(-12, 8.7, 20000)) * rng.choice([-1, 1], 20000)])
+    y = np.clip(y, -447.9, 447.9).astype(np.float32)
+    ref = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(float(v)) for v in y], dtype=np.uint8)
+    assert np.array_equal(got, ref)
+
+
+def test_e4m3_encode_saturation_and_signed_zero():
+    assert oracle.e4m3_encode(448.0) == 0x7E
+    assert oracle.e4m3_encode(1e6) == 0x7E
+    assert oracle.e4m3_encode(-1e6) == 0xFE
+    assert oracle.e4m3_encode(float("inf")) == 0x7E
+    assert oracle.e4m3_encode(0.0) == 0x00
+    assert oracle.e4m3_encode(-0.0) == 0x80
+    assert oracle.e4m3_encode(-1e-9) == 0x80
+    assert oracle.e4m3_encode(float("nan")) == 0x7F
+
+
+# ------------------------------------------------------------------ the write
+def _one_block_write(kv_dtype, rows, offsets, head_dim=64, block_size=16, dtype=W.BF16,
+                     num_kv_heads=1):
+    """Write `rows` (float32 [n, D]) at `offsets` of physical block 1; return cache."""
+    nb = 3
+    k, v, s = oracle.alloc_cache(kv_dtype, nb, num_kv_heads, head_dim, block_size)
+    x = W.to_bits(np.repeat(np.asarray(rows, np.float32)[:, None, :], num_kv_heads, 1), dtype)
+    slots = np.array([1 * block_size + o for o in offsets], np.int64)
+    oracle.kv_write(x, x, dtype, slots, k, v, s, kv_dtype, nb, num_kv_heads, head_dim,
+                    block_size)
+    return k, v, s, x
+
+
+def test_write_16bit_is_a_copy_at_the_translated_slot():
+    rng = np.random.default_rng(3)
+    rows = rng.standard_normal((3, 64)).astype(np.float32)
+    k, v, s, x = _one_block_write(W.BF16, rows, [5, 0, 15])
+    for i, o in enumerate([5, 0, 15]):
+        assert np.array_equal(k[1, 0, o], x[i, 0])
+        assert np.array_equal(v[1, 0, o], x[i, 0])
+    assert not k[0].any() and not k[2].any()
+
+
+def test_write_fp8_scale_is_amax_over_448():
+    f = FACTS["fp8_scale_rule"]
+    rng = np.random.default_rng(4)
+    row = (rng.standard_normal(64) * 3).astype(np.float32)
+    row[17] = -9.5
+    k, v, s, x = _one_block_write(W.FP8_E4M3, row[None], [0])
+    xr = W.bits_to_f32(x[0, 0], W.BF16)
+    amax = np.float32(np.abs(xr).max())
+    assert s[0, 1, 0] == np.float32(amax / np.float32(f["fp8_max"]))
+    assert s[1, 1, 0] == s[0, 1, 0]
+    # the largest magnitude lands on the largest code, with its sign
+    assert k[1, 0, 0, 17] == 0xFE
+    # round trip within half an E4M3 step (2^-4 relative for normals)
+    deq = np.array([oracle.e4m3_to_double(c) for c in k[1, 0, 0]]) * float(s[0, 1, 0])
+    err = np.abs(deq - xr)
+    assert np.all(err <= np.maximum(np.abs(xr) * 2.0**-4, 2.0**-10 * float(s[0, 1, 0])) + 1e-12)
+
+
+def test_write_fp8_zero_row_uses_eps_scale():
+    f = FACTS["fp8_scale_rule"]
+    k, v, s, x = _one_block_write(W.FP8_E4M3, np.zeros((1, 64)), [0])
+    assert s[0, 1, 0] == np.float32(f["eps"])
+    assert not k[1, 0, 0].any()
+
+
+def test_write_fp8_scale_frozen_after_offset_zero_and_order_independent():
+    rng = np.random.default_rng(5)
+    r0 = rng.standard_normal(64).astype(np.float32)
+    r1 = (r0 * 50).astype(np.float32)          # far larger: must saturate
+    ka, _, sa, _ = _one_block_write(W.FP8_E4M3, np.stack([r0, r1]), [0, 1])
+    kb, _, sb, _ = _one_block_write(W.FP8_E4M3, np.stack([r1, r0]), [1, 0])
+    assert np.array_equal(ka, kb) and np.array_equal(sa, sb)
+    big = np.abs(r1) >= np.abs(r0).max() * 1.01
+    assert np.all((ka[1, 0, 1][big] & 0x7F) == 0x7E)
+    # a later single write at offset 3 keeps the block's scale
+    nb, bs = 3, 16
+    x = W.to_bits(r0[None, None, :] * 0.5, W.BF16)
+    oracle.kv_write(x, x, W.BF16, np.array([1 * bs + 3]), ka, ka.copy(), sa, W.FP8_E4M3, nb, 1,
+                    64, bs)
+    assert np.array_equal(sa, sb)
+
+
+def test_write_int4_round_trip_bound_and_extremes():
+    rng = np.random.default_rng(6)
+    rows = (rng.standard_normal((4, 64)) * np.array([[1], [10], [0.01], [300]])).astype(np.float32)
+    k, v, s, x = _one_block_write(W.INT4_G32, rows, [0, 1, 2, 3])
+    for i in range(4):
+        xr = W.bits_to_f32(x[i, 0], W.BF16).astype(np.float64)
+        codes = np.empty(64, np.int64)
+        codes[0::2] = k[1, 0, i] & 0xF
+        codes[1::2] = k[1, 0, i] >> 4
+        for g in range(2):
+            sc = np.float16(s[0, 1, 0, i, g, 0].view(np.float16)).astype(np.float64)
+            z = np.float16(s[0, 1, 0, i, g, 1].view(np.float16)).astype(np.float64)
+            seg = xr[32 * g:32 * (g + 1)]
+            c = codes[32 * g:32 * (g + 1)]
+            assert c.min() >= 0 and c.max() <= 15
+            assert c[np.argmin(seg)] == 0 and c[np.argmax(seg)] == 15
+            rec = c * sc + z
+            # half a step, plus the fp16 rounding of the zero point
+            assert np.all(np.abs(rec - seg) <= sc / 2 + abs(z - seg.min()) + 1e-6 * np.abs(seg).max())
+            # the dequantizer reads the same layout
+            row = oracle.dequant_row(k, s, 0, W.INT4_G32, 3, 1, 64, 16, 1, 0, i)
+            assert np.allclose(row[32 * g:32 * (g + 1)], rec, rtol=0, atol=1e-12)
+
+
+def test_write_int4_worked_example():
+    # one group holding 0..31: min 0, max 31 -> scale fp16(31/15) = 2.06640625, zero 0
+    row = np.concatenate([np.arange(32), np.full(32, 7.0)]).astype(np.float32)
+    k, v, s, x = _one_block_write(W.INT4_G32, row[None], [0])
+    assert s[0, 1, 0, 0, 0, 0].view(np.float16) == np.float16(2.06640625)
+    assert s[0, 1, 0, 0, 0, 1].view(np.float16) == 0
+    codes = np.empty(64, np.int64)
+    codes[0::2] = k[1, 0, 0] & 0xF
+    codes[1::2] = k[1, 0, 0] >> 4
+    # i / 2.0664 rounded: 0,0,1,1,2,2,3,3,4,4,5,5,6,6,7,7,8,8,9,9,10,10,11,11,12,12,13,13,14,14,15,15
+    assert list(codes[:32]) == [i // 2 for i in range(32)]
+    # a constant group: range 0 -> scale 0 -> every code 0, zero = the value
+    assert s[0, 1, 0, 0, 1, 0].view(np.float16) == 0
+    assert s[0, 1, 0, 0, 1, 1].view(np.float16) == np.float16(7.0)
+    assert not codes[32:].any()
+
+
+def test_write_skips_negative_slots():
+    k, v, s, x = _one_block_write(W.F16, np.ones((1, 64)), [0], dtype=W.F16)
+    k2 = k.copy()
+    oracle.kv_write(x, x, W.F16, np.array([-1], np.int64), k2, v, s, W.F16, 3, 1, 64, 16)
+    assert np.array_equal(k, k2)
+
+
+# ------------------------------------------------------------------ attention
+def _dense_reference(q, kd, vd, scale, group):
+    """torch SDPA (fp64) on contiguous K/V: q [Hq, D], kd/vd [Hkv, T, D]."""
+    qt = torch.from_numpy(q)[None, :, None, :]                       # [1, Hq, 1, D]
+    kt = torch.from_numpy(kd).repeat_interleave(group, 0)[None]      # [1, Hq, T, D]
+    vt = torch.from_numpy(vd).repeat_interleave(group, 0)[None]
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale)
+    return o[0, :, 0, :].numpy()
+
+
+def _gathered(case, k, v, s, b):
+    """Dequantize sequence b's K/V by an independent route (library decoders)."""
+    w = case.w
+    n = int(case.context_lens[b])
+    bs, h, d = w.block_size, w.num_kv_heads, w.head_dim
+    kd = np.zeros((h, n, d))
+    vd = np.zeros((h, n, d))
+    for t in range(n):
+        p = case.block_tables[b, t // bs]
+        o = t % bs
+        for j, (cache, out) in enumerate(((k, kd), (v, vd))):
+            raw = cache[p, :, o]
+            if w.kv_dtype == W.F16:
+                out[:, t] = raw.view(np.float16).astype(np.float64)
+            elif w.kv_dtype == W.BF16:
+                out[:, t] = torch.from_numpy(raw.view(np.int16)).view(torch.bfloat16).double().numpy()
+            elif w.kv_dtype == W.FP8_E4M3:
+                dec = torch.from_numpy(np.ascontiguousarray(raw)).view(torch.float8_e4m3fn).double().numpy()
+                out[:, t] = dec * s[j, p, :, None].astype(np.float64)
+            else:
+                lo = (raw & 0xF).astype(np.float64)
+                hi = (raw >> 4).astype(np.float64)
+                codes = np.stack([lo, hi], -1).reshape(h, d)
+                sz = s[j, p, :, o].view(np.float16).astype(np.float64)   # [h, D/32, 2]
+                out[:, t] = codes * np.repeat(sz[..., 0], 32, 1) + np.repeat(sz[..., 1], 32, 1)
+    return kd, vd
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_attention_matches_sdpa_on_gathered_kv(cfg):
+    w = W.CONFIGS[cfg].scaled(batch=3, ctx_cap=70, seed=100 + cfg)
+    case = W.make_case(w)
+    k, v, s = oracle.prefill_case(case)
+    out = oracle.step_case(case, k, v, s)
+    for b in range(w.batch):
+        q = W.bits_to_f32(case.q[b], w.q_dtype).astype(np.float64)
+        kd, vd = _gathered(case, k, v, s, b)
+        ref = _dense_reference(q, kd, vd, w.softmax_scale, w.group)
+        assert np.allclose(out[b], ref, rtol=0, atol=1e-12), (cfg, b)
+
+
+def _tiny_case(cfg=1, **kw):
+    w = W.CONFIGS[cfg].scaled(**kw)
+    return W.make_case(w)
+
+
+def test_attention_gqa_mapping_uses_contiguous_groups():
+    w = W.Workload("gqa", 1, 8, 4, 64, 16, W.F16, W.F16, "fixed", 20, 20, pool_blocks=4, seed=9)
+    case = W.make_case(w)
+    k, v, s = oracle.prefill_case(case)
+    oracle.kv_write(case.k_new, case.v_new, w.q_dtype, case.new_slots, k, v, s, w.kv_dtype,
+                    case.num_blocks, 4, 64, 16)
+    for h in range(4):
+        v[:, h] = np.float16(h + 1).view(np.uint16)
+    out = oracle.decode_attention(case.q, w.q_dtype, k, v, case.block_tables, case.context_lens,
+                                  s, w.kv_dtype, case.num_blocks, w.softmax_scale, 8, 4, 64, 16)
+    for h in range(8):
+        assert np.allclose(out[0, h], h // 2 + 1, atol=1e-12)
+
+
+def test_attention_context_one_returns_v():
+    case = _tiny_case(batch=4, ctx_cap=1, seed=21)
+    k, v, s = oracle.prefill_case(case)
+    out = oracle.step_case(case, k, v, s)
+    for b in range(4):
+        p = case.block_tables[b, 0]
+        vrow = v[p, :, 0].view(np.float16).astype(np.float64)         # [Hkv, D]
+        assert np.array_equal(out[b], np.repeat(vrow, 4, 0))
+
+
+def test_attention_constant_keys_give_mean_of_values():
+    case = _tiny_case(batch=2, seed=22)
+    k, v, s = oracle.prefill_case(case)
+    oracle.kv_write(case.k_new, case.v_new, 0, case.new_slots, k, v, s, 0, case.num_blocks, 2,
+                    64, 16)
+    k[:] = np.float16(0.37).view(np.uint16)
+    out = oracle.decode_attention(case.q, 0, k, v, case.block_tables, case.context_lens, s, 0,
+                                  case.num_blocks, 0.125, 8, 2, 64, 16)
+    for b in range(2):
+        n = case.context_lens[b]
+        rows = np.stack([v[case.block_tables[b, t // 16], :, t % 16] for t in range(n)])
+        mean = rows.view(np.float16).astype(np.float64).mean(0)
+        assert np.allclose(out[b], np.repeat(mean, 4, 0), atol=1e-12)
+
+
+def test_attention_two_token_closed_form():
+    # q = e0, K0 = 0, K1 = ln(3)/scale * e0: weights exactly 1/4 and 3/4
+    w = W.Workload("two", 1, 1, 1, 64, 16, W.BF16, W.BF16, "fixed", 2, 2, pool_blocks=2, seed=1)
+    case = W.make_case(w)
+    k, v, s = oracle.alloc_cache(W.BF16, 2, 1, 64, 16)
+    q = np.zeros((1, 1, 64), np.float32); q[0, 0, 0] = 1.0
+    p = case.block_tables[0, 0]
+    kk = np.zeros((2, 64), np.float64)
+    kk[1, 0] = math.log(3.0) * 8.0
+    vv = np.zeros((2, 64), np.float64); vv[0] = 1.0; vv[1] = -1.0
+    # use values exactly representable in bf16 by picking the scale from the stored key
+    kbits = W.to_bits(kk.astype(np.float32), W.BF16)
+    k[p, 0, :2] = kbits
+    v[p, 0, :2] = W.to_bits(vv.astype(np.float32), W.BF16)
+    stored = float(W.bits_to_f32(kbits[1:2, :1], W.BF16)[0, 0])
+    scale = math.log(3.0) / stored
+    out = oracle.decode_attention(W.to_bits(q, W.BF16), W.BF16, k, v, case.block_tables,
+                                  case.context_lens, None, W.BF16, 2, scale, 1, 1, 64, 16)
+    assert np.allclose(out[0, 0], 0.25 * 1 + 0.75 * -1, atol=1e-14)
+
+
+def test_attention_context_zero_gives_zeros():
+    case = _tiny_case(batch=2, seed=23)
+    k, v, s = oracle.prefill_case(case)
+    cl = case.context_lens.copy(); cl[1] = 0
+    out = oracle.decode_attention(case.q, 0, k, v, case.block_tables, cl, s, 0, case.num_blocks,
+                                  0.125, 8, 2, 64, 16)
+    assert not out[1].any() and out[0].any()
+
+
+def test_attention_masks_tokens_past_context():
+    case = _tiny_case(batch=3, seed=24)
+    k, v, s = oracle.prefill_case(case)
+    oracle.kv_write(case.k_new, case.v_new, 0, case.new_slots, k, v, s, 0, case.num_blocks, 2,
+                    64, 16)
+    args = (case.block_tables, case.context_lens, s, 0, case.num_blocks, 0.125, 8, 2, 64, 16)
+    out = oracle.decode_attention(case.q, 0, k, v, *args)
+    k2, v2 = k.copy(), v.copy()
+    for b in range(3):
+        n = case.context_lens[b]
+        last = case.block_tables[b, (n - 1) // 16]
+        k2[last, :, (n - 1) % 16 + 1:] = np.float16(300.0).view(np.uint16)
+        v2[last, :, (n - 1) % 16 + 1:] = np.float16(-300.0).view(np.uint16)
+    out2 = oracle.decode_attention(case.q, 0, k2, v2, *args)
+    assert np.array_equal(out, out2)
+
+
+@pytest.mark.parametrize("cfg", [1, 3, 4])
+def test_attention_invariant_under_block_permutation(cfg):
+    w = W.CONFIGS[cfg].scaled(batch=3, ctx_cap=90, seed=30 + cfg)
+    case = W.make_case(w)
+    k, v, s = oracle.prefill_case(case)
+    out = oracle.step_case(case, k, v, s)
+    rng = np.random.default_rng(1)
+    perm = rng.permutation(case.num_blocks)                # new id of old block i = perm[i]
+    k2, v2 = np.empty_like(k), np.empty_like(v)
+    k2[perm], v2[perm] = k, v
+    s2 = None
+    if s is not None:
+        s2 = np.empty_like(s)
+        s2[:, perm] = s
+    bt = np.where(case.block_tables >= 0, perm[np.maximum(case.block_tables, 0)], -1).astype(np.int32)
+    out2 = oracle.decode_attention(case.q, w.q_dtype, k2, v2, bt, case.context_lens, s2,
+                                   w.kv_dtype, case.num_blocks, w.softmax_scale, w.num_q_heads,
+                                   w.num_kv_heads, w.head_dim, w.block_size)
+    assert np.array_equal(out, out2)
+
+
+def test_attention_paged_equals_contiguous_layout():
+    w = W.CONFIGS[2].scaled(batch=2, ctx_cap=100, seed=41)
+    a = W.make_case(w)
+    b = W.make_case(w, identity_tables=True)
+    assert np.array_equal(a.prefill_k, b.prefill_k)
+    ka, va, sa = oracle.prefill_case(a)
+    kb, vb, sb = oracle.prefill_case(b)
+    oa = oracle.step_case(a, ka, va, sa)
+    ob = oracle.step_case(b, kb, vb, sb)
+    assert np.array_equal(oa, ob)
+
+
+def test_attention_pairs_match_full():
+    w = W.CONFIGS[3].scaled(batch=4, ctx_cap=64, seed=51)
+    case = W.make_case(w)
+    k, v, s = oracle.prefill_case(case)
+    full = oracle.step_case(case, k, v, s)
+    ps = np.array([0, 3, 2, 1]); ph = np.array([5, 0, 31, 17])
+    sub = oracle.decode_attention_pairs(case.q, w.q_dtype, k, v, case.block_tables,
+                                        case.context_lens, s, w.kv_dtype, case.num_blocks,
+                                        w.softmax_scale, w.num_q_heads, w.num_kv_heads,
+                                        w.head_dim, w.block_size, ps, ph)
+    assert np.array_equal(sub, full[ps, ph])
