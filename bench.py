@@ -1,0 +1,441 @@
+"""Benchmark: paged decode-attention KV GB/s (% of GB300 HBM peak) and seq-steps/s.
+
+One step = the whole hot path for one decode step of one layer: the
+quantize-on-write of every sequence's new token (paged_kv_write) followed by
+paged decode attention over the block-table-mapped cache.  Inputs are seeded
+and synthetic, shaped like the chosen workload (default: the Llama-3-8B-shaped
+bf16 layer, batch 64, 32/8 heads, D 128, bs 16, context 4096).  The KV cache
+(1 GiB) is far larger than L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  Under torchrun each rank runs an independent
+replica on its own GPU (the path has no exchange step).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged decode-attention KV GB/s (% of GB300 HBM peak) and seq-steps/sec, 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2**20
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except FileNotFoundError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _bits_to_tensor(bits, code):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(torch.float16 if code == W.F16 else torch.bfloat16).cuda()
+
+
+def _kernel_launches_per_step(w: W.Workload, nparts: int) -> int:
+    write = 2 if w.kv_dtype == W.FP8_E4M3 else 1
+    return write + 1 + (1 if nparts > 1 else 0)
+
+
+def run_ours(args, rank: int, world: int):
+    import torch
+    import paged_quantized_kv_write_gb300 as pkv
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = W.CONFIGS[args.config]
+    case = W.make_case(w)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        k, v, s = pkv.alloc_cache(w.kv_dtype, case.num_blocks, w.num_kv_heads, w.head_dim,
+                                  w.block_size)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        # prefill the context through the library's own write (untimed)
+        chunk = 1 << 20
+        for i in range(0, len(case.prefill_slots), chunk):
+            sl = slice(i, i + chunk)
+            pkv.paged_kv_write(_bits_to_tensor(case.prefill_k[sl], w.q_dtype),
+                               _bits_to_tensor(case.prefill_v[sl], w.q_dtype),
+                               torch.from_numpy(case.prefill_slots[sl]).to(dev), k, v, s,
+                               w.kv_dtype, w.block_size, w.head_dim, status, stream)
+        q = _bits_to_tensor(case.q, w.q_dtype)
+        kn = _bits_to_tensor(case.k_new, w.q_dtype)
+        vn = _bits_to_tensor(case.v_new, w.q_dtype)
+        slots = torch.from_numpy(case.new_slots).to(dev)
+        tables = torch.from_numpy(case.block_tables).to(dev)
+        ctx = torch.from_numpy(case.context_lens).to(dev)
+        out = torch.empty_like(q)
+        mb = case.max_blocks_per_seq
+        part = pkv.paged_decode_partition_size(w.batch, w.num_q_heads, w.num_kv_heads, mb,
+                                               w.block_size, w.partition_size)
+        nparts = -(-mb * w.block_size // part)
+        ws = pkv.make_workspace(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, mb,
+                                w.block_size, w.partition_size, device=dev)
+    torch.cuda.synchronize()
+    assert status.item() == 0, "prefill flagged an out-of-range slot"
+
+    total_bytes = W.algorithmic_bytes(case, unique=True)
+    attn_bytes = W.attention_bytes(case, unique=True)
+    logical_bytes = W.algorithmic_bytes(case, unique=False)
+    small = total_bytes < 4 * L2_BYTES
+    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev) if small else None
+
+    def step():
+        pkv.paged_kv_write(kn, vn, slots, k, v, s, w.kv_dtype, w.block_size, w.head_dim,
+                           status, stream)
+        a0.record(stream)
+        pkv.paged_decode_attention(q, k, v, tables, ctx, s, out, w.softmax_scale,
+                                   w.num_kv_heads, w.kv_dtype, w.block_size, w.partition_size,
+                                   ws, status, stream)
+        a1.record(stream)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            a0, a1 = ev[0][1], ev[0][2]
+            if flush is not None:
+                flush.zero_()
+            step()
+        torch.cuda.synchronize()
+        _barrier(world)
+        clocks = ClockSampler(dev.index)
+        clocks.start()
+        time.sleep(0.3)
+        torch.cuda.synchronize()
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            s0, a0, a1, s1 = ev[i]
+            if flush is not None:
+                flush.zero_()
+            s0.record(stream)
+            step()
+            s1.record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+        clk = clocks.stop()
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    dev_ms = sum(step_ms)
+    dev_ms = _max_over_ranks(dev_ms, world)
+    assert status.item() == 0
+
+    # end to end through the public API with host buffers: H2D of the step's
+    # inputs from pinned memory, both calls, D2H of the output, every step
+    host_in = {n: t.cpu().pin_memory() for n, t in
+               (("q", q), ("kn", kn), ("vn", vn), ("slots", slots), ("tables", tables),
+                ("ctx", ctx))}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dev_in = {"q": q, "kn": kn, "vn": vn, "slots": slots, "tables": tables, "ctx": ctx}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            if flush is not None:
+                flush.zero_()
+            if i >= args.warmup:
+                e2e_ev[i - args.warmup][0].record(stream)
+            for n, t in host_in.items():
+                dev_in[n].copy_(t, non_blocking=True)
+            a0, a1 = ev[0][1], ev[0][2]
+            step()
+            host_out.copy_(out, non_blocking=True)
+            if i >= args.warmup:
+                e2e_ev[i - args.warmup][1].record(stream)
+        torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev), world)
+
+    peak, peak_kind = _peaks()
+    ms_per_step = dev_ms / args.steps
+    gbs = world * total_bytes * args.steps / (dev_ms * 1e-3) / 1e9
+    attn_avg_ms = statistics.mean(attn_ms)
+    achieved = attn_bytes / (attn_avg_ms * 1e-3) / 1e9
+    result = {
+        "metric": METRIC,
+        "value": round(gbs, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": {W.F16: "f16", W.BF16: "bf16", W.FP8_E4M3: "fp8_e4m3+bf16",
+                  W.INT4_G32: "int4_g32+bf16"}[w.kv_dtype],
+        "data": "synthetic (seeded N(0,1) q/K/V, shuffled block tables; no model weights)",
+        "config": {
+            "workload": f"config {args.config}: {w.name}",
+            "batch": w.batch, "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "block_size": w.block_size,
+            "kv_dtype": W.DTYPE_NAMES[w.kv_dtype],
+            "context_tokens": int(case.context_lens.sum()),
+            "partition_size": part, "num_partitions": nparts,
+            "l2": "inputs larger than L2 (no flush)" if not small else "L2 flushed (256 MB write) between steps",
+            "parallelism": f"replicas x{world}",
+        },
+        "seq_steps_per_s": round(world * w.batch * args.steps / (dev_ms * 1e-3), 1),
+        "pct_hbm_peak": round(100.0 * gbs / world / peak, 2),
+        "bytes_per_step": total_bytes,
+        "logical_bytes_per_step": logical_bytes,
+        "e2e": {
+            "value": round(world * total_bytes * args.steps / (e2e_ms * 1e-3) / 1e9, 2),
+            "unit": "GB/s",
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(e2e_ms / args.steps, 5),
+        },
+        "roofline": {
+            "kernel": "paged_decode_kernel (+ pkv_lse_reduce when split)",
+            "bound": "hbm",
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6.8 TB/s",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": _traffic(args.config),
+            "avg_launch_us": round(attn_avg_ms * 1e3, 3),
+            "algorithmic_bytes": attn_bytes,
+        },
+        "gpu_launches": _kernel_launches_per_step(w, nparts) * args.steps,
+        "clocks": clk,
+        "wall_s_timed": round(t_wall, 4),
+    }
+    return result
+
+
+def _traffic(config: int):
+    """DRAM bytes per launch of the decode kernel from a committed ncu summary, if one
+    exists for this workload and the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        ent = d.get(str(config))
+        if not ent or ent.get("source_sha") != _kernel_sha():
+            return None
+        return ent["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+def _kernel_sha() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("pkv_decode.cu", "pkv_common.cuh"):
+        with open(os.path.join(ROOT, "paged_quantized_kv_write_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def cpu_baseline(config: int, budget_s: float = 20.0):
+    """The oracle as it stands on the host cores, over a bounded sample of the workload."""
+    import oracle
+    w = W.CONFIGS[config]
+    # sample: the first n sequences of the workload, n sized to a few seconds of CPU work
+    n = w.batch
+    probe = W.make_case(w.scaled(batch=min(4, w.batch)))
+    pk, pv, ps = oracle.prefill_case(probe)
+    t0 = time.perf_counter()
+    oracle.step_case(probe, pk, pv, ps)
+    per_seq = (time.perf_counter() - t0) / probe.w.batch
+    n = int(max(1, min(w.batch, budget_s / max(per_seq, 1e-6))))
+    case = W.make_case(w.scaled(batch=n))
+    k, v, s = oracle.prefill_case(case)
+    t0 = time.perf_counter()
+    oracle.step_case(case, k, v, s)
+    dt = time.perf_counter() - t0
+    return {
+        "value": round(W.algorithmic_bytes(case) / dt / 1e9, 4),
+        "unit": "GB/s",
+        "seq_steps_per_s": round(n / dt, 3),
+        "cores": oracle.max_threads(),
+        "kind": "oracle",
+        "sample": f"{n} of {w.batch} sequences of config {config} (same heads, dims, lengths "
+                  f"distribution), one decode step, fp64 C oracle with OpenMP",
+        "seconds": round(dt, 3),
+    }
+
+
+def run_reference(args, rank: int, world: int):
+    """The reference arm: the CPU oracle, timed on this machine's host cores."""
+    import oracle
+    w = W.CONFIGS[args.config]
+    probe = W.make_case(w.scaled(batch=min(2, w.batch)))
+    pk, pv, ps = oracle.prefill_case(probe)
+    t0 = time.perf_counter()
+    oracle.step_case(probe, pk, pv, ps)
+    per_seq = (time.perf_counter() - t0) / probe.w.batch
+    budget = 120.0 / max(1, args.steps + args.warmup)        # whole run within ~2 minutes
+    n = int(max(1, min(w.batch, budget / max(per_seq, 1e-6))))
+    case = W.make_case(w.scaled(batch=n))
+    k, v, s = oracle.prefill_case(case)
+    for _ in range(args.warmup):
+        oracle.step_case(case, k, v, s)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.step_case(case, k, v, s)
+    dt = time.perf_counter() - t0
+    val = W.algorithmic_bytes(case) * args.steps / dt / 1e9
+    sample = (f"{n} of {w.batch} sequences of config {args.config} per step, fp64 C oracle "
+              f"with OpenMP")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(val, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3 / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": f"config {args.config}: {w.name}", "sample": sample},
+        "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    return rank, world
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=2, choices=sorted(W.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world = _dist()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            res["cpu_baseline"] = cpu_baseline(args.config)
+        elif not args.no_cpu_baseline:
+            res["cpu_baseline"] = None
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,149 @@
+/* pagedkv — paged, quantized KV cache for decode on GB300 (sm_103a).
+ *
+ * Two operations, as the PagedAttention pages state the problem:
+ *   paged_kv_write          store each step's new K/V rows into their physical
+ *                           block slots, quantizing on the way in;
+ *   paged_decode_attention  one decode step of attention for every sequence,
+ *                           reading K/V through a block table.
+ *
+ * Sources: "Reducing LLM Inference Latency: KV Cache Quantization and
+ * PagedAttention in vLLM" (mohashari.github.io) — block pool, block table,
+ * address translation (snippet-3), block-wise FP8 E4M3 scale and cast
+ * (snippet-4); "KV Cache Compression & Paged Attention" (myaihardware.com),
+ * "Implementation Details" — the kernel's inputs and its loop over logical
+ * blocks; "Optimizing KV-Cache Memory Footprint" (publishertech.pages.dev),
+ * section 4 — INT4 group-wise quantization; "KV Cache Optimization: 3x
+ * Faster LLM Inference" (tildalice.io) — softmax(q K^T / sqrt(d)) V and GQA.
+ *
+ * Conventions shared by every call:
+ *  - Every buffer is caller-owned DEVICE memory, 16-byte aligned.  The
+ *    library allocates nothing and keeps no state between calls.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t, NULL = the legacy
+ *    default stream) and never synchronize.  Host-visible argument errors
+ *    return a nonzero pkv_status before anything is launched.
+ *  - `dev_status` (optional, may be NULL) is one int in device memory.  A
+ *    kernel that meets a block id or slot outside the pool ORs
+ *    PKV_ERR_DEVICE_BOUNDS into it and skips that block or token; it never
+ *    traps.  The caller reads it back whenever it likes.
+ *  - Cache layout per KV tensor (K and V are separate buffers):
+ *      [num_blocks][num_kv_heads][block_size][row], where a row holds one
+ *      token of one head: head_dim 16-bit values (F16/BF16), head_dim E4M3
+ *      bytes (FP8), or head_dim/2 bytes of 4-bit codes (INT4: element 2i in
+ *      the low nibble of byte i, 2i+1 in the high nibble).
+ *  - `scales` layout (index 0 of the leading 2 is K, 1 is V):
+ *      FP8:  float [2][num_blocks][num_kv_heads] — one scale per block and
+ *            KV head;
+ *      INT4: half  [2][num_blocks][num_kv_heads][block_size][head_dim/32][2]
+ *            — (scale, zero) per token, head and group of 32 elements;
+ *      F16/BF16: unused (may be NULL).
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_F16 = 0,       /* IEEE half */
+    PKV_BF16 = 1,      /* bfloat16 */
+    PKV_FP8_E4M3 = 2,  /* OCP E4M3 ("e4m3fn"), per-(block, kv-head) fp32 scale */
+    PKV_INT4_G32 = 3   /* asymmetric 4-bit, groups of 32 along head_dim, fp16 scale+zero */
+} pkv_dtype;
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,    /* NULL, negative size, misaligned pointer, Hq % Hkv != 0 */
+    PKV_ERR_UNSUPPORTED = 2,    /* a shape or dtype combination this build has no kernel for */
+    PKV_ERR_CUDA = 3,           /* a CUDA launch failed (see cudaGetLastError) */
+    PKV_ERR_DEVICE_BOUNDS = 4,  /* written to *dev_status by a kernel, never returned */
+    PKV_ERR_WORKSPACE = 5       /* workspace missing or smaller than required */
+} pkv_status;
+
+/* paged_kv_write — quantize-on-write of new K/V rows into their slots.
+ *
+ * k_new, v_new   [num_tokens][num_kv_heads][head_dim] in new_dtype (F16 or BF16).
+ * slot_mapping   int64 [num_tokens]; slot = physical_block * block_size + offset
+ *                (the block manager's address translation, snippet-3 of the
+ *                mohashari page).  -1 skips the token; any other value outside
+ *                [0, num_blocks * block_size) is skipped and flagged in dev_status.
+ * k_cache, v_cache, scales   the pool, layouts above, updated in place.
+ * kv_dtype       F16/BF16: a plain copy (new_dtype must equal kv_dtype).
+ *                FP8_E4M3: the token written at offset 0 of a block sets that
+ *                block's K and V scales per KV head to max(amax / 448, 1e-12)
+ *                in fp32 (snippet-4's block-wise rule); a token at any other
+ *                offset reuses the stored scales.  code = E4M3 round-to-nearest-
+ *                even with saturation to +-448 of the fp32 quotient x / scale.
+ *                Within one call the offset-0 tokens are applied first.
+ *                INT4_G32: per token, head and 32-element group,
+ *                scale = fp16(fp32(max - min) / 15), zero = fp16(min),
+ *                code = clamp(rint((x - zero) / scale), 0, 15) in fp32 (0 when
+ *                scale is 0).  head_dim must be a multiple of 32.
+ * Supported: head_dim in {64, 128}, block_size a multiple of 16 up to 256.
+ * Two tokens of one call must not target the same slot (the result would
+ * depend on the order the GPU runs them in).
+ */
+int paged_kv_write(const void* k_new, const void* v_new, int new_dtype,
+                   const int64_t* slot_mapping, int64_t num_tokens,
+                   void* k_cache, void* v_cache, void* scales, int kv_dtype,
+                   int num_blocks, int num_kv_heads, int head_dim, int block_size,
+                   int* dev_status, void* stream);
+
+/* paged_decode_attention — one decode step over a paged, optionally
+ * quantized KV cache (the PagedAttention kernel of the myaihardware page,
+ * "Implementation Details": per head, walk the logical blocks, translate
+ * each to its physical block, load K and V, score, softmax, weighted sum).
+ *
+ * q              [num_seqs][num_q_heads][head_dim] in q_dtype (F16 or BF16).
+ * block_tables   int32 [num_seqs][max_blocks_per_seq]; entry j of row b is
+ *                the physical block holding tokens [j*bs, (j+1)*bs) of b.
+ * context_lens   int32 [num_seqs]; tokens to attend over, the new token
+ *                included (write first, then attend).  0 gives out = 0.
+ * out            [num_seqs][num_q_heads][head_dim] in q_dtype:
+ *                out = sum_t softmax_t(softmax_scale * q.K_t) V_t, fp32
+ *                accumulation, over K/V dequantized in registers.
+ * GQA            query head h reads KV head h / (num_q_heads / num_kv_heads).
+ * partition_size tokens per split-KV partition (multiple of 16), or 0 for
+ *                the library's choice.  With more than one partition each
+ *                partition writes a partial (max, sum, output) to `workspace`
+ *                and a second kernel merges them by log-sum-exp.
+ * workspace      device scratch of at least paged_decode_workspace_bytes(...)
+ *                bytes (may be NULL when that is 0).
+ * Supported: head_dim in {64, 128}; num_q_heads / num_kv_heads <= 8;
+ * block_size a multiple of 16 up to 256; F16/BF16 caches need q_dtype equal
+ * to kv_dtype; FP8/INT4 caches take F16 or BF16 q.
+ */
+int paged_decode_attention(const void* q, int q_dtype,
+                           const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, int max_blocks_per_seq,
+                           const int32_t* context_lens, int num_seqs,
+                           const void* scales, int kv_dtype, int num_blocks,
+                           void* out, float softmax_scale,
+                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                           int partition_size, void* workspace, size_t workspace_bytes,
+                           int* dev_status, void* stream);
+
+/* Partition size paged_decode_attention will use for these arguments
+ * (resolves partition_size == 0); 0 if the arguments are invalid. */
+int paged_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                int max_blocks_per_seq, int block_size, int partition_size);
+
+/* Workspace bytes paged_decode_attention needs for these arguments (0 when
+ * every sequence fits one partition). */
+size_t paged_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                    int head_dim, int max_blocks_per_seq, int block_size,
+                                    int partition_size);
+
+/* Human-readable name of a pkv_status value. */
+const char* paged_kv_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int paged_kv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

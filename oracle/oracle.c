@@ -34,7 +34,8 @@
  *  R5  FP8 code = E4M3 round-to-nearest-even with saturation to +-448 of
  *      the fp32 quotient x / scale (one IEEE fp32 division).
  *  R6  INT4: per (token, kv-head, 32 consecutive d), asymmetric:
- *      scale = fp16(fp32(max - min) / 15), zero = fp16(min),
+ *      scale = fp16(fp32(max - min + 0) / 15), zero = fp16(min + 0) (the
+ *      "+ 0" makes a signed-zero min or range +0),
  *      code = clamp(rint((x - zero) / scale), 0, 15) in fp32 (0 if scale is
  *      0); element 2i in the low nibble of byte i, 2i+1 in the high nibble.
  *  R7  context_len == 0 gives out = 0; slot -1 means "skip this token".
@@ -275,9 +276,11 @@ static void encode_row(const float* x, int head_dim, int kv_dtype, uint8_t* dst,
             if (xg[i] < mn) mn = xg[i];
             if (xg[i] > mx) mx = xg[i];
         }
-        float range = mx - mn;
+        /* "+ 0.0f" turns a -0 minimum or range into +0, so the stored bits do
+         * not depend on which of two signed zeros a min/max search meets first */
+        float range = (mx - mn) + 0.0f;
         uint16_t sh = oracle_f32_to_f16_rne(range / 15.0f);
-        uint16_t zh = oracle_f32_to_f16_rne(mn);
+        uint16_t zh = oracle_f32_to_f16_rne(mn + 0.0f);
         float sf = (float)oracle_f16_to_double(sh);
         float zf = (float)oracle_f16_to_double(zh);
         int4_pairs[2 * g] = sh;

@@ -1,0 +1,759 @@
+// paged_decode_attention: decode-phase PagedAttention over a paged, optionally
+// quantized KV cache, with split-KV partitions merged by log-sum-exp.
+//
+// What it computes (softmax(q K^T / sqrt(d)) V per query head, GQA groups
+// sharing one KV head: "KV Cache Optimization: 3x Faster LLM Inference",
+// GQA section; the per-head walk over logical blocks -> physical blocks ->
+// K, V -> scores -> softmax -> weighted sum: "KV Cache Compression & Paged
+// Attention", Implementation Details):
+//   out[b,h] = sum_t exp(s_t - max) V_t / sum_t exp(s_t - max),
+//   s_t = softmax_scale * q[b,h] . K_t, t < context_lens[b],
+//   K_t, V_t read at block_tables[b][t / bs], offset t % bs, dequantized.
+//
+// Design (GB300, sm_103a):
+//  * CTA = (partition, KV head, sequence), 4 warps.  Every warp walks its own
+//    16-token tiles of the partition (tiles w, w+4, ...) with its own online
+//    softmax state; the warps merge through shared memory at the end.
+//  * Each warp stages its tiles in a private shared-memory ring with 16-byte
+//    cp.async copies (K rows, V rows, INT4 scale rows, FP8 block scales), a
+//    few tiles ahead, so several KB per warp are in flight from HBM.  The
+//    16-byte chunks are XOR-swizzled per row so the fragment reads below hit
+//    all 32 banks.
+//  * The G query heads of one KV head are the N=8 columns of an
+//    mma.sync.m16n8k16: S^T[t, g] = K_tile(16 x D) . Q^T(D x 8) and
+//    O^T[d, g] += V_tile^T(D x 16) . P^T(16 x 8), fp32 accumulate.  Each K/V
+//    element is read once from shared memory, converted in registers and used
+//    for all G heads.  FP8 codes become exact f16 (cvt.rn.f16x2.e4m3x2); INT4
+//    codes become exact f16 0..15 (mantissa trick); the scales are applied
+//    outside the products (FP8: per tile; INT4: per token and group, with the
+//    zero point through sum(q) and sum(p)).
+//  * The probabilities P enter the second product as a hi + lo pair of 16-bit
+//    values (P = hi + lo to ~2^-17 relative), so rounding P to 16 bits costs
+//    no accuracy; f16 pairs are pre-scaled by 2^8 (2^0 for INT4) to stay
+//    clear of f16 subnormals.
+//  * With more than one partition each CTA writes (max, sum, O/sum) per head
+//    to the workspace and pkv_lse_reduce merges them.
+#include <math.h>
+
+#include <atomic>
+
+#include "pkv_common.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kDecodeWarps = 4;
+constexpr int kTile = 16;            // tokens per tile (the mma M / K extent)
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int KV, int D> struct Geo {
+  static constexpr bool kHalf = (KV == PKV_F16 || KV == PKV_BF16);
+  static constexpr int kRowBytes = kHalf ? 2 * D : (KV == PKV_FP8_E4M3 ? D : D / 2);
+  static constexpr int kCpr = kRowBytes / 16;                   // 16-byte chunks per row
+  static constexpr int kTileBytes = kTile * kRowBytes;          // one of K or V
+  static constexpr int kScaleRowBytes = (KV == PKV_INT4_G32) ? (D / 32) * 4 : 0;
+  static constexpr int kScaleTileBytes = kTile * kScaleRowBytes;
+  // stage: K tile | V tile | K scale rows | V scale rows | 16 B misc (FP8 scales, phys)
+  static constexpr int kStageBytes = 2 * kTileBytes + 2 * kScaleTileBytes + 16;
+  static constexpr int kStages = kHalf ? 3 : (KV == PKV_FP8_E4M3 ? 4 : 6);
+  static constexpr int kWarpRing = kStages * kStageBytes;
+  static constexpr int kRingBytes = kDecodeWarps * kWarpRing;
+  static constexpr int kMergeBytes = kDecodeWarps * 8 * (D + 2) * 4;
+  static constexpr int kSmemBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
+};
+
+// XOR swizzle of the 16-byte chunk position within a row (see the bank
+// analysis in the fragment readers below).
+template <int KV, int D>
+__device__ __forceinline__ int swz(int r) {
+  if constexpr (KV == PKV_F16 || KV == PKV_BF16 || (KV == PKV_FP8_E4M3 && D == 128)) {
+    return (((r ^ (r >> 1)) & 1) << 2) | ((r >> 2) & 1);
+  } else if constexpr (KV == PKV_INT4_G32) {
+    return D == 128 ? ((r >> 1) & 3) : ((r >> 1) & 1);
+  } else {
+    return 0;
+  }
+}
+
+template <int KV, int D>
+__device__ __forceinline__ uint32_t chunk_off(int row, int ch) {
+  using G = Geo<KV, D>;
+  return static_cast<uint32_t>((row * G::kCpr + (ch ^ swz<KV, D>(row))) * 16);
+}
+
+struct Params {
+  const uint16_t* q;
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const void* scales;
+  void* out;
+  float* ws_out;
+  float* ws_ml;
+  int* dev_status;
+  int max_blocks_per_seq;
+  int num_blocks;
+  int num_q_heads;
+  int num_kv_heads;
+  int block_size;
+  int partition_size;
+  int num_partitions;
+  float softmax_scale;
+};
+
+// Issue the copies of one 16-token tile into a stage (lane-parallel).
+template <int KV, int D>
+__device__ __forceinline__ void issue_tile(const Params& p, int b, int kvh, int t0,
+                                           uint32_t stage, uint8_t* stage_ptr, int lane) {
+  using G = Geo<KV, D>;
+  const int logical = t0 / p.block_size;
+  const int phys = p.block_tables[static_cast<int64_t>(b) * p.max_blocks_per_seq + logical];
+  const bool ok = phys >= 0 && phys < p.num_blocks;
+  int* misc = reinterpret_cast<int*>(stage_ptr + G::kStageBytes - 16);
+  if (lane == 0) misc[2] = ok ? 1 : 0;
+  if (!ok) {
+    if (lane == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  const int off = t0 - logical * p.block_size;
+  const int64_t row0 = (static_cast<int64_t>(phys) * p.num_kv_heads + kvh) * p.block_size + off;
+  const uint8_t* ksrc = p.k_cache + row0 * G::kRowBytes;
+  const uint8_t* vsrc = p.v_cache + row0 * G::kRowBytes;
+  constexpr int kChunks = G::kTileBytes / 16;
+#pragma unroll
+  for (int i = 0; i < (kChunks + kWarp - 1) / kWarp; ++i) {
+    const int ch = lane + i * kWarp;
+    if (kChunks % kWarp == 0 || ch < kChunks) {
+      const int r = ch / G::kCpr, c = ch % G::kCpr;
+      const uint32_t o = chunk_off<KV, D>(r, c);
+      cp_async_16(stage + o, ksrc + ch * 16);
+      cp_async_16(stage + G::kTileBytes + o, vsrc + ch * 16);
+    }
+  }
+  if constexpr (KV == PKV_INT4_G32) {
+    // (scale, zero) rows of the tile's 16 tokens, K then V: contiguous runs
+    constexpr int kSc = G::kScaleTileBytes / 16;            // 16 (D=128) or 8 (D=64)
+    const uint16_t* sc = static_cast<const uint16_t*>(p.scales);
+    const int64_t per_kv = static_cast<int64_t>(p.num_blocks) * p.num_kv_heads * p.block_size *
+                           (D / 32) * 2;
+    const uint8_t* ksc = reinterpret_cast<const uint8_t*>(sc + row0 * (D / 32) * 2);
+    const uint8_t* vsc = reinterpret_cast<const uint8_t*>(sc + per_kv + row0 * (D / 32) * 2);
+    if (lane < kSc) {
+      cp_async_16(stage + 2 * G::kTileBytes + lane * 16, ksc + lane * 16);
+    } else if (lane >= 16 && lane < 16 + kSc) {
+      cp_async_16(stage + 2 * G::kTileBytes + G::kScaleTileBytes + (lane - 16) * 16,
+                  vsc + (lane - 16) * 16);
+    }
+  } else if constexpr (KV == PKV_FP8_E4M3) {
+    const float* sc = static_cast<const float*>(p.scales);
+    const int64_t idx = static_cast<int64_t>(phys) * p.num_kv_heads + kvh;
+    const int64_t per_kv = static_cast<int64_t>(p.num_blocks) * p.num_kv_heads;
+    const uint32_t mo = stage + G::kStageBytes - 16;
+    if (lane == 0) asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(mo), "l"(sc + idx) : "memory");
+    if (lane == 1) asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(mo + 4), "l"(sc + per_kv + idx) : "memory");
+  }
+}
+
+template <int KV, int QT, int D>
+__global__ void __launch_bounds__(kDecodeWarps * kWarp)
+paged_decode_kernel(const Params p) {
+  using G = Geo<KV, D>;
+  constexpr bool kHalf = G::kHalf;
+  constexpr int MT = D / 16;                 // m-tiles of O^T (and k-steps of S^T)
+  // mma operand type: the cache's type for 16-bit caches, f16 for FP8/INT4
+  constexpr int MMA_T = kHalf ? KV : PKV_F16;
+  constexpr float kPScale = (KV == PKV_BF16) ? 1.f : (KV == PKV_INT4_G32 ? 1.f : 256.f);
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int q4 = lane >> 2, c4 = lane & 3;   // mma groupID / thread-in-group
+  const int part = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int group = p.num_q_heads / p.num_kv_heads;
+  // a context longer than its table row can hold is clamped (and flagged)
+  const int cap = p.max_blocks_per_seq * p.block_size;
+  int ctx = p.context_lens[b];
+  if (ctx > cap) {
+    if (threadIdx.x == 0 && part == 0 && kvh == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
+    ctx = cap;
+  }
+  const int tok_begin = part * p.partition_size;
+  if (part > 0 && tok_begin >= ctx) return;
+  const int tok_end = min(ctx, tok_begin + p.partition_size);
+  const int ntiles = ctx > 0 ? (tok_end - tok_begin + kTile - 1) / kTile : 0;
+
+  // ---------------------------------------------------------------- Q fragments
+  // B operand of S^T = K Q^T: column n = head q4 of the group, rows = d in the
+  // order the K fragments below use.  Heads >= group are zero columns.
+  const int hq = kvh * group + q4;
+  const bool head_ok = q4 < group;
+  const uint16_t* qrow = p.q + (static_cast<int64_t>(b) * p.num_q_heads + (head_ok ? hq : 0)) * D;
+  uint32_t qb[MT][2];
+  float qexp = 1.f;                            // score multiplier undoing the f16 Q scaling
+  float qsum[kHalf ? 1 : D / 32][2];           // INT4: sum of q over each group (heads 2c4, 2c4+1)
+  if constexpr (kHalf) {
+#pragma unroll
+    for (int jp = 0; jp < D / 32; ++jp) {
+      uint4 v = head_ok ? ld_global_nc_v4(qrow + 8 * (4 * jp + c4)) : make_uint4(0, 0, 0, 0);
+      qb[2 * jp][0] = v.x; qb[2 * jp][1] = v.y;
+      qb[2 * jp + 1][0] = v.z; qb[2 * jp + 1][1] = v.w;
+    }
+    qsum[0][0] = qsum[0][1] = 0.f;
+  } else {
+    // each thread's 32 d values, as float
+    float qf[32];
+    if constexpr (KV == PKV_FP8_E4M3) {
+      // d = 16*(4i + c4) + 0..15 for i < D/64
+#pragma unroll
+      for (int i = 0; i < D / 64; ++i) {
+#pragma unroll
+        for (int hlf = 0; hlf < 2; ++hlf) {
+          uint4 v = head_ok ? ld_global_nc_v4(qrow + 16 * (4 * i + c4) + 8 * hlf) : make_uint4(0, 0, 0, 0);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            qf[16 * i + 8 * hlf + 2 * k] = Half16<QT>::to_float(w[k] & 0xFFFF);
+            qf[16 * i + 8 * hlf + 2 * k + 1] = Half16<QT>::to_float(w[k] >> 16);
+          }
+        }
+      }
+    } else {
+      // INT4: d = 32*grp + 8*c4 + 0..7
+#pragma unroll
+      for (int grp = 0; grp < D / 32; ++grp) {
+        uint4 v = head_ok ? ld_global_nc_v4(qrow + 32 * grp + 8 * c4) : make_uint4(0, 0, 0, 0);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          qf[8 * grp + 2 * k] = Half16<QT>::to_float(w[k] & 0xFFFF);
+          qf[8 * grp + 2 * k + 1] = Half16<QT>::to_float(w[k] >> 16);
+        }
+      }
+    }
+    constexpr int NQ = D / 4;                  // values per thread: 32 (D=128) or 16 (D=64)
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) amax = fmaxf(amax, fabsf(qf[i]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    // keep |q| * 2^-e below 2^15 so the f16 copy is exact in the normal range
+    int e = 0;
+    if (amax >= 32768.f) e = ilogbf(amax) - 14;
+    const float qs = ldexpf(1.f, -e);
+    qexp = ldexpf(1.f, e);
+    if constexpr (KV == PKV_FP8_E4M3) {
+      // k-step 4i+h: lo pair = d 16(4i+c4) + 4h + {0,1}, hi pair = + 4h + {2,3}
+#pragma unroll
+      for (int i = 0; i < D / 64; ++i)
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          qb[4 * i + h][0] = Half16<PKV_F16>::pack_rn(qf[16 * i + 4 * h] * qs, qf[16 * i + 4 * h + 1] * qs);
+          qb[4 * i + h][1] = Half16<PKV_F16>::pack_rn(qf[16 * i + 4 * h + 2] * qs, qf[16 * i + 4 * h + 3] * qs);
+        }
+    } else {
+      // k-step 2grp+h: lo pair = d (8c4 + 2h, 8c4 + 2h + 4), hi pair = (8c4 + 2h + 1, 8c4 + 2h + 5)
+#pragma unroll
+      for (int grp = 0; grp < D / 32; ++grp) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float* x = qf + 8 * grp;
+          qb[2 * grp + h][0] = Half16<PKV_F16>::pack_rn(x[2 * h] * qs, x[2 * h + 4] * qs);
+          qb[2 * grp + h][1] = Half16<PKV_F16>::pack_rn(x[2 * h + 1] * qs, x[2 * h + 5] * qs);
+        }
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) s += qf[8 * grp + k];
+        s += __shfl_xor_sync(0xffffffffu, s, 1);
+        s += __shfl_xor_sync(0xffffffffu, s, 2);        // sum over d of head q4, group grp
+        qsum[grp][0] = __shfl_sync(0xffffffffu, s, (2 * c4) * 4);
+        qsum[grp][1] = __shfl_sync(0xffffffffu, s, (2 * c4 + 1) * 4);
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- state
+  float oacc[MT][4];
+#pragma unroll
+  for (int i = 0; i < MT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+  float mrow[2] = {-INFINITY, -INFINITY};    // running max (log2 units), heads 2c4, 2c4+1
+  float lrow[2] = {0.f, 0.f};                // this thread's share of the running sum
+  float zacc[KV == PKV_INT4_G32 ? D / 32 : 1][2];
+#pragma unroll
+  for (int g = 0; g < (KV == PKV_INT4_G32 ? D / 32 : 1); ++g) zacc[g][0] = zacc[g][1] = 0.f;
+  float vscale_cur = 1.f;                    // FP8: oacc is in units of this V scale
+  const float base = p.softmax_scale * kLog2e * qexp;
+
+  uint8_t* ring_ptr = smem + warp * G::kWarpRing;
+  const uint32_t ring = smem_u32(ring_ptr);
+
+  // ---------------------------------------------------------------- pipeline
+#pragma unroll
+  for (int s = 0; s < G::kStages; ++s) {
+    const int tile = warp + s * kDecodeWarps;
+    if (tile < ntiles)
+      issue_tile<KV, D>(p, b, kvh, tok_begin + tile * kTile, ring + s * G::kStageBytes,
+                        ring_ptr + s * G::kStageBytes, lane);
+    cp_async_commit();
+  }
+
+  int stage = 0;
+  for (int it = 0;; ++it) {
+    const int tile = warp + it * kDecodeWarps;
+    if (tile >= ntiles) break;
+    cp_async_wait<G::kStages - 1>();
+    __syncwarp();
+    const uint32_t st = ring + stage * G::kStageBytes;
+    const uint8_t* st_ptr = ring_ptr + stage * G::kStageBytes;
+    const int* misc = reinterpret_cast<const int*>(st_ptr + G::kStageBytes - 16);
+    const int t0 = tok_begin + tile * kTile;
+    const int nvalid = misc[2] ? min(kTile, tok_end - t0) : 0;
+
+    if (nvalid > 0) {
+      // ------------------------------------------------ S^T = K_tile Q^T
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (kHalf) {
+#pragma unroll
+        for (int jp = 0; jp < D / 32; ++jp) {
+          // thread reads chunk 4jp+c4 of rows q4 and q4+8: words = d pairs
+          const uint4 r0 = ld_shared_v4(st + chunk_off<KV, D>(q4, 4 * jp + c4));
+          const uint4 r1 = ld_shared_v4(st + chunk_off<KV, D>(q4 + 8, 4 * jp + c4));
+          const uint32_t a0[4] = {r0.x, r1.x, r0.y, r1.y};
+          mma_16816<MMA_T>(sc, a0, qb[2 * jp][0], qb[2 * jp][1]);
+          const uint32_t a1[4] = {r0.z, r1.z, r0.w, r1.w};
+          mma_16816<MMA_T>(sc, a1, qb[2 * jp + 1][0], qb[2 * jp + 1][1]);
+        }
+      } else if constexpr (KV == PKV_FP8_E4M3) {
+#pragma unroll
+        for (int i = 0; i < D / 64; ++i) {
+          const uint4 r0 = ld_shared_v4(st + chunk_off<KV, D>(q4, 4 * i + c4));
+          const uint4 r1 = ld_shared_v4(st + chunk_off<KV, D>(q4 + 8, 4 * i + c4));
+          const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w};
+          const uint32_t w1[4] = {r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const uint32_t a[4] = {e4m3x2_to_f16x2(w0[h] & 0xFFFF), e4m3x2_to_f16x2(w1[h] & 0xFFFF),
+                                   e4m3x2_to_f16x2(w0[h] >> 16), e4m3x2_to_f16x2(w1[h] >> 16)};
+            mma_16816<PKV_F16>(sc, a, qb[4 * i + h][0], qb[4 * i + h][1]);
+          }
+        }
+      } else {
+        // INT4: one fresh accumulator per 32-element group, then
+        // s += scale_t * acc + zero_t * sum(q)
+        constexpr int SR = G::kScaleRowBytes;
+        const uint32_t ksc = st + 2 * G::kTileBytes;
+        uint32_t sz0[D / 32], sz1[D / 32];
+        if constexpr (D == 128) {
+          const uint4 a = ld_shared_v4(ksc + q4 * SR), c = ld_shared_v4(ksc + (q4 + 8) * SR);
+          sz0[0] = a.x; sz0[1] = a.y; sz0[2] = a.z; sz0[3] = a.w;
+          sz1[0] = c.x; sz1[1] = c.y; sz1[2] = c.z; sz1[3] = c.w;
+        } else {
+          const uint2 a = ld_shared_v2(ksc + q4 * SR), c = ld_shared_v2(ksc + (q4 + 8) * SR);
+          sz0[0] = a.x; sz0[1] = a.y; sz1[0] = c.x; sz1[1] = c.y;
+        }
+#pragma unroll
+        for (int grp = 0; grp < D / 32; ++grp) {
+          const uint32_t w0 = ld_shared_b32(st + q4 * G::kRowBytes + 16 * (grp ^ swz<KV, D>(q4)) + 4 * c4);
+          const uint32_t w1 = ld_shared_b32(st + (q4 + 8) * G::kRowBytes +
+                                            16 * (grp ^ swz<KV, D>(q4 + 8)) + 4 * c4);
+          float g4[4] = {0.f, 0.f, 0.f, 0.f};
+          const uint32_t a0[4] = {nibbles_to_f16x2(w0, 0), nibbles_to_f16x2(w1, 0),
+                                  nibbles_to_f16x2(w0, 1), nibbles_to_f16x2(w1, 1)};
+          mma_16816<PKV_F16>(g4, a0, qb[2 * grp][0], qb[2 * grp][1]);
+          const uint32_t a1[4] = {nibbles_to_f16x2(w0, 2), nibbles_to_f16x2(w1, 2),
+                                  nibbles_to_f16x2(w0, 3), nibbles_to_f16x2(w1, 3)};
+          mma_16816<PKV_F16>(g4, a1, qb[2 * grp + 1][0], qb[2 * grp + 1][1]);
+          const float2 f0 = Half16<PKV_F16>::unpack(sz0[grp]);   // (scale, zero) token q4
+          const float2 f1 = Half16<PKV_F16>::unpack(sz1[grp]);   // token q4 + 8
+          sc[0] += f0.x * qexp * g4[0] + f0.y * qsum[grp][0];
+          sc[1] += f0.x * qexp * g4[1] + f0.y * qsum[grp][1];
+          sc[2] += f1.x * qexp * g4[2] + f1.y * qsum[grp][0];
+          sc[3] += f1.x * qexp * g4[3] + f1.y * qsum[grp][1];
+        }
+      }
+
+      // ------------------------------------------------ scale, mask, online softmax
+      float mult = base;
+      float vs_tile = 1.f;
+      if constexpr (KV == PKV_FP8_E4M3) {
+        const float* fs = reinterpret_cast<const float*>(misc);
+        mult *= fs[0];
+        vs_tile = fs[1];
+      } else if constexpr (KV == PKV_INT4_G32) {
+        mult = p.softmax_scale * kLog2e;       // qexp already folded into the group sums
+      }
+      const bool v0 = q4 < nvalid, v1 = q4 + 8 < nvalid;
+      sc[0] = v0 ? sc[0] * mult : -INFINITY;
+      sc[1] = v0 ? sc[1] * mult : -INFINITY;
+      sc[2] = v1 ? sc[2] * mult : -INFINITY;
+      sc[3] = v1 ? sc[3] * mult : -INFINITY;
+      float tmax0 = fmaxf(sc[0], sc[2]), tmax1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        tmax0 = fmaxf(tmax0, __shfl_xor_sync(0xffffffffu, tmax0, o));
+        tmax1 = fmaxf(tmax1, __shfl_xor_sync(0xffffffffu, tmax1, o));
+      }
+      const float mnew0 = fmaxf(mrow[0], tmax0), mnew1 = fmaxf(mrow[1], tmax1);
+      // mnew is finite: at least one token of the tile is valid
+      float alpha0 = exp2f(mrow[0] - mnew0), alpha1 = exp2f(mrow[1] - mnew1);
+      mrow[0] = mnew0; mrow[1] = mnew1;
+      const float pr[4] = {exp2f(sc[0] - mnew0), exp2f(sc[1] - mnew1),
+                           exp2f(sc[2] - mnew0), exp2f(sc[3] - mnew1)};
+      lrow[0] = lrow[0] * alpha0 + pr[0] + pr[2];
+      lrow[1] = lrow[1] * alpha1 + pr[1] + pr[3];
+      if constexpr (KV == PKV_FP8_E4M3) {
+        // keep oacc in units of the current tile's V scale
+        const float ratio = vscale_cur / vs_tile;
+        alpha0 *= ratio; alpha1 *= ratio;
+        vscale_cur = vs_tile;
+      }
+#pragma unroll
+      for (int i = 0; i < MT; ++i) {
+        oacc[i][0] *= alpha0; oacc[i][1] *= alpha1;
+        oacc[i][2] *= alpha0; oacc[i][3] *= alpha1;
+      }
+      if constexpr (KV == PKV_INT4_G32) {
+#pragma unroll
+        for (int g = 0; g < D / 32; ++g) { zacc[g][0] *= alpha0; zacc[g][1] *= alpha1; }
+      }
+
+      // ------------------------------------------------ O^T += V_tile^T P^T
+      const uint32_t vt = st + G::kTileBytes;
+      // rows (tokens) this thread's V fragments cover: 2c4, 2c4+1, 2c4+8, 2c4+9
+      const int tA = 2 * c4, tB = 2 * c4 + 1, tC = 2 * c4 + 8, tE = 2 * c4 + 9;
+      const bool partial = nvalid < kTile;
+      const uint32_t mA = (tA < nvalid) ? 0xFFFFFFFFu : 0u, mB = (tB < nvalid) ? 0xFFFFFFFFu : 0u;
+      const uint32_t mC = (tC < nvalid) ? 0xFFFFFFFFu : 0u, mE = (tE < nvalid) ? 0xFFFFFFFFu : 0u;
+
+      if constexpr (KV != PKV_INT4_G32) {
+        // P as B fragments (hi + lo split)
+        using H = Half16<MMA_T>;
+        const float pp[4] = {pr[0] * kPScale, pr[1] * kPScale, pr[2] * kPScale, pr[3] * kPScale};
+        const uint32_t h01 = H::pack_rn(pp[0], pp[1]), h23 = H::pack_rn(pp[2], pp[3]);
+        const float2 f01 = H::unpack(h01), f23 = H::unpack(h23);
+        const uint32_t l01 = H::pack_rn(pp[0] - f01.x, pp[1] - f01.y);
+        const uint32_t l23 = H::pack_rn(pp[2] - f23.x, pp[3] - f23.y);
+        const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+        const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+
+        if constexpr (kHalf) {
+#pragma unroll
+          for (int hc = 0; hc < D / 64; ++hc) {
+            // chunk (D/64 == 2 ? 2*q4 + hc : q4): d = 16*q4 + 8*hc + 0..7 (D=128) or 8*q4 + 0..7
+            const int ch = (D == 128) ? 2 * q4 + hc : q4;
+            uint4 A = ld_shared_v4(vt + chunk_off<KV, D>(tA, ch));
+            uint4 B = ld_shared_v4(vt + chunk_off<KV, D>(tB, ch));
+            uint4 C = ld_shared_v4(vt + chunk_off<KV, D>(tC, ch));
+            uint4 E = ld_shared_v4(vt + chunk_off<KV, D>(tE, ch));
+            if (partial) {
+              A.x &= mA; A.y &= mA; A.z &= mA; A.w &= mA;
+              B.x &= mB; B.y &= mB; B.z &= mB; B.w &= mB;
+              C.x &= mC; C.y &= mC; C.z &= mC; C.w &= mC;
+              E.x &= mE; E.y &= mE; E.z &= mE; E.w &= mE;
+            }
+            const uint32_t wa[4] = {A.x, A.y, A.z, A.w}, wb[4] = {B.x, B.y, B.z, B.w};
+            const uint32_t wc[4] = {C.x, C.y, C.z, C.w}, we[4] = {E.x, E.y, E.z, E.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int i = 4 * hc + k;                       // m-tile: d = base + 2i (+1)
+              const uint32_t a[4] = {__byte_perm(wa[k], wb[k], 0x5410), __byte_perm(wa[k], wb[k], 0x7632),
+                                     __byte_perm(wc[k], we[k], 0x5410), __byte_perm(wc[k], we[k], 0x7632)};
+              mma_16816<MMA_T>(oacc[i], a, bh0, bh1);
+              mma_16816<MMA_T>(oacc[i], a, bl0, bl1);
+            }
+          }
+        } else {
+          // FP8: d = base(q4) + 0..15 (D=128) or 8*q4 + 0..7 (D=64)
+          constexpr int NW = D / 32;                          // words per token: 4 or 2
+          uint32_t wa[NW], wb[NW], wc[NW], we[NW];
+          if constexpr (D == 128) {
+            const int pi = ((q4 & 1) << 1) | ((q4 >> 1) & 1) | (q4 & 4);
+            const uint4 A = ld_shared_v4(vt + chunk_off<KV, D>(tA, pi));
+            const uint4 B = ld_shared_v4(vt + chunk_off<KV, D>(tB, pi));
+            const uint4 C = ld_shared_v4(vt + chunk_off<KV, D>(tC, pi));
+            const uint4 E = ld_shared_v4(vt + chunk_off<KV, D>(tE, pi));
+            wa[0] = A.x; wa[1] = A.y; wa[2] = A.z; wa[3] = A.w;
+            wb[0] = B.x; wb[1] = B.y; wb[2] = B.z; wb[3] = B.w;
+            wc[0] = C.x; wc[1] = C.y; wc[2] = C.z; wc[3] = C.w;
+            we[0] = E.x; we[1] = E.y; we[2] = E.z; we[3] = E.w;
+          } else {
+            const uint2 A = ld_shared_v2(vt + tA * G::kRowBytes + 8 * q4);
+            const uint2 B = ld_shared_v2(vt + tB * G::kRowBytes + 8 * q4);
+            const uint2 C = ld_shared_v2(vt + tC * G::kRowBytes + 8 * q4);
+            const uint2 E = ld_shared_v2(vt + tE * G::kRowBytes + 8 * q4);
+            wa[0] = A.x; wa[1] = A.y; wb[0] = B.x; wb[1] = B.y;
+            wc[0] = C.x; wc[1] = C.y; we[0] = E.x; we[1] = E.y;
+          }
+          if (partial) {
+#pragma unroll
+            for (int k = 0; k < NW; ++k) { wa[k] &= mA; wb[k] &= mB; wc[k] &= mC; we[k] &= mE; }
+          }
+#pragma unroll
+          for (int k = 0; k < NW; ++k) {
+            const uint32_t x01 = __byte_perm(wa[k], wb[k], 0x5140), x23 = __byte_perm(wa[k], wb[k], 0x7362);
+            const uint32_t y01 = __byte_perm(wc[k], we[k], 0x5140), y23 = __byte_perm(wc[k], we[k], 0x7362);
+            const uint32_t a0[4] = {e4m3x2_to_f16x2(x01 & 0xFFFF), e4m3x2_to_f16x2(x01 >> 16),
+                                    e4m3x2_to_f16x2(y01 & 0xFFFF), e4m3x2_to_f16x2(y01 >> 16)};
+            mma_16816<PKV_F16>(oacc[2 * k], a0, bh0, bh1);
+            mma_16816<PKV_F16>(oacc[2 * k], a0, bl0, bl1);
+            const uint32_t a1[4] = {e4m3x2_to_f16x2(x23 & 0xFFFF), e4m3x2_to_f16x2(x23 >> 16),
+                                    e4m3x2_to_f16x2(y23 & 0xFFFF), e4m3x2_to_f16x2(y23 >> 16)};
+            mma_16816<PKV_F16>(oacc[2 * k + 1], a1, bh0, bh1);
+            mma_16816<PKV_F16>(oacc[2 * k + 1], a1, bl0, bl1);
+          }
+        }
+      } else {
+        // INT4: P'_g = p * scale_t,g per group g; zero point through sum_t z_t,g p_t
+        constexpr int SR = G::kScaleRowBytes;
+        const uint32_t vsc = st + 2 * G::kTileBytes + G::kScaleTileBytes;
+        uint32_t sz0[D / 32], sz1[D / 32];
+        if constexpr (D == 128) {
+          const uint4 a = ld_shared_v4(vsc + q4 * SR), c = ld_shared_v4(vsc + (q4 + 8) * SR);
+          sz0[0] = a.x; sz0[1] = a.y; sz0[2] = a.z; sz0[3] = a.w;
+          sz1[0] = c.x; sz1[1] = c.y; sz1[2] = c.z; sz1[3] = c.w;
+        } else {
+          const uint2 a = ld_shared_v2(vsc + q4 * SR), c = ld_shared_v2(vsc + (q4 + 8) * SR);
+          sz0[0] = a.x; sz0[1] = a.y; sz1[0] = c.x; sz1[1] = c.y;
+        }
+        using H = Half16<PKV_F16>;
+#pragma unroll
+        for (int grp = 0; grp < D / 32; ++grp) {
+          const float2 f0 = H::unpack(sz0[grp]), f1 = H::unpack(sz1[grp]);
+          // masked tokens have p == 0; keep stale scales out of the products
+          const float pp0 = pr[0] > 0.f ? pr[0] * f0.x : 0.f, pp1 = pr[1] > 0.f ? pr[1] * f0.x : 0.f;
+          const float pp2 = pr[2] > 0.f ? pr[2] * f1.x : 0.f, pp3 = pr[3] > 0.f ? pr[3] * f1.x : 0.f;
+          zacc[grp][0] += (pr[0] > 0.f ? pr[0] * f0.y : 0.f) + (pr[2] > 0.f ? pr[2] * f1.y : 0.f);
+          zacc[grp][1] += (pr[1] > 0.f ? pr[1] * f0.y : 0.f) + (pr[3] > 0.f ? pr[3] * f1.y : 0.f);
+          const uint32_t h01 = H::pack_rn(pp0, pp1), h23 = H::pack_rn(pp2, pp3);
+          const float2 g01 = H::unpack(h01), g23 = H::unpack(h23);
+          const uint32_t l01 = H::pack_rn(pp0 - g01.x, pp1 - g01.y);
+          const uint32_t l23 = H::pack_rn(pp2 - g23.x, pp3 - g23.y);
+          const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+          const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+          const uint32_t rowoff = 2 * q4;
+          const uint32_t hA = ld_shared_u16(vt + tA * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tA)) + rowoff);
+          const uint32_t hB = ld_shared_u16(vt + tB * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tB)) + rowoff);
+          const uint32_t hC = ld_shared_u16(vt + tC * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tC)) + rowoff);
+          const uint32_t hE = ld_shared_u16(vt + tE * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tE)) + rowoff);
+          const uint32_t x = hA | (hB << 16), y = hC | (hE << 16);
+          const uint32_t a0[4] = {nibbles_to_f16x2(x, 0), nibbles_to_f16x2(x, 1),
+                                  nibbles_to_f16x2(y, 0), nibbles_to_f16x2(y, 1)};
+          mma_16816<PKV_F16>(oacc[2 * grp], a0, bh0, bh1);
+          mma_16816<PKV_F16>(oacc[2 * grp], a0, bl0, bl1);
+          const uint32_t a1[4] = {nibbles_to_f16x2(x, 2), nibbles_to_f16x2(x, 3),
+                                  nibbles_to_f16x2(y, 2), nibbles_to_f16x2(y, 3)};
+          mma_16816<PKV_F16>(oacc[2 * grp + 1], a1, bh0, bh1);
+          mma_16816<PKV_F16>(oacc[2 * grp + 1], a1, bl0, bl1);
+        }
+      }
+    }
+    __syncwarp();
+    const int next = warp + (it + G::kStages) * kDecodeWarps;
+    if (next < ntiles)
+      issue_tile<KV, D>(p, b, kvh, tok_begin + next * kTile, st, ring_ptr + stage * G::kStageBytes, lane);
+    cp_async_commit();
+    stage = (stage + 1 == G::kStages) ? 0 : stage + 1;
+  }
+  cp_async_wait<0>();
+
+  // ---------------------------------------------------------------- warp epilogue
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    lrow[0] += __shfl_xor_sync(0xffffffffu, lrow[0], o);
+    lrow[1] += __shfl_xor_sync(0xffffffffu, lrow[1], o);
+  }
+  float post = 1.f / kPScale;
+  if constexpr (KV == PKV_FP8_E4M3) post *= vscale_cur;
+#pragma unroll
+  for (int i = 0; i < MT; ++i)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) oacc[i][k] *= post;
+  if constexpr (KV == PKV_INT4_G32) {
+#pragma unroll
+    for (int g = 0; g < D / 32; ++g) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        zacc[g][0] += __shfl_xor_sync(0xffffffffu, zacc[g][0], o);
+        zacc[g][1] += __shfl_xor_sync(0xffffffffu, zacc[g][1], o);
+      }
+      oacc[2 * g][0] += zacc[g][0]; oacc[2 * g][2] += zacc[g][0];
+      oacc[2 * g][1] += zacc[g][1]; oacc[2 * g][3] += zacc[g][1];
+      oacc[2 * g + 1][0] += zacc[g][0]; oacc[2 * g + 1][2] += zacc[g][0];
+      oacc[2 * g + 1][1] += zacc[g][1]; oacc[2 * g + 1][3] += zacc[g][1];
+    }
+  }
+
+  __syncthreads();   // every warp is done with its ring: reuse it for the merge
+  float* mo = reinterpret_cast<float*>(smem);                 // [warp][8][D]
+  float* ml = mo + kDecodeWarps * 8 * D;                      // [warp][8][2]
+#pragma unroll
+  for (int i = 0; i < MT; ++i) {
+    int d0;
+    if constexpr (KV == PKV_INT4_G32) {
+      d0 = 32 * (i >> 1) + 4 * q4 + 2 * (i & 1);
+    } else if constexpr (KV == PKV_FP8_E4M3 && D == 128) {
+      d0 = 16 * (((q4 & 1) << 1) | ((q4 >> 1) & 1) | (q4 & 4)) + 2 * i;
+    } else {
+      d0 = (D == 128 ? 16 : 8) * q4 + 2 * i;
+    }
+    float* w0 = mo + (warp * 8 + 2 * c4) * D;
+    float* w1 = w0 + D;
+    w0[d0] = oacc[i][0]; w1[d0] = oacc[i][1];
+    w0[d0 + 1] = oacc[i][2]; w1[d0 + 1] = oacc[i][3];
+  }
+  if (q4 == 0) {
+    ml[(warp * 8 + 2 * c4) * 2 + 0] = mrow[0];
+    ml[(warp * 8 + 2 * c4) * 2 + 1] = lrow[0];
+    ml[(warp * 8 + 2 * c4 + 1) * 2 + 0] = mrow[1];
+    ml[(warp * 8 + 2 * c4 + 1) * 2 + 1] = lrow[1];
+  }
+  __syncthreads();
+
+  // ---------------------------------------------------------------- CTA merge
+  const bool direct = p.num_partitions == 1;
+  for (int idx = threadIdx.x; idx < group * D; idx += blockDim.x) {
+    const int h = idx / D, d = idx - h * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kDecodeWarps; ++w) M = fmaxf(M, ml[(w * 8 + h) * 2]);
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kDecodeWarps; ++w) {
+        const float mw = ml[(w * 8 + h) * 2];
+        if (mw == -INFINITY) continue;
+        const float f = exp2f(mw - M);
+        L += ml[(w * 8 + h) * 2 + 1] * f;
+        O += mo[(w * 8 + h) * D + d] * f;
+      }
+    }
+    const float val = L > 0.f ? O / L : 0.f;
+    const int64_t head = static_cast<int64_t>(b) * p.num_q_heads + kvh * group + h;
+    if (direct) {
+      uint16_t* outp = static_cast<uint16_t*>(p.out);
+      if constexpr (QT == PKV_F16) {
+        outp[head * D + d] = __half_as_ushort(__float2half_rn(val));
+      } else {
+        outp[head * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+      }
+    } else {
+      const int64_t slot = head * p.num_partitions + part;
+      p.ws_out[slot * D + d] = val;
+      if (d == 0) {
+        p.ws_ml[slot * 2] = M;
+        p.ws_ml[slot * 2 + 1] = L;
+      }
+    }
+  }
+}
+
+// Merge the partitions of one (sequence, q head): M = max m_p,
+// L = sum l_p 2^(m_p - M), out = sum l_p 2^(m_p - M) O_p / L.
+template <int QT, int D>
+__global__ void __launch_bounds__(D)
+pkv_lse_reduce(const Params p) {
+  const int64_t head = blockIdx.x;                 // b * Hq + h
+  const int b = static_cast<int>(head / p.num_q_heads);
+  const int d = threadIdx.x;
+  const int ctx = min(p.context_lens[b], p.max_blocks_per_seq * p.block_size);
+  const int np = max(1, (ctx + p.partition_size - 1) / p.partition_size);
+  const float* ml = p.ws_ml + head * p.num_partitions * 2;
+  const float* o = p.ws_out + head * p.num_partitions * D;
+  float M = -INFINITY;
+  for (int i = 0; i < np; ++i) M = fmaxf(M, ml[2 * i]);
+  float L = 0.f, acc = 0.f;
+  if (M != -INFINITY) {
+    for (int i = 0; i < np; ++i) {
+      const float m = ml[2 * i];
+      if (m == -INFINITY) continue;
+      const float w = ml[2 * i + 1] * exp2f(m - M);
+      L += w;
+      acc += w * o[i * D + d];
+    }
+  }
+  const float val = L > 0.f ? acc / L : 0.f;
+  uint16_t* outp = static_cast<uint16_t*>(p.out);
+  if constexpr (QT == PKV_F16) {
+    outp[head * D + d] = __half_as_ushort(__float2half_rn(val));
+  } else {
+    outp[head * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+  }
+}
+
+template <int KV, int QT, int D>
+cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t st) {
+  using G = Geo<KV, D>;
+  Params p;
+  p.q = static_cast<const uint16_t*>(a.q);
+  p.k_cache = static_cast<const uint8_t*>(a.k_cache);
+  p.v_cache = static_cast<const uint8_t*>(a.v_cache);
+  p.block_tables = a.block_tables;
+  p.context_lens = a.context_lens;
+  p.scales = a.scales;
+  p.out = a.out;
+  p.ws_out = a.ws_out;
+  p.ws_ml = a.ws_ml;
+  p.dev_status = a.dev_status;
+  p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.num_blocks = a.num_blocks;
+  p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.block_size = a.block_size;
+  p.partition_size = a.partition_size;
+  p.num_partitions = a.num_partitions;
+  p.softmax_scale = a.softmax_scale;
+  auto kern = paged_decode_kernel<KV, QT, D>;
+  // the shared-memory opt-in is per device: set it once on each
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (!bit || !(configured.load(std::memory_order_relaxed) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_relaxed);
+  }
+  dim3 grid(a.num_partitions, a.num_kv_heads, a.num_seqs);
+  kern<<<grid, kDecodeWarps * kWarp, G::kSmemBytes, st>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || a.num_partitions == 1) return e;
+  pkv_lse_reduce<QT, D><<<a.num_seqs * a.num_q_heads, D, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <int KV, int QT>
+cudaError_t launch_d(const DecodeArgs& a, cudaStream_t st) {
+  return a.head_dim == 64 ? launch_typed<KV, QT, 64>(a, st) : launch_typed<KV, QT, 128>(a, st);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
+  if (a.num_seqs == 0) return cudaSuccess;
+  switch (a.kv_dtype) {
+    case PKV_F16: return launch_d<PKV_F16, PKV_F16>(a, st);
+    case PKV_BF16: return launch_d<PKV_BF16, PKV_BF16>(a, st);
+    case PKV_FP8_E4M3:
+      return a.q_dtype == PKV_F16 ? launch_d<PKV_FP8_E4M3, PKV_F16>(a, st)
+                                  : launch_d<PKV_FP8_E4M3, PKV_BF16>(a, st);
+    default:
+      return a.q_dtype == PKV_F16 ? launch_d<PKV_INT4_G32, PKV_F16>(a, st)
+                                  : launch_d<PKV_INT4_G32, PKV_BF16>(a, st);
+  }
+}
+
+int resolve_partition_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                           int max_blocks_per_seq, int block_size, int requested) {
+  if (requested > 0) return ((requested + kTile - 1) / kTile) * kTile;
+  const int64_t max_ctx = static_cast<int64_t>(max_blocks_per_seq) * block_size;
+  const int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads;
+  int part = 512;
+  if (pairs * ((max_ctx + 511) / 512) < 2 * 152) part = 256;
+  if (max_ctx <= part) part = static_cast<int>(((max_ctx + kTile - 1) / kTile) * kTile);
+  if (part <= 0) part = kTile;
+  (void)num_q_heads;
+  return part;
+}
+
+}  // namespace pkv

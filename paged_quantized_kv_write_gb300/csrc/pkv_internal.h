@@ -1,0 +1,58 @@
+// Host-side argument bundles passed from the C ABI to the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+struct WriteArgs {
+  const void* k_new;
+  const void* v_new;
+  int new_dtype;
+  const int64_t* slot_mapping;
+  int64_t num_tokens;
+  void* k_cache;
+  void* v_cache;
+  void* scales;
+  int kv_dtype;
+  int num_blocks;
+  int num_kv_heads;
+  int head_dim;
+  int block_size;
+  int* dev_status;
+};
+
+struct DecodeArgs {
+  const void* q;
+  int q_dtype;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  int max_blocks_per_seq;
+  const int32_t* context_lens;
+  int num_seqs;
+  const void* scales;
+  int kv_dtype;
+  int num_blocks;
+  void* out;
+  float softmax_scale;
+  int num_q_heads;
+  int num_kv_heads;
+  int head_dim;
+  int block_size;
+  int partition_size;   // resolved, multiple of 16
+  int num_partitions;   // grid.x: ceil(max_blocks_per_seq * block_size / partition_size)
+  float* ws_out;        // [num_seqs][num_q_heads][num_partitions][head_dim]
+  float* ws_ml;         // [num_seqs][num_q_heads][num_partitions][2]
+  int* dev_status;
+};
+
+cudaError_t launch_kv_write(const WriteArgs& a, cudaStream_t st);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
+
+int resolve_partition_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                           int max_blocks_per_seq, int block_size, int requested);
+
+}  // namespace pkv

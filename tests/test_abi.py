@@ -1,0 +1,91 @@
+"""CPU checks of the C ABI: the library loads, exports every declared symbol,
+and rejects bad arguments on the host before touching the GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedkv.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(paged_[a-z_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_quantized_kv_write_gb300 import build
+    build.build()
+    import paged_quantized_kv_write_gb300 as pkv
+    return pkv
+
+
+def test_header_declares_the_two_calls():
+    names = _declared()
+    assert "paged_kv_write" in names and "paged_decode_attention" in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    dll = ctypes.CDLL(lib.LIB_PATH)
+    for name in _declared():
+        assert hasattr(dll, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert lib.version() == 100
+    assert lib.lib.paged_kv_status_string(0) == b"ok"
+    assert b"outside" in lib.lib.paged_kv_status_string(4)
+
+
+def test_host_validation_without_gpu(lib):
+    L = lib.lib
+    V = ctypes.c_void_p
+    fake = V(0x10000)          # never dereferenced: validation fails first
+    # num_q_heads not a multiple of num_kv_heads
+    assert L.paged_decode_attention(fake, 1, fake, fake, fake, 4, fake, 2, None, 1, 10, fake,
+                                    0.1, 6, 4, 128, 16, 0, None, 0, None, None) == 1
+    # unsupported head_dim
+    assert L.paged_decode_attention(fake, 1, fake, fake, fake, 4, fake, 2, None, 1, 10, fake,
+                                    0.1, 8, 2, 96, 16, 0, None, 0, None, None) == 2
+    # 16-bit cache with a different q dtype
+    assert L.paged_decode_attention(fake, 0, fake, fake, fake, 4, fake, 2, None, 1, 10, fake,
+                                    0.1, 8, 2, 128, 16, 0, None, 0, None, None) == 2
+    # group larger than 8
+    assert L.paged_decode_attention(fake, 1, fake, fake, fake, 4, fake, 2, None, 1, 10, fake,
+                                    0.1, 32, 2, 128, 16, 0, None, 0, None, None) == 2
+    # FP8 without scales
+    assert L.paged_decode_attention(fake, 1, fake, fake, fake, 4, fake, 2, None, 2, 10, fake,
+                                    0.1, 8, 2, 128, 16, 0, None, 0, None, None) == 1
+    # misaligned q
+    assert L.paged_decode_attention(V(0x10002), 1, fake, fake, fake, 4, fake, 2, None, 1, 10,
+                                    fake, 0.1, 8, 2, 128, 16, 0, None, 0, None, None) == 1
+    # split-KV without workspace
+    assert L.paged_decode_attention(fake, 1, fake, fake, fake, 400, fake, 2, None, 1, 10, fake,
+                                    0.1, 8, 2, 128, 16, 64, None, 0, None, None) == 5
+    # bad block size, bad dtype, NULL buffers on the write
+    assert L.paged_kv_write(fake, fake, 1, fake, 4, fake, fake, None, 1, 10, 2, 128, 24,
+                            None, None) == 2
+    assert L.paged_kv_write(fake, fake, 1, fake, 4, fake, fake, None, 7, 10, 2, 128, 16,
+                            None, None) == 2
+    assert L.paged_kv_write(None, fake, 1, fake, 4, fake, fake, None, 1, 10, 2, 128, 16,
+                            None, None) == 1
+    assert L.paged_kv_write(fake, fake, 1, fake, 4, fake, fake, None, 3, 10, 2, 128, 16,
+                            None, None) == 1
+    # zero tokens / zero sequences are no-ops
+    assert L.paged_kv_write(None, None, 1, None, 0, None, None, None, 1, 10, 2, 128, 16,
+                            None, None) == 0
+
+
+def test_workspace_and_partition_queries(lib):
+    # short contexts: one partition, no workspace
+    assert lib.paged_decode_workspace_bytes(4, 8, 2, 64, 8, 16) == 0
+    assert lib.paged_decode_partition_size(4, 8, 2, 8, 16) == 128
+    # explicit partition: B * Hq * NP * (D + 2) floats (+ alignment)
+    n = lib.paged_decode_workspace_bytes(16, 64, 8, 128, 2048, 16, 512)
+    assert n >= 16 * 64 * 64 * 130 * 4
+    assert lib.paged_decode_partition_size(16, 64, 8, 2048, 16, 500) == 512
