@@ -33,7 +33,7 @@ def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(
             f"libpagedkv.so not found at {LIB_PATH}; build it with "
-            "`python -m paged_quantized_kv_write_gb300.build` (needs nvcc)")
+            "`python paged_quantized_kv_write_gb300/build.py` (needs nvcc)")
     lib = ctypes.CDLL(LIB_PATH)
     P, I, I64, F, SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
                         ctypes.c_size_t)

@@ -4,7 +4,9 @@ Targets sm_103a only.  Translation units compile in parallel, then link into
 paged_quantized_kv_write_gb300/_lib/libpagedkv.so.  The CUDA runtime is
 linked statically, so the library needs only the driver at run time.
 
-    python -m paged_quantized_kv_write_gb300.build [--force] [--verbose-ptxas]
+    python paged_quantized_kv_write_gb300/build.py [--force] [--verbose-ptxas]
+
+(run it by path: importing the package itself needs the built library)
 """
 
 import concurrent.futures as cf

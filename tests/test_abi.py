@@ -19,8 +19,8 @@ def _declared():
 
 @pytest.fixture(scope="module")
 def lib():
-    from paged_quantized_kv_write_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import paged_quantized_kv_write_gb300 as pkv
     return pkv
 
