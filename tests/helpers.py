@@ -63,7 +63,18 @@ def half_ulp(x: np.ndarray, code: int) -> np.ndarray:
     return 2.0 ** (e - mant - 1)
 
 
+def round_to(x: np.ndarray, code: int) -> np.ndarray:
+    """fp64 values rounded (nearest even) to the 16-bit output dtype, back as fp64."""
+    if code == W.F16:
+        return x.astype(np.float16).astype(np.float64)
+    return W.bits_to_f32(W.f32_to_bf16_bits(x.astype(np.float32)), W.BF16).astype(np.float64)
+
+
 def check_close(gpu: np.ndarray, ref: np.ndarray, kv_dtype: int, out_dtype: int, what=""):
+    """Assert |gpu - oracle| <= tol + half an ulp of the output dtype at |oracle|.
+
+    Returns (max |gpu - oracle|, max |gpu - oracle rounded to the output dtype|,
+    max error / bound)."""
     err = np.abs(gpu - ref)
     bound = TOL[kv_dtype] + half_ulp(ref, out_dtype)
     bad = err > bound
@@ -72,7 +83,10 @@ def check_close(gpu: np.ndarray, ref: np.ndarray, kv_dtype: int, out_dtype: int,
         raise AssertionError(
             f"{what}: {int(bad.sum())} of {err.size} outputs exceed tolerance; worst at {i}: "
             f"gpu {gpu[i]!r} oracle {ref[i]!r} err {err[i]:.3g} bound {bound[i]:.3g}")
-    return float(err.max()) if err.size else 0.0
+    if not err.size:
+        return 0.0, 0.0, 0.0
+    err_r = np.abs(gpu - round_to(ref, out_dtype))
+    return float(err.max()), float(err_r.max()), float((err / bound).max())
 
 
 class GpuCase:
