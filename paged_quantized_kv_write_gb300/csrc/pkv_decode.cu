@@ -401,11 +401,17 @@ paged_decode_kernel(const Params p) {
                            exp2f(sc[2] - mnew0), exp2f(sc[3] - mnew1)};
       lrow[0] = lrow[0] * alpha0 + pr[0] + pr[2];
       lrow[1] = lrow[1] * alpha1 + pr[1] + pr[3];
+      // A block whose FP8 scale is 0 was never written: its V rows dequantize
+      // to 0 and add nothing (its scores still count in the softmax sum).
+      bool v_on = true;
       if constexpr (KV == PKV_FP8_E4M3) {
-        // keep oacc in units of the current tile's V scale
-        const float ratio = vscale_cur / vs_tile;
-        alpha0 *= ratio; alpha1 *= ratio;
-        vscale_cur = vs_tile;
+        v_on = vs_tile > 0.f;
+        if (v_on) {
+          // keep oacc in units of the current tile's V scale
+          const float ratio = vscale_cur / vs_tile;
+          alpha0 *= ratio; alpha1 *= ratio;
+          vscale_cur = vs_tile;
+        }
       }
 #pragma unroll
       for (int i = 0; i < MT; ++i) {
@@ -425,6 +431,7 @@ paged_decode_kernel(const Params p) {
       const uint32_t mA = (tA < nvalid) ? 0xFFFFFFFFu : 0u, mB = (tB < nvalid) ? 0xFFFFFFFFu : 0u;
       const uint32_t mC = (tC < nvalid) ? 0xFFFFFFFFu : 0u, mE = (tE < nvalid) ? 0xFFFFFFFFu : 0u;
 
+      if (v_on) {
       if constexpr (KV != PKV_INT4_G32) {
         // P as B fragments (hi + lo split)
         using H = Half16<MMA_T>;
@@ -546,6 +553,7 @@ paged_decode_kernel(const Params p) {
           mma_16816<PKV_F16>(oacc[2 * grp + 1], a1, bl0, bl1);
         }
       }
+      }  // v_on
     }
     __syncwarp();
     const int next = warp + (it + G::kStages) * kDecodeWarps;

@@ -134,6 +134,21 @@ def test_constant_keys_give_mean_of_values():
         H.check_close(out[b], np.repeat(mean, 4, 0), W.BF16, W.BF16, "constant K")
 
 
+@pytest.mark.parametrize("kv", [W.FP8_E4M3, W.INT4_G32, W.BF16])
+def test_unwritten_last_token_matches_oracle(kv):
+    """Attend over a context whose last token was never written (zeroed pool):
+    an FP8 block with scale 0 and INT4 rows with scale 0 dequantize to 0, so the
+    output stays finite and equal to the oracle's."""
+    w = W.Workload("unwritten", 8, 16, 2, 128, 16, kv, W.BF16, "fixed", 33, 33, seed=61 + kv)
+    case = W.make_case(w)
+    k, v, s = oracle.prefill_case(case)          # the new token (offset 0 of block 2) stays 0
+    g = H.GpuCase(case, k, v, s, 16)
+    out = g.attend()
+    ref = H.oracle_attention(case, k, v, s)
+    assert np.isfinite(out).all()
+    H.check_close(out, ref, kv, W.BF16, "unwritten last token")
+
+
 def test_bad_block_id_is_flagged_and_skipped():
     import paged_quantized_kv_write_gb300 as pkv
     w = W.Workload("badid", 3, 8, 2, 64, 16, W.BF16, W.BF16, "fixed", 40, 40, seed=4)
