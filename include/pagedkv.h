@@ -126,6 +126,37 @@ int paged_decode_attention(const void* q, int q_dtype,
                            int partition_size, void* workspace, size_t workspace_bytes,
                            int* dev_status, void* stream);
 
+/* paged_decode_attention_noalloc — paged_decode_attention without a
+ * caller-supplied workspace, for callers that cannot allocate device memory.
+ * The pages have no counterpart: this is a convenience of this library.
+ *
+ * Some callers cannot call cudaMalloc at all: code running inside a custom
+ * allocator's callbacks, processes whose device memory is one fixed pool
+ * handed out up front, runtimes that forbid allocation on their hot path,
+ * or plain C callers with no allocator at hand.  For them this variant takes
+ * the split-KV scratch (the per-partition partial results) from one static
+ * device array inside the library: 64 MiB on every GPU that loads the
+ * library, held until the process exits.
+ *
+ * Arguments, layouts and results are those of paged_decode_attention, minus
+ * workspace/workspace_bytes.  Requests whose scratch
+ * (paged_decode_workspace_bytes(...)) exceeds 64 MiB return
+ * PKV_ERR_WORKSPACE before anything is launched.  The first call on each
+ * device looks up the array's address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  Every
+ * call shares the one array, so calls that overlap on the GPU (other
+ * streams, other host threads) race on it: serialize them.
+ */
+int paged_decode_attention_noalloc(const void* q, int q_dtype,
+                                   const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, int max_blocks_per_seq,
+                                   const int32_t* context_lens, int num_seqs,
+                                   const void* scales, int kv_dtype, int num_blocks,
+                                   void* out, float softmax_scale,
+                                   int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, int partition_size,
+                                   int* dev_status, void* stream);
+
 /* Partition size paged_decode_attention will use for these arguments
  * (resolves partition_size == 0); 0 if the arguments are invalid. */
 int paged_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads,
