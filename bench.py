@@ -16,6 +16,7 @@ replica on its own GPU (the path has no exchange step).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -119,7 +120,9 @@ def run_ours(args, rank: int, world: int):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     w = W.CONFIGS[args.config]
-    case = W.make_case(w)
+    if args.partition:
+        w = dataclasses.replace(w, partition_size=args.partition)
+    case = W.make_case(w, identity_tables=args.identity)
     stream = torch.cuda.Stream(dev)
     with torch.cuda.stream(stream):
         k, v, s = pkv.alloc_cache(w.kv_dtype, case.num_blocks, w.num_kv_heads, w.head_dim,
@@ -156,6 +159,7 @@ def run_ours(args, rank: int, world: int):
     flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev) if small else None
 
     def step():
+        w0.record(stream)
         pkv.paged_kv_write(kn, vn, slots, k, v, s, w.kv_dtype, w.block_size, w.head_dim,
                            status, stream)
         a0.record(stream)
@@ -167,6 +171,8 @@ def run_ours(args, rank: int, world: int):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
+    wev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    w0 = wev[0]
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             a0, a1 = ev[0][1], ev[0][2]
@@ -182,6 +188,7 @@ def run_ours(args, rank: int, world: int):
         t_wall0 = time.perf_counter()
         for i in range(args.steps):
             s0, a0, a1, s1 = ev[i]
+            w0 = wev[i]
             if flush is not None:
                 flush.zero_()
             s0.record(stream)
@@ -192,6 +199,7 @@ def run_ours(args, rank: int, world: int):
         clk = clocks.stop()
     step_ms = [e[0].elapsed_time(e[3]) for e in ev]
     attn_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    write_ms = [wev[i].elapsed_time(ev[i][1]) for i in range(args.steps)]
     dev_ms = sum(step_ms)
     dev_ms = _max_over_ranks(dev_ms, world)
     assert status.item() == 0
@@ -251,6 +259,7 @@ def run_ours(args, rank: int, world: int):
             "partition_size": part, "num_partitions": nparts,
             "l2": "inputs larger than L2 (no flush)" if not small else "L2 flushed (256 MB write) between steps",
             "parallelism": f"replicas x{world}",
+            "block_tables": "identity (contiguous)" if args.identity else "shuffled",
         },
         "seq_steps_per_s": round(world * w.batch * args.steps / (dev_ms * 1e-3), 1),
         "pct_hbm_peak": round(100.0 * gbs / world / peak, 2),
@@ -273,6 +282,7 @@ def run_ours(args, rank: int, world: int):
             "frac": round(achieved / peak, 4),
             "traffic": _traffic(args.config),
             "avg_launch_us": round(attn_avg_ms * 1e3, 3),
+            "write_avg_us": round(statistics.mean(write_ms) * 1e3, 3),
             "algorithmic_bytes": attn_bytes,
         },
         "gpu_launches": _kernel_launches_per_step(w, nparts) * args.steps,
@@ -414,6 +424,10 @@ def main():
     ap.add_argument("--config", type=int, default=2, choices=sorted(W.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--identity", action="store_true",
+                    help="lay every sequence out in consecutive blocks (paging-overhead comparator)")
+    ap.add_argument("--partition", type=int, default=0,
+                    help="override the workload's split-KV partition size (0: keep)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

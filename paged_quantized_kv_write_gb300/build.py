@@ -46,7 +46,7 @@ def _deps():
 
 
 def _stale(target: str) -> bool:
-    if not os.path.exists(target):
+    if not os.path.exists(target) or os.environ.get("PKV_NVCC_EXTRA"):
         return True
     t = os.path.getmtime(target)
     return any(os.path.getmtime(f) > t for f in _deps())
@@ -59,6 +59,8 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
     os.makedirs(OBJ_DIR, exist_ok=True)
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+    # tuning hook: extra nvcc flags (e.g. -DPKV_STAGES_FP8=6) from the environment
+    extra += os.environ.get("PKV_NVCC_EXTRA", "").split()
 
     def compile_one(src):
         obj = os.path.join(OBJ_DIR, os.path.basename(src) + ".o")

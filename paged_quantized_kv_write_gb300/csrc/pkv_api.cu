@@ -4,7 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/pagedkv.h"
+#include "pagedkv.h"
 #include "pkv_internal.h"
 
 namespace {

@@ -6,7 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/pagedkv.h"
+#include "pagedkv.h"
 
 namespace pkv {
 
@@ -78,6 +78,12 @@ __device__ __forceinline__ uint32_t nibbles_to_f16x2(uint32_t w, int k) {
   __half2 h = *reinterpret_cast<__half2*>(&x);
   h = __hsub2(h, __half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Same nibbles as f16 1024 + n (no subtraction): for products whose 1024 * sum
+// is taken off afterwards.
+__device__ __forceinline__ uint32_t nibbles_offset_f16x2(uint32_t w, int k) {
+  return ((w >> (4 * k)) & 0x000F000Fu) | 0x64006400u;
 }
 
 // ------------------------------------------------------------------ tensor cores

@@ -35,6 +35,7 @@
 //    to the workspace and pkv_lse_reduce merges them.
 #include <math.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "pkv_common.cuh"
@@ -43,8 +44,37 @@
 namespace pkv {
 namespace {
 
-constexpr int kDecodeWarps = 4;
+// ring depth (tiles in flight per warp, plus the one being computed); build-time knobs
+#ifndef PKV_STAGES_HALF
+#define PKV_STAGES_HALF 2
+#endif
+#ifndef PKV_STAGES_FP8
+#define PKV_STAGES_FP8 3
+#endif
+#ifndef PKV_STAGES_INT4
+#define PKV_STAGES_INT4 4
+#endif
+// CTAs per SM the register allocation must allow (__launch_bounds__ minimum)
+#ifndef PKV_MINB_HALF
+#define PKV_MINB_HALF 3
+#endif
+#ifndef PKV_MINB_QUANT
+#define PKV_MINB_QUANT 4
+#endif
+
+#ifndef PKV_DECODE_WARPS
+#define PKV_DECODE_WARPS 4
+#endif
+constexpr int kDecodeWarps = PKV_DECODE_WARPS;   // warps per CTA (each walks its own tiles)
 constexpr int kTile = 16;            // tokens per tile (the mma M / K extent)
+constexpr int kMaxDevices = 64;
+// partitions per CTA (0: choose), and the longest run of tokens one CTA takes
+#ifndef PKV_PPC
+#define PKV_PPC 0
+#endif
+#ifndef PKV_RUN_TOKENS
+#define PKV_RUN_TOKENS 2048
+#endif
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int KV, int D> struct Geo {
@@ -56,12 +86,24 @@ template <int KV, int D> struct Geo {
   static constexpr int kScaleTileBytes = kTile * kScaleRowBytes;
   // stage: K tile | V tile | K scale rows | V scale rows | 16 B misc (FP8 scales, phys)
   static constexpr int kStageBytes = 2 * kTileBytes + 2 * kScaleTileBytes + 16;
-  static constexpr int kStages = kHalf ? 3 : (KV == PKV_FP8_E4M3 ? 4 : 6);
+  static constexpr int kStages =
+      kHalf ? PKV_STAGES_HALF : (KV == PKV_FP8_E4M3 ? PKV_STAGES_FP8 : PKV_STAGES_INT4);
   static constexpr int kWarpRing = kStages * kStageBytes;
   static constexpr int kRingBytes = kDecodeWarps * kWarpRing;
-  static constexpr int kMergeBytes = kDecodeWarps * 8 * (D + 2) * 4;
-  static constexpr int kSmemBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
+  // merge buffer: one warp's state, lane-major with an odd stride (no bank conflicts)
+  static constexpr int kMbStride = (D / 16) * 4 + 5;
+  static constexpr int kMbufBytes = kWarp * kMbStride * 4;
+  static constexpr int kSmemBytes = kRingBytes + kMbufBytes;
+  static constexpr int kMinBlocks = kHalf ? PKV_MINB_HALF : PKV_MINB_QUANT;
 };
+
+// 2^x on the SFU (ex2.approx; 2^-inf = +0).  Scores and probabilities use it
+// consistently, so the softmax stays exact up to its ~2 ulp.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // XOR swizzle of the 16-byte chunk position within a row (see the bank
 // analysis in the fragment readers below).
@@ -94,22 +136,23 @@ struct Params {
   float* ws_ml;
   int* dev_status;
   int max_blocks_per_seq;
+  int num_seqs;
   int num_blocks;
   int num_q_heads;
   int num_kv_heads;
   int block_size;
   int partition_size;
   int num_partitions;
+  int parts_per_cta;
   float softmax_scale;
 };
 
 // Issue the copies of one 16-token tile into a stage (lane-parallel).
 template <int KV, int D>
-__device__ __forceinline__ void issue_tile(const Params& p, int b, int kvh, int t0,
+__device__ __forceinline__ void issue_tile(const Params& p, int kvh, int t0, int phys,
                                            uint32_t stage, uint8_t* stage_ptr, int lane) {
   using G = Geo<KV, D>;
   const int logical = t0 / p.block_size;
-  const int phys = p.block_tables[static_cast<int64_t>(b) * p.max_blocks_per_seq + logical];
   const bool ok = phys >= 0 && phys < p.num_blocks;
   int* misc = reinterpret_cast<int*>(stage_ptr + G::kStageBytes - 16);
   if (lane == 0) misc[2] = ok ? 1 : 0;
@@ -156,42 +199,38 @@ __device__ __forceinline__ void issue_tile(const Params& p, int b, int kvh, int 
   }
 }
 
+// One unit of work: partition `part` of sequence b, KV head kvh.
+struct Unit {
+  int b, kvh, part, tok_begin, tok_end, ntiles;
+};
+
+// A CTA owns partitions [blockIdx.x * PPC, +PPC) of sequence b, KV head kvh
+// (those below the sequence's partition count); unit j is the j-th of them.
+__device__ __forceinline__ Unit make_unit(const Params& p, int b, int kvh, int ctx, int j) {
+  Unit u;
+  u.b = b;
+  u.kvh = kvh;
+  u.part = blockIdx.x * p.parts_per_cta + j;
+  u.tok_begin = u.part * p.partition_size;
+  u.tok_end = min(ctx, u.tok_begin + p.partition_size);
+  u.ntiles = ctx > 0 ? (u.tok_end - u.tok_begin + kTile - 1) / kTile : 0;
+  return u;
+}
+
+// Q of the unit's G heads as the B operand of S^T = K Q^T (column n = head q4
+// of the group, rows = d in the order the K fragments use; heads >= group are
+// zero columns), plus the f16 scaling and INT4 group sums.
 template <int KV, int QT, int D>
-__global__ void __launch_bounds__(kDecodeWarps * kWarp)
-paged_decode_kernel(const Params p) {
-  using G = Geo<KV, D>;
-  constexpr bool kHalf = G::kHalf;
-  constexpr int MT = D / 16;                 // m-tiles of O^T (and k-steps of S^T)
-  // mma operand type: the cache's type for 16-bit caches, f16 for FP8/INT4
-  constexpr int MMA_T = kHalf ? KV : PKV_F16;
-  constexpr float kPScale = (KV == PKV_BF16) ? 1.f : (KV == PKV_INT4_G32 ? 1.f : 256.f);
-
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int q4 = lane >> 2, c4 = lane & 3;   // mma groupID / thread-in-group
-  const int part = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+__device__ __forceinline__ void load_q(const Params& p, const Unit& u, int q4, int c4,
+                                       uint32_t (&qb)[D / 16][2], float& qexp,
+                                       float (&qsum)[(KV == PKV_F16 || KV == PKV_BF16) ? 1 : D / 32][2],
+                                       float (&qoff)[(KV == PKV_F16 || KV == PKV_BF16) ? 1 : D / 32][2]) {
+  constexpr bool kHalf = (KV == PKV_F16 || KV == PKV_BF16);
   const int group = p.num_q_heads / p.num_kv_heads;
-  // a context longer than its table row can hold is clamped (and flagged)
-  const int cap = p.max_blocks_per_seq * p.block_size;
-  int ctx = p.context_lens[b];
-  if (ctx > cap) {
-    if (threadIdx.x == 0 && part == 0 && kvh == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
-    ctx = cap;
-  }
-  const int tok_begin = part * p.partition_size;
-  if (part > 0 && tok_begin >= ctx) return;
-  const int tok_end = min(ctx, tok_begin + p.partition_size);
-  const int ntiles = ctx > 0 ? (tok_end - tok_begin + kTile - 1) / kTile : 0;
-
-  // ---------------------------------------------------------------- Q fragments
-  // B operand of S^T = K Q^T: column n = head q4 of the group, rows = d in the
-  // order the K fragments below use.  Heads >= group are zero columns.
-  const int hq = kvh * group + q4;
   const bool head_ok = q4 < group;
-  const uint16_t* qrow = p.q + (static_cast<int64_t>(b) * p.num_q_heads + (head_ok ? hq : 0)) * D;
-  uint32_t qb[MT][2];
-  float qexp = 1.f;                            // score multiplier undoing the f16 Q scaling
-  float qsum[kHalf ? 1 : D / 32][2];           // INT4: sum of q over each group (heads 2c4, 2c4+1)
+  const uint16_t* qrow =
+      p.q + (static_cast<int64_t>(u.b) * p.num_q_heads + u.kvh * group + (head_ok ? q4 : 0)) * D;
+  qexp = 1.f;
   if constexpr (kHalf) {
 #pragma unroll
     for (int jp = 0; jp < D / 32; ++jp) {
@@ -200,6 +239,7 @@ paged_decode_kernel(const Params p) {
       qb[2 * jp + 1][0] = v.z; qb[2 * jp + 1][1] = v.w;
     }
     qsum[0][0] = qsum[0][1] = 0.f;
+    qoff[0][0] = qoff[0][1] = 0.f;
   } else {
     // each thread's 32 d values, as float
     float qf[32];
@@ -261,398 +301,547 @@ paged_decode_kernel(const Params p) {
           qb[2 * grp + h][0] = Half16<PKV_F16>::pack_rn(x[2 * h] * qs, x[2 * h + 4] * qs);
           qb[2 * grp + h][1] = Half16<PKV_F16>::pack_rn(x[2 * h + 1] * qs, x[2 * h + 5] * qs);
         }
-        float s = 0.f;
+        float s = 0.f, s16 = 0.f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) s += qf[8 * grp + k];
-        s += __shfl_xor_sync(0xffffffffu, s, 1);
-        s += __shfl_xor_sync(0xffffffffu, s, 2);        // sum over d of head q4, group grp
+        for (int k = 0; k < 4; ++k) {
+          s += qf[8 * grp + k] + qf[8 * grp + k + 4];
+          const float2 lo = Half16<PKV_F16>::unpack(qb[2 * grp + (k >> 1)][k & 1]);
+          s16 += lo.x + lo.y;                           // the f16 values the mma sees
+        }
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+          s += __shfl_xor_sync(0xffffffffu, s, o);
+          s16 += __shfl_xor_sync(0xffffffffu, s16, o);  // sums over d of head q4, group grp
+        }
         qsum[grp][0] = __shfl_sync(0xffffffffu, s, (2 * c4) * 4);
         qsum[grp][1] = __shfl_sync(0xffffffffu, s, (2 * c4 + 1) * 4);
+        qoff[grp][0] = 1024.f * __shfl_sync(0xffffffffu, s16, (2 * c4) * 4);
+        qoff[grp][1] = 1024.f * __shfl_sync(0xffffffffu, s16, (2 * c4 + 1) * 4);
       }
     }
   }
+}
 
-  // ---------------------------------------------------------------- state
-  float oacc[MT][4];
+// Fold state B (mb, lb, ob) into state A for the thread's two head columns.
+template <int MT>
+__device__ __forceinline__ void merge_state(float (&ma)[2], float (&la)[2], float (&oa)[MT][4],
+                                            const float* mb, const float* lb, const float* ob) {
+  float fa[2], fb[2];
 #pragma unroll
-  for (int i = 0; i < MT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
-  float mrow[2] = {-INFINITY, -INFINITY};    // running max (log2 units), heads 2c4, 2c4+1
-  float lrow[2] = {0.f, 0.f};                // this thread's share of the running sum
-  float zacc[KV == PKV_INT4_G32 ? D / 32 : 1][2];
+  for (int h = 0; h < 2; ++h) {
+    const float M = fmaxf(ma[h], mb[h]);
+    fa[h] = ma[h] == -INFINITY ? 0.f : fast_exp2(ma[h] - M);
+    fb[h] = mb[h] == -INFINITY ? 0.f : fast_exp2(mb[h] - M);
+    la[h] = la[h] * fa[h] + lb[h] * fb[h];
+    ma[h] = M;
+  }
 #pragma unroll
-  for (int g = 0; g < (KV == PKV_INT4_G32 ? D / 32 : 1); ++g) zacc[g][0] = zacc[g][1] = 0.f;
-  float vscale_cur = 1.f;                    // FP8: oacc is in units of this V scale
-  const float base = p.softmax_scale * kLog2e * qexp;
+  for (int i = 0; i < MT; ++i) {
+    oa[i][0] = oa[i][0] * fa[0] + ob[4 * i + 0] * fb[0];
+    oa[i][1] = oa[i][1] * fa[1] + ob[4 * i + 1] * fb[1];
+    oa[i][2] = oa[i][2] * fa[0] + ob[4 * i + 2] * fb[0];
+    oa[i][3] = oa[i][3] * fa[1] + ob[4 * i + 3] * fb[1];
+  }
+}
+
+// Decode kernel.  CTA = (run of PPC consecutive partitions, KV head,
+// sequence).  The warps share each partition's 16-token tiles (tile t goes to
+// warp t % W) and keep their copy rings running across partition boundaries,
+// so the next partition's tiles are already in flight while a partition's
+// four warp states are merged; Q and the setup are paid once per run.
+template <int KV, int QT, int D>
+__global__ void __launch_bounds__(kDecodeWarps * kWarp, Geo<KV, D>::kMinBlocks)
+paged_decode_kernel(const Params p) {
+  using G = Geo<KV, D>;
+  constexpr bool kHalf = G::kHalf;
+  constexpr int MT = D / 16;                 // m-tiles of O^T (and k-steps of S^T)
+  // mma operand type: the cache's type for 16-bit caches, f16 for FP8/INT4
+  constexpr int MMA_T = kHalf ? KV : PKV_F16;
+  // P enters the second product as 16-bit values times kPScale (clear of f16
+  // subnormals).  kTau: the running max is only raised (and O rescaled) when a
+  // tile's max exceeds it by more than kTau (log2 units), so P <= 2^kTau; the
+  // f16 cases keep kPScale * 2^kTau (* 16 for the FP8 scale ratio) below 2^15.
+  constexpr float kPScale = (KV == PKV_BF16 || KV == PKV_INT4_G32) ? 1.f
+                                                                   : (KV == PKV_F16 ? 256.f : 64.f);
+  constexpr float kTau = (KV == PKV_BF16) ? 8.f : (KV == PKV_F16 ? 6.f : (KV == PKV_FP8_E4M3 ? 4.f : 0.f));
+  constexpr int kQN = kHalf ? 1 : D / 32;
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int q4 = lane >> 2, c4 = lane & 3;   // mma groupID / thread-in-group
+  const int group = p.num_q_heads / p.num_kv_heads;
+  const int cap = p.max_blocks_per_seq * p.block_size;
+
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  int ctx = p.context_lens[b];
+  if (ctx > cap) {
+    // a context longer than its table row can hold is clamped (and flagged)
+    if (threadIdx.x == 0 && blockIdx.x == 0 && kvh == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
+    ctx = cap;
+  }
+  const int nparts_seq = ctx > 0 ? (ctx + p.partition_size - 1) / p.partition_size : 1;
+  const int nunits = min(p.parts_per_cta, nparts_seq - static_cast<int>(blockIdx.x) * p.parts_per_cta);
+  if (nunits <= 0) return;
 
   uint8_t* ring_ptr = smem + warp * G::kWarpRing;
   const uint32_t ring = smem_u32(ring_ptr);
+  float* mbuf = reinterpret_cast<float*>(smem + G::kRingBytes);                 // [32][kMbStride]
 
-  // ---------------------------------------------------------------- pipeline
-#pragma unroll
-  for (int s = 0; s < G::kStages; ++s) {
-    const int tile = warp + s * kDecodeWarps;
-    if (tile < ntiles)
-      issue_tile<KV, D>(p, b, kvh, tok_begin + tile * kTile, ring + s * G::kStageBytes,
-                        ring_ptr + s * G::kStageBytes, lane);
+  // ---------------------------------------------------------------- issue cursor
+  // Walks (unit, tile) pairs with tile = warp, warp + W, ... < ntiles, in unit
+  // order.  The physical block ids of the warp's tiles of a unit are loaded 32
+  // at a time into a register (lane l: the warp's tile 32k + l); the first
+  // window of the next unit is prefetched on entering a unit.
+  int iu = -1, it = 0, i_tb = 0, i_next_tb = -1, i_win = 0;
+  Unit iunit;
+  iunit.ntiles = 0;
+  auto window = [&](const Unit& u, int k) -> int {
+    const int tile = warp + kDecodeWarps * (32 * k + lane);
+    if (tile >= u.ntiles) return -1;
+    const int32_t* trow = p.block_tables + static_cast<int64_t>(u.b) * p.max_blocks_per_seq;
+    return __ldg(trow + (u.tok_begin + tile * kTile) / p.block_size);
+  };
+  auto next_window_unit = [&](int j) -> int {          // window 0 of unit j (or -1s)
+    return j < nunits ? window(make_unit(p, b, kvh, ctx, j), 0) : -1;
+  };
+  // advance to the next pair this warp issues; false when the stream is done
+  auto issue_advance = [&]() -> bool {
+    it += kDecodeWarps;
+    while (it >= iunit.ntiles) {
+      if (iu + 1 >= nunits) return false;
+      ++iu;
+      iunit = make_unit(p, b, kvh, ctx, iu);
+      it = warp;
+      i_tb = i_next_tb;                                  // prefetched window 0 of unit iu
+      i_win = 0;
+      i_next_tb = next_window_unit(iu + 1);
+    }
+    const int k = (it - warp) / kDecodeWarps;             // the warp's tile index in the unit
+    if ((k >> 5) != i_win) {                              // beyond 32 tiles: next window
+      i_win = k >> 5;
+      i_tb = window(iunit, i_win);
+    }
+    return true;
+  };
+  int issued = 0;                                        // pairs issued so far (ring position)
+  auto issue_next = [&]() {
+    if (issue_advance()) {
+      const int phys = __shfl_sync(0xffffffffu, i_tb, ((it - warp) / kDecodeWarps) & 31);
+      const int s = issued % G::kStages;
+      issue_tile<KV, D>(p, iunit.kvh, iunit.tok_begin + it * kTile, phys,
+                        ring + s * G::kStageBytes, ring_ptr + s * G::kStageBytes, lane);
+    }
+    ++issued;
     cp_async_commit();
-  }
+  };
+  // the first advance enters unit 0 (it + W >= ntiles = 0) with its prefetched window
+  it = 0;
+  i_next_tb = next_window_unit(0);
+#pragma unroll 1
+  for (int s = 0; s < G::kStages; ++s) issue_next();
 
-  int stage = 0;
-  for (int it = 0;; ++it) {
-    const int tile = warp + it * kDecodeWarps;
-    if (tile >= ntiles) break;
-    cp_async_wait<G::kStages - 1>();
-    __syncwarp();
-    const uint32_t st = ring + stage * G::kStageBytes;
-    const uint8_t* st_ptr = ring_ptr + stage * G::kStageBytes;
-    const int* misc = reinterpret_cast<const int*>(st_ptr + G::kStageBytes - 16);
-    const int t0 = tok_begin + tile * kTile;
-    const int nvalid = misc[2] ? min(kTile, tok_end - t0) : 0;
+  // ---------------------------------------------------------------- state
+  uint32_t qb[MT][2];
+  float qexp = 1.f;
+  float qsum[kQN][2], qoff[kQN][2];
+  float oacc[MT][4];
+  float mrow[2], lrow[2];
+  float zacc[KV == PKV_INT4_G32 ? D / 32 : 1][2];
+  float vref, inv_vref;                      // FP8: oacc is in units of vref / kPScale
+  int consumed = 0;                          // pairs computed so far (ring position)
+  load_q<KV, QT, D>(p, make_unit(p, b, kvh, ctx, 0), q4, c4, qb, qexp, qsum, qoff);
 
-    if (nvalid > 0) {
-      // ------------------------------------------------ S^T = K_tile Q^T
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
-      if constexpr (kHalf) {
+#pragma unroll 1
+  for (int cu = 0; cu < nunits; ++cu) {
+    const Unit unit = make_unit(p, b, kvh, ctx, cu);
 #pragma unroll
-        for (int jp = 0; jp < D / 32; ++jp) {
-          // thread reads chunk 4jp+c4 of rows q4 and q4+8: words = d pairs
-          const uint4 r0 = ld_shared_v4(st + chunk_off<KV, D>(q4, 4 * jp + c4));
-          const uint4 r1 = ld_shared_v4(st + chunk_off<KV, D>(q4 + 8, 4 * jp + c4));
-          const uint32_t a0[4] = {r0.x, r1.x, r0.y, r1.y};
-          mma_16816<MMA_T>(sc, a0, qb[2 * jp][0], qb[2 * jp][1]);
-          const uint32_t a1[4] = {r0.z, r1.z, r0.w, r1.w};
-          mma_16816<MMA_T>(sc, a1, qb[2 * jp + 1][0], qb[2 * jp + 1][1]);
-        }
-      } else if constexpr (KV == PKV_FP8_E4M3) {
+    for (int i = 0; i < MT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+    mrow[0] = mrow[1] = -INFINITY;           // running max (log2 units), heads 2c4, 2c4+1
+    lrow[0] = lrow[1] = 0.f;                 // this thread's share of the running sum
 #pragma unroll
-        for (int i = 0; i < D / 64; ++i) {
-          const uint4 r0 = ld_shared_v4(st + chunk_off<KV, D>(q4, 4 * i + c4));
-          const uint4 r1 = ld_shared_v4(st + chunk_off<KV, D>(q4 + 8, 4 * i + c4));
-          const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w};
-          const uint32_t w1[4] = {r1.x, r1.y, r1.z, r1.w};
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const uint32_t a[4] = {e4m3x2_to_f16x2(w0[h] & 0xFFFF), e4m3x2_to_f16x2(w1[h] & 0xFFFF),
-                                   e4m3x2_to_f16x2(w0[h] >> 16), e4m3x2_to_f16x2(w1[h] >> 16)};
-            mma_16816<PKV_F16>(sc, a, qb[4 * i + h][0], qb[4 * i + h][1]);
-          }
-        }
-      } else {
-        // INT4: one fresh accumulator per 32-element group, then
-        // s += scale_t * acc + zero_t * sum(q)
-        constexpr int SR = G::kScaleRowBytes;
-        const uint32_t ksc = st + 2 * G::kTileBytes;
-        uint32_t sz0[D / 32], sz1[D / 32];
-        if constexpr (D == 128) {
-          const uint4 a = ld_shared_v4(ksc + q4 * SR), c = ld_shared_v4(ksc + (q4 + 8) * SR);
-          sz0[0] = a.x; sz0[1] = a.y; sz0[2] = a.z; sz0[3] = a.w;
-          sz1[0] = c.x; sz1[1] = c.y; sz1[2] = c.z; sz1[3] = c.w;
-        } else {
-          const uint2 a = ld_shared_v2(ksc + q4 * SR), c = ld_shared_v2(ksc + (q4 + 8) * SR);
-          sz0[0] = a.x; sz0[1] = a.y; sz1[0] = c.x; sz1[1] = c.y;
-        }
-#pragma unroll
-        for (int grp = 0; grp < D / 32; ++grp) {
-          const uint32_t w0 = ld_shared_b32(st + q4 * G::kRowBytes + 16 * (grp ^ swz<KV, D>(q4)) + 4 * c4);
-          const uint32_t w1 = ld_shared_b32(st + (q4 + 8) * G::kRowBytes +
-                                            16 * (grp ^ swz<KV, D>(q4 + 8)) + 4 * c4);
-          float g4[4] = {0.f, 0.f, 0.f, 0.f};
-          const uint32_t a0[4] = {nibbles_to_f16x2(w0, 0), nibbles_to_f16x2(w1, 0),
-                                  nibbles_to_f16x2(w0, 1), nibbles_to_f16x2(w1, 1)};
-          mma_16816<PKV_F16>(g4, a0, qb[2 * grp][0], qb[2 * grp][1]);
-          const uint32_t a1[4] = {nibbles_to_f16x2(w0, 2), nibbles_to_f16x2(w1, 2),
-                                  nibbles_to_f16x2(w0, 3), nibbles_to_f16x2(w1, 3)};
-          mma_16816<PKV_F16>(g4, a1, qb[2 * grp + 1][0], qb[2 * grp + 1][1]);
-          const float2 f0 = Half16<PKV_F16>::unpack(sz0[grp]);   // (scale, zero) token q4
-          const float2 f1 = Half16<PKV_F16>::unpack(sz1[grp]);   // token q4 + 8
-          sc[0] += f0.x * qexp * g4[0] + f0.y * qsum[grp][0];
-          sc[1] += f0.x * qexp * g4[1] + f0.y * qsum[grp][1];
-          sc[2] += f1.x * qexp * g4[2] + f1.y * qsum[grp][0];
-          sc[3] += f1.x * qexp * g4[3] + f1.y * qsum[grp][1];
-        }
-      }
+    for (int g = 0; g < (KV == PKV_INT4_G32 ? D / 32 : 1); ++g) zacc[g][0] = zacc[g][1] = 0.f;
+    vref = 0.f;
+    inv_vref = 0.f;
+    const float base = p.softmax_scale * kLog2e * qexp;
+    const int tok_end = unit.tok_end;
 
-      // ------------------------------------------------ scale, mask, online softmax
-      float mult = base;
-      float vs_tile = 1.f;
-      if constexpr (KV == PKV_FP8_E4M3) {
-        const float* fs = reinterpret_cast<const float*>(misc);
-        mult *= fs[0];
-        vs_tile = fs[1];
-      } else if constexpr (KV == PKV_INT4_G32) {
-        mult = p.softmax_scale * kLog2e;       // qexp already folded into the group sums
-      }
-      const bool v0 = q4 < nvalid, v1 = q4 + 8 < nvalid;
-      sc[0] = v0 ? sc[0] * mult : -INFINITY;
-      sc[1] = v0 ? sc[1] * mult : -INFINITY;
-      sc[2] = v1 ? sc[2] * mult : -INFINITY;
-      sc[3] = v1 ? sc[3] * mult : -INFINITY;
-      float tmax0 = fmaxf(sc[0], sc[2]), tmax1 = fmaxf(sc[1], sc[3]);
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        tmax0 = fmaxf(tmax0, __shfl_xor_sync(0xffffffffu, tmax0, o));
-        tmax1 = fmaxf(tmax1, __shfl_xor_sync(0xffffffffu, tmax1, o));
-      }
-      const float mnew0 = fmaxf(mrow[0], tmax0), mnew1 = fmaxf(mrow[1], tmax1);
-      // mnew is finite: at least one token of the tile is valid
-      float alpha0 = exp2f(mrow[0] - mnew0), alpha1 = exp2f(mrow[1] - mnew1);
-      mrow[0] = mnew0; mrow[1] = mnew1;
-      const float pr[4] = {exp2f(sc[0] - mnew0), exp2f(sc[1] - mnew1),
-                           exp2f(sc[2] - mnew0), exp2f(sc[3] - mnew1)};
-      lrow[0] = lrow[0] * alpha0 + pr[0] + pr[2];
-      lrow[1] = lrow[1] * alpha1 + pr[1] + pr[3];
-      // A block whose FP8 scale is 0 was never written: its V rows dequantize
-      // to 0 and add nothing (its scores still count in the softmax sum).
-      bool v_on = true;
-      if constexpr (KV == PKV_FP8_E4M3) {
-        v_on = vs_tile > 0.f;
-        if (v_on) {
-          // keep oacc in units of the current tile's V scale
-          const float ratio = vscale_cur / vs_tile;
-          alpha0 *= ratio; alpha1 *= ratio;
-          vscale_cur = vs_tile;
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < MT; ++i) {
-        oacc[i][0] *= alpha0; oacc[i][1] *= alpha1;
-        oacc[i][2] *= alpha0; oacc[i][3] *= alpha1;
-      }
-      if constexpr (KV == PKV_INT4_G32) {
-#pragma unroll
-        for (int g = 0; g < D / 32; ++g) { zacc[g][0] *= alpha0; zacc[g][1] *= alpha1; }
-      }
+#pragma unroll 1
+    for (int ct = warp; ct < unit.ntiles; ct += kDecodeWarps) {
+      cp_async_wait<G::kStages - 1>();
+      __syncwarp();
+      const int stage = consumed % G::kStages;
+      const uint32_t st = ring + stage * G::kStageBytes;
+      const uint8_t* st_ptr = ring_ptr + stage * G::kStageBytes;
+      const int* misc = reinterpret_cast<const int*>(st_ptr + G::kStageBytes - 16);
+      const int t0 = unit.tok_begin + ct * kTile;
+      const int nvalid = misc[2] ? min(kTile, tok_end - t0) : 0;
 
-      // ------------------------------------------------ O^T += V_tile^T P^T
-      const uint32_t vt = st + G::kTileBytes;
-      // rows (tokens) this thread's V fragments cover: 2c4, 2c4+1, 2c4+8, 2c4+9
-      const int tA = 2 * c4, tB = 2 * c4 + 1, tC = 2 * c4 + 8, tE = 2 * c4 + 9;
-      const bool partial = nvalid < kTile;
-      const uint32_t mA = (tA < nvalid) ? 0xFFFFFFFFu : 0u, mB = (tB < nvalid) ? 0xFFFFFFFFu : 0u;
-      const uint32_t mC = (tC < nvalid) ? 0xFFFFFFFFu : 0u, mE = (tE < nvalid) ? 0xFFFFFFFFu : 0u;
-
-      if (v_on) {
-      if constexpr (KV != PKV_INT4_G32) {
-        // P as B fragments (hi + lo split)
-        using H = Half16<MMA_T>;
-        const float pp[4] = {pr[0] * kPScale, pr[1] * kPScale, pr[2] * kPScale, pr[3] * kPScale};
-        const uint32_t h01 = H::pack_rn(pp[0], pp[1]), h23 = H::pack_rn(pp[2], pp[3]);
-        const float2 f01 = H::unpack(h01), f23 = H::unpack(h23);
-        const uint32_t l01 = H::pack_rn(pp[0] - f01.x, pp[1] - f01.y);
-        const uint32_t l23 = H::pack_rn(pp[2] - f23.x, pp[3] - f23.y);
-        const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-        const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
-
+      if (nvalid > 0) {
+        // ------------------------------------------------ S^T = K_tile Q^T
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        float sc2[4] = {0.f, 0.f, 0.f, 0.f};     // second chain: halves the mma dependency depth
         if constexpr (kHalf) {
 #pragma unroll
-          for (int hc = 0; hc < D / 64; ++hc) {
-            // chunk (D/64 == 2 ? 2*q4 + hc : q4): d = 16*q4 + 8*hc + 0..7 (D=128) or 8*q4 + 0..7
-            const int ch = (D == 128) ? 2 * q4 + hc : q4;
-            uint4 A = ld_shared_v4(vt + chunk_off<KV, D>(tA, ch));
-            uint4 B = ld_shared_v4(vt + chunk_off<KV, D>(tB, ch));
-            uint4 C = ld_shared_v4(vt + chunk_off<KV, D>(tC, ch));
-            uint4 E = ld_shared_v4(vt + chunk_off<KV, D>(tE, ch));
-            if (partial) {
-              A.x &= mA; A.y &= mA; A.z &= mA; A.w &= mA;
-              B.x &= mB; B.y &= mB; B.z &= mB; B.w &= mB;
-              C.x &= mC; C.y &= mC; C.z &= mC; C.w &= mC;
-              E.x &= mE; E.y &= mE; E.z &= mE; E.w &= mE;
-            }
-            const uint32_t wa[4] = {A.x, A.y, A.z, A.w}, wb[4] = {B.x, B.y, B.z, B.w};
-            const uint32_t wc[4] = {C.x, C.y, C.z, C.w}, we[4] = {E.x, E.y, E.z, E.w};
+          for (int jp = 0; jp < D / 32; ++jp) {
+            // thread reads chunk 4jp+c4 of rows q4 and q4+8: words = d pairs
+            const uint4 r0 = ld_shared_v4(st + chunk_off<KV, D>(q4, 4 * jp + c4));
+            const uint4 r1 = ld_shared_v4(st + chunk_off<KV, D>(q4 + 8, 4 * jp + c4));
+            const uint32_t a0[4] = {r0.x, r1.x, r0.y, r1.y};
+            mma_16816<MMA_T>(sc, a0, qb[2 * jp][0], qb[2 * jp][1]);
+            const uint32_t a1[4] = {r0.z, r1.z, r0.w, r1.w};
+            mma_16816<MMA_T>(sc2, a1, qb[2 * jp + 1][0], qb[2 * jp + 1][1]);
+          }
+        } else if constexpr (KV == PKV_FP8_E4M3) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int i = 4 * hc + k;                       // m-tile: d = base + 2i (+1)
-              const uint32_t a[4] = {__byte_perm(wa[k], wb[k], 0x5410), __byte_perm(wa[k], wb[k], 0x7632),
-                                     __byte_perm(wc[k], we[k], 0x5410), __byte_perm(wc[k], we[k], 0x7632)};
-              mma_16816<MMA_T>(oacc[i], a, bh0, bh1);
-              mma_16816<MMA_T>(oacc[i], a, bl0, bl1);
+          for (int i = 0; i < D / 64; ++i) {
+            const uint4 r0 = ld_shared_v4(st + chunk_off<KV, D>(q4, 4 * i + c4));
+            const uint4 r1 = ld_shared_v4(st + chunk_off<KV, D>(q4 + 8, 4 * i + c4));
+            const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w};
+            const uint32_t w1[4] = {r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const uint32_t a[4] = {e4m3x2_to_f16x2(w0[h] & 0xFFFF), e4m3x2_to_f16x2(w1[h] & 0xFFFF),
+                                     e4m3x2_to_f16x2(w0[h] >> 16), e4m3x2_to_f16x2(w1[h] >> 16)};
+              if (h & 1)
+                mma_16816<PKV_F16>(sc2, a, qb[4 * i + h][0], qb[4 * i + h][1]);
+              else
+                mma_16816<PKV_F16>(sc, a, qb[4 * i + h][0], qb[4 * i + h][1]);
             }
           }
         } else {
-          // FP8: d = base(q4) + 0..15 (D=128) or 8*q4 + 0..7 (D=64)
-          constexpr int NW = D / 32;                          // words per token: 4 or 2
-          uint32_t wa[NW], wb[NW], wc[NW], we[NW];
+          // INT4: one fresh accumulator per 32-element group, then
+          // s += scale_t * acc + zero_t * sum(q)
+          constexpr int SR = G::kScaleRowBytes;
+          const uint32_t ksc = st + 2 * G::kTileBytes;
+          uint32_t sz0[D / 32], sz1[D / 32];
           if constexpr (D == 128) {
-            const int pi = ((q4 & 1) << 1) | ((q4 >> 1) & 1) | (q4 & 4);
-            const uint4 A = ld_shared_v4(vt + chunk_off<KV, D>(tA, pi));
-            const uint4 B = ld_shared_v4(vt + chunk_off<KV, D>(tB, pi));
-            const uint4 C = ld_shared_v4(vt + chunk_off<KV, D>(tC, pi));
-            const uint4 E = ld_shared_v4(vt + chunk_off<KV, D>(tE, pi));
-            wa[0] = A.x; wa[1] = A.y; wa[2] = A.z; wa[3] = A.w;
-            wb[0] = B.x; wb[1] = B.y; wb[2] = B.z; wb[3] = B.w;
-            wc[0] = C.x; wc[1] = C.y; wc[2] = C.z; wc[3] = C.w;
-            we[0] = E.x; we[1] = E.y; we[2] = E.z; we[3] = E.w;
+            const uint4 a = ld_shared_v4(ksc + q4 * SR), c = ld_shared_v4(ksc + (q4 + 8) * SR);
+            sz0[0] = a.x; sz0[1] = a.y; sz0[2] = a.z; sz0[3] = a.w;
+            sz1[0] = c.x; sz1[1] = c.y; sz1[2] = c.z; sz1[3] = c.w;
           } else {
-            const uint2 A = ld_shared_v2(vt + tA * G::kRowBytes + 8 * q4);
-            const uint2 B = ld_shared_v2(vt + tB * G::kRowBytes + 8 * q4);
-            const uint2 C = ld_shared_v2(vt + tC * G::kRowBytes + 8 * q4);
-            const uint2 E = ld_shared_v2(vt + tE * G::kRowBytes + 8 * q4);
-            wa[0] = A.x; wa[1] = A.y; wb[0] = B.x; wb[1] = B.y;
-            wc[0] = C.x; wc[1] = C.y; we[0] = E.x; we[1] = E.y;
-          }
-          if (partial) {
-#pragma unroll
-            for (int k = 0; k < NW; ++k) { wa[k] &= mA; wb[k] &= mB; wc[k] &= mC; we[k] &= mE; }
+            const uint2 a = ld_shared_v2(ksc + q4 * SR), c = ld_shared_v2(ksc + (q4 + 8) * SR);
+            sz0[0] = a.x; sz0[1] = a.y; sz1[0] = c.x; sz1[1] = c.y;
           }
 #pragma unroll
-          for (int k = 0; k < NW; ++k) {
-            const uint32_t x01 = __byte_perm(wa[k], wb[k], 0x5140), x23 = __byte_perm(wa[k], wb[k], 0x7362);
-            const uint32_t y01 = __byte_perm(wc[k], we[k], 0x5140), y23 = __byte_perm(wc[k], we[k], 0x7362);
-            const uint32_t a0[4] = {e4m3x2_to_f16x2(x01 & 0xFFFF), e4m3x2_to_f16x2(x01 >> 16),
-                                    e4m3x2_to_f16x2(y01 & 0xFFFF), e4m3x2_to_f16x2(y01 >> 16)};
-            mma_16816<PKV_F16>(oacc[2 * k], a0, bh0, bh1);
-            mma_16816<PKV_F16>(oacc[2 * k], a0, bl0, bl1);
-            const uint32_t a1[4] = {e4m3x2_to_f16x2(x23 & 0xFFFF), e4m3x2_to_f16x2(x23 >> 16),
-                                    e4m3x2_to_f16x2(y23 & 0xFFFF), e4m3x2_to_f16x2(y23 >> 16)};
-            mma_16816<PKV_F16>(oacc[2 * k + 1], a1, bh0, bh1);
-            mma_16816<PKV_F16>(oacc[2 * k + 1], a1, bl0, bl1);
+          for (int grp = 0; grp < D / 32; ++grp) {
+            const uint32_t w0 = ld_shared_b32(st + q4 * G::kRowBytes + 16 * (grp ^ swz<KV, D>(q4)) + 4 * c4);
+            const uint32_t w1 = ld_shared_b32(st + (q4 + 8) * G::kRowBytes +
+                                              16 * (grp ^ swz<KV, D>(q4 + 8)) + 4 * c4);
+            float g4[4] = {0.f, 0.f, 0.f, 0.f};
+            // codes enter as f16 1024 + n; 1024 * sum(q) is taken off the group sum
+            const uint32_t a0[4] = {nibbles_offset_f16x2(w0, 0), nibbles_offset_f16x2(w1, 0),
+                                    nibbles_offset_f16x2(w0, 1), nibbles_offset_f16x2(w1, 1)};
+            mma_16816<PKV_F16>(g4, a0, qb[2 * grp][0], qb[2 * grp][1]);
+            const uint32_t a1[4] = {nibbles_offset_f16x2(w0, 2), nibbles_offset_f16x2(w1, 2),
+                                    nibbles_offset_f16x2(w0, 3), nibbles_offset_f16x2(w1, 3)};
+            mma_16816<PKV_F16>(g4, a1, qb[2 * grp + 1][0], qb[2 * grp + 1][1]);
+            const float2 f0 = Half16<PKV_F16>::unpack(sz0[grp]);   // (scale, zero) token q4
+            const float2 f1 = Half16<PKV_F16>::unpack(sz1[grp]);   // token q4 + 8
+            const float s0 = f0.x * qexp, s1 = f1.x * qexp;
+            sc[0] += s0 * (g4[0] - qoff[grp][0]) + f0.y * qsum[grp][0];
+            sc[1] += s0 * (g4[1] - qoff[grp][1]) + f0.y * qsum[grp][1];
+            sc[2] += s1 * (g4[2] - qoff[grp][0]) + f1.y * qsum[grp][0];
+            sc[3] += s1 * (g4[3] - qoff[grp][1]) + f1.y * qsum[grp][1];
           }
         }
-      } else {
-        // INT4: P'_g = p * scale_t,g per group g; zero point through sum_t z_t,g p_t
-        constexpr int SR = G::kScaleRowBytes;
-        const uint32_t vsc = st + 2 * G::kTileBytes + G::kScaleTileBytes;
-        uint32_t sz0[D / 32], sz1[D / 32];
-        if constexpr (D == 128) {
-          const uint4 a = ld_shared_v4(vsc + q4 * SR), c = ld_shared_v4(vsc + (q4 + 8) * SR);
-          sz0[0] = a.x; sz0[1] = a.y; sz0[2] = a.z; sz0[3] = a.w;
-          sz1[0] = c.x; sz1[1] = c.y; sz1[2] = c.z; sz1[3] = c.w;
-        } else {
-          const uint2 a = ld_shared_v2(vsc + q4 * SR), c = ld_shared_v2(vsc + (q4 + 8) * SR);
-          sz0[0] = a.x; sz0[1] = a.y; sz1[0] = c.x; sz1[1] = c.y;
-        }
-        using H = Half16<PKV_F16>;
+
 #pragma unroll
-        for (int grp = 0; grp < D / 32; ++grp) {
-          const float2 f0 = H::unpack(sz0[grp]), f1 = H::unpack(sz1[grp]);
-          // masked tokens have p == 0; keep stale scales out of the products
-          const float pp0 = pr[0] > 0.f ? pr[0] * f0.x : 0.f, pp1 = pr[1] > 0.f ? pr[1] * f0.x : 0.f;
-          const float pp2 = pr[2] > 0.f ? pr[2] * f1.x : 0.f, pp3 = pr[3] > 0.f ? pr[3] * f1.x : 0.f;
-          zacc[grp][0] += (pr[0] > 0.f ? pr[0] * f0.y : 0.f) + (pr[2] > 0.f ? pr[2] * f1.y : 0.f);
-          zacc[grp][1] += (pr[1] > 0.f ? pr[1] * f0.y : 0.f) + (pr[3] > 0.f ? pr[3] * f1.y : 0.f);
-          const uint32_t h01 = H::pack_rn(pp0, pp1), h23 = H::pack_rn(pp2, pp3);
-          const float2 g01 = H::unpack(h01), g23 = H::unpack(h23);
-          const uint32_t l01 = H::pack_rn(pp0 - g01.x, pp1 - g01.y);
-          const uint32_t l23 = H::pack_rn(pp2 - g23.x, pp3 - g23.y);
+        for (int k = 0; k < 4; ++k) sc[k] += sc2[k];
+
+        // ------------------------------------------------ scale, mask, online softmax
+        float mult = base;
+        float vs_tile = 1.f;
+        if constexpr (KV == PKV_FP8_E4M3) {
+          const float* fs = reinterpret_cast<const float*>(misc);
+          mult *= fs[0];
+          vs_tile = fs[1];
+        } else if constexpr (KV == PKV_INT4_G32) {
+          mult = p.softmax_scale * kLog2e;       // qexp already folded into the group sums
+        }
+        const bool v0 = q4 < nvalid, v1 = q4 + 8 < nvalid;
+        sc[0] = v0 ? sc[0] * mult : -INFINITY;
+        sc[1] = v0 ? sc[1] * mult : -INFINITY;
+        sc[2] = v1 ? sc[2] * mult : -INFINITY;
+        sc[3] = v1 ? sc[3] * mult : -INFINITY;
+        float tmax0 = fmaxf(sc[0], sc[2]), tmax1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          tmax0 = fmaxf(tmax0, __shfl_xor_sync(0xffffffffu, tmax0, o));
+          tmax1 = fmaxf(tmax1, __shfl_xor_sync(0xffffffffu, tmax1, o));
+        }
+        // Lazy rescale: the running max moves (and O, l, the INT4 zero sums are
+        // rescaled) only when some head's tile max exceeds it by more than kTau,
+        // or when the FP8 reference V scale must be rebased.
+        // A block whose FP8 scale is 0 was never written: its V rows dequantize
+        // to 0 and add nothing (its scores still count in the softmax sum).
+        bool v_on = true, rebase = false;
+        float vfac = 1.f;                          // FP8: this tile's V scale / vref
+        if constexpr (KV == PKV_FP8_E4M3) {
+          v_on = vs_tile > 0.f;
+          if (v_on) {
+            vfac = vs_tile * inv_vref;             // 0 while no reference is set
+            rebase = !(vfac >= 0.0625f && vfac <= 16.f);
+          }
+        }
+        const bool grow = tmax0 > mrow[0] + kTau || tmax1 > mrow[1] + kTau;
+        if (__any_sync(0xffffffffu, grow) || rebase) {
+          const float mnew0 = fmaxf(mrow[0], tmax0), mnew1 = fmaxf(mrow[1], tmax1);
+          // mnew is finite: at least one token of the tile is valid
+          float alpha0 = fast_exp2(mrow[0] - mnew0), alpha1 = fast_exp2(mrow[1] - mnew1);
+          mrow[0] = mnew0; mrow[1] = mnew1;
+          lrow[0] *= alpha0; lrow[1] *= alpha1;
+          if constexpr (KV == PKV_INT4_G32) {
+#pragma unroll
+            for (int g = 0; g < D / 32; ++g) { zacc[g][0] *= alpha0; zacc[g][1] *= alpha1; }
+          }
+          if constexpr (KV == PKV_FP8_E4M3) {
+            if (rebase) {
+              // O_true = oacc * vref / kPScale stays invariant across the rebase
+              const float r = __frcp_rn(vs_tile);
+              const float f = vref > 0.f ? vref * r : 1.f;
+              alpha0 *= f; alpha1 *= f;
+              vref = vs_tile; inv_vref = r; vfac = 1.f;
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < MT; ++i) {
+            oacc[i][0] *= alpha0; oacc[i][1] *= alpha1;
+            oacc[i][2] *= alpha0; oacc[i][3] *= alpha1;
+          }
+        }
+        const float pr[4] = {fast_exp2(sc[0] - mrow[0]), fast_exp2(sc[1] - mrow[1]),
+                             fast_exp2(sc[2] - mrow[0]), fast_exp2(sc[3] - mrow[1])};
+        lrow[0] += pr[0] + pr[2];
+        lrow[1] += pr[1] + pr[3];
+
+        // ------------------------------------------------ O^T += V_tile^T P^T
+        const uint32_t vt = st + G::kTileBytes;
+        // rows (tokens) this thread's V fragments cover: 2c4, 2c4+1, 2c4+8, 2c4+9
+        const int tA = 2 * c4, tB = 2 * c4 + 1, tC = 2 * c4 + 8, tE = 2 * c4 + 9;
+        const bool partial = nvalid < kTile;
+        const uint32_t mA = (tA < nvalid) ? 0xFFFFFFFFu : 0u, mB = (tB < nvalid) ? 0xFFFFFFFFu : 0u;
+        const uint32_t mC = (tC < nvalid) ? 0xFFFFFFFFu : 0u, mE = (tE < nvalid) ? 0xFFFFFFFFu : 0u;
+
+        if (v_on) {
+        if constexpr (KV != PKV_INT4_G32) {
+          // P as B fragments (hi + lo split)
+          using H = Half16<MMA_T>;
+          const float ps = kPScale * vfac;
+          const float pp[4] = {pr[0] * ps, pr[1] * ps, pr[2] * ps, pr[3] * ps};
+          const uint32_t h01 = H::pack_rn(pp[0], pp[1]), h23 = H::pack_rn(pp[2], pp[3]);
+          const float2 f01 = H::unpack(h01), f23 = H::unpack(h23);
+          const uint32_t l01 = H::pack_rn(pp[0] - f01.x, pp[1] - f01.y);
+          const uint32_t l23 = H::pack_rn(pp[2] - f23.x, pp[3] - f23.y);
           const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
           const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
-          const uint32_t rowoff = 2 * q4;
-          const uint32_t hA = ld_shared_u16(vt + tA * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tA)) + rowoff);
-          const uint32_t hB = ld_shared_u16(vt + tB * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tB)) + rowoff);
-          const uint32_t hC = ld_shared_u16(vt + tC * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tC)) + rowoff);
-          const uint32_t hE = ld_shared_u16(vt + tE * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tE)) + rowoff);
-          const uint32_t x = hA | (hB << 16), y = hC | (hE << 16);
-          const uint32_t a0[4] = {nibbles_to_f16x2(x, 0), nibbles_to_f16x2(x, 1),
-                                  nibbles_to_f16x2(y, 0), nibbles_to_f16x2(y, 1)};
-          mma_16816<PKV_F16>(oacc[2 * grp], a0, bh0, bh1);
-          mma_16816<PKV_F16>(oacc[2 * grp], a0, bl0, bl1);
-          const uint32_t a1[4] = {nibbles_to_f16x2(x, 2), nibbles_to_f16x2(x, 3),
-                                  nibbles_to_f16x2(y, 2), nibbles_to_f16x2(y, 3)};
-          mma_16816<PKV_F16>(oacc[2 * grp + 1], a1, bh0, bh1);
-          mma_16816<PKV_F16>(oacc[2 * grp + 1], a1, bl0, bl1);
+
+          if constexpr (kHalf) {
+#pragma unroll
+            for (int hc = 0; hc < D / 64; ++hc) {
+              // chunk (D/64 == 2 ? 2*q4 + hc : q4): d = 16*q4 + 8*hc + 0..7 (D=128) or 8*q4 + 0..7
+              const int ch = (D == 128) ? 2 * q4 + hc : q4;
+              uint4 A = ld_shared_v4(vt + chunk_off<KV, D>(tA, ch));
+              uint4 B = ld_shared_v4(vt + chunk_off<KV, D>(tB, ch));
+              uint4 C = ld_shared_v4(vt + chunk_off<KV, D>(tC, ch));
+              uint4 E = ld_shared_v4(vt + chunk_off<KV, D>(tE, ch));
+              if (partial) {
+                A.x &= mA; A.y &= mA; A.z &= mA; A.w &= mA;
+                B.x &= mB; B.y &= mB; B.z &= mB; B.w &= mB;
+                C.x &= mC; C.y &= mC; C.z &= mC; C.w &= mC;
+                E.x &= mE; E.y &= mE; E.z &= mE; E.w &= mE;
+              }
+              const uint32_t wa[4] = {A.x, A.y, A.z, A.w}, wb[4] = {B.x, B.y, B.z, B.w};
+              const uint32_t wc[4] = {C.x, C.y, C.z, C.w}, we[4] = {E.x, E.y, E.z, E.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int i = 4 * hc + k;                       // m-tile: d = base + 2i (+1)
+                const uint32_t a[4] = {__byte_perm(wa[k], wb[k], 0x5410), __byte_perm(wa[k], wb[k], 0x7632),
+                                       __byte_perm(wc[k], we[k], 0x5410), __byte_perm(wc[k], we[k], 0x7632)};
+                mma_16816<MMA_T>(oacc[i], a, bh0, bh1);
+                mma_16816<MMA_T>(oacc[i], a, bl0, bl1);
+              }
+            }
+          } else {
+            // FP8: d = base(q4) + 0..15 (D=128) or 8*q4 + 0..7 (D=64)
+            constexpr int NW = D / 32;                          // words per token: 4 or 2
+            uint32_t wa[NW], wb[NW], wc[NW], we[NW];
+            if constexpr (D == 128) {
+              const int pi = ((q4 & 1) << 1) | ((q4 >> 1) & 1) | (q4 & 4);
+              const uint4 A = ld_shared_v4(vt + chunk_off<KV, D>(tA, pi));
+              const uint4 B = ld_shared_v4(vt + chunk_off<KV, D>(tB, pi));
+              const uint4 C = ld_shared_v4(vt + chunk_off<KV, D>(tC, pi));
+              const uint4 E = ld_shared_v4(vt + chunk_off<KV, D>(tE, pi));
+              wa[0] = A.x; wa[1] = A.y; wa[2] = A.z; wa[3] = A.w;
+              wb[0] = B.x; wb[1] = B.y; wb[2] = B.z; wb[3] = B.w;
+              wc[0] = C.x; wc[1] = C.y; wc[2] = C.z; wc[3] = C.w;
+              we[0] = E.x; we[1] = E.y; we[2] = E.z; we[3] = E.w;
+            } else {
+              const uint2 A = ld_shared_v2(vt + tA * G::kRowBytes + 8 * q4);
+              const uint2 B = ld_shared_v2(vt + tB * G::kRowBytes + 8 * q4);
+              const uint2 C = ld_shared_v2(vt + tC * G::kRowBytes + 8 * q4);
+              const uint2 E = ld_shared_v2(vt + tE * G::kRowBytes + 8 * q4);
+              wa[0] = A.x; wa[1] = A.y; wb[0] = B.x; wb[1] = B.y;
+              wc[0] = C.x; wc[1] = C.y; we[0] = E.x; we[1] = E.y;
+            }
+            if (partial) {
+#pragma unroll
+              for (int k = 0; k < NW; ++k) { wa[k] &= mA; wb[k] &= mB; wc[k] &= mC; we[k] &= mE; }
+            }
+#pragma unroll
+            for (int k = 0; k < NW; ++k) {
+              const uint32_t x01 = __byte_perm(wa[k], wb[k], 0x5140), x23 = __byte_perm(wa[k], wb[k], 0x7362);
+              const uint32_t y01 = __byte_perm(wc[k], we[k], 0x5140), y23 = __byte_perm(wc[k], we[k], 0x7362);
+              const uint32_t a0[4] = {e4m3x2_to_f16x2(x01 & 0xFFFF), e4m3x2_to_f16x2(x01 >> 16),
+                                      e4m3x2_to_f16x2(y01 & 0xFFFF), e4m3x2_to_f16x2(y01 >> 16)};
+              mma_16816<PKV_F16>(oacc[2 * k], a0, bh0, bh1);
+              mma_16816<PKV_F16>(oacc[2 * k], a0, bl0, bl1);
+              const uint32_t a1[4] = {e4m3x2_to_f16x2(x23 & 0xFFFF), e4m3x2_to_f16x2(x23 >> 16),
+                                      e4m3x2_to_f16x2(y23 & 0xFFFF), e4m3x2_to_f16x2(y23 >> 16)};
+              mma_16816<PKV_F16>(oacc[2 * k + 1], a1, bh0, bh1);
+              mma_16816<PKV_F16>(oacc[2 * k + 1], a1, bl0, bl1);
+            }
+          }
+        } else {
+          // INT4: P'_g = p * scale_t,g per group g; zero point through sum_t z_t,g p_t
+          constexpr int SR = G::kScaleRowBytes;
+          const uint32_t vsc = st + 2 * G::kTileBytes + G::kScaleTileBytes;
+          uint32_t sz0[D / 32], sz1[D / 32];
+          if constexpr (D == 128) {
+            const uint4 a = ld_shared_v4(vsc + q4 * SR), c = ld_shared_v4(vsc + (q4 + 8) * SR);
+            sz0[0] = a.x; sz0[1] = a.y; sz0[2] = a.z; sz0[3] = a.w;
+            sz1[0] = c.x; sz1[1] = c.y; sz1[2] = c.z; sz1[3] = c.w;
+          } else {
+            const uint2 a = ld_shared_v2(vsc + q4 * SR), c = ld_shared_v2(vsc + (q4 + 8) * SR);
+            sz0[0] = a.x; sz0[1] = a.y; sz1[0] = c.x; sz1[1] = c.y;
+          }
+          if (partial) {
+            // rows past the context may hold stale scale bits: make them 0
+#pragma unroll
+            for (int g = 0; g < D / 32; ++g) {
+              if (!v0) sz0[g] = 0u;
+              if (!v1) sz1[g] = 0u;
+            }
+          }
+          using H = Half16<PKV_F16>;
+#pragma unroll
+          for (int grp = 0; grp < D / 32; ++grp) {
+            const float2 f0 = H::unpack(sz0[grp]), f1 = H::unpack(sz1[grp]);
+            const float pp0 = pr[0] * f0.x, pp1 = pr[1] * f0.x;
+            const float pp2 = pr[2] * f1.x, pp3 = pr[3] * f1.x;
+            zacc[grp][0] += pr[0] * f0.y + pr[2] * f1.y;
+            zacc[grp][1] += pr[1] * f0.y + pr[3] * f1.y;
+            // one f16 rounding of P' (relative 2^-11): the output moves by at most
+            // 2^-11 * the largest group range, far below the quantization step
+            const uint32_t bh0 = movmatrix_trans(H::pack_rn(pp0, pp1));
+            const uint32_t bh1 = movmatrix_trans(H::pack_rn(pp2, pp3));
+            const uint32_t rowoff = 2 * q4;
+            const uint32_t hA = ld_shared_u16(vt + tA * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tA)) + rowoff);
+            const uint32_t hB = ld_shared_u16(vt + tB * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tB)) + rowoff);
+            const uint32_t hC = ld_shared_u16(vt + tC * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tC)) + rowoff);
+            const uint32_t hE = ld_shared_u16(vt + tE * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tE)) + rowoff);
+            const uint32_t x = hA | (hB << 16), y = hC | (hE << 16);
+            const uint32_t a0[4] = {nibbles_to_f16x2(x, 0), nibbles_to_f16x2(x, 1),
+                                    nibbles_to_f16x2(y, 0), nibbles_to_f16x2(y, 1)};
+            mma_16816<PKV_F16>(oacc[2 * grp], a0, bh0, bh1);
+            const uint32_t a1[4] = {nibbles_to_f16x2(x, 2), nibbles_to_f16x2(x, 3),
+                                    nibbles_to_f16x2(y, 2), nibbles_to_f16x2(y, 3)};
+            mma_16816<PKV_F16>(oacc[2 * grp + 1], a1, bh0, bh1);
+          }
+        }
+        }  // v_on
+      }
+
+      __syncwarp();
+      issue_next();
+      ++consumed;
+    }
+
+    // -------------------------------------------------------------- unit epilogue
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      lrow[0] += __shfl_xor_sync(0xffffffffu, lrow[0], o);
+      lrow[1] += __shfl_xor_sync(0xffffffffu, lrow[1], o);
+    }
+    float post = 1.f / kPScale;
+    if constexpr (KV == PKV_FP8_E4M3) post *= vref;
+#pragma unroll
+    for (int i = 0; i < MT; ++i)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) oacc[i][k] *= post;
+    if constexpr (KV == PKV_INT4_G32) {
+#pragma unroll
+      for (int g = 0; g < D / 32; ++g) {
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          zacc[g][0] += __shfl_xor_sync(0xffffffffu, zacc[g][0], o);
+          zacc[g][1] += __shfl_xor_sync(0xffffffffu, zacc[g][1], o);
+        }
+        oacc[2 * g][0] += zacc[g][0]; oacc[2 * g][2] += zacc[g][0];
+        oacc[2 * g][1] += zacc[g][1]; oacc[2 * g][3] += zacc[g][1];
+        oacc[2 * g + 1][0] += zacc[g][0]; oacc[2 * g + 1][2] += zacc[g][0];
+        oacc[2 * g + 1][1] += zacc[g][1]; oacc[2 * g + 1][3] += zacc[g][1];
+      }
+    }
+
+    // merge the warps' states in registers (lane i of every warp holds the same
+    // output positions), passing them through one buffer: 1 -> 0, 3 -> 2, 2 -> 0
+    float* mb = mbuf + lane * G::kMbStride;
+    auto put = [&]() {
+#pragma unroll
+      for (int i = 0; i < MT; ++i)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mb[4 * i + k] = oacc[i][k];
+      mb[4 * MT + 0] = mrow[0]; mb[4 * MT + 1] = mrow[1];
+      mb[4 * MT + 2] = lrow[0]; mb[4 * MT + 3] = lrow[1];
+    };
+    auto take = [&]() { merge_state<MT>(mrow, lrow, oacc, mb + 4 * MT, mb + 4 * MT + 2, mb); };
+    if (warp == 1) put();
+    __syncthreads();
+    if (warp == 0) take();
+    __syncthreads();
+    if (warp == 3) put();
+    __syncthreads();
+    if (warp == 2) take();
+    __syncthreads();
+    if (warp == 2) put();
+    __syncthreads();
+    if (warp == 0) {
+      take();
+      const int64_t head0 = static_cast<int64_t>(unit.b) * p.num_q_heads + unit.kvh * group;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int g = 2 * c4 + h;
+        if (g >= group) continue;
+        const float inv = lrow[h] > 0.f ? 1.f / lrow[h] : 0.f;
+        const int64_t head = head0 + g;
+        const int64_t slot = head * p.num_partitions + unit.part;
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+          int d0;
+          if constexpr (KV == PKV_INT4_G32) {
+            d0 = 32 * (i >> 1) + 4 * q4 + 2 * (i & 1);
+          } else if constexpr (KV == PKV_FP8_E4M3 && D == 128) {
+            d0 = 16 * (((q4 & 1) << 1) | ((q4 >> 1) & 1) | (q4 & 4)) + 2 * i;
+          } else {
+            d0 = (D == 128 ? 16 : 8) * q4 + 2 * i;
+          }
+          const float v0 = oacc[i][h] * inv, v1 = oacc[i][2 + h] * inv;
+          if (p.num_partitions == 1) {
+            uint32_t* outp = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + head * D + d0);
+            *outp = Half16<QT>::pack_rn(v0, v1);
+          } else {
+            *reinterpret_cast<float2*>(p.ws_out + slot * D + d0) = make_float2(v0, v1);
+          }
+        }
+        if (p.num_partitions > 1 && q4 == 0) {
+          p.ws_ml[slot * 2] = mrow[h];
+          p.ws_ml[slot * 2 + 1] = lrow[h];
         }
       }
-      }  // v_on
     }
-    __syncwarp();
-    const int next = warp + (it + G::kStages) * kDecodeWarps;
-    if (next < ntiles)
-      issue_tile<KV, D>(p, b, kvh, tok_begin + next * kTile, st, ring_ptr + stage * G::kStageBytes, lane);
-    cp_async_commit();
-    stage = (stage + 1 == G::kStages) ? 0 : stage + 1;
+    __syncthreads();                         // the buffer is free for the next unit
   }
   cp_async_wait<0>();
-
-  // ---------------------------------------------------------------- warp epilogue
-#pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    lrow[0] += __shfl_xor_sync(0xffffffffu, lrow[0], o);
-    lrow[1] += __shfl_xor_sync(0xffffffffu, lrow[1], o);
-  }
-  float post = 1.f / kPScale;
-  if constexpr (KV == PKV_FP8_E4M3) post *= vscale_cur;
-#pragma unroll
-  for (int i = 0; i < MT; ++i)
-#pragma unroll
-    for (int k = 0; k < 4; ++k) oacc[i][k] *= post;
-  if constexpr (KV == PKV_INT4_G32) {
-#pragma unroll
-    for (int g = 0; g < D / 32; ++g) {
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        zacc[g][0] += __shfl_xor_sync(0xffffffffu, zacc[g][0], o);
-        zacc[g][1] += __shfl_xor_sync(0xffffffffu, zacc[g][1], o);
-      }
-      oacc[2 * g][0] += zacc[g][0]; oacc[2 * g][2] += zacc[g][0];
-      oacc[2 * g][1] += zacc[g][1]; oacc[2 * g][3] += zacc[g][1];
-      oacc[2 * g + 1][0] += zacc[g][0]; oacc[2 * g + 1][2] += zacc[g][0];
-      oacc[2 * g + 1][1] += zacc[g][1]; oacc[2 * g + 1][3] += zacc[g][1];
-    }
-  }
-
-  __syncthreads();   // every warp is done with its ring: reuse it for the merge
-  float* mo = reinterpret_cast<float*>(smem);                 // [warp][8][D]
-  float* ml = mo + kDecodeWarps * 8 * D;                      // [warp][8][2]
-#pragma unroll
-  for (int i = 0; i < MT; ++i) {
-    int d0;
-    if constexpr (KV == PKV_INT4_G32) {
-      d0 = 32 * (i >> 1) + 4 * q4 + 2 * (i & 1);
-    } else if constexpr (KV == PKV_FP8_E4M3 && D == 128) {
-      d0 = 16 * (((q4 & 1) << 1) | ((q4 >> 1) & 1) | (q4 & 4)) + 2 * i;
-    } else {
-      d0 = (D == 128 ? 16 : 8) * q4 + 2 * i;
-    }
-    float* w0 = mo + (warp * 8 + 2 * c4) * D;
-    float* w1 = w0 + D;
-    w0[d0] = oacc[i][0]; w1[d0] = oacc[i][1];
-    w0[d0 + 1] = oacc[i][2]; w1[d0 + 1] = oacc[i][3];
-  }
-  if (q4 == 0) {
-    ml[(warp * 8 + 2 * c4) * 2 + 0] = mrow[0];
-    ml[(warp * 8 + 2 * c4) * 2 + 1] = lrow[0];
-    ml[(warp * 8 + 2 * c4 + 1) * 2 + 0] = mrow[1];
-    ml[(warp * 8 + 2 * c4 + 1) * 2 + 1] = lrow[1];
-  }
-  __syncthreads();
-
-  // ---------------------------------------------------------------- CTA merge
-  const bool direct = p.num_partitions == 1;
-  for (int idx = threadIdx.x; idx < group * D; idx += blockDim.x) {
-    const int h = idx / D, d = idx - h * D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kDecodeWarps; ++w) M = fmaxf(M, ml[(w * 8 + h) * 2]);
-    float L = 0.f, O = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kDecodeWarps; ++w) {
-        const float mw = ml[(w * 8 + h) * 2];
-        if (mw == -INFINITY) continue;
-        const float f = exp2f(mw - M);
-        L += ml[(w * 8 + h) * 2 + 1] * f;
-        O += mo[(w * 8 + h) * D + d] * f;
-      }
-    }
-    const float val = L > 0.f ? O / L : 0.f;
-    const int64_t head = static_cast<int64_t>(b) * p.num_q_heads + kvh * group + h;
-    if (direct) {
-      uint16_t* outp = static_cast<uint16_t*>(p.out);
-      if constexpr (QT == PKV_F16) {
-        outp[head * D + d] = __half_as_ushort(__float2half_rn(val));
-      } else {
-        outp[head * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
-      }
-    } else {
-      const int64_t slot = head * p.num_partitions + part;
-      p.ws_out[slot * D + d] = val;
-      if (d == 0) {
-        p.ws_ml[slot * 2] = M;
-        p.ws_ml[slot * 2 + 1] = L;
-      }
-    }
-  }
 }
 
 // Merge the partitions of one (sequence, q head): M = max m_p,
@@ -703,6 +892,7 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t st) {
   p.ws_ml = a.ws_ml;
   p.dev_status = a.dev_status;
   p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.num_seqs = a.num_seqs;
   p.num_blocks = a.num_blocks;
   p.num_q_heads = a.num_q_heads;
   p.num_kv_heads = a.num_kv_heads;
@@ -711,18 +901,39 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t st) {
   p.num_partitions = a.num_partitions;
   p.softmax_scale = a.softmax_scale;
   auto kern = paged_decode_kernel<KV, QT, D>;
-  // the shared-memory opt-in is per device: set it once on each
-  static std::atomic<uint64_t> configured{0};
+  // per device, once: the shared-memory opt-in and the resident CTAs per SM
+  static std::atomic<int> slots_per_dev[kMaxDevices];     // SMs x resident CTAs (0: unknown)
+  p.parts_per_cta = 1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
-  if (!bit || !(configured.load(std::memory_order_relaxed) & bit)) {
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int slots = slots_per_dev[dev].load(std::memory_order_relaxed);
+  if (slots == 0) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured.fetch_or(bit, std::memory_order_relaxed);
+    int occ = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kDecodeWarps * kWarp,
+                                                      G::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    slots = max(1, occ) * max(1, sms);
+    slots_per_dev[dev].store(slots, std::memory_order_relaxed);
   }
-  dim3 grid(a.num_partitions, a.num_kv_heads, a.num_seqs);
+  // partitions per CTA: runs of up to PKV_RUN_TOKENS tokens, as long as the
+  // grid keeps at least four waves of CTAs
+  int ppc = PKV_PPC;
+  if (ppc <= 0) {
+    ppc = 1;
+    const int64_t pairs = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
+    while (ppc * 2 * a.partition_size <= PKV_RUN_TOKENS && ppc * 2 <= a.num_partitions &&
+           ((a.num_partitions + ppc * 2 - 1) / (ppc * 2)) * pairs >= 4 * static_cast<int64_t>(slots))
+      ppc *= 2;
+  }
+  ppc = std::max(1, std::min(ppc, a.num_partitions));
+  p.parts_per_cta = ppc;
+  dim3 grid((a.num_partitions + ppc - 1) / ppc, a.num_kv_heads, a.num_seqs);
   kern<<<grid, kDecodeWarps * kWarp, G::kSmemBytes, st>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.num_partitions == 1) return e;

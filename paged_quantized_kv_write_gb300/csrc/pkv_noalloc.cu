@@ -27,7 +27,7 @@
 
 #include <mutex>
 
-#include "../../include/pagedkv.h"
+#include "pagedkv.h"
 #include "pkv_internal.h"
 
 #define PKV_NOALLOC_SCRATCH_BYTES (size_t(64) << 20)
