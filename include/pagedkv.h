@@ -112,6 +112,10 @@ int paged_kv_write(const void* k_new, const void* v_new, int new_dtype,
  *                and a second kernel merges them by log-sum-exp.
  * workspace      device scratch of at least paged_decode_workspace_bytes(...)
  *                bytes (may be NULL when that is 0).
+ * Work split: the library picks between CTAs whose warps share a partition
+ * (merging their states) and warps that each own a (partition, KV head)
+ * unit; the environment variable PKV_DECODE_MODE=shared|warp, read on each
+ * call, forces one (for testing; results agree to rounding).
  * Supported: head_dim in {64, 128}; num_q_heads / num_kv_heads <= 8;
  * block_size a multiple of 16 up to 256; F16/BF16 caches need q_dtype equal
  * to kv_dtype; FP8/INT4 caches take F16 or BF16 q.

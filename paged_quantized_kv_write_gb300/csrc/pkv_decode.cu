@@ -34,6 +34,8 @@
 //  * With more than one partition each CTA writes (max, sum, O/sum) per head
 //    to the workspace and pkv_lse_reduce merges them.
 #include <math.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include <algorithm>
 #include <atomic>
@@ -49,17 +51,17 @@ namespace {
 #define PKV_STAGES_HALF 2
 #endif
 #ifndef PKV_STAGES_FP8
-#define PKV_STAGES_FP8 3
+#define PKV_STAGES_FP8 2
 #endif
 #ifndef PKV_STAGES_INT4
-#define PKV_STAGES_INT4 4
+#define PKV_STAGES_INT4 3
 #endif
 // CTAs per SM the register allocation must allow (__launch_bounds__ minimum)
 #ifndef PKV_MINB_HALF
 #define PKV_MINB_HALF 3
 #endif
 #ifndef PKV_MINB_QUANT
-#define PKV_MINB_QUANT 4
+#define PKV_MINB_QUANT 3
 #endif
 
 #ifndef PKV_DECODE_WARPS
@@ -75,6 +77,20 @@ constexpr int kMaxDevices = 64;
 #ifndef PKV_RUN_TOKENS
 #define PKV_RUN_TOKENS 2048
 #endif
+#ifndef PKV_RUN_TOKENS_WU
+#define PKV_RUN_TOKENS_WU 512
+#endif
+// warp-owned units from this many waves of warp-units (large: never)
+#ifndef PKV_WU_WAVES
+#define PKV_WU_WAVES 3
+#endif
+// 16-token sub-tiles per ring stage (one softmax step covers them all)
+#ifndef PKV_SUB_HALF
+#define PKV_SUB_HALF 1
+#endif
+#ifndef PKV_SUB_QUANT
+#define PKV_SUB_QUANT 2
+#endif
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int KV, int D> struct Geo {
@@ -84,8 +100,13 @@ template <int KV, int D> struct Geo {
   static constexpr int kTileBytes = kTile * kRowBytes;          // one of K or V
   static constexpr int kScaleRowBytes = (KV == PKV_INT4_G32) ? (D / 32) * 4 : 0;
   static constexpr int kScaleTileBytes = kTile * kScaleRowBytes;
-  // stage: K tile | V tile | K scale rows | V scale rows | 16 B misc (FP8 scales, phys)
-  static constexpr int kStageBytes = 2 * kTileBytes + 2 * kScaleTileBytes + 16;
+  // A stage holds kSub 16-token sub-tiles, each K rows | V rows | K scale rows |
+  // V scale rows, then 16 B of misc per sub-tile (FP8 K and V scale, valid flag).
+  static constexpr int kSub = kHalf ? PKV_SUB_HALF : PKV_SUB_QUANT;
+  static constexpr int kTileTok = kTile * kSub;                 // tokens per stage
+  static constexpr int kSubBytes = 2 * kTileBytes + 2 * kScaleTileBytes;
+  static constexpr int kMiscOffset = kSub * kSubBytes;
+  static constexpr int kStageBytes = kSub * kSubBytes + 16 * kSub;
   static constexpr int kStages =
       kHalf ? PKV_STAGES_HALF : (KV == PKV_FP8_E4M3 ? PKV_STAGES_FP8 : PKV_STAGES_INT4);
   static constexpr int kWarpRing = kStages * kStageBytes;
@@ -147,15 +168,20 @@ struct Params {
   float softmax_scale;
 };
 
-// Issue the copies of one 16-token tile into a stage (lane-parallel).
+// Issue the copies of one 16-token sub-tile (tokens [t0, t0 + 16) of the
+// sequence) into its place in a stage (lane-parallel).  `stage` is the
+// sub-tile's shared-memory base, `misc_smem`/`misc` its 16-byte misc slot.
+// Sub-tiles past the unit's end copy nothing and are marked empty.
 template <int KV, int D>
-__device__ __forceinline__ void issue_tile(const Params& p, int kvh, int t0, int phys,
-                                           uint32_t stage, uint8_t* stage_ptr, int lane) {
+__device__ __forceinline__ void issue_tile(const Params& p, int kvh, int t0, int tok_end, int phys,
+                                           uint32_t stage, uint32_t misc_smem, int* misc,
+                                           int lane) {
   using G = Geo<KV, D>;
   const int logical = t0 / p.block_size;
+  const bool live = t0 < tok_end;
   const bool ok = phys >= 0 && phys < p.num_blocks;
-  int* misc = reinterpret_cast<int*>(stage_ptr + G::kStageBytes - 16);
-  if (lane == 0) misc[2] = ok ? 1 : 0;
+  if (lane == 0) misc[2] = (live && ok) ? 1 : 0;
+  if (!live) return;
   if (!ok) {
     if (lane == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
     return;
@@ -193,7 +219,7 @@ __device__ __forceinline__ void issue_tile(const Params& p, int kvh, int t0, int
     const float* sc = static_cast<const float*>(p.scales);
     const int64_t idx = static_cast<int64_t>(phys) * p.num_kv_heads + kvh;
     const int64_t per_kv = static_cast<int64_t>(p.num_blocks) * p.num_kv_heads;
-    const uint32_t mo = stage + G::kStageBytes - 16;
+    const uint32_t mo = misc_smem;
     if (lane == 0) asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(mo), "l"(sc + idx) : "memory");
     if (lane == 1) asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(mo + 4), "l"(sc + per_kv + idx) : "memory");
   }
@@ -204,16 +230,16 @@ struct Unit {
   int b, kvh, part, tok_begin, tok_end, ntiles;
 };
 
-// A CTA owns partitions [blockIdx.x * PPC, +PPC) of sequence b, KV head kvh
-// (those below the sequence's partition count); unit j is the j-th of them.
-__device__ __forceinline__ Unit make_unit(const Params& p, int b, int kvh, int ctx, int j) {
+// Unit = partition `part` of sequence b, KV head kvh.
+template <int kTok>
+__device__ __forceinline__ Unit make_unit(const Params& p, int b, int kvh, int ctx, int part) {
   Unit u;
   u.b = b;
   u.kvh = kvh;
-  u.part = blockIdx.x * p.parts_per_cta + j;
+  u.part = part;
   u.tok_begin = u.part * p.partition_size;
   u.tok_end = min(ctx, u.tok_begin + p.partition_size);
-  u.ntiles = ctx > 0 ? (u.tok_end - u.tok_begin + kTile - 1) / kTile : 0;
+  u.ntiles = ctx > 0 ? (u.tok_end - u.tok_begin + kTok - 1) / kTok : 0;
   return u;
 }
 
@@ -349,7 +375,15 @@ __device__ __forceinline__ void merge_state(float (&ma)[2], float (&la)[2], floa
 // warp t % W) and keep their copy rings running across partition boundaries,
 // so the next partition's tiles are already in flight while a partition's
 // four warp states are merged; Q and the setup are paid once per run.
-template <int KV, int QT, int D>
+//
+// Two ways to share the work (WU):
+//  WU = false: the CTA's units are partitions [blockIdx.x * PPC, +PPC); the
+//    four warps share each partition's tiles and merge their states at its end.
+//  WU = true (split-KV with many partitions): each warp owns whole units: warp
+//    w takes KV head blockIdx.y * W + w of partitions [blockIdx.x * PPC, +PPC),
+//    streams their tiles alone and writes its own partial results -- no
+//    merges, no barriers, and every warp of a CTA has the same token count.
+template <int KV, int QT, int D, bool WU>
 __global__ void __launch_bounds__(kDecodeWarps * kWarp, Geo<KV, D>::kMinBlocks)
 paged_decode_kernel(const Params p) {
   using G = Geo<KV, D>;
@@ -372,16 +406,23 @@ paged_decode_kernel(const Params p) {
   const int group = p.num_q_heads / p.num_kv_heads;
   const int cap = p.max_blocks_per_seq * p.block_size;
 
-  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int kvh = WU ? static_cast<int>(blockIdx.y) * kDecodeWarps + warp : static_cast<int>(blockIdx.y);
+  const int b = blockIdx.z;
+  if (WU && kvh >= p.num_kv_heads) return;
   int ctx = p.context_lens[b];
   if (ctx > cap) {
     // a context longer than its table row can hold is clamped (and flagged)
-    if (threadIdx.x == 0 && blockIdx.x == 0 && kvh == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
+    if (lane == 0 && blockIdx.x == 0 && kvh == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
     ctx = cap;
   }
   const int nparts_seq = ctx > 0 ? (ctx + p.partition_size - 1) / p.partition_size : 1;
-  const int nunits = min(p.parts_per_cta, nparts_seq - static_cast<int>(blockIdx.x) * p.parts_per_cta);
-  if (nunits <= 0) return;
+  // unit j -> partition; tiles of a unit this warp takes: kFirst, kFirst + kStride, ...
+  constexpr int kStride = WU ? 1 : kDecodeWarps;
+  const int kFirst = WU ? 0 : warp;
+  const int pbase = static_cast<int>(blockIdx.x) * p.parts_per_cta;
+  auto part_of = [&](int j) -> int { return pbase + j; };
+  const int nunits = min(p.parts_per_cta, nparts_seq - pbase);
+  if (nunits <= 0) return;                 // the whole CTA (same b and partitions for all warps)
 
   uint8_t* ring_ptr = smem + warp * G::kWarpRing;
   const uint32_t ring = smem_u32(ring_ptr);
@@ -389,35 +430,38 @@ paged_decode_kernel(const Params p) {
 
   // ---------------------------------------------------------------- issue cursor
   // Walks (unit, tile) pairs with tile = warp, warp + W, ... < ntiles, in unit
-  // order.  The physical block ids of the warp's tiles of a unit are loaded 32
-  // at a time into a register (lane l: the warp's tile 32k + l); the first
-  // window of the next unit is prefetched on entering a unit.
+  // order.  The physical block ids of the warp's 16-token sub-tiles of a unit
+  // are loaded 32 at a time into a register (lane l of window k: the warp's
+  // sub-tile 32k + l, i.e. sub-tile (32k + l) % kSub of its tile (32k + l) /
+  // kSub); window 0 of the next unit is prefetched on entering a unit.
   int iu = -1, it = 0, i_tb = 0, i_next_tb = -1, i_win = 0;
   Unit iunit;
   iunit.ntiles = 0;
   auto window = [&](const Unit& u, int k) -> int {
-    const int tile = warp + kDecodeWarps * (32 * k + lane);
-    if (tile >= u.ntiles) return -1;
+    const int sidx = 32 * k + lane;
+    const int tile = kFirst + kStride * (sidx / G::kSub);
+    const int tok = u.tok_begin + tile * G::kTileTok + (sidx % G::kSub) * kTile;
+    if (tile >= u.ntiles || tok >= u.tok_end) return -1;
     const int32_t* trow = p.block_tables + static_cast<int64_t>(u.b) * p.max_blocks_per_seq;
-    return __ldg(trow + (u.tok_begin + tile * kTile) / p.block_size);
+    return __ldg(trow + tok / p.block_size);
   };
   auto next_window_unit = [&](int j) -> int {          // window 0 of unit j (or -1s)
-    return j < nunits ? window(make_unit(p, b, kvh, ctx, j), 0) : -1;
+    return j < nunits ? window(make_unit<G::kTileTok>(p, b, kvh, ctx, part_of(j)), 0) : -1;
   };
   // advance to the next pair this warp issues; false when the stream is done
   auto issue_advance = [&]() -> bool {
-    it += kDecodeWarps;
+    it += kStride;
     while (it >= iunit.ntiles) {
       if (iu + 1 >= nunits) return false;
       ++iu;
-      iunit = make_unit(p, b, kvh, ctx, iu);
-      it = warp;
+      iunit = make_unit<G::kTileTok>(p, b, kvh, ctx, part_of(iu));
+      it = kFirst;
       i_tb = i_next_tb;                                  // prefetched window 0 of unit iu
       i_win = 0;
       i_next_tb = next_window_unit(iu + 1);
     }
-    const int k = (it - warp) / kDecodeWarps;             // the warp's tile index in the unit
-    if ((k >> 5) != i_win) {                              // beyond 32 tiles: next window
+    const int k = (it - kFirst) / kStride * G::kSub;     // the warp's first sub-tile index
+    if ((k >> 5) != i_win) {                              // beyond 32 sub-tiles: next window
       i_win = k >> 5;
       i_tb = window(iunit, i_win);
     }
@@ -426,10 +470,18 @@ paged_decode_kernel(const Params p) {
   int issued = 0;                                        // pairs issued so far (ring position)
   auto issue_next = [&]() {
     if (issue_advance()) {
-      const int phys = __shfl_sync(0xffffffffu, i_tb, ((it - warp) / kDecodeWarps) & 31);
+      const int k = (it - kFirst) / kStride * G::kSub;
       const int s = issued % G::kStages;
-      issue_tile<KV, D>(p, iunit.kvh, iunit.tok_begin + it * kTile, phys,
-                        ring + s * G::kStageBytes, ring_ptr + s * G::kStageBytes, lane);
+      const uint32_t sb = ring + s * G::kStageBytes;
+      uint8_t* sp = ring_ptr + s * G::kStageBytes;
+#pragma unroll
+      for (int u = 0; u < G::kSub; ++u) {
+        const int phys = __shfl_sync(0xffffffffu, i_tb, (k + u) & 31);
+        issue_tile<KV, D>(p, iunit.kvh, iunit.tok_begin + it * G::kTileTok + u * kTile,
+                          iunit.tok_end, phys, sb + u * G::kSubBytes,
+                          sb + G::kMiscOffset + 16 * u,
+                          reinterpret_cast<int*>(sp + G::kMiscOffset + 16 * u), lane);
+      }
     }
     ++issued;
     cp_async_commit();
@@ -449,11 +501,11 @@ paged_decode_kernel(const Params p) {
   float zacc[KV == PKV_INT4_G32 ? D / 32 : 1][2];
   float vref, inv_vref;                      // FP8: oacc is in units of vref / kPScale
   int consumed = 0;                          // pairs computed so far (ring position)
-  load_q<KV, QT, D>(p, make_unit(p, b, kvh, ctx, 0), q4, c4, qb, qexp, qsum, qoff);
+  load_q<KV, QT, D>(p, make_unit<G::kTileTok>(p, b, kvh, ctx, part_of(0)), q4, c4, qb, qexp, qsum, qoff);
 
 #pragma unroll 1
   for (int cu = 0; cu < nunits; ++cu) {
-    const Unit unit = make_unit(p, b, kvh, ctx, cu);
+    const Unit unit = make_unit<G::kTileTok>(p, b, kvh, ctx, part_of(cu));
 #pragma unroll
     for (int i = 0; i < MT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
     mrow[0] = mrow[1] = -INFINITY;           // running max (log2 units), heads 2c4, 2c4+1
@@ -466,104 +518,122 @@ paged_decode_kernel(const Params p) {
     const int tok_end = unit.tok_end;
 
 #pragma unroll 1
-    for (int ct = warp; ct < unit.ntiles; ct += kDecodeWarps) {
+    for (int ct = kFirst; ct < unit.ntiles; ct += kStride) {
       cp_async_wait<G::kStages - 1>();
       __syncwarp();
       const int stage = consumed % G::kStages;
-      const uint32_t st = ring + stage * G::kStageBytes;
+      const uint32_t stb = ring + stage * G::kStageBytes;
       const uint8_t* st_ptr = ring_ptr + stage * G::kStageBytes;
-      const int* misc = reinterpret_cast<const int*>(st_ptr + G::kStageBytes - 16);
-      const int t0 = unit.tok_begin + ct * kTile;
-      const int nvalid = misc[2] ? min(kTile, tok_end - t0) : 0;
+      const int* misc0 = reinterpret_cast<const int*>(st_ptr + G::kMiscOffset);
+      const int t0 = unit.tok_begin + ct * G::kTileTok;
+      // sub-tile u covers tokens [t0 + 16u, t0 + 16u + 16)
+      int nval[G::kSub];
+      bool any_valid = false;
+#pragma unroll
+      for (int u = 0; u < G::kSub; ++u) {
+        nval[u] = misc0[4 * u + 2] ? max(0, min(kTile, tok_end - (t0 + kTile * u))) : 0;
+        any_valid |= nval[u] > 0;
+      }
 
-      if (nvalid > 0) {
-        // ------------------------------------------------ S^T = K_tile Q^T
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
-        float sc2[4] = {0.f, 0.f, 0.f, 0.f};     // second chain: halves the mma dependency depth
-        if constexpr (kHalf) {
+      if (any_valid) {
+        float scs[G::kSub][4];
 #pragma unroll
-          for (int jp = 0; jp < D / 32; ++jp) {
-            // thread reads chunk 4jp+c4 of rows q4 and q4+8: words = d pairs
-            const uint4 r0 = ld_shared_v4(st + chunk_off<KV, D>(q4, 4 * jp + c4));
-            const uint4 r1 = ld_shared_v4(st + chunk_off<KV, D>(q4 + 8, 4 * jp + c4));
-            const uint32_t a0[4] = {r0.x, r1.x, r0.y, r1.y};
-            mma_16816<MMA_T>(sc, a0, qb[2 * jp][0], qb[2 * jp][1]);
-            const uint32_t a1[4] = {r0.z, r1.z, r0.w, r1.w};
-            mma_16816<MMA_T>(sc2, a1, qb[2 * jp + 1][0], qb[2 * jp + 1][1]);
-          }
-        } else if constexpr (KV == PKV_FP8_E4M3) {
+        for (int u = 0; u < G::kSub; ++u) {
+          const uint32_t st = stb + u * G::kSubBytes;
+          const int* misc = misc0 + 4 * u;
+          const int nvalid = nval[u];
+            // ------------------------------------------------ S^T = K_tile Q^T
+            float sc[4] = {0.f, 0.f, 0.f, 0.f};
+            float sc2[4] = {0.f, 0.f, 0.f, 0.f};     // second chain: halves the mma dependency depth
+            if constexpr (kHalf) {
 #pragma unroll
-          for (int i = 0; i < D / 64; ++i) {
-            const uint4 r0 = ld_shared_v4(st + chunk_off<KV, D>(q4, 4 * i + c4));
-            const uint4 r1 = ld_shared_v4(st + chunk_off<KV, D>(q4 + 8, 4 * i + c4));
-            const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w};
-            const uint32_t w1[4] = {r1.x, r1.y, r1.z, r1.w};
+              for (int jp = 0; jp < D / 32; ++jp) {
+                // thread reads chunk 4jp+c4 of rows q4 and q4+8: words = d pairs
+                const uint4 r0 = ld_shared_v4(st + chunk_off<KV, D>(q4, 4 * jp + c4));
+                const uint4 r1 = ld_shared_v4(st + chunk_off<KV, D>(q4 + 8, 4 * jp + c4));
+                const uint32_t a0[4] = {r0.x, r1.x, r0.y, r1.y};
+                mma_16816<MMA_T>(sc, a0, qb[2 * jp][0], qb[2 * jp][1]);
+                const uint32_t a1[4] = {r0.z, r1.z, r0.w, r1.w};
+                mma_16816<MMA_T>(sc2, a1, qb[2 * jp + 1][0], qb[2 * jp + 1][1]);
+              }
+            } else if constexpr (KV == PKV_FP8_E4M3) {
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const uint32_t a[4] = {e4m3x2_to_f16x2(w0[h] & 0xFFFF), e4m3x2_to_f16x2(w1[h] & 0xFFFF),
-                                     e4m3x2_to_f16x2(w0[h] >> 16), e4m3x2_to_f16x2(w1[h] >> 16)};
-              if (h & 1)
-                mma_16816<PKV_F16>(sc2, a, qb[4 * i + h][0], qb[4 * i + h][1]);
-              else
-                mma_16816<PKV_F16>(sc, a, qb[4 * i + h][0], qb[4 * i + h][1]);
+              for (int i = 0; i < D / 64; ++i) {
+                const uint4 r0 = ld_shared_v4(st + chunk_off<KV, D>(q4, 4 * i + c4));
+                const uint4 r1 = ld_shared_v4(st + chunk_off<KV, D>(q4 + 8, 4 * i + c4));
+                const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w};
+                const uint32_t w1[4] = {r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                  const uint32_t a[4] = {e4m3x2_to_f16x2(w0[h] & 0xFFFF), e4m3x2_to_f16x2(w1[h] & 0xFFFF),
+                                         e4m3x2_to_f16x2(w0[h] >> 16), e4m3x2_to_f16x2(w1[h] >> 16)};
+                  if (h & 1)
+                    mma_16816<PKV_F16>(sc2, a, qb[4 * i + h][0], qb[4 * i + h][1]);
+                  else
+                    mma_16816<PKV_F16>(sc, a, qb[4 * i + h][0], qb[4 * i + h][1]);
+                }
+              }
+            } else {
+              // INT4: one fresh accumulator per 32-element group, then
+              // s += scale_t * acc + zero_t * sum(q)
+              constexpr int SR = G::kScaleRowBytes;
+              const uint32_t ksc = st + 2 * G::kTileBytes;
+              uint32_t sz0[D / 32], sz1[D / 32];
+              if constexpr (D == 128) {
+                const uint4 a = ld_shared_v4(ksc + q4 * SR), c = ld_shared_v4(ksc + (q4 + 8) * SR);
+                sz0[0] = a.x; sz0[1] = a.y; sz0[2] = a.z; sz0[3] = a.w;
+                sz1[0] = c.x; sz1[1] = c.y; sz1[2] = c.z; sz1[3] = c.w;
+              } else {
+                const uint2 a = ld_shared_v2(ksc + q4 * SR), c = ld_shared_v2(ksc + (q4 + 8) * SR);
+                sz0[0] = a.x; sz0[1] = a.y; sz1[0] = c.x; sz1[1] = c.y;
+              }
+#pragma unroll
+              for (int grp = 0; grp < D / 32; ++grp) {
+                const uint32_t w0 = ld_shared_b32(st + q4 * G::kRowBytes + 16 * (grp ^ swz<KV, D>(q4)) + 4 * c4);
+                const uint32_t w1 = ld_shared_b32(st + (q4 + 8) * G::kRowBytes +
+                                                  16 * (grp ^ swz<KV, D>(q4 + 8)) + 4 * c4);
+                float g4[4] = {0.f, 0.f, 0.f, 0.f};
+                // codes enter as f16 1024 + n; 1024 * sum(q) is taken off the group sum
+                const uint32_t a0[4] = {nibbles_offset_f16x2(w0, 0), nibbles_offset_f16x2(w1, 0),
+                                        nibbles_offset_f16x2(w0, 1), nibbles_offset_f16x2(w1, 1)};
+                mma_16816<PKV_F16>(g4, a0, qb[2 * grp][0], qb[2 * grp][1]);
+                const uint32_t a1[4] = {nibbles_offset_f16x2(w0, 2), nibbles_offset_f16x2(w1, 2),
+                                        nibbles_offset_f16x2(w0, 3), nibbles_offset_f16x2(w1, 3)};
+                mma_16816<PKV_F16>(g4, a1, qb[2 * grp + 1][0], qb[2 * grp + 1][1]);
+                const float2 f0 = Half16<PKV_F16>::unpack(sz0[grp]);   // (scale, zero) token q4
+                const float2 f1 = Half16<PKV_F16>::unpack(sz1[grp]);   // token q4 + 8
+                const float s0 = f0.x * qexp, s1 = f1.x * qexp;
+                sc[0] += s0 * (g4[0] - qoff[grp][0]) + f0.y * qsum[grp][0];
+                sc[1] += s0 * (g4[1] - qoff[grp][1]) + f0.y * qsum[grp][1];
+                sc[2] += s1 * (g4[2] - qoff[grp][0]) + f1.y * qsum[grp][0];
+                sc[3] += s1 * (g4[3] - qoff[grp][1]) + f1.y * qsum[grp][1];
+              }
             }
-          }
-        } else {
-          // INT4: one fresh accumulator per 32-element group, then
-          // s += scale_t * acc + zero_t * sum(q)
-          constexpr int SR = G::kScaleRowBytes;
-          const uint32_t ksc = st + 2 * G::kTileBytes;
-          uint32_t sz0[D / 32], sz1[D / 32];
-          if constexpr (D == 128) {
-            const uint4 a = ld_shared_v4(ksc + q4 * SR), c = ld_shared_v4(ksc + (q4 + 8) * SR);
-            sz0[0] = a.x; sz0[1] = a.y; sz0[2] = a.z; sz0[3] = a.w;
-            sz1[0] = c.x; sz1[1] = c.y; sz1[2] = c.z; sz1[3] = c.w;
-          } else {
-            const uint2 a = ld_shared_v2(ksc + q4 * SR), c = ld_shared_v2(ksc + (q4 + 8) * SR);
-            sz0[0] = a.x; sz0[1] = a.y; sz1[0] = c.x; sz1[1] = c.y;
-          }
-#pragma unroll
-          for (int grp = 0; grp < D / 32; ++grp) {
-            const uint32_t w0 = ld_shared_b32(st + q4 * G::kRowBytes + 16 * (grp ^ swz<KV, D>(q4)) + 4 * c4);
-            const uint32_t w1 = ld_shared_b32(st + (q4 + 8) * G::kRowBytes +
-                                              16 * (grp ^ swz<KV, D>(q4 + 8)) + 4 * c4);
-            float g4[4] = {0.f, 0.f, 0.f, 0.f};
-            // codes enter as f16 1024 + n; 1024 * sum(q) is taken off the group sum
-            const uint32_t a0[4] = {nibbles_offset_f16x2(w0, 0), nibbles_offset_f16x2(w1, 0),
-                                    nibbles_offset_f16x2(w0, 1), nibbles_offset_f16x2(w1, 1)};
-            mma_16816<PKV_F16>(g4, a0, qb[2 * grp][0], qb[2 * grp][1]);
-            const uint32_t a1[4] = {nibbles_offset_f16x2(w0, 2), nibbles_offset_f16x2(w1, 2),
-                                    nibbles_offset_f16x2(w0, 3), nibbles_offset_f16x2(w1, 3)};
-            mma_16816<PKV_F16>(g4, a1, qb[2 * grp + 1][0], qb[2 * grp + 1][1]);
-            const float2 f0 = Half16<PKV_F16>::unpack(sz0[grp]);   // (scale, zero) token q4
-            const float2 f1 = Half16<PKV_F16>::unpack(sz1[grp]);   // token q4 + 8
-            const float s0 = f0.x * qexp, s1 = f1.x * qexp;
-            sc[0] += s0 * (g4[0] - qoff[grp][0]) + f0.y * qsum[grp][0];
-            sc[1] += s0 * (g4[1] - qoff[grp][1]) + f0.y * qsum[grp][1];
-            sc[2] += s1 * (g4[2] - qoff[grp][0]) + f1.y * qsum[grp][0];
-            sc[3] += s1 * (g4[3] - qoff[grp][1]) + f1.y * qsum[grp][1];
-          }
-        }
 
 #pragma unroll
-        for (int k = 0; k < 4; ++k) sc[k] += sc2[k];
+            for (int k = 0; k < 4; ++k) sc[k] += sc2[k];
 
-        // ------------------------------------------------ scale, mask, online softmax
-        float mult = base;
-        float vs_tile = 1.f;
-        if constexpr (KV == PKV_FP8_E4M3) {
-          const float* fs = reinterpret_cast<const float*>(misc);
-          mult *= fs[0];
-          vs_tile = fs[1];
-        } else if constexpr (KV == PKV_INT4_G32) {
-          mult = p.softmax_scale * kLog2e;       // qexp already folded into the group sums
+          // ---------------------------------------------- scale and mask
+          float mult = base;
+          if constexpr (KV == PKV_FP8_E4M3) {
+            mult *= reinterpret_cast<const float*>(misc)[0];
+          } else if constexpr (KV == PKV_INT4_G32) {
+            mult = p.softmax_scale * kLog2e;     // qexp already folded into the group sums
+          }
+          const bool v0 = q4 < nvalid, v1 = q4 + 8 < nvalid;
+          scs[u][0] = v0 ? sc[0] * mult : -INFINITY;
+          scs[u][1] = v0 ? sc[1] * mult : -INFINITY;
+          scs[u][2] = v1 ? sc[2] * mult : -INFINITY;
+          scs[u][3] = v1 ? sc[3] * mult : -INFINITY;
         }
-        const bool v0 = q4 < nvalid, v1 = q4 + 8 < nvalid;
-        sc[0] = v0 ? sc[0] * mult : -INFINITY;
-        sc[1] = v0 ? sc[1] * mult : -INFINITY;
-        sc[2] = v1 ? sc[2] * mult : -INFINITY;
-        sc[3] = v1 ? sc[3] * mult : -INFINITY;
-        float tmax0 = fmaxf(sc[0], sc[2]), tmax1 = fmaxf(sc[1], sc[3]);
+
+        // ------------------------------------------------ online softmax over the tile
+        float tmax0 = -INFINITY, tmax1 = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < G::kSub; ++u) {
+          tmax0 = fmaxf(tmax0, fmaxf(scs[u][0], scs[u][2]));
+          tmax1 = fmaxf(tmax1, fmaxf(scs[u][1], scs[u][3]));
+        }
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
           tmax0 = fmaxf(tmax0, __shfl_xor_sync(0xffffffffu, tmax0, o));
@@ -574,13 +644,22 @@ paged_decode_kernel(const Params p) {
         // or when the FP8 reference V scale must be rebased.
         // A block whose FP8 scale is 0 was never written: its V rows dequantize
         // to 0 and add nothing (its scores still count in the softmax sum).
-        bool v_on = true, rebase = false;
-        float vfac = 1.f;                          // FP8: this tile's V scale / vref
-        if constexpr (KV == PKV_FP8_E4M3) {
-          v_on = vs_tile > 0.f;
-          if (v_on) {
-            vfac = vs_tile * inv_vref;             // 0 while no reference is set
-            rebase = !(vfac >= 0.0625f && vfac <= 16.f);
+        bool von[G::kSub];
+        float vfac[G::kSub];                     // FP8: a sub-tile's V scale / vref
+        bool rebase = false;
+        float vmax = 0.f;
+#pragma unroll
+        for (int u = 0; u < G::kSub; ++u) {
+          von[u] = nval[u] > 0;
+          vfac[u] = 1.f;
+          if constexpr (KV == PKV_FP8_E4M3) {
+            const float vs = reinterpret_cast<const float*>(misc0 + 4 * u)[1];
+            von[u] = von[u] && vs > 0.f;
+            if (von[u]) {
+              vfac[u] = vs * inv_vref;           // 0 while no reference is set
+              rebase |= !(vfac[u] >= 0.0625f && vfac[u] <= 16.f);
+              vmax = fmaxf(vmax, vs);
+            }
           }
         }
         const bool grow = tmax0 > mrow[0] + kTau || tmax1 > mrow[1] + kTau;
@@ -596,11 +675,15 @@ paged_decode_kernel(const Params p) {
           }
           if constexpr (KV == PKV_FP8_E4M3) {
             if (rebase) {
-              // O_true = oacc * vref / kPScale stays invariant across the rebase
-              const float r = __frcp_rn(vs_tile);
+              // new reference: the tile's largest V scale; O_true = oacc * vref /
+              // kPScale stays invariant across the rebase
+              const float r = __frcp_rn(vmax);
               const float f = vref > 0.f ? vref * r : 1.f;
               alpha0 *= f; alpha1 *= f;
-              vref = vs_tile; inv_vref = r; vfac = 1.f;
+              vref = vmax; inv_vref = r;
+#pragma unroll
+              for (int u = 0; u < G::kSub; ++u)
+                vfac[u] = reinterpret_cast<const float*>(misc0 + 4 * u)[1] * r;
             }
           }
 #pragma unroll
@@ -609,146 +692,154 @@ paged_decode_kernel(const Params p) {
             oacc[i][2] *= alpha0; oacc[i][3] *= alpha1;
           }
         }
-        const float pr[4] = {fast_exp2(sc[0] - mrow[0]), fast_exp2(sc[1] - mrow[1]),
-                             fast_exp2(sc[2] - mrow[0]), fast_exp2(sc[3] - mrow[1])};
-        lrow[0] += pr[0] + pr[2];
-        lrow[1] += pr[1] + pr[3];
 
-        // ------------------------------------------------ O^T += V_tile^T P^T
-        const uint32_t vt = st + G::kTileBytes;
-        // rows (tokens) this thread's V fragments cover: 2c4, 2c4+1, 2c4+8, 2c4+9
-        const int tA = 2 * c4, tB = 2 * c4 + 1, tC = 2 * c4 + 8, tE = 2 * c4 + 9;
-        const bool partial = nvalid < kTile;
-        const uint32_t mA = (tA < nvalid) ? 0xFFFFFFFFu : 0u, mB = (tB < nvalid) ? 0xFFFFFFFFu : 0u;
-        const uint32_t mC = (tC < nvalid) ? 0xFFFFFFFFu : 0u, mE = (tE < nvalid) ? 0xFFFFFFFFu : 0u;
-
-        if (v_on) {
-        if constexpr (KV != PKV_INT4_G32) {
-          // P as B fragments (hi + lo split)
-          using H = Half16<MMA_T>;
-          const float ps = kPScale * vfac;
-          const float pp[4] = {pr[0] * ps, pr[1] * ps, pr[2] * ps, pr[3] * ps};
-          const uint32_t h01 = H::pack_rn(pp[0], pp[1]), h23 = H::pack_rn(pp[2], pp[3]);
-          const float2 f01 = H::unpack(h01), f23 = H::unpack(h23);
-          const uint32_t l01 = H::pack_rn(pp[0] - f01.x, pp[1] - f01.y);
-          const uint32_t l23 = H::pack_rn(pp[2] - f23.x, pp[3] - f23.y);
-          const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-          const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
-
-          if constexpr (kHalf) {
 #pragma unroll
-            for (int hc = 0; hc < D / 64; ++hc) {
-              // chunk (D/64 == 2 ? 2*q4 + hc : q4): d = 16*q4 + 8*hc + 0..7 (D=128) or 8*q4 + 0..7
-              const int ch = (D == 128) ? 2 * q4 + hc : q4;
-              uint4 A = ld_shared_v4(vt + chunk_off<KV, D>(tA, ch));
-              uint4 B = ld_shared_v4(vt + chunk_off<KV, D>(tB, ch));
-              uint4 C = ld_shared_v4(vt + chunk_off<KV, D>(tC, ch));
-              uint4 E = ld_shared_v4(vt + chunk_off<KV, D>(tE, ch));
-              if (partial) {
-                A.x &= mA; A.y &= mA; A.z &= mA; A.w &= mA;
-                B.x &= mB; B.y &= mB; B.z &= mB; B.w &= mB;
-                C.x &= mC; C.y &= mC; C.z &= mC; C.w &= mC;
-                E.x &= mE; E.y &= mE; E.z &= mE; E.w &= mE;
-              }
-              const uint32_t wa[4] = {A.x, A.y, A.z, A.w}, wb[4] = {B.x, B.y, B.z, B.w};
-              const uint32_t wc[4] = {C.x, C.y, C.z, C.w}, we[4] = {E.x, E.y, E.z, E.w};
+        for (int u = 0; u < G::kSub; ++u) {
+          const uint32_t st = stb + u * G::kSubBytes;
+          const int nvalid = nval[u];
+          const bool v0 = q4 < nvalid, v1 = q4 + 8 < nvalid;
+          const bool v_on = von[u];
+          const float pr[4] = {fast_exp2(scs[u][0] - mrow[0]), fast_exp2(scs[u][1] - mrow[1]),
+                               fast_exp2(scs[u][2] - mrow[0]), fast_exp2(scs[u][3] - mrow[1])};
+          lrow[0] += pr[0] + pr[2];
+          lrow[1] += pr[1] + pr[3];
+          const float vfac_u = vfac[u];
+            // ------------------------------------------------ O^T += V_tile^T P^T
+            const uint32_t vt = st + G::kTileBytes;
+            // rows (tokens) this thread's V fragments cover: 2c4, 2c4+1, 2c4+8, 2c4+9
+            const int tA = 2 * c4, tB = 2 * c4 + 1, tC = 2 * c4 + 8, tE = 2 * c4 + 9;
+            const bool partial = nvalid < kTile;
+            const uint32_t mA = (tA < nvalid) ? 0xFFFFFFFFu : 0u, mB = (tB < nvalid) ? 0xFFFFFFFFu : 0u;
+            const uint32_t mC = (tC < nvalid) ? 0xFFFFFFFFu : 0u, mE = (tE < nvalid) ? 0xFFFFFFFFu : 0u;
+
+            if (v_on) {
+            if constexpr (KV != PKV_INT4_G32) {
+              // P as B fragments (hi + lo split)
+              using H = Half16<MMA_T>;
+              const float ps = kPScale * vfac_u;
+              const float pp[4] = {pr[0] * ps, pr[1] * ps, pr[2] * ps, pr[3] * ps};
+              const uint32_t h01 = H::pack_rn(pp[0], pp[1]), h23 = H::pack_rn(pp[2], pp[3]);
+              const float2 f01 = H::unpack(h01), f23 = H::unpack(h23);
+              const uint32_t l01 = H::pack_rn(pp[0] - f01.x, pp[1] - f01.y);
+              const uint32_t l23 = H::pack_rn(pp[2] - f23.x, pp[3] - f23.y);
+              const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+              const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+
+              if constexpr (kHalf) {
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const int i = 4 * hc + k;                       // m-tile: d = base + 2i (+1)
-                const uint32_t a[4] = {__byte_perm(wa[k], wb[k], 0x5410), __byte_perm(wa[k], wb[k], 0x7632),
-                                       __byte_perm(wc[k], we[k], 0x5410), __byte_perm(wc[k], we[k], 0x7632)};
-                mma_16816<MMA_T>(oacc[i], a, bh0, bh1);
-                mma_16816<MMA_T>(oacc[i], a, bl0, bl1);
+                for (int hc = 0; hc < D / 64; ++hc) {
+                  // chunk (D/64 == 2 ? 2*q4 + hc : q4): d = 16*q4 + 8*hc + 0..7 (D=128) or 8*q4 + 0..7
+                  const int ch = (D == 128) ? 2 * q4 + hc : q4;
+                  uint4 A = ld_shared_v4(vt + chunk_off<KV, D>(tA, ch));
+                  uint4 B = ld_shared_v4(vt + chunk_off<KV, D>(tB, ch));
+                  uint4 C = ld_shared_v4(vt + chunk_off<KV, D>(tC, ch));
+                  uint4 E = ld_shared_v4(vt + chunk_off<KV, D>(tE, ch));
+                  if (partial) {
+                    A.x &= mA; A.y &= mA; A.z &= mA; A.w &= mA;
+                    B.x &= mB; B.y &= mB; B.z &= mB; B.w &= mB;
+                    C.x &= mC; C.y &= mC; C.z &= mC; C.w &= mC;
+                    E.x &= mE; E.y &= mE; E.z &= mE; E.w &= mE;
+                  }
+                  const uint32_t wa[4] = {A.x, A.y, A.z, A.w}, wb[4] = {B.x, B.y, B.z, B.w};
+                  const uint32_t wc[4] = {C.x, C.y, C.z, C.w}, we[4] = {E.x, E.y, E.z, E.w};
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) {
+                    const int i = 4 * hc + k;                       // m-tile: d = base + 2i (+1)
+                    const uint32_t a[4] = {__byte_perm(wa[k], wb[k], 0x5410), __byte_perm(wa[k], wb[k], 0x7632),
+                                           __byte_perm(wc[k], we[k], 0x5410), __byte_perm(wc[k], we[k], 0x7632)};
+                    mma_16816<MMA_T>(oacc[i], a, bh0, bh1);
+                    mma_16816<MMA_T>(oacc[i], a, bl0, bl1);
+                  }
+                }
+              } else {
+                // FP8: d = base(q4) + 0..15 (D=128) or 8*q4 + 0..7 (D=64)
+                constexpr int NW = D / 32;                          // words per token: 4 or 2
+                uint32_t wa[NW], wb[NW], wc[NW], we[NW];
+                if constexpr (D == 128) {
+                  const int pi = ((q4 & 1) << 1) | ((q4 >> 1) & 1) | (q4 & 4);
+                  const uint4 A = ld_shared_v4(vt + chunk_off<KV, D>(tA, pi));
+                  const uint4 B = ld_shared_v4(vt + chunk_off<KV, D>(tB, pi));
+                  const uint4 C = ld_shared_v4(vt + chunk_off<KV, D>(tC, pi));
+                  const uint4 E = ld_shared_v4(vt + chunk_off<KV, D>(tE, pi));
+                  wa[0] = A.x; wa[1] = A.y; wa[2] = A.z; wa[3] = A.w;
+                  wb[0] = B.x; wb[1] = B.y; wb[2] = B.z; wb[3] = B.w;
+                  wc[0] = C.x; wc[1] = C.y; wc[2] = C.z; wc[3] = C.w;
+                  we[0] = E.x; we[1] = E.y; we[2] = E.z; we[3] = E.w;
+                } else {
+                  const uint2 A = ld_shared_v2(vt + tA * G::kRowBytes + 8 * q4);
+                  const uint2 B = ld_shared_v2(vt + tB * G::kRowBytes + 8 * q4);
+                  const uint2 C = ld_shared_v2(vt + tC * G::kRowBytes + 8 * q4);
+                  const uint2 E = ld_shared_v2(vt + tE * G::kRowBytes + 8 * q4);
+                  wa[0] = A.x; wa[1] = A.y; wb[0] = B.x; wb[1] = B.y;
+                  wc[0] = C.x; wc[1] = C.y; we[0] = E.x; we[1] = E.y;
+                }
+                if (partial) {
+#pragma unroll
+                  for (int k = 0; k < NW; ++k) { wa[k] &= mA; wb[k] &= mB; wc[k] &= mC; we[k] &= mE; }
+                }
+#pragma unroll
+                for (int k = 0; k < NW; ++k) {
+                  const uint32_t x01 = __byte_perm(wa[k], wb[k], 0x5140), x23 = __byte_perm(wa[k], wb[k], 0x7362);
+                  const uint32_t y01 = __byte_perm(wc[k], we[k], 0x5140), y23 = __byte_perm(wc[k], we[k], 0x7362);
+                  const uint32_t a0[4] = {e4m3x2_to_f16x2(x01 & 0xFFFF), e4m3x2_to_f16x2(x01 >> 16),
+                                          e4m3x2_to_f16x2(y01 & 0xFFFF), e4m3x2_to_f16x2(y01 >> 16)};
+                  mma_16816<PKV_F16>(oacc[2 * k], a0, bh0, bh1);
+                  mma_16816<PKV_F16>(oacc[2 * k], a0, bl0, bl1);
+                  const uint32_t a1[4] = {e4m3x2_to_f16x2(x23 & 0xFFFF), e4m3x2_to_f16x2(x23 >> 16),
+                                          e4m3x2_to_f16x2(y23 & 0xFFFF), e4m3x2_to_f16x2(y23 >> 16)};
+                  mma_16816<PKV_F16>(oacc[2 * k + 1], a1, bh0, bh1);
+                  mma_16816<PKV_F16>(oacc[2 * k + 1], a1, bl0, bl1);
+                }
               }
-            }
-          } else {
-            // FP8: d = base(q4) + 0..15 (D=128) or 8*q4 + 0..7 (D=64)
-            constexpr int NW = D / 32;                          // words per token: 4 or 2
-            uint32_t wa[NW], wb[NW], wc[NW], we[NW];
-            if constexpr (D == 128) {
-              const int pi = ((q4 & 1) << 1) | ((q4 >> 1) & 1) | (q4 & 4);
-              const uint4 A = ld_shared_v4(vt + chunk_off<KV, D>(tA, pi));
-              const uint4 B = ld_shared_v4(vt + chunk_off<KV, D>(tB, pi));
-              const uint4 C = ld_shared_v4(vt + chunk_off<KV, D>(tC, pi));
-              const uint4 E = ld_shared_v4(vt + chunk_off<KV, D>(tE, pi));
-              wa[0] = A.x; wa[1] = A.y; wa[2] = A.z; wa[3] = A.w;
-              wb[0] = B.x; wb[1] = B.y; wb[2] = B.z; wb[3] = B.w;
-              wc[0] = C.x; wc[1] = C.y; wc[2] = C.z; wc[3] = C.w;
-              we[0] = E.x; we[1] = E.y; we[2] = E.z; we[3] = E.w;
             } else {
-              const uint2 A = ld_shared_v2(vt + tA * G::kRowBytes + 8 * q4);
-              const uint2 B = ld_shared_v2(vt + tB * G::kRowBytes + 8 * q4);
-              const uint2 C = ld_shared_v2(vt + tC * G::kRowBytes + 8 * q4);
-              const uint2 E = ld_shared_v2(vt + tE * G::kRowBytes + 8 * q4);
-              wa[0] = A.x; wa[1] = A.y; wb[0] = B.x; wb[1] = B.y;
-              wc[0] = C.x; wc[1] = C.y; we[0] = E.x; we[1] = E.y;
-            }
-            if (partial) {
+              // INT4: P'_g = p * scale_t,g per group g; zero point through sum_t z_t,g p_t
+              constexpr int SR = G::kScaleRowBytes;
+              const uint32_t vsc = st + 2 * G::kTileBytes + G::kScaleTileBytes;
+              uint32_t sz0[D / 32], sz1[D / 32];
+              if constexpr (D == 128) {
+                const uint4 a = ld_shared_v4(vsc + q4 * SR), c = ld_shared_v4(vsc + (q4 + 8) * SR);
+                sz0[0] = a.x; sz0[1] = a.y; sz0[2] = a.z; sz0[3] = a.w;
+                sz1[0] = c.x; sz1[1] = c.y; sz1[2] = c.z; sz1[3] = c.w;
+              } else {
+                const uint2 a = ld_shared_v2(vsc + q4 * SR), c = ld_shared_v2(vsc + (q4 + 8) * SR);
+                sz0[0] = a.x; sz0[1] = a.y; sz1[0] = c.x; sz1[1] = c.y;
+              }
+              if (partial) {
+                // rows past the context may hold stale scale bits: make them 0
 #pragma unroll
-              for (int k = 0; k < NW; ++k) { wa[k] &= mA; wb[k] &= mB; wc[k] &= mC; we[k] &= mE; }
-            }
+                for (int g = 0; g < D / 32; ++g) {
+                  if (!v0) sz0[g] = 0u;
+                  if (!v1) sz1[g] = 0u;
+                }
+              }
+              using H = Half16<PKV_F16>;
 #pragma unroll
-            for (int k = 0; k < NW; ++k) {
-              const uint32_t x01 = __byte_perm(wa[k], wb[k], 0x5140), x23 = __byte_perm(wa[k], wb[k], 0x7362);
-              const uint32_t y01 = __byte_perm(wc[k], we[k], 0x5140), y23 = __byte_perm(wc[k], we[k], 0x7362);
-              const uint32_t a0[4] = {e4m3x2_to_f16x2(x01 & 0xFFFF), e4m3x2_to_f16x2(x01 >> 16),
-                                      e4m3x2_to_f16x2(y01 & 0xFFFF), e4m3x2_to_f16x2(y01 >> 16)};
-              mma_16816<PKV_F16>(oacc[2 * k], a0, bh0, bh1);
-              mma_16816<PKV_F16>(oacc[2 * k], a0, bl0, bl1);
-              const uint32_t a1[4] = {e4m3x2_to_f16x2(x23 & 0xFFFF), e4m3x2_to_f16x2(x23 >> 16),
-                                      e4m3x2_to_f16x2(y23 & 0xFFFF), e4m3x2_to_f16x2(y23 >> 16)};
-              mma_16816<PKV_F16>(oacc[2 * k + 1], a1, bh0, bh1);
-              mma_16816<PKV_F16>(oacc[2 * k + 1], a1, bl0, bl1);
+              for (int grp = 0; grp < D / 32; ++grp) {
+                const float2 f0 = H::unpack(sz0[grp]), f1 = H::unpack(sz1[grp]);
+                const float pp0 = pr[0] * f0.x, pp1 = pr[1] * f0.x;
+                const float pp2 = pr[2] * f1.x, pp3 = pr[3] * f1.x;
+                zacc[grp][0] += pr[0] * f0.y + pr[2] * f1.y;
+                zacc[grp][1] += pr[1] * f0.y + pr[3] * f1.y;
+                // one f16 rounding of P' (relative 2^-11): the output moves by at most
+                // 2^-11 * the largest group range, far below the quantization step
+                const uint32_t bh0 = movmatrix_trans(H::pack_rn(pp0, pp1));
+                const uint32_t bh1 = movmatrix_trans(H::pack_rn(pp2, pp3));
+                const uint32_t rowoff = 2 * q4;
+                const uint32_t hA = ld_shared_u16(vt + tA * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tA)) + rowoff);
+                const uint32_t hB = ld_shared_u16(vt + tB * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tB)) + rowoff);
+                const uint32_t hC = ld_shared_u16(vt + tC * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tC)) + rowoff);
+                const uint32_t hE = ld_shared_u16(vt + tE * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tE)) + rowoff);
+                const uint32_t x = hA | (hB << 16), y = hC | (hE << 16);
+                const uint32_t a0[4] = {nibbles_to_f16x2(x, 0), nibbles_to_f16x2(x, 1),
+                                        nibbles_to_f16x2(y, 0), nibbles_to_f16x2(y, 1)};
+                mma_16816<PKV_F16>(oacc[2 * grp], a0, bh0, bh1);
+                const uint32_t a1[4] = {nibbles_to_f16x2(x, 2), nibbles_to_f16x2(x, 3),
+                                        nibbles_to_f16x2(y, 2), nibbles_to_f16x2(y, 3)};
+                mma_16816<PKV_F16>(oacc[2 * grp + 1], a1, bh0, bh1);
+              }
             }
-          }
-        } else {
-          // INT4: P'_g = p * scale_t,g per group g; zero point through sum_t z_t,g p_t
-          constexpr int SR = G::kScaleRowBytes;
-          const uint32_t vsc = st + 2 * G::kTileBytes + G::kScaleTileBytes;
-          uint32_t sz0[D / 32], sz1[D / 32];
-          if constexpr (D == 128) {
-            const uint4 a = ld_shared_v4(vsc + q4 * SR), c = ld_shared_v4(vsc + (q4 + 8) * SR);
-            sz0[0] = a.x; sz0[1] = a.y; sz0[2] = a.z; sz0[3] = a.w;
-            sz1[0] = c.x; sz1[1] = c.y; sz1[2] = c.z; sz1[3] = c.w;
-          } else {
-            const uint2 a = ld_shared_v2(vsc + q4 * SR), c = ld_shared_v2(vsc + (q4 + 8) * SR);
-            sz0[0] = a.x; sz0[1] = a.y; sz1[0] = c.x; sz1[1] = c.y;
-          }
-          if (partial) {
-            // rows past the context may hold stale scale bits: make them 0
-#pragma unroll
-            for (int g = 0; g < D / 32; ++g) {
-              if (!v0) sz0[g] = 0u;
-              if (!v1) sz1[g] = 0u;
-            }
-          }
-          using H = Half16<PKV_F16>;
-#pragma unroll
-          for (int grp = 0; grp < D / 32; ++grp) {
-            const float2 f0 = H::unpack(sz0[grp]), f1 = H::unpack(sz1[grp]);
-            const float pp0 = pr[0] * f0.x, pp1 = pr[1] * f0.x;
-            const float pp2 = pr[2] * f1.x, pp3 = pr[3] * f1.x;
-            zacc[grp][0] += pr[0] * f0.y + pr[2] * f1.y;
-            zacc[grp][1] += pr[1] * f0.y + pr[3] * f1.y;
-            // one f16 rounding of P' (relative 2^-11): the output moves by at most
-            // 2^-11 * the largest group range, far below the quantization step
-            const uint32_t bh0 = movmatrix_trans(H::pack_rn(pp0, pp1));
-            const uint32_t bh1 = movmatrix_trans(H::pack_rn(pp2, pp3));
-            const uint32_t rowoff = 2 * q4;
-            const uint32_t hA = ld_shared_u16(vt + tA * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tA)) + rowoff);
-            const uint32_t hB = ld_shared_u16(vt + tB * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tB)) + rowoff);
-            const uint32_t hC = ld_shared_u16(vt + tC * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tC)) + rowoff);
-            const uint32_t hE = ld_shared_u16(vt + tE * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tE)) + rowoff);
-            const uint32_t x = hA | (hB << 16), y = hC | (hE << 16);
-            const uint32_t a0[4] = {nibbles_to_f16x2(x, 0), nibbles_to_f16x2(x, 1),
-                                    nibbles_to_f16x2(y, 0), nibbles_to_f16x2(y, 1)};
-            mma_16816<PKV_F16>(oacc[2 * grp], a0, bh0, bh1);
-            const uint32_t a1[4] = {nibbles_to_f16x2(x, 2), nibbles_to_f16x2(x, 3),
-                                    nibbles_to_f16x2(y, 2), nibbles_to_f16x2(y, 3)};
-            mma_16816<PKV_F16>(oacc[2 * grp + 1], a1, bh0, bh1);
-          }
+            }  // v_on
         }
-        }  // v_on
       }
 
       __syncwarp();
@@ -795,18 +886,20 @@ paged_decode_kernel(const Params p) {
       mb[4 * MT + 2] = lrow[0]; mb[4 * MT + 3] = lrow[1];
     };
     auto take = [&]() { merge_state<MT>(mrow, lrow, oacc, mb + 4 * MT, mb + 4 * MT + 2, mb); };
-    if (warp == 1) put();
-    __syncthreads();
-    if (warp == 0) take();
-    __syncthreads();
-    if (warp == 3) put();
-    __syncthreads();
-    if (warp == 2) take();
-    __syncthreads();
-    if (warp == 2) put();
-    __syncthreads();
-    if (warp == 0) {
-      take();
+    if constexpr (!WU) {
+      if (warp == 1) put();
+      __syncthreads();
+      if (warp == 0) take();
+      __syncthreads();
+      if (warp == 3) put();
+      __syncthreads();
+      if (warp == 2) take();
+      __syncthreads();
+      if (warp == 2) put();
+      __syncthreads();
+      if (warp == 0) take();
+    }
+    if (WU || warp == 0) {
       const int64_t head0 = static_cast<int64_t>(unit.b) * p.num_q_heads + unit.kvh * group;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -839,7 +932,7 @@ paged_decode_kernel(const Params p) {
         }
       }
     }
-    __syncthreads();                         // the buffer is free for the next unit
+    if constexpr (!WU) __syncthreads();      // the buffer is free for the next unit
   }
   cp_async_wait<0>();
 }
@@ -877,8 +970,8 @@ pkv_lse_reduce(const Params p) {
   }
 }
 
-template <int KV, int QT, int D>
-cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t st) {
+template <int KV, int QT, int D, bool WU>
+cudaError_t launch_mode(const DecodeArgs& a, cudaStream_t st) {
   using G = Geo<KV, D>;
   Params p;
   p.q = static_cast<const uint16_t*>(a.q);
@@ -900,7 +993,7 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t st) {
   p.partition_size = a.partition_size;
   p.num_partitions = a.num_partitions;
   p.softmax_scale = a.softmax_scale;
-  auto kern = paged_decode_kernel<KV, QT, D>;
+  auto kern = paged_decode_kernel<KV, QT, D, WU>;
   // per device, once: the shared-memory opt-in and the resident CTAs per SM
   static std::atomic<int> slots_per_dev[kMaxDevices];     // SMs x resident CTAs (0: unknown)
   p.parts_per_cta = 1;
@@ -921,24 +1014,53 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t st) {
     slots = max(1, occ) * max(1, sms);
     slots_per_dev[dev].store(slots, std::memory_order_relaxed);
   }
-  // partitions per CTA: runs of up to PKV_RUN_TOKENS tokens, as long as the
-  // grid keeps at least four waves of CTAs
+  // partitions per CTA (per warp with WU): runs of up to PKV_RUN_TOKENS tokens
+  // per warp stream, as long as the grid keeps at least four waves of CTAs
+  const int heads_per_cta = WU ? kDecodeWarps : 1;
+  const int64_t head_groups = (a.num_kv_heads + heads_per_cta - 1) / heads_per_cta;
   int ppc = PKV_PPC;
   if (ppc <= 0) {
     ppc = 1;
-    const int64_t pairs = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
-    while (ppc * 2 * a.partition_size <= PKV_RUN_TOKENS && ppc * 2 <= a.num_partitions &&
-           ((a.num_partitions + ppc * 2 - 1) / (ppc * 2)) * pairs >= 4 * static_cast<int64_t>(slots))
+    const int64_t groups = static_cast<int64_t>(a.num_seqs) * head_groups;
+    const int run = WU ? PKV_RUN_TOKENS_WU : PKV_RUN_TOKENS;
+    while (ppc * 2 * a.partition_size <= run && ppc * 2 <= a.num_partitions &&
+           ((a.num_partitions + ppc * 2 - 1) / (ppc * 2)) * groups >= 4 * static_cast<int64_t>(slots))
       ppc *= 2;
   }
   ppc = std::max(1, std::min(ppc, a.num_partitions));
   p.parts_per_cta = ppc;
-  dim3 grid((a.num_partitions + ppc - 1) / ppc, a.num_kv_heads, a.num_seqs);
+  dim3 grid((a.num_partitions + ppc - 1) / ppc, static_cast<unsigned>(head_groups), a.num_seqs);
   kern<<<grid, kDecodeWarps * kWarp, G::kSmemBytes, st>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.num_partitions == 1) return e;
   pkv_lse_reduce<QT, D><<<a.num_seqs * a.num_q_heads, D, 0, st>>>(p);
   return cudaGetLastError();
+}
+
+// Warp-owned units when the split-KV work has enough (partition, sequence, KV
+// head) units for several waves of warps (PKV_WU_WAVES x SMs x 16 warps);
+// shared partitions otherwise.
+template <int KV, int QT, int D>
+cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t st) {
+  static std::atomic<int> sms_per_dev[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int sms = sms_per_dev[dev].load(std::memory_order_relaxed);
+  if (sms == 0) {
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    sms_per_dev[dev].store(sms, std::memory_order_relaxed);
+  }
+  const int64_t units = static_cast<int64_t>(a.num_partitions) * a.num_seqs * a.num_kv_heads;
+  bool wu = a.num_partitions > 1 && units >= static_cast<int64_t>(PKV_WU_WAVES) * sms * 16;
+  // PKV_DECODE_MODE=shared|warp overrides the choice (both give the same results)
+  if (const char* m = getenv("PKV_DECODE_MODE")) {
+    if (!strcmp(m, "shared")) wu = false;
+    if (!strcmp(m, "warp")) wu = true;
+  }
+  return wu ? launch_mode<KV, QT, D, true>(a, st) : launch_mode<KV, QT, D, false>(a, st);
 }
 
 template <int KV, int QT>

@@ -16,6 +16,13 @@ from tests import helpers as H
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=["shared", "warp"])
+def mode(request, monkeypatch):
+    """Run a test under both work splits of the decode kernel."""
+    monkeypatch.setenv("PKV_DECODE_MODE", request.param)
+    return request.param
+
+
 def _run(w, partition_size=0, identity=False, max_blocks_per_seq=None):
     case = W.make_case(w, identity_tables=identity, max_blocks_per_seq=max_blocks_per_seq)
     k, v, s = oracle.prefill_case(case)
@@ -30,7 +37,7 @@ def _run(w, partition_size=0, identity=False, max_blocks_per_seq=None):
 
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
 @pytest.mark.parametrize("partition_size", [0, 32, 64])
-def test_configs_small(cfg, partition_size):
+def test_configs_small(cfg, partition_size, mode):
     w = W.CONFIGS[cfg].scaled(batch=5, ctx_cap=300, seed=700 + cfg)
     case, g, out, ref, _ = _run(w, partition_size)
     H.check_close(out, ref, w.kv_dtype, w.q_dtype, f"config {cfg} P={partition_size}")
@@ -45,7 +52,7 @@ def test_config1_exact_shape():
 @pytest.mark.parametrize("kv", [W.F16, W.BF16, W.FP8_E4M3, W.INT4_G32])
 @pytest.mark.parametrize("head_dim", [64, 128])
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 2), (16, 2), (4, 1)])
-def test_heads_dims_dtypes(kv, head_dim, hq, hkv):
+def test_heads_dims_dtypes(kv, head_dim, hq, hkv, mode):
     qd = W.F16 if kv == W.F16 else W.BF16
     w = W.Workload("grid", 3, hq, hkv, head_dim, 16, kv, qd, "uniform", 1, 200, seed=hq * 7 + hkv + head_dim + kv)
     case, g, out, ref, _ = _run(w, partition_size=64)
@@ -54,14 +61,14 @@ def test_heads_dims_dtypes(kv, head_dim, hq, hkv):
 
 @pytest.mark.parametrize("kv", [W.BF16, W.FP8_E4M3, W.INT4_G32])
 @pytest.mark.parametrize("block_size", [16, 32, 64, 128])
-def test_block_sizes(kv, block_size):
+def test_block_sizes(kv, block_size, mode):
     w = W.Workload("bs", 4, 8, 2, 128, block_size, kv, W.BF16, "uniform", 1, 400, seed=block_size + kv)
     case, g, out, ref, _ = _run(w, partition_size=96)
     H.check_close(out, ref, kv, W.BF16, f"bs {block_size}")
 
 
 @pytest.mark.parametrize("kv", [W.F16, W.FP8_E4M3, W.INT4_G32])
-def test_context_length_edges(kv):
+def test_context_length_edges(kv, mode):
     """ctx in {0, 1, 15, 16, 17, P-1, P, P+1, 2P+1} with P = 64."""
     qd = W.F16 if kv == W.F16 else W.BF16
     lens = [0, 1, 15, 16, 17, 63, 64, 65, 129]
@@ -82,7 +89,7 @@ def test_context_length_edges(kv):
 
 
 @pytest.mark.parametrize("cfg", [1, 3, 4])
-def test_block_permutation_is_bit_exact(cfg):
+def test_block_permutation_is_bit_exact(cfg, mode):
     w = W.CONFIGS[cfg].scaled(batch=4, ctx_cap=250, seed=900 + cfg)
     case, g, out, ref, (k, v, s) = _run(w, partition_size=64)
     rng = np.random.default_rng(3)
@@ -109,7 +116,7 @@ def test_identity_tables_match_shuffled():
 
 
 @pytest.mark.parametrize("kv", [W.BF16, W.FP8_E4M3, W.INT4_G32])
-def test_split_matches_unsplit(kv):
+def test_split_matches_unsplit(kv, mode):
     w = W.Workload("split", 3, 16, 2, 128, 16, kv, W.BF16, "fixed", 1000, 1000, seed=kv + 101)
     _, _, out_1, ref, _ = _run(w, partition_size=1008)
     _, _, out_n, _, _ = _run(w, partition_size=48)
@@ -135,7 +142,7 @@ def test_constant_keys_give_mean_of_values():
 
 
 @pytest.mark.parametrize("kv", [W.FP8_E4M3, W.INT4_G32, W.BF16])
-def test_unwritten_last_token_matches_oracle(kv):
+def test_unwritten_last_token_matches_oracle(kv, mode):
     """Attend over a context whose last token was never written (zeroed pool):
     an FP8 block with scale 0 and INT4 rows with scale 0 dequantize to 0, so the
     output stays finite and equal to the oracle's."""
@@ -149,7 +156,7 @@ def test_unwritten_last_token_matches_oracle(kv):
     H.check_close(out, ref, kv, W.BF16, "unwritten last token")
 
 
-def test_bad_block_id_is_flagged_and_skipped():
+def test_bad_block_id_is_flagged_and_skipped(mode):
     import paged_quantized_kv_write_gb300 as pkv
     w = W.Workload("badid", 3, 8, 2, 64, 16, W.BF16, W.BF16, "fixed", 40, 40, seed=4)
     case = W.make_case(w)
