@@ -251,7 +251,7 @@ def run_ours(args, rank: int, world: int):
 
     peak, peak_kind = _peaks()
     ms_per_step = dev_ms / args.steps
-    gbs = world * total_bytes * args.steps / (dev_ms * 1e-3) / 1e9
+    gbs = whole_job_rate(total_bytes, args.steps, dev_ms, world) / 1e9
     attn_avg_ms = statistics.mean(attn_ms)
     achieved = attn_bytes / (attn_avg_ms * 1e-3) / 1e9
     result = {
@@ -279,12 +279,12 @@ def run_ours(args, rank: int, world: int):
             "parallelism": f"replicas x{world}",
             "block_tables": "identity (contiguous)" if args.identity else "shuffled",
         },
-        "seq_steps_per_s": round(world * w.batch * args.steps / (dev_ms * 1e-3), 1),
+        "seq_steps_per_s": round(whole_job_rate(w.batch, args.steps, dev_ms, world), 1),
         "pct_hbm_peak": round(100.0 * gbs / world / peak, 2),
         "bytes_per_step": total_bytes,
         "logical_bytes_per_step": logical_bytes,
         "e2e": {
-            "value": round(world * total_bytes * args.steps / (e2e_ms * 1e-3) / 1e9, 2),
+            "value": round(whole_job_rate(total_bytes, args.steps, e2e_ms, world) / 1e9, 2),
             "unit": "GB/s",
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
@@ -379,7 +379,7 @@ def run_reference(args, rank: int, world: int):
     t0 = time.perf_counter()
     oracle.step_case(probe, pk, pv, ps)
     per_seq = (time.perf_counter() - t0) / probe.w.batch
-    budget = 120.0 / max(1, args.steps + args.warmup)        # whole run within ~2 minutes
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)   # the whole run's CPU time
     n = int(max(1, min(w.batch, budget / max(per_seq, 1e-6))))
     case = W.make_case(w.scaled(batch=n))
     k, v, s = oracle.prefill_case(case)
@@ -427,13 +427,21 @@ def _barrier(world):
 
 
 def _max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's time: replicas run in lockstep between barriers."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, steps: int, max_ms: float, world: int) -> float:
+    """Units per second over all replicas: every rank processes units_per_rank per
+    step; the job takes as long as its slowest rank."""
+    return world * units_per_rank * steps / (max_ms * 1e-3)
 
 
 def main():
@@ -446,6 +454,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--identity", action="store_true",
                     help="lay every sequence out in consecutive blocks (paging-overhead comparator)")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="reference arm: CPU seconds the whole run may take (sizes its sample)")
     ap.add_argument("--partition", type=int, default=0,
                     help="override the workload's split-KV partition size (0: keep)")
     args = ap.parse_args()
