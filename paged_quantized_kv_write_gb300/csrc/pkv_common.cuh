@@ -86,6 +86,18 @@ __device__ __forceinline__ uint32_t nibbles_offset_f16x2(uint32_t w, int k) {
   return ((w >> (4 * k)) & 0x000F000Fu) | 0x64006400u;
 }
 
+// Shift-free variants on the nibbles at bits 0-3 / 16-19 (`lo`) and 4-7 /
+// 20-23 (`hi`) of w: f16x2 1024 + n and 1024 + 16 n, exact.  The factor 16 of
+// the `hi` form is undone by the caller (a power of two, so exactly).
+__device__ __forceinline__ uint32_t nib_lo_offset(uint32_t w) { return (w & 0x000F000Fu) | 0x64006400u; }
+__device__ __forceinline__ uint32_t nib_hi_offset(uint32_t w) { return (w & 0x00F000F0u) | 0x64006400u; }
+// f16x2 x - 1024 (exact for the values above)
+__device__ __forceinline__ uint32_t sub1024(uint32_t x) {
+  __half2 h = *reinterpret_cast<__half2*>(&x);
+  h = __hsub2(h, __half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
 // ------------------------------------------------------------------ tensor cores
 // D = A(16x16, row) * B(16x8, col) + D, fp32 accumulate (mma.sync m16n8k16).
 template <int DT>

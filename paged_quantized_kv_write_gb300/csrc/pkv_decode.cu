@@ -318,14 +318,17 @@ __device__ __forceinline__ void load_q(const Params& p, const Unit& u, int q4, i
           qb[4 * i + h][1] = Half16<PKV_F16>::pack_rn(qf[16 * i + 4 * h + 2] * qs, qf[16 * i + 4 * h + 3] * qs);
         }
     } else {
-      // k-step 2grp+h: lo pair = d (8c4 + 2h, 8c4 + 2h + 4), hi pair = (8c4 + 2h + 1, 8c4 + 2h + 5)
+      // k-step 2grp+h: lo pair = d (8c4 + 2h, 8c4 + 2h + 4), hi pair = (8c4 + 2h + 1, 8c4 + 2h + 5).
+      // The hi pairs meet K codes taken as 1024 + 16 n (high nibbles, no shift),
+      // so their q enters divided by 16.
 #pragma unroll
       for (int grp = 0; grp < D / 32; ++grp) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const float* x = qf + 8 * grp;
           qb[2 * grp + h][0] = Half16<PKV_F16>::pack_rn(x[2 * h] * qs, x[2 * h + 4] * qs);
-          qb[2 * grp + h][1] = Half16<PKV_F16>::pack_rn(x[2 * h + 1] * qs, x[2 * h + 5] * qs);
+          qb[2 * grp + h][1] =
+              Half16<PKV_F16>::pack_rn(x[2 * h + 1] * (qs * 0.0625f), x[2 * h + 5] * (qs * 0.0625f));
         }
         float s = 0.f, s16 = 0.f;
 #pragma unroll
@@ -593,12 +596,15 @@ paged_decode_kernel(const Params p) {
                 const uint32_t w1 = ld_shared_b32(st + (q4 + 8) * G::kRowBytes +
                                                   16 * (grp ^ swz<KV, D>(q4 + 8)) + 4 * c4);
                 float g4[4] = {0.f, 0.f, 0.f, 0.f};
-                // codes enter as f16 1024 + n; 1024 * sum(q) is taken off the group sum
-                const uint32_t a0[4] = {nibbles_offset_f16x2(w0, 0), nibbles_offset_f16x2(w1, 0),
-                                        nibbles_offset_f16x2(w0, 1), nibbles_offset_f16x2(w1, 1)};
+                // codes enter as f16 1024 + n (low nibbles) or 1024 + 16 n (high
+                // nibbles, met by q / 16); 1024 * sum(q as the mma sees it) is taken
+                // off the group sum
+                const uint32_t w0s = w0 >> 8, w1s = w1 >> 8;
+                const uint32_t a0[4] = {nib_lo_offset(w0), nib_lo_offset(w1),
+                                        nib_hi_offset(w0), nib_hi_offset(w1)};
                 mma_16816<PKV_F16>(g4, a0, qb[2 * grp][0], qb[2 * grp][1]);
-                const uint32_t a1[4] = {nibbles_offset_f16x2(w0, 2), nibbles_offset_f16x2(w1, 2),
-                                        nibbles_offset_f16x2(w0, 3), nibbles_offset_f16x2(w1, 3)};
+                const uint32_t a1[4] = {nib_lo_offset(w0s), nib_lo_offset(w1s),
+                                        nib_hi_offset(w0s), nib_hi_offset(w1s)};
                 mma_16816<PKV_F16>(g4, a1, qb[2 * grp + 1][0], qb[2 * grp + 1][1]);
                 const float2 f0 = Half16<PKV_F16>::unpack(sz0[grp]);   // (scale, zero) token q4
                 const float2 f1 = Half16<PKV_F16>::unpack(sz1[grp]);   // token q4 + 8
@@ -829,12 +835,15 @@ paged_decode_kernel(const Params p) {
                 const uint32_t hB = ld_shared_u16(vt + tB * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tB)) + rowoff);
                 const uint32_t hC = ld_shared_u16(vt + tC * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tC)) + rowoff);
                 const uint32_t hE = ld_shared_u16(vt + tE * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tE)) + rowoff);
-                const uint32_t x = hA | (hB << 16), y = hC | (hE << 16);
-                const uint32_t a0[4] = {nibbles_to_f16x2(x, 0), nibbles_to_f16x2(x, 1),
-                                        nibbles_to_f16x2(y, 0), nibbles_to_f16x2(y, 1)};
+                // token pairs (tA, tB), (tC, tE) side by side; rows q4 + 8 (odd d)
+                // take the high nibbles as 16 n, undone once in the epilogue
+                const uint32_t x = __byte_perm(hA, hB, 0x5410), y = __byte_perm(hC, hE, 0x5410);
+                const uint32_t xs = x >> 8, ys = y >> 8;
+                const uint32_t a0[4] = {sub1024(nib_lo_offset(x)), sub1024(nib_hi_offset(x)),
+                                        sub1024(nib_lo_offset(y)), sub1024(nib_hi_offset(y))};
                 mma_16816<PKV_F16>(oacc[2 * grp], a0, bh0, bh1);
-                const uint32_t a1[4] = {nibbles_to_f16x2(x, 2), nibbles_to_f16x2(x, 3),
-                                        nibbles_to_f16x2(y, 2), nibbles_to_f16x2(y, 3)};
+                const uint32_t a1[4] = {sub1024(nib_lo_offset(xs)), sub1024(nib_hi_offset(xs)),
+                                        sub1024(nib_lo_offset(ys)), sub1024(nib_hi_offset(ys))};
                 mma_16816<PKV_F16>(oacc[2 * grp + 1], a1, bh0, bh1);
               }
             }
@@ -860,6 +869,9 @@ paged_decode_kernel(const Params p) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) oacc[i][k] *= post;
     if constexpr (KV == PKV_INT4_G32) {
+      // rows q4 + 8 (odd d) carried their V codes as 16 n
+#pragma unroll
+      for (int i = 0; i < MT; ++i) { oacc[i][2] *= 0.0625f; oacc[i][3] *= 0.0625f; }
 #pragma unroll
       for (int g = 0; g < D / 32; ++g) {
 #pragma unroll
