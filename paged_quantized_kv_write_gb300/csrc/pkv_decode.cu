@@ -404,6 +404,7 @@ paged_decode_kernel(const Params p) {
   constexpr int kQN = kHalf ? 1 : D / 32;
 
   extern __shared__ __align__(128) uint8_t smem[];
+  pdl_wait();                 // the cache may have been written by the previous kernel
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int q4 = lane >> 2, c4 = lane & 3;   // mma groupID / thread-in-group
   const int group = p.num_q_heads / p.num_kv_heads;
@@ -946,6 +947,7 @@ paged_decode_kernel(const Params p) {
     }
     if constexpr (!WU) __syncthreads();      // the buffer is free for the next unit
   }
+  pdl_launch_dependents();
   cp_async_wait<0>();
 }
 
@@ -954,6 +956,7 @@ paged_decode_kernel(const Params p) {
 template <int QT, int D>
 __global__ void __launch_bounds__(D)
 pkv_lse_reduce(const Params p) {
+  pdl_wait();                                      // the partials of the decode kernel
   const int64_t head = blockIdx.x;                 // b * Hq + h
   const int b = static_cast<int>(head / p.num_q_heads);
   const int d = threadIdx.x;
@@ -1042,11 +1045,9 @@ cudaError_t launch_mode(const DecodeArgs& a, cudaStream_t st) {
   ppc = std::max(1, std::min(ppc, a.num_partitions));
   p.parts_per_cta = ppc;
   dim3 grid((a.num_partitions + ppc - 1) / ppc, static_cast<unsigned>(head_groups), a.num_seqs);
-  kern<<<grid, kDecodeWarps * kWarp, G::kSmemBytes, st>>>(p);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, grid, dim3(kDecodeWarps * kWarp), G::kSmemBytes, st, p);
   if (e != cudaSuccess || a.num_partitions == 1) return e;
-  pkv_lse_reduce<QT, D><<<a.num_seqs * a.num_q_heads, D, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(pkv_lse_reduce<QT, D>, dim3(a.num_seqs * a.num_q_heads), dim3(D), 0, st, p);
 }
 
 // Warp-owned units when the split-KV work has enough (partition, sequence, KV

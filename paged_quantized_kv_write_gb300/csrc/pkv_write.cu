@@ -31,6 +31,8 @@ kv_write_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict__
                 void* __restrict__ scales, int num_blocks, int num_kv_heads, int block_size,
                 int* __restrict__ dev_status) {
   constexpr int EPL = D / kWarp;                       // elements per lane: 2 or 4
+  pdl_wait();                 // inputs and cache may come from the previous kernel
+  pdl_launch_dependents();
   const int lane = threadIdx.x & (kWarp - 1);
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kWriteWarps + (threadIdx.x >> 5);
   if (row >= num_tokens * num_kv_heads) return;
@@ -144,12 +146,11 @@ template <int KV, int NEW, int D, int PHASE>
 cudaError_t launch_one(const WriteArgs& a, cudaStream_t st) {
   const int64_t rows = a.num_tokens * a.num_kv_heads;
   const int64_t grid = (rows + kWriteWarps - 1) / kWriteWarps;
-  kv_write_kernel<KV, NEW, D, PHASE><<<static_cast<unsigned>(grid), kWriteWarps * kWarp, 0, st>>>(
-      static_cast<const uint16_t*>(a.k_new), static_cast<const uint16_t*>(a.v_new),
-      a.slot_mapping, a.num_tokens, static_cast<uint8_t*>(a.k_cache),
-      static_cast<uint8_t*>(a.v_cache), a.scales, a.num_blocks, a.num_kv_heads, a.block_size,
-      a.dev_status);
-  return cudaGetLastError();
+  return launch_pdl(kv_write_kernel<KV, NEW, D, PHASE>, dim3(static_cast<unsigned>(grid)),
+                    dim3(kWriteWarps * kWarp), 0, st, static_cast<const uint16_t*>(a.k_new),
+                    static_cast<const uint16_t*>(a.v_new), a.slot_mapping, a.num_tokens,
+                    static_cast<uint8_t*>(a.k_cache), static_cast<uint8_t*>(a.v_cache), a.scales,
+                    a.num_blocks, a.num_kv_heads, a.block_size, a.dev_status);
 }
 
 template <int KV, int NEW, int D>
