@@ -108,8 +108,17 @@ def _bits_to_tensor(bits, code):
     return t.view(torch.float16 if code == W.F16 else torch.bfloat16).cuda()
 
 
+def _with_kv_dtype(w: W.Workload, name: str) -> W.Workload:
+    """The workload with another cache dtype (16-bit caches take the query dtype)."""
+    code = {v: k for k, v in W.DTYPE_NAMES.items()}[name]
+    upd = dict(kv_dtype=code, name=f"{w.name}, {name} cache")
+    if code in (W.F16, W.BF16):
+        upd["q_dtype"] = code
+    return dataclasses.replace(w, **upd)
+
+
 def _kernel_launches_per_step(w: W.Workload, nparts: int) -> int:
-    write = 2 if w.kv_dtype == W.FP8_E4M3 else 1
+    write = 2 if w.kv_dtype in W.FP8_TYPES else 1
     return write + 1 + (1 if nparts > 1 else 0)
 
 
@@ -122,6 +131,12 @@ def run_ours(args, rank: int, world: int):
     w = W.CONFIGS[args.config]
     if args.partition:
         w = dataclasses.replace(w, partition_size=args.partition)
+    if args.block_size:
+        w = dataclasses.replace(w, block_size=args.block_size,
+                                shared_prefix_tokens=(w.shared_prefix_tokens // args.block_size)
+                                * args.block_size)
+    if args.kv_dtype:
+        w = _with_kv_dtype(w, args.kv_dtype)
     case = W.make_case(w, identity_tables=args.identity)
     stream = torch.cuda.Stream(dev)
     with torch.cuda.stream(stream):
@@ -266,7 +281,7 @@ def run_ours(args, rank: int, world: int):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": {W.F16: "f16", W.BF16: "bf16", W.FP8_E4M3: "fp8_e4m3+bf16",
-                  W.INT4_G32: "int4_g32+bf16"}[w.kv_dtype],
+                  W.FP8_E5M2: "fp8_e5m2+bf16", W.INT4_G32: "int4_g32+bf16"}[w.kv_dtype],
         "data": "synthetic (seeded N(0,1) q/K/V, shuffled block tables; no model weights)",
         "config": {
             "workload": f"config {args.config}: {w.name}",
@@ -278,6 +293,8 @@ def run_ours(args, rank: int, world: int):
             "l2": "inputs larger than L2 (no flush)" if not small else "L2 flushed (256 MB write) between steps",
             "parallelism": f"replicas x{world}",
             "block_tables": "identity (contiguous)" if args.identity else "shuffled",
+            "block_size_override": bool(args.block_size),
+            "kv_dtype_override": bool(args.kv_dtype),
         },
         "seq_steps_per_s": round(whole_job_rate(w.batch, args.steps, dev_ms, world), 1),
         "pct_hbm_peak": round(100.0 * gbs / world / peak, 2),
@@ -298,7 +315,8 @@ def run_ours(args, rank: int, world: int):
             "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6.8 TB/s",
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": _traffic(args.config),
+            "traffic": None if (args.kv_dtype or args.block_size or args.partition)
+                       else _traffic(args.config),
             "avg_launch_us": round(attn_avg_ms * 1e3, 3),
             "write_avg_us": round(write_avg_ms * 1e3, 3),
             "algorithmic_bytes": attn_bytes,
@@ -456,6 +474,10 @@ def main():
                     help="lay every sequence out in consecutive blocks (paging-overhead comparator)")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="reference arm: CPU seconds the whole run may take (sizes its sample)")
+    ap.add_argument("--block-size", type=int, default=0,
+                    help="override the workload's block size (block-size sweep; 0: keep)")
+    ap.add_argument("--kv-dtype", default="", choices=[""] + sorted(W.DTYPE_NAMES.values()),
+                    help="override the workload's cache dtype (dtype comparison; empty: keep)")
     ap.add_argument("--partition", type=int, default=0,
                     help="override the workload's split-KV partition size (0: keep)")
     args = ap.parse_args()

@@ -31,8 +31,8 @@
  *      bytes (FP8), or head_dim/2 bytes of 4-bit codes (INT4: element 2i in
  *      the low nibble of byte i, 2i+1 in the high nibble).
  *  - `scales` layout (index 0 of the leading 2 is K, 1 is V):
- *      FP8:  float [2][num_blocks][num_kv_heads] — one scale per block and
- *            KV head;
+ *      FP8 (E4M3, E5M2):  float [2][num_blocks][num_kv_heads] — one scale per
+ *            block and KV head;
  *      INT4: half  [2][num_blocks][num_kv_heads][block_size][head_dim/32][2]
  *            — (scale, zero) per token, head and group of 32 elements;
  *      F16/BF16: unused (may be NULL).
@@ -51,7 +51,8 @@ typedef enum {
     PKV_F16 = 0,       /* IEEE half */
     PKV_BF16 = 1,      /* bfloat16 */
     PKV_FP8_E4M3 = 2,  /* OCP E4M3 ("e4m3fn"), per-(block, kv-head) fp32 scale */
-    PKV_INT4_G32 = 3   /* asymmetric 4-bit, groups of 32 along head_dim, fp16 scale+zero */
+    PKV_INT4_G32 = 3,  /* asymmetric 4-bit, groups of 32 along head_dim, fp16 scale+zero */
+    PKV_FP8_E5M2 = 4   /* OCP E5M2, per-(block, kv-head) fp32 scale */
 } pkv_dtype;
 
 typedef enum {
@@ -78,6 +79,8 @@ typedef enum {
  *                offset reuses the stored scales.  code = E4M3 round-to-nearest-
  *                even with saturation to +-448 of the fp32 quotient x / scale.
  *                Within one call the offset-0 tokens are applied first.
+ *                FP8_E5M2: the same with 57344 (the largest finite E5M2) in
+ *                place of 448, codes rounded to nearest even and saturated.
  *                INT4_G32: per token, head and 32-element group,
  *                scale = fp16(fp32(max - min) / 15), zero = fp16(min),
  *                code = clamp(rint((x - zero) / scale), 0, 15) in fp32 (0 when

@@ -40,6 +40,10 @@ def lib() -> ctypes.CDLL:
         L.oracle_e4m3_to_double.restype = D
         L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
         L.oracle_e4m3_encode.restype = ctypes.c_uint8
+        L.oracle_e5m2_to_double.argtypes = [ctypes.c_uint8]
+        L.oracle_e5m2_to_double.restype = D
+        L.oracle_e5m2_encode.argtypes = [ctypes.c_float]
+        L.oracle_e5m2_encode.restype = ctypes.c_uint8
         L.oracle_kv_cache_bytes.argtypes = [D] * 6
         L.oracle_kv_cache_bytes.restype = D
         L.oracle_num_pages.argtypes = [I64, I64]
@@ -90,6 +94,14 @@ def e4m3_encode(y: float) -> int:
     return lib().oracle_e4m3_encode(float(np.float32(y)))
 
 
+def e5m2_to_double(code: int) -> float:
+    return lib().oracle_e5m2_to_double(int(code))
+
+
+def e5m2_encode(y: float) -> int:
+    return lib().oracle_e5m2_encode(float(np.float32(y)))
+
+
 # ---------------------------------------------------------------- formulas
 def kv_cache_bytes(layers, heads, head_dim, seq_len, batch, bytes_per_elem) -> float:
     return lib().oracle_kv_cache_bytes(layers, heads, head_dim, seq_len, batch, bytes_per_elem)
@@ -116,7 +128,7 @@ def alloc_cache(kv_dtype: int, num_blocks: int, num_kv_heads: int, head_dim: int
     if kv_dtype in (0, 1):
         k = np.zeros((num_blocks, num_kv_heads, block_size, head_dim), np.uint16)
         return k, k.copy(), None
-    if kv_dtype == 2:
+    if kv_dtype in (2, 4):
         k = np.zeros((num_blocks, num_kv_heads, block_size, head_dim), np.uint8)
         return k, k.copy(), np.zeros((2, num_blocks, num_kv_heads), np.float32)
     if kv_dtype == 3:

@@ -39,6 +39,9 @@
  *      code = clamp(rint((x - zero) / scale), 0, 15) in fp32 (0 if scale is
  *      0); element 2i in the low nibble of byte i, 2i+1 in the high nibble.
  *  R7  context_len == 0 gives out = 0; slot -1 means "skip this token".
+ *  R8  FP8 E5M2 (1 sign, 5 exponent, 2 mantissa bits; the pages name E4M3
+ *      only): the same block-wise recipe as R4/R5 with 57344, E5M2's
+ *      largest finite value, in place of 448.
  *
  * Build with -ffp-contract=off: the encoders must round each fp32 step.
  */
@@ -51,7 +54,9 @@
 #include <omp.h>
 #endif
 
-enum { DT_F16 = 0, DT_BF16 = 1, DT_FP8 = 2, DT_INT4 = 3 };
+enum { DT_F16 = 0, DT_BF16 = 1, DT_FP8 = 2, DT_INT4 = 3, DT_E5M2 = 4 };
+
+static int is_fp8(int kv_dtype) { return kv_dtype == DT_FP8 || kv_dtype == DT_E5M2; }
 
 /* ------------------------------------------------------------ codecs */
 
@@ -148,6 +153,44 @@ uint8_t oracle_e4m3_encode(float yf) {
     return sign | (uint8_t)code;
 }
 
+/* OCP FP8 E5M2: 1 sign, 5 exponent (bias 15), 2 mantissa bits, IEEE-like:
+ * S.11111.00 is infinity, S.11111.xx (xx != 0) NaN; largest finite
+ * 1.75 * 2^15 = 57344 = 0x7B; subnormals m/4 * 2^-14. */
+double oracle_e5m2_to_double(uint8_t code) {
+    int sign = (code >> 7) & 1;
+    int e = (code >> 2) & 0x1F;
+    int m = code & 0x3;
+    double mag;
+    if (e == 31)
+        mag = m ? NAN : INFINITY;
+    else if (e == 0)
+        mag = ldexp((double)m, -16);
+    else
+        mag = ldexp(1.0 + m / 4.0, e - 15);
+    return sign ? -mag : mag;
+}
+
+/* E5M2, round to nearest even, saturating to +-57344 (R8); sign kept as in
+ * the E4M3 encoder; NaN gives 0x7F. */
+uint8_t oracle_e5m2_encode(float yf) {
+    double y = (double)yf;
+    if (isnan(y)) return 0x7F;
+    uint8_t sign = signbit(y) ? 0x80 : 0;
+    double a = fabs(y);
+    if (a >= 57344.0) return sign | 0x7B;
+    if (a < ldexp(1.0, -14)) {
+        double m = rint(a * ldexp(1.0, 16));         /* subnormal grid 2^-16; 4 = min normal */
+        return sign | (uint8_t)m;
+    }
+    int ex;
+    frexp(a, &ex);
+    int e = ex - 1;
+    double m = rint((a / ldexp(1.0, e) - 1.0) * 4.0);       /* 0..4 */
+    int code = ((e + 15) << 2) + (int)m;
+    if (code > 0x7B) code = 0x7B;
+    return sign | (uint8_t)code;
+}
+
 /* ------------------------------------------------------------ formulas */
 
 /* KV bytes = 2 (K and V) * layers * heads * head_dim * seq_len * batch * bytes. */
@@ -178,7 +221,7 @@ int oracle_physical_address(const int32_t* table_row, int num_entries, int block
 static int64_t row_bytes(int kv_dtype, int head_dim) {
     switch (kv_dtype) {
     case DT_F16: case DT_BF16: return 2 * (int64_t)head_dim;
-    case DT_FP8: return head_dim;
+    case DT_FP8: case DT_E5M2: return head_dim;
     case DT_INT4: return head_dim / 2;
     }
     return -1;
@@ -218,11 +261,13 @@ int oracle_dequant_row(const void* cache, const void* scales, int which_kv, int 
         for (int d = 0; d < head_dim; ++d) row[d] = half_word_to_double(h[d], kv_dtype);
         return 0;
     }
-    case DT_FP8: {
+    case DT_FP8: case DT_E5M2: {
         /* snippet-4's dequantize: code value times the block's scale */
         double s = *fp8_scale_ptr((void*)scales, which_kv, block, kv_head, num_blocks,
                                   num_kv_heads);
-        for (int d = 0; d < head_dim; ++d) row[d] = oracle_e4m3_to_double(base[d]) * s;
+        for (int d = 0; d < head_dim; ++d)
+            row[d] = (kv_dtype == DT_FP8 ? oracle_e4m3_to_double(base[d])
+                                         : oracle_e5m2_to_double(base[d])) * s;
         return 0;
     }
     case DT_INT4: {
@@ -243,7 +288,7 @@ int oracle_dequant_row(const void* cache, const void* scales, int which_kv, int 
 
 static int check_geometry(int kv_dtype, int num_blocks, int num_kv_heads, int head_dim,
                           int block_size) {
-    if (kv_dtype < DT_F16 || kv_dtype > DT_INT4) return -1;
+    if (kv_dtype < DT_F16 || kv_dtype > DT_E5M2) return -1;
     if (num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0) return -1;
     if (kv_dtype == DT_INT4 && head_dim % 32) return -1;
     return 0;
@@ -252,7 +297,8 @@ static int check_geometry(int kv_dtype, int num_blocks, int num_kv_heads, int he
 /* Encode one token row of one head (R4-R6).  x: the row as fp32 values. */
 static void encode_row(const float* x, int head_dim, int kv_dtype, uint8_t* dst,
                        int fresh_fp8_block, float* fp8_scale, uint16_t* int4_pairs) {
-    if (kv_dtype == DT_FP8) {
+    if (is_fp8(kv_dtype)) {
+        const float fmax = kv_dtype == DT_FP8 ? 448.0f : 57344.0f;     /* R8 */
         if (fresh_fp8_block) {
             /* snippet-4: scale = max|x| / 448, clamped below at 1e-12, in fp32 */
             float amax = 0.0f;
@@ -260,12 +306,14 @@ static void encode_row(const float* x, int head_dim, int kv_dtype, uint8_t* dst,
                 float a = fabsf(x[d]);
                 if (a > amax) amax = a;
             }
-            float s = amax / 448.0f;
+            float s = amax / fmax;
             if (s < 1e-12f) s = 1e-12f;
             *fp8_scale = s;
         }
         float s = *fp8_scale;
-        for (int d = 0; d < head_dim; ++d) dst[d] = oracle_e4m3_encode(x[d] / s);
+        for (int d = 0; d < head_dim; ++d)
+            dst[d] = kv_dtype == DT_FP8 ? oracle_e4m3_encode(x[d] / s)
+                                        : oracle_e5m2_encode(x[d] / s);
         return;
     }
     /* INT4, R6 */
@@ -323,8 +371,8 @@ int oracle_kv_write(const uint16_t* k_new, const uint16_t* v_new, int new_dtype,
             int32_t block = (int32_t)(slot / block_size);
             int offset = (int)(slot % block_size);
             int first = offset == 0;
-            if (kv_dtype == DT_FP8 && first != (pass == 0)) continue;
-            if (kv_dtype != DT_FP8 && pass == 1) continue;
+            if (is_fp8(kv_dtype) && first != (pass == 0)) continue;
+            if (!is_fp8(kv_dtype) && pass == 1) continue;
             for (int which = 0; which < 2; ++which) {
                 const uint16_t* src = which ? v_new : k_new;
                 uint8_t* cache = (uint8_t*)(which ? v_cache : k_cache);
@@ -338,7 +386,7 @@ int oracle_kv_write(const uint16_t* k_new, const uint16_t* v_new, int new_dtype,
                     }
                     for (int d = 0; d < head_dim; ++d)
                         x[d] = (float)half_word_to_double(srow[d], new_dtype);
-                    float* s8 = kv_dtype == DT_FP8
+                    float* s8 = is_fp8(kv_dtype)
                                     ? fp8_scale_ptr(scales, which, block, h, num_blocks,
                                                     num_kv_heads)
                                     : NULL;

@@ -22,7 +22,7 @@ from typing import Optional
 
 import torch
 
-PKV_F16, PKV_BF16, PKV_FP8_E4M3, PKV_INT4_G32 = 0, 1, 2, 3
+PKV_F16, PKV_BF16, PKV_FP8_E4M3, PKV_INT4_G32, PKV_FP8_E5M2 = 0, 1, 2, 3, 4
 PKV_OK, PKV_ERR_DEVICE_BOUNDS = 0, 4
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -87,7 +87,7 @@ def _stream(stream) -> ctypes.c_void_p:
 
 def row_bytes(kv_dtype: int, head_dim: int) -> int:
     return {PKV_F16: 2 * head_dim, PKV_BF16: 2 * head_dim, PKV_FP8_E4M3: head_dim,
-            PKV_INT4_G32: head_dim // 2}[kv_dtype]
+            PKV_FP8_E5M2: head_dim, PKV_INT4_G32: head_dim // 2}[kv_dtype]
 
 
 def alloc_cache(kv_dtype: int, num_blocks: int, num_kv_heads: int, head_dim: int,
@@ -99,7 +99,7 @@ def alloc_cache(kv_dtype: int, num_blocks: int, num_kv_heads: int, head_dim: int
         return k, torch.zeros_like(k), None
     k = torch.zeros((num_blocks, num_kv_heads, block_size, row_bytes(kv_dtype, head_dim)),
                     dtype=torch.uint8, device=device)
-    if kv_dtype == PKV_FP8_E4M3:
+    if kv_dtype in (PKV_FP8_E4M3, PKV_FP8_E5M2):
         s = torch.zeros((2, num_blocks, num_kv_heads), dtype=torch.float32, device=device)
     else:
         s = torch.zeros((2, num_blocks, num_kv_heads, block_size, head_dim // 32, 2),

@@ -70,6 +70,30 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
   return r;
 }
 
+// The same for OCP E5M2 (largest finite 57344; every E5M2 value is an f16).
+__device__ __forceinline__ uint16_t e5m2x2_from_f32(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t e5m2x2_to_f16x2(uint16_t codes) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(r) : "h"(codes));
+  return r;
+}
+
+// FP8 cache formats, by dtype tag
+__host__ __device__ constexpr bool is_fp8(int kv) { return kv == PKV_FP8_E4M3 || kv == PKV_FP8_E5M2; }
+template <int KV> __device__ __forceinline__ float fp8_max() { return KV == PKV_FP8_E5M2 ? 57344.f : 448.f; }
+template <int KV> __device__ __forceinline__ uint16_t fp8x2_from_f32(float lo, float hi) {
+  if constexpr (KV == PKV_FP8_E5M2) return e5m2x2_from_f32(lo, hi);
+  else return e4m3x2_from_f32(lo, hi);
+}
+template <int KV> __device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint16_t codes) {
+  if constexpr (KV == PKV_FP8_E5M2) return e5m2x2_to_f16x2(codes);
+  else return e4m3x2_to_f16x2(codes);
+}
+
 // ------------------------------------------------------------------ INT4
 // Nibbles k and k+4 of w (k = 0..3) as exact f16x2 values 0..15:
 // OR the nibble into the mantissa of 1024.0 (0x6400), then subtract 1024.

@@ -95,7 +95,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 template <int KV, int D> struct Geo {
   static constexpr bool kHalf = (KV == PKV_F16 || KV == PKV_BF16);
-  static constexpr int kRowBytes = kHalf ? 2 * D : (KV == PKV_FP8_E4M3 ? D : D / 2);
+  static constexpr int kRowBytes = kHalf ? 2 * D : (is_fp8(KV) ? D : D / 2);
   static constexpr int kCpr = kRowBytes / 16;                   // 16-byte chunks per row
   static constexpr int kTileBytes = kTile * kRowBytes;          // one of K or V
   static constexpr int kScaleRowBytes = (KV == PKV_INT4_G32) ? (D / 32) * 4 : 0;
@@ -108,7 +108,7 @@ template <int KV, int D> struct Geo {
   static constexpr int kMiscOffset = kSub * kSubBytes;
   static constexpr int kStageBytes = kSub * kSubBytes + 16 * kSub;
   static constexpr int kStages =
-      kHalf ? PKV_STAGES_HALF : (KV == PKV_FP8_E4M3 ? PKV_STAGES_FP8 : PKV_STAGES_INT4);
+      kHalf ? PKV_STAGES_HALF : (is_fp8(KV) ? PKV_STAGES_FP8 : PKV_STAGES_INT4);
   static constexpr int kWarpRing = kStages * kStageBytes;
   static constexpr int kRingBytes = kDecodeWarps * kWarpRing;
   // merge buffer: one warp's state, lane-major with an odd stride (no bank conflicts)
@@ -130,7 +130,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // analysis in the fragment readers below).
 template <int KV, int D>
 __device__ __forceinline__ int swz(int r) {
-  if constexpr (KV == PKV_F16 || KV == PKV_BF16 || (KV == PKV_FP8_E4M3 && D == 128)) {
+  if constexpr (KV == PKV_F16 || KV == PKV_BF16 || (is_fp8(KV) && D == 128)) {
     return (((r ^ (r >> 1)) & 1) << 2) | ((r >> 2) & 1);
   } else if constexpr (KV == PKV_INT4_G32) {
     return D == 128 ? ((r >> 1) & 3) : ((r >> 1) & 1);
@@ -215,7 +215,7 @@ __device__ __forceinline__ void issue_tile(const Params& p, int kvh, int t0, int
       cp_async_16(stage + 2 * G::kTileBytes + G::kScaleTileBytes + (lane - 16) * 16,
                   vsc + (lane - 16) * 16);
     }
-  } else if constexpr (KV == PKV_FP8_E4M3) {
+  } else if constexpr (is_fp8(KV)) {
     const float* sc = static_cast<const float*>(p.scales);
     const int64_t idx = static_cast<int64_t>(phys) * p.num_kv_heads + kvh;
     const int64_t per_kv = static_cast<int64_t>(p.num_blocks) * p.num_kv_heads;
@@ -269,7 +269,7 @@ __device__ __forceinline__ void load_q(const Params& p, const Unit& u, int q4, i
   } else {
     // each thread's 32 d values, as float
     float qf[32];
-    if constexpr (KV == PKV_FP8_E4M3) {
+    if constexpr (is_fp8(KV)) {
       // d = 16*(4i + c4) + 0..15 for i < D/64
 #pragma unroll
       for (int i = 0; i < D / 64; ++i) {
@@ -308,7 +308,7 @@ __device__ __forceinline__ void load_q(const Params& p, const Unit& u, int q4, i
     if (amax >= 32768.f) e = ilogbf(amax) - 14;
     const float qs = ldexpf(1.f, -e);
     qexp = ldexpf(1.f, e);
-    if constexpr (KV == PKV_FP8_E4M3) {
+    if constexpr (is_fp8(KV)) {
       // k-step 4i+h: lo pair = d 16(4i+c4) + 4h + {0,1}, hi pair = + 4h + {2,3}
 #pragma unroll
       for (int i = 0; i < D / 64; ++i)
@@ -400,7 +400,7 @@ paged_decode_kernel(const Params p) {
   // f16 cases keep kPScale * 2^kTau (* 16 for the FP8 scale ratio) below 2^15.
   constexpr float kPScale = (KV == PKV_BF16 || KV == PKV_INT4_G32) ? 1.f
                                                                    : (KV == PKV_F16 ? 256.f : 64.f);
-  constexpr float kTau = (KV == PKV_BF16) ? 8.f : (KV == PKV_F16 ? 6.f : (KV == PKV_FP8_E4M3 ? 4.f : 0.f));
+  constexpr float kTau = (KV == PKV_BF16) ? 8.f : (KV == PKV_F16 ? 6.f : (is_fp8(KV) ? 4.f : 0.f));
   constexpr int kQN = kHalf ? 1 : D / 32;
 
   extern __shared__ __align__(128) uint8_t smem[];
@@ -560,7 +560,7 @@ paged_decode_kernel(const Params p) {
                 const uint32_t a1[4] = {r0.z, r1.z, r0.w, r1.w};
                 mma_16816<MMA_T>(sc2, a1, qb[2 * jp + 1][0], qb[2 * jp + 1][1]);
               }
-            } else if constexpr (KV == PKV_FP8_E4M3) {
+            } else if constexpr (is_fp8(KV)) {
 #pragma unroll
               for (int i = 0; i < D / 64; ++i) {
                 const uint4 r0 = ld_shared_v4(st + chunk_off<KV, D>(q4, 4 * i + c4));
@@ -569,8 +569,8 @@ paged_decode_kernel(const Params p) {
                 const uint32_t w1[4] = {r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
-                  const uint32_t a[4] = {e4m3x2_to_f16x2(w0[h] & 0xFFFF), e4m3x2_to_f16x2(w1[h] & 0xFFFF),
-                                         e4m3x2_to_f16x2(w0[h] >> 16), e4m3x2_to_f16x2(w1[h] >> 16)};
+                  const uint32_t a[4] = {fp8x2_to_f16x2<KV>(w0[h] & 0xFFFF), fp8x2_to_f16x2<KV>(w1[h] & 0xFFFF),
+                                         fp8x2_to_f16x2<KV>(w0[h] >> 16), fp8x2_to_f16x2<KV>(w1[h] >> 16)};
                   if (h & 1)
                     mma_16816<PKV_F16>(sc2, a, qb[4 * i + h][0], qb[4 * i + h][1]);
                   else
@@ -622,7 +622,7 @@ paged_decode_kernel(const Params p) {
 
           // ---------------------------------------------- scale and mask
           float mult = base;
-          if constexpr (KV == PKV_FP8_E4M3) {
+          if constexpr (is_fp8(KV)) {
             mult *= reinterpret_cast<const float*>(misc)[0];
           } else if constexpr (KV == PKV_INT4_G32) {
             mult = p.softmax_scale * kLog2e;     // qexp already folded into the group sums
@@ -659,7 +659,7 @@ paged_decode_kernel(const Params p) {
         for (int u = 0; u < G::kSub; ++u) {
           von[u] = nval[u] > 0;
           vfac[u] = 1.f;
-          if constexpr (KV == PKV_FP8_E4M3) {
+          if constexpr (is_fp8(KV)) {
             const float vs = reinterpret_cast<const float*>(misc0 + 4 * u)[1];
             von[u] = von[u] && vs > 0.f;
             if (von[u]) {
@@ -680,7 +680,7 @@ paged_decode_kernel(const Params p) {
 #pragma unroll
             for (int g = 0; g < D / 32; ++g) { zacc[g][0] *= alpha0; zacc[g][1] *= alpha1; }
           }
-          if constexpr (KV == PKV_FP8_E4M3) {
+          if constexpr (is_fp8(KV)) {
             if (rebase) {
               // new reference: the tile's largest V scale; O_true = oacc * vref /
               // kPScale stays invariant across the rebase
@@ -788,12 +788,12 @@ paged_decode_kernel(const Params p) {
                 for (int k = 0; k < NW; ++k) {
                   const uint32_t x01 = __byte_perm(wa[k], wb[k], 0x5140), x23 = __byte_perm(wa[k], wb[k], 0x7362);
                   const uint32_t y01 = __byte_perm(wc[k], we[k], 0x5140), y23 = __byte_perm(wc[k], we[k], 0x7362);
-                  const uint32_t a0[4] = {e4m3x2_to_f16x2(x01 & 0xFFFF), e4m3x2_to_f16x2(x01 >> 16),
-                                          e4m3x2_to_f16x2(y01 & 0xFFFF), e4m3x2_to_f16x2(y01 >> 16)};
+                  const uint32_t a0[4] = {fp8x2_to_f16x2<KV>(x01 & 0xFFFF), fp8x2_to_f16x2<KV>(x01 >> 16),
+                                          fp8x2_to_f16x2<KV>(y01 & 0xFFFF), fp8x2_to_f16x2<KV>(y01 >> 16)};
                   mma_16816<PKV_F16>(oacc[2 * k], a0, bh0, bh1);
                   mma_16816<PKV_F16>(oacc[2 * k], a0, bl0, bl1);
-                  const uint32_t a1[4] = {e4m3x2_to_f16x2(x23 & 0xFFFF), e4m3x2_to_f16x2(x23 >> 16),
-                                          e4m3x2_to_f16x2(y23 & 0xFFFF), e4m3x2_to_f16x2(y23 >> 16)};
+                  const uint32_t a1[4] = {fp8x2_to_f16x2<KV>(x23 & 0xFFFF), fp8x2_to_f16x2<KV>(x23 >> 16),
+                                          fp8x2_to_f16x2<KV>(y23 & 0xFFFF), fp8x2_to_f16x2<KV>(y23 >> 16)};
                   mma_16816<PKV_F16>(oacc[2 * k + 1], a1, bh0, bh1);
                   mma_16816<PKV_F16>(oacc[2 * k + 1], a1, bl0, bl1);
                 }
@@ -864,7 +864,7 @@ paged_decode_kernel(const Params p) {
       lrow[1] += __shfl_xor_sync(0xffffffffu, lrow[1], o);
     }
     float post = 1.f / kPScale;
-    if constexpr (KV == PKV_FP8_E4M3) post *= vref;
+    if constexpr (is_fp8(KV)) post *= vref;
 #pragma unroll
     for (int i = 0; i < MT; ++i)
 #pragma unroll
@@ -926,7 +926,7 @@ paged_decode_kernel(const Params p) {
           int d0;
           if constexpr (KV == PKV_INT4_G32) {
             d0 = 32 * (i >> 1) + 4 * q4 + 2 * (i & 1);
-          } else if constexpr (KV == PKV_FP8_E4M3 && D == 128) {
+          } else if constexpr (is_fp8(KV) && D == 128) {
             d0 = 16 * (((q4 & 1) << 1) | ((q4 >> 1) & 1) | (q4 & 4)) + 2 * i;
           } else {
             d0 = (D == 128 ? 16 : 8) * q4 + 2 * i;
@@ -1091,6 +1091,9 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
     case PKV_FP8_E4M3:
       return a.q_dtype == PKV_F16 ? launch_d<PKV_FP8_E4M3, PKV_F16>(a, st)
                                   : launch_d<PKV_FP8_E4M3, PKV_BF16>(a, st);
+    case PKV_FP8_E5M2:
+      return a.q_dtype == PKV_F16 ? launch_d<PKV_FP8_E5M2, PKV_F16>(a, st)
+                                  : launch_d<PKV_FP8_E5M2, PKV_BF16>(a, st);
     default:
       return a.q_dtype == PKV_F16 ? launch_d<PKV_INT4_G32, PKV_F16>(a, st)
                                   : launch_d<PKV_INT4_G32, PKV_BF16>(a, st);
@@ -1100,10 +1103,22 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
 int resolve_partition_size(int num_seqs, int num_q_heads, int num_kv_heads,
                            int max_blocks_per_seq, int block_size, int requested) {
   if (requested > 0) return ((requested + kTile - 1) / kTile) * kTile;
+  // Measured on GB300: grids with enough units for warp-owned units run best
+  // with 512-token partitions, shared-partition grids with 1024 (fewer merges);
+  // few (sequence, KV head) pairs need short partitions to fill 152 SMs.
+  // The unit threshold below is the one the launch uses for 152 SMs.
   const int64_t max_ctx = static_cast<int64_t>(max_blocks_per_seq) * block_size;
   const int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads;
-  int part = 512;
-  if (pairs * ((max_ctx + 511) / 512) < 2 * 152) part = 256;
+  const int64_t wu_units = static_cast<int64_t>(PKV_WU_WAVES) * 152 * 16;
+  int part;
+  if (pairs * ((max_ctx + 511) / 512) >= wu_units)
+    part = 512;
+  else if (pairs * ((max_ctx + 1023) / 1024) >= 4 * 152)
+    part = 1024;
+  else if (pairs * ((max_ctx + 511) / 512) >= 2 * 152)
+    part = 512;
+  else
+    part = 256;
   if (max_ctx <= part) part = static_cast<int>(((max_ctx + kTile - 1) / kTile) * kTile);
   if (part <= 0) part = kTile;
   (void)num_q_heads;

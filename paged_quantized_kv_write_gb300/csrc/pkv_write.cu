@@ -8,8 +8,9 @@
 // Encodings (the formats' definitions; block-wise FP8 scale from snippet-4
 // of "Reducing LLM Inference Latency ... PagedAttention in vLLM"; INT4
 // group-wise from section 4 of "Optimizing KV-Cache Memory Footprint"):
-//  FP8  scale = max(amax / 448, 1e-12) (fp32), set by the token at block
-//       offset 0; code = cvt.rn.satfinite.e4m3(x / scale), IEEE fp32 division.
+//  FP8  scale = max(amax / max_finite, 1e-12) (fp32; max_finite 448 for E4M3,
+//       57344 for E5M2), set by the token at block offset 0;
+//       code = cvt.rn.satfinite.{e4m3,e5m2}(x / scale), IEEE fp32 division.
 //  INT4 per 32-element group: scale = fp16(fp32(max - min + 0) / 15),
 //       zero = fp16(min + 0), code = clamp(rint((x - zero) / scale), 0, 15).
 // Every fp32 step uses an explicitly rounded intrinsic so the codes are the
@@ -75,7 +76,7 @@ kv_write_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict__
       } else {
         *reinterpret_cast<uint32_t*>(dst) = raw[0] | (uint32_t(raw[1]) << 16);
       }
-    } else if constexpr (KV == PKV_FP8_E4M3) {
+    } else if constexpr (is_fp8(KV)) {
       float x[EPL];
 #pragma unroll
       for (int e = 0; e < EPL; ++e) x[e] = Half16<NEW>::to_float(raw[e]);
@@ -88,18 +89,18 @@ kv_write_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict__
         for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(x[e]));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        s = fmaxf(__fdiv_rn(amax, 448.0f), 1e-12f);
+        s = fmaxf(__fdiv_rn(amax, fp8_max<KV>()), 1e-12f);
         if (lane == 0) *sp = s;
       } else {
         s = *sp;
       }
       uint8_t* dst = cache + cache_row * D + lane * EPL;
       if constexpr (EPL == 4) {
-        uint32_t lo = e4m3x2_from_f32(__fdiv_rn(x[0], s), __fdiv_rn(x[1], s));
-        uint32_t hi = e4m3x2_from_f32(__fdiv_rn(x[2], s), __fdiv_rn(x[3], s));
+        uint32_t lo = fp8x2_from_f32<KV>(__fdiv_rn(x[0], s), __fdiv_rn(x[1], s));
+        uint32_t hi = fp8x2_from_f32<KV>(__fdiv_rn(x[2], s), __fdiv_rn(x[3], s));
         *reinterpret_cast<uint32_t*>(dst) = lo | (hi << 16);
       } else {
-        *reinterpret_cast<uint16_t*>(dst) = e4m3x2_from_f32(__fdiv_rn(x[0], s), __fdiv_rn(x[1], s));
+        *reinterpret_cast<uint16_t*>(dst) = fp8x2_from_f32<KV>(__fdiv_rn(x[0], s), __fdiv_rn(x[1], s));
       }
     } else {  // INT4_G32
       constexpr int LPG = 32 / EPL;                    // lanes per 32-element group
@@ -155,7 +156,7 @@ cudaError_t launch_one(const WriteArgs& a, cudaStream_t st) {
 
 template <int KV, int NEW, int D>
 cudaError_t launch_kv(const WriteArgs& a, cudaStream_t st) {
-  if constexpr (KV == PKV_FP8_E4M3) {
+  if constexpr (is_fp8(KV)) {
     // offset-0 tokens set the block scales; the rest read them afterwards
     cudaError_t e = launch_one<KV, NEW, D, 0>(a, st);
     if (e != cudaSuccess) return e;
@@ -171,6 +172,7 @@ cudaError_t dispatch_kv(const WriteArgs& a, cudaStream_t st) {
     case PKV_F16: return launch_kv<PKV_F16, NEW, D>(a, st);
     case PKV_BF16: return launch_kv<PKV_BF16, NEW, D>(a, st);
     case PKV_FP8_E4M3: return launch_kv<PKV_FP8_E4M3, NEW, D>(a, st);
+    case PKV_FP8_E5M2: return launch_kv<PKV_FP8_E5M2, NEW, D>(a, st);
     default: return launch_kv<PKV_INT4_G32, NEW, D>(a, st);
   }
 }

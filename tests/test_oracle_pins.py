@@ -173,6 +173,82 @@ def test_e4m3_encode_saturation_and_signed_zero():
     assert oracle.e4m3_encode(float("nan")) == 0x7F
 
 
+# ------------------------------------------------------------------ E5M2
+def _finite_e5m2_table():
+    codes = [c for c in range(256) if (c >> 2) & 0x1F != 0x1F]
+    return codes, np.array([oracle.e5m2_to_double(c) for c in codes])
+
+
+def test_e5m2_decode_all_codes_vs_torch():
+    f = FACTS["e5m2_format"]
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e5m2).double().numpy()
+    got = np.array([oracle.e5m2_to_double(int(c)) for c in codes])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(got[fin], ref[fin])
+    assert oracle.e5m2_to_double(0x7C) == math.inf and oracle.e5m2_to_double(0xFC) == -math.inf
+    # 1/5/2 bits with FP16's exponent range: same smallest normal and top binade
+    assert f["exponent_bits"] == 5 and f["mantissa_bits"] == 2
+    f16_min_normal = float(np.array([0x0400], np.uint16).view(np.float16)[0])
+    f16_max = float(np.finfo(np.float16).max)
+    assert oracle.e5m2_to_double(0x04) == f16_min_normal == 2.0**-14
+    assert math.frexp(oracle.e5m2_to_double(0x7B))[1] == math.frexp(f16_max)[1]
+    assert oracle.e5m2_to_double(0x7B) == 57344.0
+    assert oracle.e5m2_to_double(0x01) == 2.0**-16
+    assert oracle.e5m2_to_double(0x3D) - oracle.e5m2_to_double(0x3C) == 2.0**-2
+
+
+def _brute_force_e5m2(y: float, codes, vals) -> int:
+    """Nearest finite E5M2 value, ties to the even code; saturate at +-57344."""
+    a = abs(y)
+    neg = math.copysign(1, y) < 0
+    if a >= 57344.0:
+        return 0xFB if neg else 0x7B
+    best, bestd = None, None
+    for c, v in zip(codes, vals):
+        if c & 0x80:
+            continue
+        d = abs(a - v)
+        if bestd is None or d < bestd or (d == bestd and (c & 1) == 0):
+            best, bestd = c, d
+    return best | (0x80 if neg else 0)
+
+
+def test_e5m2_encode_vs_brute_force_nearest_even():
+    codes, vals = _finite_e5m2_table()
+    pos = sorted(set(v for c, v in zip(codes, vals) if not c & 0x80))
+    mids = [(a + b) / 2 for a, b in zip(pos[:-1], pos[1:])]
+    rng = np.random.default_rng(13)
+    xs = list(np.float32(pos)) + list(np.float32(mids))
+    xs += [np.nextafter(np.float32(m), np.float32(np.inf)) for m in mids]
+    xs += [np.nextafter(np.float32(m), np.float32(-np.inf)) for m in mids]
+    xs += list(np.exp2(rng.uniform(-18, 16, 3000)).astype(np.float32))
+    xs += [np.float32(v) for v in (57344.0, 57345.0, 61439.0, 61440.0, 65536.0, 1e9, 1e-30)]
+    for x in xs:
+        for y in (float(x), -float(x)):
+            assert oracle.e5m2_encode(y) == _brute_force_e5m2(y, codes, vals), y
+
+
+def test_e5m2_encode_vs_torch_cast_in_range():
+    rng = np.random.default_rng(14)
+    y = np.concatenate([rng.standard_normal(20000) * 3000,
+                        np.exp2(rng.uniform(-16, 15.8, 20000)) * rng.choice([-1, 1], 20000)])
+    y = np.clip(y, -57343.0, 57343.0).astype(np.float32)
+    ref = torch.from_numpy(y).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    got = np.array([oracle.e5m2_encode(float(v)) for v in y], dtype=np.uint8)
+    assert np.array_equal(got, ref)
+
+
+def test_e5m2_encode_saturation_and_signed_zero():
+    assert oracle.e5m2_encode(57344.0) == 0x7B
+    assert oracle.e5m2_encode(61440.0) == 0x7B      # would round up to 2^16 = infinity
+    assert oracle.e5m2_encode(-1e9) == 0xFB
+    assert oracle.e5m2_encode(float("inf")) == 0x7B
+    assert oracle.e5m2_encode(-0.0) == 0x80
+    assert oracle.e5m2_encode(float("nan")) == 0x7F
+
+
 # ------------------------------------------------------------------ the write
 def _one_block_write(kv_dtype, rows, offsets, head_dim=64, block_size=16, dtype=W.BF16,
                      num_kv_heads=1):
@@ -212,6 +288,19 @@ def test_write_fp8_scale_is_amax_over_448():
     deq = np.array([oracle.e4m3_to_double(c) for c in k[1, 0, 0]]) * float(s[0, 1, 0])
     err = np.abs(deq - xr)
     assert np.all(err <= np.maximum(np.abs(xr) * 2.0**-4, 2.0**-10 * float(s[0, 1, 0])) + 1e-12)
+
+
+def test_write_e5m2_scale_is_amax_over_its_largest_finite():
+    rng = np.random.default_rng(6)
+    row = (rng.standard_normal(64) * 3).astype(np.float32)
+    row[5] = 11.0
+    k, v, s, x = _one_block_write(W.FP8_E5M2, row[None], [0])
+    xr = W.bits_to_f32(x[0, 0], W.BF16)
+    assert s[0, 1, 0] == np.float32(np.float32(11.0) / np.float32(57344.0))
+    assert k[1, 0, 0, 5] == 0x7B
+    deq = np.array([oracle.e5m2_to_double(c) for c in k[1, 0, 0]]) * float(s[0, 1, 0])
+    # half an E5M2 step: 2^-3 relative for normals
+    assert np.all(np.abs(deq - xr) <= np.abs(xr) * 2.0**-3 + 2.0**-17 * float(s[0, 1, 0]))
 
 
 def test_write_fp8_zero_row_uses_eps_scale():
@@ -312,8 +401,9 @@ def _gathered(case, k, v, s, b):
                 out[:, t] = raw.view(np.float16).astype(np.float64)
             elif w.kv_dtype == W.BF16:
                 out[:, t] = torch.from_numpy(raw.view(np.int16)).view(torch.bfloat16).double().numpy()
-            elif w.kv_dtype == W.FP8_E4M3:
-                dec = torch.from_numpy(np.ascontiguousarray(raw)).view(torch.float8_e4m3fn).double().numpy()
+            elif w.kv_dtype in W.FP8_TYPES:
+                fmt = torch.float8_e4m3fn if w.kv_dtype == W.FP8_E4M3 else torch.float8_e5m2
+                dec = torch.from_numpy(np.ascontiguousarray(raw)).view(fmt).double().numpy()
                 out[:, t] = dec * s[j, p, :, None].astype(np.float64)
             else:
                 lo = (raw & 0xF).astype(np.float64)
@@ -324,9 +414,12 @@ def _gathered(case, k, v, s, b):
     return kd, vd
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, "3-e5m2"])
 def test_attention_matches_sdpa_on_gathered_kv(cfg):
-    w = W.CONFIGS[cfg].scaled(batch=3, ctx_cap=70, seed=100 + cfg)
+    if cfg == "3-e5m2":
+        w = W.CONFIGS[3].scaled(batch=3, ctx_cap=70, seed=106, kv_dtype=W.FP8_E5M2)
+    else:
+        w = W.CONFIGS[cfg].scaled(batch=3, ctx_cap=70, seed=100 + cfg)
     case = W.make_case(w)
     k, v, s = oracle.prefill_case(case)
     out = oracle.step_case(case, k, v, s)
