@@ -95,31 +95,20 @@ template <int KV> __device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint16_t co
 }
 
 // ------------------------------------------------------------------ INT4
-// Nibbles k and k+4 of w (k = 0..3) as exact f16x2 values 0..15:
-// OR the nibble into the mantissa of 1024.0 (0x6400), then subtract 1024.
-__device__ __forceinline__ uint32_t nibbles_to_f16x2(uint32_t w, int k) {
-  uint32_t x = ((w >> (4 * k)) & 0x000F000Fu) | 0x64006400u;
-  __half2 h = *reinterpret_cast<__half2*>(&x);
-  h = __hsub2(h, __half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
-  return *reinterpret_cast<uint32_t*>(&h);
-}
+// Codes as f16 subnormals.  A nibble n placed in the low mantissa bits of an
+// f16 with a zero exponent field is exactly n * 2^-24, so one AND turns two
+// packed nibbles into an f16x2 operand with no offset to take off:
+//   nib_lo: the nibbles at bits 0-3 and 16-19 of w -> n * 2^-24
+//   nib_hi: the nibbles at bits 4-7 and 20-23      -> 16 n * 2^-24
+// The products with them are exact in fp32; the caller undoes 2^24 (and the
+// 16 of the high nibbles) once, after the sums.
+__device__ __forceinline__ uint32_t nib_lo(uint32_t w) { return w & 0x000F000Fu; }
+__device__ __forceinline__ uint32_t nib_hi(uint32_t w) { return w & 0x00F000F0u; }
 
-// Same nibbles as f16 1024 + n (no subtraction): for products whose 1024 * sum
-// is taken off afterwards.
-__device__ __forceinline__ uint32_t nibbles_offset_f16x2(uint32_t w, int k) {
-  return ((w >> (4 * k)) & 0x000F000Fu) | 0x64006400u;
-}
-
-// Shift-free variants on the nibbles at bits 0-3 / 16-19 (`lo`) and 4-7 /
-// 20-23 (`hi`) of w: f16x2 1024 + n and 1024 + 16 n, exact.  The factor 16 of
-// the `hi` form is undone by the caller (a power of two, so exactly).
-__device__ __forceinline__ uint32_t nib_lo_offset(uint32_t w) { return (w & 0x000F000Fu) | 0x64006400u; }
-__device__ __forceinline__ uint32_t nib_hi_offset(uint32_t w) { return (w & 0x00F000F0u) | 0x64006400u; }
-// f16x2 x - 1024 (exact for the values above)
-__device__ __forceinline__ uint32_t sub1024(uint32_t x) {
-  __half2 h = *reinterpret_cast<__half2*>(&x);
-  h = __hsub2(h, __half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
-  return *reinterpret_cast<uint32_t*>(&h);
+// f16x2 product, round to nearest
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
 }
 
 // ------------------------------------------------------------------ tensor cores
@@ -216,6 +205,31 @@ __device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr) {
   unsigned short v;
   asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
   return v;
+}
+
+// ldmatrix: 8x8 matrices of 16-bit values, one 16-byte row per lane address
+// (lanes 8j..8j+7 give the rows of matrix j).  Without .trans lane l receives
+// row l/4, columns 2(l%4), +1 of each matrix; with .trans, rows 2(l%4), +1 of
+// column l/4.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldmatrix_x2(uint32_t addr, uint32_t (&r)[2]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldmatrix_x2_trans(uint32_t addr, uint32_t (&r)[2]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(addr));
 }
 
 __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {

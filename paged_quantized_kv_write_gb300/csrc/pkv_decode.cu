@@ -133,7 +133,7 @@ __device__ __forceinline__ int swz(int r) {
   if constexpr (KV == PKV_F16 || KV == PKV_BF16 || (is_fp8(KV) && D == 128)) {
     return (((r ^ (r >> 1)) & 1) << 2) | ((r >> 2) & 1);
   } else if constexpr (KV == PKV_INT4_G32) {
-    return D == 128 ? ((r >> 1) & 3) : ((r >> 1) & 1);
+    return D == 128 ? ((r >> 1) & 3) : ((r >> 2) & 1);
   } else {
     return 0;
   }
@@ -143,6 +143,38 @@ template <int KV, int D>
 __device__ __forceinline__ uint32_t chunk_off(int row, int ch) {
   using G = Geo<KV, D>;
   return static_cast<uint32_t>((row * G::kCpr + (ch ^ swz<KV, D>(row))) * 16);
+}
+
+// INT4 ldmatrix row addresses of one lane within a sub-tile (bytes from its
+// base).  K (no .trans): lane l gives token l % 8 of group l / 8 (D = 64:
+// token l % 8 + 8 ((l / 8) >> 1), group (l / 8) & 1), so matrix j returns,
+// for lane (q4, c4), bytes 4c4..4c4+3 of group j of token q4; tokens 8..15
+// sit kInt4K1 bytes further (the swizzle repeats every 8 rows).
+// V (.trans): matrix m of call c is tokens 8 (m & 1) + 0..7 of group
+// 2c + (m >> 1), so lane (q4, c4) gets bytes 2q4, 2q4 + 1 of tokens 2c4 and
+// 2c4 + 1 (or + 8).  kz: row (lane % 16) of the K scale tile; the V scale
+// tile's row sits kScaleTileBytes further.
+struct Int4Lanes {
+  uint32_t k0, v0, v1, kz;
+};
+constexpr uint32_t kInt4K1 = 8 * 64;          // 8 rows of 64 bytes (D = 128)
+template <int KV, int D>
+__device__ __forceinline__ Int4Lanes int4_lanes(int lane) {
+  Int4Lanes o = {0u, 0u, 0u, 0u};
+  if constexpr (KV == PKV_INT4_G32) {
+    using G = Geo<KV, D>;
+    const int r = lane & 7, m = lane >> 3;
+    if constexpr (D == 128) {
+      o.k0 = chunk_off<KV, D>(r, m);
+      o.v0 = G::kTileBytes + chunk_off<KV, D>(r + 8 * (m & 1), m >> 1);
+      o.v1 = G::kTileBytes + chunk_off<KV, D>(r + 8 * (m & 1), 2 + (m >> 1));
+    } else {
+      o.k0 = chunk_off<KV, D>(r + 8 * (m >> 1), m & 1);
+      o.v0 = G::kTileBytes + chunk_off<KV, D>(r + 8 * (m & 1), m >> 1);
+    }
+    o.kz = 2 * G::kTileBytes + (lane & 15) * G::kScaleRowBytes;
+  }
+  return o;
 }
 
 struct Params {
@@ -245,12 +277,13 @@ __device__ __forceinline__ Unit make_unit(const Params& p, int b, int kvh, int c
 
 // Q of the unit's G heads as the B operand of S^T = K Q^T (column n = head q4
 // of the group, rows = d in the order the K fragments use; heads >= group are
-// zero columns), plus the f16 scaling and INT4 group sums.
+// zero columns), plus the f16 scaling.  INT4 also gets the B operand of its
+// zero-point product (zq, hi + lo f16 words; see the score code) and the
+// factor zscale that product's sums are taken back with.
 template <int KV, int QT, int D>
 __device__ __forceinline__ void load_q(const Params& p, const Unit& u, int q4, int c4,
                                        uint32_t (&qb)[D / 16][2], float& qexp,
-                                       float (&qsum)[(KV == PKV_F16 || KV == PKV_BF16) ? 1 : D / 32][2],
-                                       float (&qoff)[(KV == PKV_F16 || KV == PKV_BF16) ? 1 : D / 32][2]) {
+                                       uint32_t (&zq)[2], float& zscale) {
   constexpr bool kHalf = (KV == PKV_F16 || KV == PKV_BF16);
   const int group = p.num_q_heads / p.num_kv_heads;
   const bool head_ok = q4 < group;
@@ -264,8 +297,8 @@ __device__ __forceinline__ void load_q(const Params& p, const Unit& u, int q4, i
       qb[2 * jp][0] = v.x; qb[2 * jp][1] = v.y;
       qb[2 * jp + 1][0] = v.z; qb[2 * jp + 1][1] = v.w;
     }
-    qsum[0][0] = qsum[0][1] = 0.f;
-    qoff[0][0] = qoff[0][1] = 0.f;
+    zq[0] = zq[1] = 0u;
+    zscale = 0.f;
   } else {
     // each thread's 32 d values, as float
     float qf[32];
@@ -309,6 +342,8 @@ __device__ __forceinline__ void load_q(const Params& p, const Unit& u, int q4, i
     const float qs = ldexpf(1.f, -e);
     qexp = ldexpf(1.f, e);
     if constexpr (is_fp8(KV)) {
+      zq[0] = zq[1] = 0u;
+      zscale = 0.f;
       // k-step 4i+h: lo pair = d 16(4i+c4) + 4h + {0,1}, hi pair = + 4h + {2,3}
 #pragma unroll
       for (int i = 0; i < D / 64; ++i)
@@ -319,8 +354,9 @@ __device__ __forceinline__ void load_q(const Params& p, const Unit& u, int q4, i
         }
     } else {
       // k-step 2grp+h: lo pair = d (8c4 + 2h, 8c4 + 2h + 4), hi pair = (8c4 + 2h + 1, 8c4 + 2h + 5).
-      // The hi pairs meet K codes taken as 1024 + 16 n (high nibbles, no shift),
-      // so their q enters divided by 16.
+      // The hi pairs meet K codes taken as 16 n (high nibbles, no shift), so
+      // their q enters divided by 16.
+      float zsel = 0.f;                        // sum of q over group c4 of head q4
 #pragma unroll
       for (int grp = 0; grp < D / 32; ++grp) {
 #pragma unroll
@@ -330,23 +366,24 @@ __device__ __forceinline__ void load_q(const Params& p, const Unit& u, int q4, i
           qb[2 * grp + h][1] =
               Half16<PKV_F16>::pack_rn(x[2 * h + 1] * (qs * 0.0625f), x[2 * h + 5] * (qs * 0.0625f));
         }
-        float s = 0.f, s16 = 0.f;
+        float s = 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          s += qf[8 * grp + k] + qf[8 * grp + k + 4];
-          const float2 lo = Half16<PKV_F16>::unpack(qb[2 * grp + (k >> 1)][k & 1]);
-          s16 += lo.x + lo.y;                           // the f16 values the mma sees
-        }
+        for (int k = 0; k < 4; ++k) s += qf[8 * grp + k] + qf[8 * grp + k + 4];
 #pragma unroll
-        for (int o = 1; o <= 2; o <<= 1) {
-          s += __shfl_xor_sync(0xffffffffu, s, o);
-          s16 += __shfl_xor_sync(0xffffffffu, s16, o);  // sums over d of head q4, group grp
-        }
-        qsum[grp][0] = __shfl_sync(0xffffffffu, s, (2 * c4) * 4);
-        qsum[grp][1] = __shfl_sync(0xffffffffu, s, (2 * c4 + 1) * 4);
-        qoff[grp][0] = 1024.f * __shfl_sync(0xffffffffu, s16, (2 * c4) * 4);
-        qoff[grp][1] = 1024.f * __shfl_sync(0xffffffffu, s16, (2 * c4 + 1) * 4);
+        for (int o = 1; o <= 2; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (grp == c4) zsel = s;
       }
+      // Zero-point product: the (scale, zero) words of a token's scale row are
+      // its A operand (k = 2g: scale of group g, k = 2g + 1: zero of group g),
+      // so its B operand is 0 at k = 2c4 and sum(q of group c4) at k = 2c4 + 1,
+      // as an f16 hi + lo pair (relative error ~2^-22).  The sum enters times
+      // qs / 32, clear of the f16 range (|q qs| < 2^15, 32 terms).
+      const float zv = zsel * (qs * 0.03125f);
+      const __half zh = __float2half_rn(zv);
+      const __half zl = __float2half_rn(zv - __half2float(zh));
+      zq[0] = static_cast<uint32_t>(__half_as_ushort(zh)) << 16;
+      zq[1] = static_cast<uint32_t>(__half_as_ushort(zl)) << 16;
+      zscale = qexp * 32.f;
     }
   }
 }
@@ -401,7 +438,6 @@ paged_decode_kernel(const Params p) {
   constexpr float kPScale = (KV == PKV_BF16 || KV == PKV_INT4_G32) ? 1.f
                                                                    : (KV == PKV_F16 ? 256.f : 64.f);
   constexpr float kTau = (KV == PKV_BF16) ? 8.f : (KV == PKV_F16 ? 6.f : (is_fp8(KV) ? 4.f : 0.f));
-  constexpr int kQN = kHalf ? 1 : D / 32;
 
   extern __shared__ __align__(128) uint8_t smem[];
   pdl_wait();                 // the cache may have been written by the previous kernel
@@ -496,16 +532,20 @@ paged_decode_kernel(const Params p) {
 #pragma unroll 1
   for (int s = 0; s < G::kStages; ++s) issue_next();
 
+  // INT4: this lane's ldmatrix row addresses within a sub-tile
+  const Int4Lanes i4 = int4_lanes<KV, D>(lane);
+
   // ---------------------------------------------------------------- state
   uint32_t qb[MT][2];
   float qexp = 1.f;
-  float qsum[kQN][2], qoff[kQN][2];
+  uint32_t zq[2];                            // INT4: B operand of the zero-point product
+  float zscale;
   float oacc[MT][4];
   float mrow[2], lrow[2];
-  float zacc[KV == PKV_INT4_G32 ? D / 32 : 1][2];
+  float zc[4];                               // INT4: zero-point sums (C fragment)
   float vref, inv_vref;                      // FP8: oacc is in units of vref / kPScale
   int consumed = 0;                          // pairs computed so far (ring position)
-  load_q<KV, QT, D>(p, make_unit<G::kTileTok>(p, b, kvh, ctx, part_of(0)), q4, c4, qb, qexp, qsum, qoff);
+  load_q<KV, QT, D>(p, make_unit<G::kTileTok>(p, b, kvh, ctx, part_of(0)), q4, c4, qb, qexp, zq, zscale);
 
 #pragma unroll 1
   for (int cu = 0; cu < nunits; ++cu) {
@@ -514,11 +554,11 @@ paged_decode_kernel(const Params p) {
     for (int i = 0; i < MT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
     mrow[0] = mrow[1] = -INFINITY;           // running max (log2 units), heads 2c4, 2c4+1
     lrow[0] = lrow[1] = 0.f;                 // this thread's share of the running sum
-#pragma unroll
-    for (int g = 0; g < (KV == PKV_INT4_G32 ? D / 32 : 1); ++g) zacc[g][0] = zacc[g][1] = 0.f;
+    zc[0] = zc[1] = zc[2] = zc[3] = 0.f;
     vref = 0.f;
     inv_vref = 0.f;
     const float base = p.softmax_scale * kLog2e * qexp;
+    const float kq24 = qexp * 16777216.f;    // INT4: undoes the codes' 2^-24 and q's scaling
     const int tok_end = unit.tok_end;
 
 #pragma unroll 1
@@ -578,11 +618,25 @@ paged_decode_kernel(const Params p) {
                 }
               }
             } else {
-              // INT4: one fresh accumulator per 32-element group, then
-              // s += scale_t * acc + zero_t * sum(q)
+              // INT4: one fresh accumulator per 32-element group for the codes
+              // (taken as n 2^-24 and 16 n 2^-24, met by q and q / 16), then
+              // s = 2^24 qexp sum_g scale_t,g acc_g + zero-point product.
+              constexpr int NG = D / 32;
               constexpr int SR = G::kScaleRowBytes;
               const uint32_t ksc = st + 2 * G::kTileBytes;
-              uint32_t sz0[D / 32], sz1[D / 32];
+              uint32_t w0[NG], w1[NG];               // codes of tokens q4, q4 + 8 per group
+              {
+                uint32_t r[4];
+                ldmatrix_x4(st + i4.k0, r);
+                if constexpr (D == 128) {
+                  w0[0] = r[0]; w0[1] = r[1]; w0[2] = r[2]; w0[3] = r[3];
+                  ldmatrix_x4(st + i4.k0 + kInt4K1, r);
+                  w1[0] = r[0]; w1[1] = r[1]; w1[2] = r[2]; w1[3] = r[3];
+                } else {
+                  w0[0] = r[0]; w0[1] = r[1]; w1[0] = r[2]; w1[1] = r[3];
+                }
+              }
+              uint32_t sz0[NG], sz1[NG];             // (scale, zero) words of tokens q4, q4 + 8
               if constexpr (D == 128) {
                 const uint4 a = ld_shared_v4(ksc + q4 * SR), c = ld_shared_v4(ksc + (q4 + 8) * SR);
                 sz0[0] = a.x; sz0[1] = a.y; sz0[2] = a.z; sz0[3] = a.w;
@@ -591,30 +645,41 @@ paged_decode_kernel(const Params p) {
                 const uint2 a = ld_shared_v2(ksc + q4 * SR), c = ld_shared_v2(ksc + (q4 + 8) * SR);
                 sz0[0] = a.x; sz0[1] = a.y; sz1[0] = c.x; sz1[1] = c.y;
               }
-#pragma unroll
-              for (int grp = 0; grp < D / 32; ++grp) {
-                const uint32_t w0 = ld_shared_b32(st + q4 * G::kRowBytes + 16 * (grp ^ swz<KV, D>(q4)) + 4 * c4);
-                const uint32_t w1 = ld_shared_b32(st + (q4 + 8) * G::kRowBytes +
-                                                  16 * (grp ^ swz<KV, D>(q4 + 8)) + 4 * c4);
-                float g4[4] = {0.f, 0.f, 0.f, 0.f};
-                // codes enter as f16 1024 + n (low nibbles) or 1024 + 16 n (high
-                // nibbles, met by q / 16); 1024 * sum(q as the mma sees it) is taken
-                // off the group sum
-                const uint32_t w0s = w0 >> 8, w1s = w1 >> 8;
-                const uint32_t a0[4] = {nib_lo_offset(w0), nib_lo_offset(w1),
-                                        nib_hi_offset(w0), nib_hi_offset(w1)};
-                mma_16816<PKV_F16>(g4, a0, qb[2 * grp][0], qb[2 * grp][1]);
-                const uint32_t a1[4] = {nib_lo_offset(w0s), nib_lo_offset(w1s),
-                                        nib_hi_offset(w0s), nib_hi_offset(w1s)};
-                mma_16816<PKV_F16>(g4, a1, qb[2 * grp + 1][0], qb[2 * grp + 1][1]);
-                const float2 f0 = Half16<PKV_F16>::unpack(sz0[grp]);   // (scale, zero) token q4
-                const float2 f1 = Half16<PKV_F16>::unpack(sz1[grp]);   // token q4 + 8
-                const float s0 = f0.x * qexp, s1 = f1.x * qexp;
-                sc[0] += s0 * (g4[0] - qoff[grp][0]) + f0.y * qsum[grp][0];
-                sc[1] += s0 * (g4[1] - qoff[grp][1]) + f0.y * qsum[grp][1];
-                sc[2] += s1 * (g4[2] - qoff[grp][0]) + f1.y * qsum[grp][0];
-                sc[3] += s1 * (g4[3] - qoff[grp][1]) + f1.y * qsum[grp][1];
+              // zero-point product: rows = tokens, k = the scale row's 16-bit
+              // columns (word c4 = scale and zero of group c4)
+              float zs[4] = {0.f, 0.f, 0.f, 0.f};
+              {
+                uint32_t za[4] = {0u, 0u, 0u, 0u};
+                if constexpr (D == 128) {
+                  uint32_t r[2];
+                  ldmatrix_x2(st + i4.kz, r);
+                  za[0] = r[0]; za[1] = r[1];
+                } else {
+                  if (c4 < NG) {
+                    za[0] = ld_shared_b32(ksc + q4 * SR + 4 * c4);
+                    za[1] = ld_shared_b32(ksc + (q4 + 8) * SR + 4 * c4);
+                  }
+                }
+                mma_16816<PKV_F16>(zs, za, zq[0], 0u);
+                mma_16816<PKV_F16>(zs, za, zq[1], 0u);
               }
+#pragma unroll
+              for (int grp = 0; grp < NG; ++grp) {
+                float g4[4] = {0.f, 0.f, 0.f, 0.f};
+                const uint32_t w0s = w0[grp] >> 8, w1s = w1[grp] >> 8;
+                const uint32_t a0[4] = {nib_lo(w0[grp]), nib_lo(w1[grp]), nib_hi(w0[grp]), nib_hi(w1[grp])};
+                mma_16816<PKV_F16>(g4, a0, qb[2 * grp][0], qb[2 * grp][1]);
+                const uint32_t a1[4] = {nib_lo(w0s), nib_lo(w1s), nib_hi(w0s), nib_hi(w1s)};
+                mma_16816<PKV_F16>(g4, a1, qb[2 * grp + 1][0], qb[2 * grp + 1][1]);
+                const float s0 = __low2float(*reinterpret_cast<const __half2*>(&sz0[grp]));
+                const float s1 = __low2float(*reinterpret_cast<const __half2*>(&sz1[grp]));
+                sc[0] += s0 * g4[0];
+                sc[1] += s0 * g4[1];
+                sc[2] += s1 * g4[2];
+                sc[3] += s1 * g4[3];
+              }
+#pragma unroll
+              for (int k = 0; k < 4; ++k) sc[k] = sc[k] * kq24 + zs[k] * zscale;
             }
 
 #pragma unroll
@@ -676,10 +741,7 @@ paged_decode_kernel(const Params p) {
           float alpha0 = fast_exp2(mrow[0] - mnew0), alpha1 = fast_exp2(mrow[1] - mnew1);
           mrow[0] = mnew0; mrow[1] = mnew1;
           lrow[0] *= alpha0; lrow[1] *= alpha1;
-          if constexpr (KV == PKV_INT4_G32) {
-#pragma unroll
-            for (int g = 0; g < D / 32; ++g) { zacc[g][0] *= alpha0; zacc[g][1] *= alpha1; }
-          }
+          if constexpr (KV == PKV_INT4_G32) { zc[0] *= alpha0; zc[1] *= alpha1; }
           if constexpr (is_fp8(KV)) {
             if (rebase) {
               // new reference: the tile's largest V scale; O_true = oacc * vref /
@@ -799,53 +861,81 @@ paged_decode_kernel(const Params p) {
                 }
               }
             } else {
-              // INT4: P'_g = p * scale_t,g per group g; zero point through sum_t z_t,g p_t
+              // INT4: O^T += V_codes^T P'_g^T per group g, with P'_g = p * scale_t,g
+              // formed on the B operand (f16), and the zero points through one
+              // more product: rows = the V scale row's 16-bit columns (scale and
+              // zero of each group), k = tokens, times P^T.
+              constexpr int NG = D / 32;
               constexpr int SR = G::kScaleRowBytes;
               const uint32_t vsc = st + 2 * G::kTileBytes + G::kScaleTileBytes;
-              uint32_t sz0[D / 32], sz1[D / 32];
-              if constexpr (D == 128) {
-                const uint4 a = ld_shared_v4(vsc + q4 * SR), c = ld_shared_v4(vsc + (q4 + 8) * SR);
-                sz0[0] = a.x; sz0[1] = a.y; sz0[2] = a.z; sz0[3] = a.w;
-                sz1[0] = c.x; sz1[1] = c.y; sz1[2] = c.z; sz1[3] = c.w;
-              } else {
-                const uint2 a = ld_shared_v2(vsc + q4 * SR), c = ld_shared_v2(vsc + (q4 + 8) * SR);
-                sz0[0] = a.x; sz0[1] = a.y; sz1[0] = c.x; sz1[1] = c.y;
-              }
-              if (partial) {
-                // rows past the context may hold stale scale bits: make them 0
+              using H = Half16<PKV_F16>;
+              // P^T as B fragments: head q4, tokens 2c4 + {0, 1} (bp0) and + 8 (bp1)
+              const uint32_t bp0 = movmatrix_trans(H::pack_rn(pr[0], pr[1]));
+              const uint32_t bp1 = movmatrix_trans(H::pack_rn(pr[2], pr[3]));
+              // P'_g = p * scale as B fragments: tokens (tA, tB) -> pb0, (tC, tE) -> pb1.
+              // One f16 rounding of p (above) and one of the product (2^-11 each).
+              // Rows past the context may hold stale scale bits (p is 0 there,
+              // but 0 * inf is not): their scales are masked to 0.
+              uint32_t pb0[NG], pb1[NG];
 #pragma unroll
-                for (int g = 0; g < D / 32; ++g) {
-                  if (!v0) sz0[g] = 0u;
-                  if (!v1) sz1[g] = 0u;
+              for (int half = 0; half < 2; ++half) {
+                const int t0 = half ? tC : tA, t1 = half ? tE : tB;
+                const uint32_t m0 = half ? mC : mA, m1 = half ? mE : mB;
+                uint32_t s0[NG], s1[NG];
+                if constexpr (D == 128) {
+                  const uint4 a = ld_shared_v4(vsc + t0 * SR), c = ld_shared_v4(vsc + t1 * SR);
+                  s0[0] = a.x; s0[1] = a.y; s0[2] = a.z; s0[3] = a.w;
+                  s1[0] = c.x; s1[1] = c.y; s1[2] = c.z; s1[3] = c.w;
+                } else {
+                  const uint2 a = ld_shared_v2(vsc + t0 * SR), c = ld_shared_v2(vsc + t1 * SR);
+                  s0[0] = a.x; s0[1] = a.y; s1[0] = c.x; s1[1] = c.y;
+                }
+#pragma unroll
+                for (int g = 0; g < NG; ++g) {
+                  const uint32_t sp = __byte_perm(s0[g] & m0, s1[g] & m1, 0x5410);
+                  (half ? pb1 : pb0)[g] = hmul2(half ? bp1 : bp0, sp);
                 }
               }
-              using H = Half16<PKV_F16>;
+              // the zero-point product's A operand: column q4 of the scale rows of
+              // tokens (tA, tB) and (tC, tE)
+              uint32_t zr[2];
+              if constexpr (D == 128) {
+                ldmatrix_x2_trans(st + i4.kz + G::kScaleTileBytes, zr);
+              } else {
+                zr[0] = zr[1] = 0u;
+                if (q4 < 2 * NG) {
+                  zr[0] = __byte_perm(ld_shared_u16(vsc + tA * SR + 2 * q4),
+                                      ld_shared_u16(vsc + tB * SR + 2 * q4), 0x5410);
+                  zr[1] = __byte_perm(ld_shared_u16(vsc + tC * SR + 2 * q4),
+                                      ld_shared_u16(vsc + tE * SR + 2 * q4), 0x5410);
+                }
+              }
+              zr[0] &= (mA & 0xFFFFu) | (mB & 0xFFFF0000u);
+              zr[1] &= (mC & 0xFFFFu) | (mE & 0xFFFF0000u);
+              {
+                const uint32_t za[4] = {zr[0], 0u, zr[1], 0u};
+                mma_16816<PKV_F16>(zc, za, bp0, bp1);
+              }
+              // codes: x = tokens (tA, tB), y = (tC, tE), 2 bytes each (d = 32 g + 4 q4 + 0..3)
+              uint32_t xv[NG], yv[NG];
+              {
+                uint32_t r[4];
+                ldmatrix_x4_trans(st + i4.v0, r);
+                xv[0] = r[0]; yv[0] = r[1]; xv[1] = r[2]; yv[1] = r[3];
+                if constexpr (D == 128) {
+                  ldmatrix_x4_trans(st + i4.v1, r);
+                  xv[2] = r[0]; yv[2] = r[1]; xv[3] = r[2]; yv[3] = r[3];
+                }
+              }
 #pragma unroll
-              for (int grp = 0; grp < D / 32; ++grp) {
-                const float2 f0 = H::unpack(sz0[grp]), f1 = H::unpack(sz1[grp]);
-                const float pp0 = pr[0] * f0.x, pp1 = pr[1] * f0.x;
-                const float pp2 = pr[2] * f1.x, pp3 = pr[3] * f1.x;
-                zacc[grp][0] += pr[0] * f0.y + pr[2] * f1.y;
-                zacc[grp][1] += pr[1] * f0.y + pr[3] * f1.y;
-                // one f16 rounding of P' (relative 2^-11): the output moves by at most
-                // 2^-11 * the largest group range, far below the quantization step
-                const uint32_t bh0 = movmatrix_trans(H::pack_rn(pp0, pp1));
-                const uint32_t bh1 = movmatrix_trans(H::pack_rn(pp2, pp3));
-                const uint32_t rowoff = 2 * q4;
-                const uint32_t hA = ld_shared_u16(vt + tA * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tA)) + rowoff);
-                const uint32_t hB = ld_shared_u16(vt + tB * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tB)) + rowoff);
-                const uint32_t hC = ld_shared_u16(vt + tC * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tC)) + rowoff);
-                const uint32_t hE = ld_shared_u16(vt + tE * G::kRowBytes + 16 * (grp ^ swz<KV, D>(tE)) + rowoff);
-                // token pairs (tA, tB), (tC, tE) side by side; rows q4 + 8 (odd d)
-                // take the high nibbles as 16 n, undone once in the epilogue
-                const uint32_t x = __byte_perm(hA, hB, 0x5410), y = __byte_perm(hC, hE, 0x5410);
-                const uint32_t xs = x >> 8, ys = y >> 8;
-                const uint32_t a0[4] = {sub1024(nib_lo_offset(x)), sub1024(nib_hi_offset(x)),
-                                        sub1024(nib_lo_offset(y)), sub1024(nib_hi_offset(y))};
-                mma_16816<PKV_F16>(oacc[2 * grp], a0, bh0, bh1);
-                const uint32_t a1[4] = {sub1024(nib_lo_offset(xs)), sub1024(nib_hi_offset(xs)),
-                                        sub1024(nib_lo_offset(ys)), sub1024(nib_hi_offset(ys))};
-                mma_16816<PKV_F16>(oacc[2 * grp + 1], a1, bh0, bh1);
+              for (int grp = 0; grp < NG; ++grp) {
+                const uint32_t b0 = pb0[grp], b1 = pb1[grp];
+                // rows q4 (even d) take n 2^-24, rows q4 + 8 (odd d) 16 n 2^-24
+                const uint32_t x = xv[grp], y = yv[grp], xs = x >> 8, ys = y >> 8;
+                const uint32_t a0[4] = {nib_lo(x), nib_hi(x), nib_lo(y), nib_hi(y)};
+                mma_16816<PKV_F16>(oacc[2 * grp], a0, b0, b1);
+                const uint32_t a1[4] = {nib_lo(xs), nib_hi(xs), nib_lo(ys), nib_hi(ys)};
+                mma_16816<PKV_F16>(oacc[2 * grp + 1], a1, b0, b1);
               }
             }
             }  // v_on
@@ -863,27 +953,26 @@ paged_decode_kernel(const Params p) {
       lrow[0] += __shfl_xor_sync(0xffffffffu, lrow[0], o);
       lrow[1] += __shfl_xor_sync(0xffffffffu, lrow[1], o);
     }
-    float post = 1.f / kPScale;
+    // INT4 codes entered as n 2^-24 (rows q4 + 8, odd d: 16 n 2^-24)
+    float post = (KV == PKV_INT4_G32) ? 16777216.f : 1.f / kPScale;
     if constexpr (is_fp8(KV)) post *= vref;
+    const float post_odd = (KV == PKV_INT4_G32) ? 1048576.f : post;
 #pragma unroll
-    for (int i = 0; i < MT; ++i)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) oacc[i][k] *= post;
+    for (int i = 0; i < MT; ++i) {
+      oacc[i][0] *= post; oacc[i][1] *= post;
+      oacc[i][2] *= post_odd; oacc[i][3] *= post_odd;
+    }
     if constexpr (KV == PKV_INT4_G32) {
-      // rows q4 + 8 (odd d) carried their V codes as 16 n
-#pragma unroll
-      for (int i = 0; i < MT; ++i) { oacc[i][2] *= 0.0625f; oacc[i][3] *= 0.0625f; }
+      // zero-point sums: row 2g + 1 of the product (lane (2g + 1) * 4 + c4)
+      // holds group g for this thread's heads 2c4, 2c4 + 1
 #pragma unroll
       for (int g = 0; g < D / 32; ++g) {
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-          zacc[g][0] += __shfl_xor_sync(0xffffffffu, zacc[g][0], o);
-          zacc[g][1] += __shfl_xor_sync(0xffffffffu, zacc[g][1], o);
-        }
-        oacc[2 * g][0] += zacc[g][0]; oacc[2 * g][2] += zacc[g][0];
-        oacc[2 * g][1] += zacc[g][1]; oacc[2 * g][3] += zacc[g][1];
-        oacc[2 * g + 1][0] += zacc[g][0]; oacc[2 * g + 1][2] += zacc[g][0];
-        oacc[2 * g + 1][1] += zacc[g][1]; oacc[2 * g + 1][3] += zacc[g][1];
+        const float z0 = __shfl_sync(0xffffffffu, zc[0], (2 * g + 1) * 4 + c4);
+        const float z1 = __shfl_sync(0xffffffffu, zc[1], (2 * g + 1) * 4 + c4);
+        oacc[2 * g][0] += z0; oacc[2 * g][2] += z0;
+        oacc[2 * g][1] += z1; oacc[2 * g][3] += z1;
+        oacc[2 * g + 1][0] += z0; oacc[2 * g + 1][2] += z0;
+        oacc[2 * g + 1][1] += z1; oacc[2 * g + 1][3] += z1;
       }
     }
 
