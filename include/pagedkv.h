@@ -121,7 +121,8 @@ int paged_kv_write(const void* k_new, const void* v_new, int new_dtype,
  * call, forces one (for testing; results agree to rounding).
  * Supported: head_dim in {64, 128}; num_q_heads / num_kv_heads <= 8;
  * block_size a multiple of 16 up to 256; F16/BF16 caches need q_dtype equal
- * to kv_dtype; FP8/INT4 caches take F16 or BF16 q.
+ * to kv_dtype; FP8/INT4 caches take F16 or BF16 q; num_blocks * num_kv_heads
+ * below 2^27 (PKV_ERR_UNSUPPORTED otherwise).
  */
 int paged_decode_attention(const void* q, int q_dtype,
                            const void* k_cache, const void* v_cache,

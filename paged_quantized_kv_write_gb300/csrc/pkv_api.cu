@@ -90,6 +90,8 @@ int paged_decode_attention(const void* q, int q_dtype,
   if (num_q_heads / num_kv_heads > 8) return PKV_ERR_UNSUPPORTED;
   if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(max_blocks_per_seq) * block_size > 0x7FFFFFFF) return PKV_ERR_UNSUPPORTED;
+  // the kernel locates a 16-token sub-tile as (block * Hkv + head) << 4 | offset / 16
+  if (static_cast<int64_t>(num_blocks) * num_kv_heads >= (int64_t(1) << 27)) return PKV_ERR_UNSUPPORTED;
   if (!(softmax_scale == softmax_scale)) return PKV_ERR_INVALID_ARG;
   if (num_seqs == 0) return PKV_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)

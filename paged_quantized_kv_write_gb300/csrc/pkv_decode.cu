@@ -54,7 +54,7 @@ namespace {
 #define PKV_STAGES_FP8 2
 #endif
 #ifndef PKV_STAGES_INT4
-#define PKV_STAGES_INT4 3
+#define PKV_STAGES_INT4 2
 #endif
 // CTAs per SM the register allocation must allow (__launch_bounds__ minimum)
 #ifndef PKV_MINB_HALF
@@ -62,6 +62,9 @@ namespace {
 #endif
 #ifndef PKV_MINB_QUANT
 #define PKV_MINB_QUANT 3
+#endif
+#ifndef PKV_MINB_INT4
+#define PKV_MINB_INT4 PKV_MINB_QUANT
 #endif
 
 #ifndef PKV_DECODE_WARPS
@@ -91,6 +94,9 @@ constexpr int kMaxDevices = 64;
 #ifndef PKV_SUB_QUANT
 #define PKV_SUB_QUANT 2
 #endif
+#ifndef PKV_SUB_INT4
+#define PKV_SUB_INT4 PKV_SUB_QUANT
+#endif
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int KV, int D> struct Geo {
@@ -102,7 +108,7 @@ template <int KV, int D> struct Geo {
   static constexpr int kScaleTileBytes = kTile * kScaleRowBytes;
   // A stage holds kSub 16-token sub-tiles, each K rows | V rows | K scale rows |
   // V scale rows, then 16 B of misc per sub-tile (FP8 K and V scale, valid flag).
-  static constexpr int kSub = kHalf ? PKV_SUB_HALF : PKV_SUB_QUANT;
+  static constexpr int kSub = kHalf ? PKV_SUB_HALF : (KV == PKV_INT4_G32 ? PKV_SUB_INT4 : PKV_SUB_QUANT);
   static constexpr int kTileTok = kTile * kSub;                 // tokens per stage
   static constexpr int kSubBytes = 2 * kTileBytes + 2 * kScaleTileBytes;
   static constexpr int kMiscOffset = kSub * kSubBytes;
@@ -115,7 +121,8 @@ template <int KV, int D> struct Geo {
   static constexpr int kMbStride = (D / 16) * 4 + 5;
   static constexpr int kMbufBytes = kWarp * kMbStride * 4;
   static constexpr int kSmemBytes = kRingBytes + kMbufBytes;
-  static constexpr int kMinBlocks = kHalf ? PKV_MINB_HALF : PKV_MINB_QUANT;
+  static constexpr int kMinBlocks =
+      kHalf ? PKV_MINB_HALF : (KV == PKV_INT4_G32 ? PKV_MINB_INT4 : PKV_MINB_QUANT);
 };
 
 // 2^x on the SFU (ex2.approx; 2^-inf = +0).  Scores and probabilities use it
@@ -200,26 +207,25 @@ struct Params {
   float softmax_scale;
 };
 
-// Issue the copies of one 16-token sub-tile (tokens [t0, t0 + 16) of the
-// sequence) into its place in a stage (lane-parallel).  `stage` is the
-// sub-tile's shared-memory base, `misc_smem`/`misc` its 16-byte misc slot.
-// Sub-tiles past the unit's end copy nothing and are marked empty.
+// Issue the copies of one 16-token sub-tile into its place in a stage
+// (lane-parallel).  `rowp` locates it: (physical block * Hkv + kvh) << 4 |
+// (offset in the block / 16), or -1 for a block id out of range; `live` is
+// false past the unit's end.  `stage` is the sub-tile's shared-memory base,
+// `misc_smem`/`misc` its 16-byte misc slot.  Sub-tiles that copy nothing are
+// marked empty.
 template <int KV, int D>
-__device__ __forceinline__ void issue_tile(const Params& p, int kvh, int t0, int tok_end, int phys,
-                                           uint32_t stage, uint32_t misc_smem, int* misc,
-                                           int lane) {
+__device__ __forceinline__ void issue_tile(const Params& p, int rowp, bool live, uint32_t stage,
+                                           uint32_t misc_smem, int* misc, int lane) {
   using G = Geo<KV, D>;
-  const int logical = t0 / p.block_size;
-  const bool live = t0 < tok_end;
-  const bool ok = phys >= 0 && phys < p.num_blocks;
+  const bool ok = rowp >= 0;
   if (lane == 0) misc[2] = (live && ok) ? 1 : 0;
   if (!live) return;
   if (!ok) {
     if (lane == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
     return;
   }
-  const int off = t0 - logical * p.block_size;
-  const int64_t row0 = (static_cast<int64_t>(phys) * p.num_kv_heads + kvh) * p.block_size + off;
+  const int blk = rowp >> 4;                               // physical block * Hkv + kvh
+  const int64_t row0 = static_cast<int64_t>(blk) * p.block_size + ((rowp & 15) << 4);
   const uint8_t* ksrc = p.k_cache + row0 * G::kRowBytes;
   const uint8_t* vsrc = p.v_cache + row0 * G::kRowBytes;
   constexpr int kChunks = G::kTileBytes / 16;
@@ -249,7 +255,7 @@ __device__ __forceinline__ void issue_tile(const Params& p, int kvh, int t0, int
     }
   } else if constexpr (is_fp8(KV)) {
     const float* sc = static_cast<const float*>(p.scales);
-    const int64_t idx = static_cast<int64_t>(phys) * p.num_kv_heads + kvh;
+    const int64_t idx = blk;
     const int64_t per_kv = static_cast<int64_t>(p.num_blocks) * p.num_kv_heads;
     const uint32_t mo = misc_smem;
     if (lane == 0) asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(mo), "l"(sc + idx) : "memory");
@@ -470,10 +476,12 @@ paged_decode_kernel(const Params p) {
 
   // ---------------------------------------------------------------- issue cursor
   // Walks (unit, tile) pairs with tile = warp, warp + W, ... < ntiles, in unit
-  // order.  The physical block ids of the warp's 16-token sub-tiles of a unit
-  // are loaded 32 at a time into a register (lane l of window k: the warp's
+  // order.  The cache rows of the warp's 16-token sub-tiles of a unit are
+  // looked up 32 at a time, one per lane (lane l of window k: the warp's
   // sub-tile 32k + l, i.e. sub-tile (32k + l) % kSub of its tile (32k + l) /
-  // kSub); window 0 of the next unit is prefetched on entering a unit.
+  // kSub), as (physical block * Hkv + kvh) << 4 | (offset in the block / 16),
+  // or -1 when the sub-tile is past the unit or its block id is out of range;
+  // window 0 of the next unit is prefetched on entering a unit.
   int iu = -1, it = 0, i_tb = 0, i_next_tb = -1, i_win = 0;
   Unit iunit;
   iunit.ntiles = 0;
@@ -483,7 +491,10 @@ paged_decode_kernel(const Params p) {
     const int tok = u.tok_begin + tile * G::kTileTok + (sidx % G::kSub) * kTile;
     if (tile >= u.ntiles || tok >= u.tok_end) return -1;
     const int32_t* trow = p.block_tables + static_cast<int64_t>(u.b) * p.max_blocks_per_seq;
-    return __ldg(trow + tok / p.block_size);
+    const int logical = tok / p.block_size;
+    const int phys = __ldg(trow + logical);
+    if (phys < 0 || phys >= p.num_blocks) return -1;
+    return ((phys * p.num_kv_heads + u.kvh) << 4) | ((tok - logical * p.block_size) >> 4);
   };
   auto next_window_unit = [&](int j) -> int {          // window 0 of unit j (or -1s)
     return j < nunits ? window(make_unit<G::kTileTok>(p, b, kvh, ctx, part_of(j)), 0) : -1;
@@ -507,23 +518,21 @@ paged_decode_kernel(const Params p) {
     }
     return true;
   };
-  int issued = 0;                                        // pairs issued so far (ring position)
+  int s_issue = 0;                                       // ring stage the next pair goes to
   auto issue_next = [&]() {
     if (issue_advance()) {
       const int k = (it - kFirst) / kStride * G::kSub;
-      const int s = issued % G::kStages;
-      const uint32_t sb = ring + s * G::kStageBytes;
-      uint8_t* sp = ring_ptr + s * G::kStageBytes;
+      const uint32_t sb = ring + s_issue * G::kStageBytes;
+      uint8_t* sp = ring_ptr + s_issue * G::kStageBytes;
 #pragma unroll
       for (int u = 0; u < G::kSub; ++u) {
-        const int phys = __shfl_sync(0xffffffffu, i_tb, (k + u) & 31);
-        issue_tile<KV, D>(p, iunit.kvh, iunit.tok_begin + it * G::kTileTok + u * kTile,
-                          iunit.tok_end, phys, sb + u * G::kSubBytes,
-                          sb + G::kMiscOffset + 16 * u,
+        const int rowp = __shfl_sync(0xffffffffu, i_tb, (k + u) & 31);
+        issue_tile<KV, D>(p, rowp, iunit.tok_begin + it * G::kTileTok + u * kTile < iunit.tok_end,
+                          sb + u * G::kSubBytes, sb + G::kMiscOffset + 16 * u,
                           reinterpret_cast<int*>(sp + G::kMiscOffset + 16 * u), lane);
       }
     }
-    ++issued;
+    s_issue = s_issue + 1 == G::kStages ? 0 : s_issue + 1;
     cp_async_commit();
   };
   // the first advance enters unit 0 (it + W >= ntiles = 0) with its prefetched window
@@ -544,7 +553,7 @@ paged_decode_kernel(const Params p) {
   float mrow[2], lrow[2];
   float zc[4];                               // INT4: zero-point sums (C fragment)
   float vref, inv_vref;                      // FP8: oacc is in units of vref / kPScale
-  int consumed = 0;                          // pairs computed so far (ring position)
+  int s_cons = 0;                            // ring stage of the next pair to compute
   load_q<KV, QT, D>(p, make_unit<G::kTileTok>(p, b, kvh, ctx, part_of(0)), q4, c4, qb, qexp, zq, zscale);
 
 #pragma unroll 1
@@ -565,7 +574,7 @@ paged_decode_kernel(const Params p) {
     for (int ct = kFirst; ct < unit.ntiles; ct += kStride) {
       cp_async_wait<G::kStages - 1>();
       __syncwarp();
-      const int stage = consumed % G::kStages;
+      const int stage = s_cons;
       const uint32_t stb = ring + stage * G::kStageBytes;
       const uint8_t* st_ptr = ring_ptr + stage * G::kStageBytes;
       const int* misc0 = reinterpret_cast<const int*>(st_ptr + G::kMiscOffset);
@@ -766,7 +775,6 @@ paged_decode_kernel(const Params p) {
         for (int u = 0; u < G::kSub; ++u) {
           const uint32_t st = stb + u * G::kSubBytes;
           const int nvalid = nval[u];
-          const bool v0 = q4 < nvalid, v1 = q4 + 8 < nvalid;
           const bool v_on = von[u];
           const float pr[4] = {fast_exp2(scs[u][0] - mrow[0]), fast_exp2(scs[u][1] - mrow[1]),
                                fast_exp2(scs[u][2] - mrow[0]), fast_exp2(scs[u][3] - mrow[1])};
@@ -875,12 +883,14 @@ paged_decode_kernel(const Params p) {
               // P'_g = p * scale as B fragments: tokens (tA, tB) -> pb0, (tC, tE) -> pb1.
               // One f16 rounding of p (above) and one of the product (2^-11 each).
               // Rows past the context may hold stale scale bits (p is 0 there,
-              // but 0 * inf is not): their scales are masked to 0.
+              // but 0 * inf is not): their products and zeros are masked to 0.
+              // (one mask per B register: low half token tA / tC, high half tB / tE)
+              const uint32_t mAB = (mA & 0xFFFFu) | (mB & 0xFFFF0000u);
+              const uint32_t mCE = (mC & 0xFFFFu) | (mE & 0xFFFF0000u);
               uint32_t pb0[NG], pb1[NG];
 #pragma unroll
               for (int half = 0; half < 2; ++half) {
                 const int t0 = half ? tC : tA, t1 = half ? tE : tB;
-                const uint32_t m0 = half ? mC : mA, m1 = half ? mE : mB;
                 uint32_t s0[NG], s1[NG];
                 if constexpr (D == 128) {
                   const uint4 a = ld_shared_v4(vsc + t0 * SR), c = ld_shared_v4(vsc + t1 * SR);
@@ -891,10 +901,9 @@ paged_decode_kernel(const Params p) {
                   s0[0] = a.x; s0[1] = a.y; s1[0] = c.x; s1[1] = c.y;
                 }
 #pragma unroll
-                for (int g = 0; g < NG; ++g) {
-                  const uint32_t sp = __byte_perm(s0[g] & m0, s1[g] & m1, 0x5410);
-                  (half ? pb1 : pb0)[g] = hmul2(half ? bp1 : bp0, sp);
-                }
+                for (int g = 0; g < NG; ++g)
+                  (half ? pb1 : pb0)[g] =
+                      hmul2(half ? bp1 : bp0, __byte_perm(s0[g], s1[g], 0x5410)) & (half ? mCE : mAB);
               }
               // the zero-point product's A operand: column q4 of the scale rows of
               // tokens (tA, tB) and (tC, tE)
@@ -910,8 +919,8 @@ paged_decode_kernel(const Params p) {
                                       ld_shared_u16(vsc + tE * SR + 2 * q4), 0x5410);
                 }
               }
-              zr[0] &= (mA & 0xFFFFu) | (mB & 0xFFFF0000u);
-              zr[1] &= (mC & 0xFFFFu) | (mE & 0xFFFF0000u);
+              zr[0] &= mAB;
+              zr[1] &= mCE;
               {
                 const uint32_t za[4] = {zr[0], 0u, zr[1], 0u};
                 mma_16816<PKV_F16>(zc, za, bp0, bp1);
@@ -944,7 +953,7 @@ paged_decode_kernel(const Params p) {
 
       __syncwarp();
       issue_next();
-      ++consumed;
+      s_cons = s_cons + 1 == G::kStages ? 0 : s_cons + 1;
     }
 
     // -------------------------------------------------------------- unit epilogue

@@ -64,6 +64,9 @@ def test_host_validation_without_gpu(lib):
     # misaligned q
     assert L.paged_decode_attention(V(0x10002), 1, fake, fake, fake, 4, fake, 2, None, 1, 10,
                                     fake, 0.1, 8, 2, 128, 16, 0, None, 0, None, None) == 1
+    # a pool of 2^27 (block, KV head) pairs or more
+    assert L.paged_decode_attention(fake, 1, fake, fake, fake, 4, fake, 2, None, 1, 1 << 24, fake,
+                                    0.1, 64, 8, 128, 16, 0, None, 0, None, None) == 2
     # split-KV without workspace
     assert L.paged_decode_attention(fake, 1, fake, fake, fake, 400, fake, 2, None, 1, 10, fake,
                                     0.1, 8, 2, 128, 16, 64, None, 0, None, None) == 5
