@@ -330,6 +330,82 @@ def run_ours(args, rank: int, world: int):
     return result
 
 
+def run_copy(args, rank: int, world: int):
+    """Copy-on-write block copies: time paged_kv_copy_blocks moving --copy-pairs
+    random (src, dst) blocks of the workload's pool per step (K, V and scales)."""
+    import torch
+    import paged_quantized_kv_write_gb300 as pkv
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = W.CONFIGS[args.config]
+    if args.kv_dtype:
+        w = _with_kv_dtype(w, args.kv_dtype)
+    case = W.make_case(w)
+    nb = case.num_blocks
+    n = min(args.copy_pairs, nb // 2)
+    rng = np.random.default_rng(7)
+    perm = rng.permutation(nb)
+    pairs = torch.from_numpy(np.stack([perm[:n], perm[n:2 * n]], 1).astype(np.int32)).to(dev)
+    k, v, s = pkv.alloc_cache(w.kv_dtype, nb, w.num_kv_heads, w.head_dim, w.block_size,
+                              device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    per_block = 2 * w.num_kv_heads * w.block_size * pkv.row_bytes(w.kv_dtype, w.head_dim)
+    if w.kv_dtype in W.FP8_TYPES:
+        per_block += 2 * 4 * w.num_kv_heads
+    elif w.kv_dtype == W.INT4_G32:
+        per_block += 2 * w.num_kv_heads * w.block_size * (w.head_dim // 32) * 4
+    step_bytes = 2 * n * per_block                   # read the sources, write the copies
+
+    def copy(st):
+        pkv.paged_kv_copy_blocks(k, v, s, w.kv_dtype, pairs, w.block_size, w.head_dim, status, st)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            copy(stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        copy(stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        _barrier(world)
+        clocks = ClockSampler(dev.index)
+        clocks.start()
+        time.sleep(0.3)
+        for a, b in ev:
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        clk = clocks.stop()
+    dev_ms = _max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), world)
+    assert status.item() == 0
+    peak, peak_kind = _peaks()
+    gbs = whole_job_rate(step_bytes, args.steps, dev_ms, world) / 1e9
+    return {
+        "metric": "paged KV block copy GB/s (bytes read + written), 1 GPU",
+        "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dev_ms / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": W.DTYPE_NAMES[w.kv_dtype], "data": "synthetic pool (zeros), random disjoint pairs",
+        "config": {"workload": f"config {args.config}: {w.name}, {n} block copies per step",
+                   "num_blocks": nb, "pairs": n, "bytes_per_block_copy": per_block,
+                   "l2": "moves far more than L2 per step (no flush)"},
+        "roofline": {"kernel": "copy_blocks_kernel", "bound": "hbm",
+                     "achieved": round(gbs / world, 2), "peak": peak,
+                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                     "unit": "GB/s", "frac": round(gbs / world / peak, 4), "traffic": None},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+
+
 def _traffic(config: int):
     """DRAM bytes per launch of the decode kernel from a committed ncu summary, if one
     exists for this workload and the current kernel source."""
@@ -478,6 +554,10 @@ def main():
                     help="override the workload's block size (block-size sweep; 0: keep)")
     ap.add_argument("--kv-dtype", default="", choices=[""] + sorted(W.DTYPE_NAMES.values()),
                     help="override the workload's cache dtype (dtype comparison; empty: keep)")
+    ap.add_argument("--op", default="step", choices=["step", "copy"],
+                    help="step: the decode step (default); copy: copy-on-write block copies")
+    ap.add_argument("--copy-pairs", type=int, default=4096,
+                    help="--op copy: block pairs copied per step")
     ap.add_argument("--partition", type=int, default=0,
                     help="override the workload's split-KV partition size (0: keep)")
     args = ap.parse_args()
@@ -496,6 +576,14 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
+    if args.op == "copy":
+        res = run_copy(args, rank, world)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     res = run_ours(args, rank, world)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:

@@ -95,6 +95,32 @@ int paged_kv_write(const void* k_new, const void* v_new, int new_dtype,
                    int num_blocks, int num_kv_heads, int head_dim, int block_size,
                    int* dev_status, void* stream);
 
+/* paged_kv_copy_blocks — copy whole physical blocks within the pool
+ * (copy-on-write and beam-search forks: "KV Cache Compression & Paged
+ * Attention Deep Dive", myaihardware page, sections "PagedAttention:
+ * Operating System-Inspired Memory Management for LLMs" and "Implementation
+ * Details: PagedAttention Kernel and Page Table").  The block manager keeps
+ * the reference counts and picks the pairs; this call moves the bytes.
+ *
+ * block_pairs    int32 [num_pairs][2] (src, dst), device memory.  For each
+ *                pair, block dst of k_cache and v_cache (all KV heads) and its
+ *                scales (FP8: the per-head K and V scales; INT4: every
+ *                (scale, zero) pair of the block) become byte copies of block
+ *                src's, so dst dequantizes to exactly what src did.  src == dst
+ *                is a no-op; an id outside [0, num_blocks) skips the pair and
+ *                flags PKV_ERR_DEVICE_BOUNDS in dev_status.  No block may be
+ *                both a source and a destination in one call, and destinations
+ *                must be distinct (otherwise the result depends on the order
+ *                the GPU runs the pairs in).
+ * k_cache, v_cache, scales, kv_dtype, num_blocks, num_kv_heads, head_dim,
+ * block_size     the pool, as for paged_kv_write.
+ * Host-visible errors as for paged_kv_write; 0 pairs is a no-op.
+ */
+int paged_kv_copy_blocks(void* k_cache, void* v_cache, void* scales, int kv_dtype,
+                         const int32_t* block_pairs, int num_pairs, int num_blocks,
+                         int num_kv_heads, int head_dim, int block_size, int* dev_status,
+                         void* stream);
+
 /* paged_decode_attention — one decode step over a paged, optionally
  * quantized KV cache (the PagedAttention kernel of the myaihardware page,
  * "Implementation Details": per head, walk the logical blocks, translate

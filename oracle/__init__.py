@@ -60,6 +60,8 @@ def lib() -> ctypes.CDLL:
         L.oracle_decode_attention_pairs.restype = I32
         L.oracle_dequant_row.argtypes = [P, P, I32, I32, I32, I32, I32, I32, I32, I32, I32, P]
         L.oracle_dequant_row.restype = I32
+        L.oracle_copy_blocks.argtypes = [P, P, P, I32, P, I32, I32, I32, I32, I32]
+        L.oracle_copy_blocks.restype = I32
         L.oracle_max_threads.argtypes = []
         L.oracle_max_threads.restype = I32
         _lib = L
@@ -148,6 +150,18 @@ def kv_write(k_new, v_new, new_dtype, slot_mapping, k_cache, v_cache, scales, kv
                               num_kv_heads, head_dim, block_size)
     if r:
         raise ValueError(f"oracle_kv_write rejected its arguments ({r})")
+
+
+def copy_blocks(k_cache, v_cache, scales, kv_dtype, pairs, num_blocks, num_kv_heads, head_dim,
+                block_size) -> int:
+    """Block dst of each (src, dst) pair becomes a copy of block src; returns the
+    number of pairs skipped for an out-of-range id."""
+    pr = np.ascontiguousarray(pairs, np.int32).reshape(-1, 2)
+    r = lib().oracle_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(scales), kv_dtype, _ptr(pr),
+                                 len(pr), num_blocks, num_kv_heads, head_dim, block_size)
+    if r < 0:
+        raise ValueError("oracle_copy_blocks rejected its arguments")
+    return r
 
 
 def decode_attention(q, q_dtype, k_cache, v_cache, block_tables, context_lens, scales,

@@ -294,6 +294,56 @@ static int check_geometry(int kv_dtype, int num_blocks, int num_kv_heads, int he
     return 0;
 }
 
+/* ------------------------------------------------------------ block copies */
+
+/* Copy-on-write / beam fork ("KV Cache Compression & Paged Attention Deep
+ * Dive", sections "PagedAttention: Operating System-Inspired Memory
+ * Management for LLMs" and "Implementation Details"): for each (src, dst)
+ * pair in order, every K and V row of every head of block dst, and the
+ * scales that belong to those rows, become those of block src.  Pairs with
+ * an id outside [0, num_blocks) are skipped; the return value counts them
+ * (negative on a bad argument). */
+int oracle_copy_blocks(void* k_cache, void* v_cache, void* scales, int kv_dtype,
+                       const int32_t* pairs, int num_pairs, int num_blocks, int num_kv_heads,
+                       int head_dim, int block_size) {
+    if (check_geometry(kv_dtype, num_blocks, num_kv_heads, head_dim, block_size)) return -1;
+    if (num_pairs < 0) return -1;
+    int64_t rb = row_bytes(kv_dtype, head_dim);
+    int skipped = 0;
+    for (int i = 0; i < num_pairs; ++i) {
+        int32_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+            ++skipped;
+            continue;
+        }
+        for (int which = 0; which < 2; ++which) {
+            uint8_t* cache = (uint8_t*)(which ? v_cache : k_cache);
+            for (int h = 0; h < num_kv_heads; ++h) {
+                for (int o = 0; o < block_size; ++o)
+                    memmove(cache + row_index(dst, h, o, num_kv_heads, block_size) * rb,
+                            cache + row_index(src, h, o, num_kv_heads, block_size) * rb,
+                            (size_t)rb);
+                if (is_fp8(kv_dtype))
+                    *fp8_scale_ptr(scales, which, dst, h, num_blocks, num_kv_heads) =
+                        *fp8_scale_ptr(scales, which, src, h, num_blocks, num_kv_heads);
+                if (kv_dtype == DT_INT4)
+                    for (int o = 0; o < block_size; ++o)
+                        for (int g = 0; g < head_dim / 32; ++g) {
+                            uint16_t* d = int4_pair_ptr(scales, which, dst, h, o, g, num_blocks,
+                                                        num_kv_heads, block_size, head_dim);
+                            const uint16_t* sp = int4_pair_ptr(scales, which, src, h, o, g,
+                                                               num_blocks, num_kv_heads,
+                                                               block_size, head_dim);
+                            d[0] = sp[0];
+                            d[1] = sp[1];
+                        }
+            }
+        }
+    }
+    return skipped;
+}
+
+
 /* Encode one token row of one head (R4-R6).  x: the row as fp32 values. */
 static void encode_row(const float* x, int head_dim, int kv_dtype, uint8_t* dst,
                        int fresh_fp8_block, float* fp8_scale, uint16_t* int4_pairs) {

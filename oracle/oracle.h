@@ -43,6 +43,12 @@ int oracle_kv_write(const uint16_t* k_new, const uint16_t* v_new, int new_dtype,
                     void* k_cache, void* v_cache, void* scales, int kv_dtype,
                     int num_blocks, int num_kv_heads, int head_dim, int block_size);
 
+/* whole-block copies (src, dst) pairs [num_pairs][2]: the number of pairs
+ * skipped for an out-of-range id, negative on a bad argument */
+int oracle_copy_blocks(void* k_cache, void* v_cache, void* scales, int kv_dtype,
+                       const int32_t* pairs, int num_pairs, int num_blocks, int num_kv_heads,
+                       int head_dim, int block_size);
+
 /* decode attention into fp64 out [num_seqs, num_q_heads, head_dim] */
 int oracle_decode_attention(const uint16_t* q, int q_dtype,
                             const void* k_cache, const void* v_cache,

@@ -39,6 +39,8 @@ def _load() -> ctypes.CDLL:
                         ctypes.c_size_t)
     lib.paged_kv_write.argtypes = [P, P, I, P, I64, P, P, P, I, I, I, I, I, P, P]
     lib.paged_kv_write.restype = I
+    lib.paged_kv_copy_blocks.argtypes = [P, P, P, I, P, I, I, I, I, I, P, P]
+    lib.paged_kv_copy_blocks.restype = I
     lib.paged_decode_attention.argtypes = [P, I, P, P, P, I, P, I, P, I, I, P, F, I, I, I, I, I,
                                            P, SZ, P, P]
     lib.paged_decode_attention.restype = I
@@ -122,6 +124,23 @@ def paged_kv_write(k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch
                             _ptr(dev_status), _stream(stream))
     if r != PKV_OK:
         raise PagedKVError(r, "paged_kv_write")
+
+
+def paged_kv_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor,
+                         scales: Optional[torch.Tensor], kv_dtype: int, block_pairs: torch.Tensor,
+                         block_size: int, head_dim: int, dev_status: Optional[torch.Tensor] = None,
+                         stream=None) -> None:
+    """block_pairs int32 [n, 2] (src, dst): block dst becomes a byte copy of block src."""
+    if block_pairs.dtype != torch.int32 or block_pairs.dim() != 2 or block_pairs.shape[1] != 2:
+        raise TypeError("block_pairs must be int32 [n, 2]")
+    if not block_pairs.is_contiguous():
+        raise ValueError("block_pairs must be contiguous")
+    r = _lib.paged_kv_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(scales), kv_dtype,
+                                  _ptr(block_pairs), block_pairs.shape[0], k_cache.shape[0],
+                                  k_cache.shape[1], head_dim, block_size, _ptr(dev_status),
+                                  _stream(stream))
+    if r != PKV_OK:
+        raise PagedKVError(r, "paged_kv_copy_blocks")
 
 
 def paged_decode_partition_size(num_seqs: int, num_q_heads: int, num_kv_heads: int,

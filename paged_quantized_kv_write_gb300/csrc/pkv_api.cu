@@ -47,6 +47,29 @@ int paged_kv_write(const void* k_new, const void* v_new, int new_dtype,
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+int paged_kv_copy_blocks(void* k_cache, void* v_cache, void* scales, int kv_dtype,
+                         const int32_t* block_pairs, int num_pairs, int num_blocks,
+                         int num_kv_heads, int head_dim, int block_size, int* dev_status,
+                         void* stream) {
+  if (num_pairs < 0 || num_blocks <= 0 || num_kv_heads <= 0) return PKV_ERR_INVALID_ARG;
+  if (!ok_kv_dtype(kv_dtype)) return PKV_ERR_UNSUPPORTED;
+  if (!ok_head_dim(head_dim) || !ok_block_size(block_size)) return PKV_ERR_UNSUPPORTED;
+  if (num_pairs == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !block_pairs) return PKV_ERR_INVALID_ARG;
+  const bool quant = kv_dtype == PKV_FP8_E4M3 || kv_dtype == PKV_FP8_E5M2 || kv_dtype == PKV_INT4_G32;
+  if (quant && !scales) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || (reinterpret_cast<uintptr_t>(block_pairs) & 3u) ||
+      (quant && !aligned16(scales)))
+    return PKV_ERR_INVALID_ARG;
+  // chunks of one block's K + V rows per grid column (<= 65535)
+  const int64_t block_bytes = static_cast<int64_t>(num_kv_heads) * block_size * 2 * head_dim;
+  if (2 * block_bytes / 16 > int64_t(65535) * 1024) return PKV_ERR_UNSUPPORTED;
+  pkv::CopyArgs a{k_cache, v_cache, scales, kv_dtype, block_pairs, num_pairs, num_blocks,
+                  num_kv_heads, head_dim, block_size, dev_status};
+  cudaError_t e = pkv::launch_copy_blocks(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 int paged_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads,
                                 int max_blocks_per_seq, int block_size, int partition_size) {
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0 ||

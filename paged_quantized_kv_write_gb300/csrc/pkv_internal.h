@@ -49,7 +49,22 @@ struct DecodeArgs {
   int* dev_status;
 };
 
+struct CopyArgs {
+  void* k_cache;
+  void* v_cache;
+  void* scales;
+  int kv_dtype;
+  const int32_t* block_pairs;   // [num_pairs][2] (src, dst)
+  int num_pairs;
+  int num_blocks;
+  int num_kv_heads;
+  int head_dim;
+  int block_size;
+  int* dev_status;
+};
+
 cudaError_t launch_kv_write(const WriteArgs& a, cudaStream_t st);
+cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 
 int resolve_partition_size(int num_seqs, int num_q_heads, int num_kv_heads,

@@ -92,12 +92,17 @@ def check_close(gpu: np.ndarray, ref: np.ndarray, kv_dtype: int, out_dtype: int,
 class GpuCase:
     """A workload's inputs on the GPU, with an oracle-written cache uploaded."""
 
-    def __init__(self, case: W.Case, k, v, s, partition_size: int = 0):
+    def __init__(self, case: W.Case, k, v, s, partition_size: int = 0, device_cache=None):
+        """device_cache: (k, v, scales) tensors already on the GPU, used instead of
+        uploading k, v, s."""
         import paged_quantized_kv_write_gb300 as pkv
         w = case.w
         self.case, self.w, self.pkv = case, w, pkv
         self.q = bits_to_tensor(case.q, w.q_dtype)
-        self.k, self.v, self.s = cache_to_device(k, v, s, w.kv_dtype)
+        if device_cache is not None:
+            self.k, self.v, self.s = device_cache
+        else:
+            self.k, self.v, self.s = cache_to_device(k, v, s, w.kv_dtype)
         self.tables = torch.from_numpy(case.block_tables).cuda()
         self.ctx = torch.from_numpy(case.context_lens).cuda()
         self.out = torch.empty_like(self.q)

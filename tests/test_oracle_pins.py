@@ -565,3 +565,65 @@ def test_attention_pairs_match_full():
                                         w.softmax_scale, w.num_q_heads, w.num_kv_heads,
                                         w.head_dim, w.block_size, ps, ph)
     assert np.array_equal(sub, full[ps, ph])
+
+
+# ------------------------------------------------------------------ block copies
+@pytest.mark.parametrize("kv", [W.F16, W.BF16, W.FP8_E4M3, W.FP8_E5M2, W.INT4_G32])
+def test_copy_blocks_equals_numpy_block_assignment(kv):
+    """Block dst of [NB, Hkv, bs, row] (and its scales) becomes block src."""
+    qd = W.F16 if kv == W.F16 else W.BF16
+    w = W.Workload("copy", 4, 8, 2, 64, 16, kv, qd, "uniform", 20, 60, seed=31 + kv)
+    case = W.make_case(w)
+    k, v, s = oracle.prefill_case(case)
+    pairs = np.array([[case.block_tables[0, 0], 3], [case.block_tables[1, 1], 5],
+                      [7, 7]], np.int32)
+    ek, ev = k.copy(), v.copy()
+    es = None if s is None else s.copy()
+    for src, dst in pairs:
+        ek[dst] = ek[src]
+        ev[dst] = ev[src]
+        if es is not None:
+            es[:, dst] = es[:, src]         # FP8 [2, NB, Hkv]; INT4 [2, NB, Hkv, bs, D/32, 2]
+    skipped = oracle.copy_blocks(k, v, s, kv, pairs, case.num_blocks, w.num_kv_heads,
+                                 w.head_dim, w.block_size)
+    assert skipped == 0
+    assert np.array_equal(k, ek) and np.array_equal(v, ev)
+    if s is not None:
+        assert np.array_equal(s.view(np.uint8), es.view(np.uint8))
+
+
+def test_copy_blocks_skips_out_of_range_ids():
+    w = W.Workload("copy", 2, 4, 1, 64, 16, W.FP8_E4M3, W.BF16, "fixed", 20, 20, seed=3)
+    case = W.make_case(w)
+    k, v, s = oracle.prefill_case(case)
+    before = (k.copy(), v.copy(), s.copy())
+    pairs = np.array([[-1, 2], [1, case.num_blocks], [case.num_blocks + 5, 0]], np.int32)
+    assert oracle.copy_blocks(k, v, s, w.kv_dtype, pairs, case.num_blocks, 1, 64, 16) == 3
+    for a, b in zip(before, (k, v, s)):
+        assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("kv", [W.FP8_E4M3, W.INT4_G32, W.BF16])
+def test_copy_on_write_fork_attends_like_the_shared_block(kv):
+    """A sequence whose table points at a copied block attends exactly as it did
+    through the original (the copy-on-write invariant)."""
+    w = W.CONFIGS[4].scaled(batch=3, ctx_cap=200, seed=55, kv_dtype=kv,
+                            q_dtype=W.BF16, pool_blocks=64)
+    case = W.make_case(w)
+    k, v, s = oracle.prefill_case(case)
+    ref = oracle.step_case(case, k, v, s)
+    used = set(case.block_tables[case.block_tables >= 0].ravel().tolist())
+    free = [b for b in range(case.num_blocks) if b not in used]
+    tables = case.block_tables.copy()
+    pairs = []
+    for b in range(w.batch):                     # fork each sequence's first block
+        src = tables[b, 0]
+        dst = free.pop()
+        pairs.append([src, dst])
+        tables[b, 0] = dst
+    assert oracle.copy_blocks(k, v, s, kv, np.array(pairs, np.int32), case.num_blocks,
+                              w.num_kv_heads, w.head_dim, w.block_size) == 0
+    out = oracle.decode_attention(case.q, w.q_dtype, k, v, tables, case.context_lens, s, kv,
+                                  case.num_blocks, w.softmax_scale, w.num_q_heads,
+                                  w.num_kv_heads, w.head_dim, w.block_size)
+    assert np.array_equal(out, ref)
