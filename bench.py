@@ -1,8 +1,10 @@
 """Benchmark: paged decode-attention KV GB/s (% of GB300 HBM peak) and seq-steps/s.
 
 One step = the whole hot path for one decode step of one layer: the
-quantize-on-write of every sequence's new token (paged_kv_write) followed by
-paged decode attention over the block-table-mapped cache.  Inputs are seeded
+quantize-on-write of every sequence's new token and paged decode attention
+over the block-table-mapped cache, by default in one launch
+(paged_decode_attention_with_write; --unfused: paged_kv_write, then
+paged_decode_attention).  Inputs are seeded
 and synthetic, shaped like the chosen workload (default: the Llama-3-8B-shaped
 bf16 layer, batch 64, 32/8 heads, D 128, bs 16, context 4096).  The KV cache
 (1 GiB) is far larger than L2, so no flush is needed between steps.
@@ -117,8 +119,8 @@ def _with_kv_dtype(w: W.Workload, name: str) -> W.Workload:
     return dataclasses.replace(w, **upd)
 
 
-def _kernel_launches_per_step(w: W.Workload, nparts: int) -> int:
-    write = 2 if w.kv_dtype in W.FP8_TYPES else 1
+def _kernel_launches_per_step(w: W.Workload, nparts: int, fused: bool = False) -> int:
+    write = 0 if fused else (2 if w.kv_dtype in W.FP8_TYPES else 1)
     return write + 1 + (1 if nparts > 1 else 0)
 
 
@@ -182,9 +184,17 @@ def run_ours(args, rank: int, world: int):
                                    w.num_kv_heads, w.kv_dtype, w.block_size, w.partition_size,
                                    ws, status, st)
 
+    def fused(st):
+        pkv.paged_decode_attention_with_write(q, kn, vn, slots, k, v, tables, ctx, s, out,
+                                              w.softmax_scale, w.kv_dtype, w.block_size,
+                                              w.partition_size, ws, status, st)
+
     def step(st):
-        write(st)
-        attend(st)
+        if not args.unfused:
+            fused(st)
+        else:
+            write(st)
+            attend(st)
 
     # Device-timed steps replay a CUDA graph of the step (the library's own
     # launches, captured once), so host-side submission gaps cannot leak into
@@ -321,7 +331,9 @@ def run_ours(args, rank: int, world: int):
             "write_avg_us": round(write_avg_ms * 1e3, 3),
             "algorithmic_bytes": attn_bytes,
         },
-        "gpu_launches": _kernel_launches_per_step(w, nparts) * args.steps,
+        "gpu_launches": _kernel_launches_per_step(w, nparts, not args.unfused) * args.steps,
+        "step_kind": "fused write + attention (one launch)" if not args.unfused
+                     else "paged_kv_write, then paged_decode_attention",
         "clocks": clk,
         "wall_s_timed": round(t_wall, 4),
         "timing": "CUDA events around CUDA-graph replays of the step (write + attention); "
@@ -554,6 +566,9 @@ def main():
                     help="override the workload's block size (block-size sweep; 0: keep)")
     ap.add_argument("--kv-dtype", default="", choices=[""] + sorted(W.DTYPE_NAMES.values()),
                     help="override the workload's cache dtype (dtype comparison; empty: keep)")
+    ap.add_argument("--unfused", action="store_true",
+                    help="run the step as paged_kv_write then paged_decode_attention (two "
+                         "launches) instead of paged_decode_attention_with_write (one)")
     ap.add_argument("--op", default="step", choices=["step", "copy"],
                     help="step: the decode step (default); copy: copy-on-write block copies")
     ap.add_argument("--copy-pairs", type=int, default=4096,

@@ -160,6 +160,37 @@ int paged_decode_attention(const void* q, int q_dtype,
                            int partition_size, void* workspace, size_t workspace_bytes,
                            int* dev_status, void* stream);
 
+/* paged_decode_attention_with_write — paged_kv_write of each sequence's new
+ * token and paged_decode_attention in one launch (the quantize-on-write step
+ * of the mohashari page's snippet-4 and the attention of the myaihardware
+ * page's "Implementation Details", fused: the write launch and its re-read
+ * disappear from the decode step).
+ *
+ * k_new, v_new   [num_seqs][num_kv_heads][head_dim] in q_dtype: the new token
+ *                of each sequence (for F16/BF16 caches q_dtype must equal
+ *                kv_dtype, as for paged_kv_write).
+ * slot_mapping   int64 [num_seqs]: -1 (sequence b writes nothing), or the slot
+ *                of position context_lens[b] - 1 of sequence b, i.e.
+ *                block_tables[b][(ctx-1)/bs] * bs + (ctx-1) % bs.  Any other
+ *                value is flagged (PKV_ERR_DEVICE_BOUNDS) and not written:
+ *                only that position's row is read by the same CTA that
+ *                writes it, which is what makes the fusion race-free.
+ * Everything else as for paged_decode_attention; the cache and scales are
+ * updated exactly as paged_kv_write would (encodings and FP8 scale rule
+ * included) and the attention sees the written token.  Results are those of
+ * paged_kv_write followed by paged_decode_attention with the same arguments.
+ */
+int paged_decode_attention_with_write(const void* q, int q_dtype, const void* k_new,
+                                      const void* v_new, const int64_t* slot_mapping,
+                                      void* k_cache, void* v_cache,
+                                      const int32_t* block_tables, int max_blocks_per_seq,
+                                      const int32_t* context_lens, int num_seqs, void* scales,
+                                      int kv_dtype, int num_blocks, void* out,
+                                      float softmax_scale, int num_q_heads, int num_kv_heads,
+                                      int head_dim, int block_size, int partition_size,
+                                      void* workspace, size_t workspace_bytes, int* dev_status,
+                                      void* stream);
+
 /* paged_decode_attention_noalloc — paged_decode_attention without a
  * caller-supplied workspace, for callers that cannot allocate device memory.
  * The pages have no counterpart: this is a convenience of this library.

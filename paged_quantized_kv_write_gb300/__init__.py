@@ -11,6 +11,8 @@ Calls (same names as the C ABI):
     paged_kv_write(k_new, v_new, slot_mapping, k_cache, v_cache, scales, kv_dtype, ...)
     paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scales, out,
                            softmax_scale, num_kv_heads, kv_dtype, block_size, ...)
+    paged_decode_attention_with_write(q, k_new, v_new, slot_mapping, k_cache, v_cache, ...)
+    paged_kv_copy_blocks(k_cache, v_cache, scales, kv_dtype, block_pairs, ...)
     paged_decode_workspace_bytes(...), paged_decode_partition_size(...)
 """
 
@@ -23,7 +25,8 @@ from typing import Optional
 import torch
 
 PKV_F16, PKV_BF16, PKV_FP8_E4M3, PKV_INT4_G32, PKV_FP8_E5M2 = 0, 1, 2, 3, 4
-PKV_OK, PKV_ERR_DEVICE_BOUNDS = 0, 4
+(PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA, PKV_ERR_DEVICE_BOUNDS,
+ PKV_ERR_WORKSPACE) = 0, 1, 2, 3, 4, 5
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libpagedkv.so")
@@ -39,6 +42,9 @@ def _load() -> ctypes.CDLL:
                         ctypes.c_size_t)
     lib.paged_kv_write.argtypes = [P, P, I, P, I64, P, P, P, I, I, I, I, I, P, P]
     lib.paged_kv_write.restype = I
+    lib.paged_decode_attention_with_write.argtypes = [P, I, P, P, P, P, P, P, I, P, I, P, I, I,
+                                                      P, F, I, I, I, I, I, P, SZ, P, P]
+    lib.paged_decode_attention_with_write.restype = I
     lib.paged_kv_copy_blocks.argtypes = [P, P, P, I, P, I, I, I, I, I, P, P]
     lib.paged_kv_copy_blocks.restype = I
     lib.paged_decode_attention.argtypes = [P, I, P, P, P, I, P, I, P, I, I, P, F, I, I, I, I, I,
@@ -178,6 +184,34 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                                     _stream(stream))
     if r != PKV_OK:
         raise PagedKVError(r, "paged_decode_attention")
+
+
+def paged_decode_attention_with_write(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                                      slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+                                      v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                      context_lens: torch.Tensor, scales: Optional[torch.Tensor],
+                                      out: torch.Tensor, softmax_scale: float, kv_dtype: int,
+                                      block_size: int, partition_size: int = 0,
+                                      workspace: Optional[torch.Tensor] = None,
+                                      dev_status: Optional[torch.Tensor] = None,
+                                      stream=None) -> None:
+    """Write each sequence's new token (k_new/v_new [B, Hkv, D], slot_mapping int64 [B])
+    and attend, in one launch."""
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    b, hq, d = q.shape
+    num_kv_heads = k_new.shape[1]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    r = _lib.paged_decode_attention_with_write(
+        _ptr(q), _dtype_code(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache),
+        _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), b,
+        _ptr(scales), kv_dtype, k_cache.shape[0], _ptr(out), float(softmax_scale), hq,
+        num_kv_heads, d, block_size, partition_size, _ptr(workspace), ws_bytes,
+        _ptr(dev_status), _stream(stream))
+    if r != PKV_OK:
+        raise PagedKVError(r, "paged_decode_attention_with_write")
 
 
 def make_workspace(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,

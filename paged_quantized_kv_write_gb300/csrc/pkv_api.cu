@@ -18,6 +18,66 @@ bool ok_half_dtype(int t) { return t == PKV_F16 || t == PKV_BF16; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// paged_decode_attention, and its fused-write form when slot_mapping is set
+int decode_impl(const void* q, int q_dtype, const void* k_new, const void* v_new,
+                const int64_t* slot_mapping, const void* k_cache, const void* v_cache,
+                const int32_t* block_tables, int max_blocks_per_seq,
+                const int32_t* context_lens, int num_seqs, const void* scales, int kv_dtype,
+                int num_blocks, void* out, float softmax_scale, int num_q_heads,
+                int num_kv_heads, int head_dim, int block_size, int partition_size,
+                void* workspace, size_t workspace_bytes, int* dev_status, void* stream) {
+  if (num_seqs < 0 || num_blocks <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      max_blocks_per_seq <= 0 || partition_size < 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads) return PKV_ERR_INVALID_ARG;
+  if (!ok_half_dtype(q_dtype) || !ok_kv_dtype(kv_dtype)) return PKV_ERR_UNSUPPORTED;
+  if ((kv_dtype == PKV_F16 || kv_dtype == PKV_BF16) && q_dtype != kv_dtype)
+    return PKV_ERR_UNSUPPORTED;
+  if (!ok_head_dim(head_dim) || !ok_block_size(block_size)) return PKV_ERR_UNSUPPORTED;
+  if (num_q_heads / num_kv_heads > 8) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(max_blocks_per_seq) * block_size > 0x7FFFFFFF) return PKV_ERR_UNSUPPORTED;
+  // the kernel locates a 16-token sub-tile as (block * Hkv + head) << 4 | offset / 16
+  if (static_cast<int64_t>(num_blocks) * num_kv_heads >= (int64_t(1) << 27)) return PKV_ERR_UNSUPPORTED;
+  if (!(softmax_scale == softmax_scale)) return PKV_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return PKV_ERR_INVALID_ARG;
+  const bool quant = kv_dtype == PKV_FP8_E4M3 || kv_dtype == PKV_FP8_E5M2 || kv_dtype == PKV_INT4_G32;
+  if (quant && !scales) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+      (reinterpret_cast<uintptr_t>(context_lens) & 3u) || (quant && !aligned16(scales)))
+    return PKV_ERR_INVALID_ARG;
+  const int part = pkv::resolve_partition_size(num_seqs, num_q_heads, num_kv_heads,
+                                               max_blocks_per_seq, block_size, partition_size);
+  const int64_t np = ceil_div(static_cast<int64_t>(max_blocks_per_seq) * block_size, part);
+  if (np > 0x7FFFFFFF) return PKV_ERR_UNSUPPORTED;
+  float* ws_out = nullptr;
+  float* ws_ml = nullptr;
+  if (np > 1) {
+    const size_t need = paged_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads,
+                                                     head_dim, max_blocks_per_seq, block_size,
+                                                     partition_size);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
+    const int64_t out_bytes = static_cast<int64_t>(num_seqs) * num_q_heads * np * head_dim * 4;
+    ws_out = static_cast<float*>(workspace);
+    ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ceil_div(out_bytes, 256) * 256);
+  }
+  if (slot_mapping && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new) ||
+                       (reinterpret_cast<uintptr_t>(slot_mapping) & 7u)))
+    return PKV_ERR_INVALID_ARG;
+  pkv::DecodeArgs a{q, q_dtype, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                    context_lens, num_seqs, scales, kv_dtype, num_blocks, out, softmax_scale,
+                    num_q_heads, num_kv_heads, head_dim, block_size, part,
+                    static_cast<int>(np), ws_out, ws_ml, dev_status};
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.slot_mapping = slot_mapping;
+  cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -102,50 +162,27 @@ int paged_decode_attention(const void* q, int q_dtype,
                            int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                            int partition_size, void* workspace, size_t workspace_bytes,
                            int* dev_status, void* stream) {
-  if (num_seqs < 0 || num_blocks <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
-      max_blocks_per_seq <= 0 || partition_size < 0)
-    return PKV_ERR_INVALID_ARG;
-  if (num_q_heads % num_kv_heads) return PKV_ERR_INVALID_ARG;
-  if (!ok_half_dtype(q_dtype) || !ok_kv_dtype(kv_dtype)) return PKV_ERR_UNSUPPORTED;
-  if ((kv_dtype == PKV_F16 || kv_dtype == PKV_BF16) && q_dtype != kv_dtype)
-    return PKV_ERR_UNSUPPORTED;
-  if (!ok_head_dim(head_dim) || !ok_block_size(block_size)) return PKV_ERR_UNSUPPORTED;
-  if (num_q_heads / num_kv_heads > 8) return PKV_ERR_UNSUPPORTED;
-  if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
-  if (static_cast<int64_t>(max_blocks_per_seq) * block_size > 0x7FFFFFFF) return PKV_ERR_UNSUPPORTED;
-  // the kernel locates a 16-token sub-tile as (block * Hkv + head) << 4 | offset / 16
-  if (static_cast<int64_t>(num_blocks) * num_kv_heads >= (int64_t(1) << 27)) return PKV_ERR_UNSUPPORTED;
-  if (!(softmax_scale == softmax_scale)) return PKV_ERR_INVALID_ARG;
-  if (num_seqs == 0) return PKV_OK;
-  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
-    return PKV_ERR_INVALID_ARG;
-  const bool quant = kv_dtype == PKV_FP8_E4M3 || kv_dtype == PKV_FP8_E5M2 || kv_dtype == PKV_INT4_G32;
-  if (quant && !scales) return PKV_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
-      (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
-      (reinterpret_cast<uintptr_t>(context_lens) & 3u) || (quant && !aligned16(scales)))
-    return PKV_ERR_INVALID_ARG;
-  const int part = pkv::resolve_partition_size(num_seqs, num_q_heads, num_kv_heads,
-                                               max_blocks_per_seq, block_size, partition_size);
-  const int64_t np = ceil_div(static_cast<int64_t>(max_blocks_per_seq) * block_size, part);
-  if (np > 0x7FFFFFFF) return PKV_ERR_UNSUPPORTED;
-  float* ws_out = nullptr;
-  float* ws_ml = nullptr;
-  if (np > 1) {
-    const size_t need = paged_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads,
-                                                     head_dim, max_blocks_per_seq, block_size,
-                                                     partition_size);
-    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
-    const int64_t out_bytes = static_cast<int64_t>(num_seqs) * num_q_heads * np * head_dim * 4;
-    ws_out = static_cast<float*>(workspace);
-    ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ceil_div(out_bytes, 256) * 256);
-  }
-  pkv::DecodeArgs a{q, q_dtype, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                    context_lens, num_seqs, scales, kv_dtype, num_blocks, out, softmax_scale,
-                    num_q_heads, num_kv_heads, head_dim, block_size, part,
-                    static_cast<int>(np), ws_out, ws_ml, dev_status};
-  cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return decode_impl(q, q_dtype, nullptr, nullptr, nullptr, k_cache, v_cache, block_tables,
+                     max_blocks_per_seq, context_lens, num_seqs, scales, kv_dtype, num_blocks,
+                     out, softmax_scale, num_q_heads, num_kv_heads, head_dim, block_size,
+                     partition_size, workspace, workspace_bytes, dev_status, stream);
+}
+
+int paged_decode_attention_with_write(const void* q, int q_dtype, const void* k_new,
+                                      const void* v_new, const int64_t* slot_mapping,
+                                      void* k_cache, void* v_cache,
+                                      const int32_t* block_tables, int max_blocks_per_seq,
+                                      const int32_t* context_lens, int num_seqs, void* scales,
+                                      int kv_dtype, int num_blocks, void* out,
+                                      float softmax_scale, int num_q_heads, int num_kv_heads,
+                                      int head_dim, int block_size, int partition_size,
+                                      void* workspace, size_t workspace_bytes, int* dev_status,
+                                      void* stream) {
+  if (num_seqs > 0 && !slot_mapping) return PKV_ERR_INVALID_ARG;
+  return decode_impl(q, q_dtype, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
+                     max_blocks_per_seq, context_lens, num_seqs, scales, kv_dtype, num_blocks,
+                     out, softmax_scale, num_q_heads, num_kv_heads, head_dim, block_size,
+                     partition_size, workspace, workspace_bytes, dev_status, stream);
 }
 
 const char* paged_kv_status_string(int status) {

@@ -41,6 +41,7 @@
 #include <atomic>
 
 #include "pkv_common.cuh"
+#include "pkv_encode.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -186,11 +187,14 @@ __device__ __forceinline__ Int4Lanes int4_lanes(int lane) {
 
 struct Params {
   const uint16_t* q;
-  const uint8_t* k_cache;
-  const uint8_t* v_cache;
+  uint8_t* k_cache;           // written only by the fused write
+  uint8_t* v_cache;
   const int32_t* block_tables;
   const int32_t* context_lens;
-  const void* scales;
+  void* scales;
+  const uint16_t* k_new;      // fused write: [num_seqs][Hkv][D] in the q dtype, or null
+  const uint16_t* v_new;
+  const int64_t* slot_mapping;
   void* out;
   float* ws_out;
   float* ws_ml;
@@ -261,6 +265,34 @@ __device__ __forceinline__ void issue_tile(const Params& p, int rowp, bool live,
     if (lane == 0) asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(mo), "l"(sc + idx) : "memory");
     if (lane == 1) asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(mo + 4), "l"(sc + per_kv + idx) : "memory");
   }
+}
+
+// Fused write: store sequence b's new token for KV head kvh (one warp), as
+// paged_kv_write would.  The slot must be -1 (nothing to write) or the slot of
+// position ctx - 1 through b's block table: only then is the row read by this
+// CTA alone; any other slot is flagged and left unwritten.
+template <int KV, int QT, int D>
+__device__ __forceinline__ void fused_write(const Params& p, int b, int kvh, int ctx, int lane) {
+  const int64_t slot = p.slot_mapping[b];
+  if (slot == -1) return;
+  int64_t expect = -2;
+  if (ctx > 0) {
+    const int t = ctx - 1;
+    const int logical = t / p.block_size;
+    const int phys = p.block_tables[static_cast<int64_t>(b) * p.max_blocks_per_seq + logical];
+    if (phys >= 0 && phys < p.num_blocks)
+      expect = static_cast<int64_t>(phys) * p.block_size + (t - logical * p.block_size);
+  }
+  if (slot != expect) {
+    if (lane == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  const int64_t block = slot / p.block_size;
+  const int offset = static_cast<int>(slot - block * p.block_size);
+  const int64_t row = static_cast<int64_t>(b) * p.num_kv_heads + kvh;
+  encode_token_head<KV, QT, D>(p.k_new + row * D, p.v_new + row * D, p.k_cache, p.v_cache,
+                               p.scales, p.num_blocks, p.num_kv_heads, p.block_size, block, kvh,
+                               offset, lane);
 }
 
 // One unit of work: partition `part` of sequence b, KV head kvh.
@@ -535,6 +567,17 @@ paged_decode_kernel(const Params p) {
     s_issue = s_issue + 1 == G::kStages ? 0 : s_issue + 1;
     cp_async_commit();
   };
+  // Fused write: the CTA (warp-owned units: the warp) holding b's last
+  // partition stores b's new token for its KV head before issuing any copy.
+  if (p.slot_mapping != nullptr && pbase + nunits == nparts_seq) {
+    if (WU || warp == 0) fused_write<KV, QT, D>(p, b, kvh, ctx, lane);
+    if constexpr (WU) {
+      __syncwarp();
+    } else {
+      __syncthreads();
+    }
+  }
+
   // the first advance enters unit 0 (it + W >= ntiles = 0) with its prefetched window
   it = 0;
   i_next_tb = next_window_unit(0);
@@ -1088,11 +1131,16 @@ cudaError_t launch_mode(const DecodeArgs& a, cudaStream_t st) {
   using G = Geo<KV, D>;
   Params p;
   p.q = static_cast<const uint16_t*>(a.q);
-  p.k_cache = static_cast<const uint8_t*>(a.k_cache);
-  p.v_cache = static_cast<const uint8_t*>(a.v_cache);
+  // the caches are written only by the fused write (a.slot_mapping set), which
+  // the C ABI allows only for caller-writable buffers
+  p.k_cache = static_cast<uint8_t*>(const_cast<void*>(a.k_cache));
+  p.v_cache = static_cast<uint8_t*>(const_cast<void*>(a.v_cache));
   p.block_tables = a.block_tables;
   p.context_lens = a.context_lens;
-  p.scales = a.scales;
+  p.scales = const_cast<void*>(a.scales);
+  p.k_new = static_cast<const uint16_t*>(a.k_new);
+  p.v_new = static_cast<const uint16_t*>(a.v_new);
+  p.slot_mapping = a.slot_mapping;
   p.out = a.out;
   p.ws_out = a.ws_out;
   p.ws_ml = a.ws_ml;

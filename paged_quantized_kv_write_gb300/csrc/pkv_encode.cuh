@@ -1,0 +1,123 @@
+// Quantize-on-write of one (token, KV head): the K row and the V row of one
+// token for one KV head, encoded into the cache by one warp.  Shared by the
+// write kernel and by the decode kernel's fused write.
+//
+// Lane l holds the EPL = head_dim/32 consecutive elements [EPL*l, EPL*l + EPL)
+// of a row, so each row is read and written with one coalesced access.
+// Encodings (the formats' definitions; block-wise FP8 scale from snippet-4
+// of "Reducing LLM Inference Latency ... PagedAttention in vLLM"; INT4
+// group-wise from section 4 of "Optimizing KV-Cache Memory Footprint"):
+//  FP8  scale = max(amax / max_finite, 1e-12) (fp32; max_finite 448 for E4M3,
+//       57344 for E5M2), set by the token at block offset 0;
+//       code = cvt.rn.satfinite.{e4m3,e5m2}(x / scale), IEEE fp32 division.
+//  INT4 per 32-element group: scale = fp16(fp32(max - min + 0) / 15),
+//       zero = fp16(min + 0), code = clamp(rint((x - zero) / scale), 0, 15).
+// Every fp32 step uses an explicitly rounded intrinsic so the codes are the
+// same bits whatever the compiler contracts.
+#pragma once
+
+#include "pkv_common.cuh"
+
+namespace pkv {
+
+// k_src / v_src: the token's rows for this head (D values of dtype NEW).
+// block, offset: where the token goes; cache_row = (block * Hkv + head) * bs + offset.
+template <int KV, int NEW, int D>
+__device__ __forceinline__ void encode_token_head(const uint16_t* __restrict__ k_src,
+                                                  const uint16_t* __restrict__ v_src,
+                                                  uint8_t* __restrict__ k_cache,
+                                                  uint8_t* __restrict__ v_cache,
+                                                  void* __restrict__ scales, int num_blocks,
+                                                  int num_kv_heads, int block_size, int64_t block,
+                                                  int head, int offset, int lane) {
+  constexpr int EPL = D / kWarp;                       // elements per lane: 2 or 4
+  const int64_t cache_row = (block * num_kv_heads + head) * block_size + offset;
+#pragma unroll
+  for (int which = 0; which < 2; ++which) {
+    const uint16_t* src = (which ? v_src : k_src) + lane * EPL;
+    uint8_t* cache = which ? v_cache : k_cache;
+    uint16_t raw[EPL];
+    if constexpr (EPL == 4) {
+      uint2 w = *reinterpret_cast<const uint2*>(src);
+      raw[0] = w.x & 0xFFFF; raw[1] = w.x >> 16; raw[2] = w.y & 0xFFFF; raw[3] = w.y >> 16;
+    } else {
+      uint32_t w = *reinterpret_cast<const uint32_t*>(src);
+      raw[0] = w & 0xFFFF; raw[1] = w >> 16;
+    }
+
+    if constexpr (KV == PKV_F16 || KV == PKV_BF16) {
+      uint16_t* dst = reinterpret_cast<uint16_t*>(cache) + cache_row * D + lane * EPL;
+      if constexpr (EPL == 4) {
+        *reinterpret_cast<uint2*>(dst) =
+            make_uint2(raw[0] | (uint32_t(raw[1]) << 16), raw[2] | (uint32_t(raw[3]) << 16));
+      } else {
+        *reinterpret_cast<uint32_t*>(dst) = raw[0] | (uint32_t(raw[1]) << 16);
+      }
+    } else if constexpr (is_fp8(KV)) {
+      float x[EPL];
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) x[e] = Half16<NEW>::to_float(raw[e]);
+      float* sp = reinterpret_cast<float*>(scales) +
+                  (static_cast<int64_t>(which) * num_blocks + block) * num_kv_heads + head;
+      float s;
+      if (offset == 0) {
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        s = fmaxf(__fdiv_rn(amax, fp8_max<KV>()), 1e-12f);
+        if (lane == 0) *sp = s;
+      } else {
+        s = *sp;
+      }
+      uint8_t* dst = cache + cache_row * D + lane * EPL;
+      if constexpr (EPL == 4) {
+        uint32_t lo = fp8x2_from_f32<KV>(__fdiv_rn(x[0], s), __fdiv_rn(x[1], s));
+        uint32_t hi = fp8x2_from_f32<KV>(__fdiv_rn(x[2], s), __fdiv_rn(x[3], s));
+        *reinterpret_cast<uint32_t*>(dst) = lo | (hi << 16);
+      } else {
+        *reinterpret_cast<uint16_t*>(dst) = fp8x2_from_f32<KV>(__fdiv_rn(x[0], s), __fdiv_rn(x[1], s));
+      }
+    } else {  // INT4_G32
+      constexpr int LPG = 32 / EPL;                    // lanes per 32-element group
+      float x[EPL];
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) x[e] = Half16<NEW>::to_float(raw[e]);
+      float mn = x[0], mx = x[0];
+#pragma unroll
+      for (int e = 1; e < EPL; ++e) { mn = fminf(mn, x[e]); mx = fmaxf(mx, x[e]); }
+#pragma unroll
+      for (int o = LPG / 2; o > 0; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      }
+      const __half sh = __float2half_rn(__fdiv_rn(__fadd_rn(__fsub_rn(mx, mn), 0.0f), 15.0f));
+      const __half zh = __float2half_rn(__fadd_rn(mn, 0.0f));
+      const float sf = __half2float(sh), zf = __half2float(zh);
+      uint32_t codes = 0;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        float c = 0.f;
+        if (sf != 0.f) c = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(x[e], zf), sf)), 0.f), 15.f);
+        codes |= static_cast<uint32_t>(c) << (4 * e);
+      }
+      uint8_t* dst = cache + cache_row * (D / 2) + lane * (EPL / 2);
+      if constexpr (EPL == 4) {
+        *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(codes);
+      } else {
+        *dst = static_cast<uint8_t>(codes);
+      }
+      if ((lane % LPG) == 0) {
+        const int group = lane / LPG;
+        uint16_t* pair = reinterpret_cast<uint16_t*>(scales) +
+                         2 * ((((static_cast<int64_t>(which) * num_blocks + block) * num_kv_heads +
+                                head) * block_size + offset) * (D / 32) + group);
+        const uint32_t packed = __half_as_ushort(sh) | (uint32_t(__half_as_ushort(zh)) << 16);
+        *reinterpret_cast<uint32_t*>(pair) = packed;
+      }
+    }
+  }
+}
+
+}  // namespace pkv

@@ -47,6 +47,10 @@ struct DecodeArgs {
   float* ws_out;        // [num_seqs][num_q_heads][num_partitions][head_dim]
   float* ws_ml;         // [num_seqs][num_q_heads][num_partitions][2]
   int* dev_status;
+  // fused write (null for attention alone): new K/V [num_seqs][Hkv][D] in q_dtype
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
+  const int64_t* slot_mapping = nullptr;
 };
 
 struct CopyArgs {
