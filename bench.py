@@ -120,7 +120,7 @@ def _with_kv_dtype(w: W.Workload, name: str) -> W.Workload:
 
 
 def _kernel_launches_per_step(w: W.Workload, nparts: int, fused: bool = False) -> int:
-    write = 0 if fused else (2 if w.kv_dtype in W.FP8_TYPES else 1)
+    write = 0 if fused else (2 if w.kv_dtype in W.BLK8_TYPES else 1)
     return write + 1 + (1 if nparts > 1 else 0)
 
 
@@ -291,7 +291,8 @@ def run_ours(args, rank: int, world: int):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": {W.F16: "f16", W.BF16: "bf16", W.FP8_E4M3: "fp8_e4m3+bf16",
-                  W.FP8_E5M2: "fp8_e5m2+bf16", W.INT4_G32: "int4_g32+bf16"}[w.kv_dtype],
+                  W.FP8_E5M2: "fp8_e5m2+bf16", W.INT8: "int8+bf16",
+                  W.INT4_G32: "int4_g32+bf16"}[w.kv_dtype],
         "data": "synthetic (seeded N(0,1) q/K/V, shuffled block tables; no model weights)",
         "config": {
             "workload": f"config {args.config}: {w.name}",
@@ -364,7 +365,7 @@ def run_copy(args, rank: int, world: int):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(dev)
     per_block = 2 * w.num_kv_heads * w.block_size * pkv.row_bytes(w.kv_dtype, w.head_dim)
-    if w.kv_dtype in W.FP8_TYPES:
+    if w.kv_dtype in W.BLK8_TYPES:
         per_block += 2 * 4 * w.num_kv_heads
     elif w.kv_dtype == W.INT4_G32:
         per_block += 2 * w.num_kv_heads * w.block_size * (w.head_dim // 32) * 4

@@ -27,12 +27,13 @@
  *    traps.  The caller reads it back whenever it likes.
  *  - Cache layout per KV tensor (K and V are separate buffers):
  *      [num_blocks][num_kv_heads][block_size][row], where a row holds one
- *      token of one head: head_dim 16-bit values (F16/BF16), head_dim E4M3
- *      bytes (FP8), or head_dim/2 bytes of 4-bit codes (INT4: element 2i in
- *      the low nibble of byte i, 2i+1 in the high nibble).
+ *      token of one head: head_dim 16-bit values (F16/BF16), head_dim FP8
+ *      bytes (E4M3, E5M2) or int8 codes (INT8), or head_dim/2 bytes of 4-bit
+ *      codes (INT4: element 2i in the low nibble of byte i, 2i+1 in the high
+ *      nibble).
  *  - `scales` layout (index 0 of the leading 2 is K, 1 is V):
- *      FP8 (E4M3, E5M2):  float [2][num_blocks][num_kv_heads] — one scale per
- *            block and KV head;
+ *      FP8 (E4M3, E5M2) and INT8:  float [2][num_blocks][num_kv_heads] — one
+ *            scale per block and KV head;
  *      INT4: half  [2][num_blocks][num_kv_heads][block_size][head_dim/32][2]
  *            — (scale, zero) per token, head and group of 32 elements;
  *      F16/BF16: unused (may be NULL).
@@ -52,7 +53,8 @@ typedef enum {
     PKV_BF16 = 1,      /* bfloat16 */
     PKV_FP8_E4M3 = 2,  /* OCP E4M3 ("e4m3fn"), per-(block, kv-head) fp32 scale */
     PKV_INT4_G32 = 3,  /* asymmetric 4-bit, groups of 32 along head_dim, fp16 scale+zero */
-    PKV_FP8_E5M2 = 4   /* OCP E5M2, per-(block, kv-head) fp32 scale */
+    PKV_FP8_E5M2 = 4,  /* OCP E5M2, per-(block, kv-head) fp32 scale */
+    PKV_INT8 = 5       /* symmetric int8 codes, per-(block, kv-head) fp32 scale */
 } pkv_dtype;
 
 typedef enum {
@@ -81,6 +83,9 @@ typedef enum {
  *                Within one call the offset-0 tokens are applied first.
  *                FP8_E5M2: the same with 57344 (the largest finite E5M2) in
  *                place of 448, codes rounded to nearest even and saturated.
+ *                INT8: the same block-wise rule with 127: scale =
+ *                max(amax / 127, 1e-12), code = clamp(rint(x / scale), -127,
+ *                127) (fp32 quotient, round half to even), two's complement.
  *                INT4_G32: per token, head and 32-element group,
  *                scale = fp16(fp32(max - min) / 15), zero = fp16(min),
  *                code = clamp(rint((x - zero) / scale), 0, 15) in fp32 (0 when

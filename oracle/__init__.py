@@ -44,6 +44,8 @@ def lib() -> ctypes.CDLL:
         L.oracle_e5m2_to_double.restype = D
         L.oracle_e5m2_encode.argtypes = [ctypes.c_float]
         L.oracle_e5m2_encode.restype = ctypes.c_uint8
+        L.oracle_int8_encode.argtypes = [ctypes.c_float]
+        L.oracle_int8_encode.restype = ctypes.c_int8
         L.oracle_kv_cache_bytes.argtypes = [D] * 6
         L.oracle_kv_cache_bytes.restype = D
         L.oracle_num_pages.argtypes = [I64, I64]
@@ -104,6 +106,10 @@ def e5m2_encode(y: float) -> int:
     return lib().oracle_e5m2_encode(float(np.float32(y)))
 
 
+def int8_encode(y: float) -> int:
+    return lib().oracle_int8_encode(float(np.float32(y)))
+
+
 # ---------------------------------------------------------------- formulas
 def kv_cache_bytes(layers, heads, head_dim, seq_len, batch, bytes_per_elem) -> float:
     return lib().oracle_kv_cache_bytes(layers, heads, head_dim, seq_len, batch, bytes_per_elem)
@@ -130,7 +136,7 @@ def alloc_cache(kv_dtype: int, num_blocks: int, num_kv_heads: int, head_dim: int
     if kv_dtype in (0, 1):
         k = np.zeros((num_blocks, num_kv_heads, block_size, head_dim), np.uint16)
         return k, k.copy(), None
-    if kv_dtype in (2, 4):
+    if kv_dtype in (2, 4, 5):
         k = np.zeros((num_blocks, num_kv_heads, block_size, head_dim), np.uint8)
         return k, k.copy(), np.zeros((2, num_blocks, num_kv_heads), np.float32)
     if kv_dtype == 3:

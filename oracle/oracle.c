@@ -42,6 +42,10 @@
  *  R8  FP8 E5M2 (1 sign, 5 exponent, 2 mantissa bits; the pages name E4M3
  *      only): the same block-wise recipe as R4/R5 with 57344, E5M2's
  *      largest finite value, in place of 448.
+ *  R9  INT8 (the pages give one byte per element and no format): the same
+ *      block-wise recipe with 127: scale = max(amax / 127, 1e-12), code =
+ *      clamp(rint(x / scale), -127, 127) of the fp32 quotient, round half to
+ *      even, stored as a two's complement byte; dequantized = code * scale.
  *
  * Build with -ffp-contract=off: the encoders must round each fp32 step.
  */
@@ -54,9 +58,12 @@
 #include <omp.h>
 #endif
 
-enum { DT_F16 = 0, DT_BF16 = 1, DT_FP8 = 2, DT_INT4 = 3, DT_E5M2 = 4 };
+enum { DT_F16 = 0, DT_BF16 = 1, DT_FP8 = 2, DT_INT4 = 3, DT_E5M2 = 4, DT_INT8 = 5 };
 
-static int is_fp8(int kv_dtype) { return kv_dtype == DT_FP8 || kv_dtype == DT_E5M2; }
+/* one byte per element, one fp32 scale per (block, KV head): FP8 and INT8 */
+static int is_blk8(int kv_dtype) {
+    return kv_dtype == DT_FP8 || kv_dtype == DT_E5M2 || kv_dtype == DT_INT8;
+}
 
 /* ------------------------------------------------------------ codecs */
 
@@ -191,6 +198,17 @@ uint8_t oracle_e5m2_encode(float yf) {
     return sign | (uint8_t)code;
 }
 
+/* INT8 code of the fp32 quotient y (R9): round half to even, clamp to
+ * [-127, 127] (NaN gives 0). */
+int8_t oracle_int8_encode(float yf) {
+    double y = (double)yf;
+    if (isnan(y)) return 0;
+    double r = rint(y);                  /* the default rounding mode: half to even */
+    if (r > 127.0) r = 127.0;
+    if (r < -127.0) r = -127.0;
+    return (int8_t)r;
+}
+
 /* ------------------------------------------------------------ formulas */
 
 /* KV bytes = 2 (K and V) * layers * heads * head_dim * seq_len * batch * bytes. */
@@ -221,7 +239,7 @@ int oracle_physical_address(const int32_t* table_row, int num_entries, int block
 static int64_t row_bytes(int kv_dtype, int head_dim) {
     switch (kv_dtype) {
     case DT_F16: case DT_BF16: return 2 * (int64_t)head_dim;
-    case DT_FP8: case DT_E5M2: return head_dim;
+    case DT_FP8: case DT_E5M2: case DT_INT8: return head_dim;
     case DT_INT4: return head_dim / 2;
     }
     return -1;
@@ -270,6 +288,12 @@ int oracle_dequant_row(const void* cache, const void* scales, int which_kv, int 
                                          : oracle_e5m2_to_double(base[d])) * s;
         return 0;
     }
+    case DT_INT8: {
+        double s = *fp8_scale_ptr((void*)scales, which_kv, block, kv_head, num_blocks,
+                                  num_kv_heads);
+        for (int d = 0; d < head_dim; ++d) row[d] = (double)(int8_t)base[d] * s;   /* R9 */
+        return 0;
+    }
     case DT_INT4: {
         for (int d = 0; d < head_dim; ++d) {
             int code = (d & 1) ? (base[d / 2] >> 4) & 0xF : base[d / 2] & 0xF;
@@ -288,7 +312,7 @@ int oracle_dequant_row(const void* cache, const void* scales, int which_kv, int 
 
 static int check_geometry(int kv_dtype, int num_blocks, int num_kv_heads, int head_dim,
                           int block_size) {
-    if (kv_dtype < DT_F16 || kv_dtype > DT_E5M2) return -1;
+    if (kv_dtype < DT_F16 || kv_dtype > DT_INT8) return -1;
     if (num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0) return -1;
     if (kv_dtype == DT_INT4 && head_dim % 32) return -1;
     return 0;
@@ -323,7 +347,7 @@ int oracle_copy_blocks(void* k_cache, void* v_cache, void* scales, int kv_dtype,
                     memmove(cache + row_index(dst, h, o, num_kv_heads, block_size) * rb,
                             cache + row_index(src, h, o, num_kv_heads, block_size) * rb,
                             (size_t)rb);
-                if (is_fp8(kv_dtype))
+                if (is_blk8(kv_dtype))
                     *fp8_scale_ptr(scales, which, dst, h, num_blocks, num_kv_heads) =
                         *fp8_scale_ptr(scales, which, src, h, num_blocks, num_kv_heads);
                 if (kv_dtype == DT_INT4)
@@ -347,8 +371,9 @@ int oracle_copy_blocks(void* k_cache, void* v_cache, void* scales, int kv_dtype,
 /* Encode one token row of one head (R4-R6).  x: the row as fp32 values. */
 static void encode_row(const float* x, int head_dim, int kv_dtype, uint8_t* dst,
                        int fresh_fp8_block, float* fp8_scale, uint16_t* int4_pairs) {
-    if (is_fp8(kv_dtype)) {
-        const float fmax = kv_dtype == DT_FP8 ? 448.0f : 57344.0f;     /* R8 */
+    if (is_blk8(kv_dtype)) {
+        const float fmax = kv_dtype == DT_FP8 ? 448.0f
+                           : kv_dtype == DT_E5M2 ? 57344.0f : 127.0f;         /* R8, R9 */
         if (fresh_fp8_block) {
             /* snippet-4: scale = max|x| / 448, clamped below at 1e-12, in fp32 */
             float amax = 0.0f;
@@ -361,9 +386,13 @@ static void encode_row(const float* x, int head_dim, int kv_dtype, uint8_t* dst,
             *fp8_scale = s;
         }
         float s = *fp8_scale;
-        for (int d = 0; d < head_dim; ++d)
-            dst[d] = kv_dtype == DT_FP8 ? oracle_e4m3_encode(x[d] / s)
-                                        : oracle_e5m2_encode(x[d] / s);
+        for (int d = 0; d < head_dim; ++d) {
+            if (kv_dtype == DT_INT8)
+                dst[d] = (uint8_t)oracle_int8_encode(x[d] / s);
+            else
+                dst[d] = kv_dtype == DT_FP8 ? oracle_e4m3_encode(x[d] / s)
+                                            : oracle_e5m2_encode(x[d] / s);
+        }
         return;
     }
     /* INT4, R6 */
@@ -421,8 +450,8 @@ int oracle_kv_write(const uint16_t* k_new, const uint16_t* v_new, int new_dtype,
             int32_t block = (int32_t)(slot / block_size);
             int offset = (int)(slot % block_size);
             int first = offset == 0;
-            if (is_fp8(kv_dtype) && first != (pass == 0)) continue;
-            if (!is_fp8(kv_dtype) && pass == 1) continue;
+            if (is_blk8(kv_dtype) && first != (pass == 0)) continue;
+            if (!is_blk8(kv_dtype) && pass == 1) continue;
             for (int which = 0; which < 2; ++which) {
                 const uint16_t* src = which ? v_new : k_new;
                 uint8_t* cache = (uint8_t*)(which ? v_cache : k_cache);
@@ -436,7 +465,7 @@ int oracle_kv_write(const uint16_t* k_new, const uint16_t* v_new, int new_dtype,
                     }
                     for (int d = 0; d < head_dim; ++d)
                         x[d] = (float)half_word_to_double(srow[d], new_dtype);
-                    float* s8 = is_fp8(kv_dtype)
+                    float* s8 = is_blk8(kv_dtype)
                                     ? fp8_scale_ptr(scales, which, block, h, num_blocks,
                                                     num_kv_heads)
                                     : NULL;

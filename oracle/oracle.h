@@ -10,7 +10,8 @@
  *
  * dtype tags: 0 = f16, 1 = bf16, 2 = FP8 E4M3 (per-(block, kv-head) fp32
  * scale), 3 = INT4 group-32 (fp16 scale + zero per token, head and group),
- * 4 = FP8 E5M2 (scaled like E4M3).
+ * 4 = FP8 E5M2 (scaled like E4M3), 5 = INT8 (symmetric codes, scaled like
+ * E4M3 with 127 in place of 448).
  * Layouts are those of the library (documented in oracle.c).
  */
 #ifndef PKV_ORACLE_H
@@ -29,6 +30,7 @@ double oracle_e4m3_to_double(uint8_t code);
 uint8_t oracle_e4m3_encode(float y);
 double oracle_e5m2_to_double(uint8_t code);
 uint8_t oracle_e5m2_encode(float y);
+int8_t oracle_int8_encode(float y);
 
 /* sizing formulas */
 double oracle_kv_cache_bytes(double layers, double heads, double head_dim, double seq_len,

@@ -24,7 +24,7 @@ from typing import Optional
 
 import torch
 
-PKV_F16, PKV_BF16, PKV_FP8_E4M3, PKV_INT4_G32, PKV_FP8_E5M2 = 0, 1, 2, 3, 4
+PKV_F16, PKV_BF16, PKV_FP8_E4M3, PKV_INT4_G32, PKV_FP8_E5M2, PKV_INT8 = 0, 1, 2, 3, 4, 5
 (PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA, PKV_ERR_DEVICE_BOUNDS,
  PKV_ERR_WORKSPACE) = 0, 1, 2, 3, 4, 5
 
@@ -95,7 +95,7 @@ def _stream(stream) -> ctypes.c_void_p:
 
 def row_bytes(kv_dtype: int, head_dim: int) -> int:
     return {PKV_F16: 2 * head_dim, PKV_BF16: 2 * head_dim, PKV_FP8_E4M3: head_dim,
-            PKV_FP8_E5M2: head_dim, PKV_INT4_G32: head_dim // 2}[kv_dtype]
+            PKV_FP8_E5M2: head_dim, PKV_INT8: head_dim, PKV_INT4_G32: head_dim // 2}[kv_dtype]
 
 
 def alloc_cache(kv_dtype: int, num_blocks: int, num_kv_heads: int, head_dim: int,
@@ -107,7 +107,7 @@ def alloc_cache(kv_dtype: int, num_blocks: int, num_kv_heads: int, head_dim: int
         return k, torch.zeros_like(k), None
     k = torch.zeros((num_blocks, num_kv_heads, block_size, row_bytes(kv_dtype, head_dim)),
                     dtype=torch.uint8, device=device)
-    if kv_dtype in (PKV_FP8_E4M3, PKV_FP8_E5M2):
+    if kv_dtype in (PKV_FP8_E4M3, PKV_FP8_E5M2, PKV_INT8):
         s = torch.zeros((2, num_blocks, num_kv_heads), dtype=torch.float32, device=device)
     else:
         s = torch.zeros((2, num_blocks, num_kv_heads, block_size, head_dim // 32, 2),

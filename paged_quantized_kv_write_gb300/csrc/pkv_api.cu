@@ -13,7 +13,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool ok_head_dim(int d) { return d == 64 || d == 128; }
 bool ok_block_size(int bs) { return bs >= 16 && bs <= 256 && bs % 16 == 0; }
-bool ok_kv_dtype(int t) { return t >= PKV_F16 && t <= PKV_FP8_E5M2; }
+bool ok_kv_dtype(int t) { return t >= PKV_F16 && t <= PKV_INT8; }
 bool ok_half_dtype(int t) { return t == PKV_F16 || t == PKV_BF16; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -43,7 +43,7 @@ int decode_impl(const void* q, int q_dtype, const void* k_new, const void* v_new
   if (num_seqs == 0) return PKV_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
     return PKV_ERR_INVALID_ARG;
-  const bool quant = kv_dtype == PKV_FP8_E4M3 || kv_dtype == PKV_FP8_E5M2 || kv_dtype == PKV_INT4_G32;
+  const bool quant = kv_dtype != PKV_F16 && kv_dtype != PKV_BF16;
   if (quant && !scales) return PKV_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
@@ -94,7 +94,7 @@ int paged_kv_write(const void* k_new, const void* v_new, int new_dtype,
   if (!ok_head_dim(head_dim) || !ok_block_size(block_size)) return PKV_ERR_UNSUPPORTED;
   if (num_tokens == 0) return PKV_OK;
   if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
-  const bool quant = kv_dtype == PKV_FP8_E4M3 || kv_dtype == PKV_FP8_E5M2 || kv_dtype == PKV_INT4_G32;
+  const bool quant = kv_dtype != PKV_F16 && kv_dtype != PKV_BF16;
   if (quant && !scales) return PKV_ERR_INVALID_ARG;
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
       (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) || (quant && !aligned16(scales)))
@@ -116,7 +116,7 @@ int paged_kv_copy_blocks(void* k_cache, void* v_cache, void* scales, int kv_dtyp
   if (!ok_head_dim(head_dim) || !ok_block_size(block_size)) return PKV_ERR_UNSUPPORTED;
   if (num_pairs == 0) return PKV_OK;
   if (!k_cache || !v_cache || !block_pairs) return PKV_ERR_INVALID_ARG;
-  const bool quant = kv_dtype == PKV_FP8_E4M3 || kv_dtype == PKV_FP8_E5M2 || kv_dtype == PKV_INT4_G32;
+  const bool quant = kv_dtype != PKV_F16 && kv_dtype != PKV_BF16;
   if (quant && !scales) return PKV_ERR_INVALID_ARG;
   if (!aligned16(k_cache) || !aligned16(v_cache) || (reinterpret_cast<uintptr_t>(block_pairs) & 3u) ||
       (quant && !aligned16(scales)))

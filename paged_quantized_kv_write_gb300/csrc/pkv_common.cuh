@@ -84,6 +84,8 @@ __device__ __forceinline__ uint32_t e5m2x2_to_f16x2(uint16_t codes) {
 
 // FP8 cache formats, by dtype tag
 __host__ __device__ constexpr bool is_fp8(int kv) { return kv == PKV_FP8_E4M3 || kv == PKV_FP8_E5M2; }
+// one byte per element and one fp32 scale per (block, KV head): FP8 and INT8
+__host__ __device__ constexpr bool is_blk8(int kv) { return is_fp8(kv) || kv == PKV_INT8; }
 template <int KV> __device__ __forceinline__ float fp8_max() { return KV == PKV_FP8_E5M2 ? 57344.f : 448.f; }
 template <int KV> __device__ __forceinline__ uint16_t fp8x2_from_f32(float lo, float hi) {
   if constexpr (KV == PKV_FP8_E5M2) return e5m2x2_from_f32(lo, hi);
@@ -92,6 +94,26 @@ template <int KV> __device__ __forceinline__ uint16_t fp8x2_from_f32(float lo, f
 template <int KV> __device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint16_t codes) {
   if constexpr (KV == PKV_FP8_E5M2) return e5m2x2_to_f16x2(codes);
   else return e4m3x2_to_f16x2(codes);
+}
+
+// One-byte codes of a 32-bit word (bytes 0..3) as f16x2 operands, by format:
+// FP8 converts exactly; INT8 codes x become (x + 128) 2^-24 (the XOR with
+// 0x80 in b8_prep makes x + 128 an unsigned byte, which placed in the low
+// mantissa bits of a zero-exponent f16 is that subnormal), so INT8 sums carry
+// an offset of 128 per code that the caller takes off.
+template <int KV> __device__ __forceinline__ uint32_t b8_prep(uint32_t w) {
+  if constexpr (KV == PKV_INT8) return w ^ 0x80808080u;
+  else return w;
+}
+// bytes 0, 1 of a prepared word
+template <int KV> __device__ __forceinline__ uint32_t b8_lo(uint32_t w) {
+  if constexpr (KV == PKV_INT8) return __byte_perm(w, 0u, 0x4140);
+  else return fp8x2_to_f16x2<KV>(static_cast<uint16_t>(w & 0xFFFFu));
+}
+// bytes 2, 3 of a prepared word
+template <int KV> __device__ __forceinline__ uint32_t b8_hi(uint32_t w) {
+  if constexpr (KV == PKV_INT8) return __byte_perm(w, 0u, 0x4342);
+  else return fp8x2_to_f16x2<KV>(static_cast<uint16_t>(w >> 16));
 }
 
 // ------------------------------------------------------------------ INT4

@@ -11,8 +11,8 @@
 //
 // One copy moves, for the pair (src, dst): the K rows and the V rows of all
 // KV heads of the block (each a contiguous run of Hkv * bs * row bytes in the
-// [num_blocks][Hkv][bs][row] layout) and the block's scales (FP8: Hkv floats
-// per K and V; INT4: Hkv * bs * D/32 (scale, zero) pairs per K and V, also
+// [num_blocks][Hkv][bs][row] layout) and the block's scales (FP8, INT8: Hkv
+// floats per K and V; INT4: Hkv * bs * D/32 (scale, zero) pairs per K and V, also
 // contiguous).  The bytes are copied as they are: a copied block dequantizes
 // to exactly what its source did.
 //
@@ -115,7 +115,7 @@ cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t st) {
   int64_t row_bytes = 2 * a.head_dim;
   p.scale_bytes = 0;
   p.fp8_scales = 0;
-  if (a.kv_dtype == PKV_FP8_E4M3 || a.kv_dtype == PKV_FP8_E5M2) {
+  if (is_blk8(a.kv_dtype)) {
     row_bytes = a.head_dim;
     p.scale_bytes = 4 * static_cast<int64_t>(a.num_kv_heads);
     p.fp8_scales = 1;

@@ -102,7 +102,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 template <int KV, int D> struct Geo {
   static constexpr bool kHalf = (KV == PKV_F16 || KV == PKV_BF16);
-  static constexpr int kRowBytes = kHalf ? 2 * D : (is_fp8(KV) ? D : D / 2);
+  static constexpr int kRowBytes = kHalf ? 2 * D : (is_blk8(KV) ? D : D / 2);
   static constexpr int kCpr = kRowBytes / 16;                   // 16-byte chunks per row
   static constexpr int kTileBytes = kTile * kRowBytes;          // one of K or V
   static constexpr int kScaleRowBytes = (KV == PKV_INT4_G32) ? (D / 32) * 4 : 0;
@@ -115,7 +115,7 @@ template <int KV, int D> struct Geo {
   static constexpr int kMiscOffset = kSub * kSubBytes;
   static constexpr int kStageBytes = kSub * kSubBytes + 16 * kSub;
   static constexpr int kStages =
-      kHalf ? PKV_STAGES_HALF : (is_fp8(KV) ? PKV_STAGES_FP8 : PKV_STAGES_INT4);
+      kHalf ? PKV_STAGES_HALF : (is_blk8(KV) ? PKV_STAGES_FP8 : PKV_STAGES_INT4);
   static constexpr int kWarpRing = kStages * kStageBytes;
   static constexpr int kRingBytes = kDecodeWarps * kWarpRing;
   // merge buffer: one warp's state, lane-major with an odd stride (no bank conflicts)
@@ -138,7 +138,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // analysis in the fragment readers below).
 template <int KV, int D>
 __device__ __forceinline__ int swz(int r) {
-  if constexpr (KV == PKV_F16 || KV == PKV_BF16 || (is_fp8(KV) && D == 128)) {
+  if constexpr (KV == PKV_F16 || KV == PKV_BF16 || (is_blk8(KV) && D == 128)) {
     return (((r ^ (r >> 1)) & 1) << 2) | ((r >> 2) & 1);
   } else if constexpr (KV == PKV_INT4_G32) {
     return D == 128 ? ((r >> 1) & 3) : ((r >> 2) & 1);
@@ -257,7 +257,7 @@ __device__ __forceinline__ void issue_tile(const Params& p, int rowp, bool live,
       cp_async_16(stage + 2 * G::kTileBytes + G::kScaleTileBytes + (lane - 16) * 16,
                   vsc + (lane - 16) * 16);
     }
-  } else if constexpr (is_fp8(KV)) {
+  } else if constexpr (is_blk8(KV)) {
     const float* sc = static_cast<const float*>(p.scales);
     const int64_t idx = blk;
     const int64_t per_kv = static_cast<int64_t>(p.num_blocks) * p.num_kv_heads;
@@ -317,11 +317,13 @@ __device__ __forceinline__ Unit make_unit(const Params& p, int b, int kvh, int c
 // of the group, rows = d in the order the K fragments use; heads >= group are
 // zero columns), plus the f16 scaling.  INT4 also gets the B operand of its
 // zero-point product (zq, hi + lo f16 words; see the score code) and the
-// factor zscale that product's sums are taken back with.
+// factor zscale that product's sums are taken back with.  INT8 gets qoff8:
+// 128 * the sum over d of q as the mma sees it, for heads 2c4 and 2c4 + 1
+// (its codes enter as x + 128).
 template <int KV, int QT, int D>
 __device__ __forceinline__ void load_q(const Params& p, const Unit& u, int q4, int c4,
                                        uint32_t (&qb)[D / 16][2], float& qexp,
-                                       uint32_t (&zq)[2], float& zscale) {
+                                       uint32_t (&zq)[2], float& zscale, float (&qoff8)[2]) {
   constexpr bool kHalf = (KV == PKV_F16 || KV == PKV_BF16);
   const int group = p.num_q_heads / p.num_kv_heads;
   const bool head_ok = q4 < group;
@@ -337,10 +339,12 @@ __device__ __forceinline__ void load_q(const Params& p, const Unit& u, int q4, i
     }
     zq[0] = zq[1] = 0u;
     zscale = 0.f;
+    qoff8[0] = qoff8[1] = 0.f;
   } else {
     // each thread's 32 d values, as float
     float qf[32];
-    if constexpr (is_fp8(KV)) {
+    qoff8[0] = qoff8[1] = 0.f;
+    if constexpr (is_blk8(KV)) {
       // d = 16*(4i + c4) + 0..15 for i < D/64
 #pragma unroll
       for (int i = 0; i < D / 64; ++i) {
@@ -379,17 +383,27 @@ __device__ __forceinline__ void load_q(const Params& p, const Unit& u, int q4, i
     if (amax >= 32768.f) e = ilogbf(amax) - 14;
     const float qs = ldexpf(1.f, -e);
     qexp = ldexpf(1.f, e);
-    if constexpr (is_fp8(KV)) {
+    if constexpr (is_blk8(KV)) {
       zq[0] = zq[1] = 0u;
       zscale = 0.f;
       // k-step 4i+h: lo pair = d 16(4i+c4) + 4h + {0,1}, hi pair = + 4h + {2,3}
+      float s16 = 0.f;
 #pragma unroll
       for (int i = 0; i < D / 64; ++i)
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           qb[4 * i + h][0] = Half16<PKV_F16>::pack_rn(qf[16 * i + 4 * h] * qs, qf[16 * i + 4 * h + 1] * qs);
           qb[4 * i + h][1] = Half16<PKV_F16>::pack_rn(qf[16 * i + 4 * h + 2] * qs, qf[16 * i + 4 * h + 3] * qs);
+          const float2 a = Half16<PKV_F16>::unpack(qb[4 * i + h][0]);
+          const float2 c = Half16<PKV_F16>::unpack(qb[4 * i + h][1]);
+          s16 += (a.x + a.y) + (c.x + c.y);
         }
+      if constexpr (KV == PKV_INT8) {
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) s16 += __shfl_xor_sync(0xffffffffu, s16, o);  // head q4
+        qoff8[0] = 128.f * __shfl_sync(0xffffffffu, s16, (2 * c4) * 4);
+        qoff8[1] = 128.f * __shfl_sync(0xffffffffu, s16, (2 * c4 + 1) * 4);
+      }
     } else {
       // k-step 2grp+h: lo pair = d (8c4 + 2h, 8c4 + 2h + 4), hi pair = (8c4 + 2h + 1, 8c4 + 2h + 5).
       // The hi pairs meet K codes taken as 16 n (high nibbles, no shift), so
@@ -475,7 +489,7 @@ paged_decode_kernel(const Params p) {
   // f16 cases keep kPScale * 2^kTau (* 16 for the FP8 scale ratio) below 2^15.
   constexpr float kPScale = (KV == PKV_BF16 || KV == PKV_INT4_G32) ? 1.f
                                                                    : (KV == PKV_F16 ? 256.f : 64.f);
-  constexpr float kTau = (KV == PKV_BF16) ? 8.f : (KV == PKV_F16 ? 6.f : (is_fp8(KV) ? 4.f : 0.f));
+  constexpr float kTau = (KV == PKV_BF16) ? 8.f : (KV == PKV_F16 ? 6.f : (is_blk8(KV) ? 4.f : 0.f));
 
   extern __shared__ __align__(128) uint8_t smem[];
   pdl_wait();                 // the cache may have been written by the previous kernel
@@ -592,12 +606,15 @@ paged_decode_kernel(const Params p) {
   float qexp = 1.f;
   uint32_t zq[2];                            // INT4: B operand of the zero-point product
   float zscale;
+  float qoff8[2];                            // INT8: 128 * sum of q (heads 2c4, 2c4 + 1)
+  float zp[2];                               // INT8: running sum of P' (heads 2c4, 2c4 + 1)
   float oacc[MT][4];
   float mrow[2], lrow[2];
   float zc[4];                               // INT4: zero-point sums (C fragment)
   float vref, inv_vref;                      // FP8: oacc is in units of vref / kPScale
   int s_cons = 0;                            // ring stage of the next pair to compute
-  load_q<KV, QT, D>(p, make_unit<G::kTileTok>(p, b, kvh, ctx, part_of(0)), q4, c4, qb, qexp, zq, zscale);
+  load_q<KV, QT, D>(p, make_unit<G::kTileTok>(p, b, kvh, ctx, part_of(0)), q4, c4, qb, qexp, zq, zscale,
+                    qoff8);
 
 #pragma unroll 1
   for (int cu = 0; cu < nunits; ++cu) {
@@ -607,6 +624,7 @@ paged_decode_kernel(const Params p) {
     mrow[0] = mrow[1] = -INFINITY;           // running max (log2 units), heads 2c4, 2c4+1
     lrow[0] = lrow[1] = 0.f;                 // this thread's share of the running sum
     zc[0] = zc[1] = zc[2] = zc[3] = 0.f;
+    zp[0] = zp[1] = 0.f;
     vref = 0.f;
     inv_vref = 0.f;
     const float base = p.softmax_scale * kLog2e * qexp;
@@ -652,17 +670,19 @@ paged_decode_kernel(const Params p) {
                 const uint32_t a1[4] = {r0.z, r1.z, r0.w, r1.w};
                 mma_16816<MMA_T>(sc2, a1, qb[2 * jp + 1][0], qb[2 * jp + 1][1]);
               }
-            } else if constexpr (is_fp8(KV)) {
+            } else if constexpr (is_blk8(KV)) {
 #pragma unroll
               for (int i = 0; i < D / 64; ++i) {
                 const uint4 r0 = ld_shared_v4(st + chunk_off<KV, D>(q4, 4 * i + c4));
                 const uint4 r1 = ld_shared_v4(st + chunk_off<KV, D>(q4 + 8, 4 * i + c4));
-                const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w};
-                const uint32_t w1[4] = {r1.x, r1.y, r1.z, r1.w};
+                const uint32_t w0[4] = {b8_prep<KV>(r0.x), b8_prep<KV>(r0.y), b8_prep<KV>(r0.z),
+                                        b8_prep<KV>(r0.w)};
+                const uint32_t w1[4] = {b8_prep<KV>(r1.x), b8_prep<KV>(r1.y), b8_prep<KV>(r1.z),
+                                        b8_prep<KV>(r1.w)};
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
-                  const uint32_t a[4] = {fp8x2_to_f16x2<KV>(w0[h] & 0xFFFF), fp8x2_to_f16x2<KV>(w1[h] & 0xFFFF),
-                                         fp8x2_to_f16x2<KV>(w0[h] >> 16), fp8x2_to_f16x2<KV>(w1[h] >> 16)};
+                  const uint32_t a[4] = {b8_lo<KV>(w0[h]), b8_lo<KV>(w1[h]), b8_hi<KV>(w0[h]),
+                                         b8_hi<KV>(w1[h])};
                   if (h & 1)
                     mma_16816<PKV_F16>(sc2, a, qb[4 * i + h][0], qb[4 * i + h][1]);
                   else
@@ -736,10 +756,17 @@ paged_decode_kernel(const Params p) {
 
 #pragma unroll
             for (int k = 0; k < 4; ++k) sc[k] += sc2[k];
+            if constexpr (KV == PKV_INT8) {
+              // codes entered as (x + 128) 2^-24: sum q x = 2^24 acc - 128 sum q
+              sc[0] = sc[0] * 16777216.f - qoff8[0];
+              sc[1] = sc[1] * 16777216.f - qoff8[1];
+              sc[2] = sc[2] * 16777216.f - qoff8[0];
+              sc[3] = sc[3] * 16777216.f - qoff8[1];
+            }
 
           // ---------------------------------------------- scale and mask
           float mult = base;
-          if constexpr (is_fp8(KV)) {
+          if constexpr (is_blk8(KV)) {
             mult *= reinterpret_cast<const float*>(misc)[0];
           } else if constexpr (KV == PKV_INT4_G32) {
             mult = p.softmax_scale * kLog2e;     // qexp already folded into the group sums
@@ -776,7 +803,7 @@ paged_decode_kernel(const Params p) {
         for (int u = 0; u < G::kSub; ++u) {
           von[u] = nval[u] > 0;
           vfac[u] = 1.f;
-          if constexpr (is_fp8(KV)) {
+          if constexpr (is_blk8(KV)) {
             const float vs = reinterpret_cast<const float*>(misc0 + 4 * u)[1];
             von[u] = von[u] && vs > 0.f;
             if (von[u]) {
@@ -794,7 +821,7 @@ paged_decode_kernel(const Params p) {
           mrow[0] = mnew0; mrow[1] = mnew1;
           lrow[0] *= alpha0; lrow[1] *= alpha1;
           if constexpr (KV == PKV_INT4_G32) { zc[0] *= alpha0; zc[1] *= alpha1; }
-          if constexpr (is_fp8(KV)) {
+          if constexpr (is_blk8(KV)) {
             if (rebase) {
               // new reference: the tile's largest V scale; O_true = oacc * vref /
               // kPScale stays invariant across the rebase
@@ -812,6 +839,7 @@ paged_decode_kernel(const Params p) {
             oacc[i][0] *= alpha0; oacc[i][1] *= alpha1;
             oacc[i][2] *= alpha0; oacc[i][3] *= alpha1;
           }
+          if constexpr (KV == PKV_INT8) { zp[0] *= alpha0; zp[1] *= alpha1; }
         }
 
 #pragma unroll
@@ -844,6 +872,12 @@ paged_decode_kernel(const Params p) {
               const uint32_t l23 = H::pack_rn(pp[2] - f23.x, pp[3] - f23.y);
               const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
               const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+              if constexpr (KV == PKV_INT8) {
+                // the P' the products see (hi + lo, within 2^-22): their sum
+                // takes the codes' offset of 128 off in the epilogue
+                zp[0] += pp[0] + pp[2];
+                zp[1] += pp[1] + pp[3];
+              }
 
               if constexpr (kHalf) {
 #pragma unroll
@@ -893,20 +927,25 @@ paged_decode_kernel(const Params p) {
                   wa[0] = A.x; wa[1] = A.y; wb[0] = B.x; wb[1] = B.y;
                   wc[0] = C.x; wc[1] = C.y; we[0] = E.x; we[1] = E.y;
                 }
-                if (partial) {
+                if constexpr (is_fp8(KV)) {
+                  // stale FP8 bytes past the context may be NaN codes (p is 0
+                  // there, but 0 * NaN is not); INT8 codes are always finite
+                  if (partial) {
 #pragma unroll
-                  for (int k = 0; k < NW; ++k) { wa[k] &= mA; wb[k] &= mB; wc[k] &= mC; we[k] &= mE; }
+                    for (int k = 0; k < NW; ++k) { wa[k] &= mA; wb[k] &= mB; wc[k] &= mC; we[k] &= mE; }
+                  }
                 }
 #pragma unroll
                 for (int k = 0; k < NW; ++k) {
-                  const uint32_t x01 = __byte_perm(wa[k], wb[k], 0x5140), x23 = __byte_perm(wa[k], wb[k], 0x7362);
-                  const uint32_t y01 = __byte_perm(wc[k], we[k], 0x5140), y23 = __byte_perm(wc[k], we[k], 0x7362);
-                  const uint32_t a0[4] = {fp8x2_to_f16x2<KV>(x01 & 0xFFFF), fp8x2_to_f16x2<KV>(x01 >> 16),
-                                          fp8x2_to_f16x2<KV>(y01 & 0xFFFF), fp8x2_to_f16x2<KV>(y01 >> 16)};
+                  // token pairs (tA, tB), (tC, tE) byte-interleaved per d
+                  const uint32_t x01 = b8_prep<KV>(__byte_perm(wa[k], wb[k], 0x5140));
+                  const uint32_t x23 = b8_prep<KV>(__byte_perm(wa[k], wb[k], 0x7362));
+                  const uint32_t y01 = b8_prep<KV>(__byte_perm(wc[k], we[k], 0x5140));
+                  const uint32_t y23 = b8_prep<KV>(__byte_perm(wc[k], we[k], 0x7362));
+                  const uint32_t a0[4] = {b8_lo<KV>(x01), b8_hi<KV>(x01), b8_lo<KV>(y01), b8_hi<KV>(y01)};
                   mma_16816<PKV_F16>(oacc[2 * k], a0, bh0, bh1);
                   mma_16816<PKV_F16>(oacc[2 * k], a0, bl0, bl1);
-                  const uint32_t a1[4] = {fp8x2_to_f16x2<KV>(x23 & 0xFFFF), fp8x2_to_f16x2<KV>(x23 >> 16),
-                                          fp8x2_to_f16x2<KV>(y23 & 0xFFFF), fp8x2_to_f16x2<KV>(y23 >> 16)};
+                  const uint32_t a1[4] = {b8_lo<KV>(x23), b8_hi<KV>(x23), b8_lo<KV>(y23), b8_hi<KV>(y23)};
                   mma_16816<PKV_F16>(oacc[2 * k + 1], a1, bh0, bh1);
                   mma_16816<PKV_F16>(oacc[2 * k + 1], a1, bl0, bl1);
                 }
@@ -1005,9 +1044,24 @@ paged_decode_kernel(const Params p) {
       lrow[0] += __shfl_xor_sync(0xffffffffu, lrow[0], o);
       lrow[1] += __shfl_xor_sync(0xffffffffu, lrow[1], o);
     }
+    if constexpr (KV == PKV_INT8) {
+      // codes entered as (x + 128) 2^-24: O = 2^24 acc - 128 sum_t P'_t
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        zp[0] += __shfl_xor_sync(0xffffffffu, zp[0], o);
+        zp[1] += __shfl_xor_sync(0xffffffffu, zp[1], o);
+      }
+#pragma unroll
+      for (int i = 0; i < MT; ++i) {
+        oacc[i][0] = oacc[i][0] * 16777216.f - 128.f * zp[0];
+        oacc[i][1] = oacc[i][1] * 16777216.f - 128.f * zp[1];
+        oacc[i][2] = oacc[i][2] * 16777216.f - 128.f * zp[0];
+        oacc[i][3] = oacc[i][3] * 16777216.f - 128.f * zp[1];
+      }
+    }
     // INT4 codes entered as n 2^-24 (rows q4 + 8, odd d: 16 n 2^-24)
     float post = (KV == PKV_INT4_G32) ? 16777216.f : 1.f / kPScale;
-    if constexpr (is_fp8(KV)) post *= vref;
+    if constexpr (is_blk8(KV)) post *= vref;
     const float post_odd = (KV == PKV_INT4_G32) ? 1048576.f : post;
 #pragma unroll
     for (int i = 0; i < MT; ++i) {
@@ -1067,7 +1121,7 @@ paged_decode_kernel(const Params p) {
           int d0;
           if constexpr (KV == PKV_INT4_G32) {
             d0 = 32 * (i >> 1) + 4 * q4 + 2 * (i & 1);
-          } else if constexpr (is_fp8(KV) && D == 128) {
+          } else if constexpr (is_blk8(KV) && D == 128) {
             d0 = 16 * (((q4 & 1) << 1) | ((q4 >> 1) & 1) | (q4 & 4)) + 2 * i;
           } else {
             d0 = (D == 128 ? 16 : 8) * q4 + 2 * i;
@@ -1240,6 +1294,9 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
     case PKV_FP8_E5M2:
       return a.q_dtype == PKV_F16 ? launch_d<PKV_FP8_E5M2, PKV_F16>(a, st)
                                   : launch_d<PKV_FP8_E5M2, PKV_BF16>(a, st);
+    case PKV_INT8:
+      return a.q_dtype == PKV_F16 ? launch_d<PKV_INT8, PKV_F16>(a, st)
+                                  : launch_d<PKV_INT8, PKV_BF16>(a, st);
     default:
       return a.q_dtype == PKV_F16 ? launch_d<PKV_INT4_G32, PKV_F16>(a, st)
                                   : launch_d<PKV_INT4_G32, PKV_BF16>(a, st);

@@ -10,6 +10,8 @@
 //  FP8  scale = max(amax / max_finite, 1e-12) (fp32; max_finite 448 for E4M3,
 //       57344 for E5M2), set by the token at block offset 0;
 //       code = cvt.rn.satfinite.{e4m3,e5m2}(x / scale), IEEE fp32 division.
+//  INT8 the same block-wise rule with 127: code = clamp(rint(x / scale),
+//       -127, 127), round half to even, two's complement byte.
 //  INT4 per 32-element group: scale = fp16(fp32(max - min + 0) / 15),
 //       zero = fp16(min + 0), code = clamp(rint((x - zero) / scale), 0, 15).
 // Every fp32 step uses an explicitly rounded intrinsic so the codes are the
@@ -53,7 +55,7 @@ __device__ __forceinline__ void encode_token_head(const uint16_t* __restrict__ k
       } else {
         *reinterpret_cast<uint32_t*>(dst) = raw[0] | (uint32_t(raw[1]) << 16);
       }
-    } else if constexpr (is_fp8(KV)) {
+    } else if constexpr (is_blk8(KV)) {
       float x[EPL];
 #pragma unroll
       for (int e = 0; e < EPL; ++e) x[e] = Half16<NEW>::to_float(raw[e]);
@@ -66,13 +68,26 @@ __device__ __forceinline__ void encode_token_head(const uint16_t* __restrict__ k
         for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(x[e]));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        s = fmaxf(__fdiv_rn(amax, fp8_max<KV>()), 1e-12f);
+        s = fmaxf(__fdiv_rn(amax, KV == PKV_INT8 ? 127.f : fp8_max<KV>()), 1e-12f);
         if (lane == 0) *sp = s;
       } else {
         s = *sp;
       }
       uint8_t* dst = cache + cache_row * D + lane * EPL;
-      if constexpr (EPL == 4) {
+      if constexpr (KV == PKV_INT8) {
+        uint32_t codes = 0;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          const float r = rintf(__fdiv_rn(x[e], s));
+          const float c = r == r ? fminf(fmaxf(r, -127.f), 127.f) : 0.f;   // NaN -> 0
+          codes |= (static_cast<uint32_t>(static_cast<int>(c)) & 0xFFu) << (8 * e);
+        }
+        if constexpr (EPL == 4) {
+          *reinterpret_cast<uint32_t*>(dst) = codes;
+        } else {
+          *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(codes);
+        }
+      } else if constexpr (EPL == 4) {
         uint32_t lo = fp8x2_from_f32<KV>(__fdiv_rn(x[0], s), __fdiv_rn(x[1], s));
         uint32_t hi = fp8x2_from_f32<KV>(__fdiv_rn(x[2], s), __fdiv_rn(x[3], s));
         *reinterpret_cast<uint32_t*>(dst) = lo | (hi << 16);

@@ -59,7 +59,7 @@ cudaError_t launch_one(const WriteArgs& a, cudaStream_t st) {
 
 template <int KV, int NEW, int D>
 cudaError_t launch_kv(const WriteArgs& a, cudaStream_t st) {
-  if constexpr (is_fp8(KV)) {
+  if constexpr (is_blk8(KV)) {
     // offset-0 tokens set the block scales; the rest read them afterwards
     cudaError_t e = launch_one<KV, NEW, D, 0>(a, st);
     if (e != cudaSuccess) return e;
@@ -76,6 +76,7 @@ cudaError_t dispatch_kv(const WriteArgs& a, cudaStream_t st) {
     case PKV_BF16: return launch_kv<PKV_BF16, NEW, D>(a, st);
     case PKV_FP8_E4M3: return launch_kv<PKV_FP8_E4M3, NEW, D>(a, st);
     case PKV_FP8_E5M2: return launch_kv<PKV_FP8_E5M2, NEW, D>(a, st);
+    case PKV_INT8: return launch_kv<PKV_INT8, NEW, D>(a, st);
     default: return launch_kv<PKV_INT4_G32, NEW, D>(a, st);
   }
 }

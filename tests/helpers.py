@@ -13,7 +13,8 @@ import workloads as W
 
 # max-abs tolerances on the attention output (the benchmark spec): 2e-3 for 16-bit
 # KV, 5e-3 for FP8/INT4 against the oracle on the same dequantized values.
-TOL = {W.F16: 2e-3, W.BF16: 2e-3, W.FP8_E4M3: 5e-3, W.INT4_G32: 5e-3, W.FP8_E5M2: 5e-3}
+TOL = {W.F16: 2e-3, W.BF16: 2e-3, W.FP8_E4M3: 5e-3, W.INT4_G32: 5e-3, W.FP8_E5M2: 5e-3,
+       W.INT8: 5e-3}
 
 
 def torch_dtype(code: int):
@@ -38,7 +39,7 @@ def cache_to_device(k: np.ndarray, v: np.ndarray, s, kv_dtype: int, device="cuda
         vt = torch.from_numpy(np.ascontiguousarray(v)).to(device)
     st = None
     if s is not None:
-        if kv_dtype in W.FP8_TYPES:
+        if kv_dtype in W.BLK8_TYPES:
             st = torch.from_numpy(np.ascontiguousarray(s)).to(device)
         else:
             st = torch.from_numpy(np.ascontiguousarray(s).view(np.int16)).view(torch.float16).to(device)
@@ -131,12 +132,15 @@ def oracle_attention(case: W.Case, k, v, s, ctx=None, tables=None) -> np.ndarray
 
 
 def workload(cfg):
-    """A benchmark workload by number; "3-e5m2" is workload 3 with an E5M2 cache."""
+    """A benchmark workload by number; "3-e5m2" / "3-int8" are workload 3 with an E5M2 /
+    INT8 cache."""
     if cfg == "3-e5m2":
         return W.CONFIGS[3].scaled(kv_dtype=W.FP8_E5M2, name="FP8 E5M2 KV with quantize-on-write")
+    if cfg == "3-int8":
+        return W.CONFIGS[3].scaled(kv_dtype=W.INT8, name="INT8 KV with quantize-on-write")
     return W.CONFIGS[cfg]
 
 
 def seed_of(cfg) -> int:
     """A fixed small integer per workload name (for seeding its scaled variants)."""
-    return cfg if isinstance(cfg, int) else 6
+    return cfg if isinstance(cfg, int) else {"3-e5m2": 6, "3-int8": 8}[cfg]

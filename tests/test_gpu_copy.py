@@ -51,7 +51,7 @@ def _assert_same(host, dev):
         assert np.array_equal(a.view(np.uint8), b.view(np.uint8)), np.argwhere(a != b)[:5]
 
 
-@pytest.mark.parametrize("kv", [W.F16, W.BF16, W.FP8_E4M3, W.FP8_E5M2, W.INT4_G32])
+@pytest.mark.parametrize("kv", [W.F16, W.BF16, W.FP8_E4M3, W.FP8_E5M2, W.INT8, W.INT4_G32])
 @pytest.mark.parametrize("head_dim,block_size", [(128, 16), (64, 32), (128, 256)])
 def test_copy_blocks_bit_exact(kv, head_dim, block_size):
     w, case, k, v, s = _pool(kv, head_dim, block_size, seed=kv * 7 + block_size,

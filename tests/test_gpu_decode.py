@@ -35,7 +35,7 @@ def _run(w, partition_size=0, identity=False, max_blocks_per_seq=None):
     return case, g, out, ref, (k, v, s)
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, "3-e5m2"])
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, "3-e5m2", "3-int8"])
 @pytest.mark.parametrize("partition_size", [0, 32, 64])
 def test_configs_small(cfg, partition_size, mode):
     w = H.workload(cfg).scaled(batch=5, ctx_cap=300, seed=700 + H.seed_of(cfg))
@@ -49,7 +49,7 @@ def test_config1_exact_shape():
     H.check_close(out, ref, w.kv_dtype, w.q_dtype, "config 1")
 
 
-@pytest.mark.parametrize("kv", [W.F16, W.BF16, W.FP8_E4M3, W.FP8_E5M2, W.INT4_G32])
+@pytest.mark.parametrize("kv", [W.F16, W.BF16, W.FP8_E4M3, W.FP8_E5M2, W.INT8, W.INT4_G32])
 @pytest.mark.parametrize("head_dim", [64, 128])
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 2), (16, 2), (4, 1)])
 def test_heads_dims_dtypes(kv, head_dim, hq, hkv, mode):
@@ -59,7 +59,7 @@ def test_heads_dims_dtypes(kv, head_dim, hq, hkv, mode):
     H.check_close(out, ref, kv, qd, f"kv {kv} D {head_dim} {hq}/{hkv}")
 
 
-@pytest.mark.parametrize("kv", [W.BF16, W.FP8_E4M3, W.FP8_E5M2, W.INT4_G32])
+@pytest.mark.parametrize("kv", [W.BF16, W.FP8_E4M3, W.FP8_E5M2, W.INT8, W.INT4_G32])
 @pytest.mark.parametrize("block_size", [16, 32, 64, 128])
 def test_block_sizes(kv, block_size, mode):
     w = W.Workload("bs", 4, 8, 2, 128, block_size, kv, W.BF16, "uniform", 1, 400, seed=block_size + kv)
@@ -67,7 +67,7 @@ def test_block_sizes(kv, block_size, mode):
     H.check_close(out, ref, kv, W.BF16, f"bs {block_size}")
 
 
-@pytest.mark.parametrize("kv", [W.F16, W.FP8_E4M3, W.FP8_E5M2, W.INT4_G32])
+@pytest.mark.parametrize("kv", [W.F16, W.FP8_E4M3, W.FP8_E5M2, W.INT8, W.INT4_G32])
 def test_context_length_edges(kv, mode):
     """ctx in {0, 1, 15, 16, 17, P-1, P, P+1, 2P+1} with P = 64."""
     qd = W.F16 if kv == W.F16 else W.BF16
@@ -115,7 +115,7 @@ def test_identity_tables_match_shuffled():
     assert np.array_equal(out_a, out_b)
 
 
-@pytest.mark.parametrize("kv", [W.BF16, W.FP8_E4M3, W.FP8_E5M2, W.INT4_G32])
+@pytest.mark.parametrize("kv", [W.BF16, W.FP8_E4M3, W.FP8_E5M2, W.INT8, W.INT4_G32])
 def test_split_matches_unsplit(kv, mode):
     w = W.Workload("split", 3, 16, 2, 128, 16, kv, W.BF16, "fixed", 1000, 1000, seed=kv + 101)
     _, _, out_1, ref, _ = _run(w, partition_size=1008)
@@ -141,7 +141,7 @@ def test_constant_keys_give_mean_of_values():
         H.check_close(out[b], np.repeat(mean, 4, 0), W.BF16, W.BF16, "constant K")
 
 
-@pytest.mark.parametrize("kv", [W.FP8_E4M3, W.FP8_E5M2, W.INT4_G32, W.BF16])
+@pytest.mark.parametrize("kv", [W.FP8_E4M3, W.FP8_E5M2, W.INT8, W.INT4_G32, W.BF16])
 def test_unwritten_last_token_matches_oracle(kv, mode):
     """Attend over a context whose last token was never written (zeroed pool):
     an FP8 block with scale 0 and INT4 rows with scale 0 dequantize to 0, so the
@@ -187,7 +187,7 @@ def test_argument_errors_return_status():
 
 # ----------------------------------------------------------------- full size
 @pytest.mark.slow
-@pytest.mark.parametrize("cfg", [2, 3, 4, 5, "3-e5m2"])
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5, "3-e5m2", "3-int8"])
 def test_full_size_sampled(cfg):
     """The benchmark's workloads at full size, in the launch configuration the
     benchmark times (partition_size from the workload, else the library's

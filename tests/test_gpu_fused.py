@@ -55,7 +55,7 @@ def _check(w, partition_size=0, slots=None, case=None):
     return case, g, out, (k, v, s)
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, "3-e5m2"])
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, "3-e5m2", "3-int8"])
 @pytest.mark.parametrize("partition_size", [0, 32])
 def test_fused_matches_oracle_and_unfused(cfg, partition_size, mode):
     pkv = _pkv()
@@ -72,7 +72,7 @@ def test_fused_matches_oracle_and_unfused(cfg, partition_size, mode):
     assert np.array_equal(out, out2)
 
 
-@pytest.mark.parametrize("kv", [W.FP8_E4M3, W.FP8_E5M2, W.INT4_G32, W.BF16])
+@pytest.mark.parametrize("kv", [W.FP8_E4M3, W.FP8_E5M2, W.INT8, W.INT4_G32, W.BF16])
 def test_fused_new_token_opens_a_block(kv, mode):
     """ctx = 16 m + 1: the new token sits at offset 0 of a fresh block, so for
     FP8 it sets that block's scales inside the fused launch."""

@@ -47,7 +47,7 @@ def _assert_same(case, host, dev):
         assert not diff.any(), f"scales differ at {np.argwhere(diff)[:5]}"
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, "3-e5m2"])
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, "3-e5m2", "3-int8"])
 def test_prefill_and_step_write_bit_exact(cfg):
     w = H.workload(cfg).scaled(batch=6, ctx_cap=200, seed=500 + H.seed_of(cfg))
     case = W.make_case(w)
@@ -62,7 +62,7 @@ def test_prefill_and_step_write_bit_exact(cfg):
     assert status.item() == 0
 
 
-@pytest.mark.parametrize("kv", [W.FP8_E4M3, W.FP8_E5M2, W.INT4_G32, W.BF16, W.F16])
+@pytest.mark.parametrize("kv", [W.FP8_E4M3, W.FP8_E5M2, W.INT8, W.INT4_G32, W.BF16, W.F16])
 @pytest.mark.parametrize("head_dim,block_size", [(64, 16), (128, 32), (64, 64), (128, 256)])
 def test_write_shapes(kv, head_dim, block_size):
     qd = W.F16 if kv == W.F16 else W.BF16
@@ -74,7 +74,7 @@ def test_write_shapes(kv, head_dim, block_size):
     assert status.item() == 0
 
 
-@pytest.mark.parametrize("kv", W.FP8_TYPES)
+@pytest.mark.parametrize("kv", W.BLK8_TYPES)
 def test_fp8_offset_zero_tokens_apply_first_in_one_call(kv):
     w = W.Workload("order", 3, 4, 2, 128, 16, kv, W.BF16, "fixed", 40, 40, seed=77)
     case = W.make_case(w)
@@ -111,7 +111,7 @@ def test_write_skips_minus_one_and_flags_out_of_range():
 
 def test_write_special_values():
     """Zero rows (FP8 eps scale), signed zeros, saturating outliers, constant INT4 groups."""
-    for kv in (W.FP8_E4M3, W.FP8_E5M2, W.INT4_G32):
+    for kv in (W.FP8_E4M3, W.FP8_E5M2, W.INT8, W.INT4_G32):
         w = W.Workload("special", 4, 4, 2, 128, 16, kv, W.BF16, "fixed", 17, 17, seed=9)
         case = W.make_case(w)
         rows = case.prefill_k.copy()
@@ -125,7 +125,7 @@ def test_write_special_values():
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("cfg", [2, 3, 4, 5, "3-e5m2"])
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5, "3-e5m2", "3-int8"])
 def test_full_size_prefill_bit_exact(cfg):
     case = W.make_case(H.workload(cfg))
     host, dev, status = _prefill_both(case)

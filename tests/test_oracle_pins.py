@@ -249,6 +249,41 @@ def test_e5m2_encode_saturation_and_signed_zero():
     assert oracle.e5m2_encode(float("nan")) == 0x7F
 
 
+# ------------------------------------------------------------------ INT8
+def test_int8_encode_is_numpy_rint_half_even_clamped():
+    """code = clamp(rint(y), -127, 127): numpy's rint rounds half to even."""
+    rng = np.random.default_rng(15)
+    halves = np.arange(-140, 140.5, 0.5)                # every tie and integer in range
+    y = np.concatenate([halves, rng.uniform(-200, 200, 5000),
+                        np.nextafter(halves, np.inf), np.nextafter(halves, -np.inf)])
+    y = y.astype(np.float32)
+    ref = np.clip(np.rint(y.astype(np.float64)), -127, 127).astype(np.int8)
+    got = np.array([oracle.int8_encode(float(v)) for v in y], dtype=np.int8)
+    assert np.array_equal(got, ref)
+    assert oracle.int8_encode(2.5) == 2 and oracle.int8_encode(3.5) == 4
+    assert oracle.int8_encode(-2.5) == -2 and oracle.int8_encode(-0.5) == 0
+    assert oracle.int8_encode(1e9) == 127 and oracle.int8_encode(-1e9) == -127   # never -128
+    assert oracle.int8_encode(float("nan")) == 0
+
+
+def test_write_int8_scale_is_amax_over_127():
+    rng = np.random.default_rng(16)
+    row = (rng.standard_normal(64) * 2).astype(np.float32)
+    row[9] = -7.25
+    k, v, s, x = _one_block_write(W.INT8, row[None], [0])
+    xr = W.bits_to_f32(x[0, 0], W.BF16)
+    assert s[0, 1, 0] == np.float32(np.float32(7.25) / np.float32(127.0))
+    codes = k[1, 0, 0].view(np.int8)
+    assert codes[9] == -127
+    # dequantized within half a step of the input
+    deq = codes.astype(np.float64) * float(s[0, 1, 0])
+    assert np.all(np.abs(deq - xr) <= 0.5 * float(s[0, 1, 0]) * (1 + 1e-6))
+    # a later, larger token saturates at +-127 under the frozen scale
+    k2, _, s2, _ = _one_block_write(W.INT8, np.stack([row, row * 3]), [0, 1])
+    big = np.abs(row * 3) > 7.25 * 1.01
+    assert np.all(np.abs(k2[1, 0, 1].view(np.int8)[big]) == 127)
+
+
 # ------------------------------------------------------------------ the write
 def _one_block_write(kv_dtype, rows, offsets, head_dim=64, block_size=16, dtype=W.BF16,
                      num_kv_heads=1):
@@ -405,6 +440,8 @@ def _gathered(case, k, v, s, b):
                 fmt = torch.float8_e4m3fn if w.kv_dtype == W.FP8_E4M3 else torch.float8_e5m2
                 dec = torch.from_numpy(np.ascontiguousarray(raw)).view(fmt).double().numpy()
                 out[:, t] = dec * s[j, p, :, None].astype(np.float64)
+            elif w.kv_dtype == W.INT8:
+                out[:, t] = raw.view(np.int8).astype(np.float64) * s[j, p, :, None].astype(np.float64)
             else:
                 lo = (raw & 0xF).astype(np.float64)
                 hi = (raw >> 4).astype(np.float64)
@@ -414,10 +451,12 @@ def _gathered(case, k, v, s, b):
     return kd, vd
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, "3-e5m2"])
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, "3-e5m2", "3-int8"])
 def test_attention_matches_sdpa_on_gathered_kv(cfg):
     if cfg == "3-e5m2":
         w = W.CONFIGS[3].scaled(batch=3, ctx_cap=70, seed=106, kv_dtype=W.FP8_E5M2)
+    elif cfg == "3-int8":
+        w = W.CONFIGS[3].scaled(batch=3, ctx_cap=70, seed=107, kv_dtype=W.INT8)
     else:
         w = W.CONFIGS[cfg].scaled(batch=3, ctx_cap=70, seed=100 + cfg)
     case = W.make_case(w)

@@ -41,10 +41,11 @@ from typing import Dict, Optional
 import numpy as np
 
 # dtype tags shared by the C ABI and the oracle (plain integers).
-F16, BF16, FP8_E4M3, INT4_G32, FP8_E5M2 = 0, 1, 2, 3, 4
+F16, BF16, FP8_E4M3, INT4_G32, FP8_E5M2, INT8 = 0, 1, 2, 3, 4, 5
 DTYPE_NAMES = {F16: "f16", BF16: "bf16", FP8_E4M3: "fp8_e4m3", INT4_G32: "int4_g32",
-               FP8_E5M2: "fp8_e5m2"}
+               FP8_E5M2: "fp8_e5m2", INT8: "int8"}
 FP8_TYPES = (FP8_E4M3, FP8_E5M2)
+BLK8_TYPES = (FP8_E4M3, FP8_E5M2, INT8)      # one byte per element, one fp32 scale per block
 
 
 @dataclasses.dataclass(frozen=True)
@@ -158,7 +159,7 @@ def cache_shapes(w: Workload, num_blocks: int):
     nb, h, bs, d = num_blocks, w.num_kv_heads, w.block_size, w.head_dim
     if w.kv_dtype in (F16, BF16):
         return (np.uint16, (nb, h, bs, d)), None
-    if w.kv_dtype in FP8_TYPES:
+    if w.kv_dtype in BLK8_TYPES:
         return (np.uint8, (nb, h, bs, d)), (np.float32, (2, nb, h))
     if w.kv_dtype == INT4_G32:
         return (np.uint8, (nb, h, bs, d // 2)), (np.uint16, (2, nb, h, bs, d // 32, 2))
@@ -296,7 +297,7 @@ def algorithmic_bytes(case: Case, unique: bool = True) -> int:
     if w.kv_dtype in (F16, BF16):
         per_tok_head = 2 * d
         scale_bytes = 0
-    elif w.kv_dtype in FP8_TYPES:
+    elif w.kv_dtype in BLK8_TYPES:
         per_tok_head = d
         nblk = (ctx + bs - 1) // bs
         if unique and w.shared_prefix_tokens:
@@ -316,7 +317,7 @@ def algorithmic_bytes(case: Case, unique: bool = True) -> int:
     write_in = 2 * nwrite * h * d * 2 + w.batch * 8
     if w.kv_dtype in (F16, BF16):
         write_out = 2 * nwrite * h * d * 2
-    elif w.kv_dtype in FP8_TYPES:
+    elif w.kv_dtype in BLK8_TYPES:
         write_out = 2 * nwrite * h * d + 2 * nwrite * h * 4
     else:
         write_out = 2 * nwrite * h * (d // 2 + (d // 32) * 4)
@@ -332,7 +333,7 @@ def attention_bytes(case: Case, unique: bool = True) -> int:
     write_in = 2 * nwrite * h * d * 2 + w.batch * 8
     if w.kv_dtype in (F16, BF16):
         write_out = 2 * nwrite * h * d * 2
-    elif w.kv_dtype in FP8_TYPES:
+    elif w.kv_dtype in BLK8_TYPES:
         write_out = 2 * nwrite * h * d + 2 * nwrite * h * 4
     else:
         write_out = 2 * nwrite * h * (d // 2 + (d // 32) * 4)
