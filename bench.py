@@ -50,6 +50,15 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _tensor_peak():
+    """Dense bf16 tensor peak (TFLOP/s): the measured burst figure, else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
 
@@ -419,6 +428,92 @@ def run_copy(args, rank: int, world: int):
     }
 
 
+def run_prefill(args, rank: int, world: int):
+    """Chunked prefill: time paged_prefill_attention on the prefill workload (8
+    sequences of 4096 cached tokens, chunks of their last 512, Llama-3-8B-shaped)."""
+    import torch
+    import paged_quantized_kv_write_gb300 as pkv
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w, n = W.prefill_workload()
+    if args.kv_dtype:
+        w = _with_kv_dtype(w, args.kv_dtype)
+    case = W.make_case(w)
+    chunk = [min(n, int(c)) for c in case.context_lens]
+    q_bits, q_start = W.prefill_chunk(case, chunk)
+    stream = torch.cuda.Stream(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    with torch.cuda.stream(stream):
+        k, v, s = pkv.alloc_cache(w.kv_dtype, case.num_blocks, w.num_kv_heads, w.head_dim,
+                                  w.block_size, device=dev)
+        slots = np.concatenate([case.prefill_slots, case.new_slots[case.new_slots >= 0]])
+        kk = np.concatenate([case.prefill_k, case.k_new[case.new_slots >= 0]])
+        vv = np.concatenate([case.prefill_v, case.v_new[case.new_slots >= 0]])
+        pkv.paged_kv_write(_bits_to_tensor(kk, w.q_dtype), _bits_to_tensor(vv, w.q_dtype),
+                           torch.from_numpy(slots).to(dev), k, v, s, w.kv_dtype, w.block_size,
+                           w.head_dim, status, stream)
+        q = _bits_to_tensor(q_bits, w.q_dtype)
+        out = torch.empty_like(q)
+        qs = torch.from_numpy(q_start).to(dev)
+        tables = torch.from_numpy(case.block_tables).to(dev)
+        ctx = torch.from_numpy(case.context_lens).to(dev)
+    torch.cuda.synchronize()
+
+    def call(st):
+        pkv.paged_prefill_attention(q, qs, k, v, tables, ctx, s, out, w.softmax_scale,
+                                    w.num_kv_heads, w.kv_dtype, w.block_size, max(chunk),
+                                    status, st)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            call(stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        call(stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        _barrier(world)
+        clocks = ClockSampler(dev.index)
+        clocks.start()
+        time.sleep(0.3)
+        for a, b in ev:
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        clk = clocks.stop()
+    assert status.item() == 0
+    dev_ms = _max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), world)
+    flops = W.prefill_flops(case.context_lens, chunk, w.num_q_heads, w.head_dim)
+    tflops = whole_job_rate(flops, args.steps, dev_ms, world) / 1e12
+    peak, kind = _tensor_peak()
+    kv_bytes = W.attention_bytes(case, unique=True)
+    return {
+        "metric": "chunked-prefill paged attention TFLOP/s (QK^T + PV over each query's causal range), 1 GPU",
+        "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dev_ms / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": W.DTYPE_NAMES[w.kv_dtype] + "+" + W.DTYPE_NAMES[w.q_dtype],
+        "data": "synthetic (seeded N(0,1) q/K/V, shuffled block tables)",
+        "config": {"workload": f"chunked prefill: {w.name}, {w.batch} sequences, chunks of "
+                               f"{max(chunk)} over {int(case.context_lens.max())}-token contexts",
+                   "query_tokens": int(q_start[-1]), "flops_per_step": flops,
+                   "kv_bytes_per_step": kv_bytes},
+        "roofline": {"kernel": "paged_decode_kernel (prefill mode, mma.sync)", "bound": "tensor",
+                     "achieved": round(tflops / world, 2), "peak": peak,
+                     "peak_kind": f"{kind} (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)",
+                     "unit": "TFLOP/s", "frac": round(tflops / world / peak, 4), "traffic": None},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+
+
 def _traffic(config: int):
     """DRAM bytes per launch of the decode kernel from a committed ncu summary, if one
     exists for this workload and the current kernel source."""
@@ -570,8 +665,9 @@ def main():
     ap.add_argument("--unfused", action="store_true",
                     help="run the step as paged_kv_write then paged_decode_attention (two "
                          "launches) instead of paged_decode_attention_with_write (one)")
-    ap.add_argument("--op", default="step", choices=["step", "copy"],
-                    help="step: the decode step (default); copy: copy-on-write block copies")
+    ap.add_argument("--op", default="step", choices=["step", "copy", "prefill"],
+                    help="step: the decode step (default); copy: copy-on-write block copies; "
+                         "prefill: chunked-prefill attention")
     ap.add_argument("--copy-pairs", type=int, default=4096,
                     help="--op copy: block pairs copied per step")
     ap.add_argument("--partition", type=int, default=0,
@@ -592,8 +688,8 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
-    if args.op == "copy":
-        res = run_copy(args, rank, world)
+    if args.op in ("copy", "prefill"):
+        res = (run_copy if args.op == "copy" else run_prefill)(args, rank, world)
         if rank == 0:
             print(json.dumps(res), flush=True)
         if world > 1:

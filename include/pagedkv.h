@@ -196,6 +196,38 @@ int paged_decode_attention_with_write(const void* q, int q_dtype, const void* k_
                                       void* workspace, size_t workspace_bytes, int* dev_status,
                                       void* stream);
 
+/* paged_prefill_attention — chunked-prefill attention over the paged cache:
+ * each sequence brings a chunk of new query tokens whose K/V are already in
+ * the cache (written with paged_kv_write), and each query attends causally
+ * to every cached token up to its own position.  The pages pair
+ * PagedAttention with chunked prefill (publishertech page, section 5,
+ * "Production Benchmarks & Implementation"); the causal rule is the usual
+ * prefill one.
+ *
+ * q              [q_start[num_seqs]][num_q_heads][head_dim] in q_dtype: the
+ *                chunks of all sequences, back to back.
+ * q_start        int32 [num_seqs + 1], device: sequence b's queries are rows
+ *                q_start[b] .. q_start[b+1] - 1 (a chunk of n_b tokens).
+ * max_query_len  an upper bound of every n_b (sizes the grid); queries past it
+ *                are not computed.
+ * context_lens   int32 [num_seqs]: tokens in the cache, the chunk included.
+ *                Query j of sequence b sits at position ctx_b - n_b + j and
+ *                attends to tokens 0 .. ctx_b - n_b + j.  A chunk longer than
+ *                its context is flagged (PKV_ERR_DEVICE_BOUNDS); its queries
+ *                at negative positions give zeros.
+ * out            [q_start[num_seqs]][num_q_heads][head_dim] in q_dtype.
+ * Everything else as for paged_decode_attention (no workspace: no split-KV).
+ * Supported: as paged_decode_attention, with num_q_heads / num_kv_heads in
+ * {1, 2, 4, 8}.
+ */
+int paged_prefill_attention(const void* q, int q_dtype, const int32_t* q_start,
+                            int max_query_len, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* context_lens, int num_seqs, const void* scales,
+                            int kv_dtype, int num_blocks, void* out, float softmax_scale,
+                            int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                            int* dev_status, void* stream);
+
 /* paged_decode_attention_noalloc — paged_decode_attention without a
  * caller-supplied workspace, for callers that cannot allocate device memory.
  * The pages have no counterpart: this is a convenience of this library.

@@ -62,6 +62,9 @@ def lib() -> ctypes.CDLL:
         L.oracle_decode_attention_pairs.restype = I32
         L.oracle_dequant_row.argtypes = [P, P, I32, I32, I32, I32, I32, I32, I32, I32, I32, P]
         L.oracle_dequant_row.restype = I32
+        L.oracle_prefill_attention.argtypes = [P, I32, P, P, P, P, I32, P, I32, P, I32, I32, P, D,
+                                                I32, I32, I32, I32, I32]
+        L.oracle_prefill_attention.restype = I32
         L.oracle_copy_blocks.argtypes = [P, P, P, I32, P, I32, I32, I32, I32, I32]
         L.oracle_copy_blocks.restype = I32
         L.oracle_max_threads.argtypes = []
@@ -184,6 +187,25 @@ def decode_attention(q, q_dtype, k_cache, v_cache, block_tables, context_lens, s
                                       num_kv_heads, head_dim, block_size, num_threads)
     if r:
         raise ValueError(f"oracle_decode_attention failed ({r})")
+    return out
+
+
+def prefill_attention(q, q_dtype, q_start, k_cache, v_cache, block_tables, context_lens, scales,
+                      kv_dtype, num_blocks, softmax_scale, num_q_heads, num_kv_heads, head_dim,
+                      block_size, num_threads: int = 0) -> np.ndarray:
+    """Chunked prefill: rows q_start[b]..q_start[b+1]-1 of q are sequence b's chunk."""
+    q = np.ascontiguousarray(q, np.uint16)
+    qs = np.ascontiguousarray(q_start, np.int32)
+    bt = np.ascontiguousarray(block_tables, np.int32)
+    cl = np.ascontiguousarray(context_lens, np.int32)
+    out = np.zeros((int(qs[-1]), num_q_heads, head_dim), np.float64)
+    r = lib().oracle_prefill_attention(_ptr(q), q_dtype, _ptr(qs), _ptr(k_cache), _ptr(v_cache),
+                                       _ptr(bt), bt.shape[1], _ptr(cl), len(cl), _ptr(scales),
+                                       kv_dtype, num_blocks, _ptr(out), softmax_scale,
+                                       num_q_heads, num_kv_heads, head_dim, block_size,
+                                       num_threads)
+    if r:
+        raise ValueError(f"oracle_prefill_attention failed ({r})")
     return out
 
 

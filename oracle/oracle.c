@@ -42,6 +42,8 @@
  *  R8  FP8 E5M2 (1 sign, 5 exponent, 2 mantissa bits; the pages name E4M3
  *      only): the same block-wise recipe as R4/R5 with 57344, E5M2's
  *      largest finite value, in place of 448.
+ *  R18 chunked prefill: query j of a chunk of n over a context of c tokens
+ *      sits at position c - n + j and sees tokens 0 .. c - n + j (causal).
  *  R9  INT8 (the pages give one byte per element and no format): the same
  *      block-wise recipe with 127: scale = max(amax / 127, 1e-12), code =
  *      clamp(rint(x / scale), -127, 127) of the fp32 quotient, round half to
@@ -612,6 +614,64 @@ int oracle_decode_attention(const uint16_t* q, int q_dtype,
     free(ps);
     free(ph);
     return r;
+}
+
+/* Chunked prefill (R18): sequence b's queries are rows q_start[b] ..
+ * q_start[b+1] - 1 of q; query j sits at position pos = ctx_b - n_b + j and
+ * attends to tokens 0 .. pos (the plain softmax definition over them, as
+ * attend_one); a query at a negative position gives zeros.  out: fp64
+ * [q_start[num_seqs]][num_q_heads][head_dim]. */
+int oracle_prefill_attention(const uint16_t* q, int q_dtype, const int32_t* q_start,
+                             const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, int max_blocks_per_seq,
+                             const int32_t* context_lens, int num_seqs, const void* scales,
+                             int kv_dtype, int num_blocks, double* out, double softmax_scale,
+                             int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                             int num_threads) {
+    if (check_attn(q_dtype, kv_dtype, num_blocks, num_q_heads, num_kv_heads, head_dim,
+                   block_size, num_seqs))
+        return -1;
+    int rows = num_seqs > 0 ? q_start[num_seqs] : 0;
+    int max_ctx = 0;
+    for (int b = 0; b < num_seqs; ++b) {
+        if (q_start[b + 1] < q_start[b]) return -1;
+        if (context_lens[b] > max_ctx) max_ctx = context_lens[b];
+    }
+    int32_t* seq_of = (int32_t*)malloc(sizeof(int32_t) * (size_t)(rows + 1));
+    if (!seq_of) return -2;
+    for (int b = 0; b < num_seqs; ++b)
+        for (int r = q_start[b]; r < q_start[b + 1]; ++r) seq_of[r] = b;
+    int err = 0;
+#ifdef _OPENMP
+    if (num_threads <= 0) num_threads = omp_get_max_threads();
+#pragma omp parallel num_threads(num_threads) reduction(| : err)
+#endif
+    {
+        double* scratch = (double*)malloc(sizeof(double) * (2 * (size_t)head_dim + max_ctx + 1));
+        if (!scratch) {
+            err |= 1;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+            for (int i = 0; i < rows * num_q_heads; ++i) {
+                int r = i / num_q_heads, h = i % num_q_heads, b = seq_of[r];
+                int n = q_start[b + 1] - q_start[b];
+                int pos = context_lens[b] - n + (r - q_start[b]);
+                double* o = out + (int64_t)i * head_dim;
+                /* attend_one reads row r of q (its `seq` argument) over pos + 1 tokens */
+                if (attend_one(q, q_dtype, k_cache, v_cache,
+                               block_tables + (int64_t)b * max_blocks_per_seq, max_blocks_per_seq,
+                               pos + 1, scales, kv_dtype, num_blocks, o, softmax_scale,
+                               num_q_heads, num_kv_heads, head_dim, block_size, r, h, scratch))
+                    err |= 1;
+            }
+            free(scratch);
+        }
+    }
+    free(seq_of);
+    (void)num_threads;
+    return err ? -1 : 0;
 }
 
 int oracle_max_threads(void) {

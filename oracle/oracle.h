@@ -72,6 +72,15 @@ int oracle_decode_attention_pairs(const uint16_t* q, int q_dtype,
                                   int block_size, const int32_t* pair_seq,
                                   const int32_t* pair_head, int n_pairs, int num_threads);
 
+/* chunked prefill: out fp64 [q_start[num_seqs], num_q_heads, head_dim] */
+int oracle_prefill_attention(const uint16_t* q, int q_dtype, const int32_t* q_start,
+                             const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, int max_blocks_per_seq,
+                             const int32_t* context_lens, int num_seqs, const void* scales,
+                             int kv_dtype, int num_blocks, double* out, double softmax_scale,
+                             int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                             int num_threads);
+
 /* dequantized K or V row of one token/head (fp64) */
 int oracle_dequant_row(const void* cache, const void* scales, int which_kv, int kv_dtype,
                        int num_blocks, int num_kv_heads, int head_dim, int block_size,

@@ -13,6 +13,7 @@ Calls (same names as the C ABI):
                            softmax_scale, num_kv_heads, kv_dtype, block_size, ...)
     paged_decode_attention_with_write(q, k_new, v_new, slot_mapping, k_cache, v_cache, ...)
     paged_kv_copy_blocks(k_cache, v_cache, scales, kv_dtype, block_pairs, ...)
+    paged_prefill_attention(q, q_start, k_cache, v_cache, block_tables, context_lens, ...)
     paged_decode_workspace_bytes(...), paged_decode_partition_size(...)
 """
 
@@ -45,6 +46,9 @@ def _load() -> ctypes.CDLL:
     lib.paged_decode_attention_with_write.argtypes = [P, I, P, P, P, P, P, P, I, P, I, P, I, I,
                                                       P, F, I, I, I, I, I, P, SZ, P, P]
     lib.paged_decode_attention_with_write.restype = I
+    lib.paged_prefill_attention.argtypes = [P, I, P, I, P, P, P, I, P, I, P, I, I, P, F, I, I, I,
+                                            I, P, P]
+    lib.paged_prefill_attention.restype = I
     lib.paged_kv_copy_blocks.argtypes = [P, P, P, I, P, I, I, I, I, I, P, P]
     lib.paged_kv_copy_blocks.restype = I
     lib.paged_decode_attention.argtypes = [P, I, P, P, P, I, P, I, P, I, I, P, F, I, I, I, I, I,
@@ -212,6 +216,27 @@ def paged_decode_attention_with_write(q: torch.Tensor, k_new: torch.Tensor, v_ne
         _ptr(dev_status), _stream(stream))
     if r != PKV_OK:
         raise PagedKVError(r, "paged_decode_attention_with_write")
+
+
+def paged_prefill_attention(q: torch.Tensor, q_start: torch.Tensor, k_cache: torch.Tensor,
+                            v_cache: torch.Tensor, block_tables: torch.Tensor,
+                            context_lens: torch.Tensor, scales: Optional[torch.Tensor],
+                            out: torch.Tensor, softmax_scale: float, num_kv_heads: int,
+                            kv_dtype: int, block_size: int, max_query_len: int,
+                            dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Chunked prefill: q/out [T, Hq, D] (sequence b's chunk = rows q_start[b]..q_start[b+1]-1),
+    q_start int32 [B + 1]; each query attends causally up to its own position."""
+    if q_start.dtype != torch.int32 or block_tables.dtype != torch.int32 or \
+            context_lens.dtype != torch.int32:
+        raise TypeError("q_start, block_tables and context_lens must be int32")
+    t, hq, d = q.shape
+    r = _lib.paged_prefill_attention(
+        _ptr(q), _dtype_code(q), _ptr(q_start), int(max_query_len), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), context_lens.numel(),
+        _ptr(scales), kv_dtype, k_cache.shape[0], _ptr(out), float(softmax_scale), hq,
+        num_kv_heads, d, block_size, _ptr(dev_status), _stream(stream))
+    if r != PKV_OK:
+        raise PagedKVError(r, "paged_prefill_attention")
 
 
 def make_workspace(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,

@@ -168,6 +168,45 @@ int paged_decode_attention(const void* q, int q_dtype,
                      partition_size, workspace, workspace_bytes, dev_status, stream);
 }
 
+int paged_prefill_attention(const void* q, int q_dtype, const int32_t* q_start,
+                            int max_query_len, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* context_lens, int num_seqs, const void* scales,
+                            int kv_dtype, int num_blocks, void* out, float softmax_scale,
+                            int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                            int* dev_status, void* stream) {
+  if (num_seqs < 0 || num_blocks <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      max_blocks_per_seq <= 0 || max_query_len < 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads) return PKV_ERR_INVALID_ARG;
+  if (!ok_half_dtype(q_dtype) || !ok_kv_dtype(kv_dtype)) return PKV_ERR_UNSUPPORTED;
+  if ((kv_dtype == PKV_F16 || kv_dtype == PKV_BF16) && q_dtype != kv_dtype)
+    return PKV_ERR_UNSUPPORTED;
+  if (!ok_head_dim(head_dim) || !ok_block_size(block_size)) return PKV_ERR_UNSUPPORTED;
+  const int group = num_q_heads / num_kv_heads;
+  if (8 % group) return PKV_ERR_UNSUPPORTED;                 // G in {1, 2, 4, 8}
+  if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(max_blocks_per_seq) * block_size > 0x7FFFFFFF) return PKV_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(num_blocks) * num_kv_heads >= (int64_t(1) << 27)) return PKV_ERR_UNSUPPORTED;
+  if (!(softmax_scale == softmax_scale)) return PKV_ERR_INVALID_ARG;
+  if (num_seqs == 0 || max_query_len == 0) return PKV_OK;
+  if (!q || !q_start || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return PKV_ERR_INVALID_ARG;
+  const bool quant = kv_dtype != PKV_F16 && kv_dtype != PKV_BF16;
+  if (quant && !scales) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+      (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(q_start) & 3u) || (quant && !aligned16(scales)))
+    return PKV_ERR_INVALID_ARG;
+  pkv::PrefillArgs a{q, q_dtype, q_start, max_query_len, k_cache, v_cache, block_tables,
+                     max_blocks_per_seq, context_lens, num_seqs, scales, kv_dtype, num_blocks,
+                     out, softmax_scale, num_q_heads, num_kv_heads, head_dim, block_size,
+                     dev_status};
+  cudaError_t e = pkv::launch_prefill(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 int paged_decode_attention_with_write(const void* q, int q_dtype, const void* k_new,
                                       const void* v_new, const int64_t* slot_mapping,
                                       void* k_cache, void* v_cache,

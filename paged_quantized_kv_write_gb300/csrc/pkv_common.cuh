@@ -132,6 +132,14 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
   return *reinterpret_cast<uint32_t*>(&r);
 }
+// f16x2 a * b + c with one rounding
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+  __half2 r = __hfma2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b),
+                      *reinterpret_cast<__half2*>(&c));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+// f16x2 negation (sign flip)
+__device__ __forceinline__ uint32_t hneg2(uint32_t a) { return a ^ 0x80008000u; }
 
 // ------------------------------------------------------------------ tensor cores
 // D = A(16x16, row) * B(16x8, col) + D, fp32 accumulate (mma.sync m16n8k16).

@@ -53,6 +53,29 @@ struct DecodeArgs {
   const int64_t* slot_mapping = nullptr;
 };
 
+struct PrefillArgs {
+  const void* q;                 // [q_start[num_seqs]][num_q_heads][head_dim]
+  int q_dtype;
+  const int32_t* q_start;        // [num_seqs + 1]
+  int max_query_len;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  int max_blocks_per_seq;
+  const int32_t* context_lens;
+  int num_seqs;
+  const void* scales;
+  int kv_dtype;
+  int num_blocks;
+  void* out;
+  float softmax_scale;
+  int num_q_heads;
+  int num_kv_heads;
+  int head_dim;
+  int block_size;
+  int* dev_status;
+};
+
 struct CopyArgs {
   void* k_cache;
   void* v_cache;
@@ -69,6 +92,7 @@ struct CopyArgs {
 
 cudaError_t launch_kv_write(const WriteArgs& a, cudaStream_t st);
 cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t st);
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 
 int resolve_partition_size(int num_seqs, int num_q_heads, int num_kv_heads,

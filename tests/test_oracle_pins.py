@@ -666,3 +666,76 @@ def test_copy_on_write_fork_attends_like_the_shared_block(kv):
                                   case.num_blocks, w.softmax_scale, w.num_q_heads,
                                   w.num_kv_heads, w.head_dim, w.block_size)
     assert np.array_equal(out, ref)
+
+
+# ------------------------------------------------------------------ chunked prefill
+def _full_cache(case):
+    """The case's cache with every context token written (the new one included)."""
+    w = case.w
+    k, v, s = oracle.prefill_case(case)
+    oracle.kv_write(case.k_new, case.v_new, w.q_dtype, case.new_slots, k, v, s, w.kv_dtype,
+                    case.num_blocks, w.num_kv_heads, w.head_dim, w.block_size)
+    return k, v, s
+
+
+def _prefill(case, k, v, s, q, q_start, ctx=None):
+    w = case.w
+    return oracle.prefill_attention(q, w.q_dtype, q_start, k, v, case.block_tables,
+                                    case.context_lens if ctx is None else ctx, s, w.kv_dtype,
+                                    case.num_blocks, w.softmax_scale, w.num_q_heads,
+                                    w.num_kv_heads, w.head_dim, w.block_size)
+
+
+@pytest.mark.parametrize("kv", [W.BF16, W.FP8_E4M3, W.INT8, W.INT4_G32])
+def test_prefill_matches_causal_sdpa_on_gathered_kv(kv):
+    w = W.Workload("pf", 3, 8, 2, 64, 16, kv, W.BF16, "uniform", 20, 60, seed=40 + kv)
+    case = W.make_case(w)
+    k, v, s = _full_cache(case)
+    n = [5, 1, 17]
+    q, q_start = W.prefill_chunk(case, n)
+    out = _prefill(case, k, v, s, q, q_start)
+    for b in range(w.batch):
+        kd, vd = _gathered(case, k, v, s, b)                  # [Hkv, ctx, D], torch decoders
+        c = int(case.context_lens[b])
+        rows = slice(q_start[b], q_start[b + 1])
+        qb = W.bits_to_f32(q[rows], w.q_dtype).astype(np.float64)      # [n, Hq, D]
+        pos = c - n[b] + np.arange(n[b])
+        mask = torch.from_numpy(np.arange(c)[None, :] <= pos[:, None])  # [n, ctx]
+        kt = torch.from_numpy(np.repeat(kd, w.group, 0))[None]          # [1, Hq, ctx, D]
+        vt = torch.from_numpy(np.repeat(vd, w.group, 0))[None]
+        qt = torch.from_numpy(qb.transpose(1, 0, 2).copy())[None]       # [1, Hq, n, D]
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask,
+                                                               scale=w.softmax_scale)
+        assert np.allclose(out[rows], ref[0].numpy().transpose(1, 0, 2), rtol=0, atol=1e-12), b
+
+
+def test_prefill_chunk_split_invariance_and_decode_limit():
+    w = W.Workload("pf", 2, 8, 4, 64, 16, W.FP8_E4M3, W.BF16, "fixed", 50, 50, seed=9)
+    case = W.make_case(w)
+    k, v, s = _full_cache(case)
+    q, q_start = W.prefill_chunk(case, [12, 12])
+    whole = _prefill(case, k, v, s, q, q_start)
+    # the same queries as two chunks: the first 7 over a context 5 shorter, then the last 5
+    first = np.concatenate([q[0:7], q[12:19]])
+    out_a = _prefill(case, k, v, s, first, np.array([0, 7, 14], np.int32),
+                     ctx=case.context_lens - 5)
+    second = np.concatenate([q[7:12], q[19:24]])
+    out_b = _prefill(case, k, v, s, second, np.array([0, 5, 10], np.int32))
+    assert np.array_equal(whole[0:7], out_a[0:7]) and np.array_equal(whole[12:19], out_a[7:14])
+    assert np.array_equal(whole[7:12], out_b[0:5]) and np.array_equal(whole[19:24], out_b[5:10])
+    # a chunk of one is a decode step with that query
+    one = _prefill(case, k, v, s, case.q, np.array([0, 1, 2], np.int32))
+    dec = oracle.decode_attention(case.q, w.q_dtype, k, v, case.block_tables, case.context_lens,
+                                  s, w.kv_dtype, case.num_blocks, w.softmax_scale,
+                                  w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size)
+    assert np.array_equal(one, dec)
+
+
+def test_prefill_negative_positions_give_zeros():
+    w = W.Workload("pf", 1, 4, 2, 64, 16, W.BF16, W.BF16, "fixed", 6, 6, seed=3)
+    case = W.make_case(w)
+    k, v, s = _full_cache(case)
+    q, q_start = W.prefill_chunk(case, [9])               # 9 queries over 6 tokens
+    out = _prefill(case, k, v, s, q, q_start)
+    assert not out[:3].any()                              # positions -3, -2, -1
+    assert np.abs(out[3:]).sum() > 0

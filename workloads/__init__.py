@@ -280,6 +280,42 @@ def make_case(w: Workload, identity_tables: bool = False,
                 new_slots, k_new, v_new)
 
 
+def prefill_chunk(case: Case, chunk_lens, seed: int = 0):
+    """Queries for a chunked-prefill step over ``case``'s cache.
+
+    ``chunk_lens[b]`` new query tokens per sequence (their K/V are the last
+    ``chunk_lens[b]`` context tokens, already in the case's cache once the
+    decode step's new token is written).  Returns (q bits [sum n, Hq, D] in
+    the query dtype, q_start int32 [B + 1]).
+    """
+    w = case.w
+    n = np.asarray(chunk_lens, dtype=np.int64)
+    q_start = np.zeros(w.batch + 1, dtype=np.int32)
+    q_start[1:] = np.cumsum(n)
+    rng = np.random.default_rng(10_000 + w.seed * 7 + seed)
+    q = to_bits(rng.standard_normal((int(q_start[-1]), w.num_q_heads, w.head_dim),
+                                    dtype=np.float32), w.q_dtype)
+    return q, q_start
+
+
+def prefill_workload():
+    """Chunked-prefill benchmark workload: workload 2's Llama-3-8B-shaped bf16 layer
+    (32/8 heads, D 128, bs 16, 4096-token contexts) for 8 sequences, each of which
+    brings a chunk of its last 512 tokens.  Returns (workload, chunk length)."""
+    return CONFIGS[2].scaled(batch=8, seed=2002), 512
+
+
+def prefill_flops(context_lens, chunk_lens, num_q_heads: int, head_dim: int) -> int:
+    """Multiply-adds x 2 of a chunked-prefill step: QK^T and PV over each query's
+    causal range (query j of a chunk of n over c tokens sees c - n + j + 1)."""
+    total = 0
+    for c, n in zip(np.asarray(context_lens, np.int64), np.asarray(chunk_lens, np.int64)):
+        first = max(0, int(c) - int(n))
+        seen = int(n) * (first + 1) + int(n) * (int(n) - 1) // 2      # sum over j of first + j + 1
+        total += seen
+    return 4 * total * num_q_heads * head_dim
+
+
 def algorithmic_bytes(case: Case, unique: bool = True) -> int:
     """Bytes one decode step must move at minimum (attention + the write).
 
