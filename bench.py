@@ -532,7 +532,7 @@ def _traffic(config: int):
 def _kernel_sha() -> str:
     import hashlib
     h = hashlib.sha256()
-    for name in ("pkv_decode.cu", "pkv_common.cuh"):
+    for name in ("pkv_attn.cuh", "pkv_decode.cu", "pkv_common.cuh"):
         with open(os.path.join(ROOT, "paged_quantized_kv_write_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
