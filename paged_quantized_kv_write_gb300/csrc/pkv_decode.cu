@@ -129,10 +129,14 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t st) {
   }
   const int64_t units = static_cast<int64_t>(a.num_partitions) * a.num_seqs * a.num_kv_heads;
   bool wu = a.num_partitions > 1 && units >= static_cast<int64_t>(PKV_WU_WAVES) * sms * 16;
-  // PKV_DECODE_MODE=shared|warp overrides the choice (both give the same results)
+  // PKV_DECODE_MODE=shared|warp overrides the choice (both give the same
+  // results); =simt runs the CUDA-core comparator instead (16-bit, FP8 and
+  // INT8 caches without the fused write; other calls keep the tensor path)
   if (const char* m = getenv("PKV_DECODE_MODE")) {
     if (!strcmp(m, "shared")) wu = false;
     if (!strcmp(m, "warp")) wu = true;
+    if (!strcmp(m, "simt") && KV != PKV_INT4_G32 && a.slot_mapping == nullptr)
+      return launch_simt(a, st);
   }
   return wu ? launch_mode<KV, QT, D, true>(a, st) : launch_mode<KV, QT, D, false>(a, st);
 }
@@ -143,6 +147,28 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t st) {
 }
 
 }  // namespace
+
+// the log-sum-exp merge of a split-KV call's partitions (also used by the
+// SIMT comparator)
+cudaError_t launch_lse_reduce(const DecodeArgs& a, cudaStream_t st) {
+  Params p = {};
+  p.context_lens = a.context_lens;
+  p.out = a.out;
+  p.ws_out = a.ws_out;
+  p.ws_ml = a.ws_ml;
+  p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.num_q_heads = a.num_q_heads;
+  p.block_size = a.block_size;
+  p.partition_size = a.partition_size;
+  p.num_partitions = a.num_partitions;
+  const dim3 grid(a.num_seqs * a.num_q_heads);
+  if (a.q_dtype == PKV_F16) {
+    return a.head_dim == 64 ? launch_pdl(pkv_lse_reduce<PKV_F16, 64>, grid, dim3(64), 0, st, p)
+                            : launch_pdl(pkv_lse_reduce<PKV_F16, 128>, grid, dim3(128), 0, st, p);
+  }
+  return a.head_dim == 64 ? launch_pdl(pkv_lse_reduce<PKV_BF16, 64>, grid, dim3(64), 0, st, p)
+                          : launch_pdl(pkv_lse_reduce<PKV_BF16, 128>, grid, dim3(128), 0, st, p);
+}
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   if (a.num_seqs == 0) return cudaSuccess;

@@ -93,6 +93,8 @@ struct CopyArgs {
 cudaError_t launch_kv_write(const WriteArgs& a, cudaStream_t st);
 cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t st);
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t st);
+cudaError_t launch_lse_reduce(const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_simt(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 
 int resolve_partition_size(int num_seqs, int num_q_heads, int num_kv_heads,

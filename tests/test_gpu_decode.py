@@ -16,9 +16,11 @@ from tests import helpers as H
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["shared", "warp"])
+@pytest.fixture(params=["shared", "warp", "simt"])
 def mode(request, monkeypatch):
-    """Run a test under both work splits of the decode kernel."""
+    """Run a test under both work splits of the decode kernel and under the SIMT
+    comparator (which takes 16-bit, FP8 and INT8 caches; INT4 stays on the
+    tensor path)."""
     monkeypatch.setenv("PKV_DECODE_MODE", request.param)
     return request.param
 
