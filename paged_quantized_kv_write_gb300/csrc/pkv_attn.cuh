@@ -222,8 +222,10 @@ struct Params {
 // (offset in the block / 16), or -1 for a block id out of range; `live` is
 // false past the unit's end.  `stage` is the sub-tile's shared-memory base,
 // `misc_smem`/`misc` its 16-byte misc slot.  Sub-tiles that copy nothing are
-// marked empty.
-template <int KV, int D>
+// marked empty.  L1: also allocate the rows in L1 (prefill, where the CTA's
+// warps stream the same tiles; decode reads each tile once and runs faster
+// without).
+template <int KV, int D, bool L1 = false>
 __device__ __forceinline__ void issue_tile(const Params& p, int rowp, bool live, uint32_t stage,
                                            uint32_t misc_smem, int* misc, int lane) {
   using G = Geo<KV, D>;
@@ -245,8 +247,13 @@ __device__ __forceinline__ void issue_tile(const Params& p, int rowp, bool live,
     if (kChunks % kWarp == 0 || ch < kChunks) {
       const int r = ch / G::kCpr, c = ch % G::kCpr;
       const uint32_t o = chunk_off<KV, D>(r, c);
-      cp_async_16(stage + o, ksrc + ch * 16);
-      cp_async_16(stage + G::kTileBytes + o, vsrc + ch * 16);
+      if constexpr (L1) {
+        cp_async_16_ca(stage + o, ksrc + ch * 16);
+        cp_async_16_ca(stage + G::kTileBytes + o, vsrc + ch * 16);
+      } else {
+        cp_async_16(stage + o, ksrc + ch * 16);
+        cp_async_16(stage + G::kTileBytes + o, vsrc + ch * 16);
+      }
     }
   }
   if constexpr (KV == PKV_INT4_G32) {
@@ -612,7 +619,7 @@ paged_decode_kernel(const Params p) {
 #pragma unroll
       for (int u = 0; u < G::kSub; ++u) {
         const int rowp = __shfl_sync(0xffffffffu, i_tb, (k + u) & 31);
-        issue_tile<KV, D>(p, rowp, iunit.tok_begin + it * G::kTileTok + u * kTile < iunit.tok_end,
+        issue_tile<KV, D, PF>(p, rowp, iunit.tok_begin + it * G::kTileTok + u * kTile < iunit.tok_end,
                           sb + u * G::kSubBytes, sb + G::kMiscOffset + 16 * u,
                           reinterpret_cast<int*>(sp + G::kMiscOffset + 16 * u), lane);
       }

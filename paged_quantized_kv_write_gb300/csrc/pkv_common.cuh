@@ -206,6 +206,10 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void* src) 
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src)
                : "memory");
 }
+// the same, also allocating the line in L1
+__device__ __forceinline__ void cp_async_16_ca(uint32_t dst_smem, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
