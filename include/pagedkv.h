@@ -63,7 +63,10 @@ typedef enum {
     PKV_ERR_UNSUPPORTED = 2,    /* a shape or dtype combination this build has no kernel for */
     PKV_ERR_CUDA = 3,           /* a CUDA launch failed (see cudaGetLastError) */
     PKV_ERR_DEVICE_BOUNDS = 4,  /* written to *dev_status by a kernel, never returned */
-    PKV_ERR_WORKSPACE = 5       /* workspace missing or smaller than required */
+    PKV_ERR_WORKSPACE = 5,      /* workspace missing or smaller than required */
+    PKV_ERR_DEVICE_TIMEOUT = 8  /* ORed into *dev_status by a kernel whose wait for its own
+                                   asynchronous work ran out (the launch then stops early
+                                   and its outputs are undefined); never returned */
 } pkv_status;
 
 /* paged_kv_write — quantize-on-write of new K/V rows into their slots.

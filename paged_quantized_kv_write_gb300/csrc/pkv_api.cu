@@ -232,6 +232,7 @@ const char* paged_kv_status_string(int status) {
     case PKV_ERR_CUDA: return "CUDA launch failed";
     case PKV_ERR_DEVICE_BOUNDS: return "block id or slot outside the pool";
     case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKV_ERR_DEVICE_TIMEOUT: return "a kernel's wait for its own asynchronous work timed out";
     default: return "unknown status";
   }
 }

@@ -94,6 +94,8 @@ cudaError_t launch_kv_write(const WriteArgs& a, cudaStream_t st);
 cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t st);
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t st);
 cudaError_t launch_lse_reduce(const DecodeArgs& a, cudaStream_t st);
+bool prefill_tc_supported(const PrefillArgs& a);
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st);
 cudaError_t launch_simt(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 

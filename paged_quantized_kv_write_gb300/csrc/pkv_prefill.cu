@@ -78,6 +78,10 @@ cudaError_t launch_prefill_q(const PrefillArgs& a, cudaStream_t st) {
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t st) {
   if (a.num_seqs == 0 || a.max_query_len == 0) return cudaSuccess;
+  // 16-bit caches with head_dim 128 run on the tcgen05 kernel
+  // (pkv_prefill_tc.cu); PKV_PREFILL_MODE=mma keeps them on this one
+  const char* mode = getenv("PKV_PREFILL_MODE");
+  if (prefill_tc_supported(a) && !(mode && !strcmp(mode, "mma"))) return launch_prefill_tc(a, st);
   switch (a.kv_dtype) {
     case PKV_F16: return launch_prefill_q<PKV_F16>(a, st);
     case PKV_BF16: return launch_prefill_q<PKV_BF16>(a, st);

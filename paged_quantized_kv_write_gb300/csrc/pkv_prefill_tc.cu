@@ -1,0 +1,513 @@
+// Chunked-prefill attention on the fifth-generation tensor cores (tcgen05,
+// accumulators in tensor memory) for 16-bit caches with head_dim 128.
+// Chunked prefill is a dense contraction (every cached token meets a whole
+// chunk of queries), unlike the decode step, so it runs where the dense
+// tensor throughput is: "Optimizing KV-Cache Memory Footprint in
+// High-Throughput LLM Serving", section 5, pairs PagedAttention with GQA and
+// chunked prefill; query j of a chunk of n over c cached tokens sits at
+// position c - n + j and sees tokens 0 .. c - n + j.
+//
+// One CTA (one warpgroup, 128 threads) takes 128 query rows -- 128/G query
+// tokens of one sequence times the G query heads of one KV head -- and walks
+// that KV head's cache in 64-token tiles:
+//   1. the tile's K rows and V rows come in with 16-byte cp.async through the
+//      block table (one row locator per token); V is then transposed in
+//      shared memory (ldmatrix.trans) so every MMA operand is K-major;
+//   2. S = Q K^T: eight tcgen05.mma (M 128, N 64, K 16) into tensor memory;
+//   3. thread r reads row r of S from tensor memory, applies the causal mask
+//      and the online softmax (running max raised lazily, by more than
+//      2^8 only), and writes P as a 16-bit hi + lo pair;
+//   4. O += P V: eight tcgen05.mma (M 128, N 128, K 16) into tensor memory,
+//      hi then lo;
+// and finally reads O from tensor memory, divides by the row sums and writes
+// the output rows.  Operands sit in shared memory in the canonical K-major
+// layout without swizzle: 8 x 16-byte core matrices, consecutive along K
+// (leading byte offset 128) and 8-row groups further apart (stride byte
+// offset).  Every wait for the tensor cores is bounded: when one runs out
+// the launch ORs PKV_ERR_DEVICE_TIMEOUT into dev_status, stops, and still
+// frees its tensor memory.
+#include <math.h>
+#include <stdint.h>
+
+#include "pagedkv.h"
+#include "pkv_common.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kTcThreads = 128;      // one warpgroup; thread r owns query row r
+constexpr int kTcRows = 128;         // MMA M
+constexpr int kTcKv = 64;            // KV tokens per tile
+constexpr int kTcD = 128;            // head_dim
+constexpr uint32_t kTmemCols = 256;  // S: columns [0, 64); O: [64, 192)
+constexpr float kTcTau = 8.f;        // lazy rescale threshold (log2 units)
+constexpr long long kTcWaitCycles = 4000000000LL;   // bounded wait: ~2 s of SM clock
+
+// shared-memory plan (bytes; every operand tile 1024-byte aligned)
+constexpr int kQBytes = kTcRows * kTcD * 2;       // 32 KiB
+constexpr int kKBytes = kTcKv * kTcD * 2;         // 16 KiB
+constexpr int kVStride = kTcD * 2 + 16;           // V staging row stride (padded: no bank conflicts)
+constexpr int kVsBytes = kTcKv * kVStride;        // 17 KiB
+constexpr int kVtBytes = kTcD * kTcKv * 2;        // 16 KiB
+constexpr int kPBytes = kTcRows * kTcKv * 2;      // 16 KiB each, hi and lo
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kQBytes;
+constexpr int kOffVs = kOffK + kKBytes;
+constexpr int kOffVt = ((kOffVs + kVsBytes + 1023) / 1024) * 1024;
+constexpr int kOffPh = kOffVt + kVtBytes;
+constexpr int kOffPl = kOffPh + kPBytes;
+constexpr int kOffBar = kOffPl + kPBytes;         // two mbarriers, the tensor-memory address, a flag
+constexpr int kTcSmem = kOffBar + 32;
+
+struct TcParams {
+  const uint16_t* q;
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* q_start;
+  void* out;
+  int* dev_status;
+  int max_blocks_per_seq;
+  int num_blocks;
+  int num_q_heads;
+  int num_kv_heads;
+  int block_size;
+  float softmax_scale;
+};
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+// make the initialized barriers visible to the tensor cores' arrivals
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// bounded wait for phase `parity` of the mbarrier; false when it ran out
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  const long long start = clock64();
+  for (;;) {
+    uint32_t done;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (clock64() - start > kTcWaitCycles) return false;
+  }
+}
+// D[tmem] (+)= A[smem] . B[smem]^T, kind::f16, fp32 accumulate
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                     uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+// 32 consecutive fp32 columns of this thread's tensor-memory lane (the load
+// and its wait in one statement: the registers are only defined after both)
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, no swizzle; start, leading byte
+// offset (next core matrix along K) and stride byte offset (next 8-row
+// group), all in 16-byte units; bit 46 marks the tcgen05 descriptor version.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46);
+}
+// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and B
+// f16 (0) or bf16 (1) at bits 7-9 and 10-12, both K-major, N / 8 at bits
+// 17-22, M / 16 at bits 24-28.
+__host__ __device__ constexpr uint32_t umma_idesc(bool bf16, int m, int n) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// byte offset of (row, 16-byte chunk c) in a K-major tile whose rows hold
+// `chunks` chunks: core matrix (row / 8, c) of 8 rows x 16 bytes
+__device__ __forceinline__ uint32_t core_off(int row, int c, int chunks) {
+  return static_cast<uint32_t>((((row >> 3) * chunks + c) << 7) + ((row & 7) << 4));
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kTcThreads) prefill_tc_kernel(const TcParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  pdl_wait();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int group = p.num_q_heads / p.num_kv_heads;
+  const int qpb = kTcRows / group;                     // query tokens of this CTA
+  const int nq = p.q_start[b + 1] - p.q_start[b];
+  const int j0 = static_cast<int>(blockIdx.x) * qpb;
+  if (j0 >= nq) return;                                // whole CTA: no query here
+  const int cap = p.max_blocks_per_seq * p.block_size;
+  int ctx = p.context_lens[b];
+  if (ctx > cap) {
+    if (tid == 0 && blockIdx.x == 0 && kvh == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
+    ctx = cap;
+  }
+  const int pos0 = ctx - nq;                           // position of query 0 of the chunk
+  if (pos0 < 0 && j0 == 0 && tid == 0 && kvh == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
+  // this thread's row: query token j0 + r / G, head r % G
+  const int jj = tid / group, g = tid % group;
+  const bool row_q = j0 + jj < nq;
+  const int pos = pos0 + j0 + jj;
+  const bool row_ok = row_q && pos >= 0;
+  const int last_j = min(j0 + qpb, nq) - 1;
+  const int kv_end = max(0, min(ctx, pos0 + last_j + 1));
+  const int ntiles = (kv_end + kTcKv - 1) / kTcKv;
+
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t bar_s = sb + kOffBar, bar_o = sb + kOffBar + 8;
+  volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(smem + kOffBar + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 20);
+
+  if (warp == 0) {
+    tmem_alloc(sb + kOffBar + 16, kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(bar_s, 1);
+    mbar_init(bar_o, 1);
+    mbar_init_fence();
+    *abort_flag = 0;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t tmem_s = tmem, tmem_o = tmem + 64;
+  const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;   // this warp's 32 lanes
+
+  // Q rows (K-major core matrices; rows without a query are zero)
+  {
+    const uint16_t* qrow =
+        p.q + ((static_cast<int64_t>(p.q_start[b]) + j0 + (row_q ? jj : 0)) * p.num_q_heads +
+               kvh * group + g) * kTcD;
+#pragma unroll
+    for (int c = 0; c < kTcD / 8; ++c) {
+      const uint32_t dst = sb + kOffQ + core_off(tid, c, kTcD / 8);
+      if (row_ok) cp_async_16(dst, qrow + 8 * c);
+      else st_shared_v4(dst, make_uint4(0, 0, 0, 0));
+    }
+  }
+
+  const float mult = p.softmax_scale * 1.4426950408889634f;
+  constexpr bool kBf = DT == PKV_BF16;
+  constexpr uint32_t kIdescS = umma_idesc(kBf, kTcRows, kTcKv);
+  constexpr uint32_t kIdescO = umma_idesc(kBf, kTcRows, kTcD);
+  float m = -INFINITY, l = 0.f;
+  bool failed = false;
+  int s_commits = 0, o_commits = 0;                   // tensor-core batches issued (same in every thread)
+  const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
+  constexpr int kRowBytes = kTcD * 2;
+
+  for (int t = 0; t < ntiles; ++t) {
+    const int t0 = t * kTcKv;
+    // 1. the tile's K rows (K-major) and V rows (staging), through the block table
+#pragma unroll 4
+    for (int idx = tid; idx < kTcKv * (kTcD / 8); idx += kTcThreads) {
+      const int tok = idx >> 4, c = idx & 15;
+      const int abs_t = t0 + tok;
+      const uint32_t kd = sb + kOffK + core_off(tok, c, kTcD / 8);
+      const uint32_t vd = sb + kOffVs + tok * kVStride + c * 16;
+      bool done = false;
+      if (abs_t < kv_end) {
+        const int logical = abs_t / p.block_size;
+        const int phys = __ldg(trow + logical);
+        if (phys >= 0 && phys < p.num_blocks) {
+          const int64_t row = (static_cast<int64_t>(phys) * p.num_kv_heads + kvh) * p.block_size +
+                              (abs_t - logical * p.block_size);
+          cp_async_16(kd, p.k_cache + row * kRowBytes + c * 16);
+          cp_async_16(vd, p.v_cache + row * kRowBytes + c * 16);
+          done = true;
+        } else if (c == 0) {
+          flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
+        }
+      }
+      if (!done) {                                     // past the range or a bad block: zeros
+        st_shared_v4(kd, make_uint4(0, 0, 0, 0));
+        st_shared_v4(vd, make_uint4(0, 0, 0, 0));
+      }
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    // 2. the previous tile's P.V has finished with V^T and P
+    if (t > 0 && !mbar_wait(bar_o, (t - 1) & 1)) {
+      flag_status(p.dev_status, PKV_ERR_DEVICE_TIMEOUT);
+      *abort_flag = 1;
+    }
+    __syncthreads();
+    if (*abort_flag) { failed = true; break; }
+    // 3. V^T (K-major: rows d, K = tokens) from the staged rows: 8 x 8 blocks
+    //    (token block tb, d block db), four per ldmatrix.x4.trans
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int blk0 = warp * 32 + i * 4;              // 128 blocks: 8 token blocks x 16 d blocks
+      const int mi = lane >> 3, rr = lane & 7;
+      const int blk = blk0 + mi, tb = blk & 7, db = blk >> 3;
+      uint32_t r[4];
+      ldmatrix_x4_trans(sb + kOffVs + (tb * 8 + rr) * kVStride + db * 16, r);
+      const int q4 = lane >> 2, c4 = lane & 3;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int bk = blk0 + k, tbk = bk & 7, dbk = bk >> 3;
+        st_shared_b32(sb + kOffVt + ((dbk * (kTcKv / 8) + tbk) << 7) + q4 * 16 + c4 * 4, r[k]);
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // 4. S = Q K^T
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < kTcD / 16; ++kk)
+        umma(tmem_s, umma_desc(sb + kOffQ + kk * 256, 128, (kTcD / 8) * 128),
+             umma_desc(sb + kOffK + kk * 256, 128, (kTcD / 8) * 128), kIdescS, kk > 0);
+      umma_commit(bar_s);
+    }
+    ++s_commits;
+    if (!mbar_wait(bar_s, t & 1)) {
+      flag_status(p.dev_status, PKV_ERR_DEVICE_TIMEOUT);
+      *abort_flag = 1;
+    }
+    tc_fence_after();
+    // 5. row tid of S, masked and scaled (log2 units)
+    float s[kTcKv];
+    {
+      float a[32];
+      tmem_ld32(tmem_s + lane_base, a);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) s[i] = a[i];
+      tmem_ld32(tmem_s + lane_base + 32, a);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) s[32 + i] = a[i];
+    }
+    float tmax = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kTcKv; ++c) {
+      const int abs_t = t0 + c;
+      const bool valid = abs_t < kv_end && (!row_ok || abs_t <= pos);
+      s[c] = valid ? s[c] * mult : -INFINITY;
+      tmax = fmaxf(tmax, s[c]);
+    }
+    // 6. online softmax; the running max moves only past m + tau
+    const bool raise = tmax > m + kTcTau;
+    float alpha = 1.f;
+    if (raise) {
+      const float mn = fmaxf(m, tmax);
+      alpha = exp2f(m - mn);
+      m = mn;
+      l *= alpha;
+    }
+    if (t > 0 && __any_sync(0xffffffffu, raise)) {    // rescale O (warp-collective)
+#pragma unroll
+      for (int k = 0; k < kTcD / 32; ++k) {
+        float o[32];
+        tmem_ld32(tmem_o + lane_base + 32 * k, o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+        tmem_st32(tmem_o + lane_base + 32 * k, o);
+      }
+    }
+    // P = 2^(s - m) as a 16-bit hi + lo pair, row tid of the K-major P tiles
+#pragma unroll
+    for (int c8 = 0; c8 < kTcKv / 8; ++c8) {
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float p0 = exp2f(s[8 * c8 + 2 * k] - m), p1 = exp2f(s[8 * c8 + 2 * k + 1] - m);
+        l += p0 + p1;
+        hw[k] = Half16<DT>::pack_rn(p0, p1);
+        const float2 f = Half16<DT>::unpack(hw[k]);
+        lw[k] = Half16<DT>::pack_rn(p0 - f.x, p1 - f.y);
+      }
+      const uint32_t off = core_off(tid, c8, kTcKv / 8);
+      st_shared_v4(sb + kOffPh + off, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+      st_shared_v4(sb + kOffPl + off, make_uint4(lw[0], lw[1], lw[2], lw[3]));
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag) { failed = true; break; }
+    // 7. O += P V (hi, then lo)
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < kTcKv / 16; ++kk)
+        umma(tmem_o, umma_desc(sb + kOffPh + kk * 256, 128, (kTcKv / 8) * 128),
+             umma_desc(sb + kOffVt + kk * 256, 128, (kTcKv / 8) * 128), kIdescO, t > 0 || kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < kTcKv / 16; ++kk)
+        umma(tmem_o, umma_desc(sb + kOffPl + kk * 256, 128, (kTcKv / 8) * 128),
+             umma_desc(sb + kOffVt + kk * 256, 128, (kTcKv / 8) * 128), kIdescO, 1u);
+      umma_commit(bar_o);
+    }
+    ++o_commits;
+  }
+
+  // the last P.V (after a failure: still a bounded wait for whatever was
+  // issued, so the tensor memory is idle when it is freed), then the output
+  if (o_commits > 0 && !mbar_wait(bar_o, (o_commits - 1) & 1)) {
+    flag_status(p.dev_status, PKV_ERR_DEVICE_TIMEOUT);
+    failed = true;
+  }
+  if (s_commits > 0 && !mbar_wait(bar_s, (s_commits - 1) & 1)) {
+    flag_status(p.dev_status, PKV_ERR_DEVICE_TIMEOUT);
+    failed = true;
+  }
+  tc_fence_after();
+  const bool all_ok = __syncthreads_and(!failed) != 0;
+  if (row_q && !(all_ok && ntiles > 0)) {
+    uint16_t* orow = static_cast<uint16_t*>(p.out) +
+                     ((static_cast<int64_t>(p.q_start[b]) + j0 + jj) * p.num_q_heads + kvh * group + g) * kTcD;
+    for (int c = 0; c < kTcD / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
+  }
+  if (all_ok && ntiles > 0) {
+#pragma unroll
+    for (int k = 0; k < kTcD / 32; ++k) {
+      float o[32];
+      tmem_ld32(tmem_o + lane_base + 32 * k, o);       // warp-collective: every row
+      if (row_q) {
+        uint16_t* orow = static_cast<uint16_t*>(p.out) +
+                         ((static_cast<int64_t>(p.q_start[b]) + j0 + jj) * p.num_q_heads +
+                          kvh * group + g) * kTcD + 32 * k;
+        const float inv = (row_ok && l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4 w;
+          w.x = Half16<DT>::pack_rn(o[8 * c] * inv, o[8 * c + 1] * inv);
+          w.y = Half16<DT>::pack_rn(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
+          w.z = Half16<DT>::pack_rn(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
+          w.w = Half16<DT>::pack_rn(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+          reinterpret_cast<uint4*>(orow)[c] = w;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  pdl_launch_dependents();
+}
+
+template <int DT>
+cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t st) {
+  TcParams p;
+  p.q = static_cast<const uint16_t*>(a.q);
+  p.k_cache = static_cast<const uint8_t*>(a.k_cache);
+  p.v_cache = static_cast<const uint8_t*>(a.v_cache);
+  p.block_tables = a.block_tables;
+  p.context_lens = a.context_lens;
+  p.q_start = a.q_start;
+  p.out = a.out;
+  p.dev_status = a.dev_status;
+  p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.num_blocks = a.num_blocks;
+  p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.block_size = a.block_size;
+  p.softmax_scale = a.softmax_scale;
+  auto kern = prefill_tc_kernel<DT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+  if (e != cudaSuccess) return e;
+  const int group = a.num_q_heads / a.num_kv_heads;
+  const int qpb = kTcRows / group;
+  const dim3 grid(static_cast<unsigned>((a.max_query_len + qpb - 1) / qpb),
+                  static_cast<unsigned>(a.num_kv_heads), static_cast<unsigned>(a.num_seqs));
+  return launch_pdl(kern, grid, dim3(kTcThreads), kTcSmem, st, p);
+}
+
+}  // namespace
+
+bool prefill_tc_supported(const PrefillArgs& a) {
+  return (a.kv_dtype == PKV_F16 || a.kv_dtype == PKV_BF16) && a.head_dim == kTcD;
+}
+
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st) {
+  if (a.num_seqs == 0 || a.max_query_len == 0) return cudaSuccess;
+  return a.kv_dtype == PKV_F16 ? launch_tc<PKV_F16>(a, st) : launch_tc<PKV_BF16>(a, st);
+}
+
+}  // namespace pkv
