@@ -7,12 +7,15 @@
 // chunked prefill; query j of a chunk of n over c cached tokens sits at
 // position c - n + j and sees tokens 0 .. c - n + j.
 //
-// One CTA (one warpgroup, 128 threads) takes 128 query rows -- 128/G query
-// tokens of one sequence times the G query heads of one KV head -- and walks
-// that KV head's cache in 64-token tiles:
+// One CTA (one warpgroup, 128 threads; two CTAs per SM) takes 128 query rows
+// -- 128/G query tokens of one sequence times the G query heads of one KV
+// head -- and walks that KV head's cache in 64-token tiles:
 //   1. the tile's K rows and V rows come in with 16-byte cp.async through the
-//      block table (one row locator per token); V is then transposed in
-//      shared memory (ldmatrix.trans) so every MMA operand is K-major;
+//      block table (one row locator per token), K as a K-major operand and V
+//      as an MN-major one (token rows as they are stored), V double-buffered;
+//      the next tile's K is requested as soon as S has been formed, its V as
+//      soon as the previous P V has finished, so the copies overlap the
+//      softmax and the tensor cores;
 //   2. S = Q K^T: eight tcgen05.mma (M 128, N 64, K 16) into tensor memory;
 //   3. thread r reads row r of S from tensor memory, applies the causal mask
 //      and the online softmax (running max raised lazily, by more than
@@ -20,12 +23,14 @@
 //   4. O += P V: eight tcgen05.mma (M 128, N 128, K 16) into tensor memory,
 //      hi then lo;
 // and finally reads O from tensor memory, divides by the row sums and writes
-// the output rows.  Operands sit in shared memory in the canonical K-major
-// layout without swizzle: 8 x 16-byte core matrices, consecutive along K
-// (leading byte offset 128) and 8-row groups further apart (stride byte
-// offset).  Every wait for the tensor cores is bounded: when one runs out
-// the launch ORs PKV_ERR_DEVICE_TIMEOUT into dev_status, stops, and still
-// frees its tensor memory.
+// the output rows.  Operands sit in shared memory in the canonical layouts
+// without swizzle, built from 8 x 16-byte core matrices: K-major (Q, K, P)
+// with the next core matrix along K 128 bytes on (leading byte offset) and
+// the next 8-row group further (stride byte offset); MN-major (V) with 8
+// tokens x 8 head_dim values per core matrix, the next token group 128 bytes
+// on and the next 8 head_dim values 1024 bytes on.  Every wait for the tensor
+// cores is bounded: when one runs out the launch ORs PKV_ERR_DEVICE_TIMEOUT
+// into dev_status, stops, and still frees its tensor memory.
 #include <math.h>
 #include <stdint.h>
 
@@ -47,18 +52,16 @@ constexpr long long kTcWaitCycles = 4000000000LL;   // bounded wait: ~2 s of SM 
 // shared-memory plan (bytes; every operand tile 1024-byte aligned)
 constexpr int kQBytes = kTcRows * kTcD * 2;       // 32 KiB
 constexpr int kKBytes = kTcKv * kTcD * 2;         // 16 KiB
-constexpr int kVStride = kTcD * 2 + 16;           // V staging row stride (padded: no bank conflicts)
-constexpr int kVsBytes = kTcKv * kVStride;        // 17 KiB
-constexpr int kVtBytes = kTcD * kTcKv * 2;        // 16 KiB
+constexpr int kVBytes = kTcKv * kTcD * 2;         // 16 KiB, two of them
 constexpr int kPBytes = kTcRows * kTcKv * 2;      // 16 KiB each, hi and lo
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQBytes;
-constexpr int kOffVs = kOffK + kKBytes;
-constexpr int kOffVt = ((kOffVs + kVsBytes + 1023) / 1024) * 1024;
-constexpr int kOffPh = kOffVt + kVtBytes;
+constexpr int kOffV = kOffK + kKBytes;
+constexpr int kOffPh = kOffV + 2 * kVBytes;
 constexpr int kOffPl = kOffPh + kPBytes;
 constexpr int kOffBar = kOffPl + kPBytes;         // two mbarriers, the tensor-memory address, a flag
 constexpr int kTcSmem = kOffBar + 32;
+static_assert(2 * (kTcSmem + 1024) <= 233472, "two CTAs per SM");
 
 struct TcParams {
   const uint16_t* q;
@@ -183,9 +186,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                "r"(v.w)
                : "memory");
 }
-__device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
 
 // Shared-memory matrix descriptor: K-major, no swizzle; start, leading byte
 // offset (next core matrix along K) and stride byte offset (next 8-row
@@ -196,11 +196,13 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46);
 }
 // Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and B
-// f16 (0) or bf16 (1) at bits 7-9 and 10-12, both K-major, N / 8 at bits
-// 17-22, M / 16 at bits 24-28.
-__host__ __device__ constexpr uint32_t umma_idesc(bool bf16, int m, int n) {
+// f16 (0) or bf16 (1) at bits 7-9 and 10-12, A K-major (bit 15 = 0), B
+// K-major (bit 16 = 0) or MN-major (1), N / 8 at bits 17-22, M / 16 at bits
+// 24-28.
+__host__ __device__ constexpr uint32_t umma_idesc(bool bf16, int m, int n, bool b_mn_major) {
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
-         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 // byte offset of (row, 16-byte chunk c) in a K-major tile whose rows hold
@@ -210,10 +212,10 @@ __device__ __forceinline__ uint32_t core_off(int row, int c, int chunks) {
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kTcThreads) prefill_tc_kernel(const TcParams p) {
+__global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   pdl_wait();
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int group = p.num_q_heads / p.num_kv_heads;
   const int qpb = kTcRows / group;                     // query tokens of this CTA
@@ -274,23 +276,29 @@ __global__ void __launch_bounds__(kTcThreads) prefill_tc_kernel(const TcParams p
 
   const float mult = p.softmax_scale * 1.4426950408889634f;
   constexpr bool kBf = DT == PKV_BF16;
-  constexpr uint32_t kIdescS = umma_idesc(kBf, kTcRows, kTcKv);
-  constexpr uint32_t kIdescO = umma_idesc(kBf, kTcRows, kTcD);
+  constexpr uint32_t kIdescS = umma_idesc(kBf, kTcRows, kTcKv, false);
+  constexpr uint32_t kIdescO = umma_idesc(kBf, kTcRows, kTcD, true);
   float m = -INFINITY, l = 0.f;
   bool failed = false;
   int s_commits = 0, o_commits = 0;                   // tensor-core batches issued (same in every thread)
   const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
-  constexpr int kRowBytes = kTcD * 2;
 
-  for (int t = 0; t < ntiles; ++t) {
+  // The rows of tile t, K (into the K-major K tile) or V (into the MN-major
+  // V tile of buffer t & 1), through the block table.  Thread work item idx:
+  // token 8 (idx >> 7) + (idx & 7), 16-byte chunk (idx >> 3) & 15, so eight
+  // consecutive threads fill one 128-byte core matrix.  Tokens past the range
+  // or in an out-of-range block read as zeros.
+  auto load_rows = [&](int t, bool is_v) {
     const int t0 = t * kTcKv;
-    // 1. the tile's K rows (K-major) and V rows (staging), through the block table
+    const uint8_t* cache = is_v ? p.v_cache : p.k_cache;
+    const uint32_t base = sb + (is_v ? kOffV + (t & 1) * kVBytes : kOffK);
 #pragma unroll 4
     for (int idx = tid; idx < kTcKv * (kTcD / 8); idx += kTcThreads) {
-      const int tok = idx >> 4, c = idx & 15;
+      const int r = idx & 7, c = (idx >> 3) & 15, tb = idx >> 7;
+      const int tok = 8 * tb + r;
       const int abs_t = t0 + tok;
-      const uint32_t kd = sb + kOffK + core_off(tok, c, kTcD / 8);
-      const uint32_t vd = sb + kOffVs + tok * kVStride + c * 16;
+      const uint32_t dst = base + (is_v ? ((c * (kTcKv / 8) + tb) << 7) : ((tb * (kTcD / 8) + c) << 7)) +
+                           (r << 4);
       bool done = false;
       if (abs_t < kv_end) {
         const int logical = abs_t / p.block_size;
@@ -298,47 +306,30 @@ __global__ void __launch_bounds__(kTcThreads) prefill_tc_kernel(const TcParams p
         if (phys >= 0 && phys < p.num_blocks) {
           const int64_t row = (static_cast<int64_t>(phys) * p.num_kv_heads + kvh) * p.block_size +
                               (abs_t - logical * p.block_size);
-          cp_async_16(kd, p.k_cache + row * kRowBytes + c * 16);
-          cp_async_16(vd, p.v_cache + row * kRowBytes + c * 16);
+          cp_async_16(dst, cache + row * (kTcD * 2) + c * 16);
           done = true;
-        } else if (c == 0) {
+        } else if (c == 0 && !is_v) {
           flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
         }
       }
-      if (!done) {                                     // past the range or a bad block: zeros
-        st_shared_v4(kd, make_uint4(0, 0, 0, 0));
-        st_shared_v4(vd, make_uint4(0, 0, 0, 0));
-      }
+      if (!done) st_shared_v4(dst, make_uint4(0, 0, 0, 0));
     }
-    cp_async_commit();
+  };
+  if (ntiles > 0) {
+    load_rows(0, false);
+    load_rows(0, true);
+  }
+  cp_async_commit();
+
+  for (int t = 0; t < ntiles; ++t) {
+    const int t0 = t * kTcKv;
+    // 1. tile t's K and V (and, at t = 0, Q) are in shared memory
     cp_async_wait<0>();
-    // 2. the previous tile's P.V has finished with V^T and P
-    if (t > 0 && !mbar_wait(bar_o, (t - 1) & 1)) {
-      flag_status(p.dev_status, PKV_ERR_DEVICE_TIMEOUT);
-      *abort_flag = 1;
-    }
-    __syncthreads();
-    if (*abort_flag) { failed = true; break; }
-    // 3. V^T (K-major: rows d, K = tokens) from the staged rows: 8 x 8 blocks
-    //    (token block tb, d block db), four per ldmatrix.x4.trans
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int blk0 = warp * 32 + i * 4;              // 128 blocks: 8 token blocks x 16 d blocks
-      const int mi = lane >> 3, rr = lane & 7;
-      const int blk = blk0 + mi, tb = blk & 7, db = blk >> 3;
-      uint32_t r[4];
-      ldmatrix_x4_trans(sb + kOffVs + (tb * 8 + rr) * kVStride + db * 16, r);
-      const int q4 = lane >> 2, c4 = lane & 3;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int bk = blk0 + k, tbk = bk & 7, dbk = bk >> 3;
-        st_shared_b32(sb + kOffVt + ((dbk * (kTcKv / 8) + tbk) << 7) + q4 * 16 + c4 * 4, r[k]);
-      }
-    }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    // 4. S = Q K^T
+    if (*abort_flag) { failed = true; break; }
+    // 2. S = Q K^T
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
@@ -353,7 +344,10 @@ __global__ void __launch_bounds__(kTcThreads) prefill_tc_kernel(const TcParams p
       *abort_flag = 1;
     }
     tc_fence_after();
-    // 5. row tid of S, masked and scaled (log2 units)
+    // the K tile is free again: request the next one
+    if (t + 1 < ntiles) load_rows(t + 1, false);
+    cp_async_commit();
+    // 3. row tid of S, masked and scaled (log2 units)
     float s[kTcKv];
     {
       float a[32];
@@ -372,7 +366,16 @@ __global__ void __launch_bounds__(kTcThreads) prefill_tc_kernel(const TcParams p
       s[c] = valid ? s[c] * mult : -INFINITY;
       tmax = fmaxf(tmax, s[c]);
     }
-    // 6. online softmax; the running max moves only past m + tau
+    // 4. the previous P V has finished with O, P and the other V buffer:
+    //    request the next V tile there
+    if (t > 0 && !mbar_wait(bar_o, (t - 1) & 1)) {
+      flag_status(p.dev_status, PKV_ERR_DEVICE_TIMEOUT);
+      *abort_flag = 1;
+    }
+    tc_fence_after();
+    if (t + 1 < ntiles) load_rows(t + 1, true);
+    cp_async_commit();
+    // 5. online softmax; the running max moves only past m + tau
     const bool raise = tmax > m + kTcTau;
     float alpha = 1.f;
     if (raise) {
@@ -411,21 +414,24 @@ __global__ void __launch_bounds__(kTcThreads) prefill_tc_kernel(const TcParams p
     tc_fence_before();
     __syncthreads();
     if (*abort_flag) { failed = true; break; }
-    // 7. O += P V (hi, then lo)
+    // 6. O += P V (hi, then lo); V is MN-major: the next 16 tokens 256 bytes
+    //    on, the next 8 head_dim values (kTcKv / 8) * 128 bytes on
     if (tid == 0) {
       tc_fence_after();
+      const uint32_t vb = sb + kOffV + (t & 1) * kVBytes;
 #pragma unroll
       for (int kk = 0; kk < kTcKv / 16; ++kk)
         umma(tmem_o, umma_desc(sb + kOffPh + kk * 256, 128, (kTcKv / 8) * 128),
-             umma_desc(sb + kOffVt + kk * 256, 128, (kTcKv / 8) * 128), kIdescO, t > 0 || kk > 0);
+             umma_desc(vb + kk * 256, 128, (kTcKv / 8) * 128), kIdescO, t > 0 || kk > 0);
 #pragma unroll
       for (int kk = 0; kk < kTcKv / 16; ++kk)
         umma(tmem_o, umma_desc(sb + kOffPl + kk * 256, 128, (kTcKv / 8) * 128),
-             umma_desc(sb + kOffVt + kk * 256, 128, (kTcKv / 8) * 128), kIdescO, 1u);
+             umma_desc(vb + kk * 256, 128, (kTcKv / 8) * 128), kIdescO, 1u);
       umma_commit(bar_o);
     }
     ++o_commits;
   }
+  cp_async_wait<0>();
 
   // the last P.V (after a failure: still a bounded wait for whatever was
   // issued, so the tensor memory is idle when it is freed), then the output
@@ -491,6 +497,9 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t st) {
   p.softmax_scale = a.softmax_scale;
   auto kern = prefill_tc_kernel<DT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   const int group = a.num_q_heads / a.num_kv_heads;
   const int qpb = kTcRows / group;
