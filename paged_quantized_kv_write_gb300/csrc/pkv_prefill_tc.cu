@@ -59,7 +59,8 @@ constexpr int kOffK = kOffQ + kQBytes;
 constexpr int kOffV = kOffK + kKBytes;
 constexpr int kOffPh = kOffV + 2 * kVBytes;
 constexpr int kOffPl = kOffPh + kPBytes;
-constexpr int kOffBar = kOffPl + kPBytes;         // two mbarriers, the tensor-memory address, a flag
+constexpr int kOffLoc = kOffPl + kPBytes;         // row locators of the next tile to load (int64 each)
+constexpr int kOffBar = kOffLoc + kTcKv * 8;      // two mbarriers, the tensor-memory address, a flag
 constexpr int kTcSmem = kOffBar + 32;
 static_assert(2 * (kTcSmem + 1024) <= 233472, "two CTAs per SM");
 
@@ -187,6 +188,18 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                : "memory");
 }
 
+// 16-byte copy into shared memory that reads `bytes` (16 or 0) from src and
+// fills the rest with zeros
+__device__ __forceinline__ void cp_async_16_zfill(uint32_t dst_smem, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Shared-memory matrix descriptor: K-major, no swizzle; start, leading byte
 // offset (next core matrix along K) and stride byte offset (next 8-row
 // group), all in 16-byte units; bit 46 marks the tcgen05 descriptor version.
@@ -283,41 +296,49 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
   int s_commits = 0, o_commits = 0;                   // tensor-core batches issued (same in every thread)
   const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
 
-  // The rows of tile t, K (into the K-major K tile) or V (into the MN-major
-  // V tile of buffer t & 1), through the block table.  Thread work item idx:
-  // token 8 (idx >> 7) + (idx & 7), 16-byte chunk (idx >> 3) & 15, so eight
-  // consecutive threads fill one 128-byte core matrix.  Tokens past the range
-  // or in an out-of-range block read as zeros.
-  auto load_rows = [&](int t, bool is_v) {
-    const int t0 = t * kTcKv;
-    const uint8_t* cache = is_v ? p.v_cache : p.k_cache;
-    const uint32_t base = sb + (is_v ? kOffV + (t & 1) * kVBytes : kOffK);
-#pragma unroll 4
-    for (int idx = tid; idx < kTcKv * (kTcD / 8); idx += kTcThreads) {
-      const int r = idx & 7, c = (idx >> 3) & 15, tb = idx >> 7;
-      const int tok = 8 * tb + r;
-      const int abs_t = t0 + tok;
-      const uint32_t dst = base + (is_v ? ((c * (kTcKv / 8) + tb) << 7) : ((tb * (kTcD / 8) + c) << 7)) +
-                           (r << 4);
-      bool done = false;
+  // Row locators of tile t (threads 0-63, one token each): the cache row
+  // index (block * Hkv + kvh) * block_size + offset, or -1 for a token past
+  // the range or in an out-of-range block (those read as zeros).
+  const int64_t* locs = reinterpret_cast<const int64_t*>(smem + kOffLoc);
+  auto put_locators = [&](int t) {
+    if (tid < kTcKv) {
+      const int abs_t = t * kTcKv + tid;
+      int64_t row = -1;
       if (abs_t < kv_end) {
         const int logical = abs_t / p.block_size;
         const int phys = __ldg(trow + logical);
-        if (phys >= 0 && phys < p.num_blocks) {
-          const int64_t row = (static_cast<int64_t>(phys) * p.num_kv_heads + kvh) * p.block_size +
-                              (abs_t - logical * p.block_size);
-          cp_async_16(dst, cache + row * (kTcD * 2) + c * 16);
-          done = true;
-        } else if (c == 0 && !is_v) {
+        if (phys >= 0 && phys < p.num_blocks)
+          row = (static_cast<int64_t>(phys) * p.num_kv_heads + kvh) * p.block_size +
+                (abs_t - logical * p.block_size);
+        else
           flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
-        }
       }
-      if (!done) st_shared_v4(dst, make_uint4(0, 0, 0, 0));
+      reinterpret_cast<int64_t*>(smem + kOffLoc)[tid] = row;
+    }
+  };
+  // The rows of the tile whose locators are in place, K (into the K-major K
+  // tile) or V (into the MN-major V tile of buffer vbuf).  Thread tid copies
+  // 16-byte chunk (tid >> 3) & 15 of tokens 8 i + (tid & 7), so eight
+  // consecutive threads fill one 128-byte core matrix.
+  const int lr = tid & 7, lc = (tid >> 3) & 15;
+  auto load_rows = [&](bool is_v, int vbuf) {
+    const uint8_t* cache = is_v ? p.v_cache : p.k_cache;
+    const uint32_t base = sb + (is_v ? kOffV + vbuf * kVBytes : kOffK) + (lr << 4);
+#pragma unroll
+    for (int i = 0; i < kTcKv / 8; ++i) {
+      const int64_t row = locs[8 * i + lr];
+      const uint32_t dst = base + (is_v ? ((lc * (kTcKv / 8) + i) << 7) : ((i * (kTcD / 8) + lc) << 7));
+      const uint8_t* src = row >= 0 ? cache + row * (kTcD * 2) + lc * 16 : cache;
+      cp_async_16_zfill(dst, src, row >= 0 ? 16u : 0u);
     }
   };
   if (ntiles > 0) {
-    load_rows(0, false);
-    load_rows(0, true);
+    put_locators(0);
+    __syncthreads();
+    load_rows(false, 0);
+    load_rows(true, 0);
+    __syncthreads();
+    if (ntiles > 1) put_locators(1);
   }
   cp_async_commit();
 
@@ -345,7 +366,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
     }
     tc_fence_after();
     // the K tile is free again: request the next one
-    if (t + 1 < ntiles) load_rows(t + 1, false);
+    if (t + 1 < ntiles) load_rows(false, 0);
     cp_async_commit();
     // 3. row tid of S, masked and scaled (log2 units)
     float s[kTcKv];
@@ -358,13 +379,34 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
 #pragma unroll
       for (int i = 0; i < 32; ++i) s[32 + i] = a[i];
     }
-    float tmax = -INFINITY;
+    // tiles below the range end and below every row's causal limit (the
+    // first query's position is the smallest) need no mask: scale in the
+    // exponent's fused multiply-add; otherwise scale and mask here
+    const bool full = t0 + kTcKv <= kv_end && t0 + kTcKv - 1 <= pos0 + j0;
+    float tmax, pmul;
+    if (full) {
+      float e;
+      if (mult >= 0.f) {
+        e = -INFINITY;
 #pragma unroll
-    for (int c = 0; c < kTcKv; ++c) {
-      const int abs_t = t0 + c;
-      const bool valid = abs_t < kv_end && (!row_ok || abs_t <= pos);
-      s[c] = valid ? s[c] * mult : -INFINITY;
-      tmax = fmaxf(tmax, s[c]);
+        for (int c = 0; c < kTcKv; ++c) e = fmaxf(e, s[c]);
+      } else {
+        e = INFINITY;
+#pragma unroll
+        for (int c = 0; c < kTcKv; ++c) e = fminf(e, s[c]);
+      }
+      tmax = e * mult;
+      pmul = mult;
+    } else {
+      tmax = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kTcKv; ++c) {
+        const int abs_t = t0 + c;
+        const bool valid = abs_t < kv_end && (!row_ok || abs_t <= pos);
+        s[c] = valid ? s[c] * mult : -INFINITY;
+        tmax = fmaxf(tmax, s[c]);
+      }
+      pmul = 1.f;
     }
     // 4. the previous P V has finished with O, P and the other V buffer:
     //    request the next V tile there
@@ -373,14 +415,14 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
       *abort_flag = 1;
     }
     tc_fence_after();
-    if (t + 1 < ntiles) load_rows(t + 1, true);
+    if (t + 1 < ntiles) load_rows(true, (t + 1) & 1);
     cp_async_commit();
     // 5. online softmax; the running max moves only past m + tau
     const bool raise = tmax > m + kTcTau;
     float alpha = 1.f;
     if (raise) {
       const float mn = fmaxf(m, tmax);
-      alpha = exp2f(m - mn);
+      alpha = ex2_ftz(m - mn);
       m = mn;
       l *= alpha;
     }
@@ -400,7 +442,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
       uint32_t hw[4], lw[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float p0 = exp2f(s[8 * c8 + 2 * k] - m), p1 = exp2f(s[8 * c8 + 2 * k + 1] - m);
+        const float p0 = ex2_ftz(fmaf(s[8 * c8 + 2 * k], pmul, -m));
+        const float p1 = ex2_ftz(fmaf(s[8 * c8 + 2 * k + 1], pmul, -m));
         l += p0 + p1;
         hw[k] = Half16<DT>::pack_rn(p0, p1);
         const float2 f = Half16<DT>::unpack(hw[k]);
@@ -414,6 +457,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
     tc_fence_before();
     __syncthreads();
     if (*abort_flag) { failed = true; break; }
+    // every thread has issued its copies of tile t + 1: the locators of tile
+    // t + 2 may replace theirs (read after the next iteration's barrier)
+    if (t + 2 < ntiles) put_locators(t + 2);
     // 6. O += P V (hi, then lo); V is MN-major: the next 16 tokens 256 bytes
     //    on, the next 8 head_dim values (kTcKv / 8) * 128 bytes on
     if (tid == 0) {
