@@ -27,7 +27,7 @@ import torch
 
 PKV_F16, PKV_BF16, PKV_FP8_E4M3, PKV_INT4_G32, PKV_FP8_E5M2, PKV_INT8 = 0, 1, 2, 3, 4, 5
 (PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA, PKV_ERR_DEVICE_BOUNDS,
- PKV_ERR_WORKSPACE) = 0, 1, 2, 3, 4, 5
+ PKV_ERR_WORKSPACE, PKV_ERR_DEVICE_TIMEOUT) = 0, 1, 2, 3, 4, 5, 8
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libpagedkv.so")

@@ -1072,7 +1072,7 @@ paged_decode_kernel(const Params p) {
                 }
 #pragma unroll
                 for (int g = 0; g < NG; ++g)
-                  (half ? pb1 : pb0)[g] = __byte_perm(s0[g], s1[g], 0x5410) & (half ? mCE : mAB);
+                  (half ? pb1 : pb0)[g] = __byte_perm(s0[g], s1[g], 0x5410);
               }
               // the zero-point product's A operand: column q4 of the scale rows of
               // tokens (tA, tB) and (tC, tE)
@@ -1088,8 +1088,12 @@ paged_decode_kernel(const Params p) {
                                       ld_shared_u16(vsc + tE * SR + 2 * q4), 0x5410);
                 }
               }
-              zr[0] &= mAB;
-              zr[1] &= mCE;
+              if (partial) {
+#pragma unroll
+                for (int g = 0; g < NG; ++g) { pb0[g] &= mAB; pb1[g] &= mCE; }
+                zr[0] &= mAB;
+                zr[1] &= mCE;
+              }
               {
                 const uint32_t za[4] = {zr[0], 0u, zr[1], 0u};
                 mma_16816<PKV_F16>(zc, za, bp0, bp1);

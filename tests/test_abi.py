@@ -40,6 +40,18 @@ def test_version_and_status_strings(lib):
     assert lib.version() == 100
     assert lib.lib.paged_kv_status_string(0) == b"ok"
     assert b"outside" in lib.lib.paged_kv_status_string(4)
+    assert b"timed out" in lib.lib.paged_kv_status_string(8)
+    assert lib.lib.paged_kv_status_string(99) == b"unknown status"
+
+
+def test_binding_constants_match_the_header(lib):
+    """Every enumerator of the header's dtype and status enums has the same value
+    in the Python binding."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    enums = dict((n, int(v)) for n, v in re.findall(r"\b(PKV_[A-Z0-9_]+)\s*=\s*(\d+)", src))
+    assert "PKV_ERR_DEVICE_TIMEOUT" in enums and "PKV_INT8" in enums
+    for name, value in enums.items():
+        assert getattr(lib, name) == value, name
 
 
 def test_host_validation_without_gpu(lib):
