@@ -214,8 +214,10 @@ int paged_decode_attention_with_write(const void* q, int q_dtype, const void* k_
  *                chunks of all sequences, back to back.
  * q_start        int32 [num_seqs + 1], device: sequence b's queries are rows
  *                q_start[b] .. q_start[b+1] - 1 (a chunk of n_b tokens).
- * max_query_len  an upper bound of every n_b (sizes the grid); queries past it
- *                are not computed.
+ * max_query_len  sizes the grid; normally the largest n_b.  Queries
+ *                j >= max_query_len of a chunk are not computed and their
+ *                output rows are left untouched (positions still count from
+ *                the whole chunk of n_b).
  * context_lens   int32 [num_seqs]: tokens in the cache, the chunk included.
  *                Query j of sequence b sits at position ctx_b - n_b + j and
  *                attends to tokens 0 .. ctx_b - n_b + j.  A chunk longer than

@@ -215,6 +215,7 @@ struct Params {
   int parts_per_cta;
   float softmax_scale;
   const int32_t* q_start;     // prefill: [num_seqs + 1] offsets of each chunk's queries in q
+  int max_query_len;          // prefill: queries j >= max_query_len of a chunk are not computed
 };
 
 // Issue the copies of one 16-token sub-tile into its place in a stage
@@ -526,18 +527,20 @@ paged_decode_kernel(const Params p) {
     ctx = cap;
   }
   // prefill: this warp's queries j0 .. j0 + qpw - 1 of the chunk, query j at
-  // position pos0 + j (pos0 = ctx - nq), the cache tokens they see [0, pf_end).
+  // position pos0 + j (pos0 = ctx - nq), the cache tokens they see [0, pf_end);
+  // queries from max_query_len on are not computed (nqc = computed queries).
   // A chunk longer than the context is flagged; its queries at negative
   // positions see nothing and give zeros.
   const int qpw = PF ? kWarp / 4 / group : 0;               // 8 / G query tokens per warp
-  int nq = 0, j0 = 0, pos0 = 0, pf_end = 0;
+  int nq = 0, nqc = 0, j0 = 0, pos0 = 0, pf_end = 0;
   if constexpr (PF) {
     nq = p.q_start[b + 1] - p.q_start[b];
+    nqc = min(nq, p.max_query_len);
     j0 = (static_cast<int>(blockIdx.x) * kDecodeWarps + warp) * qpw;
-    if (j0 >= nq) return;                                    // no query for this warp
+    if (j0 >= nqc) return;                                   // no query for this warp
     pos0 = ctx - nq;
     if (pos0 < 0 && j0 == 0 && lane == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
-    pf_end = max(0, pos0 + min(j0 + qpw, nq));
+    pf_end = max(0, pos0 + min(j0 + qpw, nqc));
   }
   const int nparts_seq = PF ? 1 : (ctx > 0 ? (ctx + p.partition_size - 1) / p.partition_size : 1);
   // unit j -> partition; tiles of a unit this warp takes: kFirst, kFirst + kStride, ...
@@ -654,7 +657,7 @@ paged_decode_kernel(const Params p) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int jj = (2 * c4 + h) / group;
-      col_q[h] = jj < qpw && j0 + jj < nq;
+      col_q[h] = jj < qpw && j0 + jj < nqc;
       if (col_q[h]) {
         const int pos = pos0 + j0 + jj;
         if (pos >= 0) lim[h] = pos;
@@ -681,7 +684,7 @@ paged_decode_kernel(const Params p) {
   int64_t q_row;
   if constexpr (PF) {
     const int jj = q4 / group;
-    q_ok = jj < qpw && j0 + jj < nq && pos0 + j0 + jj >= 0;
+    q_ok = jj < qpw && j0 + jj < nqc && pos0 + j0 + jj >= 0;
     q_row = static_cast<int64_t>(p.q_start[b]) + j0 + (q_ok ? jj : 0);
   } else {
     q_ok = q4 < group;

@@ -69,6 +69,7 @@ cudaError_t launch_mode(const DecodeArgs& a, cudaStream_t st) {
   p.num_partitions = a.num_partitions;
   p.softmax_scale = a.softmax_scale;
   p.q_start = nullptr;
+  p.max_query_len = 0;
   auto kern = paged_decode_kernel<KV, QT, D, WU>;
   // per device, once: the shared-memory opt-in and the resident CTAs per SM
   static std::atomic<int> slots_per_dev[kMaxDevices];     // SMs x resident CTAs (0: unknown)

@@ -40,6 +40,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t st) {
   p.parts_per_cta = 1;
   p.softmax_scale = a.softmax_scale;
   p.q_start = a.q_start;
+  p.max_query_len = a.max_query_len;
   auto kern = paged_decode_kernel<KV, QT, D, true, true>;
   static std::atomic<int> attr_set[kMaxDevices];
   int dev = 0;

@@ -71,6 +71,8 @@ struct TcParams {
   const int32_t* block_tables;
   const int32_t* context_lens;
   const int32_t* q_start;
+  const float* scales;        // one-byte caches: fp32 [2][num_blocks][num_kv_heads]
+  int max_query_len;          // queries j >= max_query_len of a chunk are not computed
   void* out;
   int* dev_status;
   int max_blocks_per_seq;
@@ -233,8 +235,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
   const int group = p.num_q_heads / p.num_kv_heads;
   const int qpb = kTcRows / group;                     // query tokens of this CTA
   const int nq = p.q_start[b + 1] - p.q_start[b];
+  const int nqc = min(nq, p.max_query_len);            // queries computed
   const int j0 = static_cast<int>(blockIdx.x) * qpb;
-  if (j0 >= nq) return;                                // whole CTA: no query here
+  if (j0 >= nqc) return;                                // whole CTA: no query here
   const int cap = p.max_blocks_per_seq * p.block_size;
   int ctx = p.context_lens[b];
   if (ctx > cap) {
@@ -245,10 +248,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
   if (pos0 < 0 && j0 == 0 && tid == 0 && kvh == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
   // this thread's row: query token j0 + r / G, head r % G
   const int jj = tid / group, g = tid % group;
-  const bool row_q = j0 + jj < nq;
+  const bool row_q = j0 + jj < nqc;
   const int pos = pos0 + j0 + jj;
   const bool row_ok = row_q && pos >= 0;
-  const int last_j = min(j0 + qpb, nq) - 1;
+  const int last_j = min(j0 + qpb, nqc) - 1;
   const int kv_end = max(0, min(ctx, pos0 + last_j + 1));
   const int ntiles = (kv_end + kTcKv - 1) / kTcKv;
 
@@ -524,8 +527,426 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
   pdl_launch_dependents();
 }
 
-template <int DT>
-cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t st) {
+// ----------------------------------------------------------------------------
+// One-byte caches (FP8 E4M3, FP8 E5M2, INT8; one fp32 scale per block and KV
+// head).  The same tiles and tensor-core steps as above, with f16 operands:
+//   * the codes of the next tile are fetched into registers one tile ahead
+//     (16-byte loads through the block table) and converted exactly to f16
+//     into the K-major K tile and the MN-major V tile (E4M3 and E5M2 by cvt,
+//     INT8 as 1024 + (x + 128) - 1152 in f16);
+//   * q in bf16 enters as f16 with a power-of-two scale per row (exact for
+//     every value above 2^-28 of the row's largest), taken off in the softmax
+//     multiplier;
+//   * a token's K block scale multiplies its score column; its V block scale
+//     multiplies its column of P, in units of a running reference scale vu
+//     (the largest V scale seen so far): P'' = p s_V / vu <= 1.  When a tile
+//     raises vu, O and the row sum (kept in the same units) are rescaled, and
+//     the output O / l is free of vu.
+template <int KV> __device__ __forceinline__ void codes16_to_f16(const uint4 raw, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  uint32_t h[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (KV == PKV_INT8) {
+      // 0x64 over the byte x + 128 is the f16 1024 + x + 128
+      const uint32_t u = w[i] ^ 0x80808080u;
+      const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+      const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140), b = __byte_perm(u, 0x64646464u, 0x4342);
+      const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+      const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+      h[2 * i] = *reinterpret_cast<const uint32_t*>(&ha);
+      h[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hb);
+    } else {
+      h[2 * i] = fp8x2_to_f16x2<KV>(static_cast<uint16_t>(w[i] & 0xFFFFu));
+      h[2 * i + 1] = fp8x2_to_f16x2<KV>(static_cast<uint16_t>(w[i] >> 16));
+    }
+  }
+  lo = make_uint4(h[0], h[1], h[2], h[3]);
+  hi = make_uint4(h[4], h[5], h[6], h[7]);
+}
+
+// shared-memory plan of the one-byte kernel: Q, K, one V tile, P hi and lo,
+// the per-token scales of two tiles (by tile parity), barriers
+constexpr int kSc8Floats = 2 * kTcKv + 8;          // K scales, V scales, V max per half-tile
+constexpr int kOffV8 = kOffK + kKBytes;
+constexpr int kOffPh8 = kOffV8 + kVBytes;
+constexpr int kOffPl8 = kOffPh8 + kPBytes;
+constexpr int kOffS8 = kOffPl8 + kPBytes;
+constexpr int kOffBar8 = kOffS8 + 2 * kSc8Floats * 4;
+constexpr int kTc8Smem = kOffBar8 + 32;
+static_assert(2 * (kTc8Smem + 1024) <= 233472, "two CTAs per SM");
+
+template <int KV, int QT>
+__global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  pdl_wait();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int group = p.num_q_heads / p.num_kv_heads;
+  const int qpb = kTcRows / group;
+  const int nq = p.q_start[b + 1] - p.q_start[b];
+  const int nqc = min(nq, p.max_query_len);            // queries computed
+  const int j0 = static_cast<int>(blockIdx.x) * qpb;
+  if (j0 >= nqc) return;
+  const int cap = p.max_blocks_per_seq * p.block_size;
+  int ctx = p.context_lens[b];
+  if (ctx > cap) {
+    if (tid == 0 && blockIdx.x == 0 && kvh == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
+    ctx = cap;
+  }
+  const int pos0 = ctx - nq;
+  if (pos0 < 0 && j0 == 0 && tid == 0 && kvh == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
+  const int jj = tid / group, g = tid % group;
+  const bool row_q = j0 + jj < nqc;
+  const int pos = pos0 + j0 + jj;
+  const bool row_ok = row_q && pos >= 0;
+  const int last_j = min(j0 + qpb, nqc) - 1;
+  const int kv_end = max(0, min(ctx, pos0 + last_j + 1));
+  const int ntiles = (kv_end + kTcKv - 1) / kTcKv;
+
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t bar_s = sb + kOffBar8, bar_o = sb + kOffBar8 + 8;
+  volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(smem + kOffBar8 + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar8 + 20);
+  float* scb = reinterpret_cast<float*>(smem + kOffS8);   // [2][kSc8Floats]
+
+  if (warp == 0) {
+    tmem_alloc(sb + kOffBar8 + 16, kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(bar_s, 1);
+    mbar_init(bar_o, 1);
+    mbar_init_fence();
+    *abort_flag = 0;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t tmem_s = tmem, tmem_o = tmem + 64;
+  const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+
+  // Q row tid as f16 (bf16 q: times 2^qe, the row's largest magnitude in [2^13, 2^14))
+  int qe = 0;
+  {
+    const uint16_t* qrow =
+        p.q + ((static_cast<int64_t>(p.q_start[b]) + j0 + (row_q ? jj : 0)) * p.num_q_heads +
+               kvh * group + g) * kTcD;
+    if constexpr (QT == PKV_F16) {
+#pragma unroll
+      for (int c = 0; c < kTcD / 8; ++c) {
+        const uint32_t dst = sb + kOffQ + core_off(tid, c, kTcD / 8);
+        if (row_ok) cp_async_16(dst, qrow + 8 * c);
+        else st_shared_v4(dst, make_uint4(0, 0, 0, 0));
+      }
+      cp_async_commit();
+    } else {
+      float amax = 0.f;
+      if (row_ok) {
+#pragma unroll 4
+        for (int c = 0; c < kTcD / 8; ++c) {
+          const uint4 v = ld_global_nc_v4(qrow + 8 * c);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[i] << 16)),
+                                     fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+        }
+      }
+      if (amax > 0.f && amax <= 3.0e38f) {
+        int ex;
+        frexpf(amax, &ex);                             // amax = f 2^ex, f in [0.5, 1)
+        qe = 14 - ex;
+      }
+#pragma unroll 4
+      for (int c = 0; c < kTcD / 8; ++c) {
+        uint4 o = make_uint4(0, 0, 0, 0);
+        if (row_ok) {
+          const uint4 v = ld_global_nc_v4(qrow + 8 * c);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          uint32_t h[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            h[i] = Half16<PKV_F16>::pack_rn(ldexpf(__uint_as_float(w[i] << 16), qe),
+                                            ldexpf(__uint_as_float(w[i] & 0xFFFF0000u), qe));
+          o = make_uint4(h[0], h[1], h[2], h[3]);
+        }
+        st_shared_v4(sb + kOffQ + core_off(tid, c, kTcD / 8), o);
+      }
+    }
+  }
+
+  const float mult = ldexpf(p.softmax_scale * 1.4426950408889634f, -qe);
+  constexpr uint32_t kIdescS = umma_idesc(false, kTcRows, kTcKv, false);
+  constexpr uint32_t kIdescO = umma_idesc(false, kTcRows, kTcD, true);
+  float m = -INFINITY, l = 0.f;                       // l in units of 1 / vu
+  float vu = 1.f, lg_vu = 0.f;                         // V reference scale (1 until one is seen) and its log2
+  bool vu_set = false;
+  bool failed = false;
+  int s_commits = 0, o_commits = 0;
+  const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
+  const int64_t per_kv = static_cast<int64_t>(p.num_blocks) * p.num_kv_heads;
+
+  // this thread's share of a tile: 16-byte code chunk lrc of tokens 8 (lth + 2 j) + lr
+  const int lr = tid & 7, lrc = (tid >> 3) & 7, lth = tid >> 6;
+  uint4 kraw[4], vraw[4];
+  auto fetch = [&](int t) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int abs_t = t * kTcKv + 8 * (lth + 2 * j) + lr;
+      kraw[j] = make_uint4(0, 0, 0, 0);
+      vraw[j] = make_uint4(0, 0, 0, 0);
+      if (abs_t < kv_end) {
+        const int logical = abs_t / p.block_size;
+        const int phys = __ldg(trow + logical);
+        if (phys >= 0 && phys < p.num_blocks) {
+          const int64_t row = (static_cast<int64_t>(phys) * p.num_kv_heads + kvh) * p.block_size +
+                              (abs_t - logical * p.block_size);
+          kraw[j] = ld_global_nc_v4(p.k_cache + row * kTcD + lrc * 16);
+          vraw[j] = ld_global_nc_v4(p.v_cache + row * kTcD + lrc * 16);
+        } else if (lrc == 0) {
+          flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
+        }
+      }
+    }
+  };
+  // threads 0-63: the K and V scales of token tid of tile t (0 past the range
+  // or for an out-of-range block), and per warp the largest V scale
+  auto put_scales = [&](int t) {
+    if (tid < kTcKv) {
+      const int abs_t = t * kTcKv + tid;
+      float ks = 0.f, vs = 0.f;
+      if (abs_t < kv_end) {
+        const int phys = __ldg(trow + abs_t / p.block_size);
+        if (phys >= 0 && phys < p.num_blocks) {
+          const int64_t idx = static_cast<int64_t>(phys) * p.num_kv_heads + kvh;
+          ks = __ldg(p.scales + idx);
+          vs = __ldg(p.scales + per_kv + idx);
+        }
+      }
+      float* sc = scb + (t & 1) * kSc8Floats;
+      sc[tid] = ks;
+      sc[kTcKv + tid] = vs;
+      float vm = vs;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
+      if (lane == 0) sc[2 * kTcKv + warp] = vm;
+    }
+  };
+  // codes in registers -> f16 operand tile (K: K-major; V: MN-major)
+  auto convert = [&](const uint4 (&raw)[4], bool is_v) {
+    const uint32_t base = sb + (is_v ? kOffV8 : kOffK) + (lr << 4);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int tb = lth + 2 * j;
+      uint4 lo, hi;
+      codes16_to_f16<KV>(raw[j], lo, hi);
+      const int c0 = 2 * lrc, c1 = 2 * lrc + 1;
+      const uint32_t o0 = is_v ? ((c0 * (kTcKv / 8) + tb) << 7) : ((tb * (kTcD / 8) + c0) << 7);
+      const uint32_t o1 = is_v ? ((c1 * (kTcKv / 8) + tb) << 7) : ((tb * (kTcD / 8) + c1) << 7);
+      st_shared_v4(base + o0, lo);
+      st_shared_v4(base + o1, hi);
+    }
+  };
+  if (ntiles > 0) {
+    fetch(0);
+    put_scales(0);
+  }
+  if constexpr (QT == PKV_F16) cp_async_wait<0>();
+
+  for (int t = 0; t < ntiles; ++t) {
+    const int t0 = t * kTcKv;
+    // 1. K(t) into its operand tile (the previous S has finished with it)
+    convert(kraw, false);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag) { failed = true; break; }
+    // 2. S = Q K^T
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < kTcD / 16; ++kk)
+        umma(tmem_s, umma_desc(sb + kOffQ + kk * 256, 128, (kTcD / 8) * 128),
+             umma_desc(sb + kOffK + kk * 256, 128, (kTcD / 8) * 128), kIdescS, kk > 0);
+      umma_commit(bar_s);
+    }
+    ++s_commits;
+    // 3. the previous P V has finished with O, P and the V tile: V(t) goes in,
+    //    and the next tile's codes and scales are requested
+    if (t > 0 && !mbar_wait(bar_o, (t - 1) & 1)) {
+      flag_status(p.dev_status, PKV_ERR_DEVICE_TIMEOUT);
+      *abort_flag = 1;
+    }
+    tc_fence_after();
+    convert(vraw, true);
+    if (t + 1 < ntiles) {
+      fetch(t + 1);
+      put_scales(t + 1);
+    }
+    if (!mbar_wait(bar_s, t & 1)) {
+      flag_status(p.dev_status, PKV_ERR_DEVICE_TIMEOUT);
+      *abort_flag = 1;
+    }
+    tc_fence_after();
+    // 4. row tid of S times each column's K scale
+    const float* sc = scb + (t & 1) * kSc8Floats;
+    float s[kTcKv];
+    {
+      float a[32];
+      tmem_ld32(tmem_s + lane_base, a);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) s[i] = a[i];
+      tmem_ld32(tmem_s + lane_base + 32, a);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) s[32 + i] = a[i];
+    }
+#pragma unroll
+    for (int c4 = 0; c4 < kTcKv / 4; ++c4) {
+      const float4 ks = *reinterpret_cast<const float4*>(sc + 4 * c4);
+      s[4 * c4] *= ks.x;
+      s[4 * c4 + 1] *= ks.y;
+      s[4 * c4 + 2] *= ks.z;
+      s[4 * c4 + 3] *= ks.w;
+    }
+    const bool full = t0 + kTcKv <= kv_end && t0 + kTcKv - 1 <= pos0 + j0;
+    float tmax, pmul;
+    if (full) {
+      float e;
+      if (mult >= 0.f) {
+        e = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kTcKv; ++c) e = fmaxf(e, s[c]);
+      } else {
+        e = INFINITY;
+#pragma unroll
+        for (int c = 0; c < kTcKv; ++c) e = fminf(e, s[c]);
+      }
+      tmax = e * mult;
+      pmul = mult;
+    } else {
+      tmax = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kTcKv; ++c) {
+        const int abs_t = t0 + c;
+        const bool valid = abs_t < kv_end && (!row_ok || abs_t <= pos);
+        s[c] = valid ? s[c] * mult : -INFINITY;
+        tmax = fmaxf(tmax, s[c]);
+      }
+      pmul = 1.f;
+    }
+    // 5. online softmax (lazy max) and the V reference (same in every thread)
+    const bool raise = tmax > m + kTcTau;
+    float alpha = 1.f;
+    if (raise) {
+      const float mn = fmaxf(m, tmax);
+      alpha = ex2_ftz(m - mn);
+      m = mn;
+    }
+    const float vmax = fmaxf(sc[2 * kTcKv], sc[2 * kTcKv + 1]);
+    const bool rebase = vmax > (vu_set ? vu : 0.f);
+    if (rebase) {
+      alpha *= vu_set ? vu / vmax : 1.f / vmax;
+      vu = vmax;
+      lg_vu = __log2f(vmax);
+      vu_set = true;
+    }
+    l *= alpha;
+    if (t > 0 && (__any_sync(0xffffffffu, raise) || rebase)) {
+#pragma unroll
+      for (int k = 0; k < kTcD / 32; ++k) {
+        float o[32];
+        tmem_ld32(tmem_o + lane_base + 32 * k, o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+        tmem_st32(tmem_o + lane_base + 32 * k, o);
+      }
+    }
+    // P / vu = 2^(x - m - log2 vu); P'' = (P / vu) s_V as an f16 hi + lo pair
+    const float moff = m + lg_vu;
+#pragma unroll
+    for (int c8 = 0; c8 < kTcKv / 8; ++c8) {
+      const float4 va = *reinterpret_cast<const float4*>(sc + kTcKv + 8 * c8);
+      const float4 vb = *reinterpret_cast<const float4*>(sc + kTcKv + 8 * c8 + 4);
+      const float vsc[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float p0 = ex2_ftz(fmaf(s[8 * c8 + 2 * k], pmul, -moff));
+        const float p1 = ex2_ftz(fmaf(s[8 * c8 + 2 * k + 1], pmul, -moff));
+        l += p0 + p1;
+        const float q0 = p0 * vsc[2 * k], q1 = p1 * vsc[2 * k + 1];
+        hw[k] = Half16<PKV_F16>::pack_rn(q0, q1);
+        const float2 f = Half16<PKV_F16>::unpack(hw[k]);
+        lw[k] = Half16<PKV_F16>::pack_rn(q0 - f.x, q1 - f.y);
+      }
+      const uint32_t off = core_off(tid, c8, kTcKv / 8);
+      st_shared_v4(sb + kOffPh8 + off, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+      st_shared_v4(sb + kOffPl8 + off, make_uint4(lw[0], lw[1], lw[2], lw[3]));
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag) { failed = true; break; }
+    // 6. O += P'' V (hi, then lo)
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < kTcKv / 16; ++kk)
+        umma(tmem_o, umma_desc(sb + kOffPh8 + kk * 256, 128, (kTcKv / 8) * 128),
+             umma_desc(sb + kOffV8 + kk * 256, 128, (kTcKv / 8) * 128), kIdescO, t > 0 || kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < kTcKv / 16; ++kk)
+        umma(tmem_o, umma_desc(sb + kOffPl8 + kk * 256, 128, (kTcKv / 8) * 128),
+             umma_desc(sb + kOffV8 + kk * 256, 128, (kTcKv / 8) * 128), kIdescO, 1u);
+      umma_commit(bar_o);
+    }
+    ++o_commits;
+  }
+
+  if (o_commits > 0 && !mbar_wait(bar_o, (o_commits - 1) & 1)) {
+    flag_status(p.dev_status, PKV_ERR_DEVICE_TIMEOUT);
+    failed = true;
+  }
+  if (s_commits > 0 && !mbar_wait(bar_s, (s_commits - 1) & 1)) {
+    flag_status(p.dev_status, PKV_ERR_DEVICE_TIMEOUT);
+    failed = true;
+  }
+  tc_fence_after();
+  const bool all_ok = __syncthreads_and(!failed) != 0;
+  uint16_t* orow = static_cast<uint16_t*>(p.out) +
+                   ((static_cast<int64_t>(p.q_start[b]) + j0 + jj) * p.num_q_heads + kvh * group + g) * kTcD;
+  if (row_q && !(all_ok && ntiles > 0)) {
+    for (int c = 0; c < kTcD / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
+  }
+  if (all_ok && ntiles > 0) {
+    const float inv = (row_ok && l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+    for (int k = 0; k < kTcD / 32; ++k) {
+      float o[32];
+      tmem_ld32(tmem_o + lane_base + 32 * k, o);       // warp-collective: every row
+      if (row_q) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4 w;
+          w.x = Half16<QT>::pack_rn(o[8 * c] * inv, o[8 * c + 1] * inv);
+          w.y = Half16<QT>::pack_rn(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
+          w.z = Half16<QT>::pack_rn(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
+          w.w = Half16<QT>::pack_rn(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+          reinterpret_cast<uint4*>(orow + 32 * k)[c] = w;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  pdl_launch_dependents();
+}
+
+template <typename Kern>
+cudaError_t launch_tc(Kern kern, int smem_bytes, const PrefillArgs& a, cudaStream_t st) {
   TcParams p;
   p.q = static_cast<const uint16_t*>(a.q);
   p.k_cache = static_cast<const uint8_t*>(a.k_cache);
@@ -533,6 +954,7 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t st) {
   p.block_tables = a.block_tables;
   p.context_lens = a.context_lens;
   p.q_start = a.q_start;
+  p.scales = static_cast<const float*>(a.scales);
   p.out = a.out;
   p.dev_status = a.dev_status;
   p.max_blocks_per_seq = a.max_blocks_per_seq;
@@ -541,8 +963,8 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t st) {
   p.num_kv_heads = a.num_kv_heads;
   p.block_size = a.block_size;
   p.softmax_scale = a.softmax_scale;
-  auto kern = prefill_tc_kernel<DT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+  p.max_query_len = a.max_query_len;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
@@ -551,18 +973,32 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t st) {
   const int qpb = kTcRows / group;
   const dim3 grid(static_cast<unsigned>((a.max_query_len + qpb - 1) / qpb),
                   static_cast<unsigned>(a.num_kv_heads), static_cast<unsigned>(a.num_seqs));
-  return launch_pdl(kern, grid, dim3(kTcThreads), kTcSmem, st, p);
+  return launch_pdl(kern, grid, dim3(kTcThreads), smem_bytes, st, p);
+}
+
+template <int KV>
+cudaError_t launch_tc8(const PrefillArgs& a, cudaStream_t st) {
+  return a.q_dtype == PKV_F16 ? launch_tc(prefill_tc8_kernel<KV, PKV_F16>, kTc8Smem, a, st)
+                              : launch_tc(prefill_tc8_kernel<KV, PKV_BF16>, kTc8Smem, a, st);
 }
 
 }  // namespace
 
 bool prefill_tc_supported(const PrefillArgs& a) {
-  return (a.kv_dtype == PKV_F16 || a.kv_dtype == PKV_BF16) && a.head_dim == kTcD;
+  return (a.kv_dtype == PKV_F16 || a.kv_dtype == PKV_BF16 || is_blk8(a.kv_dtype)) &&
+         a.head_dim == kTcD;
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st) {
   if (a.num_seqs == 0 || a.max_query_len == 0) return cudaSuccess;
-  return a.kv_dtype == PKV_F16 ? launch_tc<PKV_F16>(a, st) : launch_tc<PKV_BF16>(a, st);
+  switch (a.kv_dtype) {
+    case PKV_F16: return launch_tc(prefill_tc_kernel<PKV_F16>, kTcSmem, a, st);
+    case PKV_BF16: return launch_tc(prefill_tc_kernel<PKV_BF16>, kTcSmem, a, st);
+    case PKV_FP8_E4M3: return launch_tc8<PKV_FP8_E4M3>(a, st);
+    case PKV_FP8_E5M2: return launch_tc8<PKV_FP8_E5M2>(a, st);
+    case PKV_INT8: return launch_tc8<PKV_INT8>(a, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace pkv

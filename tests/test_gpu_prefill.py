@@ -49,10 +49,21 @@ def _run(case, chunk, max_query_len=None, seed=0, ctx=None):
     return H.tensor_to_f64(out), ref, status.item(), q_start
 
 
+@pytest.fixture(params=["default", "mma"])
+def pf_mode(request, monkeypatch):
+    """default: tcgen05 for 16-bit and one-byte caches with head_dim 128, the
+    mma.sync kernel otherwise; mma: the mma.sync kernel for every call."""
+    if request.param == "mma":
+        monkeypatch.setenv("PKV_PREFILL_MODE", "mma")
+    else:
+        monkeypatch.delenv("PKV_PREFILL_MODE", raising=False)
+    return request.param
+
+
 @pytest.mark.parametrize("kv", [W.F16, W.BF16, W.FP8_E4M3, W.FP8_E5M2, W.INT8, W.INT4_G32])
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (8, 2), (16, 2)])
 @pytest.mark.parametrize("head_dim", [64, 128])
-def test_prefill_dtypes_groups_dims(kv, hq, hkv, head_dim):
+def test_prefill_dtypes_groups_dims(kv, hq, hkv, head_dim, pf_mode):
     qd = W.F16 if kv == W.F16 else W.BF16
     w = W.Workload("pf", 4, hq, hkv, head_dim, 16, kv, qd, "uniform", 40, 260,
                    outlier_prob=0.01, outlier_scale=20.0, seed=hq + hkv + head_dim + 3 * kv)
@@ -61,6 +72,20 @@ def test_prefill_dtypes_groups_dims(kv, hq, hkv, head_dim):
     gpu, ref, st, _ = _run(case, chunk)
     assert st == 0
     H.check_close(gpu, ref, kv, qd, f"prefill kv {kv} {hq}/{hkv} D {head_dim}")
+
+
+@pytest.mark.parametrize("kv", [W.FP8_E4M3, W.FP8_E5M2, W.INT8])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (32, 8), (64, 8)])
+def test_prefill_one_byte_cache_with_f16_queries(kv, hq, hkv, pf_mode):
+    """f16 queries over one-byte caches (the bf16-query cases are above), with
+    ragged chunks that leave partial tiles and whole-context chunks."""
+    w = W.Workload("pf16", 3, hq, hkv, 128, 16, kv, W.F16, "uniform", 60, 330,
+                   outlier_prob=0.01, outlier_scale=20.0, seed=31 + hq + 7 * kv)
+    case = W.make_case(w)
+    chunk = [int(min(c, n)) for c, n in zip(case.context_lens, [5, 64, 400])]
+    gpu, ref, st, _ = _run(case, chunk)
+    assert st == 0
+    H.check_close(gpu, ref, kv, W.F16, f"prefill f16 q, kv {kv} {hq}/{hkv}")
 
 
 @pytest.mark.parametrize("kv", [W.BF16, W.FP8_E4M3, W.INT4_G32])
@@ -93,23 +118,28 @@ def test_prefill_chunk_of_one_matches_decode():
     H.check_close(gpu, dec, w.kv_dtype, w.q_dtype, "prefill vs decode")
 
 
-def test_prefill_chunk_longer_than_context_is_flagged_and_zero():
+EDGE_KERNELS = [(W.BF16, 64), (W.BF16, 128), (W.FP8_E4M3, 128), (W.INT8, 128)]
+
+
+@pytest.mark.parametrize("kv,head_dim", EDGE_KERNELS)
+def test_prefill_chunk_longer_than_context_is_flagged_and_zero(kv, head_dim):
     pkv = _pkv()
-    w = W.Workload("pf", 2, 8, 2, 64, 16, W.BF16, W.BF16, "fixed", 6, 6, seed=4)
+    w = W.Workload("pf", 2, 8, 2, head_dim, 16, kv, W.BF16, "fixed", 6, 6, seed=4)
     case = W.make_case(w)
     gpu, ref, st, _ = _run(case, [9, 3])
     assert st == pkv.PKV_ERR_DEVICE_BOUNDS
     assert not gpu[:3].any()                       # queries at positions -3..-1
-    H.check_close(gpu, ref, W.BF16, W.BF16, "long chunk")
+    H.check_close(gpu, ref, kv, W.BF16, "long chunk")
 
 
-def test_prefill_max_query_len_bounds_the_grid():
-    w = W.Workload("pf", 2, 8, 2, 64, 16, W.BF16, W.BF16, "fixed", 100, 100, seed=5)
+@pytest.mark.parametrize("kv,head_dim", EDGE_KERNELS)
+def test_prefill_max_query_len_bounds_the_grid(kv, head_dim):
+    w = W.Workload("pf", 2, 8, 2, head_dim, 16, kv, W.BF16, "fixed", 100, 100, seed=5)
     case = W.make_case(w)
     gpu, ref, st, q_start = _run(case, [40, 10], max_query_len=16)
     assert st == 0
     computed = np.r_[0:16, 40:50]
-    H.check_close(gpu[computed], ref[computed], W.BF16, W.BF16, "bounded")
+    H.check_close(gpu[computed], ref[computed], kv, W.BF16, "bounded")
     assert np.isnan(gpu[16:40]).all()              # beyond max_query_len: not written
 
 
