@@ -138,6 +138,7 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t st) {
     if (!strcmp(m, "warp")) wu = true;
     if (!strcmp(m, "simt") && KV != PKV_INT4_G32 && a.slot_mapping == nullptr)
       return launch_simt(a, st);
+    if (!strcmp(m, "tc") && decode_tc_supported(a)) return launch_decode_tc(a, st);
   }
   return wu ? launch_mode<KV, QT, D, true>(a, st) : launch_mode<KV, QT, D, false>(a, st);
 }

@@ -95,6 +95,9 @@ cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t st);
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t st);
 cudaError_t launch_lse_reduce(const DecodeArgs& a, cudaStream_t st);
 bool prefill_tc_supported(const PrefillArgs& a);
+// decode on the tcgen05 tensor cores (one-byte caches, head_dim 128, G <= 8)
+bool decode_tc_supported(const DecodeArgs& a);
+cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st);
 cudaError_t launch_simt(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);

@@ -16,11 +16,12 @@ from tests import helpers as H
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["shared", "warp", "simt"])
+@pytest.fixture(params=["shared", "warp", "simt", "tc"])
 def mode(request, monkeypatch):
-    """Run a test under both work splits of the decode kernel and under the SIMT
+    """Run a test under both work splits of the decode kernel, under the SIMT
     comparator (which takes 16-bit, FP8 and INT8 caches; INT4 stays on the
-    tensor path)."""
+    tensor path), and under the tcgen05 kernel (one-byte caches with head_dim
+    128; other calls keep the mma.sync kernel)."""
     monkeypatch.setenv("PKV_DECODE_MODE", request.param)
     return request.param
 
@@ -158,9 +159,10 @@ def test_unwritten_last_token_matches_oracle(kv, mode):
     H.check_close(out, ref, kv, W.BF16, "unwritten last token")
 
 
-def test_bad_block_id_is_flagged_and_skipped(mode):
+@pytest.mark.parametrize("kv,head_dim", [(W.BF16, 64), (W.FP8_E4M3, 128)])
+def test_bad_block_id_is_flagged_and_skipped(kv, head_dim, mode):
     import paged_quantized_kv_write_gb300 as pkv
-    w = W.Workload("badid", 3, 8, 2, 64, 16, W.BF16, W.BF16, "fixed", 40, 40, seed=4)
+    w = W.Workload("badid", 3, 8, 2, head_dim, 16, kv, W.BF16, "fixed", 40, 40, seed=4)
     case = W.make_case(w)
     k, v, s = oracle.prefill_case(case)
     bt = case.block_tables.copy()
@@ -170,7 +172,7 @@ def test_bad_block_id_is_flagged_and_skipped(mode):
     assert g.status.item() == pkv.PKV_ERR_DEVICE_BOUNDS
     # the other sequences are untouched
     ref = H.oracle_attention(case, k, v, s)
-    H.check_close(out[[0, 2]], ref[[0, 2]], W.BF16, W.BF16, "other sequences")
+    H.check_close(out[[0, 2]], ref[[0, 2]], kv, W.BF16, "other sequences")
 
 
 def test_argument_errors_return_status():
