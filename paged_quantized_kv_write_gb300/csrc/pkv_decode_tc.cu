@@ -81,30 +81,6 @@ __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
   asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
-// 16 one-byte codes -> 16 exact f16 values (two 16-byte chunks)
-template <int KV> __device__ __forceinline__ void codes16_f16(const uint4 raw, uint4& lo, uint4& hi) {
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-  uint32_t h[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if constexpr (KV == PKV_INT8) {
-      // 0x64 over the byte x + 128 is the f16 1024 + x + 128; minus 1152 (0x6480)
-      const uint32_t u = w[i] ^ 0x80808080u;
-      const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-      const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140), b = __byte_perm(u, 0x64646464u, 0x4342);
-      const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
-      const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
-      h[2 * i] = *reinterpret_cast<const uint32_t*>(&ha);
-      h[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hb);
-    } else {
-      h[2 * i] = fp8x2_to_f16x2<KV>(static_cast<uint16_t>(w[i] & 0xFFFFu));
-      h[2 * i + 1] = fp8x2_to_f16x2<KV>(static_cast<uint16_t>(w[i] >> 16));
-    }
-  }
-  lo = make_uint4(h[0], h[1], h[2], h[3]);
-  hi = make_uint4(h[4], h[5], h[6], h[7]);
-}
-
 template <int KV, int QT>
 __global__ void __launch_bounds__(kDtThreads, 3) decode_tc_kernel(const Params p) {
   extern __shared__ __align__(1024) uint8_t dtc_smem[];
@@ -261,7 +237,7 @@ __global__ void __launch_bounds__(kDtThreads, 3) decode_tc_kernel(const Params p
     for (int r = 0; r < 8; ++r) {
       const int tok = 32 * warp + 8 * (r >> 1) + lk, c = 4 * (r & 1) + lj;
       uint4 lo, hi;
-      codes16_f16<KV>(kraw[r], lo, hi);
+      codes16_to_f16<KV>(kraw[r], lo, hi);
       st_shared_v4(sb + kDtOffK + core_off(tok, 2 * c, kDtD / 8), lo);
       st_shared_v4(sb + kDtOffK + core_off(tok, 2 * c + 1, kDtD / 8), hi);
     }
@@ -271,7 +247,7 @@ __global__ void __launch_bounds__(kDtThreads, 3) decode_tc_kernel(const Params p
     for (int r = 0; r < 8; ++r) {
       const int tok = 32 * warp + 8 * (r >> 1) + lk, c = 4 * (r & 1) + lj;
       uint4 lo, hi;
-      codes16_f16<KV>(vraw[r], lo, hi);
+      codes16_to_f16<KV>(vraw[r], lo, hi);
       // MN-major: head_dim group m (8 values) of token group tok / 8 at
       // (m * 16 + tok / 8) * 128, token tok % 8 at 16 (tok % 8)
       const uint32_t base = sb + kDtOffV + ((tok & 7) << 4);

@@ -400,29 +400,6 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
 //     (the largest V scale seen so far): P'' = p s_V / vu <= 1.  When a tile
 //     raises vu, O and the row sum (kept in the same units) are rescaled, and
 //     the output O / l is free of vu.
-template <int KV> __device__ __forceinline__ void codes16_to_f16(const uint4 raw, uint4& lo, uint4& hi) {
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-  uint32_t h[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if constexpr (KV == PKV_INT8) {
-      // 0x64 over the byte x + 128 is the f16 1024 + x + 128
-      const uint32_t u = w[i] ^ 0x80808080u;
-      const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
-      const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140), b = __byte_perm(u, 0x64646464u, 0x4342);
-      const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
-      const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
-      h[2 * i] = *reinterpret_cast<const uint32_t*>(&ha);
-      h[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hb);
-    } else {
-      h[2 * i] = fp8x2_to_f16x2<KV>(static_cast<uint16_t>(w[i] & 0xFFFFu));
-      h[2 * i + 1] = fp8x2_to_f16x2<KV>(static_cast<uint16_t>(w[i] >> 16));
-    }
-  }
-  lo = make_uint4(h[0], h[1], h[2], h[3]);
-  hi = make_uint4(h[4], h[5], h[6], h[7]);
-}
-
 // shared-memory plan of the one-byte kernel: Q, K, one V tile, P hi and lo,
 // the per-token scales of two tiles (by tile parity), barriers
 constexpr int kSc8Floats = 2 * kTcKv + 8;          // K scales, V scales, V max per half-tile

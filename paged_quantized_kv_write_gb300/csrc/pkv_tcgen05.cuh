@@ -1,7 +1,8 @@
 // tcgen05 building blocks shared by the tensor-memory kernels: tensor-memory
 // allocation, fences, mbarriers with bounded waits, the MMA and its commit,
 // tensor-memory loads and stores, shared-memory matrix descriptors in the
-// canonical no-swizzle layouts, and a few small helpers.
+// canonical no-swizzle layouts, the exact one-byte-code to f16 conversion,
+// and a few small helpers.
 #pragma once
 
 #include <stdint.h>
@@ -176,6 +177,31 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
       "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
       "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
       : "memory");
+}
+
+// 16 one-byte codes (FP8 E4M3 / E5M2 or INT8) -> 16 exact f16 values, as two
+// 16-byte chunks: FP8 by cvt; INT8 as 0x64 over the byte x + 128, which is
+// the f16 1024 + x + 128, minus 1152 (0x6480)
+template <int KV> __device__ __forceinline__ void codes16_to_f16(const uint4 raw, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  uint32_t h[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (KV == PKV_INT8) {
+      const uint32_t u = w[i] ^ 0x80808080u;
+      const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+      const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140), b = __byte_perm(u, 0x64646464u, 0x4342);
+      const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+      const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+      h[2 * i] = *reinterpret_cast<const uint32_t*>(&ha);
+      h[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hb);
+    } else {
+      h[2 * i] = fp8x2_to_f16x2<KV>(static_cast<uint16_t>(w[i] & 0xFFFFu));
+      h[2 * i + 1] = fp8x2_to_f16x2<KV>(static_cast<uint16_t>(w[i] >> 16));
+    }
+  }
+  lo = make_uint4(h[0], h[1], h[2], h[3]);
+  hi = make_uint4(h[4], h[5], h[6], h[7]);
 }
 
 }  // namespace tc
