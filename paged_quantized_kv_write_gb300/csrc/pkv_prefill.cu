@@ -7,11 +7,15 @@
 // causal rule is the usual one for prefill (query j of a chunk of n over a
 // context of c tokens sits at position c - n + j and sees tokens 0..c - n + j).
 //
-// The kernel is the decode kernel of pkv_attn.cuh in its PF mode: a warp's
-// 8 score columns are 8/G query tokens times the G query heads of one KV
-// head, each column masked at its query's position; the warp streams the
-// cache from token 0 to its last query's position through the same copy
-// ring, dequantization and online softmax as a decode step.
+// Two kernels compute it.  16-bit and one-byte caches with head_dim 128 go to
+// the tcgen05 kernels of pkv_prefill_tc.cu (128 query rows per CTA against
+// 64-token tiles, accumulators in tensor memory).  Everything else -- INT4
+// caches, head_dim 64, or any call under PKV_PREFILL_MODE=mma -- runs the
+// decode kernel of pkv_attn.cuh in its PF mode: a warp's 8 score columns are
+// 8/G query tokens times the G query heads of one KV head, each column masked
+// at its query's position; the warp streams the cache from token 0 to its
+// last query's position through the same copy ring, dequantization and online
+// softmax as a decode step.
 #include "pkv_attn.cuh"
 
 namespace pkv {

@@ -1,5 +1,6 @@
 // Chunked-prefill attention on the fifth-generation tensor cores (tcgen05,
-// accumulators in tensor memory) for 16-bit caches with head_dim 128.
+// accumulators in tensor memory) for head_dim 128: prefill_tc_kernel for
+// 16-bit caches, prefill_tc8_kernel (further down) for one-byte caches.
 // Chunked prefill is a dense contraction (every cached token meets a whole
 // chunk of queries), unlike the decode step, so it runs where the dense
 // tensor throughput is: "Optimizing KV-Cache Memory Footprint in
