@@ -230,7 +230,7 @@ int paged_decode_attention_with_write(const void* q, int q_dtype, const void* k_
  * Everything else as for paged_decode_attention (no workspace: no split-KV).
  * Supported: as paged_decode_attention, with num_q_heads / num_kv_heads in
  * {1, 2, 4, 8}.
- * F16/BF16, FP8 and INT8 caches with head_dim 128 run on the tcgen05 tensor cores
+ * F16/BF16, FP8 and INT8 caches (head_dim 64 or 128) run on the tcgen05 tensor cores
  * (accumulators in tensor memory); their waits on the tensor cores are
  * bounded, and one that runs out sets PKV_ERR_DEVICE_TIMEOUT in dev_status
  * and leaves the affected output rows zero.  Other caches, or the

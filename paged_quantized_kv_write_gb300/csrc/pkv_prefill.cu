@@ -7,10 +7,10 @@
 // causal rule is the usual one for prefill (query j of a chunk of n over a
 // context of c tokens sits at position c - n + j and sees tokens 0..c - n + j).
 //
-// Two kernels compute it.  16-bit and one-byte caches with head_dim 128 go to
-// the tcgen05 kernels of pkv_prefill_tc.cu (128 query rows per CTA against
-// 64-token tiles, accumulators in tensor memory).  Everything else -- INT4
-// caches, head_dim 64, or any call under PKV_PREFILL_MODE=mma -- runs the
+// Two kernels compute it.  16-bit and one-byte caches go to the tcgen05
+// kernels of pkv_prefill_tc.cu (128 query rows per CTA against 64-token
+// tiles, accumulators in tensor memory).  INT4 caches, or any call under
+// PKV_PREFILL_MODE=mma, run the
 // decode kernel of pkv_attn.cuh in its PF mode: a warp's 8 score columns are
 // 8/G query tokens times the G query heads of one KV head, each column masked
 // at its query's position; the warp streams the cache from token 0 to its
@@ -83,8 +83,8 @@ cudaError_t launch_prefill_q(const PrefillArgs& a, cudaStream_t st) {
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t st) {
   if (a.num_seqs == 0 || a.max_query_len == 0) return cudaSuccess;
-  // 16-bit caches with head_dim 128 run on the tcgen05 kernel
-  // (pkv_prefill_tc.cu); PKV_PREFILL_MODE=mma keeps them on this one
+  // 16-bit and one-byte caches run on the tcgen05 kernels (pkv_prefill_tc.cu);
+  // PKV_PREFILL_MODE=mma keeps them on this one
   const char* mode = getenv("PKV_PREFILL_MODE");
   if (prefill_tc_supported(a) && !(mode && !strcmp(mode, "mma"))) return launch_prefill_tc(a, st);
   switch (a.kv_dtype) {

@@ -1,6 +1,6 @@
 // Chunked-prefill attention on the fifth-generation tensor cores (tcgen05,
-// accumulators in tensor memory) for head_dim 128: prefill_tc_kernel for
-// 16-bit caches, prefill_tc8_kernel (further down) for one-byte caches.
+// accumulators in tensor memory) for head_dim 64 and 128: prefill_tc_kernel
+// for 16-bit caches, prefill_tc8_kernel (further down) for one-byte caches.
 // Chunked prefill is a dense contraction (every cached token meets a whole
 // chunk of queries), unlike the decode step, so it runs where the dense
 // tensor throughput is: "Optimizing KV-Cache Memory Footprint in
@@ -47,24 +47,38 @@ using namespace tc;
 constexpr int kTcThreads = 128;      // one warpgroup; thread r owns query row r
 constexpr int kTcRows = 128;         // MMA M
 constexpr int kTcKv = 64;            // KV tokens per tile
-constexpr int kTcD = 128;            // head_dim
-constexpr uint32_t kTmemCols = 256;  // S: columns [0, 64); O: [64, 192)
 constexpr float kTcTau = 8.f;        // lazy rescale threshold (log2 units)
-
-// shared-memory plan (bytes; every operand tile 1024-byte aligned)
-constexpr int kQBytes = kTcRows * kTcD * 2;       // 32 KiB
-constexpr int kKBytes = kTcKv * kTcD * 2;         // 16 KiB
-constexpr int kVBytes = kTcKv * kTcD * 2;         // 16 KiB, two of them
 constexpr int kPBytes = kTcRows * kTcKv * 2;      // 16 KiB each, hi and lo
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kQBytes;
-constexpr int kOffV = kOffK + kKBytes;
-constexpr int kOffPh = kOffV + 2 * kVBytes;
-constexpr int kOffPl = kOffPh + kPBytes;
-constexpr int kOffLoc = kOffPl + kPBytes;         // row locators of the next tile to load (int64 each)
-constexpr int kOffBar = kOffLoc + kTcKv * 8;      // two mbarriers, the tensor-memory address, a flag
-constexpr int kTcSmem = kOffBar + 32;
-static_assert(2 * (kTcSmem + 1024) <= 233472, "two CTAs per SM");
+
+// Shared-memory plans (bytes; operand tiles 1024-byte aligned) and tensor
+// memory (S: columns [0, 64); O: [64, 64 + D)) for head_dim D.
+template <int D> struct TcPlan {
+  static constexpr uint32_t kTmemCols = D == 64 ? 128 : 256;
+  static constexpr int kQBytes = kTcRows * D * 2;
+  static constexpr int kKBytes = kTcKv * D * 2;
+  static constexpr int kVBytes = kTcKv * D * 2;
+  // 16-bit caches: Q, K, two V tiles, P hi and lo, the row locators of the
+  // next tile to load (int64 each), two mbarriers + tensor-memory address + flag
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kOffV = kOffK + kKBytes;
+  static constexpr int kOffPh = kOffV + 2 * kVBytes;
+  static constexpr int kOffPl = kOffPh + kPBytes;
+  static constexpr int kOffLoc = kOffPl + kPBytes;
+  static constexpr int kOffBar = kOffLoc + kTcKv * 8;
+  static constexpr int kSmem = kOffBar + 32;
+  // one-byte caches: Q, K, one V tile, P hi and lo, the per-token scales of
+  // two tiles (by tile parity: K scales, V scales, V max per half-tile), barriers
+  static constexpr int kSc8Floats = 2 * kTcKv + 8;
+  static constexpr int kOffV8 = kOffK + kKBytes;
+  static constexpr int kOffPh8 = kOffV8 + kVBytes;
+  static constexpr int kOffPl8 = kOffPh8 + kPBytes;
+  static constexpr int kOffS8 = kOffPl8 + kPBytes;
+  static constexpr int kOffBar8 = kOffS8 + 2 * kSc8Floats * 4;
+  static constexpr int kSmem8 = kOffBar8 + 32;
+  static_assert(2 * (kSmem + 1024) <= 233472 && 2 * (kSmem8 + 1024) <= 233472,
+                "two CTAs per SM");
+};
 
 struct TcParams {
   const uint16_t* q;
@@ -85,9 +99,10 @@ struct TcParams {
   float softmax_scale;
 };
 
-template <int DT>
+template <int DT, int D>
 __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  using PL = TcPlan<D>;
   pdl_wait();
   const int tid = threadIdx.x, warp = tid >> 5;
   const int kvh = blockIdx.y, b = blockIdx.z;
@@ -115,12 +130,12 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
   const int ntiles = (kv_end + kTcKv - 1) / kTcKv;
 
   const uint32_t sb = smem_u32(smem);
-  const uint32_t bar_s = sb + kOffBar, bar_o = sb + kOffBar + 8;
-  volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(smem + kOffBar + 16);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 20);
+  const uint32_t bar_s = sb + PL::kOffBar, bar_o = sb + PL::kOffBar + 8;
+  volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(smem + PL::kOffBar + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + PL::kOffBar + 20);
 
   if (warp == 0) {
-    tmem_alloc(sb + kOffBar + 16, kTmemCols);
+    tmem_alloc(sb + PL::kOffBar + 16, PL::kTmemCols);
     tmem_relinquish();
   }
   if (tid == 0) {
@@ -140,10 +155,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
   {
     const uint16_t* qrow =
         p.q + ((static_cast<int64_t>(p.q_start[b]) + j0 + (row_q ? jj : 0)) * p.num_q_heads +
-               kvh * group + g) * kTcD;
+               kvh * group + g) * D;
 #pragma unroll
-    for (int c = 0; c < kTcD / 8; ++c) {
-      const uint32_t dst = sb + kOffQ + core_off(tid, c, kTcD / 8);
+    for (int c = 0; c < D / 8; ++c) {
+      const uint32_t dst = sb + PL::kOffQ + core_off(tid, c, D / 8);
       if (row_ok) cp_async_16(dst, qrow + 8 * c);
       else st_shared_v4(dst, make_uint4(0, 0, 0, 0));
     }
@@ -152,7 +167,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
   const float mult = p.softmax_scale * 1.4426950408889634f;
   constexpr bool kBf = DT == PKV_BF16;
   constexpr uint32_t kIdescS = umma_idesc(kBf, kTcRows, kTcKv, false);
-  constexpr uint32_t kIdescO = umma_idesc(kBf, kTcRows, kTcD, true);
+  constexpr uint32_t kIdescO = umma_idesc(kBf, kTcRows, D, true);
   float m = -INFINITY, l = 0.f;
   bool failed = false;
   int s_commits = 0, o_commits = 0;                   // tensor-core batches issued (same in every thread)
@@ -161,7 +176,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
   // Row locators of tile t (threads 0-63, one token each): the cache row
   // index (block * Hkv + kvh) * block_size + offset, or -1 for a token past
   // the range or in an out-of-range block (those read as zeros).
-  const int64_t* locs = reinterpret_cast<const int64_t*>(smem + kOffLoc);
+  const int64_t* locs = reinterpret_cast<const int64_t*>(smem + PL::kOffLoc);
   auto put_locators = [&](int t) {
     if (tid < kTcKv) {
       const int abs_t = t * kTcKv + tid;
@@ -175,22 +190,26 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
         else
           flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
       }
-      reinterpret_cast<int64_t*>(smem + kOffLoc)[tid] = row;
+      reinterpret_cast<int64_t*>(smem + PL::kOffLoc)[tid] = row;
     }
   };
   // The rows of the tile whose locators are in place, K (into the K-major K
   // tile) or V (into the MN-major V tile of buffer vbuf).  Thread tid copies
   // 16-byte chunk (tid >> 3) & 15 of tokens 8 i + (tid & 7), so eight
   // consecutive threads fill one 128-byte core matrix.
-  const int lr = tid & 7, lc = (tid >> 3) & 15;
+  // (D / 8 chunks per row: D = 128 -> every thread takes all 8 token groups
+  // of its chunk; D = 64 -> two thread sets take alternate groups)
+  constexpr int kCh = D / 8, kSets = kTcThreads / (8 * kCh);
+  const int lr = tid & 7, lc = (tid >> 3) % kCh, lset = (tid >> 3) / kCh;
   auto load_rows = [&](bool is_v, int vbuf) {
     const uint8_t* cache = is_v ? p.v_cache : p.k_cache;
-    const uint32_t base = sb + (is_v ? kOffV + vbuf * kVBytes : kOffK) + (lr << 4);
+    const uint32_t base = sb + (is_v ? PL::kOffV + vbuf * PL::kVBytes : PL::kOffK) + (lr << 4);
 #pragma unroll
-    for (int i = 0; i < kTcKv / 8; ++i) {
+    for (int k = 0; k < kTcKv / 8 / kSets; ++k) {
+      const int i = lset + kSets * k;
       const int64_t row = locs[8 * i + lr];
-      const uint32_t dst = base + (is_v ? ((lc * (kTcKv / 8) + i) << 7) : ((i * (kTcD / 8) + lc) << 7));
-      const uint8_t* src = row >= 0 ? cache + row * (kTcD * 2) + lc * 16 : cache;
+      const uint32_t dst = base + (is_v ? ((lc * (kTcKv / 8) + i) << 7) : ((i * (D / 8) + lc) << 7));
+      const uint8_t* src = row >= 0 ? cache + row * (D * 2) + lc * 16 : cache;
       cp_async_16_zfill(dst, src, row >= 0 ? 16u : 0u);
     }
   };
@@ -216,9 +235,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
-      for (int kk = 0; kk < kTcD / 16; ++kk)
-        umma(tmem_s, umma_desc(sb + kOffQ + kk * 256, 128, (kTcD / 8) * 128),
-             umma_desc(sb + kOffK + kk * 256, 128, (kTcD / 8) * 128), kIdescS, kk > 0);
+      for (int kk = 0; kk < D / 16; ++kk)
+        umma(tmem_s, umma_desc(sb + PL::kOffQ + kk * 256, 128, (D / 8) * 128),
+             umma_desc(sb + PL::kOffK + kk * 256, 128, (D / 8) * 128), kIdescS, kk > 0);
       umma_commit(bar_s);
     }
     ++s_commits;
@@ -290,7 +309,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
     }
     if (t > 0 && __any_sync(0xffffffffu, raise)) {    // rescale O (warp-collective)
 #pragma unroll
-      for (int k = 0; k < kTcD / 32; ++k) {
+      for (int k = 0; k < D / 32; ++k) {
         float o[32];
         tmem_ld32(tmem_o + lane_base + 32 * k, o);
 #pragma unroll
@@ -312,8 +331,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
         lw[k] = Half16<DT>::pack_rn(p0 - f.x, p1 - f.y);
       }
       const uint32_t off = core_off(tid, c8, kTcKv / 8);
-      st_shared_v4(sb + kOffPh + off, make_uint4(hw[0], hw[1], hw[2], hw[3]));
-      st_shared_v4(sb + kOffPl + off, make_uint4(lw[0], lw[1], lw[2], lw[3]));
+      st_shared_v4(sb + PL::kOffPh + off, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+      st_shared_v4(sb + PL::kOffPl + off, make_uint4(lw[0], lw[1], lw[2], lw[3]));
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -326,14 +345,14 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
     //    on, the next 8 head_dim values (kTcKv / 8) * 128 bytes on
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t vb = sb + kOffV + (t & 1) * kVBytes;
+      const uint32_t vb = sb + PL::kOffV + (t & 1) * PL::kVBytes;
 #pragma unroll
       for (int kk = 0; kk < kTcKv / 16; ++kk)
-        umma(tmem_o, umma_desc(sb + kOffPh + kk * 256, 128, (kTcKv / 8) * 128),
+        umma(tmem_o, umma_desc(sb + PL::kOffPh + kk * 256, 128, (kTcKv / 8) * 128),
              umma_desc(vb + kk * 256, 128, (kTcKv / 8) * 128), kIdescO, t > 0 || kk > 0);
 #pragma unroll
       for (int kk = 0; kk < kTcKv / 16; ++kk)
-        umma(tmem_o, umma_desc(sb + kOffPl + kk * 256, 128, (kTcKv / 8) * 128),
+        umma(tmem_o, umma_desc(sb + PL::kOffPl + kk * 256, 128, (kTcKv / 8) * 128),
              umma_desc(vb + kk * 256, 128, (kTcKv / 8) * 128), kIdescO, 1u);
       umma_commit(bar_o);
     }
@@ -355,18 +374,18 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
   const bool all_ok = __syncthreads_and(!failed) != 0;
   if (row_q && !(all_ok && ntiles > 0)) {
     uint16_t* orow = static_cast<uint16_t*>(p.out) +
-                     ((static_cast<int64_t>(p.q_start[b]) + j0 + jj) * p.num_q_heads + kvh * group + g) * kTcD;
-    for (int c = 0; c < kTcD / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
+                     ((static_cast<int64_t>(p.q_start[b]) + j0 + jj) * p.num_q_heads + kvh * group + g) * D;
+    for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
   }
   if (all_ok && ntiles > 0) {
 #pragma unroll
-    for (int k = 0; k < kTcD / 32; ++k) {
+    for (int k = 0; k < D / 32; ++k) {
       float o[32];
       tmem_ld32(tmem_o + lane_base + 32 * k, o);       // warp-collective: every row
       if (row_q) {
         uint16_t* orow = static_cast<uint16_t*>(p.out) +
                          ((static_cast<int64_t>(p.q_start[b]) + j0 + jj) * p.num_q_heads +
-                          kvh * group + g) * kTcD + 32 * k;
+                          kvh * group + g) * D + 32 * k;
         const float inv = (row_ok && l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -382,7 +401,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 0) tmem_dealloc(tmem, PL::kTmemCols);
   pdl_launch_dependents();
 }
 
@@ -401,20 +420,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
 //     (the largest V scale seen so far): P'' = p s_V / vu <= 1.  When a tile
 //     raises vu, O and the row sum (kept in the same units) are rescaled, and
 //     the output O / l is free of vu.
-// shared-memory plan of the one-byte kernel: Q, K, one V tile, P hi and lo,
-// the per-token scales of two tiles (by tile parity), barriers
-constexpr int kSc8Floats = 2 * kTcKv + 8;          // K scales, V scales, V max per half-tile
-constexpr int kOffV8 = kOffK + kKBytes;
-constexpr int kOffPh8 = kOffV8 + kVBytes;
-constexpr int kOffPl8 = kOffPh8 + kPBytes;
-constexpr int kOffS8 = kOffPl8 + kPBytes;
-constexpr int kOffBar8 = kOffS8 + 2 * kSc8Floats * 4;
-constexpr int kTc8Smem = kOffBar8 + 32;
-static_assert(2 * (kTc8Smem + 1024) <= 233472, "two CTAs per SM");
-
-template <int KV, int QT>
+template <int KV, int QT, int D>
 __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  using PL = TcPlan<D>;
   pdl_wait();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kvh = blockIdx.y, b = blockIdx.z;
@@ -441,13 +450,13 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
   const int ntiles = (kv_end + kTcKv - 1) / kTcKv;
 
   const uint32_t sb = smem_u32(smem);
-  const uint32_t bar_s = sb + kOffBar8, bar_o = sb + kOffBar8 + 8;
-  volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(smem + kOffBar8 + 16);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar8 + 20);
-  float* scb = reinterpret_cast<float*>(smem + kOffS8);   // [2][kSc8Floats]
+  const uint32_t bar_s = sb + PL::kOffBar8, bar_o = sb + PL::kOffBar8 + 8;
+  volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(smem + PL::kOffBar8 + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + PL::kOffBar8 + 20);
+  float* scb = reinterpret_cast<float*>(smem + PL::kOffS8);   // [2][PL::kSc8Floats]
 
   if (warp == 0) {
-    tmem_alloc(sb + kOffBar8 + 16, kTmemCols);
+    tmem_alloc(sb + PL::kOffBar8 + 16, PL::kTmemCols);
     tmem_relinquish();
   }
   if (tid == 0) {
@@ -468,11 +477,11 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
   {
     const uint16_t* qrow =
         p.q + ((static_cast<int64_t>(p.q_start[b]) + j0 + (row_q ? jj : 0)) * p.num_q_heads +
-               kvh * group + g) * kTcD;
+               kvh * group + g) * D;
     if constexpr (QT == PKV_F16) {
 #pragma unroll
-      for (int c = 0; c < kTcD / 8; ++c) {
-        const uint32_t dst = sb + kOffQ + core_off(tid, c, kTcD / 8);
+      for (int c = 0; c < D / 8; ++c) {
+        const uint32_t dst = sb + PL::kOffQ + core_off(tid, c, D / 8);
         if (row_ok) cp_async_16(dst, qrow + 8 * c);
         else st_shared_v4(dst, make_uint4(0, 0, 0, 0));
       }
@@ -481,7 +490,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
       float amax = 0.f;
       if (row_ok) {
 #pragma unroll 4
-        for (int c = 0; c < kTcD / 8; ++c) {
+        for (int c = 0; c < D / 8; ++c) {
           const uint4 v = ld_global_nc_v4(qrow + 8 * c);
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -496,7 +505,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
         qe = 14 - ex;
       }
 #pragma unroll 4
-      for (int c = 0; c < kTcD / 8; ++c) {
+      for (int c = 0; c < D / 8; ++c) {
         uint4 o = make_uint4(0, 0, 0, 0);
         if (row_ok) {
           const uint4 v = ld_global_nc_v4(qrow + 8 * c);
@@ -508,14 +517,14 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
                                             ldexpf(__uint_as_float(w[i] & 0xFFFF0000u), qe));
           o = make_uint4(h[0], h[1], h[2], h[3]);
         }
-        st_shared_v4(sb + kOffQ + core_off(tid, c, kTcD / 8), o);
+        st_shared_v4(sb + PL::kOffQ + core_off(tid, c, D / 8), o);
       }
     }
   }
 
   const float mult = ldexpf(p.softmax_scale * 1.4426950408889634f, -qe);
   constexpr uint32_t kIdescS = umma_idesc(false, kTcRows, kTcKv, false);
-  constexpr uint32_t kIdescO = umma_idesc(false, kTcRows, kTcD, true);
+  constexpr uint32_t kIdescO = umma_idesc(false, kTcRows, D, true);
   float m = -INFINITY, l = 0.f;                       // l in units of 1 / vu
   float vu = 1.f, lg_vu = 0.f;                         // V reference scale (1 until one is seen) and its log2
   bool vu_set = false;
@@ -524,13 +533,16 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
   const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
   const int64_t per_kv = static_cast<int64_t>(p.num_blocks) * p.num_kv_heads;
 
-  // this thread's share of a tile: 16-byte code chunk lrc of tokens 8 (lth + 2 j) + lr
-  const int lr = tid & 7, lrc = (tid >> 3) & 7, lth = tid >> 6;
+  // this thread's share of a tile: item tid + 128 j (j < D / 32) is 16-byte
+  // code chunk (item >> 3) % (D / 16) of token 8 ((item >> 3) / (D / 16)) + (tid & 7)
+  constexpr int kRc = D / 16, kNj = D / 32;
+  const int lr = tid & 7, lrc = (tid >> 3) % kRc;
+  auto tgroup = [&](int j) { return ((tid >> 3) + 16 * j) / kRc; };
   uint4 kraw[4], vraw[4];
   auto fetch = [&](int t) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int abs_t = t * kTcKv + 8 * (lth + 2 * j) + lr;
+    for (int j = 0; j < kNj; ++j) {
+      const int abs_t = t * kTcKv + 8 * tgroup(j) + lr;
       kraw[j] = make_uint4(0, 0, 0, 0);
       vraw[j] = make_uint4(0, 0, 0, 0);
       if (abs_t < kv_end) {
@@ -539,8 +551,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
         if (phys >= 0 && phys < p.num_blocks) {
           const int64_t row = (static_cast<int64_t>(phys) * p.num_kv_heads + kvh) * p.block_size +
                               (abs_t - logical * p.block_size);
-          kraw[j] = ld_global_nc_v4(p.k_cache + row * kTcD + lrc * 16);
-          vraw[j] = ld_global_nc_v4(p.v_cache + row * kTcD + lrc * 16);
+          kraw[j] = ld_global_nc_v4(p.k_cache + row * D + lrc * 16);
+          vraw[j] = ld_global_nc_v4(p.v_cache + row * D + lrc * 16);
         } else if (lrc == 0) {
           flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
         }
@@ -561,7 +573,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
           vs = __ldg(p.scales + per_kv + idx);
         }
       }
-      float* sc = scb + (t & 1) * kSc8Floats;
+      float* sc = scb + (t & 1) * PL::kSc8Floats;
       sc[tid] = ks;
       sc[kTcKv + tid] = vs;
       float vm = vs;
@@ -572,15 +584,15 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
   };
   // codes in registers -> f16 operand tile (K: K-major; V: MN-major)
   auto convert = [&](const uint4 (&raw)[4], bool is_v) {
-    const uint32_t base = sb + (is_v ? kOffV8 : kOffK) + (lr << 4);
+    const uint32_t base = sb + (is_v ? PL::kOffV8 : PL::kOffK) + (lr << 4);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int tb = lth + 2 * j;
+    for (int j = 0; j < kNj; ++j) {
+      const int tb = tgroup(j);
       uint4 lo, hi;
       codes16_to_f16<KV>(raw[j], lo, hi);
       const int c0 = 2 * lrc, c1 = 2 * lrc + 1;
-      const uint32_t o0 = is_v ? ((c0 * (kTcKv / 8) + tb) << 7) : ((tb * (kTcD / 8) + c0) << 7);
-      const uint32_t o1 = is_v ? ((c1 * (kTcKv / 8) + tb) << 7) : ((tb * (kTcD / 8) + c1) << 7);
+      const uint32_t o0 = is_v ? ((c0 * (kTcKv / 8) + tb) << 7) : ((tb * (D / 8) + c0) << 7);
+      const uint32_t o1 = is_v ? ((c1 * (kTcKv / 8) + tb) << 7) : ((tb * (D / 8) + c1) << 7);
       st_shared_v4(base + o0, lo);
       st_shared_v4(base + o1, hi);
     }
@@ -603,9 +615,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
-      for (int kk = 0; kk < kTcD / 16; ++kk)
-        umma(tmem_s, umma_desc(sb + kOffQ + kk * 256, 128, (kTcD / 8) * 128),
-             umma_desc(sb + kOffK + kk * 256, 128, (kTcD / 8) * 128), kIdescS, kk > 0);
+      for (int kk = 0; kk < D / 16; ++kk)
+        umma(tmem_s, umma_desc(sb + PL::kOffQ + kk * 256, 128, (D / 8) * 128),
+             umma_desc(sb + PL::kOffK + kk * 256, 128, (D / 8) * 128), kIdescS, kk > 0);
       umma_commit(bar_s);
     }
     ++s_commits;
@@ -627,7 +639,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
     }
     tc_fence_after();
     // 4. row tid of S times each column's K scale
-    const float* sc = scb + (t & 1) * kSc8Floats;
+    const float* sc = scb + (t & 1) * PL::kSc8Floats;
     float s[kTcKv];
     {
       float a[32];
@@ -691,7 +703,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
     l *= alpha;
     if (t > 0 && (__any_sync(0xffffffffu, raise) || rebase)) {
 #pragma unroll
-      for (int k = 0; k < kTcD / 32; ++k) {
+      for (int k = 0; k < D / 32; ++k) {
         float o[32];
         tmem_ld32(tmem_o + lane_base + 32 * k, o);
 #pragma unroll
@@ -718,8 +730,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
         lw[k] = Half16<PKV_F16>::pack_rn(q0 - f.x, q1 - f.y);
       }
       const uint32_t off = core_off(tid, c8, kTcKv / 8);
-      st_shared_v4(sb + kOffPh8 + off, make_uint4(hw[0], hw[1], hw[2], hw[3]));
-      st_shared_v4(sb + kOffPl8 + off, make_uint4(lw[0], lw[1], lw[2], lw[3]));
+      st_shared_v4(sb + PL::kOffPh8 + off, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+      st_shared_v4(sb + PL::kOffPl8 + off, make_uint4(lw[0], lw[1], lw[2], lw[3]));
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -730,12 +742,12 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < kTcKv / 16; ++kk)
-        umma(tmem_o, umma_desc(sb + kOffPh8 + kk * 256, 128, (kTcKv / 8) * 128),
-             umma_desc(sb + kOffV8 + kk * 256, 128, (kTcKv / 8) * 128), kIdescO, t > 0 || kk > 0);
+        umma(tmem_o, umma_desc(sb + PL::kOffPh8 + kk * 256, 128, (kTcKv / 8) * 128),
+             umma_desc(sb + PL::kOffV8 + kk * 256, 128, (kTcKv / 8) * 128), kIdescO, t > 0 || kk > 0);
 #pragma unroll
       for (int kk = 0; kk < kTcKv / 16; ++kk)
-        umma(tmem_o, umma_desc(sb + kOffPl8 + kk * 256, 128, (kTcKv / 8) * 128),
-             umma_desc(sb + kOffV8 + kk * 256, 128, (kTcKv / 8) * 128), kIdescO, 1u);
+        umma(tmem_o, umma_desc(sb + PL::kOffPl8 + kk * 256, 128, (kTcKv / 8) * 128),
+             umma_desc(sb + PL::kOffV8 + kk * 256, 128, (kTcKv / 8) * 128), kIdescO, 1u);
       umma_commit(bar_o);
     }
     ++o_commits;
@@ -752,14 +764,14 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
   tc_fence_after();
   const bool all_ok = __syncthreads_and(!failed) != 0;
   uint16_t* orow = static_cast<uint16_t*>(p.out) +
-                   ((static_cast<int64_t>(p.q_start[b]) + j0 + jj) * p.num_q_heads + kvh * group + g) * kTcD;
+                   ((static_cast<int64_t>(p.q_start[b]) + j0 + jj) * p.num_q_heads + kvh * group + g) * D;
   if (row_q && !(all_ok && ntiles > 0)) {
-    for (int c = 0; c < kTcD / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
+    for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
   }
   if (all_ok && ntiles > 0) {
     const float inv = (row_ok && l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
-    for (int k = 0; k < kTcD / 32; ++k) {
+    for (int k = 0; k < D / 32; ++k) {
       float o[32];
       tmem_ld32(tmem_o + lane_base + 32 * k, o);       // warp-collective: every row
       if (row_q) {
@@ -777,7 +789,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 0) tmem_dealloc(tmem, PL::kTmemCols);
   pdl_launch_dependents();
 }
 
@@ -812,29 +824,35 @@ cudaError_t launch_tc(Kern kern, int smem_bytes, const PrefillArgs& a, cudaStrea
   return launch_pdl(kern, grid, dim3(kTcThreads), smem_bytes, st, p);
 }
 
-template <int KV>
+template <int KV, int D>
 cudaError_t launch_tc8(const PrefillArgs& a, cudaStream_t st) {
-  return a.q_dtype == PKV_F16 ? launch_tc(prefill_tc8_kernel<KV, PKV_F16>, kTc8Smem, a, st)
-                              : launch_tc(prefill_tc8_kernel<KV, PKV_BF16>, kTc8Smem, a, st);
+  constexpr int kSmem = TcPlan<D>::kSmem8;
+  return a.q_dtype == PKV_F16 ? launch_tc(prefill_tc8_kernel<KV, PKV_F16, D>, kSmem, a, st)
+                              : launch_tc(prefill_tc8_kernel<KV, PKV_BF16, D>, kSmem, a, st);
+}
+
+template <int D>
+cudaError_t launch_tc_d(const PrefillArgs& a, cudaStream_t st) {
+  switch (a.kv_dtype) {
+    case PKV_F16: return launch_tc(prefill_tc_kernel<PKV_F16, D>, TcPlan<D>::kSmem, a, st);
+    case PKV_BF16: return launch_tc(prefill_tc_kernel<PKV_BF16, D>, TcPlan<D>::kSmem, a, st);
+    case PKV_FP8_E4M3: return launch_tc8<PKV_FP8_E4M3, D>(a, st);
+    case PKV_FP8_E5M2: return launch_tc8<PKV_FP8_E5M2, D>(a, st);
+    case PKV_INT8: return launch_tc8<PKV_INT8, D>(a, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
 bool prefill_tc_supported(const PrefillArgs& a) {
   return (a.kv_dtype == PKV_F16 || a.kv_dtype == PKV_BF16 || is_blk8(a.kv_dtype)) &&
-         a.head_dim == kTcD;
+         (a.head_dim == 64 || a.head_dim == 128);
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st) {
   if (a.num_seqs == 0 || a.max_query_len == 0) return cudaSuccess;
-  switch (a.kv_dtype) {
-    case PKV_F16: return launch_tc(prefill_tc_kernel<PKV_F16>, kTcSmem, a, st);
-    case PKV_BF16: return launch_tc(prefill_tc_kernel<PKV_BF16>, kTcSmem, a, st);
-    case PKV_FP8_E4M3: return launch_tc8<PKV_FP8_E4M3>(a, st);
-    case PKV_FP8_E5M2: return launch_tc8<PKV_FP8_E5M2>(a, st);
-    case PKV_INT8: return launch_tc8<PKV_INT8>(a, st);
-    default: return cudaErrorInvalidValue;
-  }
+  return a.head_dim == 64 ? launch_tc_d<64>(a, st) : launch_tc_d<128>(a, st);
 }
 
 }  // namespace pkv
