@@ -53,18 +53,19 @@ constexpr int kPBytes = kTcRows * kTcKv * 2;      // 16 KiB each, hi and lo
 // Shared-memory plans (bytes; operand tiles 1024-byte aligned) and tensor
 // memory (S: columns [0, 64); O: [64, 64 + D)) for head_dim D.
 template <int D> struct TcPlan {
-  static constexpr uint32_t kTmemCols = D == 64 ? 128 : 256;
+  // 16-bit caches: S [0, 64), O [64, 64 + D), P hi and lo [64 + D, 128 + D)
+  static constexpr uint32_t kTmemCols = 256;
+  // one-byte caches (P in shared memory): S [0, 64), O [64, 64 + D)
+  static constexpr uint32_t kTmemCols8 = D == 64 ? 128 : 256;
   static constexpr int kQBytes = kTcRows * D * 2;
   static constexpr int kKBytes = kTcKv * D * 2;
   static constexpr int kVBytes = kTcKv * D * 2;
-  // 16-bit caches: Q, K, two V tiles, P hi and lo, the row locators of the
-  // next tile to load (int64 each), two mbarriers + tensor-memory address + flag
+  // 16-bit caches: Q, K, two V tiles, the row locators of the next tile to
+  // load (int64 each), two mbarriers + tensor-memory address + flag
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBytes;
   static constexpr int kOffV = kOffK + kKBytes;
-  static constexpr int kOffPh = kOffV + 2 * kVBytes;
-  static constexpr int kOffPl = kOffPh + kPBytes;
-  static constexpr int kOffLoc = kOffPl + kPBytes;
+  static constexpr int kOffLoc = kOffV + 2 * kVBytes;
   static constexpr int kOffBar = kOffLoc + kTcKv * 8;
   static constexpr int kSmem = kOffBar + 32;
   // one-byte caches: Q, K, one V tile, P hi and lo, the per-token scales of
@@ -148,7 +149,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t tmem_s = tmem, tmem_o = tmem + 64;
+  const uint32_t tmem_s = tmem, tmem_o = tmem + 64, tmem_p = tmem + 64 + D;
   const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;   // this warp's 32 lanes
 
   // Q rows (K-major core matrices; rows without a query are zero)
@@ -317,7 +318,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
         tmem_st32(tmem_o + lane_base + 32 * k, o);
       }
     }
-    // P = 2^(s - m) as a 16-bit hi + lo pair, row tid of the K-major P tiles
+    // P = 2^(s - m) as a 16-bit hi + lo pair into row tid of the tensor-memory
+    // A operand (two tokens per 32-bit column): hi at tmem_p, lo 32 columns on
 #pragma unroll
     for (int c8 = 0; c8 < kTcKv / 8; ++c8) {
       uint32_t hw[4], lw[4];
@@ -330,30 +332,30 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
         const float2 f = Half16<DT>::unpack(hw[k]);
         lw[k] = Half16<DT>::pack_rn(p0 - f.x, p1 - f.y);
       }
-      const uint32_t off = core_off(tid, c8, kTcKv / 8);
-      st_shared_v4(sb + PL::kOffPh + off, make_uint4(hw[0], hw[1], hw[2], hw[3]));
-      st_shared_v4(sb + PL::kOffPl + off, make_uint4(lw[0], lw[1], lw[2], lw[3]));
+      tmem_st4(tmem_p + lane_base + 4 * c8, hw[0], hw[1], hw[2], hw[3]);
+      tmem_st4(tmem_p + lane_base + kTcKv / 2 + 4 * c8, lw[0], lw[1], lw[2], lw[3]);
     }
-    fence_proxy_async_smem();
+    tmem_store_wait();
     tc_fence_before();
     __syncthreads();
     if (*abort_flag) { failed = true; break; }
     // every thread has issued its copies of tile t + 1: the locators of tile
     // t + 2 may replace theirs (read after the next iteration's barrier)
     if (t + 2 < ntiles) put_locators(t + 2);
-    // 6. O += P V (hi, then lo); V is MN-major: the next 16 tokens 256 bytes
-    //    on, the next 8 head_dim values (kTcKv / 8) * 128 bytes on
+    // 6. O += P V (hi, then lo), P from tensor memory (16 tokens = 8 columns
+    //    per MMA); V is MN-major: the next 16 tokens 256 bytes on, the next 8
+    //    head_dim values (kTcKv / 8) * 128 bytes on
     if (tid == 0) {
       tc_fence_after();
       const uint32_t vb = sb + PL::kOffV + (t & 1) * PL::kVBytes;
 #pragma unroll
       for (int kk = 0; kk < kTcKv / 16; ++kk)
-        umma(tmem_o, umma_desc(sb + PL::kOffPh + kk * 256, 128, (kTcKv / 8) * 128),
-             umma_desc(vb + kk * 256, 128, (kTcKv / 8) * 128), kIdescO, t > 0 || kk > 0);
+        umma_ts(tmem_o, tmem_p + kk * 8, umma_desc(vb + kk * 256, 128, (kTcKv / 8) * 128),
+                kIdescO, t > 0 || kk > 0);
 #pragma unroll
       for (int kk = 0; kk < kTcKv / 16; ++kk)
-        umma(tmem_o, umma_desc(sb + PL::kOffPl + kk * 256, 128, (kTcKv / 8) * 128),
-             umma_desc(vb + kk * 256, 128, (kTcKv / 8) * 128), kIdescO, 1u);
+        umma_ts(tmem_o, tmem_p + kTcKv / 2 + kk * 8, umma_desc(vb + kk * 256, 128, (kTcKv / 8) * 128),
+                kIdescO, 1u);
       umma_commit(bar_o);
     }
     ++o_commits;
@@ -456,7 +458,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
   float* scb = reinterpret_cast<float*>(smem + PL::kOffS8);   // [2][PL::kSc8Floats]
 
   if (warp == 0) {
-    tmem_alloc(sb + PL::kOffBar8 + 16, PL::kTmemCols);
+    tmem_alloc(sb + PL::kOffBar8 + 16, PL::kTmemCols8);
     tmem_relinquish();
   }
   if (tid == 0) {
@@ -789,7 +791,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, PL::kTmemCols);
+  if (warp == 0) tmem_dealloc(tmem, PL::kTmemCols8);
   pdl_launch_dependents();
 }
 
