@@ -48,15 +48,12 @@ constexpr int kTcThreads = 128;      // one warpgroup; thread r owns query row r
 constexpr int kTcRows = 128;         // MMA M
 constexpr int kTcKv = 64;            // KV tokens per tile
 constexpr float kTcTau = 8.f;        // lazy rescale threshold (log2 units)
-constexpr int kPBytes = kTcRows * kTcKv * 2;      // 16 KiB each, hi and lo
 
 // Shared-memory plans (bytes; operand tiles 1024-byte aligned) and tensor
 // memory (S: columns [0, 64); O: [64, 64 + D)) for head_dim D.
 template <int D> struct TcPlan {
-  // 16-bit caches: S [0, 64), O [64, 64 + D), P hi and lo [64 + D, 128 + D)
+  // S [0, 64), O [64, 64 + D), P hi and lo [64 + D, 128 + D)
   static constexpr uint32_t kTmemCols = 256;
-  // one-byte caches (P in shared memory): S [0, 64), O [64, 64 + D)
-  static constexpr uint32_t kTmemCols8 = D == 64 ? 128 : 256;
   static constexpr int kQBytes = kTcRows * D * 2;
   static constexpr int kKBytes = kTcKv * D * 2;
   static constexpr int kVBytes = kTcKv * D * 2;
@@ -68,13 +65,11 @@ template <int D> struct TcPlan {
   static constexpr int kOffLoc = kOffV + 2 * kVBytes;
   static constexpr int kOffBar = kOffLoc + kTcKv * 8;
   static constexpr int kSmem = kOffBar + 32;
-  // one-byte caches: Q, K, one V tile, P hi and lo, the per-token scales of
-  // two tiles (by tile parity: K scales, V scales, V max per half-tile), barriers
+  // one-byte caches: Q, K, one V tile, the per-token scales of two tiles (by
+  // tile parity: K scales, V scales, V max per half-tile), barriers
   static constexpr int kSc8Floats = 2 * kTcKv + 8;
   static constexpr int kOffV8 = kOffK + kKBytes;
-  static constexpr int kOffPh8 = kOffV8 + kVBytes;
-  static constexpr int kOffPl8 = kOffPh8 + kPBytes;
-  static constexpr int kOffS8 = kOffPl8 + kPBytes;
+  static constexpr int kOffS8 = kOffV8 + kVBytes;
   static constexpr int kOffBar8 = kOffS8 + 2 * kSc8Floats * 4;
   static constexpr int kSmem8 = kOffBar8 + 32;
   static_assert(2 * (kSmem + 1024) <= 233472 && 2 * (kSmem8 + 1024) <= 233472,
@@ -458,7 +453,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
   float* scb = reinterpret_cast<float*>(smem + PL::kOffS8);   // [2][PL::kSc8Floats]
 
   if (warp == 0) {
-    tmem_alloc(sb + PL::kOffBar8 + 16, PL::kTmemCols8);
+    tmem_alloc(sb + PL::kOffBar8 + 16, PL::kTmemCols);
     tmem_relinquish();
   }
   if (tid == 0) {
@@ -471,7 +466,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t tmem_s = tmem, tmem_o = tmem + 64;
+  const uint32_t tmem_s = tmem, tmem_o = tmem + 64, tmem_p = tmem + 64 + D;
   const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
 
   // Q row tid as f16 (bf16 q: times 2^qe, the row's largest magnitude in [2^13, 2^14))
@@ -731,11 +726,11 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
         const float2 f = Half16<PKV_F16>::unpack(hw[k]);
         lw[k] = Half16<PKV_F16>::pack_rn(q0 - f.x, q1 - f.y);
       }
-      const uint32_t off = core_off(tid, c8, kTcKv / 8);
-      st_shared_v4(sb + PL::kOffPh8 + off, make_uint4(hw[0], hw[1], hw[2], hw[3]));
-      st_shared_v4(sb + PL::kOffPl8 + off, make_uint4(lw[0], lw[1], lw[2], lw[3]));
+      tmem_st4(tmem_p + lane_base + 4 * c8, hw[0], hw[1], hw[2], hw[3]);
+      tmem_st4(tmem_p + lane_base + kTcKv / 2 + 4 * c8, lw[0], lw[1], lw[2], lw[3]);
     }
-    fence_proxy_async_smem();
+    tmem_store_wait();
+    fence_proxy_async_smem();                          // the V tile's converted rows
     tc_fence_before();
     __syncthreads();
     if (*abort_flag) { failed = true; break; }
@@ -744,12 +739,12 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < kTcKv / 16; ++kk)
-        umma(tmem_o, umma_desc(sb + PL::kOffPh8 + kk * 256, 128, (kTcKv / 8) * 128),
-             umma_desc(sb + PL::kOffV8 + kk * 256, 128, (kTcKv / 8) * 128), kIdescO, t > 0 || kk > 0);
+        umma_ts(tmem_o, tmem_p + kk * 8, umma_desc(sb + PL::kOffV8 + kk * 256, 128, (kTcKv / 8) * 128),
+                kIdescO, t > 0 || kk > 0);
 #pragma unroll
       for (int kk = 0; kk < kTcKv / 16; ++kk)
-        umma(tmem_o, umma_desc(sb + PL::kOffPl8 + kk * 256, 128, (kTcKv / 8) * 128),
-             umma_desc(sb + PL::kOffV8 + kk * 256, 128, (kTcKv / 8) * 128), kIdescO, 1u);
+        umma_ts(tmem_o, tmem_p + kTcKv / 2 + kk * 8,
+                umma_desc(sb + PL::kOffV8 + kk * 256, 128, (kTcKv / 8) * 128), kIdescO, 1u);
       umma_commit(bar_o);
     }
     ++o_commits;
@@ -791,7 +786,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, PL::kTmemCols8);
+  if (warp == 0) tmem_dealloc(tmem, PL::kTmemCols);
   pdl_launch_dependents();
 }
 
