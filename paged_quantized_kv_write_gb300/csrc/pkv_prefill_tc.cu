@@ -650,10 +650,12 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
 #pragma unroll
     for (int c4 = 0; c4 < kTcKv / 4; ++c4) {
       const float4 ks = *reinterpret_cast<const float4*>(sc + 4 * c4);
-      s[4 * c4] *= ks.x;
-      s[4 * c4 + 1] *= ks.y;
-      s[4 * c4 + 2] *= ks.z;
-      s[4 * c4 + 3] *= ks.w;
+      const float2 a = f2_unpack(f2_mul(f2_pack(s[4 * c4], s[4 * c4 + 1]), f2_pack(ks.x, ks.y)));
+      const float2 c = f2_unpack(f2_mul(f2_pack(s[4 * c4 + 2], s[4 * c4 + 3]), f2_pack(ks.z, ks.w)));
+      s[4 * c4] = a.x;
+      s[4 * c4 + 1] = a.y;
+      s[4 * c4 + 2] = c.x;
+      s[4 * c4 + 3] = c.y;
     }
     const bool full = t0 + kTcKv <= kv_end && t0 + kTcKv - 1 <= pos0 + j0;
     float tmax, pmul;
@@ -710,6 +712,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
     }
     // P / vu = 2^(x - m - log2 vu); P'' = (P / vu) s_V as an f16 hi + lo pair
     const float moff = m + lg_vu;
+    // (score pairs as packed fp32: one fused multiply-add, one add to the
+    // pair of row-sum halves, one multiply and one subtraction per two scores)
+    const uint64_t pm2 = f2_pack(pmul, pmul), nm2 = f2_pack(-moff, -moff);
+    uint64_t l2 = f2_pack(0.f, 0.f);
 #pragma unroll
     for (int c8 = 0; c8 < kTcKv / 8; ++c8) {
       const float4 va = *reinterpret_cast<const float4*>(sc + kTcKv + 8 * c8);
@@ -718,16 +724,22 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
       uint32_t hw[4], lw[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float p0 = ex2_ftz(fmaf(s[8 * c8 + 2 * k], pmul, -moff));
-        const float p1 = ex2_ftz(fmaf(s[8 * c8 + 2 * k + 1], pmul, -moff));
-        l += p0 + p1;
-        const float q0 = p0 * vsc[2 * k], q1 = p1 * vsc[2 * k + 1];
-        hw[k] = Half16<PKV_F16>::pack_rn(q0, q1);
+        const float2 x = f2_unpack(f2_fma(f2_pack(s[8 * c8 + 2 * k], s[8 * c8 + 2 * k + 1]), pm2, nm2));
+        const uint64_t pp = f2_pack(ex2_ftz(x.x), ex2_ftz(x.y));
+        l2 = f2_add(l2, pp);
+        const uint64_t qq = f2_mul(pp, f2_pack(vsc[2 * k], vsc[2 * k + 1]));
+        const float2 q = f2_unpack(qq);
+        hw[k] = Half16<PKV_F16>::pack_rn(q.x, q.y);
         const float2 f = Half16<PKV_F16>::unpack(hw[k]);
-        lw[k] = Half16<PKV_F16>::pack_rn(q0 - f.x, q1 - f.y);
+        const float2 d = f2_unpack(f2_sub(qq, f2_pack(f.x, f.y)));
+        lw[k] = Half16<PKV_F16>::pack_rn(d.x, d.y);
       }
       tmem_st4(tmem_p + lane_base + 4 * c8, hw[0], hw[1], hw[2], hw[3]);
       tmem_st4(tmem_p + lane_base + kTcKv / 2 + 4 * c8, lw[0], lw[1], lw[2], lw[3]);
+    }
+    {
+      const float2 lh = f2_unpack(l2);
+      l += lh.x + lh.y;
     }
     tmem_store_wait();
     fence_proxy_async_smem();                          // the V tile's converted rows
