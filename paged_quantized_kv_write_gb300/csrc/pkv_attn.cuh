@@ -48,6 +48,7 @@
 #include "pkv_common.cuh"
 #include "pkv_encode.cuh"
 #include "pkv_internal.h"
+#include "pkv_tcgen05.cuh"
 
 namespace pkv {
 namespace {
@@ -787,6 +788,7 @@ paged_decode_kernel(const Params p) {
                 }
               }
               uint32_t sz0[NG], sz1[NG];             // (scale, zero) words of tokens q4, q4 + 8
+              uint64_t sc01 = tc::f2_pack(0.f, 0.f), sc23 = tc::f2_pack(0.f, 0.f);
               if constexpr (D == 128) {
                 const uint4 a = ld_shared_v4(ksc + q4 * SR), c = ld_shared_v4(ksc + (q4 + 8) * SR);
                 sz0[0] = a.x; sz0[1] = a.y; sz0[2] = a.z; sz0[3] = a.w;
@@ -823,13 +825,15 @@ paged_decode_kernel(const Params p) {
                 mma_16816<PKV_F16>(g4, a1, qb[2 * grp + 1][0], qb[2 * grp + 1][1]);
                 const float s0 = __low2float(*reinterpret_cast<const __half2*>(&sz0[grp]));
                 const float s1 = __low2float(*reinterpret_cast<const __half2*>(&sz1[grp]));
-                sc[0] += s0 * g4[0];
-                sc[1] += s0 * g4[1];
-                sc[2] += s1 * g4[2];
-                sc[3] += s1 * g4[3];
+                sc01 = tc::f2_fma(tc::f2_pack(s0, s0), tc::f2_pack(g4[0], g4[1]), sc01);
+                sc23 = tc::f2_fma(tc::f2_pack(s1, s1), tc::f2_pack(g4[2], g4[3]), sc23);
               }
-#pragma unroll
-              for (int k = 0; k < 4; ++k) sc[k] = sc[k] * kq24 + zs[k] * zscale;
+              {
+                const uint64_t q2 = tc::f2_pack(kq24, kq24), z2 = tc::f2_pack(zscale, zscale);
+                const float2 a = tc::f2_unpack(tc::f2_fma(sc01, q2, tc::f2_mul(tc::f2_pack(zs[0], zs[1]), z2)));
+                const float2 c = tc::f2_unpack(tc::f2_fma(sc23, q2, tc::f2_mul(tc::f2_pack(zs[2], zs[3]), z2)));
+                sc[0] = a.x; sc[1] = a.y; sc[2] = c.x; sc[3] = c.y;
+              }
             }
 
 #pragma unroll
