@@ -20,16 +20,17 @@
 //   2. S = Q K^T: eight tcgen05.mma (M 128, N 64, K 16) into tensor memory;
 //   3. thread r reads row r of S from tensor memory, applies the causal mask
 //      and the online softmax (running max raised lazily, by more than
-//      2^8 only), and writes P as a 16-bit hi + lo pair;
-//   4. O += P V: eight tcgen05.mma (M 128, N 128, K 16) into tensor memory,
-//      hi then lo;
+//      2^8 only), and writes row r of P as a 16-bit hi + lo pair back into
+//      tensor memory (two tokens per 32-bit column);
+//   4. O += P V: eight tcgen05.mma (M 128, N = head_dim, K 16) into tensor
+//      memory, hi then lo, with P read from tensor memory as the A operand;
 // and finally reads O from tensor memory, divides by the row sums and writes
-// the output rows.  Operands sit in shared memory in the canonical layouts
-// without swizzle, built from 8 x 16-byte core matrices: K-major (Q, K, P)
-// with the next core matrix along K 128 bytes on (leading byte offset) and
-// the next 8-row group further (stride byte offset); MN-major (V) with 8
-// tokens x 8 head_dim values per core matrix, the next token group 128 bytes
-// on and the next 8 head_dim values 1024 bytes on.  Every wait for the tensor
+// the output rows.  The other operands sit in shared memory in the canonical
+// layouts without swizzle, built from 8 x 16-byte core matrices: K-major
+// (Q, K) with the next core matrix along K 128 bytes on (leading byte
+// offset) and the next 8-row group further (stride byte offset); MN-major (V)
+// with 8 tokens x 8 head_dim values per core matrix, the next token group 128
+// bytes on and the next 8 head_dim values 1024 bytes on.  Every wait for the tensor
 // cores is bounded: when one runs out the launch ORs PKV_ERR_DEVICE_TIMEOUT
 // into dev_status, stops, and still frees its tensor memory.
 #include <math.h>
@@ -414,9 +415,11 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
 //     multiplier;
 //   * a token's K block scale multiplies its score column; its V block scale
 //     multiplies its column of P, in units of a running reference scale vu
-//     (the largest V scale seen so far): P'' = p s_V / vu <= 1.  When a tile
+//     (the largest V scale seen so far): P'' = p s_V / vu <= 2^8.  When a tile
 //     raises vu, O and the row sum (kept in the same units) are rescaled, and
-//     the output O / l is free of vu.
+//     the output O / l is free of vu;
+//   * P'' goes to tensor memory as in the 16-bit kernel, and the softmax works
+//     on packed fp32 pairs (two scores per fma / add / mul / sub).
 template <int KV, int QT, int D>
 __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
