@@ -1,9 +1,14 @@
 // Decode-phase PagedAttention for one-byte caches (FP8 E4M3, FP8 E5M2, INT8;
 // one fp32 scale per block and KV head) with head_dim 128 on the
-// fifth-generation tensor cores, accumulators in tensor memory.  Same
-// results as paged_decode_kernel (the mma.sync kernel), computed with fewer
-// instructions per cached token: the dequantized tiles feed the tensor cores
-// from shared memory, and the softmax runs with one thread per token.
+// fifth-generation tensor cores, accumulators in tensor memory: the
+// dequantized tiles feed the tensor cores from shared memory, and the
+// softmax runs with one thread per token.  It computes what
+// paged_decode_kernel (the mma.sync kernel) computes and is kept as a
+// comparator (PKV_DECODE_MODE=tc), never chosen by the library: on GB300 it
+// runs about 2.7x slower, because each CTA works through one serial chain
+// per tile (row lookup, code loads, conversion, S, softmax vote, P V) and
+// only three such chains fit on an SM, against twelve independent copy rings
+// per SM in the mma.sync kernel.
 //
 // The computation is the one "KV Cache Compression & Paged Attention"
 // (myaihardware.com, section "Implementation Details") describes for the
