@@ -104,3 +104,27 @@ def test_workspace_and_partition_queries(lib):
     n = lib.paged_decode_workspace_bytes(16, 64, 8, 128, 2048, 16, 512)
     assert n >= 16 * 64 * 64 * 130 * 4
     assert lib.paged_decode_partition_size(16, 64, 8, 2048, 16, 500) == 512
+
+
+@pytest.mark.parametrize("cfg,expected", [(2, 1024), (3, 512), (4, 512), (5, 512)])
+def test_partition_heuristic_and_workspace_for_the_benchmark_workloads(lib, cfg, expected):
+    """The library's own partition choice for each benchmark workload (the one the
+    block-size / partition sweep found best or within 1.5% of it), and the
+    workspace it needs: one fp32 row of head_dim per (sequence, q head,
+    partition), 256-byte aligned, then (max, sum) per partition."""
+    import workloads as W
+    w = W.CONFIGS[cfg]
+    mb = -(-w.ctx_hi // w.block_size)            # the table width of the longest context
+    part = lib.lib.paged_decode_partition_size(w.batch, w.num_q_heads, w.num_kv_heads, mb,
+                                               w.block_size, 0)
+    assert part == expected and part % 16 == 0
+    np_ = -(-mb * w.block_size // part)
+    heads = w.batch * w.num_q_heads
+    out_bytes = heads * np_ * w.head_dim * 4
+    want = (-(-out_bytes // 256)) * 256 + heads * np_ * 2 * 4
+    got = lib.lib.paged_decode_workspace_bytes(w.batch, w.num_q_heads, w.num_kv_heads,
+                                               w.head_dim, mb, w.block_size, 0)
+    assert got == want
+    # an explicit request is rounded up to a multiple of 16 tokens
+    assert lib.lib.paged_decode_partition_size(w.batch, w.num_q_heads, w.num_kv_heads, mb,
+                                               w.block_size, 100) == 112
