@@ -34,6 +34,7 @@
 // cores is bounded: when one runs out the launch ORs PKV_ERR_DEVICE_TIMEOUT
 // into dev_status, stops, and still frees its tensor memory.
 #include <math.h>
+#include <stdlib.h>
 #include <stdint.h>
 
 #include "pagedkv.h"
@@ -86,6 +87,7 @@ struct TcParams {
   const int32_t* q_start;
   const float* scales;        // one-byte caches: fp32 [2][num_blocks][num_kv_heads]
   int max_query_len;          // queries j >= max_query_len of a chunk are not computed
+  int test_drop_commit;       // test of the bounded waits: the first S batch is not committed
   void* out;
   int* dev_status;
   int max_blocks_per_seq;
@@ -235,7 +237,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
       for (int kk = 0; kk < D / 16; ++kk)
         umma(tmem_s, umma_desc(sb + PL::kOffQ + kk * 256, 128, (D / 8) * 128),
              umma_desc(sb + PL::kOffK + kk * 256, 128, (D / 8) * 128), kIdescS, kk > 0);
-      umma_commit(bar_s);
+      // (a test of the bounded waits leaves the first batch uncommitted: the
+      // wait below then runs out and the launch reports PKV_ERR_DEVICE_TIMEOUT)
+      if (!(p.test_drop_commit && t == 0)) umma_commit(bar_s);
     }
     ++s_commits;
     if (!mbar_wait(bar_s, t & 1)) {
@@ -824,6 +828,7 @@ cudaError_t launch_tc(Kern kern, int smem_bytes, const PrefillArgs& a, cudaStrea
   p.block_size = a.block_size;
   p.softmax_scale = a.softmax_scale;
   p.max_query_len = a.max_query_len;
+  p.test_drop_commit = getenv("PKV_TEST_DROP_COMMIT") != nullptr;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,

@@ -176,3 +176,22 @@ def test_prefill_benchmark_workload_sampled():
                                        s, w.kv_dtype, case.num_blocks, w.softmax_scale,
                                        w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size)
         H.check_close(gpu[r:r + 1], ref, w.kv_dtype, w.q_dtype, f"row {r}")
+
+
+def test_prefill_tc_bounded_wait_reports_a_timeout(monkeypatch):
+    """The tcgen05 prefill with its first S batch left uncommitted
+    (PKV_TEST_DROP_COMMIT): the bounded wait on it runs out (about 2 s), the call
+    reports PKV_ERR_DEVICE_TIMEOUT through dev_status and zeros in its rows, and
+    the next call on the same context is exact again."""
+    pkv = _pkv()
+    monkeypatch.delenv("PKV_PREFILL_MODE", raising=False)
+    w = W.Workload("timeout", 1, 8, 2, 128, 16, W.BF16, W.BF16, "fixed", 40, 40, seed=9)
+    case = W.make_case(w)
+    monkeypatch.setenv("PKV_TEST_DROP_COMMIT", "1")
+    gpu, _, st, _ = _run(case, [8])
+    assert st & pkv.PKV_ERR_DEVICE_TIMEOUT
+    assert not gpu.any()
+    monkeypatch.delenv("PKV_TEST_DROP_COMMIT")
+    gpu, ref, st, _ = _run(case, [8])
+    assert st == 0
+    H.check_close(gpu, ref, W.BF16, W.BF16, "after a timed-out launch")
