@@ -519,9 +519,11 @@ static int attend_one(const uint16_t* q, int q_dtype, const void* k_cache,
     double denom = 0.0;
     for (int t = 0; t < ctx; ++t) {
         int32_t phys, off;
-        oracle_physical_address(table_row, max_blocks_per_seq, block_size, t, &phys, &off);
-        oracle_dequant_row(v_cache, scales, 1, kv_dtype, num_blocks, num_kv_heads, head_dim,
-                           block_size, phys, kv_head, off, row);
+        if (oracle_physical_address(table_row, max_blocks_per_seq, block_size, t, &phys, &off))
+            return -1;
+        if (oracle_dequant_row(v_cache, scales, 1, kv_dtype, num_blocks, num_kv_heads, head_dim,
+                               block_size, phys, kv_head, off, row))
+            return -1;
         double w = exp(scores[t] - mx);
         denom += w;
         for (int d = 0; d < head_dim; ++d) out[d] += w * row[d];
