@@ -99,3 +99,24 @@ def test_algorithmic_bytes_config2():
     kv = 2 * int(case.context_lens.sum()) * 8 * 128 * 2
     got = W.attention_bytes(case)
     assert got == kv + 2 * 2 * 32 * 128 * 2 + 2 * 256 * 4 + 2 * 4
+
+
+def test_prefill_flops_closed_form_matches_brute_force():
+    """The prefill FLOP count behind the TFLOP/s figures: QK^T and PV over each
+    query's causal range (query j of a chunk of n over c tokens sees c - n + j + 1
+    tokens), 2 flops per multiply-add, counted query by query."""
+    rng = np.random.default_rng(5)
+    for _ in range(20):
+        b = int(rng.integers(1, 5))
+        ctx = rng.integers(1, 300, size=b)
+        chunk = [int(rng.integers(1, c + 1)) for c in ctx]
+        hq, d = int(rng.choice([4, 32])), int(rng.choice([64, 128]))
+        brute = 0
+        for c, n in zip(ctx, chunk):
+            for j in range(n):
+                seen = int(c) - n + j + 1
+                brute += 2 * 2 * seen * d * hq          # QK^T and PV, 2 flops per multiply-add
+        assert W.prefill_flops(ctx, chunk, hq, d) == brute
+    # the benchmark's workload: 8 chunks of 512 over 4096-token contexts, 32 heads, D 128
+    w, n = W.prefill_workload()
+    assert W.prefill_flops([4096] * 8, [n] * 8, w.num_q_heads, w.head_dim) == 257_731_592_192
