@@ -27,10 +27,13 @@
  *  R1  pool layout per KV tensor [num_blocks, num_kv_heads, block_size, row].
  *  R2  GQA: query head h reads KV head h / (Hq / Hkv).
  *  R3  the page loop runs over ceil(ctx / bs) blocks; tokens >= ctx masked.
- *  R4  FP8 scale per (block, kv-head), separately for K and V; the token
- *      written at offset 0 of a block sets it from its own amax; later
- *      tokens reuse it and saturate at +-448.  Within one call the offset-0
- *      tokens are applied first.
+ *  R4  FP8 scale per (block, kv-head), separately for K and V.  A call
+ *      that writes the token at offset 0 of a block opens that block: its
+ *      scale is max(amax / 448, 1e-12) with amax over every token that the
+ *      same call writes into the block ("Block-Wise Scaling Factors",
+ *      snippet-4: one scale from the absolute maximum of the block).  Tokens
+ *      that a later call appends to the block reuse that scale and saturate
+ *      at +-448 (the tokens to come are not known when the block opens).
  *  R5  FP8 code = E4M3 round-to-nearest-even with saturation to +-448 of
  *      the fp32 quotient x / scale (one IEEE fp32 division).
  *  R6  INT4: per (token, kv-head, 32 consecutive d), asymmetric:
@@ -370,23 +373,27 @@ int oracle_copy_blocks(void* k_cache, void* v_cache, void* scales, int kv_dtype,
 }
 
 
-/* Encode one token row of one head (R4-R6).  x: the row as fp32 values. */
+/* largest finite code value of a one-byte format: E4M3 448 (snippet-4),
+ * E5M2 57344 (R8), INT8 127 (R9) */
+static float blk8_max(int kv_dtype) {
+    return kv_dtype == DT_FP8 ? 448.0f : kv_dtype == DT_E5M2 ? 57344.0f : 127.0f;
+}
+
+/* max |x_d| of one row in fp32; a NaN element is passed over */
+static float row_amax(const float* x, int head_dim) {
+    float amax = 0.0f;
+    for (int d = 0; d < head_dim; ++d) {
+        float a = fabsf(x[d]);
+        if (a > amax) amax = a;
+    }
+    return amax;
+}
+
+/* Encode one token row of one head (R4-R6).  x: the row as fp32 values;
+ * one-byte formats use the block's scale, already set (*fp8_scale). */
 static void encode_row(const float* x, int head_dim, int kv_dtype, uint8_t* dst,
-                       int fresh_fp8_block, float* fp8_scale, uint16_t* int4_pairs) {
+                       const float* fp8_scale, uint16_t* int4_pairs) {
     if (is_blk8(kv_dtype)) {
-        const float fmax = kv_dtype == DT_FP8 ? 448.0f
-                           : kv_dtype == DT_E5M2 ? 57344.0f : 127.0f;         /* R8, R9 */
-        if (fresh_fp8_block) {
-            /* snippet-4: scale = max|x| / 448, clamped below at 1e-12, in fp32 */
-            float amax = 0.0f;
-            for (int d = 0; d < head_dim; ++d) {
-                float a = fabsf(x[d]);
-                if (a > amax) amax = a;
-            }
-            float s = amax / fmax;
-            if (s < 1e-12f) s = 1e-12f;
-            *fp8_scale = s;
-        }
         float s = *fp8_scale;
         for (int d = 0; d < head_dim; ++d) {
             if (kv_dtype == DT_INT8)
@@ -433,6 +440,19 @@ static void encode_row(const float* x, int head_dim, int kv_dtype, uint8_t* dst,
     }
 }
 
+static void row_to_f32(const uint16_t* srow, int new_dtype, int head_dim, float* x) {
+    for (int d = 0; d < head_dim; ++d) x[d] = (float)half_word_to_double(srow[d], new_dtype);
+}
+
+/* The quantize-on-write of one call (R4-R9), in four plain steps:
+ *  1. the blocks this call opens: those whose offset-0 slot it writes;
+ *  2. for each opened block, KV head and K/V: amax over every token of the
+ *     call that lands in the block (snippet-4's block-wide absolute max);
+ *  3. the opened blocks' scales: max(amax / max_finite, 1e-12) in fp32;
+ *  4. every token row encoded with its block's scale (set in step 3, or by
+ *     an earlier call).
+ * Steps 1-3 concern the one-byte formats only.  Slots of -1 (and any slot
+ * outside the pool) are skipped. */
 int oracle_kv_write(const uint16_t* k_new, const uint16_t* v_new, int new_dtype,
                     const int64_t* slot_mapping, int64_t num_tokens,
                     void* k_cache, void* v_cache, void* scales, int kv_dtype,
@@ -444,40 +464,77 @@ int oracle_kv_write(const uint16_t* k_new, const uint16_t* v_new, int new_dtype,
     int64_t rb = row_bytes(kv_dtype, head_dim);
     float* x = (float*)malloc(sizeof(float) * head_dim);
     if (!x) return -2;
-    /* pass 0: offset-0 tokens (they set FP8 scales); pass 1: the rest (R4) */
-    for (int pass = 0; pass < 2; ++pass) {
-        for (int64_t i = 0; i < num_tokens; ++i) {
+
+    if (is_blk8(kv_dtype)) {
+        int64_t nscale = 2 * (int64_t)num_blocks * num_kv_heads;
+        uint8_t* opened = (uint8_t*)calloc((size_t)num_blocks, 1);
+        float* amax = (float*)calloc((size_t)nscale, sizeof(float));
+        if (!opened || !amax) {
+            free(opened);
+            free(amax);
+            free(x);
+            return -2;
+        }
+        for (int64_t i = 0; i < num_tokens; ++i) {                       /* step 1 */
             int64_t slot = slot_mapping[i];
-            if (slot < 0 || slot >= nslots) continue;            /* -1: skip (R7) */
+            if (slot >= 0 && slot < nslots && slot % block_size == 0)
+                opened[slot / block_size] = 1;
+        }
+        for (int64_t i = 0; i < num_tokens; ++i) {                       /* step 2 */
+            int64_t slot = slot_mapping[i];
+            if (slot < 0 || slot >= nslots || !opened[slot / block_size]) continue;
             int32_t block = (int32_t)(slot / block_size);
-            int offset = (int)(slot % block_size);
-            int first = offset == 0;
-            if (is_blk8(kv_dtype) && first != (pass == 0)) continue;
-            if (!is_blk8(kv_dtype) && pass == 1) continue;
-            for (int which = 0; which < 2; ++which) {
-                const uint16_t* src = which ? v_new : k_new;
-                uint8_t* cache = (uint8_t*)(which ? v_cache : k_cache);
+            for (int which = 0; which < 2; ++which)
                 for (int h = 0; h < num_kv_heads; ++h) {
-                    const uint16_t* srow = src + (i * num_kv_heads + h) * (int64_t)head_dim;
-                    uint8_t* dst = cache + row_index(block, h, offset, num_kv_heads,
-                                                     block_size) * rb;
-                    if (kv_dtype == DT_F16 || kv_dtype == DT_BF16) {
-                        memcpy(dst, srow, (size_t)rb);
-                        continue;
-                    }
-                    for (int d = 0; d < head_dim; ++d)
-                        x[d] = (float)half_word_to_double(srow[d], new_dtype);
-                    float* s8 = is_blk8(kv_dtype)
-                                    ? fp8_scale_ptr(scales, which, block, h, num_blocks,
-                                                    num_kv_heads)
-                                    : NULL;
-                    uint16_t* p4 = kv_dtype == DT_INT4
-                                       ? int4_pair_ptr(scales, which, block, h, offset, 0,
-                                                       num_blocks, num_kv_heads, block_size,
-                                                       head_dim)
-                                       : NULL;
-                    encode_row(x, head_dim, kv_dtype, dst, first, s8, p4);
+                    const uint16_t* src = which ? v_new : k_new;
+                    row_to_f32(src + (i * num_kv_heads + h) * (int64_t)head_dim, new_dtype,
+                               head_dim, x);
+                    float a = row_amax(x, head_dim);
+                    float* m = &amax[((int64_t)which * num_blocks + block) * num_kv_heads + h];
+                    if (a > *m) *m = a;
                 }
+        }
+        for (int32_t b = 0; b < num_blocks; ++b) {                       /* step 3 */
+            if (!opened[b]) continue;
+            for (int which = 0; which < 2; ++which)
+                for (int h = 0; h < num_kv_heads; ++h) {
+                    float s = amax[((int64_t)which * num_blocks + b) * num_kv_heads + h] /
+                              blk8_max(kv_dtype);
+                    if (s < 1e-12f) s = 1e-12f;
+                    *fp8_scale_ptr(scales, which, b, h, num_blocks, num_kv_heads) = s;
+                }
+        }
+        free(opened);
+        free(amax);
+    }
+
+    for (int64_t i = 0; i < num_tokens; ++i) {                           /* step 4 */
+        int64_t slot = slot_mapping[i];
+        if (slot < 0 || slot >= nslots) continue;                        /* -1: skip (R7) */
+        int32_t block = (int32_t)(slot / block_size);
+        int offset = (int)(slot % block_size);
+        for (int which = 0; which < 2; ++which) {
+            const uint16_t* src = which ? v_new : k_new;
+            uint8_t* cache = (uint8_t*)(which ? v_cache : k_cache);
+            for (int h = 0; h < num_kv_heads; ++h) {
+                const uint16_t* srow = src + (i * num_kv_heads + h) * (int64_t)head_dim;
+                uint8_t* dst = cache + row_index(block, h, offset, num_kv_heads,
+                                                 block_size) * rb;
+                if (kv_dtype == DT_F16 || kv_dtype == DT_BF16) {
+                    memcpy(dst, srow, (size_t)rb);
+                    continue;
+                }
+                row_to_f32(srow, new_dtype, head_dim, x);
+                const float* s8 = is_blk8(kv_dtype)
+                                      ? fp8_scale_ptr(scales, which, block, h, num_blocks,
+                                                      num_kv_heads)
+                                      : NULL;
+                uint16_t* p4 = kv_dtype == DT_INT4
+                                   ? int4_pair_ptr(scales, which, block, h, offset, 0,
+                                                   num_blocks, num_kv_heads, block_size,
+                                                   head_dim)
+                                   : NULL;
+                encode_row(x, head_dim, kv_dtype, dst, s8, p4);
             }
         }
     }

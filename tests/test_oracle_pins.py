@@ -278,10 +278,17 @@ def test_write_int8_scale_is_amax_over_127():
     # dequantized within half a step of the input
     deq = codes.astype(np.float64) * float(s[0, 1, 0])
     assert np.all(np.abs(deq - xr) <= 0.5 * float(s[0, 1, 0]) * (1 + 1e-6))
-    # a later, larger token saturates at +-127 under the frozen scale
+    # one call writing both tokens: the block's scale comes from both (amax 3 * 7.25)
     k2, _, s2, _ = _one_block_write(W.INT8, np.stack([row, row * 3]), [0, 1])
+    assert s2[0, 1, 0] == np.float32(np.float32(21.75) / np.float32(127.0))
+    assert k2[1, 0, 1].view(np.int8)[9] == -127
+    # a larger token that a later call appends saturates at +-127 under the kept scale
+    nb, bs = 3, 16
+    x3 = W.to_bits((row * 3)[None, None, :], W.BF16)
+    oracle.kv_write(x3, x3, W.BF16, np.array([1 * bs + 1]), k, v, s, W.INT8, nb, 1, 64, bs)
+    assert s[0, 1, 0] == np.float32(np.float32(7.25) / np.float32(127.0))
     big = np.abs(row * 3) > 7.25 * 1.01
-    assert np.all(np.abs(k2[1, 0, 1].view(np.int8)[big]) == 127)
+    assert np.all(np.abs(k[1, 0, 1].view(np.int8)[big]) == 127)
 
 
 # ------------------------------------------------------------------ the write
@@ -345,21 +352,93 @@ def test_write_fp8_zero_row_uses_eps_scale():
     assert not k[1, 0, 0].any()
 
 
-def test_write_fp8_scale_frozen_after_offset_zero_and_order_independent():
+def test_write_fp8_block_scale_is_the_amax_of_every_token_the_call_writes():
+    """"Block-Wise Scaling Factors" (snippet-4): one scale per block from the absolute
+    maximum over the whole block.  A 16-token block written in one call with a x20
+    outlier at offset 9: scale = |outlier| / 448, the outlier takes the largest code
+    with its sign, and no other code saturates."""
+    f = FACTS["fp8_scale_rule"]
+    rng = np.random.default_rng(21)
+    rows = rng.standard_normal((16, 64)).astype(np.float32)
+    rows[9, 40] = -20.0 * 1.375                       # the block's largest magnitude
+    k, v, s, x = _one_block_write(W.FP8_E4M3, rows, list(range(16)))
+    xr = W.bits_to_f32(x[:, 0], W.BF16)
+    assert s[0, 1, 0] == np.float32(np.float32(27.5) / np.float32(f["fp8_max"]))
+    assert s[1, 1, 0] == s[0, 1, 0]
+    assert k[1, 0, 9, 40] == 0xFE
+    mag = k[1, 0] & 0x7F
+    assert (mag == 0x7E).sum() == 1 and not (mag == 0x7F).any()
+    # every code within half an E4M3 step of x / scale (nothing clipped)
+    deq = np.vectorize(oracle.e4m3_to_double)(k[1, 0]) * float(s[0, 1, 0])
+    step = np.maximum(np.abs(xr) * 2.0**-4, 2.0**-10 * float(s[0, 1, 0]))
+    assert np.all(np.abs(deq - xr) <= step + 1e-12)
+    # the order of the tokens within the call does not matter
+    kb, _, sb, _ = _one_block_write(W.FP8_E4M3, rows[::-1].copy(), list(range(15, -1, -1)))
+    assert np.array_equal(k, kb) and np.array_equal(s, sb)
+
+
+def test_write_fp8_whole_block_equals_snippet4_through_torch():
+    """snippet-4 run by torch on one block (fp32 tensor, one KV head): scale =
+    clamp(max|x| / 448, 1e-12), codes = (x / scale).to(float8_e4m3fn).  The
+    oracle's one-call write of the same 16 tokens gives the same scale and bytes."""
+    rng = np.random.default_rng(22)
+    rows = (rng.standard_normal((16, 128)) * 5.0).astype(np.float32)
+    rows[rng.random((16, 128)) < 0.01] *= 20.0
+    k, v, s, x = _one_block_write(W.FP8_E4M3, rows, list(range(16)), head_dim=128)
+    blk = torch.from_numpy(W.bits_to_f32(x[:, 0], W.BF16).astype(np.float32))
+    scale = (torch.max(torch.abs(blk)) / 448.0).clamp(min=1e-12)
+    codes = (blk / scale).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert s[0, 1, 0] == np.float32(scale.item())
+    assert np.array_equal(k[1, 0], codes)
+
+
+def test_write_fp8_scale_kept_for_tokens_a_later_call_appends():
+    """A block opened by one call keeps its scale; a later call's tokens (no
+    offset-0 token among them) reuse it and saturate at +-448."""
     rng = np.random.default_rng(5)
-    r0 = rng.standard_normal(64).astype(np.float32)
-    r1 = (r0 * 50).astype(np.float32)          # far larger: must saturate
-    ka, _, sa, _ = _one_block_write(W.FP8_E4M3, np.stack([r0, r1]), [0, 1])
-    kb, _, sb, _ = _one_block_write(W.FP8_E4M3, np.stack([r1, r0]), [1, 0])
-    assert np.array_equal(ka, kb) and np.array_equal(sa, sb)
-    big = np.abs(r1) >= np.abs(r0).max() * 1.01
-    assert np.all((ka[1, 0, 1][big] & 0x7F) == 0x7E)
-    # a later single write at offset 3 keeps the block's scale
+    r0 = rng.standard_normal((4, 64)).astype(np.float32)
+    k, v, s, x = _one_block_write(W.FP8_E4M3, r0, [0, 1, 2, 3])
+    s_open = s.copy()
+    amax = np.abs(W.bits_to_f32(x[:, 0], W.BF16)).max()
+    assert s[0, 1, 0] == np.float32(np.float32(amax) / np.float32(448.0))
     nb, bs = 3, 16
-    x = W.to_bits(r0[None, None, :] * 0.5, W.BF16)
-    oracle.kv_write(x, x, W.BF16, np.array([1 * bs + 3]), ka, ka.copy(), sa, W.FP8_E4M3, nb, 1,
-                    64, bs)
-    assert np.array_equal(sa, sb)
+    big = (r0[0] * 50).astype(np.float32)
+    xb = W.to_bits(np.stack([big, r0[1] * 0.5])[:, None, :], W.BF16)
+    oracle.kv_write(xb, xb, W.BF16, np.array([1 * bs + 4, 1 * bs + 5]), k, v, s, W.FP8_E4M3,
+                    nb, 1, 64, bs)
+    assert np.array_equal(s, s_open)
+    sat = np.abs(W.bits_to_f32(xb[0, 0], W.BF16)) >= amax * 1.04
+    assert sat.any() and np.all((k[1, 0, 4][sat] & 0x7F) == 0x7E)
+    # a call that writes offset 0 again opens the block afresh from its own tokens
+    oracle.kv_write(xb[1:], xb[1:], W.BF16, np.array([1 * bs]), k, v, s, W.FP8_E4M3, nb, 1, 64,
+                    bs)
+    a2 = np.abs(W.bits_to_f32(xb[1, 0], W.BF16)).max()
+    assert s[0, 1, 0] == np.float32(np.float32(a2) / np.float32(448.0))
+
+
+def test_write_fp8_scales_are_per_block_and_per_head():
+    """Two blocks and two KV heads written in one call: each (block, head) scale is
+    the amax of that head's rows in that block only; K and V are scaled apart."""
+    rng = np.random.default_rng(23)
+    nb, bs, hkv, d = 4, 16, 2, 64
+    kx = rng.standard_normal((20, hkv, d)).astype(np.float32)
+    vx = (rng.standard_normal((20, hkv, d)) * 0.1).astype(np.float32)
+    kx[3, 1, 7] = 40.0                                   # block 2, head 1
+    kx[17, 0, 2] = -33.0                                 # block 0, head 0
+    slots = np.array([2 * bs + i for i in range(16)] + [0, 1, 2, 3], np.int64)
+    k, v, s = oracle.alloc_cache(W.FP8_E4M3, nb, hkv, d, bs)
+    kb, vb = W.to_bits(kx, W.BF16), W.to_bits(vx, W.BF16)
+    oracle.kv_write(kb, vb, W.BF16, slots, k, v, s, W.FP8_E4M3, nb, hkv, d, bs)
+    kf, vf = W.bits_to_f32(kb, W.BF16), W.bits_to_f32(vb, W.BF16)
+    for which, arr in ((0, kf), (1, vf)):
+        for blk, sel in ((2, slice(0, 16)), (0, slice(16, 20))):
+            for h in range(hkv):
+                want = max(np.float32(np.abs(arr[sel, h]).max()) / np.float32(448.0),
+                           np.float32(1e-12))
+                assert s[which, blk, h] == np.float32(want), (which, blk, h)
+    assert s[0, 2, 1] == np.float32(np.float32(40.0) / np.float32(448.0))
+    assert s[0, 0, 0] == np.float32(np.float32(33.0) / np.float32(448.0))
+    assert not s[:, 1].any() and not s[:, 3].any()       # untouched blocks
 
 
 def test_write_int4_round_trip_bound_and_extremes():
