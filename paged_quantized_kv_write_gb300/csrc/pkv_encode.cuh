@@ -8,7 +8,8 @@
 // of "Reducing LLM Inference Latency ... PagedAttention in vLLM"; INT4
 // group-wise from section 4 of "Optimizing KV-Cache Memory Footprint"):
 //  FP8  scale = max(amax / max_finite, 1e-12) (fp32; max_finite 448 for E4M3,
-//       57344 for E5M2), set by the token at block offset 0;
+//       57344 for E5M2), amax over every token that the call opening the
+//       block (writing its offset-0 slot) writes into it; later calls keep it;
 //       code = cvt.rn.satfinite.{e4m3,e5m2}(x / scale), IEEE fp32 division.
 //  INT8 the same block-wise rule with 127: code = clamp(rint(x / scale),
 //       -127, 127), round half to even, two's complement byte.
@@ -22,9 +23,52 @@
 
 namespace pkv {
 
+// Where a one-byte format's block scale comes from when a row is encoded.
+enum ScaleSource {
+  // The call writes one token into the block (the fused decode write): the
+  // token at offset 0 opens the block with its own amax; others read the
+  // stored scale.
+  kScaleOwnRow = 0,
+  // The write kernel's encode pass: the block's scale word holds either a
+  // kept scale (sign bit clear) or, for a block this call opened, the open
+  // mark 0x80000000 | bits(amax) of every row the call writes into it.  The
+  // offset-0 token stores the finished scale; a row that meets the mark
+  // finishes it the same way, so the order of the two does not matter.
+  kScaleFromWord = 1,
+};
+
+constexpr uint32_t kOpenMark = 0x80000000u;
+
+// max(amax / max_finite, 1e-12) in fp32, the block-wise rule of snippet-4.
+template <int KV>
+__device__ __forceinline__ float block_scale_from_amax(float amax) {
+  return fmaxf(__fdiv_rn(amax, KV == PKV_INT8 ? 127.f : fp8_max<KV>()), 1e-12f);
+}
+
+// max |x| over the token's row for this head (a warp, EPL values per lane);
+// NaN elements are passed over (fmaxf), as a plain max search does.
+template <int NEW, int D>
+__device__ __forceinline__ float row_amax(const uint16_t* __restrict__ src, int lane) {
+  constexpr int EPL = D / kWarp;
+  float amax = 0.f;
+  if constexpr (EPL == 4) {
+    const uint2 w = *reinterpret_cast<const uint2*>(src + lane * EPL);
+    amax = fmaxf(fmaxf(fabsf(Half16<NEW>::to_float(w.x & 0xFFFF)),
+                       fabsf(Half16<NEW>::to_float(w.x >> 16))),
+                 fmaxf(fabsf(Half16<NEW>::to_float(w.y & 0xFFFF)),
+                       fabsf(Half16<NEW>::to_float(w.y >> 16))));
+  } else {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(src + lane * EPL);
+    amax = fmaxf(fabsf(Half16<NEW>::to_float(w & 0xFFFF)), fabsf(Half16<NEW>::to_float(w >> 16)));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  return amax;
+}
+
 // k_src / v_src: the token's rows for this head (D values of dtype NEW).
 // block, offset: where the token goes; cache_row = (block * Hkv + head) * bs + offset.
-template <int KV, int NEW, int D>
+template <int KV, int NEW, int D, int SRC = kScaleOwnRow>
 __device__ __forceinline__ void encode_token_head(const uint16_t* __restrict__ k_src,
                                                   const uint16_t* __restrict__ v_src,
                                                   uint8_t* __restrict__ k_cache,
@@ -62,13 +106,20 @@ __device__ __forceinline__ void encode_token_head(const uint16_t* __restrict__ k
       float* sp = reinterpret_cast<float*>(scales) +
                   (static_cast<int64_t>(which) * num_blocks + block) * num_kv_heads + head;
       float s;
-      if (offset == 0) {
+      if constexpr (SRC == kScaleFromWord) {
+        uint32_t word = 0;
+        if (lane == 0) word = __ldcg(reinterpret_cast<const unsigned int*>(sp));
+        word = __shfl_sync(0xffffffffu, word, 0);
+        s = (word & kOpenMark) ? block_scale_from_amax<KV>(__uint_as_float(word & ~kOpenMark))
+                               : __uint_as_float(word);
+        if (offset == 0 && lane == 0) *sp = s;
+      } else if (offset == 0) {
         float amax = 0.f;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(x[e]));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        s = fmaxf(__fdiv_rn(amax, KV == PKV_INT8 ? 127.f : fp8_max<KV>()), 1e-12f);
+        s = block_scale_from_amax<KV>(amax);
         if (lane == 0) *sp = s;
       } else {
         s = *sp;

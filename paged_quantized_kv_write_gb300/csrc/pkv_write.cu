@@ -2,8 +2,24 @@
 // the way in.
 //
 // One warp owns one (token, KV head) and handles K then V (the encoder and
-// the encodings are in pkv_encode.cuh).  FP8 runs as two launches: tokens at
-// block offset 0 first (they set the block scales), then the rest.
+// the encodings are in pkv_encode.cuh).
+//
+// One-byte formats (FP8 E4M3/E5M2, INT8) take one scale per (block, KV head)
+// from the absolute maximum of the block ("Block-Wise Scaling Factors",
+// snippet-4).  A call that writes a block's offset-0 slot opens the block,
+// and its scale is taken over every token that call writes into it.  That
+// needs the whole call's rows before any code is written, so the write runs
+// as three launches over the caller's scale array, which doubles as the
+// accumulator:
+//   open   offset-0 tokens: atomicMax(word, 0x80000000 | bits(row amax)).
+//          Any kept scale is a positive float, below every mark as an
+//          unsigned word, so the mark replaces it.
+//   grow   other tokens: if their block's word carries the mark,
+//          atomicMax(word, mark | bits(row amax)); blocks with a kept scale
+//          (sign clear) are left alone.
+//   encode every token: the scale is the word, or max(amax / max_finite,
+//          1e-12) of a marked word; the offset-0 token stores it.
+// Stored scales are never negative, so the sign bit is free for the mark.
 #include "pkv_common.cuh"
 #include "pkv_encode.cuh"
 #include "pkv_internal.h"
@@ -13,7 +29,8 @@ namespace {
 
 constexpr int kWriteWarps = 8;   // warps (token-head rows) per CTA
 
-// PHASE 0: only tokens at block offset 0; 1: only the others; 2: all tokens.
+enum WritePhase { kOpen = 0, kGrow = 1, kEncode = 2 };
+
 template <int KV, int NEW, int D, int PHASE>
 __global__ void __launch_bounds__(kWriteWarps * kWarp)
 kv_write_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
@@ -30,20 +47,36 @@ kv_write_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict__
   const int head = static_cast<int>(row - tok * num_kv_heads);
   const int64_t slot = slot_mapping[tok];
   if (slot < 0) {
-    if (slot != -1 && lane == 0 && head == 0 && PHASE != 1) flag_status(dev_status, PKV_ERR_DEVICE_BOUNDS);
+    if (slot != -1 && lane == 0 && head == 0 && PHASE == kEncode)
+      flag_status(dev_status, PKV_ERR_DEVICE_BOUNDS);
     return;
   }
   const int64_t nslots = static_cast<int64_t>(num_blocks) * block_size;
   if (slot >= nslots) {
-    if (lane == 0 && head == 0 && PHASE != 1) flag_status(dev_status, PKV_ERR_DEVICE_BOUNDS);
+    if (lane == 0 && head == 0 && PHASE == kEncode) flag_status(dev_status, PKV_ERR_DEVICE_BOUNDS);
     return;
   }
   const int64_t block = slot / block_size;
   const int offset = static_cast<int>(slot - block * block_size);
-  if (PHASE == 0 && offset != 0) return;
-  if (PHASE == 1 && offset == 0) return;
-  encode_token_head<KV, NEW, D>(k_new + row * D, v_new + row * D, k_cache, v_cache, scales,
-                                num_blocks, num_kv_heads, block_size, block, head, offset, lane);
+  if constexpr (PHASE == kEncode) {
+    encode_token_head<KV, NEW, D, is_blk8(KV) ? kScaleFromWord : kScaleOwnRow>(
+        k_new + row * D, v_new + row * D, k_cache, v_cache, scales, num_blocks, num_kv_heads,
+        block_size, block, head, offset, lane);
+  } else {
+    if ((PHASE == kOpen) != (offset == 0)) return;
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      unsigned int* word = reinterpret_cast<unsigned int*>(scales) +
+                           (static_cast<int64_t>(which) * num_blocks + block) * num_kv_heads + head;
+      if constexpr (PHASE == kGrow) {
+        uint32_t w = 0;
+        if (lane == 0) w = __ldcg(word);
+        if (!(__shfl_sync(0xffffffffu, w, 0) & kOpenMark)) continue;   // a kept scale
+      }
+      const float amax = row_amax<NEW, D>((which ? v_new : k_new) + row * D, lane);
+      if (lane == 0) atomicMax(word, kOpenMark | __float_as_uint(amax));
+    }
+  }
 }
 
 template <int KV, int NEW, int D, int PHASE>
@@ -60,12 +93,14 @@ cudaError_t launch_one(const WriteArgs& a, cudaStream_t st) {
 template <int KV, int NEW, int D>
 cudaError_t launch_kv(const WriteArgs& a, cudaStream_t st) {
   if constexpr (is_blk8(KV)) {
-    // offset-0 tokens set the block scales; the rest read them afterwards
-    cudaError_t e = launch_one<KV, NEW, D, 0>(a, st);
+    // open the blocks whose offset-0 slot this call writes, grow their amax
+    // over the call's other rows, then encode with the finished scales
+    cudaError_t e = launch_one<KV, NEW, D, kOpen>(a, st);
+    if (e == cudaSuccess) e = launch_one<KV, NEW, D, kGrow>(a, st);
     if (e != cudaSuccess) return e;
-    return launch_one<KV, NEW, D, 1>(a, st);
+    return launch_one<KV, NEW, D, kEncode>(a, st);
   } else {
-    return launch_one<KV, NEW, D, 2>(a, st);
+    return launch_one<KV, NEW, D, kEncode>(a, st);
   }
 }
 

@@ -90,6 +90,51 @@ def test_fp8_offset_zero_tokens_apply_first_in_one_call(kv):
         assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("kv", W.BLK8_TYPES)
+def test_block_scale_over_the_opening_call_then_kept(kv):
+    """The context written in two calls, split at a point inside blocks: the first
+    call opens blocks (scale = amax over its rows in them, "Block-Wise Scaling
+    Factors"), the second appends to those partial blocks (kept scale, saturating)
+    and opens new ones, in one launch set.  Bit-exact to the oracle after each call,
+    with x20 outliers so that appended rows do saturate."""
+    pkv = _pkv()
+    w = W.Workload("two calls", 5, 8, 2, 128, 16, kv, W.BF16, "uniform", 20, 260,
+                   outlier_prob=0.02, outlier_scale=20.0, seed=91 + kv)
+    case = W.make_case(w)
+    k, v, s = oracle.alloc_cache(kv, case.num_blocks, w.num_kv_heads, w.head_dim, w.block_size)
+    kd, vd, sd = pkv.alloc_cache(kv, case.num_blocks, w.num_kv_heads, w.head_dim, w.block_size)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # sequence b's prefill rows are its positions 0 .. ctx_b - 2, in order; the first
+    # call takes positions below a random cut of each sequence, the second the rest,
+    # each call in a shuffled token order
+    rng = np.random.default_rng(7)
+    first, second, base = [], [], 0
+    for c in case.context_lens:
+        n = int(c) - 1
+        cut = int(rng.integers(0, n + 1))
+        first += range(base, base + cut)
+        second += range(base + cut, base + n)
+        base += n
+    for part in (rng.permutation(np.array(first, np.int64)),
+                 rng.permutation(np.array(second, np.int64))):
+        slots = np.ascontiguousarray(case.prefill_slots[part])
+        kx = np.ascontiguousarray(case.prefill_k[part])
+        vx = np.ascontiguousarray(case.prefill_v[part])
+        oracle.kv_write(kx, vx, w.q_dtype, slots, k, v, s, kv, case.num_blocks,
+                        w.num_kv_heads, w.head_dim, w.block_size)
+        _gpu_write(case, kd, vd, sd, slots, kx, vx, status)
+        torch.cuda.synchronize()
+        _assert_same(case, (k, v, s), (kd, vd, sd))
+    assert status.item() == 0
+    # more codes at the format's largest value than opened (block, head) scales: the
+    # appended rows did saturate, so the case tests the kept scale
+    def n_top(c):
+        if kv == W.INT8:
+            return int((np.abs(c.view(np.int8).astype(np.int32)) == 127).sum())
+        return int(((c & 0x7F) == (0x7E if kv == W.FP8_E4M3 else 0x7B)).sum())
+    assert n_top(k) + n_top(v) > int((s > 0).sum())
+
+
 def test_write_skips_minus_one_and_flags_out_of_range():
     pkv = _pkv()
     w = W.Workload("bounds", 2, 4, 2, 64, 16, W.INT4_G32, W.BF16, "fixed", 20, 20, seed=5)
