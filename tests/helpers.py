@@ -17,6 +17,13 @@ TOL = {W.F16: 2e-3, W.BF16: 2e-3, W.FP8_E4M3: 5e-3, W.INT4_G32: 5e-3, W.FP8_E5M2
        W.INT8: 5e-3}
 
 
+def library_for(decode_mode: str):
+    """The library build a decode mode runs in: the comparators ("simt", "tc") are in
+    the test build only; everything else runs the product library."""
+    import paged_quantized_kv_write_gb300 as pkv
+    return pkv.library("test" if decode_mode in ("simt", "tc") else "product")
+
+
 def torch_dtype(code: int):
     return torch.float16 if code == W.F16 else torch.bfloat16
 
@@ -56,12 +63,27 @@ def cache_to_host(kt, vt, st, kv_dtype: int):
     return raw(kt), raw(vt), raw(st)
 
 
-def half_ulp(x: np.ndarray, code: int) -> np.ndarray:
-    """Half a unit in the last place of |x| in the output dtype (the final rounding)."""
-    mant = 10 if code == W.F16 else 7
-    a = np.maximum(np.abs(x), 2.0 ** -14 if code == W.F16 else 2.0 ** -126)
-    e = np.floor(np.log2(a))
-    return 2.0 ** (e - mant - 1)
+def _ulp(x: np.ndarray, code: int) -> np.ndarray:
+    """Spacing of the 16-bit output dtype in the binade of |x| (subnormal spacing
+    below the smallest normal)."""
+    mant, emin = (10, -14) if code == W.F16 else (7, -126)
+    a = np.abs(x)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.where(a > 0, np.maximum(e, emin), emin)
+    return 2.0 ** (e - mant)
+
+
+def round_down(x: np.ndarray, code: int) -> np.ndarray:
+    """x rounded toward -inf to the 16-bit output dtype (as fp64).  Multiples of the
+    binade's spacing, and the binade's ends, are all representable."""
+    u = _ulp(x, code)
+    return np.floor(x / u) * u
+
+
+def round_up(x: np.ndarray, code: int) -> np.ndarray:
+    """x rounded toward +inf to the 16-bit output dtype (as fp64)."""
+    u = _ulp(x, code)
+    return np.ceil(x / u) * u
 
 
 def round_to(x: np.ndarray, code: int) -> np.ndarray:
@@ -72,22 +94,41 @@ def round_to(x: np.ndarray, code: int) -> np.ndarray:
 
 
 def check_close(gpu: np.ndarray, ref: np.ndarray, kv_dtype: int, out_dtype: int, what=""):
-    """Assert |gpu - oracle| <= tol + half an ulp of the output dtype at |oracle|.
+    """Assert that each output is within the tolerance of the oracle before its
+    final rounding: gpu in [round_down(oracle - tol), round_up(oracle + tol)], both
+    ends rounded in the output dtype (tol: 2e-3 for 16-bit KV, 5e-3 for FP8/INT4).
+    A result computed within tol of the oracle lands there whatever its magnitude,
+    and nothing farther does.
 
     Returns (max |gpu - oracle|, max |gpu - oracle rounded to the output dtype|,
-    max error / bound)."""
-    err = np.abs(gpu - ref)
-    bound = TOL[kv_dtype] + half_ulp(ref, out_dtype)
-    bad = err > bound
+    the share of tol the worst output needs: the smallest t / tol for which
+    gpu lies in [round_down(oracle - t), round_up(oracle + t)], <= 1)."""
+    tol = TOL[kv_dtype]
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    lo = round_down(ref - tol, out_dtype)
+    hi = round_up(ref + tol, out_dtype)
+    bad = ~((gpu >= lo) & (gpu <= hi))
     if bad.any():
-        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        over = np.where(gpu > hi, gpu - hi, np.where(gpu < lo, lo - gpu, 0.0))
+        over = np.where(np.isnan(gpu), np.inf, over)
+        i = np.unravel_index(np.argmax(over), over.shape)
         raise AssertionError(
-            f"{what}: {int(bad.sum())} of {err.size} outputs exceed tolerance; worst at {i}: "
-            f"gpu {gpu[i]!r} oracle {ref[i]!r} err {err[i]:.3g} bound {bound[i]:.3g}")
-    if not err.size:
+            f"{what}: {int(bad.sum())} of {gpu.size} outputs outside the tolerance; worst at "
+            f"{i}: gpu {gpu[i]!r} oracle {ref[i]!r} err {abs(gpu[i] - ref[i]):.3g} allowed "
+            f"[{lo[i]!r}, {hi[i]!r}]")
+    if not gpu.size:
         return 0.0, 0.0, 0.0
+    err = np.abs(gpu - ref)
+    # an output above the oracle needs t past the representable value just below it
+    # (below the oracle: past the one just above it); one equal to the oracle's own
+    # rounding needs nothing
+    below = round_down(np.nextafter(gpu, -np.inf), out_dtype)
+    above = round_up(np.nextafter(gpu, np.inf), out_dtype)
+    need = np.where(gpu > ref, np.maximum(0.0, below - ref),
+                    np.where(gpu < ref, np.maximum(0.0, ref - above), 0.0))
     err_r = np.abs(gpu - round_to(ref, out_dtype))
-    return float(err.max()), float(err_r.max()), float((err / bound).max())
+    return float(err.max()), float(err_r.max()), float(need.max() / tol)
 
 
 class GpuCase:
