@@ -78,12 +78,22 @@ typedef enum {
  *                [0, num_blocks * block_size) is skipped and flagged in dev_status.
  * k_cache, v_cache, scales   the pool, layouts above, updated in place.
  * kv_dtype       F16/BF16: a plain copy (new_dtype must equal kv_dtype).
- *                FP8_E4M3: the token written at offset 0 of a block sets that
- *                block's K and V scales per KV head to max(amax / 448, 1e-12)
- *                in fp32 (snippet-4's block-wise rule); a token at any other
- *                offset reuses the stored scales.  code = E4M3 round-to-nearest-
- *                even with saturation to +-448 of the fp32 quotient x / scale.
- *                Within one call the offset-0 tokens are applied first.
+ *                FP8_E4M3: one scale per block, KV head and K/V from the
+ *                block's absolute maximum ("Block-Wise Scaling Factors",
+ *                snippet-4 of the mohashari page).  A call that writes the
+ *                slot at offset 0 of a block opens the block: its scales
+ *                become max(amax / 448, 1e-12) in fp32, amax taken over every
+ *                token this call writes into the block (a whole prefilled
+ *                block is scaled by its own maximum).  A call that writes
+ *                into a block without its offset-0 slot reuses the stored
+ *                scales, and values beyond them saturate (the tokens still to
+ *                come are unknown when a block opens).  code = E4M3 round-to-
+ *                nearest-even with saturation to +-448 of the fp32 quotient
+ *                x / scale.  The result does not depend on the order of the
+ *                tokens within the call.  Stored scales must be non-negative
+ *                (zeroed, or written by this library): the write uses the
+ *                sign bit of an opened block's scale as a mark while it runs,
+ *                as three launches (open, grow the maximum, encode).
  *                FP8_E5M2: the same with 57344 (the largest finite E5M2) in
  *                place of 448, codes rounded to nearest even and saturated.
  *                INT8: the same block-wise rule with 127: scale =
@@ -260,9 +270,10 @@ int paged_prefill_attention(const void* q, int q_dtype, const int32_t* q_start,
  * Arguments, layouts and results are those of paged_decode_attention, minus
  * workspace/workspace_bytes.  Requests whose scratch
  * (paged_decode_workspace_bytes(...)) exceeds 64 MiB return
- * PKV_ERR_WORKSPACE before anything is launched.  The first call on each
- * device looks up the array's address (cudaGetSymbolAddress) with that
- * device current; make that first call before any stream capture.  Every
+ * PKV_ERR_WORKSPACE before anything is launched.  Each call looks up the
+ * array's address (cudaGetSymbolAddress) in the current device's context;
+ * the first call on a device also loads the library's module there, so make
+ * that first call before any stream capture.  Every
  * call shares the one array, so calls that overlap on the GPU (other
  * streams, other host threads) race on it: serialize them.
  */
@@ -282,7 +293,8 @@ int paged_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads,
                                 int max_blocks_per_seq, int block_size, int partition_size);
 
 /* Workspace bytes paged_decode_attention needs for these arguments (0 when
- * every sequence fits one partition). */
+ * every sequence fits one partition, and 0 for arguments the calls reject,
+ * e.g. more than 2^40 split-KV partial rows). */
 size_t paged_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
                                     int head_dim, int max_blocks_per_seq, int block_size,
                                     int partition_size);

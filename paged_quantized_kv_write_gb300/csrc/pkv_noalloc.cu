@@ -19,13 +19,15 @@
 // calls that overlap on the GPU — on different streams, or from different
 // host threads — race on it and may return wrong results.  Serialize them.
 //
-// Set-up: the first call on each device looks up the array's device address
-// with cudaGetSymbolAddress, with that device current, and caches it.  Make
-// that first call before any stream capture.
+// Set-up: every call looks up the array's device address with
+// cudaGetSymbolAddress, with the caller's device current.  The address is
+// not cached: after cudaDeviceReset, or when a context is destroyed and
+// created again, the library's module is loaded anew and the array can sit
+// at another address, so a cached pointer could point at freed memory.  The
+// first call on a device loads the module there (CUDA loads modules lazily);
+// make that first call before any stream capture.
 #include <cuda_runtime.h>
 #include <stdint.h>
-
-#include <mutex>
 
 #include "pagedkv.h"
 #include "pkv_internal.h"
@@ -39,25 +41,13 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[PKV_NOALLOC_SCR
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = PKV_NOALLOC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
-std::mutex g_lock;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (looked up once).
+// Device address of the scratch array in the current device's context.
 cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> guard(g_lock);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return cudaSuccess;
 }
 
