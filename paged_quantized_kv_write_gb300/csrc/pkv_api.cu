@@ -18,6 +18,20 @@ bool ok_half_dtype(int t) { return t == PKV_F16 || t == PKV_BF16; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Split-KV partial results are (sequence, q head, partition) rows of
+// head_dim + 2 floats.  Bounding their count at 2^40 keeps every byte count
+// derived from it far inside int64 and size_t (at most 2^27 partitions of
+// 2^31 rows each, so the product itself cannot overflow).
+bool workspace_fits(int num_seqs, int num_q_heads, int num_kv_heads, int max_blocks_per_seq,
+                    int block_size, int partition_size) {
+  const int part = pkv::resolve_partition_size(num_seqs, num_q_heads, num_kv_heads,
+                                               max_blocks_per_seq, block_size, partition_size);
+  if (part <= 0) return false;
+  const int64_t np = ceil_div(static_cast<int64_t>(max_blocks_per_seq) * block_size, part);
+  const int64_t heads = static_cast<int64_t>(num_seqs) * num_q_heads;
+  return heads <= 0x7FFFFFFF && np <= 0x7FFFFFFF && heads * np <= (int64_t(1) << 40);
+}
+
 // paged_decode_attention, and its fused-write form when slot_mapping is set
 int decode_impl(const void* q, int q_dtype, const void* k_new, const void* v_new,
                 const int64_t* slot_mapping, const void* k_cache, const void* v_cache,
@@ -36,10 +50,15 @@ int decode_impl(const void* q, int q_dtype, const void* k_new, const void* v_new
   if (!ok_head_dim(head_dim) || !ok_block_size(block_size)) return PKV_ERR_UNSUPPORTED;
   if (num_q_heads / num_kv_heads > 8) return PKV_ERR_UNSUPPORTED;
   if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+  // the merge runs one CTA per (sequence, q head) on a 1-D grid
+  if (static_cast<int64_t>(num_seqs) * num_q_heads > 0x7FFFFFFF) return PKV_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(max_blocks_per_seq) * block_size > 0x7FFFFFFF) return PKV_ERR_UNSUPPORTED;
   // the kernel locates a 16-token sub-tile as (block * Hkv + head) << 4 | offset / 16
   if (static_cast<int64_t>(num_blocks) * num_kv_heads >= (int64_t(1) << 27)) return PKV_ERR_UNSUPPORTED;
   if (!(softmax_scale == softmax_scale)) return PKV_ERR_INVALID_ARG;
+  if (!workspace_fits(num_seqs, num_q_heads, num_kv_heads, max_blocks_per_seq, block_size,
+                      partition_size))
+    return PKV_ERR_UNSUPPORTED;
   if (num_seqs == 0) return PKV_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
     return PKV_ERR_INVALID_ARG;
@@ -100,7 +119,10 @@ int paged_kv_write(const void* k_new, const void* v_new, int new_dtype,
       (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) || (quant && !aligned16(scales)))
     return PKV_ERR_INVALID_ARG;
   if (static_cast<int64_t>(num_blocks) * block_size > (int64_t(1) << 40)) return PKV_ERR_INVALID_ARG;
-  if (ceil_div(num_tokens * num_kv_heads, 8) > 0x7FFFFFFF) return PKV_ERR_UNSUPPORTED;
+  // one warp per (token, KV head), eight per CTA, on a 1-D grid (num_tokens is
+  // bounded first so that the product cannot overflow)
+  if (num_tokens > (int64_t(1) << 34) || ceil_div(num_tokens * num_kv_heads, 8) > 0x7FFFFFFF)
+    return PKV_ERR_UNSUPPORTED;
   pkv::WriteArgs a{k_new, v_new, new_dtype, slot_mapping, num_tokens, k_cache, v_cache,
                    scales, kv_dtype, num_blocks, num_kv_heads, head_dim, block_size, dev_status};
   cudaError_t e = pkv::launch_kv_write(a, static_cast<cudaStream_t>(stream));
@@ -144,7 +166,11 @@ size_t paged_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_he
                                     int partition_size) {
   const int part = paged_decode_partition_size(num_seqs, num_q_heads, num_kv_heads,
                                                max_blocks_per_seq, block_size, partition_size);
-  if (part <= 0 || !ok_head_dim(head_dim)) return 0;
+  if (part <= 0 || !ok_head_dim(head_dim) || num_seqs > 65535 || num_q_heads > 65535 * 8 ||
+      static_cast<int64_t>(max_blocks_per_seq) * block_size > 0x7FFFFFFF ||
+      !workspace_fits(num_seqs, num_q_heads, num_kv_heads, max_blocks_per_seq, block_size,
+                      partition_size))
+    return 0;   // arguments the calls reject
   const int64_t np = ceil_div(static_cast<int64_t>(max_blocks_per_seq) * block_size, part);
   if (np <= 1) return 0;
   const int64_t heads = static_cast<int64_t>(num_seqs) * num_q_heads;

@@ -36,6 +36,25 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(dll, name), name
 
 
+def test_product_library_holds_no_comparators(lib):
+    """The decode comparators (CUDA-core and tcgen05) and the bounded-wait test switch
+    are compiled into the test build only; both builds export the same C ABI."""
+    import subprocess
+    test_path = os.path.join(os.path.dirname(lib.LIB_PATH), "libpagedkv_test.so")
+    test_dll = ctypes.CDLL(test_path)
+    for name in _declared():
+        assert hasattr(test_dll, name), name
+
+    def symbols(path):
+        r = subprocess.run(["nm", "-C", path], capture_output=True, text=True, check=True)
+        return r.stdout
+
+    prod, test = symbols(lib.LIB_PATH), symbols(test_path)
+    for marker in ("simt_decode_kernel", "decode_tc_kernel", "launch_simt", "launch_decode_tc"):
+        assert marker not in prod, marker
+        assert marker in test, marker
+
+
 def test_version_and_status_strings(lib):
     assert lib.version() == 100
     assert lib.lib.paged_kv_status_string(0) == b"ok"
@@ -82,6 +101,19 @@ def test_host_validation_without_gpu(lib):
     # split-KV without workspace
     assert L.paged_decode_attention(fake, 1, fake, fake, fake, 400, fake, 2, None, 1, 10, fake,
                                     0.1, 8, 2, 128, 16, 64, None, 0, None, None) == 5
+    # more (sequence, q head) pairs than a 1-D grid holds: 65535 x 65535*8 heads
+    assert L.paged_decode_attention(fake, 1, fake, fake, fake, 4, fake, 65535, None, 1, 10,
+                                    fake, 0.1, 8 * 65535, 65535, 128, 16, 0, None, 0, None,
+                                    None) == 2
+    # split-KV partial rows beyond 2^40 (65535 seqs x 32768 heads x 2^24 partitions of 16):
+    # refused up front, and the size query answers 0 rather than a wrapped count
+    assert L.paged_decode_attention(fake, 1, fake, fake, fake, (1 << 31) // 16 - 1, fake, 65535,
+                                    None, 1, 10, fake, 0.1, 32768, 4096, 128, 16, 16, None, 0,
+                                    None, None) == 2
+    assert lib.paged_decode_workspace_bytes(65535, 32768, 4096, 128, (1 << 31) // 16 - 1, 16,
+                                            16) == 0
+    # a partition request near INT_MAX is clamped, not wrapped
+    assert lib.paged_decode_partition_size(4, 8, 2, 8, 16, 0x7FFFFFFF) > 0
     # bad block size, bad dtype, NULL buffers on the write
     assert L.paged_kv_write(fake, fake, 1, fake, 4, fake, fake, None, 1, 10, 2, 128, 24,
                             None, None) == 2
@@ -91,6 +123,9 @@ def test_host_validation_without_gpu(lib):
                             None, None) == 1
     assert L.paged_kv_write(fake, fake, 1, fake, 4, fake, fake, None, 3, 10, 2, 128, 16,
                             None, None) == 1
+    # a token count whose warp count would overflow the grid
+    assert L.paged_kv_write(fake, fake, 1, fake, 1 << 40, fake, fake, None, 1, 10, 2, 128, 16,
+                            None, None) == 2
     # zero tokens / zero sequences are no-ops
     assert L.paged_kv_write(None, None, 1, None, 0, None, None, None, 1, 10, 2, 128, 16,
                             None, None) == 0
