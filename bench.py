@@ -129,7 +129,8 @@ def _with_kv_dtype(w: W.Workload, name: str) -> W.Workload:
 
 
 def _kernel_launches_per_step(w: W.Workload, nparts: int, fused: bool = False) -> int:
-    write = 0 if fused else (2 if w.kv_dtype in W.BLK8_TYPES else 1)
+    # paged_kv_write: one launch, three for one-byte caches (open, grow, encode)
+    write = 0 if fused else (3 if w.kv_dtype in W.BLK8_TYPES else 1)
     return write + 1 + (1 if nparts > 1 else 0)
 
 
@@ -413,6 +414,148 @@ def run_ours(args, rank: int, world: int):
     return result
 
 
+def measure_workload(cfg: int, reps: int, dev, flush, peak: float):
+    """One workload's decode step on this GPU, in the library's launch configuration:
+    CUDA-graph replays of the fused step (write + attention) and of the attention
+    alone, each timed with the L2 flushed before every replay (a 256 MB write,
+    outside the events) and warm (back to back, no flush).  The context is
+    prefilled through paged_kv_write with K/V drawn on the device (the workload's
+    distribution; host draws of a full-size context take longer than all of the
+    timing).  Returns the figures as a dict."""
+    import torch
+    import paged_quantized_kv_write_gb300 as pkv
+
+    w = W.CONFIGS[cfg]
+    case = W.make_case(w, prefill_values=False)
+    stream = torch.cuda.Stream(dev)
+    n = len(case.prefill_slots)
+    with torch.cuda.stream(stream):
+        k, v, s = pkv.alloc_cache(w.kv_dtype, case.num_blocks, w.num_kv_heads, w.head_dim,
+                                  w.block_size, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        if n:
+            kp = W.draw_kv_device(w, n, w.seed * 2 + 1, dev)
+            vp = W.draw_kv_device(w, n, w.seed * 2 + 2, dev)
+            pkv.paged_kv_write(kp, vp, torch.from_numpy(case.prefill_slots).to(dev), k, v, s,
+                               w.kv_dtype, w.block_size, w.head_dim, status, stream)
+            del kp, vp
+        q = _bits_to_tensor(case.q, w.q_dtype)
+        kn = _bits_to_tensor(case.k_new, w.q_dtype)
+        vn = _bits_to_tensor(case.v_new, w.q_dtype)
+        slots = torch.from_numpy(case.new_slots).to(dev)
+        tables = torch.from_numpy(case.block_tables).to(dev)
+        ctx = torch.from_numpy(case.context_lens).to(dev)
+        out = torch.empty_like(q)
+        mb = case.max_blocks_per_seq
+        part = pkv.paged_decode_partition_size(w.batch, w.num_q_heads, w.num_kv_heads, mb,
+                                               w.block_size, w.partition_size)
+        ws = pkv.make_workspace(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, mb,
+                                w.block_size, w.partition_size, device=dev)
+    torch.cuda.synchronize()
+
+    def attend(st):
+        pkv.paged_decode_attention(q, k, v, tables, ctx, s, out, w.softmax_scale,
+                                   w.num_kv_heads, w.kv_dtype, w.block_size, w.partition_size,
+                                   ws, status, st)
+
+    def fused(st):
+        pkv.paged_decode_attention_with_write(q, kn, vn, slots, k, v, tables, ctx, s, out,
+                                              w.softmax_scale, w.kv_dtype, w.block_size,
+                                              w.partition_size, ws, status, st)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            fused(stream)
+    torch.cuda.synchronize()
+    graphs = {}
+    for name, fn in (("step", fused), ("attn", attend)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn(stream)
+        graphs[name] = g
+    torch.cuda.synchronize()
+
+    def evict():
+        # read (not write) 256 MB, twice L2, so that L2 holds only clean lines
+        # of another buffer and no write-back competes with the timed launch
+        torch.sum(flush, dtype=torch.int32)
+
+    def time_graph(g, flushed):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                if flushed:
+                    evict()
+                g.replay()
+            for a, b in ev:
+                if flushed:
+                    evict()
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3     # us
+
+    t = {(name, fl): time_graph(graphs[name], fl) for name in graphs for fl in (True, False)}
+    assert status.item() == 0, f"config {cfg}: a kernel flagged an out-of-range id"
+    attn_u = W.attention_bytes(case, unique=True)
+    attn_l = W.attention_bytes(case, unique=False)
+    step_u = W.algorithmic_bytes(case, unique=True)
+    # the headline's rule: back-to-back replays when the step's inputs exceed L2
+    # several times over (they evict themselves), cold L2 otherwise
+    big = step_u >= 4 * L2_BYTES
+    main = ("attn", not big)
+    res = {
+        "workload": w.name,
+        "kv_dtype": W.DTYPE_NAMES[w.kv_dtype],
+        "batch": w.batch,
+        "partition_size": part,
+        "decode_us": round(t[main], 2),
+        "decode_gbs": round(attn_u / t[main] / 1e3, 1),
+        "frac": round(attn_u / t[main] / 1e3 / peak, 4),
+        "timed_as": "back-to-back (inputs > 4x L2)" if big else "L2 evicted before each replay",
+        "decode_us_flushed": round(t[("attn", True)], 2),
+        "decode_us_warm": round(t[("attn", False)], 2),
+        "frac_flushed": round(attn_u / t[("attn", True)] / 1e3 / peak, 4),
+        "frac_warm": round(attn_u / t[("attn", False)] / 1e3 / peak, 4),
+        "step_us": round(t[("step", not big)], 2),
+        "step_us_flushed": round(t[("step", True)], 2),
+        "step_us_warm": round(t[("step", False)], 2),
+        "seq_steps_per_s": round(w.batch / t[("step", not big)] * 1e6, 1),
+        "algorithmic_bytes": attn_u,
+        "traffic": _traffic(cfg),
+    }
+    if attn_l != attn_u:
+        # shared-prefix blocks: counted once (unique) or once per sequence (logical)
+        res["logical_bytes"] = attn_l
+        res["decode_gbs_logical"] = round(attn_l / t[main] / 1e3, 1)
+    del graphs, k, v, s, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_per_config(args, dev):
+    """Every workload's decode figures on this GPU (configs 1-5), with the clocks
+    sampled over the whole sweep."""
+    import torch
+    peak, _ = _peaks()
+    flush = torch.ones(256 * 2**20, dtype=torch.uint8, device=dev)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    res = {}
+    for cfg in sorted(W.CONFIGS):
+        res[str(cfg)] = measure_workload(cfg, args.per_config_reps, dev, flush, peak)
+    res["clocks"] = clocks.stop()
+    res["timing"] = (f"median of {args.per_config_reps} CUDA-graph replays per figure; "
+                     "'decode' = the attention call alone, 'step' = the fused write + "
+                     "attention; flushed = a 256 MB read before each replay (outside the "
+                     "events) evicts L2, warm = back-to-back replays; decode_us/frac use "
+                     "the headline's rule (warm when the inputs exceed 4x L2)")
+    return res
+
+
 def run_copy(args, rank: int, world: int):
     """Copy-on-write block copies: time paged_kv_copy_blocks moving --copy-pairs
     random (src, dst) blocks of the workload's pool per step (K, V and scales)."""
@@ -593,7 +736,7 @@ def _traffic(config: int):
 def _kernel_sha() -> str:
     import hashlib
     h = hashlib.sha256()
-    for name in ("pkv_attn.cuh", "pkv_decode.cu", "pkv_common.cuh"):
+    for name in ("pkv_attn.cuh", "pkv_decode.cu", "pkv_decode_launch.cuh", "pkv_common.cuh"):
         with open(os.path.join(ROOT, "paged_quantized_kv_write_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -733,6 +876,8 @@ def main():
                     help="--op copy: block pairs copied per step")
     ap.add_argument("--partition", type=int, default=0,
                     help="override the workload's split-KV partition size (0: keep)")
+    ap.add_argument("--per-config-reps", type=int, default=100,
+                    help="replays per figure in the per-workload sweep (0: skip the sweep)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -758,6 +903,12 @@ def main():
             dist.destroy_process_group()
         return
     res = run_ours(args, rank, world)
+    plain = not (args.identity or args.block_size or args.kv_dtype or args.unfused or
+                 args.partition)
+    if args.per_config_reps > 0 and plain:
+        import torch
+        res["per_config"] = run_per_config(
+            args, torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))))
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
             res["cpu_baseline"] = cpu_baseline(args.config)

@@ -162,13 +162,13 @@ int paged_kv_copy_blocks(void* k_cache, void* v_cache, void* scales, int kv_dtyp
  * Work split: the library picks between CTAs whose warps share a partition
  * (merging their states) and warps that each own a (partition, KV head)
  * unit; the environment variable PKV_DECODE_MODE=shared|warp, read on each
- * call, forces one (for testing; results agree to rounding).
- * PKV_DECODE_MODE=simt runs a CUDA-core comparator of the same computation
- * instead (16-bit, FP8 and INT8 caches; kept to measure what the tensor
- * cores buy, never chosen by the library itself).  PKV_DECODE_MODE=tc runs
- * another comparator on the tcgen05 tensor cores with tensor-memory
- * accumulators (FP8 and INT8 caches with head_dim 128; slower than the
- * default kernel, also never chosen by the library).
+ * call, forces one (for testing; results agree to rounding).  The test
+ * build of the library (libpagedkv_test.so, used by the tests only) also
+ * takes PKV_DECODE_MODE=simt, a CUDA-core comparator of the same computation
+ * (16-bit, FP8 and INT8 caches; kept to measure what the tensor cores buy),
+ * and PKV_DECODE_MODE=tc, a comparator on the tcgen05 tensor cores with
+ * tensor-memory accumulators (FP8 and INT8 caches with head_dim 128; slower
+ * than the default kernel).  The product library holds neither.
  * Supported: head_dim in {64, 128}; num_q_heads / num_kv_heads <= 8;
  * block_size a multiple of 16 up to 256; F16/BF16 caches need q_dtype equal
  * to kv_dtype; FP8/INT4 caches take F16 or BF16 q; num_blocks * num_kv_heads

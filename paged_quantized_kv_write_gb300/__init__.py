@@ -19,6 +19,7 @@ Calls (same names as the C ABI):
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from typing import Optional
@@ -31,14 +32,17 @@ PKV_F16, PKV_BF16, PKV_FP8_E4M3, PKV_INT4_G32, PKV_FP8_E5M2, PKV_INT8 = 0, 1, 2,
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libpagedkv.so")
+# the test build: the same library plus the decode comparators and the switch
+# that exercises the bounded waits (see build.py); only the tests load it
+TEST_LIB_PATH = os.path.join(_HERE, "_lib", "libpagedkv_test.so")
 
 
-def _load() -> ctypes.CDLL:
-    if not os.path.exists(LIB_PATH):
+def _load(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
         raise ImportError(
-            f"libpagedkv.so not found at {LIB_PATH}; build it with "
+            f"{os.path.basename(path)} not found at {path}; build it with "
             "`python paged_quantized_kv_write_gb300/build.py` (needs nvcc)")
-    lib = ctypes.CDLL(LIB_PATH)
+    lib = ctypes.CDLL(path)
     P, I, I64, F, SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
                         ctypes.c_size_t)
     lib.paged_kv_write.argtypes = [P, P, I, P, I64, P, P, P, I, I, I, I, I, P, P]
@@ -66,6 +70,25 @@ def _load() -> ctypes.CDLL:
 
 
 _lib = _load()
+_loaded = {"product": _lib}
+
+
+@contextlib.contextmanager
+def library(kind: str):
+    """Route the calls of this module through the product library ("product")
+    or the test build ("test") inside a with-block; both share torch's device
+    memory and streams."""
+    global _lib
+    if kind not in _loaded:
+        if kind != "test":
+            raise ValueError(f"unknown library {kind!r}")
+        _loaded[kind] = _load(TEST_LIB_PATH)
+    prev = _lib
+    _lib = _loaded[kind]
+    try:
+        yield _lib
+    finally:
+        _lib = prev
 
 
 class PagedKVError(RuntimeError):

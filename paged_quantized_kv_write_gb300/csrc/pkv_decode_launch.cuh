@@ -1,0 +1,226 @@
+// Launch side of the decode kernel (pkv_attn.cuh) and the log-sum-exp merge
+// of split-KV partitions: launch configuration, work split and partitions per
+// CTA.  Included by one translation unit per cache-dtype family
+// (pkv_decode_half.cu, pkv_decode_byte.cu, pkv_decode_int4.cu) so they
+// compile in parallel; pkv_decode.cu dispatches between them.
+#pragma once
+
+#include "pkv_attn.cuh"
+
+namespace pkv {
+namespace {
+
+// Merge the partitions of one (sequence, q head): M = max m_p,
+// L = sum l_p 2^(m_p - M), out = sum l_p 2^(m_p - M) O_p / L.
+//
+// One CTA per (sequence, q head) with W warps.  Lane l of every warp keeps
+// head_dim values [EPT l, EPT l + EPT) of the sum.  The partitions are taken
+// in blocks of 32: lane j computes the weight of partition 32k + j of its
+// warp's block k, the warp then walks the block with eight independent
+// 16-byte (8-byte at head_dim 64) loads in flight per lane, each weight
+// handed out by a shuffle; the W warps' sums meet in shared memory.
+template <int QT, int D, int W>
+__global__ void __launch_bounds__(32 * W)
+pkv_lse_reduce(const Params p) {
+  constexpr int EPT = D / kWarp;                   // 4 (D = 128) or 2 (D = 64)
+  __shared__ float s_acc[W][D];
+  __shared__ float s_l[W];
+  pdl_wait();                                      // the partials of the decode kernel
+  const int64_t head = blockIdx.x;                 // b * Hq + h
+  const int b = static_cast<int>(head / p.num_q_heads);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ctx = min(p.context_lens[b], p.max_blocks_per_seq * p.block_size);
+  const int np = max(1, (ctx + p.partition_size - 1) / p.partition_size);
+  const float* ml = p.ws_ml + head * p.num_partitions * 2;
+  const float* o = p.ws_out + head * p.num_partitions * D + EPT * lane;
+  float M = -INFINITY;
+  for (int i = lane; i < np; i += kWarp) M = fmaxf(M, __ldcg(ml + 2 * i));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float acc[EPT];
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) acc[e] = 0.f;
+  float L = 0.f;
+  if (M != -INFINITY) {
+    for (int base = warp * kWarp; base < np; base += W * kWarp) {
+      const int i = base + lane;
+      float wgt = 0.f;
+      if (i < np) {
+        const float m = __ldcg(ml + 2 * i);
+        wgt = m == -INFINITY ? 0.f : __ldcg(ml + 2 * i + 1) * exp2f(m - M);
+      }
+      L += wgt;
+      const int n = min(kWarp, np - base);
+      for (int j = 0; j < n; j += 8) {
+        float v[8][EPT];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float* src = o + static_cast<int64_t>(base + j + u) * D;
+          if (j + u < n) {
+            if constexpr (EPT == 4) {
+              const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
+              v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+            } else {
+              const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+              v[u][0] = x.x; v[u][1] = x.y;
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float wj = __shfl_sync(0xffffffffu, wgt, (j + u) & 31);
+          if (j + u < n) {
+#pragma unroll
+            for (int e = 0; e < EPT; ++e) acc[e] = fmaf(wj, v[u][e], acc[e]);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  if constexpr (W > 1) {
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) s_acc[warp][EPT * lane + e] = acc[e];
+    if (lane == 0) s_l[warp] = L;
+    __syncthreads();
+    if (warp != 0) return;
+#pragma unroll
+    for (int w = 1; w < W; ++w) {
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) acc[e] += s_acc[w][EPT * lane + e];
+      L += s_l[w];
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  uint16_t* outp = static_cast<uint16_t*>(p.out) + head * D + EPT * lane;
+  if constexpr (EPT == 4) {
+    *reinterpret_cast<uint2*>(outp) = make_uint2(Half16<QT>::pack_rn(acc[0] * inv, acc[1] * inv),
+                                                 Half16<QT>::pack_rn(acc[2] * inv, acc[3] * inv));
+  } else {
+    *reinterpret_cast<uint32_t*>(outp) = Half16<QT>::pack_rn(acc[0] * inv, acc[1] * inv);
+  }
+}
+
+// the merge for a call's partition count: warps per (sequence, q head)
+template <int QT, int D>
+cudaError_t launch_lse_typed(const Params& p, int num_heads, cudaStream_t st) {
+  const dim3 grid(static_cast<unsigned>(num_heads));
+  if (p.num_partitions <= 32) return launch_pdl(pkv_lse_reduce<QT, D, 1>, grid, dim3(32), 0, st, p);
+  if (p.num_partitions <= 64) return launch_pdl(pkv_lse_reduce<QT, D, 2>, grid, dim3(64), 0, st, p);
+  return launch_pdl(pkv_lse_reduce<QT, D, 4>, grid, dim3(128), 0, st, p);
+}
+
+template <int KV, int QT, int D, bool WU>
+cudaError_t launch_mode(const DecodeArgs& a, cudaStream_t st) {
+  using G = Geo<KV, D>;
+  Params p;
+  p.q = static_cast<const uint16_t*>(a.q);
+  // the caches are written only by the fused write (a.slot_mapping set), which
+  // the C ABI allows only for caller-writable buffers
+  p.k_cache = static_cast<uint8_t*>(const_cast<void*>(a.k_cache));
+  p.v_cache = static_cast<uint8_t*>(const_cast<void*>(a.v_cache));
+  p.block_tables = a.block_tables;
+  p.context_lens = a.context_lens;
+  p.scales = const_cast<void*>(a.scales);
+  p.k_new = static_cast<const uint16_t*>(a.k_new);
+  p.v_new = static_cast<const uint16_t*>(a.v_new);
+  p.slot_mapping = a.slot_mapping;
+  p.out = a.out;
+  p.ws_out = a.ws_out;
+  p.ws_ml = a.ws_ml;
+  p.dev_status = a.dev_status;
+  p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.num_seqs = a.num_seqs;
+  p.num_blocks = a.num_blocks;
+  p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.block_size = a.block_size;
+  p.partition_size = a.partition_size;
+  p.num_partitions = a.num_partitions;
+  p.softmax_scale = a.softmax_scale;
+  p.q_start = nullptr;
+  p.max_query_len = 0;
+  auto kern = paged_decode_kernel<KV, QT, D, WU>;
+  // per device, once: the shared-memory opt-in and the resident CTAs per SM
+  static std::atomic<int> slots_per_dev[kMaxDevices];     // SMs x resident CTAs (0: unknown)
+  p.parts_per_cta = 1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int slots = slots_per_dev[dev].load(std::memory_order_relaxed);
+  if (slots == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    int occ = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kDecodeWarps * kWarp,
+                                                      G::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    slots = max(1, occ) * max(1, sms);
+    slots_per_dev[dev].store(slots, std::memory_order_relaxed);
+  }
+  // partitions per CTA (per warp with WU): runs of up to PKV_RUN_TOKENS tokens
+  // per warp stream, as long as the grid keeps at least four waves of CTAs
+  const int heads_per_cta = WU ? kDecodeWarps : 1;
+  const int64_t head_groups = (a.num_kv_heads + heads_per_cta - 1) / heads_per_cta;
+  int ppc = PKV_PPC;
+  if (ppc <= 0) {
+    ppc = 1;
+    const int64_t groups = static_cast<int64_t>(a.num_seqs) * head_groups;
+    const int run = WU ? PKV_RUN_TOKENS_WU : PKV_RUN_TOKENS;
+    while (ppc * 2 * a.partition_size <= run && ppc * 2 <= a.num_partitions &&
+           ((a.num_partitions + ppc * 2 - 1) / (ppc * 2)) * groups >= 4 * static_cast<int64_t>(slots))
+      ppc *= 2;
+  }
+  ppc = std::max(1, std::min(ppc, a.num_partitions));
+  p.parts_per_cta = ppc;
+  dim3 grid((a.num_partitions + ppc - 1) / ppc, static_cast<unsigned>(head_groups), a.num_seqs);
+  e = launch_pdl(kern, grid, dim3(kDecodeWarps * kWarp), G::kSmemBytes, st, p);
+  if (e != cudaSuccess || a.num_partitions == 1) return e;
+  return launch_lse_typed<QT, D>(p, a.num_seqs * a.num_q_heads, st);
+}
+
+// Warp-owned units when the split-KV work has enough (partition, sequence, KV
+// head) units for several waves of warps (PKV_WU_WAVES x SMs x 16 warps);
+// shared partitions otherwise.
+template <int KV, int QT, int D>
+cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t st) {
+  static std::atomic<int> sms_per_dev[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int sms = sms_per_dev[dev].load(std::memory_order_relaxed);
+  if (sms == 0) {
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    sms_per_dev[dev].store(sms, std::memory_order_relaxed);
+  }
+  const int64_t units = static_cast<int64_t>(a.num_partitions) * a.num_seqs * a.num_kv_heads;
+  bool wu = a.num_partitions > 1 && units >= static_cast<int64_t>(PKV_WU_WAVES) * sms * 16;
+  // PKV_DECODE_MODE=shared|warp overrides the choice (both give the same
+  // results).  The test build also takes =simt, the CUDA-core comparator
+  // (16-bit, FP8 and INT8 caches without the fused write; other calls keep
+  // the tensor path), and =tc, the tcgen05 comparator for one-byte caches.
+  if (const char* m = getenv("PKV_DECODE_MODE")) {
+    if (!strcmp(m, "shared")) wu = false;
+    if (!strcmp(m, "warp")) wu = true;
+#ifdef PKV_TEST_HOOKS
+    if (!strcmp(m, "simt") && KV != PKV_INT4_G32 && a.slot_mapping == nullptr)
+      return launch_simt(a, st);
+    if (!strcmp(m, "tc") && decode_tc_supported(a)) return launch_decode_tc(a, st);
+#endif
+  }
+  return wu ? launch_mode<KV, QT, D, true>(a, st) : launch_mode<KV, QT, D, false>(a, st);
+}
+
+template <int KV, int QT>
+cudaError_t launch_d(const DecodeArgs& a, cudaStream_t st) {
+  return a.head_dim == 64 ? launch_typed<KV, QT, 64>(a, st) : launch_typed<KV, QT, 128>(a, st);
+}
+
+}  // namespace
+}  // namespace pkv

@@ -4,7 +4,8 @@
 // dequantized tiles feed the tensor cores from shared memory, and the
 // softmax runs with one thread per token.  It computes what
 // paged_decode_kernel (the mma.sync kernel) computes and is kept as a
-// comparator (PKV_DECODE_MODE=tc), never chosen by the library: on GB300 it
+// comparator (PKV_DECODE_MODE=tc) in the test build (libpagedkv_test.so,
+// compiled with PKV_TEST_HOOKS) only, never chosen by the library: on GB300 it
 // runs about 2.7x slower, because each CTA works through one serial chain
 // per tile (row lookup, code loads, conversion, S, softmax vote, P V) and
 // only three such chains fit on an SM, against twelve independent copy rings

@@ -95,12 +95,19 @@ cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t st);
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t st);
 cudaError_t launch_lse_reduce(const DecodeArgs& a, cudaStream_t st);
 bool prefill_tc_supported(const PrefillArgs& a);
-// decode on the tcgen05 tensor cores (one-byte caches, head_dim 128, G <= 8)
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st);
+#ifdef PKV_TEST_HOOKS
+// comparators, built into the test library only: decode on the tcgen05 tensor
+// cores (one-byte caches, head_dim 128, G <= 8) and on the CUDA cores
 bool decode_tc_supported(const DecodeArgs& a);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);
-cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st);
 cudaError_t launch_simt(const DecodeArgs& a, cudaStream_t st);
+#endif
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
+// the decode launchers per cache-dtype family (one translation unit each)
+cudaError_t launch_decode_half(const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_decode_byte(const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_decode_int4(const DecodeArgs& a, cudaStream_t st);
 
 int resolve_partition_size(int num_seqs, int num_q_heads, int num_kv_heads,
                            int max_blocks_per_seq, int block_size, int requested);

@@ -87,7 +87,9 @@ struct TcParams {
   const int32_t* q_start;
   const float* scales;        // one-byte caches: fp32 [2][num_blocks][num_kv_heads]
   int max_query_len;          // queries j >= max_query_len of a chunk are not computed
+#ifdef PKV_TEST_HOOKS
   int test_drop_commit;       // test of the bounded waits: the first S batch is not committed
+#endif
   void* out;
   int* dev_status;
   int max_blocks_per_seq;
@@ -237,9 +239,14 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
       for (int kk = 0; kk < D / 16; ++kk)
         umma(tmem_s, umma_desc(sb + PL::kOffQ + kk * 256, 128, (D / 8) * 128),
              umma_desc(sb + PL::kOffK + kk * 256, 128, (D / 8) * 128), kIdescS, kk > 0);
-      // (a test of the bounded waits leaves the first batch uncommitted: the
-      // wait below then runs out and the launch reports PKV_ERR_DEVICE_TIMEOUT)
+#ifdef PKV_TEST_HOOKS
+      // (the test build's check of the bounded waits leaves the first batch
+      // uncommitted: the wait below then runs out and the launch reports
+      // PKV_ERR_DEVICE_TIMEOUT)
       if (!(p.test_drop_commit && t == 0)) umma_commit(bar_s);
+#else
+      umma_commit(bar_s);
+#endif
     }
     ++s_commits;
     if (!mbar_wait(bar_s, t & 1)) {
@@ -828,7 +835,9 @@ cudaError_t launch_tc(Kern kern, int smem_bytes, const PrefillArgs& a, cudaStrea
   p.block_size = a.block_size;
   p.softmax_scale = a.softmax_scale;
   p.max_query_len = a.max_query_len;
+#ifdef PKV_TEST_HOOKS
   p.test_drop_commit = getenv("PKV_TEST_DROP_COMMIT") != nullptr;
+#endif
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,

@@ -4,7 +4,8 @@
 // Cache Compression & Paged Attention", Implementation Details: per token,
 // dot products of q with the gathered K row, softmax, weighted sum of V).
 // It exists to measure what the tensor-core formulation buys; the library
-// never picks it by itself.
+// never picks it by itself, and only the test build (libpagedkv_test.so,
+// compiled with PKV_TEST_HOOKS) contains it.
 //
 // One warp owns one (sequence, KV head, partition) unit, like the tensor
 // kernel's warp-owned mode: lane l holds elements [EPL*l, EPL*l + EPL) of q

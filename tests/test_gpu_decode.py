@@ -21,9 +21,11 @@ def mode(request, monkeypatch):
     """Run a test under both work splits of the decode kernel, under the SIMT
     comparator (which takes 16-bit, FP8 and INT8 caches; INT4 stays on the
     tensor path), and under the tcgen05 kernel (one-byte caches with head_dim
-    128; other calls keep the mma.sync kernel)."""
+    128; other calls keep the mma.sync kernel).  The comparators live in the
+    test build of the library only."""
     monkeypatch.setenv("PKV_DECODE_MODE", request.param)
-    return request.param
+    with H.library_for(request.param):
+        yield request.param
 
 
 def _run(w, partition_size=0, identity=False, max_blocks_per_seq=None):

@@ -17,7 +17,8 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(params=["shared", "warp", "tc"])
 def mode(request, monkeypatch):
     monkeypatch.setenv("PKV_DECODE_MODE", request.param)
-    return request.param
+    with H.library_for(request.param):
+        yield request.param
 
 
 def _pkv():

@@ -47,6 +47,11 @@ def test_fuzz_decode(seed, monkeypatch):
         monkeypatch.setenv("PKV_DECODE_MODE", mode)
     else:
         monkeypatch.delenv("PKV_DECODE_MODE", raising=False)
+    with H.library_for(mode):                   # the comparators are in the test build
+        _fuzz_decode_case(pkv, seed, w, partition, mode, fused)
+
+
+def _fuzz_decode_case(pkv, seed, w, partition, mode, fused):
     case = W.make_case(w)
     k, v, s = oracle.prefill_case(case)
     g = H.GpuCase(case, k, v, s, partition)

@@ -246,8 +246,13 @@ def _kv_values(w: Workload, rng: np.random.Generator, n: int) -> np.ndarray:
 
 
 def make_case(w: Workload, identity_tables: bool = False,
-              max_blocks_per_seq: Optional[int] = None) -> Case:
-    """Draw one decode step for workload ``w`` (deterministic in ``w.seed``)."""
+              max_blocks_per_seq: Optional[int] = None, prefill_values: bool = True) -> Case:
+    """Draw one decode step for workload ``w`` (deterministic in ``w.seed``).
+
+    ``prefill_values=False`` leaves ``prefill_k``/``prefill_v`` as None (a
+    caller that draws them on the device with ``draw_kv_device``); everything
+    else is drawn as usual, though k_new/v_new then take other values of the
+    same distribution (the host stream skips the prefill draws)."""
     rng = np.random.default_rng(w.seed)
     ctx = draw_context_lens(w, rng)
     tables, num_blocks = build_tables(w, ctx, rng, identity_tables, max_blocks_per_seq)
@@ -267,8 +272,8 @@ def make_case(w: Workload, identity_tables: bool = False,
             slot_parts.append(slots_for(tables[b], np.arange(lo, hi), bs))
     prefill_slots = (np.concatenate(slot_parts) if slot_parts
                      else np.zeros(0, dtype=np.int64)).astype(np.int64)
-    prefill_k = _kv_values(w, rng, len(prefill_slots))
-    prefill_v = _kv_values(w, rng, len(prefill_slots))
+    prefill_k = _kv_values(w, rng, len(prefill_slots)) if prefill_values else None
+    prefill_v = _kv_values(w, rng, len(prefill_slots)) if prefill_values else None
     new_pos = ctx.astype(np.int64) - 1
     new_slots = np.full(w.batch, -1, dtype=np.int64)
     for b in range(w.batch):
@@ -278,6 +283,28 @@ def make_case(w: Workload, identity_tables: bool = False,
     v_new = _kv_values(w, rng, w.batch)
     return Case(w, ctx, tables, num_blocks, q, prefill_slots, prefill_k, prefill_v,
                 new_slots, k_new, v_new)
+
+
+def draw_kv_device(w: Workload, n: int, seed: int, device, chunk: int = 1 << 18):
+    """K or V rows of ``n`` tokens drawn on a CUDA device with the workload's
+    distribution (N(0,1), each element times ``outlier_scale`` with probability
+    ``outlier_prob``, rounded to the 16-bit dtype): the same recipe as the host
+    draws, from torch's seeded generator, for benchmarks whose host draws would
+    take longer than the measurement.  Returns a [n, Hkv, D] tensor of w.q_dtype."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    dt = torch.float16 if w.q_dtype == F16 else torch.bfloat16
+    out = torch.empty((n, w.num_kv_heads, w.head_dim), dtype=dt, device=device)
+    for i in range(0, n, chunk):
+        m = min(chunk, n - i)
+        x = torch.randn((m, w.num_kv_heads, w.head_dim), generator=g, device=device,
+                        dtype=torch.float32)
+        if w.outlier_prob > 0:
+            mask = torch.rand(x.shape, generator=g, device=device) < w.outlier_prob
+            x = torch.where(mask, x * w.outlier_scale, x)
+        out[i:i + m] = x.to(dt)
+    return out
 
 
 def prefill_chunk(case: Case, chunk_lens, seed: int = 0):
