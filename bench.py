@@ -149,6 +149,8 @@ def run_ours(args, rank: int, world: int):
                                 * args.block_size)
     if args.kv_dtype:
         w = _with_kv_dtype(w, args.kv_dtype)
+    if args.batch:
+        w = dataclasses.replace(w, batch=args.batch, pool_blocks=0)
     case = W.make_case(w, identity_tables=args.identity)
     stream = torch.cuda.Stream(dev)
     with torch.cuda.stream(stream):
@@ -375,6 +377,7 @@ def run_ours(args, rank: int, world: int):
             "parallelism": f"replicas x{world}",
             "block_tables": "identity (contiguous)" if args.identity else "shuffled",
             "block_size_override": bool(args.block_size),
+            "batch_override": bool(args.batch),
             "kv_dtype_override": bool(args.kv_dtype),
         },
         "seq_steps_per_s": round(whole_job_rate(w.batch, args.steps, dev_ms, world), 1),
@@ -397,7 +400,7 @@ def run_ours(args, rank: int, world: int):
             "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6.8 TB/s",
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": None if (args.kv_dtype or args.block_size or args.partition)
+            "traffic": None if (args.kv_dtype or args.block_size or args.partition or args.batch)
                        else _traffic(args.config),
             "avg_launch_us": round(attn_avg_ms * 1e3, 3),
             "write_avg_us": round(write_avg_ms * 1e3, 3),
@@ -876,6 +879,8 @@ def main():
                     help="--op copy: block pairs copied per step")
     ap.add_argument("--partition", type=int, default=0,
                     help="override the workload's split-KV partition size (0: keep)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch (wave-count sweep; 0: keep)")
     ap.add_argument("--per-config-reps", type=int, default=100,
                     help="replays per figure in the per-workload sweep (0: skip the sweep)")
     args = ap.parse_args()
@@ -904,7 +909,7 @@ def main():
         return
     res = run_ours(args, rank, world)
     plain = not (args.identity or args.block_size or args.kv_dtype or args.unfused or
-                 args.partition)
+                 args.partition or args.batch)
     if args.per_config_reps > 0 and plain:
         import torch
         res["per_config"] = run_per_config(

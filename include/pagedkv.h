@@ -160,8 +160,11 @@ int paged_kv_copy_blocks(void* k_cache, void* v_cache, void* scales, int kv_dtyp
  * workspace      device scratch of at least paged_decode_workspace_bytes(...)
  *                bytes (may be NULL when that is 0).
  * Work split: the library picks between CTAs whose warps share a partition
- * (merging their states) and warps that each own a (partition, KV head)
- * unit; the environment variable PKV_DECODE_MODE=shared|warp, read on each
+ * (merging their states), warps that each own a (partition, KV head) unit,
+ * and the balanced split, in which one resident wave of warps takes equal
+ * shares of all (sequence, KV head) pairs' tiles and the merge combines the
+ * pieces (chosen where warp-owned units would be, for up to 512 sequences).
+ * The environment variable PKV_DECODE_MODE=shared|warp|balanced, read on each
  * call, forces one (for testing; results agree to rounding).  The test
  * build of the library (libpagedkv_test.so, used by the tests only) also
  * takes PKV_DECODE_MODE=simt, a CUDA-core comparator of the same computation

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "pagedkv.h"
 #include "pkv_internal.h"
 
@@ -93,6 +95,8 @@ int decode_impl(const void* q, int q_dtype, const void* k_new, const void* v_new
   a.k_new = k_new;
   a.v_new = v_new;
   a.slot_mapping = slot_mapping;
+  a.ws_base = np > 1 ? workspace : nullptr;
+  a.ws_bytes = np > 1 ? workspace_bytes : 0;
   cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
@@ -176,7 +180,13 @@ size_t paged_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_he
   const int64_t heads = static_cast<int64_t>(num_seqs) * num_q_heads;
   const int64_t out_bytes = heads * np * head_dim * 4;
   const int64_t ml_bytes = heads * np * 2 * 4;
-  return static_cast<size_t>(ceil_div(out_bytes, 256) * 256 + ml_bytes);
+  size_t bytes = static_cast<size_t>(ceil_div(out_bytes, 256) * 256 + ml_bytes);
+  // room for the balanced split's layout too, when the call may take it
+  if (num_q_heads % num_kv_heads == 0 &&
+      pkv::bal_eligible(num_seqs, num_kv_heads, max_blocks_per_seq, block_size,
+                        static_cast<int>(np)))
+    bytes = std::max(bytes, pkv::bal_layout(num_seqs, num_q_heads, num_kv_heads, head_dim).bytes);
+  return bytes;
 }
 
 int paged_decode_attention(const void* q, int q_dtype,

@@ -217,6 +217,10 @@ struct Params {
   float softmax_scale;
   const int32_t* q_start;     // prefill: [num_seqs + 1] offsets of each chunk's queries in q
   int max_query_len;          // prefill: queries j >= max_query_len of a chunk are not computed
+  // balanced split: the tile prefix over sequences, written by CTA 0 for the
+  // merge ([num_seqs + 1]), and the number of warps the tiles are split over
+  int* ws_prefix;
+  int bal_warps;
 };
 
 // Issue the copies of one 16-token sub-tile into its place in a stage
@@ -325,6 +329,92 @@ __device__ __forceinline__ Unit make_unit(const Params& p, int b, int kvh, int c
   u.tok_begin = u.part * p.partition_size;
   u.tok_end = min(ctx, u.tok_begin + p.partition_size);
   u.ntiles = ctx > 0 ? (u.tok_end - u.tok_begin + kTok - 1) / kTok : 0;
+  return u;
+}
+
+// ---------------------------------------------------------------- balanced split
+// (kBalMaxSeqs, pkv_internal.h: the most sequences the balanced split takes;
+// its tile prefix lives in the CTA's merge buffer, which warp-owned units
+// leave unused)
+static_assert((kBalMaxSeqs + 1) * 4 <= Geo<PKV_F16, 64>::kMbufBytes, "prefix fits the buffer");
+
+// pfx[b] = Hkv * sum over b' < b of ceil(min(ctx_b', cap) / kTok) for b <= B:
+// the first tile of sequence b's first pair in the list of all pairs' tiles.
+// Every thread of the CTA calls it (two barriers); CTA 0 also publishes the
+// prefix for the merge and flags contexts longer than their table rows.
+template <int kTok>
+__device__ __forceinline__ void bal_prefix(const Params& p, int* pfx, int cap) {
+  constexpr int kThreads = kDecodeWarps * kWarp;
+  __shared__ int warp_sum[kDecodeWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int B = p.num_seqs;
+  const int per = (B + kThreads - 1) / kThreads;          // consecutive sequences per thread
+  auto tiles_of = [&](int bb) -> int {
+    int c = p.context_lens[bb];
+    if (c > cap) {
+      if (blockIdx.x == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
+      c = cap;
+    }
+    return c > 0 ? (c + kTok - 1) / kTok : 0;
+  };
+  int local = 0;
+  for (int i = 0; i < per; ++i)
+    if (tid * per + i < B) local += tiles_of(tid * per + i);
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  int run = incl - local;
+  for (int w = 0; w < warp; ++w) run += warp_sum[w];
+  const int hkv = p.num_kv_heads;
+  for (int i = 0; i < per; ++i) {
+    const int bb = tid * per + i;
+    if (bb < B) {
+      pfx[bb] = run * hkv;
+      run += tiles_of(bb);
+    }
+  }
+  if (tid == kThreads - 1) pfx[B] = run * hkv;
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int i = tid; i <= B; i += kThreads) p.ws_prefix[i] = pfx[i];
+}
+
+// The pair (b * Hkv + kvh) holding tile t of the list (0 <= t < pfx[B]).
+__device__ __forceinline__ int bal_pair_of(const int* pfx, int B, int hkv, int t) {
+  int lo = 0, hi = B;                                     // pfx[lo] <= t < pfx[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pfx[mid] <= t) lo = mid;
+    else hi = mid;
+  }
+  const int nt = (pfx[lo + 1] - pfx[lo]) / hkv;
+  return lo * hkv + (t - pfx[lo]) / nt;
+}
+
+// Warp w's piece of pair `pair`: the pair's tiles that fall in [lo, hi) (none
+// for a pair without tokens).  Its partial result goes to workspace slot
+// w + pair, distinct for every (warp, pair) since consecutive pairs share at
+// most one warp.
+template <int kTok>
+__device__ __forceinline__ Unit bal_unit(const Params& p, const int* pfx, int cap, int pair,
+                                         int lo, int hi, int w) {
+  const int hkv = p.num_kv_heads;
+  Unit u;
+  u.b = pair / hkv;
+  u.kvh = pair - u.b * hkv;
+  const int nt = (pfx[u.b + 1] - pfx[u.b]) / hkv;
+  const int base = pfx[u.b] + u.kvh * nt;
+  const int tlo = max(lo, base) - base, thi = min(hi, base + nt) - base;
+  const int ctx = max(0, min(p.context_lens[u.b], cap));
+  u.part = w + pair;
+  u.tok_begin = tlo * kTok;
+  u.ntiles = max(0, thi - tlo);
+  u.tok_end = min(ctx, thi * kTok);
   return u;
 }
 
@@ -492,7 +582,7 @@ __device__ __forceinline__ void merge_state(float (&ma)[2], float (&la)[2], floa
 //    are its 8 columns; it streams the cache from token 0 up to its last
 //    query's position and masks each column causally.  No partitions, no
 //    merges, no barriers (as WU).
-template <int KV, int QT, int D, bool WU, bool PF = false>
+template <int KV, int QT, int D, bool WU, bool PF = false, bool BAL = false>
 __global__ void __launch_bounds__(kDecodeWarps * kWarp, Geo<KV, D>::kMinBlocks)
 paged_decode_kernel(const Params p) {
   using G = Geo<KV, D>;
@@ -516,13 +606,30 @@ paged_decode_kernel(const Params p) {
   const int cap = p.max_blocks_per_seq * p.block_size;
 
   static_assert(!PF || WU, "prefill runs with warp-owned units");
+  static_assert(!BAL || (WU && !PF), "the balanced split is a warp-owned decode mode");
+  // Balanced split: the tiles of every (sequence, KV head) pair, in pair order
+  // (sequence-major), are one list; warp w of the W = p.bal_warps warps takes
+  // tiles [w T / W, (w + 1) T / W) of the T in all.  pfx[b] (in the merge
+  // buffer, unused by warp-owned units) is the number of tiles of the pairs
+  // before sequence b's first: Hkv * sum over b' < b of ceil(ctx_b' / tile).
+  int* pfx = reinterpret_cast<int*>(smem + G::kRingBytes);
+  int bal_lo = 0, bal_hi = 0, bal_p0 = 0, bal_w = 0;
+  if constexpr (BAL) {
+    bal_prefix<G::kTileTok>(p, pfx, cap);
+    const int64_t T = pfx[p.num_seqs];
+    bal_w = static_cast<int>(blockIdx.x) * kDecodeWarps + warp;
+    bal_lo = static_cast<int>(static_cast<int64_t>(bal_w) * T / p.bal_warps);
+    bal_hi = static_cast<int>(static_cast<int64_t>(bal_w + 1) * T / p.bal_warps);
+    if (bal_hi > bal_lo) bal_p0 = bal_pair_of(pfx, p.num_seqs, p.num_kv_heads, bal_lo);
+  }
   const int kvh = PF ? static_cast<int>(blockIdx.y)
-                     : (WU ? static_cast<int>(blockIdx.y) * kDecodeWarps + warp
-                           : static_cast<int>(blockIdx.y));
-  const int b = blockIdx.z;
-  if (WU && kvh >= p.num_kv_heads) return;
-  int ctx = p.context_lens[b];
-  if (ctx > cap) {
+                     : (BAL ? 0
+                            : (WU ? static_cast<int>(blockIdx.y) * kDecodeWarps + warp
+                                  : static_cast<int>(blockIdx.y)));
+  const int b = BAL ? 0 : blockIdx.z;
+  if (WU && !BAL && kvh >= p.num_kv_heads) return;
+  int ctx = BAL ? 0 : p.context_lens[b];
+  if (!BAL && ctx > cap) {
     // a context longer than its table row can hold is clamped (and flagged)
     if (lane == 0 && blockIdx.x == 0 && kvh == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
     ctx = cap;
@@ -543,16 +650,41 @@ paged_decode_kernel(const Params p) {
     if (pos0 < 0 && j0 == 0 && lane == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
     pf_end = max(0, pos0 + min(j0 + qpw, nqc));
   }
-  const int nparts_seq = PF ? 1 : (ctx > 0 ? (ctx + p.partition_size - 1) / p.partition_size : 1);
+  const int nparts_seq = (PF || BAL) ? 1 : (ctx > 0 ? (ctx + p.partition_size - 1) / p.partition_size : 1);
   // unit j -> partition; tiles of a unit this warp takes: kFirst, kFirst + kStride, ...
   constexpr int kStride = WU ? 1 : kDecodeWarps;
   const int kFirst = WU ? 0 : warp;
-  const int pbase = PF ? 0 : static_cast<int>(blockIdx.x) * p.parts_per_cta;
+  const int pbase = (PF || BAL) ? 0 : static_cast<int>(blockIdx.x) * p.parts_per_cta;
   auto part_of = [&](int j) -> int { return pbase + j; };
-  const int nunits = PF ? 1 : min(p.parts_per_cta, nparts_seq - pbase);
-  if (nunits <= 0) return;                 // the whole CTA (same b and partitions for all warps)
+  int nunits;
+  if constexpr (BAL) {
+    // the pairs this warp's tiles touch: bal_p0 .. the pair of its last tile
+    nunits = bal_hi > bal_lo
+                 ? bal_pair_of(pfx, p.num_seqs, p.num_kv_heads, bal_hi - 1) - bal_p0 + 1
+                 : 0;
+    if (nunits == 0 && bal_lo < pfx[p.num_seqs]) {
+      // more warps than tiles: a warp without tiles still sits between the
+      // owners of tile bal_lo's pair, so it leaves an empty piece (max -inf,
+      // sum 0, zero rows) in its slot for the merge
+      const int pair = bal_pair_of(pfx, p.num_seqs, p.num_kv_heads, bal_lo);
+      const int64_t row0 = static_cast<int64_t>(bal_w + pair) * group;
+      for (int g = 0; g < group; ++g) {
+        for (int d = lane; d < D; d += kWarp) p.ws_out[(row0 + g) * D + d] = 0.f;
+        if (lane == 0) {
+          p.ws_ml[(row0 + g) * 2] = -INFINITY;
+          p.ws_ml[(row0 + g) * 2 + 1] = 0.f;
+        }
+      }
+    }
+  } else {
+    nunits = PF ? 1 : min(p.parts_per_cta, nparts_seq - pbase);
+  }
+  if (nunits <= 0) return;                 // the whole CTA (same b and partitions for all
+                                           // warps), or (balanced) a warp without tiles
   auto unit_at = [&](int j) -> Unit {
-    if constexpr (PF) {
+    if constexpr (BAL) {
+      return bal_unit<G::kTileTok>(p, pfx, cap, bal_p0 + j, bal_lo, bal_hi, bal_w);
+    } else if constexpr (PF) {
       Unit u;
       u.b = b;
       u.kvh = kvh;
@@ -633,7 +765,26 @@ paged_decode_kernel(const Params p) {
   };
   // Fused write: the CTA (warp-owned units: the warp) holding b's last
   // partition stores b's new token for its KV head before issuing any copy.
-  if (p.slot_mapping != nullptr && pbase + nunits == nparts_seq) {
+  // Balanced split: the warp holding a pair's last tile, for each such pair,
+  // before it issues that tile.  A piece's last tile is the new token's; when
+  // it sits among the first kStages tiles of the warp's stream (issued before
+  // the loop) the token is written first, otherwise only after those first
+  // copies are on their way, so that the write's latency overlaps theirs.
+  auto bal_writes = [&](bool early) {
+    int pos = 0;                                   // tiles of the stream before piece j's end
+#pragma unroll 1
+    for (int j = 0; j < nunits; ++j) {
+      const Unit u = unit_at(j);
+      pos += u.ntiles;
+      const int cb = max(0, min(p.context_lens[u.b], cap));
+      if (u.ntiles > 0 && u.tok_end == cb && (pos <= G::kStages) == early)
+        fused_write<KV, QT, D>(p, u.b, u.kvh, cb, lane);
+    }
+    __syncwarp();
+  };
+  if constexpr (BAL) {
+    if (p.slot_mapping != nullptr) bal_writes(true);
+  } else if (p.slot_mapping != nullptr && pbase + nunits == nparts_seq) {
     if (WU || warp == 0) fused_write<KV, QT, D>(p, b, kvh, ctx, lane);
     if constexpr (WU) {
       __syncwarp();
@@ -647,6 +798,9 @@ paged_decode_kernel(const Params p) {
   i_next_tb = next_window_unit(0);
 #pragma unroll 1
   for (int s = 0; s < G::kStages; ++s) issue_next();
+  if constexpr (BAL) {
+    if (p.slot_mapping != nullptr) bal_writes(false);
+  }
 
   // INT4: this lane's ldmatrix row addresses within a sub-tile
   const Int4Lanes i4 = int4_lanes<KV, D>(lane);
@@ -691,13 +845,21 @@ paged_decode_kernel(const Params p) {
     q_ok = q4 < group;
     q_row = b;
   }
-  const uint16_t* qrow = p.q + (q_row * p.num_q_heads + kvh * group + (q_ok ? q4 % group : 0)) * D;
-  load_q<KV, QT, D>(qrow, q_ok, q4, c4, qb, qexp, zq, zscale,
-                    qoff8);
+  if constexpr (!BAL) {
+    const uint16_t* qrow = p.q + (q_row * p.num_q_heads + kvh * group + (q_ok ? q4 % group : 0)) * D;
+    load_q<KV, QT, D>(qrow, q_ok, q4, c4, qb, qexp, zq, zscale, qoff8);
+  }
 
 #pragma unroll 1
   for (int cu = 0; cu < nunits; ++cu) {
     const Unit unit = unit_at(cu);
+    if constexpr (BAL) {
+      // each piece may belong to another sequence and KV head: its own q
+      const uint16_t* qrow =
+          p.q + ((static_cast<int64_t>(unit.b) * p.num_q_heads + unit.kvh * group +
+                  (q_ok ? q4 : 0)) * D);
+      load_q<KV, QT, D>(qrow, q_ok, q4, c4, qb, qexp, zq, zscale, qoff8);
+    }
 #pragma unroll
     for (int i = 0; i < MT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
     mrow[0] = mrow[1] = -INFINITY;           // running max (log2 units), heads 2c4, 2c4+1
@@ -1231,7 +1393,9 @@ paged_decode_kernel(const Params p) {
           head = head0 + g;
           inv = lrow[h] > 0.f ? 1.f / lrow[h] : 0.f;
         }
-        const int64_t slot = head * p.num_partitions + unit.part;
+        // balanced split: slot (piece slot, head in the group), else (head, partition)
+        const int64_t slot = BAL ? static_cast<int64_t>(unit.part) * group + g
+                                 : head * p.num_partitions + unit.part;
 #pragma unroll
         for (int i = 0; i < MT; ++i) {
           int d0;
@@ -1243,14 +1407,14 @@ paged_decode_kernel(const Params p) {
             d0 = (D == 128 ? 16 : 8) * q4 + 2 * i;
           }
           const float v0 = oacc[i][h] * inv, v1 = oacc[i][2 + h] * inv;
-          if (p.num_partitions == 1) {
+          if (!BAL && p.num_partitions == 1) {
             uint32_t* outp = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + head * D + d0);
             *outp = Half16<QT>::pack_rn(v0, v1);
           } else {
             *reinterpret_cast<float2*>(p.ws_out + slot * D + d0) = make_float2(v0, v1);
           }
         }
-        if (p.num_partitions > 1 && q4 == 0) {
+        if ((BAL || p.num_partitions > 1) && q4 == 0) {
           p.ws_ml[slot * 2] = mrow[h];
           p.ws_ml[slot * 2 + 1] = lrow[h];
         }

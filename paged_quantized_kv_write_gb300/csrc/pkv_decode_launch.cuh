@@ -12,6 +12,9 @@ namespace {
 
 // Merge the partitions of one (sequence, q head): M = max m_p,
 // L = sum l_p 2^(m_p - M), out = sum l_p 2^(m_p - M) O_p / L.
+// BAL: the partials are the pieces of the balanced split (see bal_unit):
+// those of pair (b, kvh) sit in slots w + pair for the warps w whose tiles
+// meet the pair; a pair without tokens gives zeros.
 //
 // One CTA per (sequence, q head) with W warps.  Lane l of every warp keeps
 // head_dim values [EPT l, EPT l + EPT) of the sum.  The partitions are taken
@@ -19,7 +22,7 @@ namespace {
 // warp's block k, the warp then walks the block with eight independent
 // 16-byte (8-byte at head_dim 64) loads in flight per lane, each weight
 // handed out by a shuffle; the W warps' sums meet in shared memory.
-template <int QT, int D, int W>
+template <int QT, int D, int W, bool BAL = false>
 __global__ void __launch_bounds__(32 * W)
 pkv_lse_reduce(const Params p) {
   constexpr int EPT = D / kWarp;                   // 4 (D = 128) or 2 (D = 64)
@@ -29,12 +32,48 @@ pkv_lse_reduce(const Params p) {
   const int64_t head = blockIdx.x;                 // b * Hq + h
   const int b = static_cast<int>(head / p.num_q_heads);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int ctx = min(p.context_lens[b], p.max_blocks_per_seq * p.block_size);
-  const int np = max(1, (ctx + p.partition_size - 1) / p.partition_size);
-  const float* ml = p.ws_ml + head * p.num_partitions * 2;
-  const float* o = p.ws_out + head * p.num_partitions * D + EPT * lane;
+  int np;                                          // partials of this head
+  const float* ml;
+  const float* o;
+  int64_t ml_step, o_step;                         // floats between consecutive partials
+  if constexpr (BAL) {
+    const int group = p.num_q_heads / p.num_kv_heads;
+    const int h = static_cast<int>(head - static_cast<int64_t>(b) * p.num_q_heads);
+    const int kvh = h / group, g = h - kvh * group;
+    const int pair = b * p.num_kv_heads + kvh;
+    const int* pfx = p.ws_prefix;
+    const int64_t T = __ldcg(pfx + p.num_seqs);
+    const int nt = (__ldcg(pfx + b + 1) - __ldcg(pfx + b)) / p.num_kv_heads;
+    np = 0;
+    int first = 0;
+    if (nt > 0) {
+      // warp w holds tiles [w T / W, (w + 1) T / W); tile t's warp is
+      // floor(((t + 1) W - 1) / T)
+      const int64_t Wn = p.bal_warps;
+      const int64_t t0 = __ldcg(pfx + b) + static_cast<int64_t>(kvh) * nt, t1 = t0 + nt - 1;
+      const int w0 = static_cast<int>(((t0 + 1) * Wn - 1) / T);
+      const int w1 = static_cast<int>(((t1 + 1) * Wn - 1) / T);
+      np = w1 - w0 + 1;
+      first = w0 + pair;
+    } else if (h == 0 && lane == 0 && warp == 0 && p.slot_mapping != nullptr &&
+               p.slot_mapping[b] != -1) {
+      // a sequence without tokens has no slot to write (as the other splits flag it)
+      flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
+    }
+    ml = p.ws_ml + (static_cast<int64_t>(first) * group + g) * 2;
+    o = p.ws_out + (static_cast<int64_t>(first) * group + g) * D + EPT * lane;
+    ml_step = 2 * group;
+    o_step = static_cast<int64_t>(group) * D;
+  } else {
+    const int ctx = min(p.context_lens[b], p.max_blocks_per_seq * p.block_size);
+    np = max(1, (ctx + p.partition_size - 1) / p.partition_size);
+    ml = p.ws_ml + head * p.num_partitions * 2;
+    o = p.ws_out + head * p.num_partitions * D + EPT * lane;
+    ml_step = 2;
+    o_step = D;
+  }
   float M = -INFINITY;
-  for (int i = lane; i < np; i += kWarp) M = fmaxf(M, __ldcg(ml + 2 * i));
+  for (int i = lane; i < np; i += kWarp) M = fmaxf(M, __ldcg(ml + ml_step * i));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float acc[EPT];
@@ -46,8 +85,8 @@ pkv_lse_reduce(const Params p) {
       const int i = base + lane;
       float wgt = 0.f;
       if (i < np) {
-        const float m = __ldcg(ml + 2 * i);
-        wgt = m == -INFINITY ? 0.f : __ldcg(ml + 2 * i + 1) * exp2f(m - M);
+        const float m = __ldcg(ml + ml_step * i);
+        wgt = m == -INFINITY ? 0.f : __ldcg(ml + ml_step * i + 1) * exp2f(m - M);
       }
       L += wgt;
       const int n = min(kWarp, np - base);
@@ -55,7 +94,7 @@ pkv_lse_reduce(const Params p) {
         float v[8][EPT];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const float* src = o + static_cast<int64_t>(base + j + u) * D;
+          const float* src = o + static_cast<int64_t>(base + j + u) * o_step;
           if (j + u < n) {
             if constexpr (EPT == 4) {
               const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
@@ -104,16 +143,17 @@ pkv_lse_reduce(const Params p) {
 
 // the merge for a call's partition count: warps per (sequence, q head)
 template <int QT, int D>
-cudaError_t launch_lse_typed(const Params& p, int num_heads, cudaStream_t st) {
+cudaError_t launch_lse_typed(const Params& p, int num_heads, cudaStream_t st, bool bal = false) {
+  if (bal)
+    return launch_pdl(pkv_lse_reduce<QT, D, 1, true>, dim3(static_cast<unsigned>(num_heads)),
+                      dim3(32), 0, st, p);
   const dim3 grid(static_cast<unsigned>(num_heads));
   if (p.num_partitions <= 32) return launch_pdl(pkv_lse_reduce<QT, D, 1>, grid, dim3(32), 0, st, p);
   if (p.num_partitions <= 64) return launch_pdl(pkv_lse_reduce<QT, D, 2>, grid, dim3(64), 0, st, p);
   return launch_pdl(pkv_lse_reduce<QT, D, 4>, grid, dim3(128), 0, st, p);
 }
 
-template <int KV, int QT, int D, bool WU>
-cudaError_t launch_mode(const DecodeArgs& a, cudaStream_t st) {
-  using G = Geo<KV, D>;
+inline Params params_of(const DecodeArgs& a) {
   Params p;
   p.q = static_cast<const uint16_t*>(a.q);
   // the caches are written only by the fused write (a.slot_mapping set), which
@@ -141,27 +181,68 @@ cudaError_t launch_mode(const DecodeArgs& a, cudaStream_t st) {
   p.softmax_scale = a.softmax_scale;
   p.q_start = nullptr;
   p.max_query_len = 0;
-  auto kern = paged_decode_kernel<KV, QT, D, WU>;
-  // per device, once: the shared-memory opt-in and the resident CTAs per SM
-  static std::atomic<int> slots_per_dev[kMaxDevices];     // SMs x resident CTAs (0: unknown)
   p.parts_per_cta = 1;
+  p.ws_prefix = nullptr;
+  p.bal_warps = 0;
+  return p;
+}
+
+// SMs x resident CTAs of `kern` on the current device (looked up once per
+// device, with the shared-memory opt-in set on the way)
+template <typename K>
+cudaError_t kernel_slots(K kern, size_t smem, std::atomic<int>* slots_per_dev, int* slots) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  int slots = slots_per_dev[dev].load(std::memory_order_relaxed);
-  if (slots == 0) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes);
+  *slots = slots_per_dev[dev].load(std::memory_order_relaxed);
+  if (*slots == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     int occ = 0, sms = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kDecodeWarps * kWarp,
-                                                      G::kSmemBytes);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kDecodeWarps * kWarp, smem);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    slots = max(1, occ) * max(1, sms);
-    slots_per_dev[dev].store(slots, std::memory_order_relaxed);
+    *slots = max(1, occ) * max(1, sms);
+    slots_per_dev[dev].store(*slots, std::memory_order_relaxed);
   }
+  return cudaSuccess;
+}
+
+// The balanced split: one resident wave of CTAs (at most kBalMaxWarps warps),
+// each warp an equal share of all pairs' tiles, then the merge of the pieces.
+template <int KV, int QT, int D>
+cudaError_t launch_bal(const DecodeArgs& a, cudaStream_t st) {
+  using G = Geo<KV, D>;
+  Params p = params_of(a);
+  auto kern = paged_decode_kernel<KV, QT, D, true, false, true>;
+  static std::atomic<int> slots_per_dev[kMaxDevices];
+  int slots = 0;
+  cudaError_t e = kernel_slots(kern, G::kSmemBytes, slots_per_dev, &slots);
+  if (e != cudaSuccess) return e;
+  const int ctas = std::min(slots, kBalMaxWarps / kDecodeWarps);
+  p.bal_warps = ctas * kDecodeWarps;
+  const BalLayout L = bal_layout(a.num_seqs, a.num_q_heads, a.num_kv_heads, a.head_dim);
+  uint8_t* base = static_cast<uint8_t*>(a.ws_base);
+  p.ws_out = reinterpret_cast<float*>(base);
+  p.ws_ml = reinterpret_cast<float*>(base + L.ml_off);
+  p.ws_prefix = reinterpret_cast<int*>(base + L.pfx_off);
+  e = launch_pdl(kern, dim3(ctas), dim3(kDecodeWarps * kWarp), G::kSmemBytes, st, p);
+  if (e != cudaSuccess) return e;
+  return launch_lse_typed<QT, D>(p, a.num_seqs * a.num_q_heads, st, true);
+}
+
+template <int KV, int QT, int D, bool WU>
+cudaError_t launch_mode(const DecodeArgs& a, cudaStream_t st) {
+  using G = Geo<KV, D>;
+  Params p = params_of(a);
+  auto kern = paged_decode_kernel<KV, QT, D, WU>;
+  // per device, once: the shared-memory opt-in and the resident CTAs per SM
+  static std::atomic<int> slots_per_dev[kMaxDevices];     // SMs x resident CTAs (0: unknown)
+  int slots = 0;
+  cudaError_t e = kernel_slots(kern, G::kSmemBytes, slots_per_dev, &slots);
+  if (e != cudaSuccess) return e;
   // partitions per CTA (per warp with WU): runs of up to PKV_RUN_TOKENS tokens
   // per warp stream, as long as the grid keeps at least four waves of CTAs
   const int heads_per_cta = WU ? kDecodeWarps : 1;
@@ -184,8 +265,8 @@ cudaError_t launch_mode(const DecodeArgs& a, cudaStream_t st) {
 }
 
 // Warp-owned units when the split-KV work has enough (partition, sequence, KV
-// head) units for several waves of warps (PKV_WU_WAVES x SMs x 16 warps);
-// shared partitions otherwise.
+// head) units for several waves of warps (PKV_WU_WAVES x SMs x 16 warps), in
+// the balanced split when the call allows it; shared partitions otherwise.
 template <int KV, int QT, int D>
 cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t st) {
   static std::atomic<int> sms_per_dev[kMaxDevices];
@@ -205,15 +286,26 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t st) {
   // results).  The test build also takes =simt, the CUDA-core comparator
   // (16-bit, FP8 and INT8 caches without the fused write; other calls keep
   // the tensor path), and =tc, the tcgen05 comparator for one-byte caches.
+  // Where warp-owned units would be chosen, the balanced split takes the work
+  // instead when it can (measured on GB300: config 4 198.6 -> 184.3 us,
+  // config 5 188.4 -> 184.3, config 3 110.5 -> 108.5 for the attention call).
+  const bool bal_ok = a.ws_base != nullptr &&
+                      bal_eligible(a.num_seqs, a.num_kv_heads, a.max_blocks_per_seq,
+                                   a.block_size, a.num_partitions);
+  bool bal = wu && bal_ok;
   if (const char* m = getenv("PKV_DECODE_MODE")) {
-    if (!strcmp(m, "shared")) wu = false;
-    if (!strcmp(m, "warp")) wu = true;
+    // shared / warp: the partitioned splits (shared or warp-owned partitions);
+    // balanced: the balanced split wherever it can run
+    if (!strcmp(m, "shared")) wu = bal = false;
+    if (!strcmp(m, "warp")) { wu = true; bal = false; }
+    if (!strcmp(m, "balanced")) bal = bal_ok;
 #ifdef PKV_TEST_HOOKS
     if (!strcmp(m, "simt") && KV != PKV_INT4_G32 && a.slot_mapping == nullptr)
       return launch_simt(a, st);
     if (!strcmp(m, "tc") && decode_tc_supported(a)) return launch_decode_tc(a, st);
 #endif
   }
+  if (bal) return launch_bal<KV, QT, D>(a, st);
   return wu ? launch_mode<KV, QT, D, true>(a, st) : launch_mode<KV, QT, D, false>(a, st);
 }
 

@@ -51,7 +51,38 @@ struct DecodeArgs {
   const void* k_new = nullptr;
   const void* v_new = nullptr;
   const int64_t* slot_mapping = nullptr;
+  // the whole caller workspace (the balanced split lays it out its own way)
+  void* ws_base = nullptr;
+  size_t ws_bytes = 0;
 };
+
+// Balanced split of the decode work (warp-owned, equal tile counts per warp):
+// at most kBalMaxSeqs sequences, at most kBalMaxWarps warps (152 SMs x 4 CTAs
+// x 4 warps).  Its workspace: partial rows [slots][G][D] floats, then
+// (max, sum) [slots][G][2], then the tile prefix [num_seqs + 1] ints, with
+// slots = kBalMaxWarps + num_seqs * num_kv_heads (each 256-byte aligned).
+constexpr int kBalMaxSeqs = 512;
+constexpr int kBalMaxWarps = 152 * 4 * 4;
+struct BalLayout {
+  size_t ml_off, pfx_off, bytes;
+};
+inline BalLayout bal_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim) {
+  const size_t slots = static_cast<size_t>(kBalMaxWarps) + static_cast<size_t>(num_seqs) * num_kv_heads;
+  const size_t rows = slots * static_cast<size_t>(num_q_heads / num_kv_heads);
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  BalLayout L;
+  L.ml_off = up(rows * head_dim * 4);
+  L.pfx_off = L.ml_off + up(rows * 2 * 4);
+  L.bytes = L.pfx_off + (static_cast<size_t>(num_seqs) + 1) * 4;
+  return L;
+}
+// whether a call may take the balanced split (the tile list must fit int)
+inline bool bal_eligible(int num_seqs, int num_kv_heads, int max_blocks_per_seq, int block_size,
+                         int num_partitions) {
+  if (num_partitions <= 1 || num_seqs > kBalMaxSeqs) return false;
+  const int64_t tiles = (static_cast<int64_t>(max_blocks_per_seq) * block_size + 15) / 16;
+  return static_cast<int64_t>(num_seqs) * num_kv_heads * tiles < (int64_t(1) << 30);
+}
 
 struct PrefillArgs {
   const void* q;                 // [q_start[num_seqs]][num_q_heads][head_dim]

@@ -16,9 +16,11 @@ from tests import helpers as H
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["shared", "warp", "simt", "tc"])
+@pytest.fixture(params=["shared", "warp", "balanced", "simt", "tc"])
 def mode(request, monkeypatch):
-    """Run a test under both work splits of the decode kernel, under the SIMT
+    """Run a test under the decode kernel's work splits (shared partitions,
+    warp-owned partitions, the balanced split of all tiles over one wave of
+    warps), under the SIMT
     comparator (which takes 16-bit, FP8 and INT8 caches; INT4 stays on the
     tensor path), and under the tcgen05 kernel (one-byte caches with head_dim
     128; other calls keep the mma.sync kernel).  The comparators live in the

@@ -14,7 +14,7 @@ from tests import helpers as H
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["shared", "warp", "tc"])
+@pytest.fixture(params=["shared", "warp", "balanced", "tc"])
 def mode(request, monkeypatch):
     monkeypatch.setenv("PKV_DECODE_MODE", request.param)
     with H.library_for(request.param):

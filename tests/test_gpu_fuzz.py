@@ -16,7 +16,7 @@ from tests import helpers as H
 pytestmark = pytest.mark.gpu
 
 KV_TYPES = [W.F16, W.BF16, W.FP8_E4M3, W.FP8_E5M2, W.INT8, W.INT4_G32]
-DECODE_MODES = ["default", "shared", "warp", "simt", "tc"]
+DECODE_MODES = ["default", "shared", "warp", "balanced", "simt", "tc"]
 
 
 def _draw(seed: int, max_ctx=(17, 100, 700, 2000)):
