@@ -217,9 +217,7 @@ struct Params {
   float softmax_scale;
   const int32_t* q_start;     // prefill: [num_seqs + 1] offsets of each chunk's queries in q
   int max_query_len;          // prefill: queries j >= max_query_len of a chunk are not computed
-  // balanced split: the tile prefix over sequences, written by CTA 0 for the
-  // merge ([num_seqs + 1]), and the number of warps the tiles are split over
-  int* ws_prefix;
+  // balanced split: the number of warps the tiles are split over
   int bal_warps;
 };
 
@@ -292,26 +290,28 @@ __device__ __forceinline__ void issue_tile(const Params& p, int rowp, bool live,
 // CTA alone; any other slot is flagged and left unwritten.
 template <int KV, int QT, int D>
 __device__ __forceinline__ void fused_write(const Params& p, int b, int kvh, int ctx, int lane) {
+  // the slot, the table entry of position ctx - 1 and the new K and V rows are
+  // independent loads: issued together, they cost one memory latency
+  const int64_t row = static_cast<int64_t>(b) * p.num_kv_heads + kvh;
   const int64_t slot = p.slot_mapping[b];
+  const int t = ctx - 1;
+  const int logical = ctx > 0 ? t / p.block_size : 0;
+  const int phys = ctx > 0 ? p.block_tables[static_cast<int64_t>(b) * p.max_blocks_per_seq + logical]
+                           : -1;
+  const RowWords<D> kw = load_row_words<D>(p.k_new + row * D, lane);
+  const RowWords<D> vw = load_row_words<D>(p.v_new + row * D, lane);
   if (slot == -1) return;
   int64_t expect = -2;
-  if (ctx > 0) {
-    const int t = ctx - 1;
-    const int logical = t / p.block_size;
-    const int phys = p.block_tables[static_cast<int64_t>(b) * p.max_blocks_per_seq + logical];
-    if (phys >= 0 && phys < p.num_blocks)
-      expect = static_cast<int64_t>(phys) * p.block_size + (t - logical * p.block_size);
-  }
+  if (ctx > 0 && phys >= 0 && phys < p.num_blocks)
+    expect = static_cast<int64_t>(phys) * p.block_size + (t - logical * p.block_size);
   if (slot != expect) {
     if (lane == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
     return;
   }
   const int64_t block = slot / p.block_size;
   const int offset = static_cast<int>(slot - block * p.block_size);
-  const int64_t row = static_cast<int64_t>(b) * p.num_kv_heads + kvh;
-  encode_token_head<KV, QT, D>(p.k_new + row * D, p.v_new + row * D, p.k_cache, p.v_cache,
-                               p.scales, p.num_blocks, p.num_kv_heads, p.block_size, block, kvh,
-                               offset, lane);
+  encode_token_head_words<KV, QT, D>(kw, vw, p.k_cache, p.v_cache, p.scales, p.num_blocks,
+                                     p.num_kv_heads, p.block_size, block, kvh, offset, lane);
 }
 
 // One unit of work: partition `part` of sequence b, KV head kvh.
@@ -340,8 +340,8 @@ static_assert((kBalMaxSeqs + 1) * 4 <= Geo<PKV_F16, 64>::kMbufBytes, "prefix fit
 
 // pfx[b] = Hkv * sum over b' < b of ceil(min(ctx_b', cap) / kTok) for b <= B:
 // the first tile of sequence b's first pair in the list of all pairs' tiles.
-// Every thread of the CTA calls it (two barriers); CTA 0 also publishes the
-// prefix for the merge and flags contexts longer than their table rows.
+// Every thread of the CTA calls it (two barriers); CTA 0 also flags contexts
+// longer than their table rows.
 template <int kTok>
 __device__ __forceinline__ void bal_prefix(const Params& p, int* pfx, int cap) {
   constexpr int kThreads = kDecodeWarps * kWarp;
@@ -380,8 +380,6 @@ __device__ __forceinline__ void bal_prefix(const Params& p, int* pfx, int cap) {
   }
   if (tid == kThreads - 1) pfx[B] = run * hkv;
   __syncthreads();
-  if (blockIdx.x == 0)
-    for (int i = tid; i <= B; i += kThreads) p.ws_prefix[i] = pfx[i];
 }
 
 // The pair (b * Hkv + kvh) holding tile t of the list (0 <= t < pfx[B]).

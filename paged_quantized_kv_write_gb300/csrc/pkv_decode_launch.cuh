@@ -12,9 +12,6 @@ namespace {
 
 // Merge the partitions of one (sequence, q head): M = max m_p,
 // L = sum l_p 2^(m_p - M), out = sum l_p 2^(m_p - M) O_p / L.
-// BAL: the partials are the pieces of the balanced split (see bal_unit):
-// those of pair (b, kvh) sit in slots w + pair for the warps w whose tiles
-// meet the pair; a pair without tokens gives zeros.
 //
 // One CTA per (sequence, q head) with W warps.  Lane l of every warp keeps
 // head_dim values [EPT l, EPT l + EPT) of the sum.  The partitions are taken
@@ -22,7 +19,7 @@ namespace {
 // warp's block k, the warp then walks the block with eight independent
 // 16-byte (8-byte at head_dim 64) loads in flight per lane, each weight
 // handed out by a shuffle; the W warps' sums meet in shared memory.
-template <int QT, int D, int W, bool BAL = false>
+template <int QT, int D, int W>
 __global__ void __launch_bounds__(32 * W)
 pkv_lse_reduce(const Params p) {
   constexpr int EPT = D / kWarp;                   // 4 (D = 128) or 2 (D = 64)
@@ -32,46 +29,11 @@ pkv_lse_reduce(const Params p) {
   const int64_t head = blockIdx.x;                 // b * Hq + h
   const int b = static_cast<int>(head / p.num_q_heads);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int np;                                          // partials of this head
-  const float* ml;
-  const float* o;
-  int64_t ml_step, o_step;                         // floats between consecutive partials
-  if constexpr (BAL) {
-    const int group = p.num_q_heads / p.num_kv_heads;
-    const int h = static_cast<int>(head - static_cast<int64_t>(b) * p.num_q_heads);
-    const int kvh = h / group, g = h - kvh * group;
-    const int pair = b * p.num_kv_heads + kvh;
-    const int* pfx = p.ws_prefix;
-    const int64_t T = __ldcg(pfx + p.num_seqs);
-    const int nt = (__ldcg(pfx + b + 1) - __ldcg(pfx + b)) / p.num_kv_heads;
-    np = 0;
-    int first = 0;
-    if (nt > 0) {
-      // warp w holds tiles [w T / W, (w + 1) T / W); tile t's warp is
-      // floor(((t + 1) W - 1) / T)
-      const int64_t Wn = p.bal_warps;
-      const int64_t t0 = __ldcg(pfx + b) + static_cast<int64_t>(kvh) * nt, t1 = t0 + nt - 1;
-      const int w0 = static_cast<int>(((t0 + 1) * Wn - 1) / T);
-      const int w1 = static_cast<int>(((t1 + 1) * Wn - 1) / T);
-      np = w1 - w0 + 1;
-      first = w0 + pair;
-    } else if (h == 0 && lane == 0 && warp == 0 && p.slot_mapping != nullptr &&
-               p.slot_mapping[b] != -1) {
-      // a sequence without tokens has no slot to write (as the other splits flag it)
-      flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
-    }
-    ml = p.ws_ml + (static_cast<int64_t>(first) * group + g) * 2;
-    o = p.ws_out + (static_cast<int64_t>(first) * group + g) * D + EPT * lane;
-    ml_step = 2 * group;
-    o_step = static_cast<int64_t>(group) * D;
-  } else {
-    const int ctx = min(p.context_lens[b], p.max_blocks_per_seq * p.block_size);
-    np = max(1, (ctx + p.partition_size - 1) / p.partition_size);
-    ml = p.ws_ml + head * p.num_partitions * 2;
-    o = p.ws_out + head * p.num_partitions * D + EPT * lane;
-    ml_step = 2;
-    o_step = D;
-  }
+  const int ctx = min(p.context_lens[b], p.max_blocks_per_seq * p.block_size);
+  const int np = max(1, (ctx + p.partition_size - 1) / p.partition_size);
+  const float* ml = p.ws_ml + head * p.num_partitions * 2;
+  const float* o = p.ws_out + head * p.num_partitions * D + EPT * lane;
+  constexpr int64_t ml_step = 2, o_step = D;
   float M = -INFINITY;
   for (int i = lane; i < np; i += kWarp) M = fmaxf(M, __ldcg(ml + ml_step * i));
 #pragma unroll
@@ -141,12 +103,130 @@ pkv_lse_reduce(const Params p) {
   }
 }
 
+// The merge of the balanced split: one CTA per (sequence, KV head) pair, warp
+// g merging query head g of the group.  The pair's tile range and the warps
+// that hold its pieces come from the tile prefix, which the CTA computes from
+// context_lens (a CTA-wide scan) before it waits for the decode kernel, so
+// that this chain overlaps the decode kernel's end; then each warp merges its
+// head's pieces (slots w + pair, see bal_unit) as pkv_lse_reduce does.
+template <int QT, int D, int kTok>
+__global__ void __launch_bounds__(8 * kWarp)
+pkv_bal_merge(const Params p) {
+  constexpr int EPT = D / kWarp;
+  __shared__ int s_before[8], s_all[8];            // per warp: tiles before sequence b, in all
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nthreads = blockDim.x, nwarps = nthreads / kWarp;
+  const int hkv = p.num_kv_heads, group = p.num_q_heads / hkv;
+  const int b = static_cast<int>(blockIdx.x) / hkv, kvh = static_cast<int>(blockIdx.x) - b * hkv;
+  const int cap = p.max_blocks_per_seq * p.block_size;
+  auto tiles_of = [&](int bb) -> int {
+    const int c = min(p.context_lens[bb], cap);
+    return c > 0 ? (c + kTok - 1) / kTok : 0;
+  };
+  int before = 0, all = 0;
+  for (int bb = tid; bb < p.num_seqs; bb += nthreads) {
+    const int t = tiles_of(bb);
+    all += t;
+    if (bb < b) before += t;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    before += __shfl_xor_sync(0xffffffffu, before, o);
+    all += __shfl_xor_sync(0xffffffffu, all, o);
+  }
+  if (lane == 0) {
+    s_before[warp] = before;
+    s_all[warp] = all;
+  }
+  __syncthreads();
+  before = 0;
+  all = 0;
+  for (int w = 0; w < nwarps; ++w) {
+    before += s_before[w];
+    all += s_all[w];
+  }
+  const int nt = tiles_of(b);
+  const int t0 = before * hkv + kvh * nt;          // the pair's first tile in the list
+  const int64_t T = static_cast<int64_t>(all) * hkv;
+  pdl_wait();                                      // the pieces of the decode kernel
+  if (warp >= group) return;
+  const int pair = b * hkv + kvh;
+  int np = 0, first = 0;
+  if (nt > 0) {
+    const int64_t Wn = p.bal_warps;
+    const int w0 = static_cast<int>((static_cast<int64_t>(t0 + 1) * Wn - 1) / T);
+    const int w1 = static_cast<int>((static_cast<int64_t>(t0 + nt) * Wn - 1) / T);
+    np = w1 - w0 + 1;
+    first = w0 + pair;
+  } else if (kvh == 0 && warp == 0 && lane == 0 && p.slot_mapping != nullptr &&
+             p.slot_mapping[b] != -1) {
+    // a sequence without tokens has no slot to write (as the other splits flag it)
+    flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
+  }
+  const int g = warp;
+  const float* ml = p.ws_ml + (static_cast<int64_t>(first) * group + g) * 2;
+  const float* o = p.ws_out + (static_cast<int64_t>(first) * group + g) * D + EPT * lane;
+  const int64_t ml_step = 2 * group, o_step = static_cast<int64_t>(group) * D;
+  float M = -INFINITY;
+  for (int i = lane; i < np; i += kWarp) M = fmaxf(M, __ldcg(ml + ml_step * i));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float acc[EPT];
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) acc[e] = 0.f;
+  float L = 0.f;
+  if (M != -INFINITY) {
+    for (int base = 0; base < np; base += kWarp) {
+      const int i = base + lane;
+      float wgt = 0.f;
+      if (i < np) {
+        const float m = __ldcg(ml + ml_step * i);
+        wgt = m == -INFINITY ? 0.f : __ldcg(ml + ml_step * i + 1) * exp2f(m - M);
+      }
+      L += wgt;
+      const int n = min(kWarp, np - base);
+      for (int j = 0; j < n; j += 4) {
+        float v[4][EPT];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float* src = o + static_cast<int64_t>(base + j + u) * o_step;
+          if (j + u < n) {
+            if constexpr (EPT == 4) {
+              const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
+              v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+            } else {
+              const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+              v[u][0] = x.x; v[u][1] = x.y;
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float wj = __shfl_sync(0xffffffffu, wgt, (j + u) & 31);
+          if (j + u < n) {
+#pragma unroll
+            for (int e = 0; e < EPT; ++e) acc[e] = fmaf(wj, v[u][e], acc[e]);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const int64_t head = static_cast<int64_t>(b) * p.num_q_heads + kvh * group + g;
+  uint16_t* outp = static_cast<uint16_t*>(p.out) + head * D + EPT * lane;
+  if constexpr (EPT == 4) {
+    *reinterpret_cast<uint2*>(outp) = make_uint2(Half16<QT>::pack_rn(acc[0] * inv, acc[1] * inv),
+                                                 Half16<QT>::pack_rn(acc[2] * inv, acc[3] * inv));
+  } else {
+    *reinterpret_cast<uint32_t*>(outp) = Half16<QT>::pack_rn(acc[0] * inv, acc[1] * inv);
+  }
+}
+
 // the merge for a call's partition count: warps per (sequence, q head)
 template <int QT, int D>
-cudaError_t launch_lse_typed(const Params& p, int num_heads, cudaStream_t st, bool bal = false) {
-  if (bal)
-    return launch_pdl(pkv_lse_reduce<QT, D, 1, true>, dim3(static_cast<unsigned>(num_heads)),
-                      dim3(32), 0, st, p);
+cudaError_t launch_lse_typed(const Params& p, int num_heads, cudaStream_t st) {
   const dim3 grid(static_cast<unsigned>(num_heads));
   if (p.num_partitions <= 32) return launch_pdl(pkv_lse_reduce<QT, D, 1>, grid, dim3(32), 0, st, p);
   if (p.num_partitions <= 64) return launch_pdl(pkv_lse_reduce<QT, D, 2>, grid, dim3(64), 0, st, p);
@@ -182,7 +262,6 @@ inline Params params_of(const DecodeArgs& a) {
   p.q_start = nullptr;
   p.max_query_len = 0;
   p.parts_per_cta = 1;
-  p.ws_prefix = nullptr;
   p.bal_warps = 0;
   return p;
 }
@@ -227,10 +306,14 @@ cudaError_t launch_bal(const DecodeArgs& a, cudaStream_t st) {
   uint8_t* base = static_cast<uint8_t*>(a.ws_base);
   p.ws_out = reinterpret_cast<float*>(base);
   p.ws_ml = reinterpret_cast<float*>(base + L.ml_off);
-  p.ws_prefix = reinterpret_cast<int*>(base + L.pfx_off);
   e = launch_pdl(kern, dim3(ctas), dim3(kDecodeWarps * kWarp), G::kSmemBytes, st, p);
   if (e != cudaSuccess) return e;
-  return launch_lse_typed<QT, D>(p, a.num_seqs * a.num_q_heads, st, true);
+  // one CTA per (sequence, KV head), a warp per query head of the group (at
+  // least 4 warps, which the prefix scan needs)
+  const int group = a.num_q_heads / a.num_kv_heads;
+  return launch_pdl(pkv_bal_merge<QT, D, G::kTileTok>,
+                    dim3(static_cast<unsigned>(a.num_seqs * a.num_kv_heads)),
+                    dim3(kWarp * std::max(4, group)), 0, st, p);
 }
 
 template <int KV, int QT, int D, bool WU>

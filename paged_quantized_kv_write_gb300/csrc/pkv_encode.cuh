@@ -66,29 +66,46 @@ __device__ __forceinline__ float row_amax(const uint16_t* __restrict__ src, int 
   return amax;
 }
 
-// k_src / v_src: the token's rows for this head (D values of dtype NEW).
-// block, offset: where the token goes; cache_row = (block * Hkv + head) * bs + offset.
+// This lane's EPL = D/32 consecutive 16-bit values of a row, as 32-bit words.
+template <int D>
+struct RowWords {
+  uint32_t w[D / kWarp / 2];
+};
+template <int D>
+__device__ __forceinline__ RowWords<D> load_row_words(const uint16_t* __restrict__ src, int lane) {
+  RowWords<D> r;
+  if constexpr (D / kWarp == 4) {
+    const uint2 v = *reinterpret_cast<const uint2*>(src + lane * 4);
+    r.w[0] = v.x;
+    r.w[1] = v.y;
+  } else {
+    r.w[0] = *reinterpret_cast<const uint32_t*>(src + lane * 2);
+  }
+  return r;
+}
+
+// The encoding of one (token, KV head) from this lane's words of its K and V
+// rows (see encode_token_head).
 template <int KV, int NEW, int D, int SRC = kScaleOwnRow>
-__device__ __forceinline__ void encode_token_head(const uint16_t* __restrict__ k_src,
-                                                  const uint16_t* __restrict__ v_src,
-                                                  uint8_t* __restrict__ k_cache,
-                                                  uint8_t* __restrict__ v_cache,
-                                                  void* __restrict__ scales, int num_blocks,
-                                                  int num_kv_heads, int block_size, int64_t block,
-                                                  int head, int offset, int lane) {
+__device__ __forceinline__ void encode_token_head_words(const RowWords<D>& kw,
+                                                        const RowWords<D>& vw,
+                                                        uint8_t* __restrict__ k_cache,
+                                                        uint8_t* __restrict__ v_cache,
+                                                        void* __restrict__ scales, int num_blocks,
+                                                        int num_kv_heads, int block_size,
+                                                        int64_t block, int head, int offset,
+                                                        int lane) {
   constexpr int EPL = D / kWarp;                       // elements per lane: 2 or 4
   const int64_t cache_row = (block * num_kv_heads + head) * block_size + offset;
 #pragma unroll
   for (int which = 0; which < 2; ++which) {
-    const uint16_t* src = (which ? v_src : k_src) + lane * EPL;
+    const RowWords<D>& words = which ? vw : kw;
     uint8_t* cache = which ? v_cache : k_cache;
     uint16_t raw[EPL];
-    if constexpr (EPL == 4) {
-      uint2 w = *reinterpret_cast<const uint2*>(src);
-      raw[0] = w.x & 0xFFFF; raw[1] = w.x >> 16; raw[2] = w.y & 0xFFFF; raw[3] = w.y >> 16;
-    } else {
-      uint32_t w = *reinterpret_cast<const uint32_t*>(src);
-      raw[0] = w & 0xFFFF; raw[1] = w >> 16;
+#pragma unroll
+    for (int e = 0; e < EPL / 2; ++e) {
+      raw[2 * e] = words.w[e] & 0xFFFF;
+      raw[2 * e + 1] = words.w[e] >> 16;
     }
 
     if constexpr (KV == PKV_F16 || KV == PKV_BF16) {
@@ -184,6 +201,22 @@ __device__ __forceinline__ void encode_token_head(const uint16_t* __restrict__ k
       }
     }
   }
+}
+
+// k_src / v_src: the token's rows for this head (D values of dtype NEW).
+// block, offset: where the token goes; cache_row = (block * Hkv + head) * bs + offset.
+template <int KV, int NEW, int D, int SRC = kScaleOwnRow>
+__device__ __forceinline__ void encode_token_head(const uint16_t* __restrict__ k_src,
+                                                  const uint16_t* __restrict__ v_src,
+                                                  uint8_t* __restrict__ k_cache,
+                                                  uint8_t* __restrict__ v_cache,
+                                                  void* __restrict__ scales, int num_blocks,
+                                                  int num_kv_heads, int block_size, int64_t block,
+                                                  int head, int offset, int lane) {
+  const RowWords<D> kw = load_row_words<D>(k_src, lane);
+  const RowWords<D> vw = load_row_words<D>(v_src, lane);
+  encode_token_head_words<KV, NEW, D, SRC>(kw, vw, k_cache, v_cache, scales, num_blocks,
+                                           num_kv_heads, block_size, block, head, offset, lane);
 }
 
 }  // namespace pkv

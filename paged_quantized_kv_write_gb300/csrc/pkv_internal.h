@@ -59,21 +59,19 @@ struct DecodeArgs {
 // Balanced split of the decode work (warp-owned, equal tile counts per warp):
 // at most kBalMaxSeqs sequences, at most kBalMaxWarps warps (152 SMs x 4 CTAs
 // x 4 warps).  Its workspace: partial rows [slots][G][D] floats, then
-// (max, sum) [slots][G][2], then the tile prefix [num_seqs + 1] ints, with
-// slots = kBalMaxWarps + num_seqs * num_kv_heads (each 256-byte aligned).
+// (max, sum) [slots][G][2], with slots = kBalMaxWarps + num_seqs *
+// num_kv_heads (the second part 256-byte aligned).
 constexpr int kBalMaxSeqs = 512;
 constexpr int kBalMaxWarps = 152 * 4 * 4;
 struct BalLayout {
-  size_t ml_off, pfx_off, bytes;
+  size_t ml_off, bytes;
 };
 inline BalLayout bal_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim) {
   const size_t slots = static_cast<size_t>(kBalMaxWarps) + static_cast<size_t>(num_seqs) * num_kv_heads;
   const size_t rows = slots * static_cast<size_t>(num_q_heads / num_kv_heads);
-  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   BalLayout L;
-  L.ml_off = up(rows * head_dim * 4);
-  L.pfx_off = L.ml_off + up(rows * 2 * 4);
-  L.bytes = L.pfx_off + (static_cast<size_t>(num_seqs) + 1) * 4;
+  L.ml_off = (rows * head_dim * 4 + 255) / 256 * 256;
+  L.bytes = L.ml_off + rows * 2 * 4;
   return L;
 }
 // whether a call may take the balanced split (the tile list must fit int)

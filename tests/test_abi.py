@@ -159,13 +159,11 @@ def test_partition_heuristic_and_workspace_for_the_benchmark_workloads(lib, cfg,
     want = (-(-out_bytes // 256)) * 256 + heads * np_ * 2 * 4
     # ... or the balanced split's layout when that is larger and the call may take
     # it: (2432 warp slots + one per (sequence, KV head)) x G rows of head_dim
-    # floats, then (max, sum) per row, then the tile prefix, each 256-byte aligned
+    # floats, then (max, sum) per row from a 256-byte boundary
     tiles = -(-mb * w.block_size // 16)
     if np_ > 1 and w.batch <= 512 and w.batch * w.num_kv_heads * tiles < 2**30:
-        up = lambda x: -(-x // 256) * 256                               # noqa: E731
         rows = (2432 + w.batch * w.num_kv_heads) * (w.num_q_heads // w.num_kv_heads)
-        ml_off = up(rows * w.head_dim * 4)
-        want = max(want, ml_off + up(rows * 2 * 4) + (w.batch + 1) * 4)
+        want = max(want, -(-(rows * w.head_dim * 4) // 256) * 256 + rows * 2 * 4)
     got = lib.lib.paged_decode_workspace_bytes(w.batch, w.num_q_heads, w.num_kv_heads,
                                                w.head_dim, mb, w.block_size, 0)
     assert got == want
