@@ -18,6 +18,11 @@
 // softmax as a decode step.
 #include "pkv_attn.cuh"
 
+// 16-bit caches on the warp-role tcgen05 kernel (1) or on prefill_tc_kernel (0)
+#ifndef PKV_PREFILL_WS
+#define PKV_PREFILL_WS 1
+#endif
+
 namespace pkv {
 namespace {
 
@@ -86,7 +91,11 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t st) {
   // 16-bit and one-byte caches run on the tcgen05 kernels (pkv_prefill_tc.cu);
   // PKV_PREFILL_MODE=mma keeps them on this one
   const char* mode = getenv("PKV_PREFILL_MODE");
-  if (prefill_tc_supported(a) && !(mode && !strcmp(mode, "mma"))) return launch_prefill_tc(a, st);
+  const bool mma = mode && !strcmp(mode, "mma");
+#if PKV_PREFILL_WS
+  if (prefill_ws_supported(a) && !mma) return launch_prefill_ws(a, st);
+#endif
+  if (prefill_tc_supported(a) && !mma) return launch_prefill_tc(a, st);
   switch (a.kv_dtype) {
     case PKV_F16: return launch_prefill_q<PKV_F16>(a, st);
     case PKV_BF16: return launch_prefill_q<PKV_BF16>(a, st);

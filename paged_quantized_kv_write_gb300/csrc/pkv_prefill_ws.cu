@@ -1,0 +1,679 @@
+// Chunked-prefill attention for 16-bit caches on the tcgen05 tensor cores,
+// with warp roles: the same computation as prefill_tc_kernel
+// (pkv_prefill_tc.cu; "Optimizing KV-Cache Memory Footprint in
+// High-Throughput LLM Serving", section 5: query j of a chunk of n over c
+// cached tokens sits at position c - n + j and sees tokens 0 .. c - n + j),
+// arranged so that the tensor cores and the softmax work at the same time.
+//
+// One CTA per SM (320 threads, all 512 tensor-memory columns) takes two
+// adjacent Q tiles of 128 query rows each -- 128/G query tokens of one
+// sequence times the G query heads of one KV head per tile -- and walks that
+// KV head's cache in 64-token tiles, K and V of a tile shared by both Q tiles:
+//  * load warp (warp 9): looks up the tile's four 16-token pieces in the block
+//    table and brings K and V into a ring of three (head_dim 64: four) stages
+//    with TMA tensor copies (a 16 x 64 box per piece and 128-byte column
+//    block, 128-byte swizzle), signalled on mbarriers by byte count.  The
+//    piece that straddles the end of the range has its V rows copied by the
+//    warp's lanes instead, with the rows past the end zero-filled, so that
+//    P = 0 never meets a non-finite value from an unwritten slot;
+//  * MMA warp (warp 8, one lane): S_A = Q_A K^T, then O_B += P_B V of the
+//    previous tile, then S_B = Q_B K^T, then O_A += P_A V, so that each
+//    softmax warpgroup works while the tensor cores serve the other tile;
+//    each batch is committed to an mbarrier;
+//  * softmax warpgroups (warps 0-3: tile A, 4-7: tile B): thread r reads row
+//    r of S from tensor memory, frees S for the next tile, applies the causal
+//    mask and the online softmax (running max raised lazily, by more than 2^8
+//    only, O rescaled in tensor memory when it is), writes row r of P as a
+//    16-bit hi + lo pair into tensor memory and signals the MMA warp.
+// Shared-memory operands use the canonical 128-byte-swizzle layouts: Q and K
+// K-major (rows of 128 bytes, 8-row atoms 1024 bytes apart, the second half
+// of head_dim 128 in its own region), V MN-major (token rows of 128 bytes, 8
+// tokens per atom, the two 64-value halves of head_dim 128 one region apart).
+// Every wait is bounded and also ends when another role has given up: the
+// launch then ORs PKV_ERR_DEVICE_TIMEOUT into dev_status, waits (bounded) for
+// its own copies and products in flight, writes zeros and frees its tensor
+// memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include <atomic>
+
+#include "pagedkv.h"
+#include "pkv_common.cuh"
+#include "pkv_internal.h"
+#include "pkv_tcgen05.cuh"
+
+namespace pkv {
+namespace {
+using namespace tc;
+
+constexpr int kWsRows = 128;                         // query rows per Q tile (the MMA M)
+constexpr int kWsKv = 64;                            // KV tokens per tile
+constexpr int kWsPiece = 16;                         // tokens per TMA box
+constexpr int kWsPieces = kWsKv / kWsPiece;
+constexpr int kWsMmaWarp = 8;
+constexpr int kWsLoadWarp = 9;
+constexpr int kWsThreads = 320;
+constexpr float kWsTau = 8.f;                        // lazy rescale threshold (log2 units)
+constexpr int kWsBoxBytes = kWsPiece * 128;          // one box: 16 rows of 128 bytes
+
+// Shared memory (operand regions 1024-byte aligned; V first, so that every
+// operand address stays low in the CTA's window) and tensor memory: Q tile i
+// owns columns [256 i, 256 i + 256): S [0, 64), P hi [64, 96), P lo [96, 128),
+// O [128, 128 + D).
+template <int D> struct WsPlan {
+  static constexpr int kHalves = D / 64;             // 128-byte column blocks per row
+  static constexpr int kStages = D == 128 ? 3 : 4;
+  static constexpr int kTileBytes = kWsKv * D * 2;   // one K or V tile
+  static constexpr int kKvHalf = kWsKv * 128;        // one column block of a K or V tile
+  static constexpr int kQBytes = kWsRows * D * 2;
+  static constexpr int kQHalf = kWsRows * 128;
+  static constexpr int kOffV = 0;
+  static constexpr int kOffK = kOffV + kStages * kTileBytes;
+  static constexpr int kOffQ = kOffK + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffQ + 2 * kQBytes;
+  // mbarriers: k_full, v_full, kv_empty per stage; q_full; s_full, s_free,
+  // p_full, o_done per Q tile; final.  Then the tensor-memory address and the
+  // abort flag.
+  static constexpr int kBarKFull = 0, kBarVFull = kStages, kBarEmpty = 2 * kStages;
+  static constexpr int kBarQ = 3 * kStages, kBarSFull = kBarQ + 1, kBarSFree = kBarSFull + 2;
+  static constexpr int kBarPFull = kBarSFree + 2, kBarODone = kBarPFull + 2;
+  static constexpr int kBarFinal = kBarODone + 2, kNumBars = kBarFinal + 1;
+  static constexpr int kOffSlot = kOffBar + 8 * kNumBars;
+  static constexpr int kSmem = kOffSlot + 16;
+  // one CTA per SM: it takes all of tensor memory, so the request is at least
+  // half of shared memory
+  static constexpr int kSmemRequest = kSmem > 120 * 1024 ? kSmem : 120 * 1024;
+  static_assert(kSmemRequest <= 232448, "shared memory");
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+struct WsParams {
+  CUtensorMap tmap_k;          // the cache as [num_blocks * Hkv][block_size][D] 16-bit values
+  CUtensorMap tmap_v;
+  const uint16_t* q;
+  const uint8_t* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* q_start;
+  void* out;
+  int* dev_status;
+  int max_query_len;
+  int max_blocks_per_seq;
+  int num_blocks;
+  int num_q_heads;
+  int num_kv_heads;
+  int block_size;
+  float softmax_scale;
+#ifdef PKV_TEST_HOOKS
+  int test_drop_commit;        // test of the bounded waits: tile A's first S is not committed
+#endif
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+// an arrival once this thread's earlier cp.async copies have landed (the
+// barrier's expected count includes it)
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+// one box of a 3-D tensor map into shared memory, completing bytes on `bar`
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Shared-memory descriptor of a 128-byte-swizzled operand: start address,
+// leading byte offset (MN-major: the next 64-value column block; unused for
+// K-major), stride byte offset 1024 (the next 8-row atom), version bit 46,
+// layout type 2 (128-byte swizzle) at bits 61-63.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
+// Bounded wait for phase `parity` that also ends when another role has set
+// the abort flag; a wait that runs out flags the timeout and sets the flag.
+__device__ __forceinline__ bool ws_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                        int* dev_status) {
+  const long long start = clock64();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try(bar, parity)) return true;
+    if ((i & 15) == 15 && *abort_flag) return false;
+    if (clock64() - start > kWaitCycles) {
+      flag_status(dev_status, PKV_ERR_DEVICE_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+// Bounded wait that ignores the abort flag (the clean-up waits for work in
+// flight); running out flags the timeout and the abort.
+__device__ __forceinline__ void ws_drain(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         int* dev_status) {
+  if (!mbar_wait(bar, parity)) {
+    flag_status(dev_status, PKV_ERR_DEVICE_TIMEOUT);
+    *abort_flag = 1;
+  }
+}
+
+template <int DT, int D>
+__global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_constant__ WsParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  using PL = WsPlan<D>;
+  constexpr int S = PL::kStages;
+  pdl_wait();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int group = p.num_q_heads / p.num_kv_heads;
+  const int qpb = kWsRows / group;                     // query tokens per Q tile
+  const int nq = p.q_start[b + 1] - p.q_start[b];
+  const int nqc = min(nq, p.max_query_len);            // queries computed
+  const int j0 = static_cast<int>(blockIdx.x) * 2 * qpb;   // tile A's first query, B's: j0 + qpb
+  if (j0 >= nqc) return;                                // whole CTA: no query here
+  const int cap = p.max_blocks_per_seq * p.block_size;
+  int ctx = p.context_lens[b];
+  if (ctx > cap) {
+    if (tid == 0 && blockIdx.x == 0 && kvh == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
+    ctx = cap;
+  }
+  const int pos0 = ctx - nq;                           // position of query 0 of the chunk
+  if (pos0 < 0 && j0 == 0 && tid == 0 && kvh == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
+  const int last_j = min(j0 + 2 * qpb, nqc) - 1;
+  const int kv_end = max(0, min(ctx, pos0 + last_j + 1));  // tokens any row of the CTA sees
+  const int nt = (kv_end + kWsKv - 1) / kWsKv;
+
+  const uint32_t sb = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sb + PL::kOffBar + 8 * i; };
+  volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(smem + PL::kOffSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + PL::kOffSlot + 4);
+
+  if (warp == kWsMmaWarp) {
+    tmem_alloc(sb + PL::kOffSlot, PL::kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar(PL::kBarKFull + s), 1);
+      mbar_init(bar(PL::kBarVFull + s), 1 + kWarp);     // the TMA bytes + the load warp's lanes
+      mbar_init(bar(PL::kBarEmpty + s), 1);
+    }
+    mbar_init(bar(PL::kBarQ), 8);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(PL::kBarSFull + i), 1);
+      mbar_init(bar(PL::kBarSFree + i), 4);
+      mbar_init(bar(PL::kBarPFull + i), 4);
+      mbar_init(bar(PL::kBarODone + i), 1);
+    }
+    mbar_init(bar(PL::kBarFinal), 1);
+    mbar_init_fence();
+    *abort_flag = 0;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  // softmax rows: warpgroup i = warp / 4 owns Q tile i, thread r its row r =
+  // query token ji + r / G, head r % G
+  const int qt = warp >> 2, r = tid & 127;
+  const int ji = j0 + qt * qpb;
+  const int jj = r / group, g = r % group;
+  const bool row_q = warp < 8 && ji + jj < nqc;
+  const int pos = pos0 + ji + jj;
+  const bool row_ok = row_q && pos >= 0;
+  const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+  const uint32_t t_s = tmem + lane_base + 256 * qt;    // S; P hi at + 64, lo at + 96; O at + 128
+  float l = 0.f;
+
+  if (warp < 8) {
+    // ------------------------------------------------------------ softmax
+    {
+      // Q row r of tile qt (128-byte swizzle; zeros for rows without a query)
+      const uint16_t* qrow =
+          p.q + ((static_cast<int64_t>(p.q_start[b]) + ji + (row_q ? jj : 0)) * p.num_q_heads +
+                 kvh * group + g) * D;
+      const uint32_t qbase = sb + PL::kOffQ + qt * PL::kQBytes + r * 128;
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        const uint32_t dst = qbase + (c >> 3) * PL::kQHalf + (((c & 7) ^ (r & 7)) << 4);
+        if (row_ok) cp_async_16(dst, qrow + 8 * c);
+        else st_shared_v4(dst, make_uint4(0, 0, 0, 0));
+      }
+      cp_async_wait_all();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(PL::kBarQ));
+    }
+    const float mult = p.softmax_scale * 1.4426950408889634f;
+    float m = -INFINITY;
+#pragma unroll 1
+    for (int t = 0; t < nt; ++t) {
+      const int t0 = t * kWsKv;
+      // 1. row r of S_qt(t), then S is free for the next tile's product
+      bool ok = ws_wait(bar(PL::kBarSFull + qt), t & 1, abort_flag, p.dev_status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      float s[kWsKv];
+      {
+        float a[32];
+        tmem_ld32(t_s, a);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[i] = a[i];
+        tmem_ld32(t_s + 32, a);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[32 + i] = a[i];
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(PL::kBarSFree + qt));
+      // 2. mask and scale (log2 units); tiles below the range end and below
+      //    every row's causal limit need no mask (scale in the exponent's fma)
+      const bool full = t0 + kWsKv <= kv_end && t0 + kWsKv - 1 <= pos0 + ji;
+      float tmax, pmul;
+      if (full) {
+        float e;
+        if (mult >= 0.f) {
+          e = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < kWsKv; ++c) e = fmaxf(e, s[c]);
+        } else {
+          e = INFINITY;
+#pragma unroll
+          for (int c = 0; c < kWsKv; ++c) e = fminf(e, s[c]);
+        }
+        tmax = e * mult;
+        pmul = mult;
+      } else {
+        tmax = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kWsKv; ++c) {
+          const int abs_t = t0 + c;
+          const bool valid = abs_t < kv_end && (!row_ok || abs_t <= pos);
+          s[c] = valid ? s[c] * mult : -INFINITY;
+          tmax = fmaxf(tmax, s[c]);
+        }
+        pmul = 1.f;
+      }
+      // 3. the previous P V of this tile has finished with O and P
+      if (t > 0) {
+        ok = ws_wait(bar(PL::kBarODone + qt), (t - 1) & 1, abort_flag, p.dev_status);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc_fence_after();
+      }
+      // 4. online softmax; the running max moves only past m + tau
+      const bool raise = tmax > m + kWsTau;
+      float alpha = 1.f;
+      if (raise) {
+        const float mn = fmaxf(m, tmax);
+        alpha = ex2_ftz(m - mn);
+        m = mn;
+        l *= alpha;
+      }
+      if (t > 0 && __any_sync(0xffffffffu, raise)) {    // rescale O (warp-collective)
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k) {
+          float o[32];
+          tmem_ld32(t_s + 128 + 32 * k, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(t_s + 128 + 32 * k, o);
+        }
+      }
+      // 5. P = 2^(s - m) as a 16-bit hi + lo pair into row r of the
+      //    tensor-memory A operand (two tokens per 32-bit column)
+#pragma unroll
+      for (int c8 = 0; c8 < kWsKv / 8; ++c8) {
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float p0 = ex2_ftz(fmaf(s[8 * c8 + 2 * k], pmul, -m));
+          const float p1 = ex2_ftz(fmaf(s[8 * c8 + 2 * k + 1], pmul, -m));
+          l += p0 + p1;
+          hw[k] = Half16<DT>::pack_rn(p0, p1);
+          const float2 f = Half16<DT>::unpack(hw[k]);
+          lw[k] = Half16<DT>::pack_rn(p0 - f.x, p1 - f.y);
+        }
+        tmem_st4(t_s + 64 + 4 * c8, hw[0], hw[1], hw[2], hw[3]);
+        tmem_st4(t_s + 96 + 4 * c8, lw[0], lw[1], lw[2], lw[3]);
+      }
+      tmem_store_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(PL::kBarPFull + qt));
+    }
+    // the last P V
+    if (nt > 0) ws_wait(bar(PL::kBarODone + qt), (nt - 1) & 1, abort_flag, p.dev_status);
+  } else if (warp == kWsMmaWarp) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr bool kBf = DT == PKV_BF16;
+      constexpr uint32_t kIdescS = umma_idesc(kBf, kWsRows, kWsKv, false);
+      constexpr uint32_t kIdescO = umma_idesc(kBf, kWsRows, D, true);
+      // S_i = Q_i K^T over head_dim in steps of 16 (32 bytes inside a
+      // 128-byte swizzle row; the second column block in its own region)
+      auto issue_s = [&](int i, int st) {
+        const uint32_t qb = sb + PL::kOffQ + i * PL::kQBytes;
+        const uint32_t kb = sb + PL::kOffK + st * PL::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk & 3) * 32;
+          umma(tmem + 256 * i, sw128_desc(qb + (kk >> 2) * PL::kQHalf + off, 16),
+               sw128_desc(kb + (kk >> 2) * PL::kKvHalf + off, 16), kIdescS, kk > 0);
+        }
+      };
+      // O_i += P_i V: 16 tokens per product (two 8-token atoms of V, 8
+      // tensor-memory columns of P), the hi part and then the lo part
+      auto issue_pv = [&](int i, int st, bool acc) {
+        const uint32_t vb = sb + PL::kOffV + st * PL::kTileBytes;
+        const uint32_t o = tmem + 256 * i + 128;
+#pragma unroll
+        for (int kk = 0; kk < kWsKv / 16; ++kk)
+          umma_ts(o, tmem + 256 * i + 64 + 8 * kk, sw128_desc(vb + kk * 2048, PL::kKvHalf), kIdescO,
+                  acc || kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kWsKv / 16; ++kk)
+          umma_ts(o, tmem + 256 * i + 96 + 8 * kk, sw128_desc(vb + kk * 2048, PL::kKvHalf), kIdescO,
+                  1u);
+      };
+      bool ok = nt == 0 || ws_wait(bar(PL::kBarQ), 0, abort_flag, p.dev_status);
+#pragma unroll 1
+      for (int t = 0; ok && t < nt; ++t) {
+        const int st = t % S;
+        const uint32_t ph = (t / S) & 1;
+        const int prev = (t + S - 1) % S;
+        // S_A(t)
+        if (!ws_wait(bar(PL::kBarKFull + st), ph, abort_flag, p.dev_status)) break;
+        if (t > 0 && !ws_wait(bar(PL::kBarSFree + 0), (t - 1) & 1, abort_flag, p.dev_status)) break;
+        tc_fence_after();
+        issue_s(0, st);
+#ifdef PKV_TEST_HOOKS
+        // (the test build's check of the bounded waits leaves the first S_A
+        // uncommitted: tile A's wait for it runs out)
+        if (!(p.test_drop_commit && t == 0)) umma_commit(bar(PL::kBarSFull + 0));
+#else
+        umma_commit(bar(PL::kBarSFull + 0));
+#endif
+        // O_B += P_B V(t - 1); then stage t - 1 is free
+        if (t > 0) {
+          if (!ws_wait(bar(PL::kBarPFull + 1), (t - 1) & 1, abort_flag, p.dev_status)) break;
+          tc_fence_after();
+          issue_pv(1, prev, t > 1);
+          umma_commit(bar(PL::kBarODone + 1));
+          umma_commit(bar(PL::kBarEmpty + prev));
+        }
+        // S_B(t)
+        if (t > 0 && !ws_wait(bar(PL::kBarSFree + 1), (t - 1) & 1, abort_flag, p.dev_status)) break;
+        tc_fence_after();
+        issue_s(1, st);
+        umma_commit(bar(PL::kBarSFull + 1));
+        // O_A += P_A V(t) (rows the load warp wrote itself: visible to the
+        // tensor cores after the proxy fence)
+        if (!ws_wait(bar(PL::kBarVFull + st), ph, abort_flag, p.dev_status)) break;
+        fence_proxy_async_smem();
+        if (!ws_wait(bar(PL::kBarPFull + 0), t & 1, abort_flag, p.dev_status)) break;
+        tc_fence_after();
+        issue_pv(0, st, t > 0);
+        umma_commit(bar(PL::kBarODone + 0));
+        if (t == nt - 1) {
+          if (!ws_wait(bar(PL::kBarPFull + 1), t & 1, abort_flag, p.dev_status)) break;
+          tc_fence_after();
+          issue_pv(1, st, t > 0);
+          umma_commit(bar(PL::kBarODone + 1));
+        }
+      }
+      // every product issued has finished before the tensor memory is read or freed
+      umma_commit(bar(PL::kBarFinal));
+      ws_drain(bar(PL::kBarFinal), 0, abort_flag, p.dev_status);
+    }
+    __syncwarp();
+  } else if (warp == kWsLoadWarp) {
+    // ------------------------------------------------------------ loads
+    const int nbh = p.num_blocks * p.num_kv_heads;      // the maps' outer extent
+    const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
+    int issued = 0;
+#pragma unroll 1
+    for (int t = 0; t < nt; ++t) {
+      const int st = t % S;
+      if (t >= S) {
+        const bool ok = ws_wait(bar(PL::kBarEmpty + st), ((t / S) - 1) & 1, abort_flag, p.dev_status);
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
+      // lane j < 4 locates piece j (tokens t0 + 16 j ..): z = physical block *
+      // Hkv + kvh, y = offset in the block; past the range or in an
+      // out-of-range block, z = nbh, which the copies read as zeros
+      int z = nbh, y = 0, strad = 0;
+      if (lane < kWsPieces) {
+        const int tok = t * kWsKv + lane * kWsPiece;
+        if (tok < kv_end) {
+          const int logical = tok / p.block_size;
+          const int phys = __ldg(trow + logical);
+          if (phys >= 0 && phys < p.num_blocks) {
+            z = phys * p.num_kv_heads + kvh;
+            y = tok - logical * p.block_size;
+            strad = tok + kWsPiece > kv_end;
+          } else {
+            flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
+          }
+        }
+      }
+      int pz[kWsPieces], py[kWsPieces], ps[kWsPieces], nstrad = 0;
+#pragma unroll
+      for (int j = 0; j < kWsPieces; ++j) {
+        pz[j] = __shfl_sync(0xffffffffu, z, j);
+        py[j] = __shfl_sync(0xffffffffu, y, j);
+        ps[j] = __shfl_sync(0xffffffffu, strad, j);
+        nstrad += ps[j];
+      }
+      const uint32_t kst = sb + PL::kOffK + st * PL::kTileBytes;
+      const uint32_t vst = sb + PL::kOffV + st * PL::kTileBytes;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(PL::kBarKFull + st), kWsPieces * PL::kHalves * kWsBoxBytes);
+#pragma unroll
+        for (int j = 0; j < kWsPieces; ++j)
+#pragma unroll
+          for (int h = 0; h < PL::kHalves; ++h)
+            tma_load_3d(kst + h * PL::kKvHalf + j * kWsBoxBytes, &p.tmap_k, 64 * h, py[j], pz[j],
+                        bar(PL::kBarKFull + st));
+        mbar_arrive_expect_tx(bar(PL::kBarVFull + st),
+                              (kWsPieces - nstrad) * PL::kHalves * kWsBoxBytes);
+#pragma unroll
+        for (int j = 0; j < kWsPieces; ++j)
+          if (!ps[j])
+#pragma unroll
+            for (int h = 0; h < PL::kHalves; ++h)
+              tma_load_3d(vst + h * PL::kKvHalf + j * kWsBoxBytes, &p.tmap_v, 64 * h, py[j], pz[j],
+                          bar(PL::kBarVFull + st));
+      }
+      // the straddling piece's V rows, copied by the lanes in the same
+      // swizzled layout, rows past the range end zero-filled
+#pragma unroll
+      for (int j = 0; j < kWsPieces; ++j) {
+        if (!ps[j]) continue;
+        const int tok0 = t * kWsKv + j * kWsPiece;
+        const uint8_t* src0 =
+            p.v_cache + (static_cast<int64_t>(pz[j]) * p.block_size + py[j]) * (D * 2);
+        for (int idx = lane; idx < kWsPiece * (D / 8); idx += kWarp) {
+          const int rr = idx / (D / 8), c = idx % (D / 8);
+          const int row = j * kWsPiece + rr;
+          const uint32_t dst = vst + (c >> 3) * PL::kKvHalf + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+          const bool valid = tok0 + rr < kv_end;
+          cp_async_16_zfill(dst, valid ? src0 + rr * (D * 2) + c * 16 : p.v_cache, valid ? 16u : 0u);
+        }
+      }
+      cp_async_arrive_noinc(bar(PL::kBarVFull + st));
+      issued = t + 1;
+    }
+    // the copies still in flight land before the CTA ends: the last fill of each stage
+    cp_async_wait_all();
+    if (lane == 0) {
+      for (int st = 0; st < S; ++st) {
+        const int fills = issued > st ? (issued - st + S - 1) / S : 0;
+        if (fills > 0) {
+          ws_drain(bar(PL::kBarKFull + st), (fills - 1) & 1, abort_flag, p.dev_status);
+          ws_drain(bar(PL::kBarVFull + st), (fills - 1) & 1, abort_flag, p.dev_status);
+        }
+      }
+    }
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------ output
+  __syncthreads();
+  const bool all_ok = *abort_flag == 0;
+  if (warp < 8) {
+    tc_fence_after();
+    uint16_t* orow = static_cast<uint16_t*>(p.out) +
+                     ((static_cast<int64_t>(p.q_start[b]) + ji + jj) * p.num_q_heads +
+                      kvh * group + g) * D;
+    if (all_ok && nt > 0) {
+      const float inv = (row_ok && l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+      for (int k = 0; k < D / 32; ++k) {
+        float o[32];
+        tmem_ld32(t_s + 128 + 32 * k, o);                // warp-collective: every row
+        if (row_q) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint4 w;
+            w.x = Half16<DT>::pack_rn(o[8 * c] * inv, o[8 * c + 1] * inv);
+            w.y = Half16<DT>::pack_rn(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
+            w.z = Half16<DT>::pack_rn(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
+            w.w = Half16<DT>::pack_rn(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+            reinterpret_cast<uint4*>(orow + 32 * k)[c] = w;
+          }
+        }
+      }
+    } else if (row_q) {
+      for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWsMmaWarp) tmem_dealloc(tmem, PL::kTmemCols);
+  pdl_launch_dependents();
+}
+
+// ---------------------------------------------------------------- host side
+using EncodeTiled = PFN_cuTensorMapEncodeTiled_v12000;
+
+// cuTensorMapEncodeTiled, taken from the driver once
+EncodeTiled encode_tiled() {
+  static std::atomic<EncodeTiled> fn{nullptr};
+  EncodeTiled f = fn.load(std::memory_order_acquire);
+  if (f == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess && ptr != nullptr) {
+      f = reinterpret_cast<EncodeTiled>(ptr);
+      fn.store(f, std::memory_order_release);
+    }
+  }
+  return f;
+}
+
+// The cache [num_blocks][Hkv][block_size][D] of 16-bit values as a 3-D tensor
+// (D, block_size, num_blocks * Hkv), read in boxes of 64 values x 16 rows with
+// the 128-byte swizzle; boxes outside it read as zeros.
+bool cache_map(CUtensorMap* map, const void* cache, int num_blocks, int num_kv_heads,
+               int block_size, int head_dim) {
+  const EncodeTiled enc = encode_tiled();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(block_size),
+                              static_cast<cuuint64_t>(num_blocks) * num_kv_heads};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                                 static_cast<cuuint64_t>(block_size) * head_dim * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kWsPiece), 1};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(cache), dims, strides, box,
+             elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int DT, int D>
+cudaError_t launch_ws_t(const PrefillArgs& a, cudaStream_t st) {
+  using PL = WsPlan<D>;
+  WsParams p;
+  if (!cache_map(&p.tmap_k, a.k_cache, a.num_blocks, a.num_kv_heads, a.block_size, D) ||
+      !cache_map(&p.tmap_v, a.v_cache, a.num_blocks, a.num_kv_heads, a.block_size, D))
+    return cudaErrorInvalidValue;
+  p.q = static_cast<const uint16_t*>(a.q);
+  p.v_cache = static_cast<const uint8_t*>(a.v_cache);
+  p.block_tables = a.block_tables;
+  p.context_lens = a.context_lens;
+  p.q_start = a.q_start;
+  p.out = a.out;
+  p.dev_status = a.dev_status;
+  p.max_query_len = a.max_query_len;
+  p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.num_blocks = a.num_blocks;
+  p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.block_size = a.block_size;
+  p.softmax_scale = a.softmax_scale;
+#ifdef PKV_TEST_HOOKS
+  p.test_drop_commit = getenv("PKV_TEST_DROP_COMMIT") != nullptr;
+#endif
+  auto kern = prefill_ws_kernel<DT, D>;
+  static std::atomic<int> attr_set[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev].load(std::memory_order_relaxed)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PL::kSmemRequest);
+    if (e != cudaSuccess) return e;
+    attr_set[dev].store(1, std::memory_order_relaxed);
+  }
+  const int group = a.num_q_heads / a.num_kv_heads;
+  const int rows = 2 * (kWsRows / group);               // query tokens per CTA
+  const dim3 grid(static_cast<unsigned>((a.max_query_len + rows - 1) / rows),
+                  static_cast<unsigned>(a.num_kv_heads), static_cast<unsigned>(a.num_seqs));
+  return launch_pdl(kern, grid, dim3(kWsThreads), PL::kSmemRequest, st, p);
+}
+
+}  // namespace
+
+bool prefill_ws_supported(const PrefillArgs& a) {
+  return (a.kv_dtype == PKV_F16 || a.kv_dtype == PKV_BF16) && (a.head_dim == 64 || a.head_dim == 128);
+}
+
+cudaError_t launch_prefill_ws(const PrefillArgs& a, cudaStream_t st) {
+  if (a.num_seqs == 0 || a.max_query_len == 0) return cudaSuccess;
+  if (a.kv_dtype == PKV_F16)
+    return a.head_dim == 64 ? launch_ws_t<PKV_F16, 64>(a, st) : launch_ws_t<PKV_F16, 128>(a, st);
+  return a.head_dim == 64 ? launch_ws_t<PKV_BF16, 64>(a, st) : launch_ws_t<PKV_BF16, 128>(a, st);
+}
+
+}  // namespace pkv
