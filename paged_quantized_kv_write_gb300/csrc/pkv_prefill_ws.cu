@@ -8,9 +8,9 @@
 // One CTA per SM (320 threads, all 512 tensor-memory columns) takes two
 // adjacent Q tiles of 128 query rows each -- 128/G query tokens of one
 // sequence times the G query heads of one KV head per tile -- and walks that
-// KV head's cache in 64-token tiles, K and V of a tile shared by both Q tiles:
-//  * load warp (warp 9): looks up the tile's four 16-token pieces in the block
-//    table and brings K and V into a ring of three (head_dim 64: four) stages
+// KV head's cache in 128-token tiles, K and V of a tile shared by both Q tiles:
+//  * load warp (warp 9): looks up the tile's eight 16-token pieces in the block
+//    table and brings K and V into rings of two (head_dim 64: three) stages
 //    with TMA tensor copies (a 16 x 64 box per piece and 128-byte column
 //    block, 128-byte swizzle), signalled on mbarriers by byte count.  The
 //    piece that straddles the end of the range has its V rows copied by the
@@ -19,12 +19,16 @@
 //  * MMA warp (warp 8, one lane): S_A = Q_A K^T, then O_B += P_B V of the
 //    previous tile, then S_B = Q_B K^T, then O_A += P_A V, so that each
 //    softmax warpgroup works while the tensor cores serve the other tile;
-//    each batch is committed to an mbarrier;
+//    each batch is committed to an mbarrier.  Products of N = 128 (S over
+//    128 tokens, O over head_dim 128) keep the tensor cores' work per
+//    instruction large;
 //  * softmax warpgroups (warps 0-3: tile A, 4-7: tile B): thread r reads row
-//    r of S from tensor memory, frees S for the next tile, applies the causal
-//    mask and the online softmax (running max raised lazily, by more than 2^8
-//    only, O rescaled in tensor memory when it is), writes row r of P as a
-//    16-bit hi + lo pair into tensor memory and signals the MMA warp.
+//    r of S from tensor memory, applies the causal mask and the online
+//    softmax (running max raised lazily, by more than 2^8 only, O rescaled in
+//    tensor memory when it is), writes row r of P as a 16-bit hi + lo pair
+//    over S's own columns and signals the MMA warp.  The tensor cores run a
+//    thread's products in issue order, so S(t + 1), issued after P V(t),
+//    overwrites P(t) only after that product has read it.
 // Shared-memory operands use the canonical 128-byte-swizzle layouts: Q and K
 // K-major (rows of 128 bytes, 8-row atoms 1024 bytes apart, the second half
 // of head_dim 128 in its own region), V MN-major (token rows of 128 bytes, 8
@@ -51,7 +55,7 @@ namespace {
 using namespace tc;
 
 constexpr int kWsRows = 128;                         // query rows per Q tile (the MMA M)
-constexpr int kWsKv = 64;                            // KV tokens per tile
+constexpr int kWsKv = 128;                           // KV tokens per tile
 constexpr int kWsPiece = 16;                         // tokens per TMA box
 constexpr int kWsPieces = kWsKv / kWsPiece;
 constexpr int kWsMmaWarp = 8;
@@ -62,11 +66,12 @@ constexpr int kWsBoxBytes = kWsPiece * 128;          // one box: 16 rows of 128 
 
 // Shared memory (operand regions 1024-byte aligned; V first, so that every
 // operand address stays low in the CTA's window) and tensor memory: Q tile i
-// owns columns [256 i, 256 i + 256): S [0, 64), P hi [64, 96), P lo [96, 128),
-// O [128, 128 + D).
+// owns columns [256 i, 256 i + 256): S [0, 128), overwritten by P (tokens
+// 32c .. 32c + 31: hi at columns 32c .. 32c + 15, lo at 32c + 16 .. 32c + 31),
+// and O [128, 128 + D).
 template <int D> struct WsPlan {
   static constexpr int kHalves = D / 64;             // 128-byte column blocks per row
-  static constexpr int kStages = D == 128 ? 3 : 4;
+  static constexpr int kStages = D == 128 ? 2 : 3;
   static constexpr int kTileBytes = kWsKv * D * 2;   // one K or V tile
   static constexpr int kKvHalf = kWsKv * 128;        // one column block of a K or V tile
   static constexpr int kQBytes = kWsRows * D * 2;
@@ -75,12 +80,13 @@ template <int D> struct WsPlan {
   static constexpr int kOffK = kOffV + kStages * kTileBytes;
   static constexpr int kOffQ = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffQ + 2 * kQBytes;
-  // mbarriers: k_full, v_full, kv_empty per stage; q_full; s_full, s_free,
+  // mbarriers: k_full, v_full, k_empty, v_empty per stage; q_full; s_full,
   // p_full, o_done per Q tile; final.  Then the tensor-memory address and the
   // abort flag.
-  static constexpr int kBarKFull = 0, kBarVFull = kStages, kBarEmpty = 2 * kStages;
-  static constexpr int kBarQ = 3 * kStages, kBarSFull = kBarQ + 1, kBarSFree = kBarSFull + 2;
-  static constexpr int kBarPFull = kBarSFree + 2, kBarODone = kBarPFull + 2;
+  static constexpr int kBarKFull = 0, kBarVFull = kStages, kBarKEmpty = 2 * kStages;
+  static constexpr int kBarVEmpty = 3 * kStages;
+  static constexpr int kBarQ = 4 * kStages, kBarSFull = kBarQ + 1;
+  static constexpr int kBarPFull = kBarSFull + 2, kBarODone = kBarPFull + 2;
   static constexpr int kBarFinal = kBarODone + 2, kNumBars = kBarFinal + 1;
   static constexpr int kOffSlot = kOffBar + 8 * kNumBars;
   static constexpr int kSmem = kOffSlot + 16;
@@ -186,6 +192,58 @@ __device__ __forceinline__ void ws_drain(uint32_t bar, uint32_t parity, volatile
   }
 }
 
+// 128 consecutive fp32 columns of this thread's tensor-memory lane in one
+// load, and its wait (the registers are defined only after both)
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[kWsKv]) {
+  uint32_t r[128];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]),
+        "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]),
+        "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]),
+        "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]),
+        "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]),
+        "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]),
+        "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]),
+        "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]),
+        "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// The largest of a row's 128 scores, and the largest of their negations, as
+// pairwise trees (seven dependent steps instead of 128)
+__device__ __forceinline__ float row_max(const float (&s)[kWsKv]) {
+  float v[kWsKv / 2];
+#pragma unroll
+  for (int i = 0; i < kWsKv / 2; ++i) v[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+  for (int n = kWsKv / 4; n >= 1; n >>= 1)
+#pragma unroll
+    for (int i = 0; i < n; ++i) v[i] = fmaxf(v[2 * i], v[2 * i + 1]);
+  return v[0];
+}
+__device__ __forceinline__ float row_max_neg(const float (&s)[kWsKv]) {
+  float v[kWsKv / 2];
+#pragma unroll
+  for (int i = 0; i < kWsKv / 2; ++i) v[i] = fmaxf(-s[2 * i], -s[2 * i + 1]);
+#pragma unroll
+  for (int n = kWsKv / 4; n >= 1; n >>= 1)
+#pragma unroll
+    for (int i = 0; i < n; ++i) v[i] = fmaxf(v[2 * i], v[2 * i + 1]);
+  return v[0];
+}
+
 template <int DT, int D>
 __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_constant__ WsParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -225,12 +283,12 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
     for (int s = 0; s < S; ++s) {
       mbar_init(bar(PL::kBarKFull + s), 1);
       mbar_init(bar(PL::kBarVFull + s), 1 + kWarp);     // the TMA bytes + the load warp's lanes
-      mbar_init(bar(PL::kBarEmpty + s), 1);
+      mbar_init(bar(PL::kBarKEmpty + s), 1);
+      mbar_init(bar(PL::kBarVEmpty + s), 1);
     }
     mbar_init(bar(PL::kBarQ), 8);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(PL::kBarSFull + i), 1);
-      mbar_init(bar(PL::kBarSFree + i), 4);
       mbar_init(bar(PL::kBarPFull + i), 4);
       mbar_init(bar(PL::kBarODone + i), 1);
     }
@@ -252,7 +310,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
   const int pos = pos0 + ji + jj;
   const bool row_ok = row_q && pos >= 0;
   const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-  const uint32_t t_s = tmem + lane_base + 256 * qt;    // S; P hi at + 64, lo at + 96; O at + 128
+  const uint32_t t_s = tmem + lane_base + 256 * qt;    // S and P; O at + 128
   float l = 0.f;
 
   if (warp < 8) {
@@ -279,58 +337,32 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
 #pragma unroll 1
     for (int t = 0; t < nt; ++t) {
       const int t0 = t * kWsKv;
-      // 1. row r of S_qt(t), then S is free for the next tile's product
+      // 1. row r of S_qt(t)
       bool ok = ws_wait(bar(PL::kBarSFull + qt), t & 1, abort_flag, p.dev_status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      float s[kWsKv];
-      {
-        float a[32];
-        tmem_ld32(t_s, a);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[i] = a[i];
-        tmem_ld32(t_s + 32, a);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[32 + i] = a[i];
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(PL::kBarSFree + qt));
-      // 2. mask and scale (log2 units); tiles below the range end and below
-      //    every row's causal limit need no mask (scale in the exponent's fma)
+      // 2. row r of S in registers (one load of all 128 columns), scaled to
+      //    log2 units and masked where needed (tiles below the range end and
+      //    below every row's causal limit need no mask; the scale then goes
+      //    into the exponent's fma), and its largest value
+      float sv[kWsKv];
+      tmem_ld128(t_s, sv);
       const bool full = t0 + kWsKv <= kv_end && t0 + kWsKv - 1 <= pos0 + ji;
       float tmax, pmul;
       if (full) {
-        float e;
-        if (mult >= 0.f) {
-          e = -INFINITY;
-#pragma unroll
-          for (int c = 0; c < kWsKv; ++c) e = fmaxf(e, s[c]);
-        } else {
-          e = INFINITY;
-#pragma unroll
-          for (int c = 0; c < kWsKv; ++c) e = fminf(e, s[c]);
-        }
-        tmax = e * mult;
+        // (a negative scale turns the row's smallest score into its largest)
+        tmax = (mult >= 0.f ? row_max(sv) : -row_max_neg(sv)) * mult;
         pmul = mult;
       } else {
-        tmax = -INFINITY;
 #pragma unroll
         for (int c = 0; c < kWsKv; ++c) {
           const int abs_t = t0 + c;
-          const bool valid = abs_t < kv_end && (!row_ok || abs_t <= pos);
-          s[c] = valid ? s[c] * mult : -INFINITY;
-          tmax = fmaxf(tmax, s[c]);
+          sv[c] = abs_t < kv_end && (!row_ok || abs_t <= pos) ? sv[c] * mult : -INFINITY;
         }
+        tmax = row_max(sv);
         pmul = 1.f;
       }
-      // 3. the previous P V of this tile has finished with O and P
-      if (t > 0) {
-        ok = ws_wait(bar(PL::kBarODone + qt), (t - 1) & 1, abort_flag, p.dev_status);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        tc_fence_after();
-      }
-      // 4. online softmax; the running max moves only past m + tau
+      // 3. online softmax; the running max moves only past m + tau
       const bool raise = tmax > m + kWsTau;
       float alpha = 1.f;
       if (raise) {
@@ -339,32 +371,53 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
         m = mn;
         l *= alpha;
       }
-      if (t > 0 && __any_sync(0xffffffffu, raise)) {    // rescale O (warp-collective)
-#pragma unroll
-        for (int k = 0; k < D / 32; ++k) {
-          float o[32];
-          tmem_ld32(t_s + 128 + 32 * k, o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st32(t_s + 128 + 32 * k, o);
-        }
-      }
-      // 5. P = 2^(s - m) as a 16-bit hi + lo pair into row r of the
-      //    tensor-memory A operand (two tokens per 32-bit column)
+      // 4. P = 2^(s - m) as a 16-bit hi + lo pair over row r's S columns
+      //    (two tokens per 32-bit column; tokens 32c .. 32c + 31: hi at
+      //    columns 32c .. 32c + 15, lo at 32c + 16 .. 32c + 31); exponent
+      //    arguments, the lo parts and the row sum on packed fp32 pairs, the
+      //    sum in two interleaved chains
+      const uint64_t pm2 = f2_pack(pmul, pmul), nm2 = f2_pack(-m, -m);
+      uint64_t lsum[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
       for (int c8 = 0; c8 < kWsKv / 8; ++c8) {
         uint32_t hw[4], lw[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float p0 = ex2_ftz(fmaf(s[8 * c8 + 2 * k], pmul, -m));
-          const float p1 = ex2_ftz(fmaf(s[8 * c8 + 2 * k + 1], pmul, -m));
-          l += p0 + p1;
-          hw[k] = Half16<DT>::pack_rn(p0, p1);
+          const int i = 8 * c8 + 2 * k;
+          const float2 x = f2_unpack(f2_fma(f2_pack(sv[i], sv[i + 1]), pm2, nm2));
+          const uint64_t pp = f2_pack(ex2_ftz(x.x), ex2_ftz(x.y));
+          lsum[k & 1] = f2_add(lsum[k & 1], pp);
+          const float2 pf = f2_unpack(pp);
+          hw[k] = Half16<DT>::pack_rn(pf.x, pf.y);
           const float2 f = Half16<DT>::unpack(hw[k]);
-          lw[k] = Half16<DT>::pack_rn(p0 - f.x, p1 - f.y);
+          const float2 d = f2_unpack(f2_sub(pp, f2_pack(f.x, f.y)));
+          lw[k] = Half16<DT>::pack_rn(d.x, d.y);
         }
-        tmem_st4(t_s + 64 + 4 * c8, hw[0], hw[1], hw[2], hw[3]);
-        tmem_st4(t_s + 96 + 4 * c8, lw[0], lw[1], lw[2], lw[3]);
+        // tokens 8 c8 .. 8 c8 + 7: chunk c8 / 4 of 32 tokens, its 4-column group c8 % 4
+        const uint32_t col = 32 * (c8 >> 2) + 4 * (c8 & 3);
+        tmem_st4(t_s + col, hw[0], hw[1], hw[2], hw[3]);
+        tmem_st4(t_s + col + 16, lw[0], lw[1], lw[2], lw[3]);
+      }
+      {
+        const float2 a = f2_unpack(lsum[0]), c = f2_unpack(lsum[1]);
+        l += (a.x + a.y) + (c.x + c.y);
+      }
+      // 5. O rescaled when the max rose, once the previous P V of this tile
+      //    has finished with it (S(t) was computed after it, so it has)
+      if (t > 0) {
+        ok = ws_wait(bar(PL::kBarODone + qt), (t - 1) & 1, abort_flag, p.dev_status);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, raise)) {           // warp-collective
+#pragma unroll
+          for (int k = 0; k < D / 32; ++k) {
+            float o[32];
+            tmem_ld32(t_s + 128 + 32 * k, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(t_s + 128 + 32 * k, o);
+          }
+        }
       }
       tmem_store_wait();
       tc_fence_before();
@@ -392,18 +445,20 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
         }
       };
       // O_i += P_i V: 16 tokens per product (two 8-token atoms of V, 8
-      // tensor-memory columns of P), the hi part and then the lo part
+      // tensor-memory columns of P: tokens 16kk .. sit at column
+      // 32 (kk / 2) + 8 (kk % 2), their lo parts 16 columns on), the hi part
+      // and then the lo part
       auto issue_pv = [&](int i, int st, bool acc) {
         const uint32_t vb = sb + PL::kOffV + st * PL::kTileBytes;
         const uint32_t o = tmem + 256 * i + 128;
 #pragma unroll
         for (int kk = 0; kk < kWsKv / 16; ++kk)
-          umma_ts(o, tmem + 256 * i + 64 + 8 * kk, sw128_desc(vb + kk * 2048, PL::kKvHalf), kIdescO,
-                  acc || kk > 0);
+          umma_ts(o, tmem + 256 * i + 32 * (kk >> 1) + 8 * (kk & 1),
+                  sw128_desc(vb + kk * 2048, PL::kKvHalf), kIdescO, acc || kk > 0);
 #pragma unroll
         for (int kk = 0; kk < kWsKv / 16; ++kk)
-          umma_ts(o, tmem + 256 * i + 96 + 8 * kk, sw128_desc(vb + kk * 2048, PL::kKvHalf), kIdescO,
-                  1u);
+          umma_ts(o, tmem + 256 * i + 32 * (kk >> 1) + 16 + 8 * (kk & 1),
+                  sw128_desc(vb + kk * 2048, PL::kKvHalf), kIdescO, 1u);
       };
       bool ok = nt == 0 || ws_wait(bar(PL::kBarQ), 0, abort_flag, p.dev_status);
 #pragma unroll 1
@@ -411,9 +466,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
         const int st = t % S;
         const uint32_t ph = (t / S) & 1;
         const int prev = (t + S - 1) % S;
-        // S_A(t)
+        // S_A(t) (over P_A(t - 1), whose product was issued before)
         if (!ws_wait(bar(PL::kBarKFull + st), ph, abort_flag, p.dev_status)) break;
-        if (t > 0 && !ws_wait(bar(PL::kBarSFree + 0), (t - 1) & 1, abort_flag, p.dev_status)) break;
         tc_fence_after();
         issue_s(0, st);
 #ifdef PKV_TEST_HOOKS
@@ -423,19 +477,18 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
 #else
         umma_commit(bar(PL::kBarSFull + 0));
 #endif
-        // O_B += P_B V(t - 1); then stage t - 1 is free
+        // O_B += P_B V(t - 1); then V of tile t - 1 is free
         if (t > 0) {
           if (!ws_wait(bar(PL::kBarPFull + 1), (t - 1) & 1, abort_flag, p.dev_status)) break;
           tc_fence_after();
           issue_pv(1, prev, t > 1);
           umma_commit(bar(PL::kBarODone + 1));
-          umma_commit(bar(PL::kBarEmpty + prev));
+          umma_commit(bar(PL::kBarVEmpty + prev));
         }
-        // S_B(t)
-        if (t > 0 && !ws_wait(bar(PL::kBarSFree + 1), (t - 1) & 1, abort_flag, p.dev_status)) break;
-        tc_fence_after();
+        // S_B(t) (over P_B(t - 1)); then K of tile t is free
         issue_s(1, st);
         umma_commit(bar(PL::kBarSFull + 1));
+        umma_commit(bar(PL::kBarKEmpty + st));
         // O_A += P_A V(t) (rows the load warp wrote itself: visible to the
         // tensor cores after the proxy fence)
         if (!ws_wait(bar(PL::kBarVFull + st), ph, abort_flag, p.dev_status)) break;
@@ -460,15 +513,16 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
     // ------------------------------------------------------------ loads
     const int nbh = p.num_blocks * p.num_kv_heads;      // the maps' outer extent
     const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
-    int issued = 0;
+    int k_issued = 0, v_issued = 0;                     // tiles whose K / V copies were issued
 #pragma unroll 1
     for (int t = 0; t < nt; ++t) {
       const int st = t % S;
+      // K of tile t - S has been used by both S products
       if (t >= S) {
-        const bool ok = ws_wait(bar(PL::kBarEmpty + st), ((t / S) - 1) & 1, abort_flag, p.dev_status);
+        const bool ok = ws_wait(bar(PL::kBarKEmpty + st), ((t / S) - 1) & 1, abort_flag, p.dev_status);
         if (!__all_sync(0xffffffffu, ok)) break;
       }
-      // lane j < 4 locates piece j (tokens t0 + 16 j ..): z = physical block *
+      // lane j < 8 locates piece j (tokens t0 + 16 j ..): z = physical block *
       // Hkv + kvh, y = offset in the block; past the range or in an
       // out-of-range block, z = nbh, which the copies read as zeros
       int z = nbh, y = 0, strad = 0;
@@ -504,6 +558,14 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
           for (int h = 0; h < PL::kHalves; ++h)
             tma_load_3d(kst + h * PL::kKvHalf + j * kWsBoxBytes, &p.tmap_k, 64 * h, py[j], pz[j],
                         bar(PL::kBarKFull + st));
+      }
+      k_issued = t + 1;
+      // V of tile t - S has been used by both P V products
+      if (t >= S) {
+        const bool ok = ws_wait(bar(PL::kBarVEmpty + st), ((t / S) - 1) & 1, abort_flag, p.dev_status);
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
+      if (lane == 0) {
         mbar_arrive_expect_tx(bar(PL::kBarVFull + st),
                               (kWsPieces - nstrad) * PL::kHalves * kWsBoxBytes);
 #pragma unroll
@@ -531,17 +593,16 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
         }
       }
       cp_async_arrive_noinc(bar(PL::kBarVFull + st));
-      issued = t + 1;
+      v_issued = t + 1;
     }
     // the copies still in flight land before the CTA ends: the last fill of each stage
     cp_async_wait_all();
     if (lane == 0) {
       for (int st = 0; st < S; ++st) {
-        const int fills = issued > st ? (issued - st + S - 1) / S : 0;
-        if (fills > 0) {
-          ws_drain(bar(PL::kBarKFull + st), (fills - 1) & 1, abort_flag, p.dev_status);
-          ws_drain(bar(PL::kBarVFull + st), (fills - 1) & 1, abort_flag, p.dev_status);
-        }
+        const int kf = k_issued > st ? (k_issued - st + S - 1) / S : 0;
+        const int vf = v_issued > st ? (v_issued - st + S - 1) / S : 0;
+        if (kf > 0) ws_drain(bar(PL::kBarKFull + st), (kf - 1) & 1, abort_flag, p.dev_status);
+        if (vf > 0) ws_drain(bar(PL::kBarVFull + st), (vf - 1) & 1, abort_flag, p.dev_status);
       }
     }
     __syncwarp();
@@ -551,6 +612,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
   __syncthreads();
   const bool all_ok = *abort_flag == 0;
   if (warp < 8) {
+    tmem_store_wait();                                   // (a launch that gave up mid-tile)
     tc_fence_after();
     uint16_t* orow = static_cast<uint16_t*>(p.out) +
                      ((static_cast<int64_t>(p.q_start[b]) + ji + jj) * p.num_q_heads +
