@@ -635,6 +635,15 @@ def run_copy(args, rank: int, world: int):
     }
 
 
+def _prefill_kernel_name(kv_dtype: int) -> str:
+    """The kernel paged_prefill_attention runs for this cache dtype."""
+    if os.environ.get("PKV_PREFILL_MODE") == "mma" or kv_dtype == W.INT4_G32:
+        return "paged_decode_kernel (prefill mode, mma.sync)"
+    if kv_dtype in (W.F16, W.BF16):
+        return "prefill_ws_kernel (tcgen05, load / MMA / softmax warp roles)"
+    return "prefill_tc8_kernel (tcgen05)"
+
+
 def run_prefill(args, rank: int, world: int):
     """Chunked prefill: time paged_prefill_attention on the prefill workload (8
     sequences of 4096 cached tokens, chunks of their last 512, Llama-3-8B-shaped)."""
@@ -712,7 +721,7 @@ def run_prefill(args, rank: int, world: int):
                                f"{max(chunk)} over {int(case.context_lens.max())}-token contexts",
                    "query_tokens": int(q_start[-1]), "flops_per_step": flops,
                    "kv_bytes_per_step": kv_bytes},
-        "roofline": {"kernel": "paged_decode_kernel (prefill mode, mma.sync)", "bound": "tensor",
+        "roofline": {"kernel": _prefill_kernel_name(w.kv_dtype), "bound": "tensor",
                      "achieved": round(tflops / world, 2), "peak": peak,
                      "peak_kind": f"{kind} (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)",
                      "unit": "TFLOP/s", "frac": round(tflops / world / peak, 4), "traffic": None},

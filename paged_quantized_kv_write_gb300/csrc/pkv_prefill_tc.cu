@@ -1,22 +1,19 @@
 // Chunked-prefill attention on the fifth-generation tensor cores (tcgen05,
-// accumulators in tensor memory) for head_dim 64 and 128: prefill_tc_kernel
-// for 16-bit caches, prefill_tc8_kernel (further down) for one-byte caches.
-// Chunked prefill is a dense contraction (every cached token meets a whole
-// chunk of queries), unlike the decode step, so it runs where the dense
-// tensor throughput is: "Optimizing KV-Cache Memory Footprint in
-// High-Throughput LLM Serving", section 5, pairs PagedAttention with GQA and
-// chunked prefill; query j of a chunk of n over c cached tokens sits at
-// position c - n + j and sees tokens 0 .. c - n + j.
+// accumulators in tensor memory) for one-byte caches (FP8 E4M3, FP8 E5M2,
+// INT8) at head_dim 64 and 128: prefill_tc8_kernel.  (16-bit caches take the
+// warp-role kernel of pkv_prefill_ws.cu.)  Chunked prefill is a dense
+// contraction (every cached token meets a whole chunk of queries), unlike the
+// decode step, so it runs where the dense tensor throughput is: "Optimizing
+// KV-Cache Memory Footprint in High-Throughput LLM Serving", section 5, pairs
+// PagedAttention with GQA and chunked prefill; query j of a chunk of n over c
+// cached tokens sits at position c - n + j and sees tokens 0 .. c - n + j.
 //
 // One CTA (one warpgroup, 128 threads; two CTAs per SM) takes 128 query rows
 // -- 128/G query tokens of one sequence times the G query heads of one KV
 // head -- and walks that KV head's cache in 64-token tiles:
-//   1. the tile's K rows and V rows come in with 16-byte cp.async through the
-//      block table (one row locator per token), K as a K-major operand and V
-//      as an MN-major one (token rows as they are stored), V double-buffered;
-//      the next tile's K is requested as soon as S has been formed, its V as
-//      soon as the previous P V has finished, so the copies overlap the
-//      softmax and the tensor cores;
+//   1. the tile's K and V codes come in through the block table and are
+//      converted to f16 operands in shared memory, K as a K-major operand and
+//      V as an MN-major one (token rows as they are stored);
 //   2. S = Q K^T: eight tcgen05.mma (M 128, N 64, K 16) into tensor memory;
 //   3. thread r reads row r of S from tensor memory, applies the causal mask
 //      and the online softmax (running max raised lazily, by more than
@@ -30,9 +27,10 @@
 // (Q, K) with the next core matrix along K 128 bytes on (leading byte
 // offset) and the next 8-row group further (stride byte offset); MN-major (V)
 // with 8 tokens x 8 head_dim values per core matrix, the next token group 128
-// bytes on and the next 8 head_dim values 1024 bytes on.  Every wait for the tensor
-// cores is bounded: when one runs out the launch ORs PKV_ERR_DEVICE_TIMEOUT
-// into dev_status, stops, and still frees its tensor memory.
+// bytes on and the next 8 head_dim values 1024 bytes on.  Every wait for the
+// tensor cores is bounded: when one runs out the launch ORs
+// PKV_ERR_DEVICE_TIMEOUT into dev_status, stops, and still frees its tensor
+// memory.
 #include <math.h>
 #include <stdlib.h>
 #include <stdint.h>
@@ -59,23 +57,16 @@ template <int D> struct TcPlan {
   static constexpr int kQBytes = kTcRows * D * 2;
   static constexpr int kKBytes = kTcKv * D * 2;
   static constexpr int kVBytes = kTcKv * D * 2;
-  // 16-bit caches: Q, K, two V tiles, the row locators of the next tile to
-  // load (int64 each), two mbarriers + tensor-memory address + flag
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBytes;
-  static constexpr int kOffV = kOffK + kKBytes;
-  static constexpr int kOffLoc = kOffV + 2 * kVBytes;
-  static constexpr int kOffBar = kOffLoc + kTcKv * 8;
-  static constexpr int kSmem = kOffBar + 32;
-  // one-byte caches: Q, K, one V tile, the per-token scales of two tiles (by
-  // tile parity: K scales, V scales, V max per half-tile), barriers
+  // Q, K, one V tile, the per-token scales of two tiles (by tile parity: K
+  // scales, V scales, V max per half-tile), barriers
   static constexpr int kSc8Floats = 2 * kTcKv + 8;
   static constexpr int kOffV8 = kOffK + kKBytes;
   static constexpr int kOffS8 = kOffV8 + kVBytes;
   static constexpr int kOffBar8 = kOffS8 + 2 * kSc8Floats * 4;
   static constexpr int kSmem8 = kOffBar8 + 32;
-  static_assert(2 * (kSmem + 1024) <= 233472 && 2 * (kSmem8 + 1024) <= 233472,
-                "two CTAs per SM");
+  static_assert(2 * (kSmem8 + 1024) <= 233472, "two CTAs per SM");
 };
 
 struct TcParams {
@@ -87,9 +78,6 @@ struct TcParams {
   const int32_t* q_start;
   const float* scales;        // one-byte caches: fp32 [2][num_blocks][num_kv_heads]
   int max_query_len;          // queries j >= max_query_len of a chunk are not computed
-#ifdef PKV_TEST_HOOKS
-  int test_drop_commit;       // test of the bounded waits: the first S batch is not committed
-#endif
   void* out;
   int* dev_status;
   int max_blocks_per_seq;
@@ -100,323 +88,10 @@ struct TcParams {
   float softmax_scale;
 };
 
-template <int DT, int D>
-__global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParams p) {
-  extern __shared__ __align__(1024) uint8_t smem[];
-  using PL = TcPlan<D>;
-  pdl_wait();
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int kvh = blockIdx.y, b = blockIdx.z;
-  const int group = p.num_q_heads / p.num_kv_heads;
-  const int qpb = kTcRows / group;                     // query tokens of this CTA
-  const int nq = p.q_start[b + 1] - p.q_start[b];
-  const int nqc = min(nq, p.max_query_len);            // queries computed
-  const int j0 = static_cast<int>(blockIdx.x) * qpb;
-  if (j0 >= nqc) return;                                // whole CTA: no query here
-  const int cap = p.max_blocks_per_seq * p.block_size;
-  int ctx = p.context_lens[b];
-  if (ctx > cap) {
-    if (tid == 0 && blockIdx.x == 0 && kvh == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
-    ctx = cap;
-  }
-  const int pos0 = ctx - nq;                           // position of query 0 of the chunk
-  if (pos0 < 0 && j0 == 0 && tid == 0 && kvh == 0) flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
-  // this thread's row: query token j0 + r / G, head r % G
-  const int jj = tid / group, g = tid % group;
-  const bool row_q = j0 + jj < nqc;
-  const int pos = pos0 + j0 + jj;
-  const bool row_ok = row_q && pos >= 0;
-  const int last_j = min(j0 + qpb, nqc) - 1;
-  const int kv_end = max(0, min(ctx, pos0 + last_j + 1));
-  const int ntiles = (kv_end + kTcKv - 1) / kTcKv;
-
-  const uint32_t sb = smem_u32(smem);
-  const uint32_t bar_s = sb + PL::kOffBar, bar_o = sb + PL::kOffBar + 8;
-  volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(smem + PL::kOffBar + 16);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + PL::kOffBar + 20);
-
-  if (warp == 0) {
-    tmem_alloc(sb + PL::kOffBar + 16, PL::kTmemCols);
-    tmem_relinquish();
-  }
-  if (tid == 0) {
-    mbar_init(bar_s, 1);
-    mbar_init(bar_o, 1);
-    mbar_init_fence();
-    *abort_flag = 0;
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tslot;
-  const uint32_t tmem_s = tmem, tmem_o = tmem + 64, tmem_p = tmem + 64 + D;
-  const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;   // this warp's 32 lanes
-
-  // Q rows (K-major core matrices; rows without a query are zero)
-  {
-    const uint16_t* qrow =
-        p.q + ((static_cast<int64_t>(p.q_start[b]) + j0 + (row_q ? jj : 0)) * p.num_q_heads +
-               kvh * group + g) * D;
-#pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
-      const uint32_t dst = sb + PL::kOffQ + core_off(tid, c, D / 8);
-      if (row_ok) cp_async_16(dst, qrow + 8 * c);
-      else st_shared_v4(dst, make_uint4(0, 0, 0, 0));
-    }
-  }
-
-  const float mult = p.softmax_scale * 1.4426950408889634f;
-  constexpr bool kBf = DT == PKV_BF16;
-  constexpr uint32_t kIdescS = umma_idesc(kBf, kTcRows, kTcKv, false);
-  constexpr uint32_t kIdescO = umma_idesc(kBf, kTcRows, D, true);
-  float m = -INFINITY, l = 0.f;
-  bool failed = false;
-  int s_commits = 0, o_commits = 0;                   // tensor-core batches issued (same in every thread)
-  const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
-
-  // Row locators of tile t (threads 0-63, one token each): the cache row
-  // index (block * Hkv + kvh) * block_size + offset, or -1 for a token past
-  // the range or in an out-of-range block (those read as zeros).
-  const int64_t* locs = reinterpret_cast<const int64_t*>(smem + PL::kOffLoc);
-  auto put_locators = [&](int t) {
-    if (tid < kTcKv) {
-      const int abs_t = t * kTcKv + tid;
-      int64_t row = -1;
-      if (abs_t < kv_end) {
-        const int logical = abs_t / p.block_size;
-        const int phys = __ldg(trow + logical);
-        if (phys >= 0 && phys < p.num_blocks)
-          row = (static_cast<int64_t>(phys) * p.num_kv_heads + kvh) * p.block_size +
-                (abs_t - logical * p.block_size);
-        else
-          flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
-      }
-      reinterpret_cast<int64_t*>(smem + PL::kOffLoc)[tid] = row;
-    }
-  };
-  // The rows of the tile whose locators are in place, K (into the K-major K
-  // tile) or V (into the MN-major V tile of buffer vbuf).  Thread tid copies
-  // 16-byte chunk (tid >> 3) & 15 of tokens 8 i + (tid & 7), so eight
-  // consecutive threads fill one 128-byte core matrix.
-  // (D / 8 chunks per row: D = 128 -> every thread takes all 8 token groups
-  // of its chunk; D = 64 -> two thread sets take alternate groups)
-  constexpr int kCh = D / 8, kSets = kTcThreads / (8 * kCh);
-  const int lr = tid & 7, lc = (tid >> 3) % kCh, lset = (tid >> 3) / kCh;
-  auto load_rows = [&](bool is_v, int vbuf) {
-    const uint8_t* cache = is_v ? p.v_cache : p.k_cache;
-    const uint32_t base = sb + (is_v ? PL::kOffV + vbuf * PL::kVBytes : PL::kOffK) + (lr << 4);
-#pragma unroll
-    for (int k = 0; k < kTcKv / 8 / kSets; ++k) {
-      const int i = lset + kSets * k;
-      const int64_t row = locs[8 * i + lr];
-      const uint32_t dst = base + (is_v ? ((lc * (kTcKv / 8) + i) << 7) : ((i * (D / 8) + lc) << 7));
-      const uint8_t* src = row >= 0 ? cache + row * (D * 2) + lc * 16 : cache;
-      cp_async_16_zfill(dst, src, row >= 0 ? 16u : 0u);
-    }
-  };
-  if (ntiles > 0) {
-    put_locators(0);
-    __syncthreads();
-    load_rows(false, 0);
-    load_rows(true, 0);
-    __syncthreads();
-    if (ntiles > 1) put_locators(1);
-  }
-  cp_async_commit();
-
-  for (int t = 0; t < ntiles; ++t) {
-    const int t0 = t * kTcKv;
-    // 1. tile t's K and V (and, at t = 0, Q) are in shared memory
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (*abort_flag) { failed = true; break; }
-    // 2. S = Q K^T
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        umma(tmem_s, umma_desc(sb + PL::kOffQ + kk * 256, 128, (D / 8) * 128),
-             umma_desc(sb + PL::kOffK + kk * 256, 128, (D / 8) * 128), kIdescS, kk > 0);
-#ifdef PKV_TEST_HOOKS
-      // (the test build's check of the bounded waits leaves the first batch
-      // uncommitted: the wait below then runs out and the launch reports
-      // PKV_ERR_DEVICE_TIMEOUT)
-      if (!(p.test_drop_commit && t == 0)) umma_commit(bar_s);
-#else
-      umma_commit(bar_s);
-#endif
-    }
-    ++s_commits;
-    if (!mbar_wait(bar_s, t & 1)) {
-      flag_status(p.dev_status, PKV_ERR_DEVICE_TIMEOUT);
-      *abort_flag = 1;
-    }
-    tc_fence_after();
-    // the K tile is free again: request the next one
-    if (t + 1 < ntiles) load_rows(false, 0);
-    cp_async_commit();
-    // 3. row tid of S, masked and scaled (log2 units)
-    float s[kTcKv];
-    {
-      float a[32];
-      tmem_ld32(tmem_s + lane_base, a);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) s[i] = a[i];
-      tmem_ld32(tmem_s + lane_base + 32, a);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) s[32 + i] = a[i];
-    }
-    // tiles below the range end and below every row's causal limit (the
-    // first query's position is the smallest) need no mask: scale in the
-    // exponent's fused multiply-add; otherwise scale and mask here
-    const bool full = t0 + kTcKv <= kv_end && t0 + kTcKv - 1 <= pos0 + j0;
-    float tmax, pmul;
-    if (full) {
-      float e;
-      if (mult >= 0.f) {
-        e = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < kTcKv; ++c) e = fmaxf(e, s[c]);
-      } else {
-        e = INFINITY;
-#pragma unroll
-        for (int c = 0; c < kTcKv; ++c) e = fminf(e, s[c]);
-      }
-      tmax = e * mult;
-      pmul = mult;
-    } else {
-      tmax = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < kTcKv; ++c) {
-        const int abs_t = t0 + c;
-        const bool valid = abs_t < kv_end && (!row_ok || abs_t <= pos);
-        s[c] = valid ? s[c] * mult : -INFINITY;
-        tmax = fmaxf(tmax, s[c]);
-      }
-      pmul = 1.f;
-    }
-    // 4. the previous P V has finished with O, P and the other V buffer:
-    //    request the next V tile there
-    if (t > 0 && !mbar_wait(bar_o, (t - 1) & 1)) {
-      flag_status(p.dev_status, PKV_ERR_DEVICE_TIMEOUT);
-      *abort_flag = 1;
-    }
-    tc_fence_after();
-    if (t + 1 < ntiles) load_rows(true, (t + 1) & 1);
-    cp_async_commit();
-    // 5. online softmax; the running max moves only past m + tau
-    const bool raise = tmax > m + kTcTau;
-    float alpha = 1.f;
-    if (raise) {
-      const float mn = fmaxf(m, tmax);
-      alpha = ex2_ftz(m - mn);
-      m = mn;
-      l *= alpha;
-    }
-    if (t > 0 && __any_sync(0xffffffffu, raise)) {    // rescale O (warp-collective)
-#pragma unroll
-      for (int k = 0; k < D / 32; ++k) {
-        float o[32];
-        tmem_ld32(tmem_o + lane_base + 32 * k, o);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-        tmem_st32(tmem_o + lane_base + 32 * k, o);
-      }
-    }
-    // P = 2^(s - m) as a 16-bit hi + lo pair into row tid of the tensor-memory
-    // A operand (two tokens per 32-bit column): hi at tmem_p, lo 32 columns on
-#pragma unroll
-    for (int c8 = 0; c8 < kTcKv / 8; ++c8) {
-      uint32_t hw[4], lw[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float p0 = ex2_ftz(fmaf(s[8 * c8 + 2 * k], pmul, -m));
-        const float p1 = ex2_ftz(fmaf(s[8 * c8 + 2 * k + 1], pmul, -m));
-        l += p0 + p1;
-        hw[k] = Half16<DT>::pack_rn(p0, p1);
-        const float2 f = Half16<DT>::unpack(hw[k]);
-        lw[k] = Half16<DT>::pack_rn(p0 - f.x, p1 - f.y);
-      }
-      tmem_st4(tmem_p + lane_base + 4 * c8, hw[0], hw[1], hw[2], hw[3]);
-      tmem_st4(tmem_p + lane_base + kTcKv / 2 + 4 * c8, lw[0], lw[1], lw[2], lw[3]);
-    }
-    tmem_store_wait();
-    tc_fence_before();
-    __syncthreads();
-    if (*abort_flag) { failed = true; break; }
-    // every thread has issued its copies of tile t + 1: the locators of tile
-    // t + 2 may replace theirs (read after the next iteration's barrier)
-    if (t + 2 < ntiles) put_locators(t + 2);
-    // 6. O += P V (hi, then lo), P from tensor memory (16 tokens = 8 columns
-    //    per MMA); V is MN-major: the next 16 tokens 256 bytes on, the next 8
-    //    head_dim values (kTcKv / 8) * 128 bytes on
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t vb = sb + PL::kOffV + (t & 1) * PL::kVBytes;
-#pragma unroll
-      for (int kk = 0; kk < kTcKv / 16; ++kk)
-        umma_ts(tmem_o, tmem_p + kk * 8, umma_desc(vb + kk * 256, 128, (kTcKv / 8) * 128),
-                kIdescO, t > 0 || kk > 0);
-#pragma unroll
-      for (int kk = 0; kk < kTcKv / 16; ++kk)
-        umma_ts(tmem_o, tmem_p + kTcKv / 2 + kk * 8, umma_desc(vb + kk * 256, 128, (kTcKv / 8) * 128),
-                kIdescO, 1u);
-      umma_commit(bar_o);
-    }
-    ++o_commits;
-  }
-  cp_async_wait<0>();
-
-  // the last P.V (after a failure: still a bounded wait for whatever was
-  // issued, so the tensor memory is idle when it is freed), then the output
-  if (o_commits > 0 && !mbar_wait(bar_o, (o_commits - 1) & 1)) {
-    flag_status(p.dev_status, PKV_ERR_DEVICE_TIMEOUT);
-    failed = true;
-  }
-  if (s_commits > 0 && !mbar_wait(bar_s, (s_commits - 1) & 1)) {
-    flag_status(p.dev_status, PKV_ERR_DEVICE_TIMEOUT);
-    failed = true;
-  }
-  tc_fence_after();
-  const bool all_ok = __syncthreads_and(!failed) != 0;
-  if (row_q && !(all_ok && ntiles > 0)) {
-    uint16_t* orow = static_cast<uint16_t*>(p.out) +
-                     ((static_cast<int64_t>(p.q_start[b]) + j0 + jj) * p.num_q_heads + kvh * group + g) * D;
-    for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
-  }
-  if (all_ok && ntiles > 0) {
-#pragma unroll
-    for (int k = 0; k < D / 32; ++k) {
-      float o[32];
-      tmem_ld32(tmem_o + lane_base + 32 * k, o);       // warp-collective: every row
-      if (row_q) {
-        uint16_t* orow = static_cast<uint16_t*>(p.out) +
-                         ((static_cast<int64_t>(p.q_start[b]) + j0 + jj) * p.num_q_heads +
-                          kvh * group + g) * D + 32 * k;
-        const float inv = (row_ok && l > 0.f) ? 1.f / l : 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint4 w;
-          w.x = Half16<DT>::pack_rn(o[8 * c] * inv, o[8 * c + 1] * inv);
-          w.y = Half16<DT>::pack_rn(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
-          w.z = Half16<DT>::pack_rn(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
-          w.w = Half16<DT>::pack_rn(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
-          reinterpret_cast<uint4*>(orow)[c] = w;
-        }
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, PL::kTmemCols);
-  pdl_launch_dependents();
-}
-
 // ----------------------------------------------------------------------------
 // One-byte caches (FP8 E4M3, FP8 E5M2, INT8; one fp32 scale per block and KV
-// head).  The same tiles and tensor-core steps as above, with f16 operands:
+// head).  The tiles and tensor-core steps of the file's header, with f16
+// operands:
 //   * the codes of the next tile are fetched into registers one tile ahead
 //     (16-byte loads through the block table) and converted exactly to f16
 //     into the K-major K tile and the MN-major V tile (E4M3 and E5M2 by cvt,
@@ -429,7 +104,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const TcParam
 //     (the largest V scale seen so far): P'' = p s_V / vu <= 2^8.  When a tile
 //     raises vu, O and the row sum (kept in the same units) are rescaled, and
 //     the output O / l is free of vu;
-//   * P'' goes to tensor memory as in the 16-bit kernel, and the softmax works
+//   * P'' goes to tensor memory as a hi + lo pair, and the softmax works
 //     on packed fp32 pairs (two scores per fma / add / mul / sub).
 template <int KV, int QT, int D>
 __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcParams p) {
@@ -835,9 +510,6 @@ cudaError_t launch_tc(Kern kern, int smem_bytes, const PrefillArgs& a, cudaStrea
   p.block_size = a.block_size;
   p.softmax_scale = a.softmax_scale;
   p.max_query_len = a.max_query_len;
-#ifdef PKV_TEST_HOOKS
-  p.test_drop_commit = getenv("PKV_TEST_DROP_COMMIT") != nullptr;
-#endif
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -860,8 +532,6 @@ cudaError_t launch_tc8(const PrefillArgs& a, cudaStream_t st) {
 template <int D>
 cudaError_t launch_tc_d(const PrefillArgs& a, cudaStream_t st) {
   switch (a.kv_dtype) {
-    case PKV_F16: return launch_tc(prefill_tc_kernel<PKV_F16, D>, TcPlan<D>::kSmem, a, st);
-    case PKV_BF16: return launch_tc(prefill_tc_kernel<PKV_BF16, D>, TcPlan<D>::kSmem, a, st);
     case PKV_FP8_E4M3: return launch_tc8<PKV_FP8_E4M3, D>(a, st);
     case PKV_FP8_E5M2: return launch_tc8<PKV_FP8_E5M2, D>(a, st);
     case PKV_INT8: return launch_tc8<PKV_INT8, D>(a, st);
@@ -872,8 +542,7 @@ cudaError_t launch_tc_d(const PrefillArgs& a, cudaStream_t st) {
 }  // namespace
 
 bool prefill_tc_supported(const PrefillArgs& a) {
-  return (a.kv_dtype == PKV_F16 || a.kv_dtype == PKV_BF16 || is_blk8(a.kv_dtype)) &&
-         (a.head_dim == 64 || a.head_dim == 128);
+  return is_blk8(a.kv_dtype) && (a.head_dim == 64 || a.head_dim == 128);
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st) {

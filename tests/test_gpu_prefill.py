@@ -179,8 +179,9 @@ def test_prefill_benchmark_workload_sampled():
 
 
 def test_prefill_tc_bounded_wait_reports_a_timeout(monkeypatch):
-    """The tcgen05 prefill with its first S batch left uncommitted
-    (PKV_TEST_DROP_COMMIT): the bounded wait on it runs out (about 2 s), the call
+    """The 16-bit tcgen05 prefill (warp roles) with its first S batch left
+    uncommitted (PKV_TEST_DROP_COMMIT): the softmax's bounded wait on it runs out
+    (about 2 s), every other role's wait ends on the abort, the call
     reports PKV_ERR_DEVICE_TIMEOUT through dev_status and zeros in its rows, and
     the next call on the same context is exact again."""
     pkv = _pkv()
