@@ -245,18 +245,24 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
       }
     }
   };
-  // threads 0-63: the K and V scales of token tid of tile t (0 past the range
-  // or for an out-of-range block), and per warp the largest V scale
+  // threads 0-63: the K and V scales of token tid of tile t (0 past the range;
+  // for a token in an out-of-range block, which takes no part, a K scale of
+  // NaN and a V scale of 0), and per warp the largest V scale and whether
+  // any of its tokens is in an out-of-range block
   auto put_scales = [&](int t) {
     if (tid < kTcKv) {
       const int abs_t = t * kTcKv + tid;
       float ks = 0.f, vs = 0.f;
+      bool bad = false;
       if (abs_t < kv_end) {
         const int phys = __ldg(trow + abs_t / p.block_size);
         if (phys >= 0 && phys < p.num_blocks) {
           const int64_t idx = static_cast<int64_t>(phys) * p.num_kv_heads + kvh;
           ks = __ldg(p.scales + idx);
           vs = __ldg(p.scales + per_kv + idx);
+        } else {
+          ks = __int_as_float(0x7fc00000);
+          bad = true;
         }
       }
       float* sc = scb + (t & 1) * PL::kSc8Floats;
@@ -265,7 +271,11 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
       float vm = vs;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
-      if (lane == 0) sc[2 * kTcKv + warp] = vm;
+      const bool any_bad = __any_sync(0xffffffffu, bad);
+      if (lane == 0) {
+        sc[2 * kTcKv + warp] = vm;
+        sc[2 * kTcKv + 2 + warp] = any_bad ? 1.f : 0.f;
+      }
     }
   };
   // codes in registers -> f16 operand tile (K: K-major; V: MN-major)
@@ -346,7 +356,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
       s[4 * c4 + 2] = c.x;
       s[4 * c4 + 3] = c.y;
     }
-    const bool full = t0 + kTcKv <= kv_end && t0 + kTcKv - 1 <= pos0 + j0;
+    const bool bad_tile = sc[2 * kTcKv + 2] != 0.f || sc[2 * kTcKv + 3] != 0.f;
+    const bool full = t0 + kTcKv <= kv_end && t0 + kTcKv - 1 <= pos0 + j0 && !bad_tile;
     float tmax, pmul;
     if (full) {
       float e;
@@ -366,7 +377,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc8_kernel(const TcPara
 #pragma unroll
       for (int c = 0; c < kTcKv; ++c) {
         const int abs_t = t0 + c;
-        const bool valid = abs_t < kv_end && (!row_ok || abs_t <= pos);
+        const bool valid = abs_t < kv_end && (!row_ok || abs_t <= pos) && sc[c] == sc[c];
         s[c] = valid ? s[c] * mult : -INFINITY;
         tmax = fmaxf(tmax, s[c]);
       }

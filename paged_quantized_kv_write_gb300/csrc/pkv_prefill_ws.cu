@@ -296,8 +296,19 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
     mbar_init_fence();
     *abort_flag = 0;
   }
+  // whether any block of the range is out of the pool (then the softmax looks
+  // up each tile's pieces; a table of valid ids costs it nothing)
+  bool bad_here = false;
+  {
+    const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
+    const int nblk = (kv_end + p.block_size - 1) / p.block_size;
+    for (int i = tid; i < nblk; i += kWsThreads) {
+      const int phys = __ldg(trow + i);
+      bad_here |= phys < 0 || phys >= p.num_blocks;
+    }
+  }
   tc_fence_before();
-  __syncthreads();
+  const bool any_bad = __syncthreads_or(bad_here) != 0;
   tc_fence_after();
   const uint32_t tmem = *tslot;
 
@@ -333,10 +344,23 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
       if (lane == 0) mbar_arrive(bar(PL::kBarQ));
     }
     const float mult = p.softmax_scale * 1.4426950408889634f;
+    const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
     float m = -INFINITY;
 #pragma unroll 1
     for (int t = 0; t < nt; ++t) {
       const int t0 = t * kWsKv;
+      // the tile's 16-token pieces in an out-of-range block (bit j: piece j),
+      // which take no part (the load warp reads them as zeros and flags them)
+      uint32_t bad = 0;
+      if (any_bad) {
+        const int tok = t0 + lane * kWsPiece;
+        bool b = false;
+        if (lane < kWsPieces && tok < kv_end) {
+          const int phys = __ldg(trow + tok / p.block_size);
+          b = phys < 0 || phys >= p.num_blocks;
+        }
+        bad = __ballot_sync(0xffffffffu, b);
+      }
       // 1. row r of S_qt(t)
       bool ok = ws_wait(bar(PL::kBarSFull + qt), t & 1, abort_flag, p.dev_status);
       if (!__all_sync(0xffffffffu, ok)) break;
@@ -347,7 +371,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
       //    into the exponent's fma), and its largest value
       float sv[kWsKv];
       tmem_ld128(t_s, sv);
-      const bool full = t0 + kWsKv <= kv_end && t0 + kWsKv - 1 <= pos0 + ji;
+      const bool full = t0 + kWsKv <= kv_end && t0 + kWsKv - 1 <= pos0 + ji && bad == 0;
       float tmax, pmul;
       if (full) {
         // (a negative scale turns the row's smallest score into its largest)
@@ -357,7 +381,9 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
 #pragma unroll
         for (int c = 0; c < kWsKv; ++c) {
           const int abs_t = t0 + c;
-          sv[c] = abs_t < kv_end && (!row_ok || abs_t <= pos) ? sv[c] * mult : -INFINITY;
+          const bool valid = abs_t < kv_end && (!row_ok || abs_t <= pos) &&
+                             !((bad >> (c / kWsPiece)) & 1u);
+          sv[c] = valid ? sv[c] * mult : -INFINITY;
         }
         tmax = row_max(sv);
         pmul = 1.f;

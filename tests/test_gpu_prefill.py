@@ -25,8 +25,9 @@ def _full_cache(case):
     return k, v, s
 
 
-def _run(case, chunk, max_query_len=None, seed=0, ctx=None):
-    """GPU and oracle prefill for the given chunk lengths; returns (gpu, ref, status, q_start)."""
+def _run(case, chunk, max_query_len=None, seed=0, ctx=None, tables=None, oracle_ref=True):
+    """GPU and oracle prefill for the given chunk lengths; returns (gpu, ref, status, q_start)
+    (ref None without oracle_ref).  `tables` replaces the case's block tables on the GPU."""
     pkv = _pkv()
     w = case.w
     k, v, s = _full_cache(case)
@@ -38,14 +39,17 @@ def _run(case, chunk, max_query_len=None, seed=0, ctx=None):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     mql = int(max(chunk)) if max_query_len is None else max_query_len
     pkv.paged_prefill_attention(qt, torch.from_numpy(q_start).cuda(), kd, vd,
-                                torch.from_numpy(case.block_tables).cuda(),
+                                torch.from_numpy(case.block_tables if tables is None
+                                                 else tables).cuda(),
                                 torch.from_numpy(np.ascontiguousarray(ctx, np.int32)).cuda(),
                                 sd, out, w.softmax_scale, w.num_kv_heads, w.kv_dtype,
                                 w.block_size, mql, status)
     torch.cuda.synchronize()
-    ref = oracle.prefill_attention(q, w.q_dtype, q_start, k, v, case.block_tables, ctx, s,
-                                   w.kv_dtype, case.num_blocks, w.softmax_scale, w.num_q_heads,
-                                   w.num_kv_heads, w.head_dim, w.block_size)
+    ref = None
+    if oracle_ref:
+        ref = oracle.prefill_attention(q, w.q_dtype, q_start, k, v, case.block_tables, ctx, s,
+                                       w.kv_dtype, case.num_blocks, w.softmax_scale,
+                                       w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size)
     return H.tensor_to_f64(out), ref, status.item(), q_start
 
 
@@ -141,6 +145,32 @@ def test_prefill_max_query_len_bounds_the_grid(kv, head_dim):
     computed = np.r_[0:16, 40:50]
     H.check_close(gpu[computed], ref[computed], kv, W.BF16, "bounded")
     assert np.isnan(gpu[16:40]).all()              # beyond max_query_len: not written
+
+
+@pytest.mark.parametrize("kv,head_dim", EDGE_KERNELS + [(W.INT4_G32, 128)])
+def test_prefill_bad_block_id_is_flagged_and_skipped(kv, head_dim, monkeypatch):
+    """A block id outside the pool in one sequence's table (tokens 32..47 of
+    sequence 1): the call flags PKV_ERR_DEVICE_BOUNDS, the other sequences
+    match the oracle, and sequence 1 matches the mma.sync path, which leaves
+    that block's tokens out in the same way."""
+    pkv = _pkv()
+    w = W.Workload("pfbad", 3, 8, 2, head_dim, 16, kv, W.BF16, "fixed", 200, 200, seed=8)
+    case = W.make_case(w)
+    bad = case.block_tables.copy()
+    bad[1, 2] = case.num_blocks + 7
+    chunk = [16, 40, 24]
+    monkeypatch.delenv("PKV_PREFILL_MODE", raising=False)
+    gpu, _, st, q_start = _run(case, chunk, tables=bad, oracle_ref=False)
+    assert st == pkv.PKV_ERR_DEVICE_BOUNDS
+    _, ref, _, _ = _run(case, chunk)
+    others = np.r_[q_start[0]:q_start[1], q_start[2]:q_start[3]]
+    H.check_close(gpu[others], ref[others], kv, W.BF16, "other sequences")
+    monkeypatch.setenv("PKV_PREFILL_MODE", "mma")
+    mma, _, st_mma, _ = _run(case, chunk, tables=bad, oracle_ref=False)
+    assert st_mma == pkv.PKV_ERR_DEVICE_BOUNDS
+    rows = np.r_[q_start[1]:q_start[2]]
+    assert np.isfinite(gpu[rows]).all()
+    H.check_close(gpu[rows], mma[rows], kv, W.BF16, "sequence with the bad block")
 
 
 @pytest.mark.slow
