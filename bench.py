@@ -639,9 +639,7 @@ def _prefill_kernel_name(kv_dtype: int) -> str:
     """The kernel paged_prefill_attention runs for this cache dtype."""
     if os.environ.get("PKV_PREFILL_MODE") == "mma" or kv_dtype == W.INT4_G32:
         return "paged_decode_kernel (prefill mode, mma.sync)"
-    if kv_dtype in (W.F16, W.BF16):
-        return "prefill_ws_kernel (tcgen05, load / MMA / softmax warp roles)"
-    return "prefill_tc8_kernel (tcgen05)"
+    return "prefill_ws_kernel (tcgen05, load / MMA / softmax warp roles)"
 
 
 def run_prefill(args, rank: int, world: int):

@@ -123,9 +123,7 @@ cudaError_t launch_kv_write(const WriteArgs& a, cudaStream_t st);
 cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t st);
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t st);
 cudaError_t launch_lse_reduce(const DecodeArgs& a, cudaStream_t st);
-bool prefill_tc_supported(const PrefillArgs& a);
-cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st);
-// 16-bit caches: the tcgen05 prefill with warp roles (pkv_prefill_ws.cu)
+// 16-bit and one-byte caches: the tcgen05 prefill with warp roles (pkv_prefill_ws.cu)
 bool prefill_ws_supported(const PrefillArgs& a);
 cudaError_t launch_prefill_ws(const PrefillArgs& a, cudaStream_t st);
 #ifdef PKV_TEST_HOOKS

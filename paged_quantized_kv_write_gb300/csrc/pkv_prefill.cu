@@ -7,11 +7,10 @@
 // causal rule is the usual one for prefill (query j of a chunk of n over a
 // context of c tokens sits at position c - n + j and sees tokens 0..c - n + j).
 //
-// Three kernels compute it.  16-bit caches go to the warp-role tcgen05 kernel
-// of pkv_prefill_ws.cu (two 128-row Q tiles per CTA against 128-token tiles,
-// TMA loads, accumulators in tensor memory), one-byte caches to the tcgen05
-// kernel of pkv_prefill_tc.cu (128 query rows per CTA against 64-token tiles,
-// codes converted to f16 operands).  INT4 caches, or any call under
+// Two kernels compute it.  16-bit and one-byte caches go to the warp-role
+// tcgen05 kernel of pkv_prefill_ws.cu (two 128-row Q tiles per CTA against
+// 128-token tiles, accumulators in tensor memory; one-byte codes converted to
+// f16 operands by its load warps).  INT4 caches, or any call under
 // PKV_PREFILL_MODE=mma, run the
 // decode kernel of pkv_attn.cuh in its PF mode: a warp's 8 score columns are
 // 8/G query tokens times the G query heads of one KV head, each column masked
@@ -85,12 +84,11 @@ cudaError_t launch_prefill_q(const PrefillArgs& a, cudaStream_t st) {
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t st) {
   if (a.num_seqs == 0 || a.max_query_len == 0) return cudaSuccess;
-  // 16-bit and one-byte caches run on the tcgen05 kernels (pkv_prefill_ws.cu,
-  // pkv_prefill_tc.cu); PKV_PREFILL_MODE=mma keeps them on this one
+  // 16-bit and one-byte caches run on the tcgen05 kernel (pkv_prefill_ws.cu);
+  // PKV_PREFILL_MODE=mma keeps them on this one
   const char* mode = getenv("PKV_PREFILL_MODE");
   const bool mma = mode && !strcmp(mode, "mma");
   if (prefill_ws_supported(a) && !mma) return launch_prefill_ws(a, st);
-  if (prefill_tc_supported(a) && !mma) return launch_prefill_tc(a, st);
   switch (a.kv_dtype) {
     case PKV_F16: return launch_prefill_q<PKV_F16>(a, st);
     case PKV_BF16: return launch_prefill_q<PKV_BF16>(a, st);

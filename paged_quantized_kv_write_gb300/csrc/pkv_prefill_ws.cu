@@ -1,21 +1,30 @@
-// Chunked-prefill attention for 16-bit caches on the tcgen05 tensor cores,
-// with warp roles: the same computation as prefill_tc_kernel
-// (pkv_prefill_tc.cu; "Optimizing KV-Cache Memory Footprint in
-// High-Throughput LLM Serving", section 5: query j of a chunk of n over c
-// cached tokens sits at position c - n + j and sees tokens 0 .. c - n + j),
-// arranged so that the tensor cores and the softmax work at the same time.
+// Chunked-prefill attention on the tcgen05 tensor cores, with warp roles,
+// for 16-bit caches (F16, BF16) and one-byte caches (FP8 E4M3 / E5M2, INT8;
+// one fp32 scale per block and KV head).  Chunked prefill is a dense
+// contraction (every cached token meets a whole chunk of queries), unlike the
+// decode step, so it runs where the dense tensor throughput is: "Optimizing
+// KV-Cache Memory Footprint in High-Throughput LLM Serving", section 5, pairs
+// PagedAttention with GQA and chunked prefill; query j of a chunk of n over c
+// cached tokens sits at position c - n + j and sees tokens 0 .. c - n + j.
 //
-// One CTA per SM (320 threads, all 512 tensor-memory columns) takes two
-// adjacent Q tiles of 128 query rows each -- 128/G query tokens of one
-// sequence times the G query heads of one KV head per tile -- and walks that
-// KV head's cache in 128-token tiles, K and V of a tile shared by both Q tiles:
-//  * load warp (warp 9): looks up the tile's eight 16-token pieces in the block
-//    table and brings K and V into rings of two (head_dim 64: three) stages
-//    with TMA tensor copies (a 16 x 64 box per piece and 128-byte column
-//    block, 128-byte swizzle), signalled on mbarriers by byte count.  The
-//    piece that straddles the end of the range has its V rows copied by the
-//    warp's lanes instead, with the rows past the end zero-filled, so that
-//    P = 0 never meets a non-finite value from an unwritten slot;
+// One CTA per SM (320 threads, 384 for one-byte caches; all 512
+// tensor-memory columns) takes two adjacent Q tiles of 128 query rows each --
+// 128/G query tokens of one sequence times the G query heads of one KV head
+// per tile -- and walks that KV head's cache in 128-token tiles, K and V of a
+// tile shared by both Q tiles:
+//  * load warp (warp 9, 16-bit caches): looks up the tile's eight 16-token
+//    pieces in the block table and brings K and V into rings of two (head_dim
+//    64: three) stages with TMA tensor copies (a 16 x 64 box per piece and
+//    128-byte column block, 128-byte swizzle), signalled on mbarriers by byte
+//    count.  The piece that straddles the end of the range has its V rows
+//    copied by the warp's lanes instead, with the rows past the end
+//    zero-filled, so that P = 0 never meets a non-finite value from an
+//    unwritten slot; a piece in an out-of-range block reads as zeros and is
+//    flagged (the softmax leaves it out);
+//  * load warps (warps 9-11, one-byte caches): bring the codes with 16-byte
+//    loads through the block table and convert them exactly to f16 operands
+//    in the same layouts (E4M3 / E5M2 by cvt, INT8 as 1024 + (x + 128) -
+//    1152), zeros past the range or in an out-of-range block;
 //  * MMA warp (warp 8, one lane): S_A = Q_A K^T, then O_B += P_B V of the
 //    previous tile, then S_B = Q_B K^T, then O_A += P_A V, so that each
 //    softmax warpgroup works while the tensor cores serve the other tile;
@@ -29,6 +38,12 @@
 //    over S's own columns and signals the MMA warp.  The tensor cores run a
 //    thread's products in issue order, so S(t + 1), issued after P V(t),
 //    overwrites P(t) only after that product has read it.
+// One-byte caches also: bf16 queries enter as f16 times a power of two per
+// row (exact for every value above 2^-28 of the row's largest), taken off in
+// the softmax multiplier; each token's K block scale multiplies its score
+// column; its V block scale enters P as vs / vu, vu the largest V scale of the
+// CTA's blocks (found before the tiles), so P'' = p vs / vu <= p and the
+// output is O / l times vu.
 // Shared-memory operands use the canonical 128-byte-swizzle layouts: Q and K
 // K-major (rows of 128 bytes, 8-row atoms 1024 bytes apart, the second half
 // of head_dim 128 in its own region), V MN-major (token rows of 128 bytes, 8
@@ -59,8 +74,16 @@ constexpr int kWsKv = 128;                           // KV tokens per tile
 constexpr int kWsPiece = 16;                         // tokens per TMA box
 constexpr int kWsPieces = kWsKv / kWsPiece;
 constexpr int kWsMmaWarp = 8;
-constexpr int kWsLoadWarp = 9;
-constexpr int kWsThreads = 320;
+constexpr int kWsLoadWarp = 9;                       // the first load warp
+
+// The warps of a cache dtype: 0-7 softmax, 8 MMA, then the load warps: one
+// issuing TMA copies for 16-bit caches, three that load and convert the codes
+// for one-byte caches (12 warps still leave 168 registers per thread).
+template <int KV> struct WsRoles {
+  static constexpr bool kB8 = is_blk8(KV);
+  static constexpr int kLoadWarps = kB8 ? 3 : 1;
+  static constexpr int kThreads = (kWsLoadWarp + kLoadWarps) * kWarp;
+};
 constexpr float kWsTau = 8.f;                        // lazy rescale threshold (log2 units)
 constexpr int kWsBoxBytes = kWsPiece * 128;          // one box: 16 rows of 128 bytes
 
@@ -89,7 +112,9 @@ template <int D> struct WsPlan {
   static constexpr int kBarPFull = kBarSFull + 2, kBarODone = kBarPFull + 2;
   static constexpr int kBarFinal = kBarODone + 2, kNumBars = kBarFinal + 1;
   static constexpr int kOffSlot = kOffBar + 8 * kNumBars;
-  static constexpr int kSmem = kOffSlot + 16;
+  // one-byte caches: each warp's largest V scale over the CTA's blocks
+  static constexpr int kOffVu = kOffSlot + 16;
+  static constexpr int kSmem = kOffVu + 16 * 4;
   // one CTA per SM: it takes all of tensor memory, so the request is at least
   // half of shared memory
   static constexpr int kSmemRequest = kSmem > 120 * 1024 ? kSmem : 120 * 1024;
@@ -98,10 +123,12 @@ template <int D> struct WsPlan {
 };
 
 struct WsParams {
-  CUtensorMap tmap_k;          // the cache as [num_blocks * Hkv][block_size][D] 16-bit values
+  CUtensorMap tmap_k;          // 16-bit caches: [num_blocks * Hkv][block_size][D] values
   CUtensorMap tmap_v;
   const uint16_t* q;
+  const uint8_t* k_cache;
   const uint8_t* v_cache;
+  const float* scales;         // one-byte caches: fp32 [2][num_blocks][num_kv_heads]
   const int32_t* block_tables;
   const int32_t* context_lens;
   const int32_t* q_start;
@@ -244,10 +271,17 @@ __device__ __forceinline__ float row_max_neg(const float (&s)[kWsKv]) {
   return v[0];
 }
 
-template <int DT, int D>
-__global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_constant__ WsParams p) {
+// KV: the cache dtype; QT: the query dtype; the operands of the products are
+// QT for 16-bit caches and f16 for one-byte caches (codes converted exactly,
+// bf16 q as f16 times a power of two per row).
+template <int KV, int QT, int D>
+__global__ void __launch_bounds__(WsRoles<KV>::kThreads, 1)
+prefill_ws_kernel(const __grid_constant__ WsParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   using PL = WsPlan<D>;
+  using R = WsRoles<KV>;
+  constexpr bool kB8 = R::kB8;
+  constexpr int OT = kB8 ? PKV_F16 : KV;               // operand type of the products
   constexpr int S = PL::kStages;
   pdl_wait();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -281,8 +315,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
   }
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(bar(PL::kBarKFull + s), 1);
-      mbar_init(bar(PL::kBarVFull + s), 1 + kWarp);     // the TMA bytes + the load warp's lanes
+      // 16-bit: the TMA bytes (and, for V, the load warp's lanes); one-byte:
+      // one arrival per load warp
+      mbar_init(bar(PL::kBarKFull + s), kB8 ? R::kLoadWarps : 1);
+      mbar_init(bar(PL::kBarVFull + s), kB8 ? R::kLoadWarps : 1 + kWarp);
       mbar_init(bar(PL::kBarKEmpty + s), 1);
       mbar_init(bar(PL::kBarVEmpty + s), 1);
     }
@@ -297,20 +333,38 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
     *abort_flag = 0;
   }
   // whether any block of the range is out of the pool (then the softmax looks
-  // up each tile's pieces; a table of valid ids costs it nothing)
+  // up each tile's pieces; a table of valid ids costs it nothing), and for
+  // one-byte caches the largest V scale of the range's blocks (vu)
   bool bad_here = false;
+  float vmax_here = 0.f;
+  const int64_t per_kv = static_cast<int64_t>(p.num_blocks) * p.num_kv_heads;
   {
     const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
     const int nblk = (kv_end + p.block_size - 1) / p.block_size;
-    for (int i = tid; i < nblk; i += kWsThreads) {
+    for (int i = tid; i < nblk; i += R::kThreads) {
       const int phys = __ldg(trow + i);
-      bad_here |= phys < 0 || phys >= p.num_blocks;
+      const bool bad = phys < 0 || phys >= p.num_blocks;
+      bad_here |= bad;
+      if (kB8 && !bad)
+        vmax_here = fmaxf(vmax_here, __ldg(p.scales + per_kv + static_cast<int64_t>(phys) * p.num_kv_heads + kvh));
     }
+  }
+  if constexpr (kB8) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) vmax_here = fmaxf(vmax_here, __shfl_xor_sync(0xffffffffu, vmax_here, o));
+    if (lane == 0) reinterpret_cast<float*>(smem + PL::kOffVu)[warp] = vmax_here;
   }
   tc_fence_before();
   const bool any_bad = __syncthreads_or(bad_here) != 0;
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  // V scales enter P as vs / vu <= 1 (a range without written V blocks: vu 1)
+  float vu = 1.f;
+  if constexpr (kB8) {
+    float v = 0.f;
+    for (int w = 0; w < R::kThreads / kWarp; ++w) v = fmaxf(v, reinterpret_cast<const float*>(smem + PL::kOffVu)[w]);
+    if (v > 0.f) vu = v;
+  }
 
   // softmax rows: warpgroup i = warp / 4 owns Q tile i, thread r its row r =
   // query token ji + r / G, head r % G
@@ -326,24 +380,70 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
 
   if (warp < 8) {
     // ------------------------------------------------------------ softmax
+    float qexp = 1.f;                                    // one-byte caches: q's row scale undone
     {
       // Q row r of tile qt (128-byte swizzle; zeros for rows without a query)
       const uint16_t* qrow =
           p.q + ((static_cast<int64_t>(p.q_start[b]) + ji + (row_q ? jj : 0)) * p.num_q_heads +
                  kvh * group + g) * D;
       const uint32_t qbase = sb + PL::kOffQ + qt * PL::kQBytes + r * 128;
+      if constexpr (!kB8) {
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const uint32_t dst = qbase + (c >> 3) * PL::kQHalf + (((c & 7) ^ (r & 7)) << 4);
-        if (row_ok) cp_async_16(dst, qrow + 8 * c);
-        else st_shared_v4(dst, make_uint4(0, 0, 0, 0));
+        for (int c = 0; c < D / 8; ++c) {
+          const uint32_t dst = qbase + (c >> 3) * PL::kQHalf + (((c & 7) ^ (r & 7)) << 4);
+          if (row_ok) cp_async_16(dst, qrow + 8 * c);
+          else st_shared_v4(dst, make_uint4(0, 0, 0, 0));
+        }
+        cp_async_wait_all();
+      } else {
+        // f16 operands: a bf16 row enters as f16 times 2^e, e putting its
+        // largest magnitude in [2^13, 2^14) (exact for every value above 2^-28
+        // of it); qexp = 2^-e goes into the softmax multiplier
+        uint4 w[D / 8];
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c)
+          w[c] = row_ok ? __ldg(reinterpret_cast<const uint4*>(qrow) + c) : make_uint4(0, 0, 0, 0);
+        float scale = 1.f;
+        if constexpr (QT == PKV_BF16) {
+          float qmax = 0.f;
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) {
+            const uint32_t ww[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 f = Half16<PKV_BF16>::unpack(ww[k]);
+              qmax = fmaxf(qmax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+          }
+          if (qmax > 0.f) {
+            int ex;
+            frexpf(qmax, &ex);                            // qmax in [2^(ex-1), 2^ex)
+            scale = ldexpf(1.f, 14 - ex);
+            qexp = ldexpf(1.f, ex - 14);
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          uint4 h = w[c];
+          if constexpr (QT == PKV_BF16) {
+            const uint32_t ww[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
+            uint32_t hh[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 f = Half16<PKV_BF16>::unpack(ww[k]);
+              hh[k] = Half16<PKV_F16>::pack_rn(f.x * scale, f.y * scale);
+            }
+            h = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+          }
+          st_shared_v4(qbase + (c >> 3) * PL::kQHalf + (((c & 7) ^ (r & 7)) << 4), h);
+        }
       }
-      cp_async_wait_all();
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(PL::kBarQ));
     }
-    const float mult = p.softmax_scale * 1.4426950408889634f;
+    const float mult = p.softmax_scale * 1.4426950408889634f * qexp;
+    const float inv_vu = 1.f / vu;
     const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
     float m = -INFINITY;
 #pragma unroll 1
@@ -351,15 +451,22 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
       const int t0 = t * kWsKv;
       // the tile's 16-token pieces in an out-of-range block (bit j: piece j),
       // which take no part (the load warp reads them as zeros and flags them)
+      // One-byte caches: lane j < 8 also takes piece j's K scale and V scale / vu.
       uint32_t bad = 0;
-      if (any_bad) {
+      float pk = 0.f, pv = 0.f;
+      if (kB8 || any_bad) {
         const int tok = t0 + lane * kWsPiece;
-        bool b = false;
+        bool bb = false;
         if (lane < kWsPieces && tok < kv_end) {
           const int phys = __ldg(trow + tok / p.block_size);
-          b = phys < 0 || phys >= p.num_blocks;
+          bb = phys < 0 || phys >= p.num_blocks;
+          if (kB8 && !bb) {
+            const int64_t idx = static_cast<int64_t>(phys) * p.num_kv_heads + kvh;
+            pk = __ldg(p.scales + idx);
+            pv = __ldg(p.scales + per_kv + idx) * inv_vu;
+          }
         }
-        bad = __ballot_sync(0xffffffffu, b);
+        bad = __ballot_sync(0xffffffffu, bb);
       }
       // 1. row r of S_qt(t)
       bool ok = ws_wait(bar(PL::kBarSFull + qt), t & 1, abort_flag, p.dev_status);
@@ -373,7 +480,32 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
       tmem_ld128(t_s, sv);
       const bool full = t0 + kWsKv <= kv_end && t0 + kWsKv - 1 <= pos0 + ji && bad == 0;
       float tmax, pmul;
-      if (full) {
+      if constexpr (kB8) {
+        // each piece's column of scores times its K scale and this row's
+        // multiplier
+#pragma unroll
+        for (int j = 0; j < kWsPieces; ++j) {
+          const float kj = __shfl_sync(0xffffffffu, pk, j) * mult;
+          const uint64_t k2 = f2_pack(kj, kj);
+#pragma unroll
+          for (int c = 0; c < kWsPiece; c += 2) {
+            const float2 x = f2_unpack(f2_mul(f2_pack(sv[kWsPiece * j + c], sv[kWsPiece * j + c + 1]), k2));
+            sv[kWsPiece * j + c] = x.x;
+            sv[kWsPiece * j + c + 1] = x.y;
+          }
+        }
+        if (!full) {
+#pragma unroll
+          for (int c = 0; c < kWsKv; ++c) {
+            const int abs_t = t0 + c;
+            const bool valid = abs_t < kv_end && (!row_ok || abs_t <= pos) &&
+                               !((bad >> (c / kWsPiece)) & 1u);
+            if (!valid) sv[c] = -INFINITY;
+          }
+        }
+        tmax = row_max(sv);
+        pmul = 1.f;
+      } else if (full) {
         // (a negative scale turns the row's smallest score into its largest)
         tmax = (mult >= 0.f ? row_max(sv) : -row_max_neg(sv)) * mult;
         pmul = mult;
@@ -402,22 +534,26 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
       //    columns 32c .. 32c + 15, lo at 32c + 16 .. 32c + 31); exponent
       //    arguments, the lo parts and the row sum on packed fp32 pairs, the
       //    sum in two interleaved chains
+      //    One-byte caches: the pair is of P'' = p vs / vu (the token's V
+      //    scale over the range's largest), and the row sum stays in p.
       const uint64_t pm2 = f2_pack(pmul, pmul), nm2 = f2_pack(-m, -m);
       uint64_t lsum[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
       for (int c8 = 0; c8 < kWsKv / 8; ++c8) {
         uint32_t hw[4], lw[4];
+        const float vr = kB8 ? __shfl_sync(0xffffffffu, pv, c8 >> 1) : 1.f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int i = 8 * c8 + 2 * k;
           const float2 x = f2_unpack(f2_fma(f2_pack(sv[i], sv[i + 1]), pm2, nm2));
-          const uint64_t pp = f2_pack(ex2_ftz(x.x), ex2_ftz(x.y));
+          uint64_t pp = f2_pack(ex2_ftz(x.x), ex2_ftz(x.y));
           lsum[k & 1] = f2_add(lsum[k & 1], pp);
+          if constexpr (kB8) pp = f2_mul(pp, f2_pack(vr, vr));
           const float2 pf = f2_unpack(pp);
-          hw[k] = Half16<DT>::pack_rn(pf.x, pf.y);
-          const float2 f = Half16<DT>::unpack(hw[k]);
+          hw[k] = Half16<OT>::pack_rn(pf.x, pf.y);
+          const float2 f = Half16<OT>::unpack(hw[k]);
           const float2 d = f2_unpack(f2_sub(pp, f2_pack(f.x, f.y)));
-          lw[k] = Half16<DT>::pack_rn(d.x, d.y);
+          lw[k] = Half16<OT>::pack_rn(d.x, d.y);
         }
         // tokens 8 c8 .. 8 c8 + 7: chunk c8 / 4 of 32 tokens, its 4-column group c8 % 4
         const uint32_t col = 32 * (c8 >> 2) + 4 * (c8 & 3);
@@ -455,7 +591,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
   } else if (warp == kWsMmaWarp) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      constexpr bool kBf = DT == PKV_BF16;
+      constexpr bool kBf = OT == PKV_BF16;
       constexpr uint32_t kIdescS = umma_idesc(kBf, kWsRows, kWsKv, false);
       constexpr uint32_t kIdescO = umma_idesc(kBf, kWsRows, D, true);
       // S_i = Q_i K^T over head_dim in steps of 16 (32 bytes inside a
@@ -535,103 +671,176 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
       ws_drain(bar(PL::kBarFinal), 0, abort_flag, p.dev_status);
     }
     __syncwarp();
-  } else if (warp == kWsLoadWarp) {
-    // ------------------------------------------------------------ loads
-    const int nbh = p.num_blocks * p.num_kv_heads;      // the maps' outer extent
-    const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
-    int k_issued = 0, v_issued = 0;                     // tiles whose K / V copies were issued
-#pragma unroll 1
-    for (int t = 0; t < nt; ++t) {
-      const int st = t % S;
-      // K of tile t - S has been used by both S products
-      if (t >= S) {
-        const bool ok = ws_wait(bar(PL::kBarKEmpty + st), ((t / S) - 1) & 1, abort_flag, p.dev_status);
-        if (!__all_sync(0xffffffffu, ok)) break;
-      }
-      // lane j < 8 locates piece j (tokens t0 + 16 j ..): z = physical block *
-      // Hkv + kvh, y = offset in the block; past the range or in an
-      // out-of-range block, z = nbh, which the copies read as zeros
-      int z = nbh, y = 0, strad = 0;
-      if (lane < kWsPieces) {
-        const int tok = t * kWsKv + lane * kWsPiece;
-        if (tok < kv_end) {
-          const int logical = tok / p.block_size;
-          const int phys = __ldg(trow + logical);
-          if (phys >= 0 && phys < p.num_blocks) {
-            z = phys * p.num_kv_heads + kvh;
-            y = tok - logical * p.block_size;
-            strad = tok + kWsPiece > kv_end;
-          } else {
-            flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
+  } else if (warp >= kWsLoadWarp) {
+    if constexpr (!kB8) {
+      // ------------------------------------------------------------ loads
+      const int nbh = p.num_blocks * p.num_kv_heads;      // the maps' outer extent
+      const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
+      int k_issued = 0, v_issued = 0;                     // tiles whose K / V copies were issued
+  #pragma unroll 1
+      for (int t = 0; t < nt; ++t) {
+        const int st = t % S;
+        // K of tile t - S has been used by both S products
+        if (t >= S) {
+          const bool ok = ws_wait(bar(PL::kBarKEmpty + st), ((t / S) - 1) & 1, abort_flag, p.dev_status);
+          if (!__all_sync(0xffffffffu, ok)) break;
+        }
+        // lane j < 8 locates piece j (tokens t0 + 16 j ..): z = physical block *
+        // Hkv + kvh, y = offset in the block; past the range or in an
+        // out-of-range block, z = nbh, which the copies read as zeros
+        int z = nbh, y = 0, strad = 0;
+        if (lane < kWsPieces) {
+          const int tok = t * kWsKv + lane * kWsPiece;
+          if (tok < kv_end) {
+            const int logical = tok / p.block_size;
+            const int phys = __ldg(trow + logical);
+            if (phys >= 0 && phys < p.num_blocks) {
+              z = phys * p.num_kv_heads + kvh;
+              y = tok - logical * p.block_size;
+              strad = tok + kWsPiece > kv_end;
+            } else {
+              flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
+            }
           }
         }
-      }
-      int pz[kWsPieces], py[kWsPieces], ps[kWsPieces], nstrad = 0;
-#pragma unroll
-      for (int j = 0; j < kWsPieces; ++j) {
-        pz[j] = __shfl_sync(0xffffffffu, z, j);
-        py[j] = __shfl_sync(0xffffffffu, y, j);
-        ps[j] = __shfl_sync(0xffffffffu, strad, j);
-        nstrad += ps[j];
-      }
-      const uint32_t kst = sb + PL::kOffK + st * PL::kTileBytes;
-      const uint32_t vst = sb + PL::kOffV + st * PL::kTileBytes;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(PL::kBarKFull + st), kWsPieces * PL::kHalves * kWsBoxBytes);
-#pragma unroll
-        for (int j = 0; j < kWsPieces; ++j)
-#pragma unroll
-          for (int h = 0; h < PL::kHalves; ++h)
-            tma_load_3d(kst + h * PL::kKvHalf + j * kWsBoxBytes, &p.tmap_k, 64 * h, py[j], pz[j],
-                        bar(PL::kBarKFull + st));
-      }
-      k_issued = t + 1;
-      // V of tile t - S has been used by both P V products
-      if (t >= S) {
-        const bool ok = ws_wait(bar(PL::kBarVEmpty + st), ((t / S) - 1) & 1, abort_flag, p.dev_status);
-        if (!__all_sync(0xffffffffu, ok)) break;
-      }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(PL::kBarVFull + st),
-                              (kWsPieces - nstrad) * PL::kHalves * kWsBoxBytes);
-#pragma unroll
-        for (int j = 0; j < kWsPieces; ++j)
-          if (!ps[j])
-#pragma unroll
+        int pz[kWsPieces], py[kWsPieces], ps[kWsPieces], nstrad = 0;
+  #pragma unroll
+        for (int j = 0; j < kWsPieces; ++j) {
+          pz[j] = __shfl_sync(0xffffffffu, z, j);
+          py[j] = __shfl_sync(0xffffffffu, y, j);
+          ps[j] = __shfl_sync(0xffffffffu, strad, j);
+          nstrad += ps[j];
+        }
+        const uint32_t kst = sb + PL::kOffK + st * PL::kTileBytes;
+        const uint32_t vst = sb + PL::kOffV + st * PL::kTileBytes;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(PL::kBarKFull + st), kWsPieces * PL::kHalves * kWsBoxBytes);
+  #pragma unroll
+          for (int j = 0; j < kWsPieces; ++j)
+  #pragma unroll
             for (int h = 0; h < PL::kHalves; ++h)
-              tma_load_3d(vst + h * PL::kKvHalf + j * kWsBoxBytes, &p.tmap_v, 64 * h, py[j], pz[j],
-                          bar(PL::kBarVFull + st));
+              tma_load_3d(kst + h * PL::kKvHalf + j * kWsBoxBytes, &p.tmap_k, 64 * h, py[j], pz[j],
+                          bar(PL::kBarKFull + st));
+        }
+        k_issued = t + 1;
+        // V of tile t - S has been used by both P V products
+        if (t >= S) {
+          const bool ok = ws_wait(bar(PL::kBarVEmpty + st), ((t / S) - 1) & 1, abort_flag, p.dev_status);
+          if (!__all_sync(0xffffffffu, ok)) break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(PL::kBarVFull + st),
+                                (kWsPieces - nstrad) * PL::kHalves * kWsBoxBytes);
+  #pragma unroll
+          for (int j = 0; j < kWsPieces; ++j)
+            if (!ps[j])
+  #pragma unroll
+              for (int h = 0; h < PL::kHalves; ++h)
+                tma_load_3d(vst + h * PL::kKvHalf + j * kWsBoxBytes, &p.tmap_v, 64 * h, py[j], pz[j],
+                            bar(PL::kBarVFull + st));
+        }
+        // the straddling piece's V rows, copied by the lanes in the same
+        // swizzled layout, rows past the range end zero-filled
+  #pragma unroll
+        for (int j = 0; j < kWsPieces; ++j) {
+          if (!ps[j]) continue;
+          const int tok0 = t * kWsKv + j * kWsPiece;
+          const uint8_t* src0 =
+              p.v_cache + (static_cast<int64_t>(pz[j]) * p.block_size + py[j]) * (D * 2);
+          for (int idx = lane; idx < kWsPiece * (D / 8); idx += kWarp) {
+            const int rr = idx / (D / 8), c = idx % (D / 8);
+            const int row = j * kWsPiece + rr;
+            const uint32_t dst = vst + (c >> 3) * PL::kKvHalf + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+            const bool valid = tok0 + rr < kv_end;
+            cp_async_16_zfill(dst, valid ? src0 + rr * (D * 2) + c * 16 : p.v_cache, valid ? 16u : 0u);
+          }
+        }
+        cp_async_arrive_noinc(bar(PL::kBarVFull + st));
+        v_issued = t + 1;
       }
-      // the straddling piece's V rows, copied by the lanes in the same
-      // swizzled layout, rows past the range end zero-filled
-#pragma unroll
-      for (int j = 0; j < kWsPieces; ++j) {
-        if (!ps[j]) continue;
-        const int tok0 = t * kWsKv + j * kWsPiece;
-        const uint8_t* src0 =
-            p.v_cache + (static_cast<int64_t>(pz[j]) * p.block_size + py[j]) * (D * 2);
-        for (int idx = lane; idx < kWsPiece * (D / 8); idx += kWarp) {
-          const int rr = idx / (D / 8), c = idx % (D / 8);
-          const int row = j * kWsPiece + rr;
-          const uint32_t dst = vst + (c >> 3) * PL::kKvHalf + row * 128 + (((c & 7) ^ (row & 7)) << 4);
-          const bool valid = tok0 + rr < kv_end;
-          cp_async_16_zfill(dst, valid ? src0 + rr * (D * 2) + c * 16 : p.v_cache, valid ? 16u : 0u);
+      // the copies still in flight land before the CTA ends: the last fill of each stage
+      cp_async_wait_all();
+      if (lane == 0) {
+        for (int st = 0; st < S; ++st) {
+          const int kf = k_issued > st ? (k_issued - st + S - 1) / S : 0;
+          const int vf = v_issued > st ? (v_issued - st + S - 1) / S : 0;
+          if (kf > 0) ws_drain(bar(PL::kBarKFull + st), (kf - 1) & 1, abort_flag, p.dev_status);
+          if (vf > 0) ws_drain(bar(PL::kBarVFull + st), (vf - 1) & 1, abort_flag, p.dev_status);
         }
       }
-      cp_async_arrive_noinc(bar(PL::kBarVFull + st));
-      v_issued = t + 1;
-    }
-    // the copies still in flight land before the CTA ends: the last fill of each stage
-    cp_async_wait_all();
-    if (lane == 0) {
-      for (int st = 0; st < S; ++st) {
-        const int kf = k_issued > st ? (k_issued - st + S - 1) / S : 0;
-        const int vf = v_issued > st ? (v_issued - st + S - 1) / S : 0;
-        if (kf > 0) ws_drain(bar(PL::kBarKFull + st), (kf - 1) & 1, abort_flag, p.dev_status);
-        if (vf > 0) ws_drain(bar(PL::kBarVFull + st), (vf - 1) & 1, abort_flag, p.dev_status);
+      __syncwarp();
+
+    } else {
+      // ---------------------------------------------------------- code loads
+      // One-byte caches: the three load warps bring each tile's K and V codes
+      // with 16-byte loads through the block table and convert them exactly to
+      // f16 (E4M3 / E5M2 by cvt, INT8 as 1024 + (x + 128) - 1152) into the
+      // same swizzled operand layouts, zeros past the range or in an
+      // out-of-range block; each warp then fences its stores for the tensor
+      // cores and arrives once.
+      const int lt = (warp - kWsLoadWarp) * kWarp + lane;       // 0 .. 95
+      constexpr int kLoaders = R::kLoadWarps * kWarp;
+      constexpr int kItems = kWsKv * (D / 16);                  // 16-code chunks per tile
+      constexpr int kPer = (kItems + kLoaders - 1) / kLoaders;
+      const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
+      auto convert_tile = [&](const uint8_t* cache, uint32_t dst, int t) {
+        // lane j < 8: the first cache row of piece j, or -1
+        int64_t base = -1;
+        if (lane < kWsPieces) {
+          const int tok = t * kWsKv + lane * kWsPiece;
+          if (tok < kv_end) {
+            const int logical = tok / p.block_size;
+            const int phys = __ldg(trow + logical);
+            if (phys >= 0 && phys < p.num_blocks)
+              base = (static_cast<int64_t>(phys) * p.num_kv_heads + kvh) * p.block_size +
+                     (tok - logical * p.block_size);
+            else
+              flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
+          }
+        }
+        uint4 raw[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+          const int idx = lt + k * kLoaders;
+          const int rr = idx / (D / 16), cc = idx % (D / 16);
+          const int64_t rb = __shfl_sync(0xffffffffu, base, (rr / kWsPiece) & 7);
+          raw[k] = make_uint4(0, 0, 0, 0);
+          if (idx < kItems && rb >= 0 && t * kWsKv + rr < kv_end)
+            raw[k] = ld_global_nc_v4(cache + (rb + rr % kWsPiece) * D + cc * 16);
+        }
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+          const int idx = lt + k * kLoaders;
+          if (idx < kItems) {
+            const int rr = idx / (D / 16), cc = idx % (D / 16);
+            uint4 lo, hi;
+            codes16_to_f16<KV>(raw[k], lo, hi);
+            const int c0 = 2 * cc;                       // f16 chunks c0, c0 + 1 of row rr
+            const uint32_t row = dst + (c0 >> 3) * PL::kKvHalf + rr * 128;
+            st_shared_v4(row + (((c0 & 7) ^ (rr & 7)) << 4), lo);
+            st_shared_v4(row + ((((c0 + 1) & 7) ^ (rr & 7)) << 4), hi);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      };
+#pragma unroll 1
+      for (int t = 0; t < nt; ++t) {
+        const int st = t % S;
+        if (t >= S) {
+          const bool ok = ws_wait(bar(PL::kBarKEmpty + st), ((t / S) - 1) & 1, abort_flag, p.dev_status);
+          if (!__all_sync(0xffffffffu, ok)) break;
+        }
+        convert_tile(p.k_cache, sb + PL::kOffK + st * PL::kTileBytes, t);
+        if (lane == 0) mbar_arrive(bar(PL::kBarKFull + st));
+        if (t >= S) {
+          const bool ok = ws_wait(bar(PL::kBarVEmpty + st), ((t / S) - 1) & 1, abort_flag, p.dev_status);
+          if (!__all_sync(0xffffffffu, ok)) break;
+        }
+        convert_tile(p.v_cache, sb + PL::kOffV + st * PL::kTileBytes, t);
+        if (lane == 0) mbar_arrive(bar(PL::kBarVFull + st));
       }
     }
-    __syncwarp();
   }
 
   // ------------------------------------------------------------ output
@@ -644,7 +853,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
                      ((static_cast<int64_t>(p.q_start[b]) + ji + jj) * p.num_q_heads +
                       kvh * group + g) * D;
     if (all_ok && nt > 0) {
-      const float inv = (row_ok && l > 0.f) ? 1.f / l : 0.f;
+      // (one-byte caches: O is in units of vu)
+      const float inv = (row_ok && l > 0.f) ? (kB8 ? vu : 1.f) / l : 0.f;
 #pragma unroll
       for (int k = 0; k < D / 32; ++k) {
         float o[32];
@@ -653,10 +863,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_kernel(const __grid_
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint4 w;
-            w.x = Half16<DT>::pack_rn(o[8 * c] * inv, o[8 * c + 1] * inv);
-            w.y = Half16<DT>::pack_rn(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
-            w.z = Half16<DT>::pack_rn(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
-            w.w = Half16<DT>::pack_rn(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+            w.x = Half16<QT>::pack_rn(o[8 * c] * inv, o[8 * c + 1] * inv);
+            w.y = Half16<QT>::pack_rn(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
+            w.z = Half16<QT>::pack_rn(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
+            w.w = Half16<QT>::pack_rn(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
             reinterpret_cast<uint4*>(orow + 32 * k)[c] = w;
           }
         }
@@ -709,15 +919,19 @@ bool cache_map(CUtensorMap* map, const void* cache, int num_blocks, int num_kv_h
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int DT, int D>
+template <int KV, int QT, int D>
 cudaError_t launch_ws_t(const PrefillArgs& a, cudaStream_t st) {
   using PL = WsPlan<D>;
+  using R = WsRoles<KV>;
   WsParams p;
-  if (!cache_map(&p.tmap_k, a.k_cache, a.num_blocks, a.num_kv_heads, a.block_size, D) ||
-      !cache_map(&p.tmap_v, a.v_cache, a.num_blocks, a.num_kv_heads, a.block_size, D))
+  if (!R::kB8 &&
+      (!cache_map(&p.tmap_k, a.k_cache, a.num_blocks, a.num_kv_heads, a.block_size, D) ||
+       !cache_map(&p.tmap_v, a.v_cache, a.num_blocks, a.num_kv_heads, a.block_size, D)))
     return cudaErrorInvalidValue;
   p.q = static_cast<const uint16_t*>(a.q);
+  p.k_cache = static_cast<const uint8_t*>(a.k_cache);
   p.v_cache = static_cast<const uint8_t*>(a.v_cache);
+  p.scales = static_cast<const float*>(a.scales);
   p.block_tables = a.block_tables;
   p.context_lens = a.context_lens;
   p.q_start = a.q_start;
@@ -733,7 +947,7 @@ cudaError_t launch_ws_t(const PrefillArgs& a, cudaStream_t st) {
 #ifdef PKV_TEST_HOOKS
   p.test_drop_commit = getenv("PKV_TEST_DROP_COMMIT") != nullptr;
 #endif
-  auto kern = prefill_ws_kernel<DT, D>;
+  auto kern = prefill_ws_kernel<KV, QT, D>;
   static std::atomic<int> attr_set[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -748,20 +962,41 @@ cudaError_t launch_ws_t(const PrefillArgs& a, cudaStream_t st) {
   const int rows = 2 * (kWsRows / group);               // query tokens per CTA
   const dim3 grid(static_cast<unsigned>((a.max_query_len + rows - 1) / rows),
                   static_cast<unsigned>(a.num_kv_heads), static_cast<unsigned>(a.num_seqs));
-  return launch_pdl(kern, grid, dim3(kWsThreads), PL::kSmemRequest, st, p);
+  return launch_pdl(kern, grid, dim3(R::kThreads), PL::kSmemRequest, st, p);
+}
+
+template <int KV, int D>
+cudaError_t launch_ws_q(const PrefillArgs& a, cudaStream_t st) {
+  if constexpr (KV == PKV_F16 || KV == PKV_BF16) {
+    return launch_ws_t<KV, KV, D>(a, st);
+  } else {
+    return a.q_dtype == PKV_F16 ? launch_ws_t<KV, PKV_F16, D>(a, st)
+                                : launch_ws_t<KV, PKV_BF16, D>(a, st);
+  }
+}
+
+template <int D>
+cudaError_t launch_ws_d(const PrefillArgs& a, cudaStream_t st) {
+  switch (a.kv_dtype) {
+    case PKV_F16: return launch_ws_q<PKV_F16, D>(a, st);
+    case PKV_BF16: return launch_ws_q<PKV_BF16, D>(a, st);
+    case PKV_FP8_E4M3: return launch_ws_q<PKV_FP8_E4M3, D>(a, st);
+    case PKV_FP8_E5M2: return launch_ws_q<PKV_FP8_E5M2, D>(a, st);
+    case PKV_INT8: return launch_ws_q<PKV_INT8, D>(a, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
 bool prefill_ws_supported(const PrefillArgs& a) {
-  return (a.kv_dtype == PKV_F16 || a.kv_dtype == PKV_BF16) && (a.head_dim == 64 || a.head_dim == 128);
+  return (a.kv_dtype == PKV_F16 || a.kv_dtype == PKV_BF16 || is_blk8(a.kv_dtype)) &&
+         (a.head_dim == 64 || a.head_dim == 128);
 }
 
 cudaError_t launch_prefill_ws(const PrefillArgs& a, cudaStream_t st) {
   if (a.num_seqs == 0 || a.max_query_len == 0) return cudaSuccess;
-  if (a.kv_dtype == PKV_F16)
-    return a.head_dim == 64 ? launch_ws_t<PKV_F16, 64>(a, st) : launch_ws_t<PKV_F16, 128>(a, st);
-  return a.head_dim == 64 ? launch_ws_t<PKV_BF16, 64>(a, st) : launch_ws_t<PKV_BF16, 128>(a, st);
+  return a.head_dim == 64 ? launch_ws_d<64>(a, st) : launch_ws_d<128>(a, st);
 }
 
 }  // namespace pkv
