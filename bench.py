@@ -637,7 +637,7 @@ def run_copy(args, rank: int, world: int):
 
 def _prefill_kernel_name(kv_dtype: int) -> str:
     """The kernel paged_prefill_attention runs for this cache dtype."""
-    if os.environ.get("PKV_PREFILL_MODE") == "mma" or kv_dtype == W.INT4_G32:
+    if os.environ.get("PKV_PREFILL_MODE") == "mma":
         return "paged_decode_kernel (prefill mode, mma.sync)"
     return "prefill_ws_kernel (tcgen05, load / MMA / softmax warp roles)"
 

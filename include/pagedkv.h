@@ -243,12 +243,14 @@ int paged_decode_attention_with_write(const void* q, int q_dtype, const void* k_
  * Everything else as for paged_decode_attention (no workspace: no split-KV).
  * Supported: as paged_decode_attention, with num_q_heads / num_kv_heads in
  * {1, 2, 4, 8}.
- * F16/BF16, FP8 and INT8 caches (head_dim 64 or 128) run on the tcgen05 tensor cores
- * (accumulators in tensor memory); their waits on the tensor cores are
- * bounded, and one that runs out sets PKV_ERR_DEVICE_TIMEOUT in dev_status
- * and leaves the affected output rows zero.  Other caches, or the
- * environment variable PKV_PREFILL_MODE=mma (read on each call), use the
- * mma.sync kernel.  Both compute the same definition.
+ * Every cache dtype (head_dim 64 or 128) runs on the tcgen05 tensor cores
+ * (accumulators in tensor memory; INT4 caches dequantized into hi + lo
+ * operand pairs in the query's type, so with f16 queries their values must
+ * lie in the f16 range); the waits on the tensor cores are bounded, and one
+ * that runs out sets PKV_ERR_DEVICE_TIMEOUT in dev_status and leaves the
+ * affected output rows zero.  The environment variable PKV_PREFILL_MODE=mma
+ * (read on each call) selects the mma.sync kernel instead.  Both compute the
+ * same definition.
  */
 int paged_prefill_attention(const void* q, int q_dtype, const int32_t* q_start,
                             int max_query_len, const void* k_cache, const void* v_cache,

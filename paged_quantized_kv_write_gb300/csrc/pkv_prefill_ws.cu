@@ -70,19 +70,24 @@ namespace {
 using namespace tc;
 
 constexpr int kWsRows = 128;                         // query rows per Q tile (the MMA M)
-constexpr int kWsKv = 128;                           // KV tokens per tile
 constexpr int kWsPiece = 16;                         // tokens per TMA box
-constexpr int kWsPieces = kWsKv / kWsPiece;
 constexpr int kWsMmaWarp = 8;
 constexpr int kWsLoadWarp = 9;                       // the first load warp
 
 // The warps of a cache dtype: 0-7 softmax, 8 MMA, then the load warps: one
 // issuing TMA copies for 16-bit caches, three that load and convert the codes
-// for one-byte caches (12 warps still leave 168 registers per thread).
+// for one-byte and INT4 caches (12 warps still leave 168 registers per
+// thread).  INT4 caches dequantize into hi + lo operand pairs, which double
+// the K and V tiles, so they walk the cache in 64-token tiles.
 template <int KV> struct WsRoles {
   static constexpr bool kB8 = is_blk8(KV);
-  static constexpr int kLoadWarps = kB8 ? 3 : 1;
+  static constexpr bool kI4 = KV == PKV_INT4_G32;
+  static constexpr bool kConvert = kB8 || kI4;     // load warps convert the codes
+  static constexpr int kLoadWarps = kConvert ? 3 : 1;
   static constexpr int kThreads = (kWsLoadWarp + kLoadWarps) * kWarp;
+  static constexpr int kTok = kI4 ? 64 : 128;       // KV tokens per tile
+  static constexpr int kPieces = kTok / kWsPiece;
+  static constexpr int kParts = kI4 ? 2 : 1;        // operand tiles per K or V stage (hi, lo)
 };
 constexpr float kWsTau = 8.f;                        // lazy rescale threshold (log2 units)
 constexpr int kWsBoxBytes = kWsPiece * 128;          // one box: 16 rows of 128 bytes
@@ -92,16 +97,18 @@ constexpr int kWsBoxBytes = kWsPiece * 128;          // one box: 16 rows of 128 
 // owns columns [256 i, 256 i + 256): S [0, 128), overwritten by P (tokens
 // 32c .. 32c + 31: hi at columns 32c .. 32c + 15, lo at 32c + 16 .. 32c + 31),
 // and O [128, 128 + D).
-template <int D> struct WsPlan {
+template <int D, int KV> struct WsPlan {
+  using R = WsRoles<KV>;
   static constexpr int kHalves = D / 64;             // 128-byte column blocks per row
   static constexpr int kStages = D == 128 ? 2 : 3;
-  static constexpr int kTileBytes = kWsKv * D * 2;   // one K or V tile
-  static constexpr int kKvHalf = kWsKv * 128;        // one column block of a K or V tile
+  static constexpr int kTileBytes = R::kTok * D * 2;  // one K or V operand tile
+  static constexpr int kStageBytes = R::kParts * kTileBytes;
+  static constexpr int kKvHalf = R::kTok * 128;      // one column block of an operand tile
   static constexpr int kQBytes = kWsRows * D * 2;
   static constexpr int kQHalf = kWsRows * 128;
   static constexpr int kOffV = 0;
-  static constexpr int kOffK = kOffV + kStages * kTileBytes;
-  static constexpr int kOffQ = kOffK + kStages * kTileBytes;
+  static constexpr int kOffK = kOffV + kStages * kStageBytes;
+  static constexpr int kOffQ = kOffK + kStages * kStageBytes;
   static constexpr int kOffBar = kOffQ + 2 * kQBytes;
   // mbarriers: k_full, v_full, k_empty, v_empty per stage; q_full; s_full,
   // p_full, o_done per Q tile; final.  Then the tensor-memory address and the
@@ -221,7 +228,7 @@ __device__ __forceinline__ void ws_drain(uint32_t bar, uint32_t parity, volatile
 
 // 128 consecutive fp32 columns of this thread's tensor-memory lane in one
 // load, and its wait (the registers are defined only after both)
-__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[kWsKv]) {
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
   uint32_t r[128];
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n"
@@ -248,24 +255,51 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[kWsKv]) {
   for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// The largest of a row's 128 scores, and the largest of their negations, as
-// pairwise trees (seven dependent steps instead of 128)
-__device__ __forceinline__ float row_max(const float (&s)[kWsKv]) {
-  float v[kWsKv / 2];
+// 64 consecutive fp32 columns, likewise
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
 #pragma unroll
-  for (int i = 0; i < kWsKv / 2; ++i) v[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+template <int N>
+__device__ __forceinline__ void tmem_ld_row(uint32_t taddr, float (&v)[N]) {
+  if constexpr (N == 128) tmem_ld128(taddr, v);
+  else tmem_ld64(taddr, v);
+}
+
+// The largest of a row's N scores, and the largest of their negations, as
+// pairwise trees (log2 N dependent steps instead of N)
+template <int N>
+__device__ __forceinline__ float row_max(const float (&s)[N]) {
+  float v[N / 2];
 #pragma unroll
-  for (int n = kWsKv / 4; n >= 1; n >>= 1)
+  for (int i = 0; i < N / 2; ++i) v[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+  for (int n = N / 4; n >= 1; n >>= 1)
 #pragma unroll
     for (int i = 0; i < n; ++i) v[i] = fmaxf(v[2 * i], v[2 * i + 1]);
   return v[0];
 }
-__device__ __forceinline__ float row_max_neg(const float (&s)[kWsKv]) {
-  float v[kWsKv / 2];
+template <int N>
+__device__ __forceinline__ float row_max_neg(const float (&s)[N]) {
+  float v[N / 2];
 #pragma unroll
-  for (int i = 0; i < kWsKv / 2; ++i) v[i] = fmaxf(-s[2 * i], -s[2 * i + 1]);
+  for (int i = 0; i < N / 2; ++i) v[i] = fmaxf(-s[2 * i], -s[2 * i + 1]);
 #pragma unroll
-  for (int n = kWsKv / 4; n >= 1; n >>= 1)
+  for (int n = N / 4; n >= 1; n >>= 1)
 #pragma unroll
     for (int i = 0; i < n; ++i) v[i] = fmaxf(v[2 * i], v[2 * i + 1]);
   return v[0];
@@ -278,10 +312,11 @@ template <int KV, int QT, int D>
 __global__ void __launch_bounds__(WsRoles<KV>::kThreads, 1)
 prefill_ws_kernel(const __grid_constant__ WsParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  using PL = WsPlan<D>;
+  using PL = WsPlan<D, KV>;
   using R = WsRoles<KV>;
-  constexpr bool kB8 = R::kB8;
-  constexpr int OT = kB8 ? PKV_F16 : KV;               // operand type of the products
+  constexpr bool kB8 = R::kB8, kI4 = R::kI4;
+  constexpr int kWsKv = R::kTok, kWsPieces = R::kPieces;
+  constexpr int OT = kB8 ? PKV_F16 : QT;               // operand type of the products
   constexpr int S = PL::kStages;
   pdl_wait();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -317,8 +352,8 @@ prefill_ws_kernel(const __grid_constant__ WsParams p) {
     for (int s = 0; s < S; ++s) {
       // 16-bit: the TMA bytes (and, for V, the load warp's lanes); one-byte:
       // one arrival per load warp
-      mbar_init(bar(PL::kBarKFull + s), kB8 ? R::kLoadWarps : 1);
-      mbar_init(bar(PL::kBarVFull + s), kB8 ? R::kLoadWarps : 1 + kWarp);
+      mbar_init(bar(PL::kBarKFull + s), R::kConvert ? R::kLoadWarps : 1);
+      mbar_init(bar(PL::kBarVFull + s), R::kConvert ? R::kLoadWarps : 1 + kWarp);
       mbar_init(bar(PL::kBarKEmpty + s), 1);
       mbar_init(bar(PL::kBarVEmpty + s), 1);
     }
@@ -477,7 +512,7 @@ prefill_ws_kernel(const __grid_constant__ WsParams p) {
       //    below every row's causal limit need no mask; the scale then goes
       //    into the exponent's fma), and its largest value
       float sv[kWsKv];
-      tmem_ld128(t_s, sv);
+      tmem_ld_row<kWsKv>(t_s, sv);
       const bool full = t0 + kWsKv <= kv_end && t0 + kWsKv - 1 <= pos0 + ji && bad == 0;
       float tmax, pmul;
       if constexpr (kB8) {
@@ -596,22 +631,27 @@ prefill_ws_kernel(const __grid_constant__ WsParams p) {
       constexpr uint32_t kIdescO = umma_idesc(kBf, kWsRows, D, true);
       // S_i = Q_i K^T over head_dim in steps of 16 (32 bytes inside a
       // 128-byte swizzle row; the second column block in its own region)
+      // (INT4: K as its hi and then its lo operand tile, one sum)
       auto issue_s = [&](int i, int st) {
         const uint32_t qb = sb + PL::kOffQ + i * PL::kQBytes;
-        const uint32_t kb = sb + PL::kOffK + st * PL::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk & 3) * 32;
-          umma(tmem + 256 * i, sw128_desc(qb + (kk >> 2) * PL::kQHalf + off, 16),
-               sw128_desc(kb + (kk >> 2) * PL::kKvHalf + off, 16), kIdescS, kk > 0);
+        for (int part = 0; part < R::kParts; ++part) {
+          const uint32_t kb = sb + PL::kOffK + st * PL::kStageBytes + part * PL::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk & 3) * 32;
+            umma(tmem + 256 * i, sw128_desc(qb + (kk >> 2) * PL::kQHalf + off, 16),
+                 sw128_desc(kb + (kk >> 2) * PL::kKvHalf + off, 16), kIdescS, part > 0 || kk > 0);
+          }
         }
       };
       // O_i += P_i V: 16 tokens per product (two 8-token atoms of V, 8
       // tensor-memory columns of P: tokens 16kk .. sit at column
       // 32 (kk / 2) + 8 (kk % 2), their lo parts 16 columns on), the hi part
       // and then the lo part
+      // (INT4: P hi V hi, P lo V hi, P hi V lo)
       auto issue_pv = [&](int i, int st, bool acc) {
-        const uint32_t vb = sb + PL::kOffV + st * PL::kTileBytes;
+        const uint32_t vb = sb + PL::kOffV + st * PL::kStageBytes;
         const uint32_t o = tmem + 256 * i + 128;
 #pragma unroll
         for (int kk = 0; kk < kWsKv / 16; ++kk)
@@ -621,6 +661,12 @@ prefill_ws_kernel(const __grid_constant__ WsParams p) {
         for (int kk = 0; kk < kWsKv / 16; ++kk)
           umma_ts(o, tmem + 256 * i + 32 * (kk >> 1) + 16 + 8 * (kk & 1),
                   sw128_desc(vb + kk * 2048, PL::kKvHalf), kIdescO, 1u);
+        if constexpr (kI4) {
+#pragma unroll
+          for (int kk = 0; kk < kWsKv / 16; ++kk)
+            umma_ts(o, tmem + 256 * i + 32 * (kk >> 1) + 8 * (kk & 1),
+                    sw128_desc(vb + PL::kTileBytes + kk * 2048, PL::kKvHalf), kIdescO, 1u);
+        }
       };
       bool ok = nt == 0 || ws_wait(bar(PL::kBarQ), 0, abort_flag, p.dev_status);
 #pragma unroll 1
@@ -672,7 +718,7 @@ prefill_ws_kernel(const __grid_constant__ WsParams p) {
     }
     __syncwarp();
   } else if (warp >= kWsLoadWarp) {
-    if constexpr (!kB8) {
+    if constexpr (!R::kConvert) {
       // ------------------------------------------------------------ loads
       const int nbh = p.num_blocks * p.num_kv_heads;      // the maps' outer extent
       const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
@@ -711,8 +757,8 @@ prefill_ws_kernel(const __grid_constant__ WsParams p) {
           ps[j] = __shfl_sync(0xffffffffu, strad, j);
           nstrad += ps[j];
         }
-        const uint32_t kst = sb + PL::kOffK + st * PL::kTileBytes;
-        const uint32_t vst = sb + PL::kOffV + st * PL::kTileBytes;
+        const uint32_t kst = sb + PL::kOffK + st * PL::kStageBytes;
+        const uint32_t vst = sb + PL::kOffV + st * PL::kStageBytes;
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(PL::kBarKFull + st), kWsPieces * PL::kHalves * kWsBoxBytes);
   #pragma unroll
@@ -778,13 +824,20 @@ prefill_ws_kernel(const __grid_constant__ WsParams p) {
       // same swizzled operand layouts, zeros past the range or in an
       // out-of-range block; each warp then fences its stores for the tensor
       // cores and arrives once.
+      // INT4 caches: an item is one 32-element group of a token (16 bytes of
+      // codes and its fp16 scale and zero point); each element x = scale n +
+      // zero (one rounding in fp32) becomes a hi + lo pair in the query's
+      // 16-bit type, hi = x rounded, lo = (x - hi) rounded, into the stage's hi
+      // and lo operand tiles.
       const int lt = (warp - kWsLoadWarp) * kWarp + lane;       // 0 .. 95
       constexpr int kLoaders = R::kLoadWarps * kWarp;
-      constexpr int kItems = kWsKv * (D / 16);                  // 16-code chunks per tile
+      constexpr int kItemCols = kI4 ? 32 : 16;                  // elements per item
+      constexpr int kItems = kWsKv * (D / kItemCols);
       constexpr int kPer = (kItems + kLoaders - 1) / kLoaders;
       const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
-      auto convert_tile = [&](const uint8_t* cache, uint32_t dst, int t) {
-        // lane j < 8: the first cache row of piece j, or -1
+      const int64_t rows_total = static_cast<int64_t>(p.num_blocks) * p.num_kv_heads * p.block_size;
+      auto convert_tile = [&](const uint8_t* cache, int which, uint32_t dst, int t) {
+        // lane j < pieces: the first cache row of piece j, or -1
         int64_t base = -1;
         if (lane < kWsPieces) {
           const int tok = t * kWsKv + lane * kWsPiece;
@@ -798,27 +851,59 @@ prefill_ws_kernel(const __grid_constant__ WsParams p) {
               flag_status(p.dev_status, PKV_ERR_DEVICE_BOUNDS);
           }
         }
+        constexpr int kRowBytes = kI4 ? D / 2 : D;              // code bytes per cache row
         uint4 raw[kPer];
+        uint32_t szp[kPer];                                     // INT4: fp16 scale | zero << 16
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
           const int idx = lt + k * kLoaders;
-          const int rr = idx / (D / 16), cc = idx % (D / 16);
+          const int rr = idx / (D / kItemCols), cc = idx % (D / kItemCols);
           const int64_t rb = __shfl_sync(0xffffffffu, base, (rr / kWsPiece) & 7);
           raw[k] = make_uint4(0, 0, 0, 0);
-          if (idx < kItems && rb >= 0 && t * kWsKv + rr < kv_end)
-            raw[k] = ld_global_nc_v4(cache + (rb + rr % kWsPiece) * D + cc * 16);
+          szp[k] = 0;
+          if (idx < kItems && rb >= 0 && t * kWsKv + rr < kv_end) {
+            const int64_t row = rb + rr % kWsPiece;
+            raw[k] = ld_global_nc_v4(cache + row * kRowBytes + cc * 16);
+            if constexpr (kI4)
+              szp[k] = __ldg(reinterpret_cast<const uint32_t*>(p.scales) +
+                             (which * rows_total + row) * (D / 32) + cc);
+          }
         }
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
           const int idx = lt + k * kLoaders;
           if (idx < kItems) {
-            const int rr = idx / (D / 16), cc = idx % (D / 16);
-            uint4 lo, hi;
-            codes16_to_f16<KV>(raw[k], lo, hi);
-            const int c0 = 2 * cc;                       // f16 chunks c0, c0 + 1 of row rr
-            const uint32_t row = dst + (c0 >> 3) * PL::kKvHalf + rr * 128;
-            st_shared_v4(row + (((c0 & 7) ^ (rr & 7)) << 4), lo);
-            st_shared_v4(row + ((((c0 + 1) & 7) ^ (rr & 7)) << 4), hi);
+            const int rr = idx / (D / kItemCols), cc = idx % (D / kItemCols);
+            const uint32_t row = dst + rr * 128;
+            if constexpr (kI4) {
+              // f16 chunks 4 cc .. 4 cc + 3 of row rr, in the hi and the lo tile
+              const float sc = __half2float(__ushort_as_half(static_cast<uint16_t>(szp[k] & 0xFFFFu)));
+              const float zp = __half2float(__ushort_as_half(static_cast<uint16_t>(szp[k] >> 16)));
+              const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const uint32_t byte = (w[q4] >> (8 * e)) & 0xFFu;
+                  const float x0 = __fmaf_rn(sc, static_cast<float>(byte & 15u), zp);
+                  const float x1 = __fmaf_rn(sc, static_cast<float>(byte >> 4), zp);
+                  hw[e] = Half16<QT>::pack_rn(x0, x1);
+                  const float2 f = Half16<QT>::unpack(hw[e]);
+                  lw[e] = Half16<QT>::pack_rn(x0 - f.x, x1 - f.y);
+                }
+                const int c = 4 * cc + q4;
+                const uint32_t at = row + (c >> 3) * PL::kKvHalf + (((c & 7) ^ (rr & 7)) << 4);
+                st_shared_v4(at, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+                st_shared_v4(at + PL::kTileBytes, make_uint4(lw[0], lw[1], lw[2], lw[3]));
+              }
+            } else {
+              uint4 lo, hi;
+              codes16_to_f16<KV>(raw[k], lo, hi);
+              const int c0 = 2 * cc;                     // f16 chunks c0, c0 + 1 of row rr
+              st_shared_v4(row + (c0 >> 3) * PL::kKvHalf + (((c0 & 7) ^ (rr & 7)) << 4), lo);
+              st_shared_v4(row + ((c0 + 1) >> 3) * PL::kKvHalf + ((((c0 + 1) & 7) ^ (rr & 7)) << 4), hi);
+            }
           }
         }
         fence_proxy_async_smem();
@@ -831,13 +916,13 @@ prefill_ws_kernel(const __grid_constant__ WsParams p) {
           const bool ok = ws_wait(bar(PL::kBarKEmpty + st), ((t / S) - 1) & 1, abort_flag, p.dev_status);
           if (!__all_sync(0xffffffffu, ok)) break;
         }
-        convert_tile(p.k_cache, sb + PL::kOffK + st * PL::kTileBytes, t);
+        convert_tile(p.k_cache, 0, sb + PL::kOffK + st * PL::kStageBytes, t);
         if (lane == 0) mbar_arrive(bar(PL::kBarKFull + st));
         if (t >= S) {
           const bool ok = ws_wait(bar(PL::kBarVEmpty + st), ((t / S) - 1) & 1, abort_flag, p.dev_status);
           if (!__all_sync(0xffffffffu, ok)) break;
         }
-        convert_tile(p.v_cache, sb + PL::kOffV + st * PL::kTileBytes, t);
+        convert_tile(p.v_cache, 1, sb + PL::kOffV + st * PL::kStageBytes, t);
         if (lane == 0) mbar_arrive(bar(PL::kBarVFull + st));
       }
     }
@@ -921,10 +1006,10 @@ bool cache_map(CUtensorMap* map, const void* cache, int num_blocks, int num_kv_h
 
 template <int KV, int QT, int D>
 cudaError_t launch_ws_t(const PrefillArgs& a, cudaStream_t st) {
-  using PL = WsPlan<D>;
+  using PL = WsPlan<D, KV>;
   using R = WsRoles<KV>;
   WsParams p;
-  if (!R::kB8 &&
+  if (!R::kConvert &&
       (!cache_map(&p.tmap_k, a.k_cache, a.num_blocks, a.num_kv_heads, a.block_size, D) ||
        !cache_map(&p.tmap_v, a.v_cache, a.num_blocks, a.num_kv_heads, a.block_size, D)))
     return cudaErrorInvalidValue;
@@ -983,6 +1068,7 @@ cudaError_t launch_ws_d(const PrefillArgs& a, cudaStream_t st) {
     case PKV_FP8_E4M3: return launch_ws_q<PKV_FP8_E4M3, D>(a, st);
     case PKV_FP8_E5M2: return launch_ws_q<PKV_FP8_E5M2, D>(a, st);
     case PKV_INT8: return launch_ws_q<PKV_INT8, D>(a, st);
+    case PKV_INT4_G32: return launch_ws_q<PKV_INT4_G32, D>(a, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -990,7 +1076,8 @@ cudaError_t launch_ws_d(const PrefillArgs& a, cudaStream_t st) {
 }  // namespace
 
 bool prefill_ws_supported(const PrefillArgs& a) {
-  return (a.kv_dtype == PKV_F16 || a.kv_dtype == PKV_BF16 || is_blk8(a.kv_dtype)) &&
+  return (a.kv_dtype == PKV_F16 || a.kv_dtype == PKV_BF16 || is_blk8(a.kv_dtype) ||
+          a.kv_dtype == PKV_INT4_G32) &&
          (a.head_dim == 64 || a.head_dim == 128);
 }
 
