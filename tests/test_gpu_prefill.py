@@ -55,8 +55,8 @@ def _run(case, chunk, max_query_len=None, seed=0, ctx=None, tables=None, oracle_
 
 @pytest.fixture(params=["default", "mma"])
 def pf_mode(request, monkeypatch):
-    """default: tcgen05 for 16-bit and one-byte caches with head_dim 128, the
-    mma.sync kernel otherwise; mma: the mma.sync kernel for every call."""
+    """default: the warp-role tcgen05 kernel for every cache dtype; mma: the
+    mma.sync kernel for every call."""
     if request.param == "mma":
         monkeypatch.setenv("PKV_PREFILL_MODE", "mma")
     else:
