@@ -11,8 +11,8 @@ import torch
 import oracle
 import workloads as W
 
-# max-abs tolerances on the attention output (the benchmark spec): 2e-3 for 16-bit
-# KV, 5e-3 for FP8/INT4 against the oracle on the same dequantized values.
+# max-abs tolerances on the attention output: 2e-3 for 16-bit KV, 5e-3 for
+# FP8/INT4 against the oracle on the same dequantized values.
 TOL = {W.F16: 2e-3, W.BF16: 2e-3, W.FP8_E4M3: 5e-3, W.INT4_G32: 5e-3, W.FP8_E5M2: 5e-3,
        W.INT8: 5e-3}
 
