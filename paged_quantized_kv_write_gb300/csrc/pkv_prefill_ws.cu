@@ -119,9 +119,9 @@ template <int D, int KV> struct WsPlan {
   static constexpr int kBarPFull = kBarSFull + 2, kBarODone = kBarPFull + 2;
   static constexpr int kBarFinal = kBarODone + 2, kNumBars = kBarFinal + 1;
   static constexpr int kOffSlot = kOffBar + 8 * kNumBars;
-  // one-byte caches: each warp's largest V scale over the CTA's blocks
+  // one-byte caches: each softmax warp's largest V scale over the CTA's blocks
   static constexpr int kOffVu = kOffSlot + 16;
-  static constexpr int kSmem = kOffVu + 16 * 4;
+  static constexpr int kSmem = kOffVu + 8 * 4;
   // one CTA per SM: it takes all of tensor memory, so the request is at least
   // half of shared memory
   static constexpr int kSmemRequest = kSmem > 120 * 1024 ? kSmem : 120 * 1024;
@@ -199,6 +199,17 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo) {
          (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
          (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
          (static_cast<uint64_t>(2) << 61);
+}
+
+// OR of `pred` over the eight softmax warps (named barrier 1, 256 threads);
+// the barrier also orders their shared-memory stores before it.
+__device__ __forceinline__ bool softmax_bar_or(bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(out) : "r"(pred ? 1u : 0u) : "memory");
+  return out != 0;
 }
 
 // Bounded wait for phase `parity` that also ends when another role has set
@@ -367,39 +378,11 @@ prefill_ws_kernel(const __grid_constant__ WsParams p) {
     mbar_init_fence();
     *abort_flag = 0;
   }
-  // whether any block of the range is out of the pool (then the softmax looks
-  // up each tile's pieces; a table of valid ids costs it nothing), and for
-  // one-byte caches the largest V scale of the range's blocks (vu)
-  bool bad_here = false;
-  float vmax_here = 0.f;
-  const int64_t per_kv = static_cast<int64_t>(p.num_blocks) * p.num_kv_heads;
-  {
-    const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
-    const int nblk = (kv_end + p.block_size - 1) / p.block_size;
-    for (int i = tid; i < nblk; i += R::kThreads) {
-      const int phys = __ldg(trow + i);
-      const bool bad = phys < 0 || phys >= p.num_blocks;
-      bad_here |= bad;
-      if (kB8 && !bad)
-        vmax_here = fmaxf(vmax_here, __ldg(p.scales + per_kv + static_cast<int64_t>(phys) * p.num_kv_heads + kvh));
-    }
-  }
-  if constexpr (kB8) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) vmax_here = fmaxf(vmax_here, __shfl_xor_sync(0xffffffffu, vmax_here, o));
-    if (lane == 0) reinterpret_cast<float*>(smem + PL::kOffVu)[warp] = vmax_here;
-  }
   tc_fence_before();
-  const bool any_bad = __syncthreads_or(bad_here) != 0;
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  // V scales enter P as vs / vu <= 1 (a range without written V blocks: vu 1)
-  float vu = 1.f;
-  if constexpr (kB8) {
-    float v = 0.f;
-    for (int w = 0; w < R::kThreads / kWarp; ++w) v = fmaxf(v, reinterpret_cast<const float*>(smem + PL::kOffVu)[w]);
-    if (v > 0.f) vu = v;
-  }
+  const int64_t per_kv = static_cast<int64_t>(p.num_blocks) * p.num_kv_heads;
 
   // softmax rows: warpgroup i = warp / 4 owns Q tile i, thread r its row r =
   // query token ji + r / G, head r % G
@@ -412,6 +395,7 @@ prefill_ws_kernel(const __grid_constant__ WsParams p) {
   const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
   const uint32_t t_s = tmem + lane_base + 256 * qt;    // S and P; O at + 128
   float l = 0.f;
+  float vu = 1.f;                                      // one-byte caches: the V scale unit
 
   if (warp < 8) {
     // ------------------------------------------------------------ softmax
@@ -478,8 +462,38 @@ prefill_ws_kernel(const __grid_constant__ WsParams p) {
       if (lane == 0) mbar_arrive(bar(PL::kBarQ));
     }
     const float mult = p.softmax_scale * 1.4426950408889634f * qexp;
-    const float inv_vu = 1.f / vu;
     const int32_t* trow = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
+    // While tile 0's loads and S product run, the 256 softmax threads scan the
+    // CTA's blocks: whether any is out of the pool (then each tile's pieces are
+    // looked up; a table of valid ids costs the tiles nothing) and, for
+    // one-byte caches, the largest V scale vu (V scales enter P as vs / vu <= 1;
+    // a range without written V blocks: vu 1).
+    bool any_bad;
+    {
+      const int nblk = (kv_end + p.block_size - 1) / p.block_size;
+      bool bad_here = false;
+      float vmax = 0.f;
+      for (int i = tid; i < nblk; i += 256) {
+        const int phys = __ldg(trow + i);
+        const bool bad = phys < 0 || phys >= p.num_blocks;
+        bad_here |= bad;
+        if (kB8 && !bad)
+          vmax = fmaxf(vmax, __ldg(p.scales + per_kv + static_cast<int64_t>(phys) * p.num_kv_heads + kvh));
+      }
+      if constexpr (kB8) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+        if (lane == 0) reinterpret_cast<float*>(smem + PL::kOffVu)[warp] = vmax;
+      }
+      any_bad = softmax_bar_or(bad_here);
+      if constexpr (kB8) {
+        vmax = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) vmax = fmaxf(vmax, reinterpret_cast<const float*>(smem + PL::kOffVu)[w]);
+        if (vmax > 0.f) vu = vmax;
+      }
+    }
+    const float inv_vu = 1.f / vu;
     float m = -INFINITY;
 #pragma unroll 1
     for (int t = 0; t < nt; ++t) {
@@ -939,7 +953,7 @@ prefill_ws_kernel(const __grid_constant__ WsParams p) {
                       kvh * group + g) * D;
     if (all_ok && nt > 0) {
       // (one-byte caches: O is in units of vu)
-      const float inv = (row_ok && l > 0.f) ? (kB8 ? vu : 1.f) / l : 0.f;
+      const float inv = (row_ok && l > 0.f) ? vu / l : 0.f;
 #pragma unroll
       for (int k = 0; k < D / 32; ++k) {
         float o[32];
