@@ -1030,20 +1030,19 @@ paged_decode_kernel(const Params p) {
         }
 
         // ------------------------------------------------ online softmax over the tile
+        // this lane's rows' max per head (the eight lanes of a head column are
+        // reduced only when the running max has to move)
         float tmax0 = -INFINITY, tmax1 = -INFINITY;
 #pragma unroll
         for (int u = 0; u < G::kSub; ++u) {
           tmax0 = fmaxf(tmax0, fmaxf(scs[u][0], scs[u][2]));
           tmax1 = fmaxf(tmax1, fmaxf(scs[u][1], scs[u][3]));
         }
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-          tmax0 = fmaxf(tmax0, __shfl_xor_sync(0xffffffffu, tmax0, o));
-          tmax1 = fmaxf(tmax1, __shfl_xor_sync(0xffffffffu, tmax1, o));
-        }
         // Lazy rescale: the running max moves (and O, l, the INT4 zero sums are
         // rescaled) only when some head's tile max exceeds it by more than kTau,
-        // or when the FP8 reference V scale must be rebased.
+        // or when the FP8 reference V scale must be rebased.  Some lane's row
+        // max exceeds its head's running max + kTau exactly when the head's
+        // tile max does, so the test needs no reduction across lanes.
         // A block whose FP8 scale is 0 was never written: its V rows dequantize
         // to 0 and add nothing (its scores still count in the softmax sum).
         bool von[G::kSub];
@@ -1066,6 +1065,11 @@ paged_decode_kernel(const Params p) {
         }
         const bool grow = tmax0 > mrow[0] + kTau || tmax1 > mrow[1] + kTau;
         if (__any_sync(0xffffffffu, grow) || rebase) {
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) {
+            tmax0 = fmaxf(tmax0, __shfl_xor_sync(0xffffffffu, tmax0, o));
+            tmax1 = fmaxf(tmax1, __shfl_xor_sync(0xffffffffu, tmax1, o));
+          }
           const float mnew0 = fmaxf(mrow[0], tmax0), mnew1 = fmaxf(mrow[1], tmax1);
           // mnew is finite: at least one token of the tile is valid
           float alpha0 = fast_exp2(mrow[0] - mnew0), alpha1 = fast_exp2(mrow[1] - mnew1);
