@@ -293,6 +293,19 @@ __device__ __forceinline__ void tmem_ld_row(uint32_t taddr, float (&v)[N]) {
 
 // The largest of a row's N scores, and the largest of their negations, as
 // pairwise trees (log2 N dependent steps instead of N)
+// Scores of the 16-token pieces flagged in `bad` (bit j: piece j; the same
+// for the whole warp) set to -inf.
+template <int N>
+__device__ __forceinline__ void mask_pieces(float (&s)[N], uint32_t bad) {
+  if (bad == 0) return;
+#pragma unroll
+  for (int j = 0; j < N / kWsPiece; ++j)
+    if ((bad >> j) & 1u) {
+#pragma unroll
+      for (int c = 0; c < kWsPiece; ++c) s[kWsPiece * j + c] = -INFINITY;
+    }
+}
+
 template <int N>
 __device__ __forceinline__ float row_max(const float (&s)[N]) {
   float v[N / 2];
@@ -547,10 +560,10 @@ prefill_ws_kernel(const __grid_constant__ WsParams p) {
 #pragma unroll
           for (int c = 0; c < kWsKv; ++c) {
             const int abs_t = t0 + c;
-            const bool valid = abs_t < kv_end && (!row_ok || abs_t <= pos) &&
-                               !((bad >> (c / kWsPiece)) & 1u);
+            const bool valid = abs_t < kv_end && (!row_ok || abs_t <= pos);
             if (!valid) sv[c] = -INFINITY;
           }
+          mask_pieces(sv, bad);
         }
         tmax = row_max(sv);
         pmul = 1.f;
@@ -562,10 +575,10 @@ prefill_ws_kernel(const __grid_constant__ WsParams p) {
 #pragma unroll
         for (int c = 0; c < kWsKv; ++c) {
           const int abs_t = t0 + c;
-          const bool valid = abs_t < kv_end && (!row_ok || abs_t <= pos) &&
-                             !((bad >> (c / kWsPiece)) & 1u);
+          const bool valid = abs_t < kv_end && (!row_ok || abs_t <= pos);
           sv[c] = valid ? sv[c] * mult : -INFINITY;
         }
+        mask_pieces(sv, bad);
         tmax = row_max(sv);
         pmul = 1.f;
       }
