@@ -17,6 +17,83 @@ namespace {
 // head_dim values [EPT l, EPT l + EPT) of the sum.  The partitions are taken
 // in blocks of 32: lane j computes the weight of partition 32k + j of its
 // warp's block k, the warp then walks the block with eight independent
+// One lane's EPT values of row i of a partial output, i < np.
+template <int EPT>
+__device__ __forceinline__ void load_partial(const float* src, float (&v)[EPT]) {
+  if constexpr (EPT == 4) {
+    const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+  } else {
+    const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+    v[0] = x.x; v[1] = x.y;
+  }
+}
+
+// Log-sum-exp merge of np partial states: state i is (m_i, l_i) at
+// ml + ml_step * i and its normalised output row at o + o_step * i (this
+// lane's EPT values).  The warp takes the chunks of 32 states from base0 in
+// steps of bstride; acc = sum_i l_i 2^(m_i - M) O_i and L = this lane's share
+// of sum_i l_i 2^(m_i - M), M the largest m_i of all np states.  The first
+// chunk's states and its first kPre rows are loaded together, before M is
+// known, so that the merge waits for one round of loads rather than three.
+template <int EPT, int kPre, int kStep>
+__device__ __forceinline__ void merge_states(const float* ml, int64_t ml_step, const float* o,
+                                             int64_t o_step, int np, int base0, int bstride,
+                                             int lane, float (&acc)[EPT], float& L) {
+  const int i0 = base0 + lane;
+  float2 st0 = make_float2(-INFINITY, 0.f);
+  if (i0 < np) st0 = __ldcg(reinterpret_cast<const float2*>(ml + ml_step * i0));
+  float v0[kPre][EPT];
+#pragma unroll
+  for (int u = 0; u < kPre; ++u)
+    if (base0 + u < np) load_partial<EPT>(o + static_cast<int64_t>(base0 + u) * o_step, v0[u]);
+  float M = -INFINITY;
+  for (int i = lane; i < np; i += kWarp) M = fmaxf(M, i == i0 ? st0.x : __ldcg(ml + ml_step * i));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) acc[e] = 0.f;
+  L = 0.f;
+  if (M == -INFINITY) return;
+  for (int base = base0; base < np; base += bstride) {
+    float2 st = st0;
+    if (base != base0) {
+      const int i = base + lane;
+      st = i < np ? __ldcg(reinterpret_cast<const float2*>(ml + ml_step * i))
+                  : make_float2(-INFINITY, 0.f);
+    }
+    const float wgt = st.x == -INFINITY ? 0.f : st.y * exp2f(st.x - M);
+    L += wgt;
+    const int n = min(kWarp, np - base);
+    int j = 0;
+    if (base == base0) {
+#pragma unroll
+      for (int u = 0; u < kPre; ++u) {
+        const float wj = __shfl_sync(0xffffffffu, wgt, u);
+        if (u < n) {
+#pragma unroll
+          for (int e = 0; e < EPT; ++e) acc[e] = fmaf(wj, v0[u][e], acc[e]);
+        }
+      }
+      j = kPre;
+    }
+    for (; j < n; j += kStep) {
+      float v[kStep][EPT];
+#pragma unroll
+      for (int u = 0; u < kStep; ++u)
+        if (j + u < n) load_partial<EPT>(o + static_cast<int64_t>(base + j + u) * o_step, v[u]);
+#pragma unroll
+      for (int u = 0; u < kStep; ++u) {
+        const float wj = __shfl_sync(0xffffffffu, wgt, (j + u) & 31);
+        if (j + u < n) {
+#pragma unroll
+          for (int e = 0; e < EPT; ++e) acc[e] = fmaf(wj, v[u][e], acc[e]);
+        }
+      }
+    }
+  }
+}
+
 // 16-byte (8-byte at head_dim 64) loads in flight per lane, each weight
 // handed out by a shuffle; the W warps' sums meet in shared memory.
 template <int QT, int D, int W>
@@ -34,50 +111,9 @@ pkv_lse_reduce(const Params p) {
   const float* ml = p.ws_ml + head * p.num_partitions * 2;
   const float* o = p.ws_out + head * p.num_partitions * D + EPT * lane;
   constexpr int64_t ml_step = 2, o_step = D;
-  float M = -INFINITY;
-  for (int i = lane; i < np; i += kWarp) M = fmaxf(M, __ldcg(ml + ml_step * i));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float acc[EPT];
-#pragma unroll
-  for (int e = 0; e < EPT; ++e) acc[e] = 0.f;
-  float L = 0.f;
-  if (M != -INFINITY) {
-    for (int base = warp * kWarp; base < np; base += W * kWarp) {
-      const int i = base + lane;
-      float wgt = 0.f;
-      if (i < np) {
-        const float m = __ldcg(ml + ml_step * i);
-        wgt = m == -INFINITY ? 0.f : __ldcg(ml + ml_step * i + 1) * exp2f(m - M);
-      }
-      L += wgt;
-      const int n = min(kWarp, np - base);
-      for (int j = 0; j < n; j += 8) {
-        float v[8][EPT];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float* src = o + static_cast<int64_t>(base + j + u) * o_step;
-          if (j + u < n) {
-            if constexpr (EPT == 4) {
-              const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
-              v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
-            } else {
-              const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
-              v[u][0] = x.x; v[u][1] = x.y;
-            }
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float wj = __shfl_sync(0xffffffffu, wgt, (j + u) & 31);
-          if (j + u < n) {
-#pragma unroll
-            for (int e = 0; e < EPT; ++e) acc[e] = fmaf(wj, v[u][e], acc[e]);
-          }
-        }
-      }
-    }
-  }
+  float L;
+  merge_states<EPT, 8, 8>(ml, ml_step, o, o_step, np, warp * kWarp, W * kWarp, lane, acc, L);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
   if constexpr (W > 1) {
@@ -110,7 +146,7 @@ pkv_lse_reduce(const Params p) {
 // that this chain overlaps the decode kernel's end; then each warp merges its
 // head's pieces (slots w + pair, see bal_unit) as pkv_lse_reduce does.
 template <int QT, int D, int kTok>
-__global__ void __launch_bounds__(8 * kWarp)
+__global__ void __launch_bounds__(8 * kWarp, 4)
 pkv_bal_merge(const Params p) {
   constexpr int EPT = D / kWarp;
   __shared__ int s_before[8], s_all[8];            // per warp: tiles before sequence b, in all
@@ -167,50 +203,9 @@ pkv_bal_merge(const Params p) {
   const float* ml = p.ws_ml + (static_cast<int64_t>(first) * group + g) * 2;
   const float* o = p.ws_out + (static_cast<int64_t>(first) * group + g) * D + EPT * lane;
   const int64_t ml_step = 2 * group, o_step = static_cast<int64_t>(group) * D;
-  float M = -INFINITY;
-  for (int i = lane; i < np; i += kWarp) M = fmaxf(M, __ldcg(ml + ml_step * i));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float acc[EPT];
-#pragma unroll
-  for (int e = 0; e < EPT; ++e) acc[e] = 0.f;
-  float L = 0.f;
-  if (M != -INFINITY) {
-    for (int base = 0; base < np; base += kWarp) {
-      const int i = base + lane;
-      float wgt = 0.f;
-      if (i < np) {
-        const float m = __ldcg(ml + ml_step * i);
-        wgt = m == -INFINITY ? 0.f : __ldcg(ml + ml_step * i + 1) * exp2f(m - M);
-      }
-      L += wgt;
-      const int n = min(kWarp, np - base);
-      for (int j = 0; j < n; j += 4) {
-        float v[4][EPT];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float* src = o + static_cast<int64_t>(base + j + u) * o_step;
-          if (j + u < n) {
-            if constexpr (EPT == 4) {
-              const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
-              v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
-            } else {
-              const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
-              v[u][0] = x.x; v[u][1] = x.y;
-            }
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float wj = __shfl_sync(0xffffffffu, wgt, (j + u) & 31);
-          if (j + u < n) {
-#pragma unroll
-            for (int e = 0; e < EPT; ++e) acc[e] = fmaf(wj, v[u][e], acc[e]);
-          }
-        }
-      }
-    }
-  }
+  float L;
+  merge_states<EPT, 4, 4>(ml, ml_step, o, o_step, np, 0, kWarp, lane, acc, L);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
   const float inv = L > 0.f ? 1.f / L : 0.f;
