@@ -306,27 +306,45 @@ __device__ __forceinline__ void mask_pieces(float (&s)[N], uint32_t bad) {
     }
 }
 
-template <int N>
-__device__ __forceinline__ float row_max(const float (&s)[N]) {
-  float v[N / 2];
+// Three-input max and min (sm_100 and later): a row's 128 values reduce in
+// 65 instructions over a tree of depth 5 instead of 127 over depth 7.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+template <bool kMin, int N>
+__device__ __forceinline__ float tree_reduce3(const float (&v)[N]) {
+  if constexpr (N == 1) {
+    return v[0];
+  } else {
+    constexpr int M = (N + 2) / 3;
+    float w[M];
 #pragma unroll
-  for (int i = 0; i < N / 2; ++i) v[i] = fmaxf(s[2 * i], s[2 * i + 1]);
-#pragma unroll
-  for (int n = N / 4; n >= 1; n >>= 1)
-#pragma unroll
-    for (int i = 0; i < n; ++i) v[i] = fmaxf(v[2 * i], v[2 * i + 1]);
-  return v[0];
+    for (int i = 0; i < M; ++i) {
+      if (3 * i + 2 < N)
+        w[i] = kMin ? fmin3(v[3 * i], v[3 * i + 1], v[3 * i + 2]) : fmax3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+      else if (3 * i + 1 < N)
+        w[i] = kMin ? fminf(v[3 * i], v[3 * i + 1]) : fmaxf(v[3 * i], v[3 * i + 1]);
+      else
+        w[i] = v[3 * i];
+    }
+    return tree_reduce3<kMin, M>(w);
+  }
 }
 template <int N>
+__device__ __forceinline__ float row_max(const float (&s)[N]) {
+  return tree_reduce3<false, N>(s);
+}
+// the largest of -s (= -min s)
+template <int N>
 __device__ __forceinline__ float row_max_neg(const float (&s)[N]) {
-  float v[N / 2];
-#pragma unroll
-  for (int i = 0; i < N / 2; ++i) v[i] = fmaxf(-s[2 * i], -s[2 * i + 1]);
-#pragma unroll
-  for (int n = N / 4; n >= 1; n >>= 1)
-#pragma unroll
-    for (int i = 0; i < n; ++i) v[i] = fmaxf(v[2 * i], v[2 * i + 1]);
-  return v[0];
+  return -tree_reduce3<true, N>(s);
 }
 
 // KV: the cache dtype; QT: the query dtype; the operands of the products are
