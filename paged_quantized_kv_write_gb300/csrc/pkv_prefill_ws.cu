@@ -1,17 +1,18 @@
 // Chunked-prefill attention on the tcgen05 tensor cores, with warp roles,
-// for 16-bit caches (F16, BF16) and one-byte caches (FP8 E4M3 / E5M2, INT8;
-// one fp32 scale per block and KV head).  Chunked prefill is a dense
+// for 16-bit caches (F16, BF16), one-byte caches (FP8 E4M3 / E5M2, INT8; one
+// fp32 scale per block and KV head) and INT4 caches (groups of 32 along
+// head_dim with an fp16 scale and zero point per token).  Chunked prefill is a dense
 // contraction (every cached token meets a whole chunk of queries), unlike the
 // decode step, so it runs where the dense tensor throughput is: "Optimizing
 // KV-Cache Memory Footprint in High-Throughput LLM Serving", section 5, pairs
 // PagedAttention with GQA and chunked prefill; query j of a chunk of n over c
 // cached tokens sits at position c - n + j and sees tokens 0 .. c - n + j.
 //
-// One CTA per SM (320 threads, 384 for one-byte caches; all 512
+// One CTA per SM (320 threads, 384 for one-byte and INT4 caches; all 512
 // tensor-memory columns) takes two adjacent Q tiles of 128 query rows each --
 // 128/G query tokens of one sequence times the G query heads of one KV head
-// per tile -- and walks that KV head's cache in 128-token tiles, K and V of a
-// tile shared by both Q tiles:
+// per tile -- and walks that KV head's cache in 128-token tiles (INT4: 64),
+// K and V of a tile shared by both Q tiles:
 //  * load warp (warp 9, 16-bit caches): looks up the tile's eight 16-token
 //    pieces in the block table and brings K and V into rings of two (head_dim
 //    64: three) stages with TMA tensor copies (a 16 x 64 box per piece and
@@ -25,6 +26,10 @@
 //    loads through the block table and convert them exactly to f16 operands
 //    in the same layouts (E4M3 / E5M2 by cvt, INT8 as 1024 + (x + 128) -
 //    1152), zeros past the range or in an out-of-range block;
+//  * load warps (warps 9-11, INT4 caches, 64-token tiles): dequantize each
+//    element once, x = scale n + zero in fp32, into a hi + lo pair of the
+//    query's 16-bit type, written to a hi and a lo operand tile; S sums the
+//    products with both, O takes P_hi V_hi + P_lo V_hi + P_hi V_lo;
 //  * MMA warp (warp 8, one lane): S_A = Q_A K^T, then O_B += P_B V of the
 //    previous tile, then S_B = Q_B K^T, then O_A += P_A V, so that each
 //    softmax warpgroup works while the tensor cores serve the other tile;
@@ -33,8 +38,9 @@
 //    instruction large;
 //  * softmax warpgroups (warps 0-3: tile A, 4-7: tile B): thread r reads row
 //    r of S from tensor memory, applies the causal mask and the online
-//    softmax (running max raised lazily, by more than 2^8 only, O rescaled in
-//    tensor memory when it is), writes row r of P as a 16-bit hi + lo pair
+//    softmax (the row max over a tree of three-input max instructions; the
+//    running max raised lazily, by more than 2^8 only, O rescaled in tensor
+//    memory when it is), writes row r of P as a 16-bit hi + lo pair
 //    over S's own columns and signals the MMA warp.  The tensor cores run a
 //    thread's products in issue order, so S(t + 1), issued after P V(t),
 //    overwrites P(t) only after that product has read it.
@@ -42,8 +48,8 @@
 // row (exact for every value above 2^-28 of the row's largest), taken off in
 // the softmax multiplier; each token's K block scale multiplies its score
 // column; its V block scale enters P as vs / vu, vu the largest V scale of the
-// CTA's blocks (found before the tiles), so P'' = p vs / vu <= p and the
-// output is O / l times vu.
+// CTA's blocks (found by the softmax threads while tile 0 loads), so
+// P'' = p vs / vu <= p and the output is O / l times vu.
 // Shared-memory operands use the canonical 128-byte-swizzle layouts: Q and K
 // K-major (rows of 128 bytes, 8-row atoms 1024 bytes apart, the second half
 // of head_dim 128 in its own region), V MN-major (token rows of 128 bytes, 8
