@@ -106,6 +106,7 @@ constexpr int kWsBoxBytes = kWsPiece * 128;          // one box: 16 rows of 128 
 template <int D, int KV> struct WsPlan {
   using R = WsRoles<KV>;
   static constexpr int kHalves = D / 64;             // 128-byte column blocks per row
+  static_assert(kHalves == 1 || kHalves == 2, "head_dim 64 or 128");
   static constexpr int kStages = D == 128 ? 2 : 3;
   static constexpr int kTileBytes = R::kTok * D * 2;  // one K or V operand tile
   static constexpr int kStageBytes = R::kParts * kTileBytes;
