@@ -25,11 +25,14 @@ def _full_cache(case):
     return k, v, s
 
 
-def _run(case, chunk, max_query_len=None, seed=0, ctx=None, tables=None, oracle_ref=True):
+def _run(case, chunk, max_query_len=None, seed=0, ctx=None, tables=None, oracle_ref=True,
+         scale=None):
     """GPU and oracle prefill for the given chunk lengths; returns (gpu, ref, status, q_start)
-    (ref None without oracle_ref).  `tables` replaces the case's block tables on the GPU."""
+    (ref None without oracle_ref).  `tables` replaces the case's block tables on the GPU;
+    `scale` replaces the softmax scale 1/sqrt(head_dim) on both sides."""
     pkv = _pkv()
     w = case.w
+    scale = w.softmax_scale if scale is None else scale
     k, v, s = _full_cache(case)
     q, q_start = W.prefill_chunk(case, chunk, seed)
     ctx = case.context_lens if ctx is None else ctx
@@ -42,13 +45,13 @@ def _run(case, chunk, max_query_len=None, seed=0, ctx=None, tables=None, oracle_
                                 torch.from_numpy(case.block_tables if tables is None
                                                  else tables).cuda(),
                                 torch.from_numpy(np.ascontiguousarray(ctx, np.int32)).cuda(),
-                                sd, out, w.softmax_scale, w.num_kv_heads, w.kv_dtype,
+                                sd, out, scale, w.num_kv_heads, w.kv_dtype,
                                 w.block_size, mql, status)
     torch.cuda.synchronize()
     ref = None
     if oracle_ref:
         ref = oracle.prefill_attention(q, w.q_dtype, q_start, k, v, case.block_tables, ctx, s,
-                                       w.kv_dtype, case.num_blocks, w.softmax_scale,
+                                       w.kv_dtype, case.num_blocks, scale,
                                        w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size)
     return H.tensor_to_f64(out), ref, status.item(), q_start
 
@@ -76,6 +79,21 @@ def test_prefill_dtypes_groups_dims(kv, hq, hkv, head_dim, pf_mode):
     gpu, ref, st, _ = _run(case, chunk)
     assert st == 0
     H.check_close(gpu, ref, kv, qd, f"prefill kv {kv} {hq}/{hkv} D {head_dim}")
+
+
+@pytest.mark.parametrize("kv", [W.F16, W.BF16, W.FP8_E4M3, W.INT4_G32])
+def test_prefill_negative_softmax_scale(kv, pf_mode):
+    """A negative softmax scale makes each row's smallest score its largest
+    scaled one: tiles below every causal limit take the row's minimum, the
+    masked tiles their scaled maximum."""
+    qd = W.F16 if kv == W.F16 else W.BF16
+    w = W.Workload("pfneg", 3, 32, 8, 128, 16, kv, qd, "uniform", 200, 700,
+                   outlier_prob=0.01, outlier_scale=20.0, seed=77 + kv)
+    case = W.make_case(w)
+    chunk = [int(min(c, n)) for c, n in zip(case.context_lens, [1, 150, 300])]
+    gpu, ref, st, _ = _run(case, chunk, scale=-w.softmax_scale)
+    assert st == 0
+    H.check_close(gpu, ref, kv, qd, f"prefill negative scale, kv {kv}")
 
 
 @pytest.mark.parametrize("kv", [W.FP8_E4M3, W.FP8_E5M2, W.INT8])
