@@ -153,22 +153,24 @@ class GpuCase:
                                      case.max_blocks_per_seq, w.block_size, partition_size)
         self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
 
-    def attend(self, ctx=None, tables=None):
+    def attend(self, ctx=None, tables=None, scale=None):
         w = self.w
         self.pkv.paged_decode_attention(
             self.q, self.k, self.v, self.tables if tables is None else tables,
-            self.ctx if ctx is None else ctx, self.s, self.out, w.softmax_scale,
+            self.ctx if ctx is None else ctx, self.s, self.out,
+            w.softmax_scale if scale is None else scale,
             w.num_kv_heads, w.kv_dtype, w.block_size, self.partition_size, self.ws, self.status)
         torch.cuda.synchronize()
         return tensor_to_f64(self.out)
 
 
-def oracle_attention(case: W.Case, k, v, s, ctx=None, tables=None) -> np.ndarray:
+def oracle_attention(case: W.Case, k, v, s, ctx=None, tables=None, scale=None) -> np.ndarray:
     w = case.w
     return oracle.decode_attention(case.q, w.q_dtype, k, v,
                                    case.block_tables if tables is None else tables,
                                    case.context_lens if ctx is None else ctx, s, w.kv_dtype,
-                                   case.num_blocks, w.softmax_scale, w.num_q_heads,
+                                   case.num_blocks, w.softmax_scale if scale is None else scale,
+                                   w.num_q_heads,
                                    w.num_kv_heads, w.head_dim, w.block_size)
 
 

@@ -1,8 +1,9 @@
 """GPU parity of paged_decode_attention against the fp64 oracle.
 
 The GPU reads the oracle-written cache (so both sides see the same bytes);
-outputs must agree within the stated max-abs tolerance (2e-3 for 16-bit KV,
-5e-3 for FP8/INT4) plus half an ulp of the output dtype.
+each output must lie within the stated max-abs tolerance (2e-3 for 16-bit KV,
+5e-3 for FP8/INT4) of the oracle before its final rounding to the output
+dtype (tests/helpers.py, check_close).
 """
 
 import numpy as np
@@ -64,6 +65,24 @@ def test_heads_dims_dtypes(kv, head_dim, hq, hkv, mode):
     w = W.Workload("grid", 3, hq, hkv, head_dim, 16, kv, qd, "uniform", 1, 200, seed=hq * 7 + hkv + head_dim + kv)
     case, g, out, ref, _ = _run(w, partition_size=64)
     H.check_close(out, ref, kv, qd, f"kv {kv} D {head_dim} {hq}/{hkv}")
+
+
+@pytest.mark.parametrize("kv", [W.F16, W.BF16, W.FP8_E4M3, W.INT8, W.INT4_G32])
+def test_negative_softmax_scale(kv, mode):
+    """A negative softmax scale: each head's largest scaled score is its
+    smallest raw one."""
+    qd = W.F16 if kv == W.F16 else W.BF16
+    w = W.Workload("neg", 4, 32, 8, 128, 16, kv, qd, "uniform", 50, 600,
+                   outlier_prob=0.01, outlier_scale=20.0, seed=91 + kv)
+    case = W.make_case(w)
+    k, v, s = oracle.prefill_case(case)
+    oracle.kv_write(case.k_new, case.v_new, w.q_dtype, case.new_slots, k, v, s, w.kv_dtype,
+                    case.num_blocks, w.num_kv_heads, w.head_dim, w.block_size)
+    g = H.GpuCase(case, k, v, s, 128)
+    out = g.attend(scale=-w.softmax_scale)
+    assert g.status.item() == 0
+    ref = H.oracle_attention(case, k, v, s, scale=-w.softmax_scale)
+    H.check_close(out, ref, kv, qd, f"negative scale, kv {kv}")
 
 
 @pytest.mark.parametrize("kv", [W.BF16, W.FP8_E4M3, W.FP8_E5M2, W.INT8, W.INT4_G32])
