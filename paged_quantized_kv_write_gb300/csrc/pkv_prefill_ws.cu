@@ -298,8 +298,6 @@ __device__ __forceinline__ void tmem_ld_row(uint32_t taddr, float (&v)[N]) {
   else tmem_ld64(taddr, v);
 }
 
-// The largest of a row's N scores, and the largest of their negations, as
-// pairwise trees (log2 N dependent steps instead of N)
 // Scores of the 16-token pieces flagged in `bad` (bit j: piece j; the same
 // for the whole warp) set to -inf.
 template <int N>
@@ -344,11 +342,12 @@ __device__ __forceinline__ float tree_reduce3(const float (&v)[N]) {
     return tree_reduce3<kMin, M>(w);
   }
 }
+// The largest of a row's N scores, and the largest of their negations, as
+// trees of three-input instructions (log3 N dependent steps instead of N)
 template <int N>
 __device__ __forceinline__ float row_max(const float (&s)[N]) {
   return tree_reduce3<false, N>(s);
 }
-// the largest of -s (= -min s)
 template <int N>
 __device__ __forceinline__ float row_max_neg(const float (&s)[N]) {
   return -tree_reduce3<true, N>(s);
