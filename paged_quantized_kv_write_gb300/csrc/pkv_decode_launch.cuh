@@ -10,13 +10,6 @@
 namespace pkv {
 namespace {
 
-// Merge the partitions of one (sequence, q head): M = max m_p,
-// L = sum l_p 2^(m_p - M), out = sum l_p 2^(m_p - M) O_p / L.
-//
-// One CTA per (sequence, q head) with W warps.  Lane l of every warp keeps
-// head_dim values [EPT l, EPT l + EPT) of the sum.  The partitions are taken
-// in blocks of 32: lane j computes the weight of partition 32k + j of its
-// warp's block k, the warp then walks the block with eight independent
 // One lane's EPT values of row i of a partial output, i < np.
 template <int EPT>
 __device__ __forceinline__ void load_partial(const float* src, float (&v)[EPT]) {
@@ -94,6 +87,13 @@ __device__ __forceinline__ void merge_states(const float* ml, int64_t ml_step, c
   }
 }
 
+// Merge the partitions of one (sequence, q head): M = max m_p,
+// L = sum l_p 2^(m_p - M), out = sum l_p 2^(m_p - M) O_p / L.
+//
+// One CTA per (sequence, q head) with W warps.  Lane l of every warp keeps
+// head_dim values [EPT l, EPT l + EPT) of the sum.  The partitions are taken
+// in blocks of 32: lane j computes the weight of partition 32k + j of its
+// warp's block k, the warp then walks the block with eight independent
 // 16-byte (8-byte at head_dim 64) loads in flight per lane, each weight
 // handed out by a shuffle; the W warps' sums meet in shared memory.
 template <int QT, int D, int W>
